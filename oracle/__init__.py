@@ -1,0 +1,248 @@
+"""CPU oracle for the paged sparse K-cache pipeline (ctypes over numpy).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` may import this package.  The
+product library never imports it, and it imports nothing from the product.
+
+The arithmetic lives in ``psk_oracle.c`` (plain single-threaded C, built
+without fast-math or FMA contraction).  This module only marshals numpy arrays
+into it.  Arrays must be C-contiguous; bf16 tensors travel as ``uint16`` bit
+patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "psk_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+
+GCC_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+             "-fno-fast-math", "-Wall", "-Wextra"]
+
+REC_FP8_DS_MLA = 0
+REC_MXFP4 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``liboracle.so`` beside its source."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    cmd = ["gcc", *GCC_FLAGS, _SRC, "-o", _LIB_PATH + ".tmp", "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(_LIB_PATH + ".tmp", _LIB_PATH)
+    return _LIB_PATH
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    sig = {
+        "oracle_e4m3_encode": (ctypes.c_uint8, [ctypes.c_float]),
+        "oracle_e4m3_decode": (ctypes.c_float, [ctypes.c_uint8]),
+        "oracle_e2m1_encode": (ctypes.c_uint8, [ctypes.c_float]),
+        "oracle_e2m1_decode": (ctypes.c_float, [ctypes.c_uint8]),
+        "oracle_ceil_log2": (_I32, [ctypes.c_float]),
+        "oracle_bf16_from_f32": (ctypes.c_uint16, [ctypes.c_float]),
+        "oracle_bf16_to_f32": (ctypes.c_float, [ctypes.c_uint16]),
+        "oracle_e4m3_encode_array": (None, [_P, _P, _I64]),
+        "oracle_e2m1_encode_array": (None, [_P, _P, _I64]),
+        "oracle_ceil_log2_array": (None, [_P, _P, _I64]),
+        "oracle_fp8_token_stride": (_I64, [_I32, _I32]),
+        "oracle_fp8_scale_bytes": (_I64, [_I32, _I32]),
+        "oracle_quantize_and_insert_k_cache": (
+            _I64, [_P, _I64, _P, _I64, _P, _I64, _I64, _I32, _I32, _I32, _I32]),
+        "oracle_write_indexer_mxfp4_cache": (
+            _I64, [_P, _I64, _P, _I64, _P, _I64, _I64, _I32, _I32]),
+        "oracle_compute_global_topk_indices_and_lens": (
+            None, [_P, _I64, _I64, _I32, _P, _P, _I64, _I32, _I32, _I32, _P, _P,
+                   _P, _I64, _P]),
+        "oracle_combine_topk_swa_indices": (
+            None, [_P, _P, _P, _P, _I32, _I64,
+                   _P, _I64, _I32, _P, _I32,
+                   _P, _I64, _I32, _P, _I32,
+                   _I32, _I32, _P, _I64, _I32, _P, _P, _I64, _P]),
+        "oracle_dequantize_and_gather_k_cache": (
+            None, [_P, _I64, _I64, _P, _I64, _I64, _I32, _I32, _I32, _I32, _I32,
+                   _P, _I64, _I64, _I32]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def _as(a, dtype):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    assert a.dtype == dtype, f"expected {dtype}, got {a.dtype}"
+    return a
+
+
+# ---- scalar formats ---------------------------------------------------------
+
+def e4m3_encode(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def e2m1_encode(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_e2m1_encode_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def ceil_log2(q: np.ndarray) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    out = np.empty(q.shape, dtype=np.int32)
+    _load().oracle_ceil_log2_array(_ptr(q), _ptr(out), q.size)
+    return out
+
+
+def e4m3_decode(code: int) -> float:
+    return _load().oracle_e4m3_decode(code)
+
+
+def e2m1_decode(nibble: int) -> float:
+    return _load().oracle_e2m1_decode(nibble)
+
+
+def bf16_from_f32(f: float) -> int:
+    return _load().oracle_bf16_from_f32(f)
+
+
+def fp8_token_stride(head_dim: int, rope_dim: int) -> int:
+    return _load().oracle_fp8_token_stride(head_dim, rope_dim)
+
+
+def fp8_scale_bytes(head_dim: int, is_ue8m0: bool) -> int:
+    return _load().oracle_fp8_scale_bytes(head_dim, int(bool(is_ue8m0)))
+
+
+def fp8_record_bytes(head_dim: int, rope_dim: int, is_ue8m0: bool = True) -> int:
+    return fp8_token_stride(head_dim, rope_dim) + fp8_scale_bytes(head_dim, is_ue8m0)
+
+
+def mxfp4_record_bytes(head_dim: int) -> int:
+    return head_dim // 2 + head_dim // 32
+
+
+# ---- pipeline steps ---------------------------------------------------------
+
+def quantize_and_insert_k_cache(k_bits, slot_mapping, cache, block_size, head_dim,
+                                rope_dim, is_ue8m0=True) -> int:
+    """Insert rows of ``k_bits`` (uint16 bf16 patterns [N, >=D]) into ``cache``
+    (uint8 [num_pages, page_stride]) in place.  Returns out-of-range count."""
+    k_bits = _as(k_bits, np.uint16)
+    slot_mapping = _as(slot_mapping, np.int64)
+    assert cache.dtype == np.uint8 and cache.ndim == 2 and cache.flags["C_CONTIGUOUS"]
+    return _load().oracle_quantize_and_insert_k_cache(
+        _ptr(k_bits), k_bits.shape[1], _ptr(slot_mapping), slot_mapping.shape[0],
+        _ptr(cache), cache.shape[0], cache.shape[1], block_size, head_dim, rope_dim,
+        int(bool(is_ue8m0)))
+
+
+def write_indexer_mxfp4_cache(k_bits, slot_mapping, cache, block_size, head_dim) -> int:
+    k_bits = _as(k_bits, np.uint16)
+    slot_mapping = _as(slot_mapping, np.int64)
+    assert cache.dtype == np.uint8 and cache.ndim == 2 and cache.flags["C_CONTIGUOUS"]
+    return _load().oracle_write_indexer_mxfp4_cache(
+        _ptr(k_bits), k_bits.shape[1], _ptr(slot_mapping), slot_mapping.shape[0],
+        _ptr(cache), cache.shape[0], cache.shape[1], block_size, head_dim)
+
+
+def compute_global_topk_indices_and_lens(topk_local, token_to_req, block_table,
+                                         block_size, base_offsets=None,
+                                         is_valid_token=None):
+    topk_local = _as(topk_local, np.int32)
+    token_to_req = _as(token_to_req, np.int32)
+    block_table = _as(block_table, np.int32)
+    base_offsets = _as(base_offsets, np.int32)
+    if is_valid_token is not None:
+        is_valid_token = np.ascontiguousarray(is_valid_token).astype(np.uint8)
+    T, K = topk_local.shape
+    out = np.empty((T, K), dtype=np.int32)
+    lens = np.empty((T,), dtype=np.int32)
+    _load().oracle_compute_global_topk_indices_and_lens(
+        _ptr(topk_local), K, T, K, _ptr(token_to_req), _ptr(block_table),
+        block_table.shape[1], block_table.shape[1], block_table.shape[0], block_size,
+        _ptr(base_offsets), _ptr(is_valid_token), _ptr(out), K, _ptr(lens))
+    return out, lens
+
+
+def combine_topk_swa_indices(query_start_loc, seq_lens, token_to_req, replay_start,
+                             swa_block_table, swa_block_size, comp_block_table,
+                             comp_block_size, window, compress_ratio, topk_local,
+                             swa_base_offsets=None, comp_base_offsets=None,
+                             is_valid_token=None, num_tokens=None):
+    query_start_loc = _as(query_start_loc, np.int32)
+    seq_lens = _as(seq_lens, np.int32)
+    token_to_req = _as(token_to_req, np.int32)
+    replay_start = _as(replay_start, np.int32)
+    swa_block_table = _as(swa_block_table, np.int32)
+    comp_block_table = _as(comp_block_table, np.int32)
+    swa_base_offsets = _as(swa_base_offsets, np.int32)
+    comp_base_offsets = _as(comp_base_offsets, np.int32)
+    topk_local = _as(topk_local, np.int32)
+    if is_valid_token is not None:
+        is_valid_token = np.ascontiguousarray(is_valid_token).astype(np.uint8)
+    T = topk_local.shape[0] if num_tokens is None else num_tokens
+    K = topk_local.shape[1]
+    P = (K + 3) // 4 * 4
+    num_reqs = seq_lens.shape[0]
+    out = np.empty((T, window + P), dtype=np.int32)
+    lens = np.empty((T,), dtype=np.int32)
+    cbt = comp_block_table
+    _load().oracle_combine_topk_swa_indices(
+        _ptr(query_start_loc), _ptr(seq_lens), _ptr(token_to_req), _ptr(replay_start),
+        num_reqs, T,
+        _ptr(swa_block_table), swa_block_table.shape[1], swa_block_table.shape[1],
+        _ptr(swa_base_offsets), swa_block_size,
+        _ptr(cbt), cbt.shape[1] if cbt is not None else 0,
+        cbt.shape[1] if cbt is not None else 0, _ptr(comp_base_offsets),
+        comp_block_size, window, compress_ratio, _ptr(topk_local), K, K,
+        _ptr(is_valid_token), _ptr(out), window + P, _ptr(lens))
+    return out, lens
+
+
+def dequantize_and_gather_k_cache(cache, block_size, record, head_dim, rope_dim,
+                                  indices, is_ue8m0=True) -> np.ndarray:
+    """Return uint16 bf16 patterns [rows, cols, head_dim] for ``indices``."""
+    indices = _as(indices, np.int32)
+    if indices.ndim == 1:
+        indices = indices.reshape(-1, 1)
+    rows, cols = indices.shape
+    out = np.empty((rows, cols, head_dim), dtype=np.uint16)
+    assert cache.dtype == np.uint8 and cache.ndim == 2 and cache.flags["C_CONTIGUOUS"]
+    _load().oracle_dequantize_and_gather_k_cache(
+        _ptr(out), cols * head_dim, head_dim, _ptr(cache), cache.shape[0],
+        cache.shape[1], block_size, record, head_dim, rope_dim, int(bool(is_ue8m0)),
+        _ptr(indices), cols, rows, cols)
+    return out

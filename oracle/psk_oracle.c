@@ -1,0 +1,550 @@
+/*
+ * psk_oracle.c -- CPU oracle for the paged sparse K-cache pipeline.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test-suite, the smoke check and the
+ * CPU-baseline leg of the benchmark load this file's library.  The product
+ * library never includes, links or calls it, and this file includes nothing
+ * from the product library: the two implementations share no code.
+ *
+ * Plain, slow, single-threaded C.  Each step follows the statement it cites,
+ * in the order the statement gives, with no blocking or fusion.  Floating
+ * point is IEEE binary32 with round-to-nearest-even, as the pages' torch
+ * restatements compute it; build without fast-math and without FMA
+ * contraction so the host rounds every operation once.
+ *
+ * Sources (page title, then the section/function on it):
+ *   [OPS]  TokenSpeed runtime/layers/attention/deepseek_v4_ops.py
+ *   [BE]   TokenSpeed runtime/layers/attention/backends/deepseek_v4.py
+ *   [MDL]  TokenSpeed runtime/models/deepseek_v4.py
+ *   [VLLM] vLLM API docs, vllm.models.deepseek_v41.common.ops
+ *   [OFP8] OCP 8-bit Floating Point Specification (OFP8), E4M3 encoding
+ *   [MX]   OCP Microscaling Formats (MX) v1.0, E2M1 element and E8M0 scale
+ *
+ * Parity pins live in tests/test_oracle_*.py.  The fp32-scale FP8 record
+ * (is_ue8m0 = 0) is "parity unpinned" beyond its IEEE-division identity: no
+ * page prints that rule.
+ */
+#include "psk_oracle.h"
+
+#include <math.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Scalar formats                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Round a non-negative double to the nearest integer, ties to even. */
+static double round_half_even(double q) {
+    double f = floor(q);
+    double frac = q - f;
+    if (frac > 0.5) return f + 1.0;
+    if (frac < 0.5) return f;
+    return (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+}
+
+/*
+ * [OFP8] E4M3 ("FN" variant): sign bit, 4 exponent bits (bias 7), 3 mantissa
+ * bits; no infinities; S.1111.111 is NaN; the largest finite magnitude is
+ * 1.75 * 2^8 = 448.  Exponent field 0 holds subnormals m * 2^-9.
+ * Rounding is to nearest, ties to even; magnitudes beyond 448 saturate to 448
+ * (the "satfinite" conversion).  The sign of zero is kept.
+ */
+uint8_t oracle_e4m3_encode(float v) {
+    if (isnan(v)) return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range, spacing 2^-9; a count of 8 is the smallest normal
+         * (exponent field 1, mantissa 0), which is also code 8. */
+        double m = round_half_even(a * 512.0);
+        return sign | (uint8_t)m;
+    }
+    int ex;
+    (void)frexp(a, &ex);
+    int e = ex - 1; /* 2^e <= a < 2^(e+1), e in [-6, 8] */
+    double m = round_half_even(ldexp(a, 3 - e)); /* significand * 8, in [8, 16] */
+    if (m == 16.0) {
+        e += 1;
+        m = 8.0;
+    }
+    int code = ((e + 7) << 3) | ((int)m - 8);
+    if (code > 0x7E) code = 0x7E;
+    return sign | (uint8_t)code;
+}
+
+float oracle_e4m3_decode(uint8_t code) {
+    int s = code >> 7, e = (code >> 3) & 0xF, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = (e == 0) ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return (float)(s ? -v : v);
+}
+
+/*
+ * [MX] E2M1: sign bit, 2 exponent bits (bias 1), 1 mantissa bit.  Magnitudes
+ * {0, 0.5, 1, 1.5, 2, 3, 4, 6}; no infinities or NaN.  Round to nearest, ties
+ * to the even code; saturate to 6; keep the sign of zero.
+ */
+uint8_t oracle_e2m1_encode(float v) {
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    double a = fabs((double)v);
+    if (isnan(v)) return 0x7;
+    if (a >= 6.0) return sign | 0x7;
+    if (a < 1.0) {
+        /* exponent field 0: subnormal 0.5 * m; a count of 2 is 1.0 = code 2 */
+        double m = round_half_even(a * 2.0);
+        return sign | (uint8_t)m;
+    }
+    int ex;
+    (void)frexp(a, &ex);
+    int e = ex - 1; /* e in [0, 2] */
+    double m = round_half_even(ldexp(a, 1 - e)); /* significand * 2, in [2, 4] */
+    if (m == 4.0) {
+        e += 1;
+        m = 2.0;
+    }
+    if (e > 2) return sign | 0x7;
+    return sign | (uint8_t)(((e + 1) << 1) | ((int)m - 2));
+}
+
+float oracle_e2m1_decode(uint8_t nibble) {
+    int s = (nibble >> 3) & 1, e = (nibble >> 1) & 3, f = nibble & 1;
+    double v = (e == 0) ? 0.5 * f : ldexp((double)(2 + f), e - 2);
+    return (float)(s ? -v : v);
+}
+
+/*
+ * Smallest integer e with 2^e >= q, for finite q > 0 (exact; no log2 call).
+ * frexp gives q = f * 2^ex with f in [0.5, 1): q is a power of two exactly
+ * when f == 0.5, and then e = ex - 1; otherwise e = ex.
+ */
+int32_t oracle_ceil_log2(float q) {
+    if (isinf(q)) return 128;
+    int ex;
+    double f = frexp((double)q, &ex);
+    return (f == 0.5) ? ex - 1 : ex;
+}
+
+/* bf16 is the upper half of binary32.  Rounding to bf16 drops 16 low bits,
+ * to nearest with ties to even; NaN maps to the canonical quiet NaN. */
+uint16_t oracle_bf16_from_f32(float f) {
+    if (isnan(f)) return 0x7FFF;
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+float oracle_bf16_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+void oracle_e4m3_encode_array(const float* v, uint8_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(v[i]);
+}
+
+void oracle_e2m1_encode_array(const float* v, uint8_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_encode(v[i]);
+}
+
+void oracle_ceil_log2_array(const float* q, int32_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_ceil_log2(q[i]);
+}
+
+/* 2^k as binary32: exact for k in [-149, 127], +inf above, 0 below. */
+static float pow2f(int k) {
+    if (k > 127) return INFINITY;
+    if (k < -149) return 0.0f;
+    return ldexpf(1.0f, k);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Record geometry                                                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * fp8_ds_mla record ([OPS] dequantize_deepseek_v4_fp8_ds_mla_cache and
+ * _fp8_ds_mla_cache_rows; [VLLM] quantize_and_insert_k_cache): per token the
+ * nope dims as one e4m3 byte each, then the rope dims as bf16 (2 bytes each);
+ * after block_size such data records, block_size scale records.  Quant blocks
+ * are 64 wide; a token carries head_dim/64 scale slots (448 + 64 -> 7 used +
+ * 1 zero pad = 8, as the insert docs fix for head_dim 512).
+ */
+int64_t oracle_fp8_token_stride(int32_t head_dim, int32_t rope_dim) {
+    return (int64_t)(head_dim - rope_dim) + 2 * (int64_t)rope_dim;
+}
+
+int64_t oracle_fp8_scale_bytes(int32_t head_dim, int32_t is_ue8m0) {
+    /* one UE8M0 byte per 64-block, or one little-endian binary32 per block */
+    return (int64_t)(head_dim / 64) * (is_ue8m0 ? 1 : 4);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 1a: FP8 quantize-and-insert                                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [VLLM] quantize_and_insert_k_cache; the math is [OPS] _fp8_ds_mla_cache_rows
+ * and its writer _write_fp8_ds_mla_cache_rows_capturable.
+ *
+ * For every token i with slot s = slot_mapping[i]:
+ *   s < 0 is skipped (padding); s >= num_pages * block_size is skipped and
+ *   counted (fail closed, [MDL] _deepseek_v4_swa_slot_mapping).
+ *   page = s / block_size, off = s % block_size.
+ *   For each 64-wide block of the nope dims:
+ *     is_ue8m0 = 1 (the pages' rule):
+ *       amax = max |x|, floored at 1e-4;
+ *       e = ceil(log2(amax / 448)) taken exactly on the binary32 quotient;
+ *       scale byte = clamp(e + 127, 0, 255);
+ *       code = e4m3(clamp(x * 2^-e, -448, 448)).
+ *     is_ue8m0 = 0 (fp32 scales, not on the pages -- parity unpinned):
+ *       scale = max(amax, 1e-12) / 448 (binary32, stored little-endian);
+ *       code = e4m3(clamp(x / scale, -448, 448)).
+ *   The rope dims are copied as bf16 bit patterns; unused scale slots are 0.
+ * Returns the number of out-of-range slots.
+ */
+int64_t oracle_quantize_and_insert_k_cache(
+    const uint16_t* k, int64_t k_row_stride, const int64_t* slot_mapping,
+    int64_t num_tokens, uint8_t* cache, int64_t num_pages,
+    int64_t page_stride, int32_t block_size, int32_t head_dim,
+    int32_t rope_dim, int32_t is_ue8m0) {
+    const int32_t nope = head_dim - rope_dim;
+    const int64_t ts = oracle_fp8_token_stride(head_dim, rope_dim);
+    const int64_t sdim = oracle_fp8_scale_bytes(head_dim, is_ue8m0);
+    const int32_t nblk = nope / 64;
+    const int64_t capacity = num_pages * (int64_t)block_size;
+    int64_t errors = 0;
+
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        const int64_t s = slot_mapping[i];
+        if (s < 0) continue;
+        if (s >= capacity) {
+            ++errors;
+            continue;
+        }
+        const int64_t page = s / block_size, off = s % block_size;
+        uint8_t* data = cache + page * page_stride + off * ts;
+        uint8_t* scl = cache + page * page_stride + (int64_t)block_size * ts + off * sdim;
+        const uint16_t* row = k + i * k_row_stride;
+
+        memset(scl, 0, (size_t)sdim);
+        for (int32_t b = 0; b < nblk; ++b) {
+            float x[64];
+            float amax = 0.0f;
+            for (int j = 0; j < 64; ++j) {
+                x[j] = oracle_bf16_to_f32(row[b * 64 + j]);
+                float a = fabsf(x[j]);
+                if (a > amax) amax = a;
+            }
+            if (is_ue8m0) {
+                float a = (amax < 1.0e-4f) ? 1.0e-4f : amax;
+                float q = a / 448.0f;
+                int32_t e = oracle_ceil_log2(q);
+                int32_t byte = e + 127;
+                if (byte < 0) byte = 0;
+                if (byte > 255) byte = 255;
+                scl[b] = (uint8_t)byte;
+                float p = pow2f(-e);
+                for (int j = 0; j < 64; ++j) {
+                    float v = x[j] * p;
+                    if (v > 448.0f) v = 448.0f;
+                    if (v < -448.0f) v = -448.0f;
+                    data[b * 64 + j] = oracle_e4m3_encode(v);
+                }
+            } else {
+                float a = (amax < 1.0e-12f) ? 1.0e-12f : amax;
+                float scale = a / 448.0f;
+                memcpy(scl + 4 * b, &scale, 4);
+                for (int j = 0; j < 64; ++j) {
+                    float v = x[j] / scale;
+                    if (v > 448.0f) v = 448.0f;
+                    if (v < -448.0f) v = -448.0f;
+                    data[b * 64 + j] = oracle_e4m3_encode(v);
+                }
+            }
+        }
+        /* rope tail: bf16 bit patterns, verbatim (already rotated by the caller) */
+        memcpy(data + nope, row + nope, (size_t)rope_dim * 2);
+    }
+    return errors;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 1b: MXFP4 indexer-key insert                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [OPS] write_deepseek_v4_indexer_mxfp4_cache (page layout) and
+ * read_deepseek_v4_indexer_mxfp4_cache (the inverse that fixes nibble order
+ * and scale meaning).  The writer's scale rule is not printed; the reading
+ * taken is E8M0 = ceil-pow2(amax / 6), with amax floored at 1e-4 as the FP8
+ * writer floors it.
+ *
+ * Per token and 32-wide block: e = ceil(log2(max(amax, 1e-4) / 6)),
+ * scale byte = clamp(e + 127, 0, 254), code = e2m1(x * 2^-e) (saturating).
+ * Byte j of the values holds element 2j in its low nibble and 2j+1 in its
+ * high nibble.  Page: [block_size x head_dim/2 value bytes]
+ * [block_size x head_dim/32 scale bytes].
+ */
+int64_t oracle_write_indexer_mxfp4_cache(
+    const uint16_t* k, int64_t k_row_stride, const int64_t* slot_mapping,
+    int64_t num_tokens, uint8_t* cache, int64_t num_pages,
+    int64_t page_stride, int32_t block_size, int32_t head_dim) {
+    const int64_t vbytes = head_dim / 2, sbytes = head_dim / 32;
+    const int64_t capacity = num_pages * (int64_t)block_size;
+    int64_t errors = 0;
+
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        const int64_t s = slot_mapping[i];
+        if (s < 0) continue;
+        if (s >= capacity) {
+            ++errors;
+            continue;
+        }
+        const int64_t page = s / block_size, off = s % block_size;
+        uint8_t* vals = cache + page * page_stride + off * vbytes;
+        uint8_t* scl = cache + page * page_stride + (int64_t)block_size * vbytes + off * sbytes;
+        const uint16_t* row = k + i * k_row_stride;
+
+        for (int32_t b = 0; b < head_dim / 32; ++b) {
+            float x[32];
+            float amax = 0.0f;
+            for (int j = 0; j < 32; ++j) {
+                x[j] = oracle_bf16_to_f32(row[b * 32 + j]);
+                float a = fabsf(x[j]);
+                if (a > amax) amax = a;
+            }
+            float a = (amax < 1.0e-4f) ? 1.0e-4f : amax;
+            float q = a / 6.0f;
+            int32_t e = oracle_ceil_log2(q);
+            int32_t byte = e + 127;
+            if (byte < 0) byte = 0;
+            if (byte > 254) byte = 254;
+            scl[b] = (uint8_t)byte;
+            float p = pow2f(-e);
+            for (int j = 0; j < 32; j += 2) {
+                uint8_t lo = oracle_e2m1_encode(x[j] * p);
+                uint8_t hi = oracle_e2m1_encode(x[j + 1] * p);
+                vals[(b * 32 + j) / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+    return errors;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 2: index builders                                                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Slot of logical position `pos` through one request's block-table row
+ * ([MDL] indexer prefill gather plan: page_ids * block_size + offset;
+ * [BE] dense compressed indices with safe_page_ids; [OPS]
+ * _compress_v4_state_windows_capturable for the base_logical_page offset and
+ * the validity rules):
+ *   logical page = pos / block_size - base;  outside [0, width) -> -1;
+ *   page id = row[logical page];  page id < 0 -> -1;
+ *   slot = page id * block_size + pos % block_size  (-1 if beyond int32).
+ */
+static int32_t slot_of(const int32_t* row, int32_t width, int64_t base,
+                       int32_t block_size, int64_t pos) {
+    if (pos < 0) return -1;
+    int64_t lp = pos / block_size - base;
+    if (lp < 0 || lp >= width) return -1;
+    int32_t page = row[lp];
+    if (page < 0) return -1;
+    int64_t s = (int64_t)page * block_size + pos % block_size;
+    if (s > INT32_MAX) return -1;
+    return (int32_t)s;
+}
+
+/*
+ * [VLLM] compute_global_topk_indices_and_lens: per token, map every local
+ * top-k index through the token's request block table; -1 stays -1; count the
+ * valid entries into lens; an invalid (padding) token gets lens 0 and, in the
+ * reading taken here, all of its entries written as -1.  A token whose request
+ * index is outside [0, num_reqs) is treated as invalid.  Entries are not
+ * compacted.
+ */
+void oracle_compute_global_topk_indices_and_lens(
+    const int32_t* topk_local, int64_t topk_stride, int64_t num_tokens,
+    int32_t topk, const int32_t* token_to_req, const int32_t* block_table,
+    int64_t bt_stride, int32_t bt_width, int32_t num_reqs, int32_t block_size,
+    const int32_t* base_offsets, const uint8_t* is_valid_token,
+    int32_t* out_indices, int64_t out_stride, int32_t* out_lens) {
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int32_t r = token_to_req[t];
+        const int ok = (is_valid_token ? is_valid_token[t] != 0 : 1) &&
+                       r >= 0 && r < num_reqs;
+        int32_t count = 0;
+        for (int32_t j = 0; j < topk; ++j) {
+            int32_t v = -1;
+            if (ok) {
+                int32_t l = topk_local[t * topk_stride + j];
+                if (l >= 0) {
+                    int64_t base = base_offsets ? base_offsets[r] : 0;
+                    v = slot_of(block_table + (int64_t)r * bt_stride, bt_width,
+                                base, block_size, l);
+                }
+            }
+            out_indices[t * out_stride + j] = v;
+            if (v >= 0) ++count;
+        }
+        out_lens[t] = count;
+    }
+}
+
+/*
+ * [VLLM] build_flashinfer_mixed_sparse_indices (the single-kernel form of
+ * TokenSpeed's combine_topk_swa_indices).  Per token t of request r:
+ *   position  pos = seq_lens[r] - query_len[r] + (t - query_start_loc[r])
+ *             ([BE] _decode_positions_from_metadata);
+ *   window    [lo, pos] with lo = max(replay_start[r], pos - window + 1, 0);
+ *   columns [0, window): column c holds the slot of position lo + c through
+ *             the SWA table, or -1 once lo + c > pos (left-aligned, oldest
+ *             first -- a reading);
+ *   columns [window, window + topk): local top-k index j mapped through the
+ *             compressed table (the SWA table when none is given);
+ *   columns up to window + roundup(topk, 4): -1 (16-byte row alignment);
+ *   lens[t] = number of entries >= 0 over all columns (a reading: the docs
+ *             call it the active length per token).
+ * replay_start applies to every token (null = 0).  compress_ratio is accepted
+ * for the signature and does not change the result (a reading).
+ */
+void oracle_combine_topk_swa_indices(
+    const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* token_to_req, const int32_t* replay_start, int32_t num_reqs,
+    int64_t num_tokens,
+    const int32_t* swa_block_table, int64_t swa_bt_stride, int32_t swa_bt_width,
+    const int32_t* swa_base_offsets, int32_t swa_block_size,
+    const int32_t* comp_block_table, int64_t comp_bt_stride,
+    int32_t comp_bt_width, const int32_t* comp_base_offsets,
+    int32_t comp_block_size, int32_t window, int32_t compress_ratio,
+    const int32_t* topk_local, int64_t topk_stride, int32_t topk,
+    const uint8_t* is_valid_token, int32_t* sparse_indices, int64_t out_stride,
+    int32_t* lens) {
+    (void)compress_ratio;
+    const int32_t padded = (topk + 3) / 4 * 4;
+    const int32_t width = window + padded;
+    if (comp_block_table == NULL) {
+        comp_block_table = swa_block_table;
+        comp_bt_stride = swa_bt_stride;
+        comp_bt_width = swa_bt_width;
+    }
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int32_t* row = sparse_indices + t * out_stride;
+        const int32_t r = token_to_req[t];
+        const int ok = (is_valid_token ? is_valid_token[t] != 0 : 1) &&
+                       r >= 0 && r < num_reqs;
+        if (!ok) {
+            for (int32_t c = 0; c < width; ++c) row[c] = -1;
+            lens[t] = 0;
+            continue;
+        }
+        const int64_t qstart = query_start_loc[r];
+        const int64_t qlen = (int64_t)query_start_loc[r + 1] - qstart;
+        const int64_t pos = (int64_t)seq_lens[r] - qlen + (t - qstart);
+        int64_t lo = pos - window + 1;
+        const int64_t rs = replay_start ? replay_start[r] : 0;
+        if (rs > lo) lo = rs;
+        if (lo < 0) lo = 0;
+
+        int32_t count = 0;
+        const int32_t* swa_row = swa_block_table + (int64_t)r * swa_bt_stride;
+        const int64_t swa_base = swa_base_offsets ? swa_base_offsets[r] : 0;
+        for (int32_t c = 0; c < window; ++c) {
+            int64_t p = lo + c;
+            int32_t v = (p <= pos) ? slot_of(swa_row, swa_bt_width, swa_base,
+                                             swa_block_size, p)
+                                   : -1;
+            row[c] = v;
+            if (v >= 0) ++count;
+        }
+        const int32_t* comp_row = comp_block_table + (int64_t)r * comp_bt_stride;
+        const int64_t comp_base = comp_base_offsets ? comp_base_offsets[r] : 0;
+        for (int32_t j = 0; j < topk; ++j) {
+            int32_t l = topk_local[t * topk_stride + j];
+            int32_t v = (l >= 0) ? slot_of(comp_row, comp_bt_width, comp_base,
+                                           comp_block_size, l)
+                                 : -1;
+            row[window + j] = v;
+            if (v >= 0) ++count;
+        }
+        for (int32_t j = topk; j < padded; ++j) row[window + j] = -1;
+        lens[t] = count;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 3: dequantize-and-gather                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Index form of the gather: [OPS] dequantize_deepseek_v4_fp8_ds_mla_cache
+ * (record 0) and read_deepseek_v4_indexer_mxfp4_cache (record 1), with the
+ * rows laid out as out[t][j][d] = out + t*out_stride_t + j*out_stride_j + d.
+ *   s = indices[t][j]; s < 0 or s >= capacity -> an all-zero bf16 row.
+ *   fp8_ds_mla: nope dim d -> bf16(e4m3(byte d) * 2^(scale[d/64] - 127)) (UE8M0)
+ *               or bf16(e4m3(byte d) * scale_f32[d/64]) (fp32 scales);
+ *               rope dims -> the stored bf16 bit patterns.
+ *   MXFP4:      dim d -> bf16(e2m1(nibble d) * 2^(scale[d/32] - 127)), nibble
+ *               d is the low half of byte d/2 for even d, the high half for odd.
+ * Products are formed in binary32 and rounded once more to bf16.
+ */
+void oracle_dequantize_and_gather_k_cache(
+    uint16_t* out, int64_t out_stride_t, int64_t out_stride_j,
+    const uint8_t* cache, int64_t num_pages, int64_t page_stride,
+    int32_t block_size, int32_t record, int32_t head_dim, int32_t rope_dim,
+    int32_t is_ue8m0, const int32_t* indices, int64_t idx_stride, int64_t rows,
+    int32_t cols) {
+    const int64_t capacity = num_pages * (int64_t)block_size;
+    for (int64_t t = 0; t < rows; ++t) {
+        for (int32_t j = 0; j < cols; ++j) {
+            const int64_t s = indices[t * idx_stride + j];
+            uint16_t* o = out + t * out_stride_t + (int64_t)j * out_stride_j;
+            if (s < 0 || s >= capacity) {
+                for (int32_t d = 0; d < head_dim; ++d) o[d] = 0;
+                continue;
+            }
+            const int64_t page = s / block_size, off = s % block_size;
+            const uint8_t* base = cache + page * page_stride;
+            if (record == 0) {
+                const int32_t nope = head_dim - rope_dim;
+                const int64_t ts = oracle_fp8_token_stride(head_dim, rope_dim);
+                const int64_t sdim = oracle_fp8_scale_bytes(head_dim, is_ue8m0);
+                const uint8_t* data = base + off * ts;
+                const uint8_t* scl = base + (int64_t)block_size * ts + off * sdim;
+                for (int32_t d = 0; d < nope; ++d) {
+                    float val = oracle_e4m3_decode(data[d]);
+                    float f;
+                    if (is_ue8m0) {
+                        f = val * pow2f((int)scl[d / 64] - 127);
+                    } else {
+                        float sc;
+                        memcpy(&sc, scl + 4 * (d / 64), 4);
+                        f = val * sc;
+                    }
+                    o[d] = oracle_bf16_from_f32(f);
+                }
+                for (int32_t d = nope; d < head_dim; ++d) {
+                    const uint8_t* p = data + nope + 2 * (int64_t)(d - nope);
+                    o[d] = (uint16_t)(p[0] | (p[1] << 8));
+                }
+            } else {
+                const int64_t vbytes = head_dim / 2, sbytes = head_dim / 32;
+                const uint8_t* vals = base + off * vbytes;
+                const uint8_t* scl = base + (int64_t)block_size * vbytes + off * sbytes;
+                for (int32_t d = 0; d < head_dim; ++d) {
+                    uint8_t byte = vals[d / 2];
+                    uint8_t nib = (d % 2) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+                    float f = oracle_e2m1_decode(nib) * pow2f((int)scl[d / 32] - 127);
+                    o[d] = oracle_bf16_from_f32(f);
+                }
+            }
+        }
+    }
+}
