@@ -1,0 +1,393 @@
+"""Benchmark of the paged K-cache pipeline on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode]
+                    [--impl mine|reference] [--no-cpu-baseline]
+
+A step is one pass of every hot-path row over one synthetic batch (see
+paged_sparse_kv_gb300/pipeline.py): FP8 insert, MXFP4 insert, fused index build,
+the two-part FP8 gather, the global top-k mapping and the MXFP4 gather.  The
+default workload is the decode batch (64 requests x 1 token, contexts
+U[1024, 8192], head_dim 512 = 448 fp8 + 64 bf16 rope, page 64, window 128,
+top-k 512).
+
+Timing: W untimed warm-up steps, then K steps, each preceded by an L2 flush
+(a 512 MiB memset, outside the timed events) and bracketed by CUDA events on
+the launching stream; per-kernel events give each kernel's average duration.
+`value` is query tokens per second over all ranks (weak scaling: every rank
+runs its own full batch).  `e2e` repeats the step through the public API with
+the step's inputs copied from pinned host memory and every output copied back,
+all inside the timed region.  `roofline` is for the kernel with the largest
+share of the step: algorithmic bytes per launch / its mean event duration,
+against the measured HBM copy bandwidth.  `cpu_baseline` times the CPU oracle
+(test infrastructure, single-threaded C) on a bounded sample of the same
+workload on this host.
+
+--impl reference times the CPU oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "K-cache tokens/s and achieved HBM GB/s (% of GB300 peak) per kernel, 1 GPU"
+UNIT = "tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---- algorithmic bytes per launch ----------------------------------------------------
+
+def algorithmic_bytes(p, outputs) -> dict:
+    """Compulsory bytes of each launch of a step: every distinct input byte read
+    once, every output byte written once."""
+    w = p.w
+    res = {}
+    if w.has_fp8:
+        ins = w.insert_slots
+        nv = int((ins >= 0).sum())
+        rec = w.head_dim - w.rope_dim + 2 * w.rope_dim + w.head_dim // 64
+        res["quantize_and_insert_k_cache"] = nv * (2 * w.head_dim + rec) + ins.size * 8
+    if w.index_k is not None:
+        ins = w.index_insert_slots
+        nv = int((ins >= 0).sum())
+        res["write_indexer_mxfp4_cache"] = nv * (2 * w.index_head_dim + w.index_head_dim // 2 +
+                                                 w.index_head_dim // 32) + ins.size * 8
+    T, K, R = w.num_tokens, w.topk, w.num_reqs
+    comp_tab = w.comp_block_table if w.comp_block_table is not None else w.swa_block_table
+    if w.has_fp8:
+        W, P = w.window, w.padded_topk
+        res["combine_topk_swa_indices"] = (T * (4 * K + 4 * (W + P) + 4 + 4) + R * 12 +
+                                           R * comp_tab.shape[1] * 4)
+        si = outputs["sparse_indices"]
+        rec = w.head_dim - w.rope_dim + 2 * w.rope_dim + w.head_dim // 64
+        for part, cols in (("swa", si[:, :W]), ("topk", si[:, W:])):
+            valid = cols[cols >= 0]
+            distinct = np.unique(valid).size
+            res[f"dequantize_and_gather_k_cache[{part}]"] = (distinct * rec + cols.size * 4 +
+                                                             cols.size * 2 * w.head_dim)
+    res["compute_global_topk_indices_and_lens"] = T * (8 * K + 8) + R * comp_tab.shape[1] * 4
+    gt = outputs["global_topk"]
+    distinct = np.unique(gt[gt >= 0]).size
+    D = w.index_head_dim
+    res["dequantize_and_gather_k_cache[mxfp4]"] = (distinct * (D // 2 + D // 32) + gt.size * 4 +
+                                                   gt.size * 2 * D)
+    return res
+
+
+# ---- clocks sampled during the timed region --------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---- CPU oracle (baseline / reference arm) -----------------------------------------
+
+def _oracle_state(w):
+    from paged_sparse_kv_gb300 import synthetic
+    caches = {}
+    for i, name in enumerate(("swa_cache", "comp_cache", "index_cache")):
+        g = getattr(w, name)
+        caches[name] = None if g is None else synthetic.random_cache_bytes(50 + i, g)
+    return caches
+
+
+def _oracle_sample_tokens(w, max_rows: int):
+    """A bounded sample of the batch's tokens for the oracle's gathers."""
+    cols = (w.window + w.padded_topk if w.has_fp8 else 0) + w.topk
+    n = max(1, min(w.num_tokens, max_rows // max(cols, 1)))
+    if n >= w.num_tokens:
+        return None, w.num_tokens
+    return np.linspace(0, w.num_tokens - 1, n).astype(np.int64), n
+
+
+def time_oracle(w, budget_s: float, max_rows: int = 80000):
+    """Run oracle steps until budget_s of CPU work; returns (tokens/s, desc)."""
+    from oracle.pipeline import run_step
+    caches = _oracle_state(w)
+    toks, n = _oracle_sample_tokens(w, max_rows)
+    steps, spent = 0, 0.0
+    while spent < budget_s or steps == 0:
+        t0 = time.perf_counter()
+        run_step(w, caches["swa_cache"], caches["comp_cache"], caches["index_cache"], toks)
+        spent += time.perf_counter() - t0
+        steps += 1
+    desc = (f"{steps} oracle steps of the {w.name} batch; gathers over {n} of "
+            f"{w.num_tokens} tokens (value scaled to tokens whose rows were gathered)")
+    return n * steps / spent, desc
+
+
+# ---- main ------------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="decode",
+                    choices=["tiny", "decode", "prefill", "mixed", "mxfp4"])
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    from paged_sparse_kv_gb300 import build as psk_build
+    from paged_sparse_kv_gb300 import synthetic
+    from paged_sparse_kv_gb300.pipeline import Pipeline
+
+    psk_build.build()
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    maker = synthetic.MAKERS[args.config]
+    w = maker(synthetic.BASE_SEED + synthetic.CONFIG_NAMES.index(args.config) + 1000 * rank)
+    p = Pipeline(w, dev)
+    p.fill_caches_with_quantized_rows(seed=4321 + rank)
+    launches = p.launches()
+    names = [n for n, _ in launches]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        p.step()
+    torch.cuda.synchronize(dev)
+
+    outputs = {"global_topk": p.global_topk.cpu().numpy()}
+    if w.has_fp8:
+        outputs["sparse_indices"] = p.sparse_indices.cpu().numpy()
+    alg = algorithmic_bytes(p, outputs)
+
+    visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x]
+    clocks = ClockSampler(visible[local_rank] if local_rank < len(visible) else str(local_rank))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
+          for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        ev[s][0].record(stream)
+        for i, (_, launch) in enumerate(launches):
+            launch()
+            ev[s][i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+
+    step_ms = [ev[s][0].elapsed_time(ev[s][-1]) for s in range(args.steps)]
+    kern_ms = {n: [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)]
+               for i, n in enumerate(names)}
+    ms_per_step = statistics.mean(step_ms)
+    if dist:
+        t = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    value = w.num_tokens * world / (ms_per_step / 1e3)
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = run_e2e(p, args, dev, flush)
+    if dist:
+        t = torch.tensor([e2e["ms_per_step"]], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["ms_per_step"] = float(t.item())
+    e2e_value = w.num_tokens * world / (e2e["ms_per_step"] / 1e3)
+
+    peak, peak_kind = _peaks()
+    kernels = {}
+    for n in names:
+        mean_ms = statistics.mean(kern_ms[n])
+        gbs = alg[n] / (mean_ms / 1e3) / 1e9
+        kernels[n] = {"us": round(mean_ms * 1e3, 2), "alg_bytes": int(alg[n]),
+                      "GBps": round(gbs, 1), "frac_measured": round(gbs / peak, 3),
+                      "frac_nominal_8TBps": round(gbs / NOMINAL_HBM_GBS, 3),
+                      "share": round(mean_ms / ms_per_step, 3)}
+    top = max(names, key=lambda n: kernels[n]["us"])
+    roof = {"kernel": top, "bound": "hbm", "achieved": kernels[top]["GBps"], "peak": peak,
+            "peak_kind": peak_kind, "unit": "GB/s",
+            "frac": round(kernels[top]["GBps"] / peak, 3), "traffic": None}
+    traffic_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(traffic_path):
+        try:
+            tr = json.load(open(traffic_path)).get(args.config, {}).get(top)
+            roof["traffic"] = tr
+        except Exception:
+            pass
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16/fp8/fp4",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.num_reqs} requests, {w.num_tokens} query tokens, "
+                               f"head_dim {w.head_dim} (rope {w.rope_dim}), window {w.window}, "
+                               f"top-k {w.topk}, ratio {w.compress_ratio}",
+                   "seed": w.seed, "l2": "flushed before every step (512 MiB memset)",
+                   "parallelism": f"dp{world} (independent batch per GPU)"},
+        "roofline": roof,
+        "kernels": kernels,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": round(e2e["ms_per_step"], 4)},
+        "gpu_launches": len(launches) * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc = time_oracle(w, args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(v, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_e2e(p, args, dev, flush):
+    """The step through the public API with pinned host inputs and outputs."""
+    import torch
+    ins = [t for t in (p.k, p.insert_slots, p.index_k, p.index_insert_slots, p.qsl, p.seq_lens,
+                       p.t2r, p.replay, p.topk) if t is not None]
+    outs = [t for t in (p.sparse_indices, p.lens, p.gathered, p.global_topk, p.global_lens,
+                        p.gathered_index) if t is not None]
+    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    times = []
+    for s in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        p.step()
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    return {"ms_per_step": statistics.mean(times) * 1e3, "h2d": h2d, "d2h": d2h}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle, timed on this host's cores."""
+    if rank != 0:
+        return
+    import oracle
+    from oracle.pipeline import run_step
+    from paged_sparse_kv_gb300 import synthetic
+    oracle.build()
+    w = synthetic.MAKERS[args.config]()
+    caches = _oracle_state(w)
+    toks, n = _oracle_sample_tokens(w, 80000)
+    for _ in range(args.warmup):
+        run_step(w, caches["swa_cache"], caches["comp_cache"], caches["index_cache"], toks)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run_step(w, caches["swa_cache"], caches["comp_cache"], caches["index_cache"], toks)
+        times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    value = n / (ms / 1e3)
+    desc = (f"oracle step of the {w.name} batch per timed step; gathers over {n} of "
+            f"{w.num_tokens} tokens")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16/fp8/fp4", "data": "synthetic",
+        "config": {"workload": w.name, "seed": w.seed},
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

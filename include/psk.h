@@ -1,0 +1,241 @@
+/*
+ * psk.h -- C ABI of libpsk, the GB300 (sm_103a) paged sparse K-cache library.
+ *
+ * The library implements the hot path of a DeepSeek-V4-style sparse-MLA
+ * serving runtime's paged K cache, as stated on these pages:
+ *   [OPS]  TokenSpeed runtime/layers/attention/deepseek_v4_ops.py
+ *   [BE]   TokenSpeed runtime/layers/attention/backends/deepseek_v4.py
+ *   [MDL]  TokenSpeed runtime/models/deepseek_v4.py
+ *   [VLLM] vLLM API docs, vllm.models.deepseek_v41.common.ops
+ * and the OCP OFP8 (E4M3) and OCP MX v1.0 (E2M1, E8M0) format definitions.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * - Every pointer argument is DEVICE memory owned by the caller.  The library
+ *   allocates nothing, keeps no state between calls, never synchronises, and
+ *   launches only on `stream` (NULL = the legacy default stream), so calls can
+ *   be captured into CUDA graphs.
+ * - Strides are in ELEMENTS of the pointed-to type unless the name ends in
+ *   `_bytes`/`page_stride`.
+ * - bf16 tensors are passed as `void*` pointing at IEEE bfloat16 values.
+ * - Argument errors (null required pointer, negative or inconsistent sizes,
+ *   unsupported head_dim/rope_dim, misaligned pointer or stride) return
+ *   PSK_ERR_INVALID_ARGUMENT before any launch; nothing is written.
+ * - Zero work (no tokens, no rows) returns PSK_OK without a launch.
+ * - A failed launch returns PSK_ERR_CUDA.
+ * - psk_last_error() returns a message for the calling thread's last error.
+ * - Data-dependent problems never fault: a slot, page or index outside the
+ *   cache or table is skipped or emitted as -1 ("fail closed", [MDL]
+ *   _deepseek_v4_swa_slot_mapping), as each entry point states.
+ *
+ * Cache records ("pages")
+ * -----------------------
+ * A cache is `num_pages` pages of `page_stride` bytes; `block_size` token slots
+ * per page; slot s lives in page s / block_size at offset s % block_size.
+ *
+ * fp8_ds_mla record ([OPS] dequantize_deepseek_v4_fp8_ds_mla_cache,
+ * _fp8_ds_mla_cache_rows; [VLLM] quantize_and_insert_k_cache):
+ *   nope = head_dim - rope_dim, token_stride = nope + 2 * rope_dim.
+ *   page = [block_size x token_stride data][block_size x scale_bytes scales]
+ *   data  = nope E4M3 bytes, then rope_dim bf16 values (little-endian).
+ *   scales, is_ue8m0 = 1: head_dim/64 bytes, byte b = UE8M0 exponent of 64-block
+ *           b (value 2^(byte-127)); slots past the nope blocks are 0.  For
+ *           head_dim 512 / rope 64 that is 7 scales + 1 zero pad = 8 bytes and
+ *           the record is 584 bytes.
+ *   scales, is_ue8m0 = 0: head_dim/64 little-endian binary32 scales (4 bytes
+ *           each); slots past the nope blocks are 0.0.
+ *   page_stride >= block_size * (token_stride + scale_bytes).
+ *
+ * MXFP4 record ([OPS] write/read_deepseek_v4_indexer_mxfp4_cache):
+ *   page = [block_size x head_dim/2 value bytes][block_size x head_dim/32 scales]
+ *   value byte j holds element 2j in its low nibble, 2j+1 in its high nibble
+ *   (E2M1); scale byte b = E8M0 exponent of 32-block b.  68 bytes for 128 dims.
+ *
+ * Alignment required by the kernels (checked): cache base and page_stride
+ * multiples of 16 bytes; bf16 inputs/outputs 16-byte aligned with strides that
+ * are multiples of 8 elements; int32 index matrices 4-byte aligned.
+ */
+#ifndef PSK_H
+#define PSK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Identical to cudaStream_t; declared here so callers need no CUDA headers. */
+typedef struct CUstream_st* psk_stream_t;
+
+typedef enum psk_status {
+    PSK_OK = 0,
+    PSK_ERR_INVALID_ARGUMENT = 1,
+    PSK_ERR_UNSUPPORTED = 2,
+    PSK_ERR_CUDA = 3
+} psk_status;
+
+typedef enum psk_record {
+    PSK_REC_FP8_DS_MLA = 0,
+    PSK_REC_MXFP4 = 1
+} psk_record;
+
+/* Message describing the calling thread's most recent error ("" if none). */
+const char* psk_last_error(void);
+
+/* ABI revision of this header (bumped on any signature change). */
+int32_t psk_abi_version(void);
+
+/*
+ * quantize_and_insert_k_cache -- block-scaled FP8 quantize + paged insert.
+ * [VLLM] quantize_and_insert_k_cache; math of [OPS] _fp8_ds_mla_cache_rows.
+ *
+ *   k            bf16 [num_tokens, >= head_dim], row stride k_row_stride
+ *                (elements, multiple of 8).  Only the first num_tokens rows are
+ *                read: num_tokens is the length of slot_mapping, and k may have
+ *                more (data-parallel padding) rows.
+ *   slot_mapping int64 [num_tokens]; -1 (any negative) = skip the token.
+ *   k_cache      uint8 [num_pages, page_stride] fp8_ds_mla pages (written).
+ *   head_dim     multiple of 64 in [64, 1024]; rope_dim multiple of 64 in
+ *                [0, head_dim); the rope dims are the last rope_dim of each row
+ *                and are stored verbatim (the caller has already rotated them).
+ *   is_ue8m0     1: per 64-block e = ceil(log2(max(amax, 1e-4) / 448)) exactly,
+ *                   scale byte e + 127, codes RNE-E4M3(clamp(x * 2^-e, +-448)).
+ *                0: scale = max(amax, 1e-12) / 448 (binary32, stored as fp32),
+ *                   codes RNE-E4M3(clamp(x / scale, +-448)) with IEEE division.
+ *   err_count    nullable device int32: incremented (atomically) once per token
+ *                whose slot is >= num_pages * block_size; such tokens are
+ *                skipped.  The caller zeroes it when it wants a fresh count.
+ */
+psk_status quantize_and_insert_k_cache(
+    const void* k, int64_t k_row_stride, const int64_t* slot_mapping,
+    int64_t num_tokens, uint8_t* k_cache, int64_t num_pages,
+    int64_t page_stride, int32_t block_size, int32_t head_dim,
+    int32_t rope_dim, int32_t is_ue8m0, int32_t* err_count,
+    psk_stream_t stream);
+
+/*
+ * write_indexer_mxfp4_cache -- MXFP4 quantize + paged insert of indexer keys.
+ * [OPS] write_deepseek_v4_indexer_mxfp4_cache (layout) and
+ * read_deepseek_v4_indexer_mxfp4_cache (nibble order, scale meaning).
+ *
+ *   index_k      bf16 [num_tokens, >= head_dim], row stride k_row_stride.
+ *   slot_mapping int64 [num_tokens]; negative = skip.
+ *   cache        uint8 [num_pages, page_stride] MXFP4 pages (written).
+ *   head_dim     multiple of 32 in [32, 1024].
+ *   Per 32-block: e = ceil(log2(max(amax, 1e-4) / 6)) (the pages print no
+ *   writer rule; this is E8M0 = ceil-pow2(amax / 6)), scale byte
+ *   clamp(e + 127, 0, 254), codes RNE-E2M1 of x * 2^-e, saturating at 6.
+ *   err_count    as for quantize_and_insert_k_cache.
+ */
+psk_status write_indexer_mxfp4_cache(
+    const void* index_k, int64_t k_row_stride, const int64_t* slot_mapping,
+    int64_t num_tokens, uint8_t* cache, int64_t num_pages,
+    int64_t page_stride, int32_t block_size, int32_t head_dim,
+    int32_t* err_count, psk_stream_t stream);
+
+/*
+ * compute_global_topk_indices_and_lens -- local top-k -> global cache slots.
+ * [VLLM] compute_global_topk_indices_and_lens; called for decode in [BE]
+ * _decode_compressed_attention_indices_and_lens.
+ *
+ *   topk_local     int32 [num_tokens, topk], row stride topk_stride; -1 = none.
+ *   token_to_req   int32 [num_tokens] request of each token.
+ *   block_table    int32 [num_reqs, >= bt_width], row stride bt_stride; -1 = no
+ *                  page.
+ *   base_offsets   nullable int32 [num_reqs]: logical page of each row's first
+ *                  entry (0 when null).
+ *   is_valid_token nullable uint8 [num_tokens]: 0 marks a padding token.
+ *   out_indices    int32 [num_tokens, topk], row stride out_stride (written):
+ *                  out[t][j] = page * block_size + l % block_size with
+ *                  l = topk_local[t][j], page = block_table[r][l/block_size - base];
+ *                  -1 when l < 0, the logical page is outside [0, bt_width),
+ *                  the page is < 0, or the slot exceeds INT32_MAX.  Entries are
+ *                  not compacted.
+ *   out_lens       int32 [num_tokens]: number of entries >= 0 (0 for a padding
+ *                  token, whose entries are all -1; a token whose request index
+ *                  is outside [0, num_reqs) is treated as padding).
+ */
+psk_status compute_global_topk_indices_and_lens(
+    const int32_t* topk_local, int64_t topk_stride, int64_t num_tokens,
+    int32_t topk, const int32_t* token_to_req, const int32_t* block_table,
+    int64_t bt_stride, int32_t bt_width, int32_t num_reqs, int32_t block_size,
+    const int32_t* base_offsets, const uint8_t* is_valid_token,
+    int32_t* out_indices, int64_t out_stride, int32_t* out_lens,
+    psk_stream_t stream);
+
+/*
+ * combine_topk_swa_indices -- the fused sparse-index build.
+ * [VLLM] build_flashinfer_mixed_sparse_indices (single kernel for a
+ * decode-first batch); TokenSpeed calls the same step combine_topk_swa_indices.
+ *
+ *   query_start_loc int32 [num_reqs + 1]; seq_lens int32 [num_reqs];
+ *   token_to_req    int32 [num_tokens]; replay_start nullable int32 [num_reqs]
+ *                   (0 when null).  Token t of request r sits at
+ *                   pos = seq_lens[r] - (qsl[r+1] - qsl[r]) + (t - qsl[r])
+ *                   ([BE] _decode_positions_from_metadata).
+ *   swa_*           the sliding-window cache's block table (see
+ *                   compute_global_topk_indices_and_lens for the table/base
+ *                   convention) and page size.
+ *   comp_*          the compressed cache's block table; comp_block_table NULL
+ *                   means the SWA table (with its stride and width) is used.
+ *                   comp_base_offsets is independent of the table choice.
+ *   window          W >= 0; compress_ratio >= 1 (accepted for the signature;
+ *                   it does not change the result).
+ *   topk_local      int32 [num_tokens, topk], row stride topk_stride.
+ *   sparse_indices  int32 [num_tokens, window + roundup(topk, 4)], row stride
+ *                   out_stride (written):
+ *                   columns [0, W): slots of positions lo, lo+1, ..., pos with
+ *                     lo = max(replay_start[r], pos - W + 1, 0), left-aligned
+ *                     (oldest first), -1 after pos or where no page exists;
+ *                   columns [W, W + topk): top-k mapped through the compressed
+ *                     table exactly as compute_global_topk_indices_and_lens;
+ *                   remaining columns: -1 (rows start on 16-byte boundaries
+ *                     when out_stride is a multiple of 4).
+ *   lens            int32 [num_tokens]: entries >= 0 over all columns.
+ *   A padding token (is_valid_token 0 or request out of range): all -1, lens 0.
+ */
+psk_status combine_topk_swa_indices(
+    const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* token_to_req, const int32_t* replay_start, int32_t num_reqs,
+    int64_t num_tokens,
+    const int32_t* swa_block_table, int64_t swa_bt_stride, int32_t swa_bt_width,
+    const int32_t* swa_base_offsets, int32_t swa_block_size,
+    const int32_t* comp_block_table, int64_t comp_bt_stride,
+    int32_t comp_bt_width, const int32_t* comp_base_offsets,
+    int32_t comp_block_size, int32_t window, int32_t compress_ratio,
+    const int32_t* topk_local, int64_t topk_stride, int32_t topk,
+    const uint8_t* is_valid_token, int32_t* sparse_indices, int64_t out_stride,
+    int32_t* lens, psk_stream_t stream);
+
+/*
+ * dequantize_and_gather_k_cache -- index-keyed dequantize + gather.
+ * Index form of [VLLM] dequantize_and_gather_k_cache; per-row math of [OPS]
+ * dequantize_deepseek_v4_fp8_ds_mla_cache (record 0) and
+ * read_deepseek_v4_indexer_mxfp4_cache (record 1).
+ *
+ *   out          bf16; row (t, j) starts at out + t*out_stride_t + j*out_stride_j
+ *                (elements, multiples of 8) and holds head_dim values.
+ *   cache        uint8 [num_pages, page_stride] pages of the given record.
+ *   indices      int32 [rows, cols], row stride idx_stride: slot ids.
+ *   For s = indices[t][j]: s < 0 or s >= num_pages * block_size gives an
+ *   all-zero row.  Otherwise, fp8_ds_mla: nope dim d = bf16(e4m3 * 2^(scale-127))
+ *   (or * fp32 scale when is_ue8m0 = 0), rope dims copied bit for bit; MXFP4:
+ *   dim d = bf16(e2m1 * 2^(scale-127)).  Products are formed in binary32 and
+ *   rounded to bf16 (for UE8M0 scales the product is exact).
+ *   To gather the window columns from the SWA cache and the top-k columns from
+ *   the compressed cache, make two calls on column ranges of one index matrix
+ *   and one output (pointer offsets + strides), as a k_cache / extra_k_cache
+ *   pair is read ([BE] forward_deepseek_v4_decode).
+ */
+psk_status dequantize_and_gather_k_cache(
+    void* out, int64_t out_stride_t, int64_t out_stride_j,
+    const uint8_t* cache, int64_t num_pages, int64_t page_stride,
+    int32_t block_size, psk_record record, int32_t head_dim, int32_t rope_dim,
+    int32_t is_ue8m0, const int32_t* indices, int64_t idx_stride, int64_t rows,
+    int32_t cols, psk_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSK_H */

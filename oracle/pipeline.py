@@ -1,0 +1,55 @@
+"""One pipeline step computed by the CPU oracle (test infrastructure only).
+
+Mirrors the step order of the device pipeline on host numpy arrays, calling
+only the oracle: FP8 insert, MXFP4 insert, fused index build, the two-part FP8
+gather, the global top-k mapping and the MXFP4 gather.  For large workloads the
+gathers can be restricted to a sample of tokens (every other output is still
+computed in full).
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import numpy as np
+
+from . import (REC_FP8_DS_MLA, REC_MXFP4, combine_topk_swa_indices,
+               compute_global_topk_indices_and_lens, dequantize_and_gather_k_cache,
+               quantize_and_insert_k_cache, write_indexer_mxfp4_cache)
+
+
+def run_step(w, swa_cache: Optional[np.ndarray], comp_cache: Optional[np.ndarray],
+             index_cache: Optional[np.ndarray],
+             sample_tokens: Optional[Sequence[int]] = None) -> dict:
+    """Run one step; caches are updated in place.  Returns the outputs."""
+    res: dict = {"err": 0}
+    if w.has_fp8:
+        res["err"] += quantize_and_insert_k_cache(
+            w.k, w.insert_slots, swa_cache, w.swa_cache.block_size, w.head_dim, w.rope_dim)
+    if w.index_k is not None:
+        res["err"] += write_indexer_mxfp4_cache(
+            w.index_k, w.index_insert_slots, index_cache, w.index_cache.block_size,
+            w.index_head_dim)
+    toks = None if sample_tokens is None else np.asarray(sample_tokens, dtype=np.int64)
+    if w.has_fp8:
+        W = w.window
+        si, lens = combine_topk_swa_indices(
+            w.query_start_loc, w.seq_lens, w.token_to_req, w.replay_start, w.swa_block_table,
+            w.swa_cache.block_size, w.comp_block_table, w.comp_cache.block_size, W,
+            w.compress_ratio, w.topk_local, is_valid_token=w.is_valid_token)
+        res["sparse_indices"], res["lens"] = si, lens
+        rows = si if toks is None else si[toks]
+        g_swa = dequantize_and_gather_k_cache(swa_cache, w.swa_cache.block_size, REC_FP8_DS_MLA,
+                                              w.head_dim, w.rope_dim, np.ascontiguousarray(rows[:, :W]))
+        g_top = dequantize_and_gather_k_cache(comp_cache, w.comp_cache.block_size, REC_FP8_DS_MLA,
+                                              w.head_dim, w.rope_dim, np.ascontiguousarray(rows[:, W:]))
+        res["gathered"] = np.concatenate([g_swa, g_top], axis=1)
+    table = w.comp_block_table if w.comp_block_table is not None else w.swa_block_table
+    gt, gl = compute_global_topk_indices_and_lens(
+        w.topk_local, w.token_to_req, table, w.index_cache.block_size,
+        is_valid_token=w.is_valid_token)
+    res["global_topk"], res["global_lens"] = gt, gl
+    rows = gt if toks is None else gt[toks]
+    res["gathered_index"] = dequantize_and_gather_k_cache(
+        index_cache, w.index_cache.block_size, REC_MXFP4, w.index_head_dim, 0,
+        np.ascontiguousarray(rows))
+    return res

@@ -1,0 +1,307 @@
+// abi.cu -- the extern "C" entry points of libpsk (declared in include/psk.h).
+//
+// Each entry point validates its arguments on the host, returns
+// PSK_ERR_INVALID_ARGUMENT before touching the GPU when they are wrong,
+// returns PSK_OK without a launch when there is no work, and otherwise
+// launches exactly one kernel on the caller's stream.  Nothing here
+// allocates, synchronises or keeps state beyond the per-thread error text.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "launch.h"
+#include "psk.h"
+#include "psk_common.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+psk_status fail(psk_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+psk_status ok() {
+    g_last_error.clear();
+    return PSK_OK;
+}
+
+psk_status cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return ok();
+    return fail(PSK_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+#define CHECK(cond, ...)                                                \
+    do {                                                                \
+        if (!(cond)) return fail(PSK_ERR_INVALID_ARGUMENT, __VA_ARGS__); \
+    } while (0)
+
+bool fp8_head_dim_ok(int32_t d) { return d == 64 || d == 128 || d == 256 || d == 512 || d == 1024; }
+bool mxfp4_head_dim_ok(int32_t d) {
+    return d == 32 || d == 64 || d == 128 || d == 256 || d == 512 || d == 1024;
+}
+
+int64_t fp8_record_bytes(int32_t head_dim, int32_t rope_dim, int32_t ue8m0) {
+    return (int64_t)(head_dim - rope_dim) + 2 * (int64_t)rope_dim +
+           (int64_t)(head_dim / 64) * (ue8m0 ? 1 : 4);
+}
+
+psk_status check_cache(const uint8_t* cache, int64_t num_pages, int64_t page_stride,
+                       int32_t block_size, int64_t record_bytes) {
+    CHECK(cache != nullptr, "cache is null");
+    CHECK(num_pages >= 1, "num_pages must be >= 1 (got %lld)", (long long)num_pages);
+    CHECK(block_size >= 1, "block_size must be >= 1 (got %d)", block_size);
+    CHECK(page_stride >= (int64_t)block_size * record_bytes,
+          "page_stride %lld is smaller than block_size * record bytes = %lld",
+          (long long)page_stride, (long long)block_size * record_bytes);
+    CHECK(page_stride % 16 == 0, "page_stride must be a multiple of 16 bytes");
+    CHECK(aligned(cache, 16), "cache must be 16-byte aligned");
+    CHECK(num_pages <= INT64_MAX / page_stride, "cache size overflows int64");
+    return PSK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* psk_last_error(void) { return g_last_error.c_str(); }
+
+int32_t psk_abi_version(void) { return 1; }
+
+psk_status quantize_and_insert_k_cache(const void* k, int64_t k_row_stride,
+                                       const int64_t* slot_mapping, int64_t num_tokens,
+                                       uint8_t* k_cache, int64_t num_pages, int64_t page_stride,
+                                       int32_t block_size, int32_t head_dim, int32_t rope_dim,
+                                       int32_t is_ue8m0, int32_t* err_count,
+                                       psk_stream_t stream) {
+    CHECK(num_tokens >= 0, "num_tokens must be >= 0");
+    CHECK(is_ue8m0 == 0 || is_ue8m0 == 1, "is_ue8m0 must be 0 or 1");
+    CHECK(fp8_head_dim_ok(head_dim), "head_dim must be one of 64, 128, 256, 512, 1024 (got %d)",
+          head_dim);
+    CHECK(rope_dim >= 0 && rope_dim < head_dim && rope_dim % 64 == 0,
+          "rope_dim must be a multiple of 64 in [0, head_dim) (got %d)", rope_dim);
+    psk_status st = check_cache(k_cache, num_pages, page_stride, block_size,
+                                fp8_record_bytes(head_dim, rope_dim, is_ue8m0));
+    if (st != PSK_OK) return st;
+    if (num_tokens == 0) return ok();
+    CHECK(k != nullptr && slot_mapping != nullptr, "k and slot_mapping must be non-null");
+    CHECK(aligned(k, 16), "k must be 16-byte aligned");
+    CHECK(k_row_stride >= head_dim && k_row_stride % 8 == 0,
+          "k_row_stride must be >= head_dim and a multiple of 8 elements");
+    CHECK(aligned(slot_mapping, 8), "slot_mapping must be 8-byte aligned");
+    CHECK(err_count == nullptr || aligned(err_count, 4), "err_count must be 4-byte aligned");
+    psk::InsertParams p{k, k_row_stride, slot_mapping, num_tokens, k_cache, num_pages,
+                        page_stride, block_size, head_dim, rope_dim, is_ue8m0, err_count};
+    return cuda_status(psk::launch_fp8_insert(p, reinterpret_cast<cudaStream_t>(stream)),
+                       "quantize_and_insert_k_cache launch");
+}
+
+psk_status write_indexer_mxfp4_cache(const void* index_k, int64_t k_row_stride,
+                                     const int64_t* slot_mapping, int64_t num_tokens,
+                                     uint8_t* cache, int64_t num_pages, int64_t page_stride,
+                                     int32_t block_size, int32_t head_dim, int32_t* err_count,
+                                     psk_stream_t stream) {
+    CHECK(num_tokens >= 0, "num_tokens must be >= 0");
+    CHECK(mxfp4_head_dim_ok(head_dim),
+          "head_dim must be one of 32, 64, 128, 256, 512, 1024 (got %d)", head_dim);
+    psk_status st = check_cache(cache, num_pages, page_stride, block_size,
+                                head_dim / 2 + head_dim / 32);
+    if (st != PSK_OK) return st;
+    if (num_tokens == 0) return ok();
+    CHECK(index_k != nullptr && slot_mapping != nullptr,
+          "index_k and slot_mapping must be non-null");
+    CHECK(aligned(index_k, 16), "index_k must be 16-byte aligned");
+    CHECK(k_row_stride >= head_dim && k_row_stride % 8 == 0,
+          "k_row_stride must be >= head_dim and a multiple of 8 elements");
+    CHECK(aligned(slot_mapping, 8), "slot_mapping must be 8-byte aligned");
+    CHECK(err_count == nullptr || aligned(err_count, 4), "err_count must be 4-byte aligned");
+    psk::InsertParams p{index_k, k_row_stride, slot_mapping, num_tokens, cache, num_pages,
+                        page_stride, block_size, head_dim, 0, 1, err_count};
+    return cuda_status(psk::launch_mxfp4_insert(p, reinterpret_cast<cudaStream_t>(stream)),
+                       "write_indexer_mxfp4_cache launch");
+}
+
+psk_status compute_global_topk_indices_and_lens(
+    const int32_t* topk_local, int64_t topk_stride, int64_t num_tokens, int32_t topk,
+    const int32_t* token_to_req, const int32_t* block_table, int64_t bt_stride, int32_t bt_width,
+    int32_t num_reqs, int32_t block_size, const int32_t* base_offsets,
+    const uint8_t* is_valid_token, int32_t* out_indices, int64_t out_stride, int32_t* out_lens,
+    psk_stream_t stream) {
+    CHECK(num_tokens >= 0, "num_tokens must be >= 0");
+    CHECK(topk >= 0, "topk must be >= 0");
+    CHECK(block_size >= 1, "block_size must be >= 1");
+    CHECK(bt_width >= 0 && bt_stride >= bt_width, "need 0 <= bt_width <= bt_stride");
+    CHECK(topk_stride >= topk && out_stride >= topk, "row strides must be >= topk");
+    if (num_tokens == 0) return ok();
+    CHECK(num_reqs >= 1, "num_reqs must be >= 1");
+    CHECK(token_to_req && out_lens, "token_to_req and out_lens must be non-null");
+    CHECK(topk == 0 || (topk_local && out_indices), "topk_local and out_indices must be non-null");
+    CHECK(bt_width == 0 || block_table, "block_table must be non-null");
+    CHECK(aligned(topk_local, 4) && aligned(out_indices, 4) && aligned(token_to_req, 4) &&
+              aligned(block_table, 4) && aligned(base_offsets, 4) && aligned(out_lens, 4),
+          "int32 arrays must be 4-byte aligned");
+    psk::IndexParams p{};
+    p.t2r = token_to_req;
+    p.num_reqs = num_reqs;
+    p.num_tokens = num_tokens;
+    p.comp_bt = block_table;
+    p.comp_stride = bt_stride;
+    p.comp_width = bt_width;
+    p.comp_base = base_offsets;
+    p.comp_bs = block_size;
+    p.comp_shift = psk::log2_if_pow2(block_size);
+    p.window = 0;
+    p.topk = topk;
+    p.out_cols = topk;
+    p.topk_local = topk_local;
+    p.topk_stride = topk_stride;
+    p.valid = is_valid_token;
+    p.out = out_indices;
+    p.out_stride = out_stride;
+    p.lens = out_lens;
+    return cuda_status(psk::launch_index_build(p, false, reinterpret_cast<cudaStream_t>(stream)),
+                       "compute_global_topk_indices_and_lens launch");
+}
+
+psk_status combine_topk_swa_indices(
+    const int32_t* query_start_loc, const int32_t* seq_lens, const int32_t* token_to_req,
+    const int32_t* replay_start, int32_t num_reqs, int64_t num_tokens,
+    const int32_t* swa_block_table, int64_t swa_bt_stride, int32_t swa_bt_width,
+    const int32_t* swa_base_offsets, int32_t swa_block_size, const int32_t* comp_block_table,
+    int64_t comp_bt_stride, int32_t comp_bt_width, const int32_t* comp_base_offsets,
+    int32_t comp_block_size, int32_t window, int32_t compress_ratio, const int32_t* topk_local,
+    int64_t topk_stride, int32_t topk, const uint8_t* is_valid_token, int32_t* sparse_indices,
+    int64_t out_stride, int32_t* lens, psk_stream_t stream) {
+    CHECK(num_tokens >= 0, "num_tokens must be >= 0");
+    CHECK(window >= 0 && topk >= 0, "window and topk must be >= 0");
+    CHECK(compress_ratio >= 1, "compress_ratio must be >= 1");
+    CHECK(swa_block_size >= 1 && comp_block_size >= 1, "block sizes must be >= 1");
+    CHECK(swa_bt_width >= 0 && swa_bt_stride >= swa_bt_width,
+          "need 0 <= swa_bt_width <= swa_bt_stride");
+    if (comp_block_table != nullptr) {
+        CHECK(comp_bt_width >= 0 && comp_bt_stride >= comp_bt_width,
+              "need 0 <= comp_bt_width <= comp_bt_stride");
+    }
+    const int64_t padded = ((int64_t)topk + 3) / 4 * 4;
+    const int64_t cols = (int64_t)window + padded;
+    CHECK(cols <= INT32_MAX, "window + padded topk overflows int32");
+    CHECK(topk_stride >= topk, "topk_stride must be >= topk");
+    CHECK(out_stride >= cols, "out_stride must be >= window + roundup(topk, 4)");
+    if (num_tokens == 0) return ok();
+    CHECK(num_reqs >= 1, "num_reqs must be >= 1");
+    CHECK(query_start_loc && seq_lens && token_to_req && sparse_indices && lens,
+          "query_start_loc, seq_lens, token_to_req, sparse_indices and lens must be non-null");
+    CHECK(topk == 0 || topk_local, "topk_local must be non-null");
+    CHECK(swa_bt_width == 0 || swa_block_table, "swa_block_table must be non-null");
+    CHECK(aligned(query_start_loc, 4) && aligned(seq_lens, 4) && aligned(token_to_req, 4) &&
+              aligned(replay_start, 4) && aligned(swa_block_table, 4) &&
+              aligned(swa_base_offsets, 4) && aligned(comp_block_table, 4) &&
+              aligned(comp_base_offsets, 4) && aligned(topk_local, 4) &&
+              aligned(sparse_indices, 4) && aligned(lens, 4),
+          "int32 arrays must be 4-byte aligned");
+    psk::IndexParams p{};
+    p.qsl = query_start_loc;
+    p.seq_lens = seq_lens;
+    p.t2r = token_to_req;
+    p.replay = replay_start;
+    p.num_reqs = num_reqs;
+    p.num_tokens = num_tokens;
+    p.swa_bt = swa_block_table;
+    p.swa_stride = swa_bt_stride;
+    p.swa_width = swa_bt_width;
+    p.swa_base = swa_base_offsets;
+    p.swa_bs = swa_block_size;
+    p.swa_shift = psk::log2_if_pow2(swa_block_size);
+    if (comp_block_table == nullptr) {
+        p.comp_bt = swa_block_table;
+        p.comp_stride = swa_bt_stride;
+        p.comp_width = swa_bt_width;
+    } else {
+        p.comp_bt = comp_block_table;
+        p.comp_stride = comp_bt_stride;
+        p.comp_width = comp_bt_width;
+    }
+    p.comp_base = comp_base_offsets;
+    p.comp_bs = comp_block_size;
+    p.comp_shift = psk::log2_if_pow2(comp_block_size);
+    p.window = window;
+    p.topk = topk;
+    p.out_cols = (int32_t)cols;
+    p.topk_local = topk_local;
+    p.topk_stride = topk_stride;
+    p.valid = is_valid_token;
+    p.out = sparse_indices;
+    p.out_stride = out_stride;
+    p.lens = lens;
+    return cuda_status(psk::launch_index_build(p, true, reinterpret_cast<cudaStream_t>(stream)),
+                       "combine_topk_swa_indices launch");
+}
+
+psk_status dequantize_and_gather_k_cache(void* out, int64_t out_stride_t, int64_t out_stride_j,
+                                         const uint8_t* cache, int64_t num_pages,
+                                         int64_t page_stride, int32_t block_size,
+                                         psk_record record, int32_t head_dim, int32_t rope_dim,
+                                         int32_t is_ue8m0, const int32_t* indices,
+                                         int64_t idx_stride, int64_t rows, int32_t cols,
+                                         psk_stream_t stream) {
+    CHECK(rows >= 0 && cols >= 0, "rows and cols must be >= 0");
+    CHECK(record == PSK_REC_FP8_DS_MLA || record == PSK_REC_MXFP4, "unknown record %d",
+          (int)record);
+    int64_t rec_bytes;
+    if (record == PSK_REC_FP8_DS_MLA) {
+        CHECK(is_ue8m0 == 0 || is_ue8m0 == 1, "is_ue8m0 must be 0 or 1");
+        CHECK(fp8_head_dim_ok(head_dim),
+              "head_dim must be one of 64, 128, 256, 512, 1024 (got %d)", head_dim);
+        CHECK(rope_dim >= 0 && rope_dim < head_dim && rope_dim % 64 == 0,
+              "rope_dim must be a multiple of 64 in [0, head_dim) (got %d)", rope_dim);
+        rec_bytes = fp8_record_bytes(head_dim, rope_dim, is_ue8m0);
+    } else {
+        CHECK(mxfp4_head_dim_ok(head_dim),
+              "head_dim must be one of 32, 64, 128, 256, 512, 1024 (got %d)", head_dim);
+        CHECK(rope_dim == 0, "rope_dim must be 0 for the MXFP4 record");
+        rec_bytes = head_dim / 2 + head_dim / 32;
+    }
+    psk_status st = check_cache(cache, num_pages, page_stride, block_size, rec_bytes);
+    if (st != PSK_OK) return st;
+    CHECK(idx_stride >= cols, "idx_stride must be >= cols");
+    if (rows == 0 || cols == 0) return ok();
+    CHECK(out != nullptr && indices != nullptr, "out and indices must be non-null");
+    CHECK(aligned(out, 16), "out must be 16-byte aligned");
+    CHECK(out_stride_t >= 0 && out_stride_j >= 0 && out_stride_t % 8 == 0 &&
+              out_stride_j % 8 == 0,
+          "output strides must be non-negative multiples of 8 elements");
+    CHECK(aligned(indices, 4), "indices must be 4-byte aligned");
+    CHECK(rows <= INT64_MAX / (cols > 0 ? cols : 1), "rows * cols overflows");
+    psk::GatherParams p{static_cast<uint16_t*>(out), out_stride_t, out_stride_j, cache,
+                        num_pages, page_stride, block_size, (int32_t)record, head_dim,
+                        rope_dim, is_ue8m0, indices, idx_stride, rows, cols};
+    return cuda_status(psk::launch_gather(p, reinterpret_cast<cudaStream_t>(stream)),
+                       "dequantize_and_gather_k_cache launch");
+}
+
+}  // extern "C"
+
+namespace psk {
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 148;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+}  // namespace psk

@@ -1,0 +1,87 @@
+// launch.h -- host-side launchers behind the libpsk C ABI (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace psk {
+
+// Number of SMs on the current device (queried once per device).
+int sm_count();
+
+struct InsertParams {
+    const void* k;
+    int64_t k_row_stride;
+    const int64_t* slots;
+    int64_t num_tokens;
+    uint8_t* cache;
+    int64_t num_pages;
+    int64_t page_stride;
+    int32_t block_size;
+    int32_t head_dim;
+    int32_t rope_dim;   // fp8 record only
+    int32_t is_ue8m0;   // fp8 record only
+    int32_t* err_count;
+};
+
+cudaError_t launch_fp8_insert(const InsertParams& p, cudaStream_t stream);
+cudaError_t launch_mxfp4_insert(const InsertParams& p, cudaStream_t stream);
+
+struct IndexParams {
+    const int32_t* qsl;
+    const int32_t* seq_lens;
+    const int32_t* t2r;
+    const int32_t* replay;
+    int32_t num_reqs;
+    int64_t num_tokens;
+    const int32_t* swa_bt;
+    int64_t swa_stride;
+    int32_t swa_width;
+    const int32_t* swa_base;
+    int32_t swa_bs;
+    int32_t swa_shift;   // log2(swa_bs) or -1
+    const int32_t* comp_bt;
+    int64_t comp_stride;
+    int32_t comp_width;
+    const int32_t* comp_base;
+    int32_t comp_bs;
+    int32_t comp_shift;
+    int32_t window;
+    int32_t topk;
+    int32_t out_cols;
+    const int32_t* topk_local;
+    int64_t topk_stride;
+    const uint8_t* valid;
+    int32_t* out;
+    int64_t out_stride;
+    int32_t* lens;
+    // launch shape, filled by the launcher
+    int32_t tokens_per_cta;
+    int32_t warps_per_token;
+    int32_t stage_comp;  // entries of the compressed row staged in shared memory
+};
+
+// has_swa = true: the fused window + top-k build; false: top-k mapping only.
+cudaError_t launch_index_build(IndexParams p, bool has_swa, cudaStream_t stream);
+
+struct GatherParams {
+    uint16_t* out;
+    int64_t out_stride_t;
+    int64_t out_stride_j;
+    const uint8_t* cache;
+    int64_t num_pages;
+    int64_t page_stride;
+    int32_t block_size;
+    int32_t record;
+    int32_t head_dim;
+    int32_t rope_dim;
+    int32_t is_ue8m0;
+    const int32_t* idx;
+    int64_t idx_stride;
+    int64_t rows;
+    int32_t cols;
+};
+
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
+
+}  // namespace psk

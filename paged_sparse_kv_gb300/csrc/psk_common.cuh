@@ -1,0 +1,161 @@
+// psk_common.cuh -- device helpers shared by the libpsk kernels (sm_103a).
+//
+// Conversions go through the PTX `cvt` forms for FP8/FP4 (round to nearest
+// even, satfinite) and bf16; exponent work is done on binary32 bit patterns.
+// Build without --use_fast_math: every product and quotient here must be the
+// IEEE-rounded one, with subnormals kept.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace psk {
+
+constexpr int kWarp = 32;
+
+// ---- memory ----------------------------------------------------------------
+
+// 16-byte read-only load that does not allocate in L1 (rows read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint2 ld_nc_v2(const void* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
+    uint32_t r;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_nc_u8(const void* p) {
+    uint16_t r;
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+
+// Streaming (evict-first) stores for outputs that are not re-read here.
+__device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ void st_v2(void* p, uint2 v) {
+    asm volatile("st.global.v2.u32 [%0], {%1,%2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// ---- bf16 / binary32 ----------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two binary32 -> packed bf16x2 (lo in bits 0..15), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 2^k as binary32 for k in [-149, 128] (k = 128 gives +inf).
+__device__ __forceinline__ float exp2_int(int k) {
+    if (k >= -126) return __uint_as_float((uint32_t)(k + 127) << 23);
+    return __uint_as_float(1u << (k + 149));
+}
+
+// Smallest e with 2^e >= q for finite q > 0 (normal q): read off the bits.
+// q = +inf gives 128.
+__device__ __forceinline__ int ceil_log2_pos(float q) {
+    const uint32_t b = __float_as_uint(q);
+    const int e = (int)((b >> 23) & 0xFFu) - 127;
+    return e + ((b & 0x7FFFFFu) != 0u ? 1 : 0);
+}
+
+// Decode of a UE8M0 byte: 2^(b - 127) as binary32 (b = 255 -> +inf).
+__device__ __forceinline__ float ue8m0_scale(uint32_t b) {
+    return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
+}
+
+// ---- FP8 E4M3 / FP4 E2M1 --------------------------------------------------------
+
+// Two binary32 -> two E4M3 bytes (lo in bits 0..7), RNE, satfinite.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two binary32 -> two E2M1 nibbles (lo in bits 0..3), RNE, satfinite.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+    uint16_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u16.u8 %0, t;\n\t}"
+        : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two E4M3 bytes (bits 0..15) -> f16x2, exact.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_to_f16x2(uint32_t two_bytes) {
+    uint32_t r;
+    const uint16_t in = (uint16_t)two_bytes;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(in));
+    return r;
+}
+
+// Two E2M1 nibbles (bits 0..7) -> f16x2, exact.
+__device__ __forceinline__ uint32_t cvt_e2m1x2_to_f16x2(uint32_t byte) {
+    uint32_t r;
+    const uint16_t in = (uint16_t)byte;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.u8.u16 t, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(r) : "h"(in));
+    return r;
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t h2) {
+    float f;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(h2));
+    return f;
+}
+
+__device__ __forceinline__ float f16_hi(uint32_t h2) {
+    float f;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(h2));
+    return f;
+}
+
+// Clamp to [-lim, lim] keeping NaN and the sign of zero.
+__device__ __forceinline__ float clamp_sym(float v, float lim) {
+    return v > lim ? lim : (v < -lim ? -lim : v);
+}
+
+// ---- integer helpers ---------------------------------------------------------------
+
+__host__ __device__ __forceinline__ int log2_if_pow2(int x) {
+    if (x <= 0 || (x & (x - 1))) return -1;
+    int s = 0;
+    while ((1 << s) < x) ++s;
+    return s;
+}
+
+}  // namespace psk

@@ -1,0 +1,173 @@
+"""PyTorch-facing wrappers of the libpsk C ABI (same names as include/psk.h).
+
+Argument marshalling only: every step runs in the CUDA kernels of libpsk.
+Tensors must live on a CUDA device; each call launches on the current torch
+stream of that device and returns without synchronising.  Errors from the
+library raise :class:`PskError`.
+
+Cache tensors are uint8 with pages along dim 0: ``num_pages = cache.shape[0]``
+and ``page_stride = cache.stride(0)`` bytes (a 2-D ``[pages, bytes]`` tensor or
+a 3-D ``[pages, block_size, record_bytes]`` view both work).
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _abi
+from ._abi import PSK_REC_FP8_DS_MLA, PSK_REC_MXFP4, PskError  # noqa: F401
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(dev: torch.device) -> int:
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libpsk operates on CUDA tensors only (no CPU fallback)")
+
+
+def _need(t: torch.Tensor, dtype: torch.dtype, name: str):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _pages(cache: torch.Tensor):
+    _need(cache, torch.uint8, "cache")
+    if cache.dim() < 2 or not cache[0].is_contiguous():
+        raise ValueError("cache must be [num_pages, ...] uint8 with contiguous pages")
+    return cache.shape[0], cache.stride(0)
+
+
+def _rows(t: torch.Tensor, name: str):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D with unit inner stride")
+    return t.stride(0)
+
+
+def quantize_and_insert_k_cache(k: torch.Tensor, k_cache: torch.Tensor,
+                                slot_mapping: torch.Tensor, block_size: int = 64, *,
+                                rope_dim: int = 64, is_ue8m0: bool = True,
+                                head_dim: Optional[int] = None,
+                                err_count: Optional[torch.Tensor] = None) -> None:
+    """FP8 (fp8_ds_mla) quantize + paged insert of ``k`` [N', D] bf16 at
+    ``slot_mapping`` [N] int64 (N <= N'; -1 skips)."""
+    _need_cuda(k, k_cache, slot_mapping, err_count)
+    _need(k, torch.bfloat16, "k")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    if err_count is not None:
+        _need(err_count, torch.int32, "err_count")
+    if slot_mapping.dim() != 1 or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be 1-D contiguous")
+    D = k.shape[1] if head_dim is None else head_dim
+    num_pages, page_stride = _pages(k_cache)
+    _abi.call("quantize_and_insert_k_cache", _ptr(k), _rows(k, "k"), _ptr(slot_mapping),
+              slot_mapping.shape[0], _ptr(k_cache), num_pages, page_stride, block_size, D,
+              rope_dim, int(bool(is_ue8m0)), _ptr(err_count), _stream(k.device))
+
+
+def write_indexer_mxfp4_cache(index_k: torch.Tensor, cache: torch.Tensor,
+                              slot_mapping: torch.Tensor, block_size: int = 64, *,
+                              err_count: Optional[torch.Tensor] = None) -> None:
+    """MXFP4 quantize + paged insert of indexer keys ``index_k`` [N', D] bf16."""
+    _need_cuda(index_k, cache, slot_mapping, err_count)
+    _need(index_k, torch.bfloat16, "index_k")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    if slot_mapping.dim() != 1 or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be 1-D contiguous")
+    num_pages, page_stride = _pages(cache)
+    _abi.call("write_indexer_mxfp4_cache", _ptr(index_k), _rows(index_k, "index_k"),
+              _ptr(slot_mapping), slot_mapping.shape[0], _ptr(cache), num_pages, page_stride,
+              block_size, index_k.shape[1], _ptr(err_count), _stream(index_k.device))
+
+
+def compute_global_topk_indices_and_lens(topk_indices: torch.Tensor,
+                                         token_to_req_indices: torch.Tensor,
+                                         block_table: torch.Tensor, block_size: int,
+                                         is_valid_token: Optional[torch.Tensor] = None, *,
+                                         base_offsets: Optional[torch.Tensor] = None,
+                                         out: Optional[torch.Tensor] = None,
+                                         lens: Optional[torch.Tensor] = None):
+    """Map local top-k [T, K] to global slots; returns (indices [T, K], lens [T])."""
+    _need_cuda(topk_indices, token_to_req_indices, block_table, is_valid_token, base_offsets)
+    for t, n in ((topk_indices, "topk_indices"), (token_to_req_indices, "token_to_req"),
+                 (block_table, "block_table")):
+        _need(t, torch.int32, n)
+    T, K = topk_indices.shape
+    if out is None:
+        out = torch.empty((T, K), dtype=torch.int32, device=topk_indices.device)
+    if lens is None:
+        lens = torch.empty((T,), dtype=torch.int32, device=topk_indices.device)
+    valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
+    _abi.call("compute_global_topk_indices_and_lens", _ptr(topk_indices),
+              _rows(topk_indices, "topk_indices"), T, K, _ptr(token_to_req_indices),
+              _ptr(block_table), _rows(block_table, "block_table"), block_table.shape[1],
+              block_table.shape[0], block_size, _ptr(base_offsets), _ptr(valid), _ptr(out),
+              _rows(out, "out"), _ptr(lens), _stream(topk_indices.device))
+    return out, lens
+
+
+def combine_topk_swa_indices(query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
+                             token_to_req_indices: torch.Tensor,
+                             replay_start: Optional[torch.Tensor],
+                             swa_block_table: torch.Tensor, swa_block_size: int,
+                             compressed_block_table: Optional[torch.Tensor],
+                             compressed_block_size: int, window_size: int,
+                             compress_ratio: int, topk_indices: torch.Tensor, *,
+                             swa_base_offsets: Optional[torch.Tensor] = None,
+                             compressed_base_offsets: Optional[torch.Tensor] = None,
+                             is_valid_token: Optional[torch.Tensor] = None,
+                             num_tokens: Optional[int] = None,
+                             out: Optional[torch.Tensor] = None,
+                             lens: Optional[torch.Tensor] = None):
+    """Fused sparse-index build; returns (sparse_indices [T, W + roundup4(K)], lens [T])."""
+    _need_cuda(query_start_loc, seq_lens, token_to_req_indices, replay_start, swa_block_table,
+               compressed_block_table, topk_indices, is_valid_token)
+    dev = topk_indices.device
+    T = topk_indices.shape[0] if num_tokens is None else num_tokens
+    K = topk_indices.shape[1]
+    width = window_size + (K + 3) // 4 * 4
+    if out is None:
+        out = torch.empty((T, width), dtype=torch.int32, device=dev)
+    if lens is None:
+        lens = torch.empty((T,), dtype=torch.int32, device=dev)
+    cbt = compressed_block_table
+    valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
+    _abi.call("combine_topk_swa_indices", _ptr(query_start_loc), _ptr(seq_lens),
+              _ptr(token_to_req_indices), _ptr(replay_start), seq_lens.shape[0], T,
+              _ptr(swa_block_table), _rows(swa_block_table, "swa_block_table"),
+              swa_block_table.shape[1], _ptr(swa_base_offsets), swa_block_size,
+              _ptr(cbt), _rows(cbt, "compressed_block_table") if cbt is not None else 0,
+              cbt.shape[1] if cbt is not None else 0, _ptr(compressed_base_offsets),
+              compressed_block_size, window_size, compress_ratio, _ptr(topk_indices),
+              _rows(topk_indices, "topk_indices"), K, _ptr(valid), _ptr(out), _rows(out, "out"),
+              _ptr(lens), _stream(dev))
+    return out, lens
+
+
+def dequantize_and_gather_k_cache(out: torch.Tensor, cache: torch.Tensor,
+                                  indices: torch.Tensor, block_size: int, *,
+                                  record: int = PSK_REC_FP8_DS_MLA, rope_dim: int = 64,
+                                  is_ue8m0: bool = True) -> torch.Tensor:
+    """Gather + dequantize rows ``indices`` [T, C] into ``out`` [T, C, D] bf16
+    (``out`` may be a strided view, e.g. a column range of a wider output)."""
+    _need_cuda(out, cache, indices)
+    _need(out, torch.bfloat16, "out")
+    _need(indices, torch.int32, "indices")
+    if out.dim() != 3 or out.stride(2) != 1:
+        raise ValueError("out must be [T, C, D] with unit inner stride")
+    T, C = indices.shape
+    if out.shape[0] != T or out.shape[1] != C:
+        raise ValueError(f"out {tuple(out.shape)} does not match indices {tuple(indices.shape)}")
+    num_pages, page_stride = _pages(cache)
+    _abi.call("dequantize_and_gather_k_cache", _ptr(out), out.stride(0), out.stride(1),
+              _ptr(cache), num_pages, page_stride, block_size, record, out.shape[2],
+              rope_dim if record == PSK_REC_FP8_DS_MLA else 0, int(bool(is_ue8m0)),
+              _ptr(indices), _rows(indices, "indices"), T, C, _stream(out.device))
+    return out

@@ -1,0 +1,153 @@
+"""One step of the paged K-cache pipeline on the device, for a synthetic workload.
+
+A step runs every hot-path row over one batch, in this order:
+
+  1. quantize_and_insert_k_cache   new K rows -> SWA cache (FP8 fp8_ds_mla)
+  2. write_indexer_mxfp4_cache     new indexer keys -> indexer cache (MXFP4)
+  3. combine_topk_swa_indices      window + top-k -> sparse_indices, lens
+  4. dequantize_and_gather_k_cache window columns from the SWA cache and
+                                   top-k columns from the compressed cache
+                                   (two launches into one [T, W+P, D] output)
+  5. compute_global_topk_indices_and_lens  top-k -> indexer-cache slots
+  6. dequantize_and_gather_k_cache those slots from the MXFP4 indexer cache
+
+Workloads without an FP8 part (the MXFP4 indexer workload) run 2, 5 and 6.
+All buffers are allocated once here; ``step()`` only launches kernels.
+"""
+from __future__ import annotations
+
+from typing import Callable, Optional
+
+import numpy as np
+import torch
+
+from . import ops
+from .synthetic import Workload
+
+
+def _dev_i32(a: Optional[np.ndarray], dev) -> Optional[torch.Tensor]:
+    if a is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+
+def _dev_i64(a: Optional[np.ndarray], dev) -> Optional[torch.Tensor]:
+    if a is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int64)).to(dev)
+
+
+def _dev_bf16(a: Optional[np.ndarray], dev) -> Optional[torch.Tensor]:
+    if a is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+class Pipeline:
+    """Device state for one workload: inputs, caches and outputs."""
+
+    def __init__(self, w: Workload, device: torch.device | str = "cuda:0"):
+        dev = torch.device(device)
+        self.w = w
+        self.dev = dev
+        self.k = _dev_bf16(w.k, dev)
+        self.insert_slots = _dev_i64(w.insert_slots, dev)
+        self.index_k = _dev_bf16(w.index_k, dev)
+        self.index_insert_slots = _dev_i64(w.index_insert_slots, dev)
+        self.qsl = _dev_i32(w.query_start_loc, dev)
+        self.seq_lens = _dev_i32(w.seq_lens, dev)
+        self.t2r = _dev_i32(w.token_to_req, dev)
+        self.replay = _dev_i32(w.replay_start, dev)
+        self.valid = None if w.is_valid_token is None else torch.from_numpy(
+            np.ascontiguousarray(w.is_valid_token, dtype=np.uint8)).to(dev)
+        self.swa_bt = _dev_i32(w.swa_block_table, dev)
+        self.comp_bt = _dev_i32(w.comp_block_table, dev)
+        self.topk = _dev_i32(w.topk_local, dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def cache(g):
+            return None if g is None else torch.zeros((g.num_pages, g.page_stride),
+                                                      dtype=torch.uint8, device=dev)
+        self.swa_cache = cache(w.swa_cache)
+        # the compressed cache is its own buffer even when it shares the SWA table
+        self.comp_cache = cache(w.comp_cache)
+        self.index_cache = cache(w.index_cache)
+
+        T, K = w.num_tokens, w.topk
+        self.cols = w.window + w.padded_topk
+        if w.has_fp8:
+            self.sparse_indices = torch.empty((T, self.cols), dtype=torch.int32, device=dev)
+            self.lens = torch.empty((T,), dtype=torch.int32, device=dev)
+            self.gathered = torch.empty((T, self.cols, w.head_dim), dtype=torch.bfloat16,
+                                        device=dev)
+        else:
+            self.sparse_indices = self.lens = self.gathered = None
+        self.global_topk = torch.empty((T, K), dtype=torch.int32, device=dev)
+        self.global_lens = torch.empty((T,), dtype=torch.int32, device=dev)
+        self.gathered_index = torch.empty((T, K, w.index_head_dim), dtype=torch.bfloat16,
+                                          device=dev)
+
+    # the indexer cache follows the compressed table
+    @property
+    def index_table(self) -> torch.Tensor:
+        return self.comp_bt if self.comp_bt is not None else self.swa_bt
+
+    def fill_caches_with_quantized_rows(self, seed: int = 1234, chunk: int = 1 << 18) -> None:
+        """Fill every slot of every cache with quantized N(0,1) rows, through the
+        library's own inserts (used by the benchmark to give the gathers real
+        records to read)."""
+        g = torch.Generator(device=self.dev).manual_seed(seed)
+        w = self.w
+        for cache, geom, fp8 in ((self.swa_cache, w.swa_cache, True),
+                                 (self.comp_cache, w.comp_cache, True),
+                                 (self.index_cache, w.index_cache, False)):
+            if cache is None:
+                continue
+            cap = geom.num_pages * geom.block_size
+            D = w.head_dim if fp8 else w.index_head_dim
+            for s0 in range(0, cap, chunk):
+                n = min(chunk, cap - s0)
+                rows = torch.randn((n, D), generator=g, device=self.dev).to(torch.bfloat16)
+                slots = torch.arange(s0, s0 + n, dtype=torch.int64, device=self.dev)
+                if fp8:
+                    ops.quantize_and_insert_k_cache(rows, cache, slots, geom.block_size,
+                                                    rope_dim=w.rope_dim)
+                else:
+                    ops.write_indexer_mxfp4_cache(rows, cache, slots, geom.block_size)
+
+    def launches(self) -> list[tuple[str, Callable[[], None]]]:
+        """The step as a list of (kernel name, launch) pairs, in order."""
+        w = self.w
+        L: list[tuple[str, Callable[[], None]]] = []
+        if w.has_fp8:
+            L.append(("quantize_and_insert_k_cache", lambda: ops.quantize_and_insert_k_cache(
+                self.k, self.swa_cache, self.insert_slots, w.swa_cache.block_size,
+                rope_dim=w.rope_dim, err_count=self.err)))
+        if self.index_k is not None:
+            L.append(("write_indexer_mxfp4_cache", lambda: ops.write_indexer_mxfp4_cache(
+                self.index_k, self.index_cache, self.index_insert_slots,
+                w.index_cache.block_size, err_count=self.err)))
+        if w.has_fp8:
+            W = w.window
+            L.append(("combine_topk_swa_indices", lambda: ops.combine_topk_swa_indices(
+                self.qsl, self.seq_lens, self.t2r, self.replay, self.swa_bt,
+                w.swa_cache.block_size, self.comp_bt, w.comp_cache.block_size, W,
+                w.compress_ratio, self.topk, is_valid_token=self.valid,
+                out=self.sparse_indices, lens=self.lens)))
+            L.append(("dequantize_and_gather_k_cache[swa]", lambda: ops.dequantize_and_gather_k_cache(
+                self.gathered[:, :W, :], self.swa_cache, self.sparse_indices[:, :W],
+                w.swa_cache.block_size, rope_dim=w.rope_dim)))
+            L.append(("dequantize_and_gather_k_cache[topk]", lambda: ops.dequantize_and_gather_k_cache(
+                self.gathered[:, W:, :], self.comp_cache, self.sparse_indices[:, W:],
+                w.comp_cache.block_size, rope_dim=w.rope_dim)))
+        L.append(("compute_global_topk_indices_and_lens", lambda: ops.compute_global_topk_indices_and_lens(
+            self.topk, self.t2r, self.index_table, w.index_cache.block_size, self.valid,
+            out=self.global_topk, lens=self.global_lens)))
+        L.append(("dequantize_and_gather_k_cache[mxfp4]", lambda: ops.dequantize_and_gather_k_cache(
+            self.gathered_index, self.index_cache, self.global_topk, w.index_cache.block_size,
+            record=ops.PSK_REC_MXFP4)))
+        return L
+
+    def step(self) -> None:
+        for _, launch in self.launches():
+            launch()

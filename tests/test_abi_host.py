@@ -1,0 +1,159 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+* libpsk.so loads and exports every function include/psk.h declares.
+* Argument validation: every bad-argument call returns
+  PSK_ERR_INVALID_ARGUMENT with a message, before any CUDA call, so these run
+  on a machine without a GPU.
+* Zero-work calls return PSK_OK without launching anything.
+"""
+import ctypes
+
+import pytest
+
+from paged_sparse_kv_gb300 import _abi
+
+INV = _abi.PSK_ERR_INVALID_ARGUMENT
+OK = _abi.PSK_OK
+
+# Fake but well-aligned device addresses: validation never dereferences them.
+A = 0x10000000
+B = 0x20000000
+C = 0x30000000
+
+
+def test_library_exports_every_declared_symbol(psk_lib):
+    declared = _abi.header_functions()
+    assert set(declared) >= {"quantize_and_insert_k_cache", "write_indexer_mxfp4_cache",
+                             "compute_global_topk_indices_and_lens",
+                             "combine_topk_swa_indices", "dequantize_and_gather_k_cache",
+                             "psk_last_error", "psk_abi_version"}
+    for name in declared:
+        assert hasattr(psk_lib, name), name
+        assert ctypes.cast(getattr(psk_lib, name), ctypes.c_void_p).value
+    assert psk_lib.psk_abi_version() >= 1
+
+
+def _insert(**kw):
+    a = dict(k=A, k_row_stride=512, slots=B, n=4, cache=C, num_pages=8, page_stride=64 * 584,
+             bs=64, D=512, rope=64, ue=1, err=None)
+    a.update(kw)
+    return _abi.status("quantize_and_insert_k_cache", a["k"], a["k_row_stride"], a["slots"],
+                       a["n"], a["cache"], a["num_pages"], a["page_stride"], a["bs"], a["D"],
+                       a["rope"], a["ue"], a["err"], None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(k=None), dict(slots=None), dict(cache=None), dict(n=-1), dict(ue=2),
+    dict(D=96), dict(D=500), dict(rope=32), dict(rope=512), dict(rope=-64),
+    dict(bs=0), dict(num_pages=0), dict(page_stride=64 * 584 - 16),
+    dict(page_stride=64 * 584 + 8), dict(cache=C + 8), dict(k=A + 2),
+    dict(k_row_stride=500), dict(k_row_stride=256), dict(slots=B + 4), dict(err=B + 2),
+    dict(ue=0, page_stride=64 * 584),  # fp32 scales need 32 scale bytes per token
+])
+def test_insert_rejects_bad_arguments(psk_lib, kw):
+    assert _insert(**kw) == INV
+    assert _abi.last_error()
+
+
+def test_insert_zero_tokens_is_ok_without_launch(psk_lib):
+    assert _insert(n=0, k=None, slots=None) == OK
+    assert _abi.last_error() == ""
+
+
+def _mx(**kw):
+    a = dict(k=A, ks=128, slots=B, n=4, cache=C, num_pages=8, page_stride=64 * 68, bs=64,
+             D=128, err=None)
+    a.update(kw)
+    return _abi.status("write_indexer_mxfp4_cache", a["k"], a["ks"], a["slots"], a["n"],
+                       a["cache"], a["num_pages"], a["page_stride"], a["bs"], a["D"], a["err"],
+                       None)
+
+
+@pytest.mark.parametrize("kw", [dict(D=48), dict(D=100), dict(page_stride=64 * 68 - 16),
+                                dict(cache=C + 4), dict(k=None), dict(ks=120), dict(n=-5)])
+def test_mxfp4_insert_rejects_bad_arguments(psk_lib, kw):
+    assert _mx(**kw) == INV
+
+
+def _topk(**kw):
+    a = dict(topk=A, ts=8, n=3, K=8, t2r=B, bt=C, bts=4, btw=4, R=2, bs=16, base=None,
+             valid=None, out=A + 4096, os=8, lens=B + 4096)
+    a.update(kw)
+    return _abi.status("compute_global_topk_indices_and_lens", a["topk"], a["ts"], a["n"],
+                       a["K"], a["t2r"], a["bt"], a["bts"], a["btw"], a["R"], a["bs"],
+                       a["base"], a["valid"], a["out"], a["os"], a["lens"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(K=-1), dict(ts=4), dict(os=4), dict(bs=0), dict(R=0),
+                                dict(btw=5), dict(t2r=None), dict(lens=None),
+                                dict(topk=None), dict(out=A + 2), dict(n=-1)])
+def test_global_topk_rejects_bad_arguments(psk_lib, kw):
+    assert _topk(**kw) == INV
+
+
+def test_global_topk_zero_tokens_ok(psk_lib):
+    assert _topk(n=0, topk=None, t2r=None, out=None, lens=None) == OK
+
+
+def _combine(**kw):
+    a = dict(qsl=A, seq=A + 256, t2r=A + 512, rs=None, R=2, n=3, swa=B, swas=4, swaw=4,
+             swab=None, swabs=16, comp=None, comps=0, compw=0, compb=None, compbs=16, W=8,
+             ratio=4, topk=C, ts=8, K=8, valid=None, out=C + 4096, os=16, lens=C + 8192)
+    a.update(kw)
+    return _abi.status("combine_topk_swa_indices", a["qsl"], a["seq"], a["t2r"], a["rs"],
+                       a["R"], a["n"], a["swa"], a["swas"], a["swaw"], a["swab"], a["swabs"],
+                       a["comp"], a["comps"], a["compw"], a["compb"], a["compbs"], a["W"],
+                       a["ratio"], a["topk"], a["ts"], a["K"], a["valid"], a["out"], a["os"],
+                       a["lens"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(W=-1), dict(K=-2), dict(ratio=0), dict(swabs=0),
+                                dict(compbs=0), dict(os=15), dict(ts=7), dict(R=0),
+                                dict(qsl=None), dict(seq=None), dict(out=None),
+                                dict(swa=None), dict(comp=B + 1024, comps=2, compw=3),
+                                dict(K=5, os=12), dict(swaw=5), dict(lens=C + 2)])
+def test_combine_rejects_bad_arguments(psk_lib, kw):
+    assert _combine(**kw) == INV
+
+
+def test_combine_padded_width_rule(psk_lib):
+    # K=5 pads to 8: a row of W + 8 = 16 columns is enough, 15 is not.
+    assert _combine(K=5, ts=5, os=16, n=0) == OK
+    assert _combine(K=5, ts=5, os=15, n=0) == INV
+
+
+def _gather(**kw):
+    a = dict(out=A, ost=640 * 512, osj=512, cache=B, num_pages=8, page_stride=64 * 584, bs=64,
+             rec=0, D=512, rope=64, ue=1, idx=C, ids=640, rows=4, cols=640)
+    a.update(kw)
+    return _abi.status("dequantize_and_gather_k_cache", a["out"], a["ost"], a["osj"],
+                       a["cache"], a["num_pages"], a["page_stride"], a["bs"], a["rec"], a["D"],
+                       a["rope"], a["ue"], a["idx"], a["ids"], a["rows"], a["cols"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(rec=2), dict(D=100), dict(rope=16), dict(out=A + 8),
+                                dict(osj=4), dict(ost=-8), dict(ids=100), dict(idx=None),
+                                dict(out=None), dict(rows=-1), dict(page_stride=1000),
+                                dict(rec=1, D=128, rope=64), dict(rec=1, D=48, rope=0),
+                                dict(ue=5), dict(cache=None)])
+def test_gather_rejects_bad_arguments(psk_lib, kw):
+    assert _gather(**kw) == INV
+
+
+def test_gather_zero_rows_ok(psk_lib):
+    assert _gather(rows=0, out=None, idx=None) == OK
+    assert _gather(cols=0, ids=0, out=None, idx=None) == OK
+
+
+def test_error_message_is_thread_local(psk_lib):
+    import threading
+    assert _insert(ue=7) == INV
+    seen = {}
+
+    def other():
+        seen["msg"] = _abi.last_error()
+    th = threading.Thread(target=other)
+    th.start()
+    th.join()
+    assert seen["msg"] == ""
+    assert "is_ue8m0" in _abi.last_error()

@@ -1,0 +1,388 @@
+"""GPU parity: every CUDA entry point against the CPU oracle, bit for bit.
+
+Integer outputs (slots, lens) and packed bytes (FP8/FP4 codes, scale bytes,
+untouched cache bytes) must be identical; the dequantized bf16 rows must be
+identical too (tolerance 0: the products are exact in bf16 for UE8M0 scales,
+and both sides round binary32 products the same way for fp32 scales).
+
+Sizes: the five workloads at full size through the benchmark's pipeline
+(large gathers compared on a seeded sample of tokens), exhaustive code tables,
+and randomised small cases with ragged shapes and edge cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.pipeline import run_step
+from paged_sparse_kv_gb300 import ops, synthetic
+from paged_sparse_kv_gb300.pipeline import Pipeline
+from test_oracle_index import _random_case
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16_dev(a: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def _u16(t: torch.Tensor) -> np.ndarray:
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _assert_same(got: np.ndarray, want: np.ndarray, what: str):
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    bad = np.nonzero(got.reshape(-1) != want.reshape(-1))[0]
+    assert bad.size == 0, f"{what}: {bad.size} mismatches, first at flat {bad[:5].tolist()}: " \
+                          f"got {got.reshape(-1)[bad[:5]].tolist()} want {want.reshape(-1)[bad[:5]].tolist()}"
+
+
+@pytest.fixture(autouse=True)
+def _free_gpu_memory():
+    yield
+    torch.cuda.empty_cache()
+
+
+def test_smoke(cuda_device):
+    import __graft_entry__
+    __graft_entry__.smoke()
+
+
+# ---- inserts ---------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "mixed"])
+@pytest.mark.parametrize("ue8m0", [True, False])
+def test_fp8_insert_matches_oracle(cuda_device, name, ue8m0):
+    w = synthetic.make(name)
+    g = w.swa_cache
+    rec = oracle.fp8_record_bytes(w.head_dim, w.rope_dim, ue8m0)
+    stride = (g.block_size * rec + 15) // 16 * 16
+    geom = synthetic.CacheGeom(g.num_pages, g.block_size, stride)
+    host = synthetic.random_cache_bytes(7, geom)
+    dev_cache = torch.from_numpy(host).to(cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    ops.quantize_and_insert_k_cache(_bf16_dev(w.k, cuda_device), dev_cache,
+                                    torch.from_numpy(w.insert_slots).to(cuda_device),
+                                    g.block_size, rope_dim=w.rope_dim, is_ue8m0=ue8m0,
+                                    err_count=err)
+    n_err = oracle.quantize_and_insert_k_cache(w.k, w.insert_slots, host, g.block_size,
+                                               w.head_dim, w.rope_dim, ue8m0)
+    _assert_same(dev_cache.cpu().numpy(), host, f"{name} fp8 cache (ue8m0={ue8m0})")
+    assert int(err.item()) == n_err == 0
+
+
+def _exhaustive_rows(max_code: float, e_lo: int, e_hi: int, block: int, blocks_per_row: int):
+    """bf16 rows whose blocks reach every scale exponent in [e_lo, e_hi]: each
+    block starts with an element fixing its amax at max_code * 2^e and is
+    filled with every finite bf16 value of magnitude <= that amax."""
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32)
+    fin = np.isfinite(vals)
+    bf_max = np.float32((np.uint32(0x7F7F) << 16).view(np.float32))
+    blocks = []
+    for e in range(e_lo, e_hi + 1):
+        lead = np.float32(max_code * 2.0 ** e) if max_code * 2.0 ** e <= bf_max else bf_max
+        pick = bits[fin & (np.abs(vals) <= lead)].astype(np.uint16)
+        per = block - 1
+        pad = (-pick.size) % per
+        pick = np.concatenate([pick, np.zeros(pad, np.uint16)]).reshape(-1, per)
+        lead_bits = np.uint16(np.array([lead], np.float32).view(np.uint32)[0] >> 16)
+        blk = np.concatenate([np.full((pick.shape[0], 1), lead_bits, np.uint16), pick], axis=1)
+        blocks.append(blk)
+    blocks = np.concatenate(blocks)
+    pad = (-blocks.shape[0]) % blocks_per_row
+    blocks = np.concatenate([blocks, np.zeros((pad, block), np.uint16)])
+    return blocks.reshape(-1, blocks_per_row * block)
+
+
+def test_fp8_insert_exhaustive_codes(cuda_device):
+    """Every finite bf16 value under every reachable UE8M0 exponent
+    (e in [-22, 120]) through the GPU insert, against the oracle."""
+    nope = _exhaustive_rows(448.0, -22, 120, 64, 7)
+    k = np.concatenate([nope, np.zeros((nope.shape[0], 64), np.uint16)], axis=1)
+    N, bs = k.shape[0], 64
+    pages = (N + bs - 1) // bs
+    geom = synthetic.CacheGeom(pages, bs, bs * 584)
+    host = np.zeros((geom.num_pages, geom.page_stride), np.uint8)
+    slots = np.arange(N, dtype=np.int64)
+    dev_cache = torch.from_numpy(host).to(cuda_device)
+    ops.quantize_and_insert_k_cache(_bf16_dev(k, cuda_device), dev_cache,
+                                    torch.from_numpy(slots).to(cuda_device), bs, rope_dim=64)
+    oracle.quantize_and_insert_k_cache(k, slots, host, bs, 512, 64)
+    assert N > 10000
+    _assert_same(dev_cache.cpu().numpy(), host, "exhaustive fp8 codes")
+
+
+def test_mxfp4_insert_exhaustive_codes(cuda_device):
+    rows = _exhaustive_rows(6.0, -15, 126, 32, 4)
+    N, bs = rows.shape[0], 64
+    pages = (N + bs - 1) // bs
+    host = np.zeros((pages, bs * 68), np.uint8)
+    slots = np.arange(N, dtype=np.int64)
+    dev_cache = torch.from_numpy(host).to(cuda_device)
+    ops.write_indexer_mxfp4_cache(_bf16_dev(rows, cuda_device), dev_cache,
+                                  torch.from_numpy(slots).to(cuda_device), bs)
+    oracle.write_indexer_mxfp4_cache(rows, slots, host, bs, 128)
+    _assert_same(dev_cache.cpu().numpy(), host, "exhaustive mxfp4 codes")
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "mxfp4"])
+def test_mxfp4_insert_matches_oracle(cuda_device, name):
+    w = synthetic.make(name)
+    host = synthetic.random_cache_bytes(11, w.index_cache)
+    dev_cache = torch.from_numpy(host).to(cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    ops.write_indexer_mxfp4_cache(_bf16_dev(w.index_k, cuda_device), dev_cache,
+                                  torch.from_numpy(w.index_insert_slots).to(cuda_device),
+                                  w.index_cache.block_size, err_count=err)
+    n_err = oracle.write_indexer_mxfp4_cache(w.index_k, w.index_insert_slots, host,
+                                             w.index_cache.block_size, w.index_head_dim)
+    _assert_same(dev_cache.cpu().numpy(), host, f"{name} mxfp4 cache")
+    assert int(err.item()) == n_err
+
+
+@pytest.mark.parametrize("D,rope,ue8m0", [(64, 0, True), (128, 0, True), (256, 128, True),
+                                          (512, 64, False), (1024, 64, True)])
+def test_fp8_insert_shapes_strides_and_skips(cuda_device, D, rope, ue8m0):
+    """Ragged token count, a k with extra rows and a wider row stride,
+    negative and out-of-range slots (counted), all head_dim variants."""
+    rng = np.random.default_rng(D + rope)
+    N, bs, pages = 203, 16, 20
+    rows = rng.standard_normal((N + 5, D + 24)).astype(np.float32) * 3
+    k = torch.from_numpy(rows).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    slots = rng.permutation(pages * bs)[:N].astype(np.int64)
+    slots[::7] = -1
+    slots[3] = pages * bs + 5
+    slots[11] = 1 << 40
+    rec = oracle.fp8_record_bytes(D, rope, ue8m0)
+    geom = synthetic.CacheGeom(pages, bs, (bs * rec + 31) // 16 * 16)
+    host = synthetic.random_cache_bytes(3, geom)
+    dev_cache = torch.from_numpy(host).to(cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    kd = _bf16_dev(k, cuda_device)
+    ops.quantize_and_insert_k_cache(kd[:, :D], dev_cache, torch.from_numpy(slots).to(cuda_device),
+                                    bs, rope_dim=rope, is_ue8m0=ue8m0, err_count=err)
+    n_err = oracle.quantize_and_insert_k_cache(np.ascontiguousarray(k[:N, :D]), slots, host, bs,
+                                               D, rope, ue8m0)
+    _assert_same(dev_cache.cpu().numpy(), host, f"fp8 insert D={D} rope={rope}")
+    assert int(err.item()) == n_err == 2
+
+
+@pytest.mark.parametrize("D", [32, 64, 128, 256, 512, 1024])
+def test_mxfp4_insert_shapes_and_skips(cuda_device, D):
+    rng = np.random.default_rng(D)
+    N, bs, pages = 77, 8, 12
+    rows = rng.standard_normal((N, D)).astype(np.float32)
+    rows[5] = 0.0
+    k = torch.from_numpy(rows).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    slots = rng.permutation(pages * bs)[:N].astype(np.int64)
+    slots[::5] = -1
+    slots[2] = pages * bs
+    rec = D // 2 + D // 32
+    geom = synthetic.CacheGeom(pages, bs, (bs * rec + 15) // 16 * 16)
+    host = synthetic.random_cache_bytes(4, geom)
+    dev_cache = torch.from_numpy(host).to(cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    ops.write_indexer_mxfp4_cache(_bf16_dev(k, cuda_device), dev_cache,
+                                  torch.from_numpy(slots).to(cuda_device), bs, err_count=err)
+    n_err = oracle.write_indexer_mxfp4_cache(k, slots, host, bs, D)
+    _assert_same(dev_cache.cpu().numpy(), host, f"mxfp4 insert D={D}")
+    assert int(err.item()) == n_err == 1
+
+
+def test_insert_zero_tokens_touches_nothing(cuda_device):
+    cache = torch.full((4, 64 * 584), 0xA5, dtype=torch.uint8, device=cuda_device)
+    k = torch.zeros((3, 512), dtype=torch.bfloat16, device=cuda_device)
+    ops.quantize_and_insert_k_cache(k, cache, torch.empty(0, dtype=torch.int64, device=cuda_device), 64)
+    ops.quantize_and_insert_k_cache(k, cache, torch.full((3,), -1, dtype=torch.int64, device=cuda_device), 64)
+    torch.cuda.synchronize()
+    assert bool((cache == 0xA5).all())
+
+
+# ---- index builders ------------------------------------------------------------------
+
+def _dev_i32(a, dev):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "mixed"])
+def test_combine_matches_oracle(cuda_device, name):
+    w = synthetic.make(name)
+    d = cuda_device
+    si, lens = ops.combine_topk_swa_indices(
+        _dev_i32(w.query_start_loc, d), _dev_i32(w.seq_lens, d), _dev_i32(w.token_to_req, d),
+        _dev_i32(w.replay_start, d), _dev_i32(w.swa_block_table, d), w.swa_cache.block_size,
+        _dev_i32(w.comp_block_table, d), w.comp_cache.block_size, w.window, w.compress_ratio,
+        _dev_i32(w.topk_local, d))
+    want, want_lens = oracle.combine_topk_swa_indices(
+        w.query_start_loc, w.seq_lens, w.token_to_req, w.replay_start, w.swa_block_table,
+        w.swa_cache.block_size, w.comp_block_table, w.comp_cache.block_size, w.window,
+        w.compress_ratio, w.topk_local)
+    _assert_same(si.cpu().numpy(), want, f"{name} sparse_indices")
+    _assert_same(lens.cpu().numpy(), want_lens, f"{name} lens")
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "mixed", "mxfp4"])
+def test_global_topk_matches_oracle(cuda_device, name):
+    w = synthetic.make(name)
+    d = cuda_device
+    table = w.comp_block_table if w.comp_block_table is not None else w.swa_block_table
+    out, lens = ops.compute_global_topk_indices_and_lens(
+        _dev_i32(w.topk_local, d), _dev_i32(w.token_to_req, d), _dev_i32(table, d),
+        w.index_cache.block_size)
+    want, want_lens = oracle.compute_global_topk_indices_and_lens(
+        w.topk_local, w.token_to_req, table, w.index_cache.block_size)
+    _assert_same(out.cpu().numpy(), want, f"{name} global top-k")
+    _assert_same(lens.cpu().numpy(), want_lens, f"{name} global lens")
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_index_builders_fuzz(cuda_device, seed):
+    """Random small cases: page sizes 1..64, odd windows and top-k widths (the
+    unvectorised path), -1 table and top-k entries, base offsets, replay_start,
+    invalid tokens, out-of-range request indices, shared-memory staging."""
+    rng = np.random.default_rng(1000 + seed)
+    c = _random_case(rng)
+    comp_bs = c["bs"] if rng.random() < 0.5 else int(rng.choice([1, 4, 16]))
+    d = cuda_device
+    T = c["topk"].shape[0]
+    replay = c["replay"] if c["replay"] is not None else np.zeros(len(c["seq"]), np.int32)
+    valid = None if c["valid"] is None else torch.from_numpy(c["valid"]).to(d)
+    si, lens = ops.combine_topk_swa_indices(
+        _dev_i32(c["qsl"], d), _dev_i32(c["seq"], d), _dev_i32(c["t2r"], d), _dev_i32(replay, d),
+        _dev_i32(c["swa_bt"], d), c["bs"], _dev_i32(c["comp_bt"], d), comp_bs, c["W"], 4,
+        _dev_i32(c["topk"], d), swa_base_offsets=_dev_i32(c["swa_base"], d),
+        compressed_base_offsets=_dev_i32(c["comp_base"], d), is_valid_token=valid, num_tokens=T)
+    want, want_lens = oracle.combine_topk_swa_indices(
+        c["qsl"], c["seq"], c["t2r"], replay, c["swa_bt"], c["bs"], c["comp_bt"], comp_bs,
+        c["W"], 4, c["topk"], swa_base_offsets=c["swa_base"], comp_base_offsets=c["comp_base"],
+        is_valid_token=c["valid"])
+    if T:
+        _assert_same(si.cpu().numpy(), want, "fuzz sparse_indices")
+        _assert_same(lens.cpu().numpy(), want_lens, "fuzz lens")
+    bt = c["comp_bt"] if c["comp_bt"] is not None else c["swa_bt"]
+    out, gl = ops.compute_global_topk_indices_and_lens(
+        _dev_i32(c["topk"], d), _dev_i32(c["t2r"], d), _dev_i32(bt, d), comp_bs, valid,
+        base_offsets=_dev_i32(c["comp_base"], d))
+    want_g, want_gl = oracle.compute_global_topk_indices_and_lens(
+        c["topk"], c["t2r"], bt, comp_bs, base_offsets=c["comp_base"], is_valid_token=c["valid"])
+    if T:
+        _assert_same(out.cpu().numpy(), want_g, "fuzz global top-k")
+        _assert_same(gl.cpu().numpy(), want_gl, "fuzz global lens")
+
+
+def test_index_build_strided_views(cuda_device):
+    """Top-k and output rows that are column views of wider matrices (row
+    strides not multiples of 4 -> per-column path)."""
+    w = synthetic.make("tiny")
+    d = cuda_device
+    T, K = w.topk_local.shape
+    wide = np.full((T, K + 3), 99, np.int32)
+    wide[:, 1:K + 1] = w.topk_local
+    wide_d = _dev_i32(wide, d)
+    out_wide = torch.full((T, w.window + 8 + 5), -7, dtype=torch.int32, device=d)
+    lens = torch.empty(T, dtype=torch.int32, device=d)
+    ops.combine_topk_swa_indices(
+        _dev_i32(w.query_start_loc, d), _dev_i32(w.seq_lens, d), _dev_i32(w.token_to_req, d),
+        _dev_i32(w.replay_start, d), _dev_i32(w.swa_block_table, d), w.swa_cache.block_size,
+        None, w.comp_cache.block_size, w.window, 4, wide_d[:, 1:K + 1],
+        out=out_wide[:, 2:2 + w.window + 8], lens=lens)
+    want, want_lens = oracle.combine_topk_swa_indices(
+        w.query_start_loc, w.seq_lens, w.token_to_req, w.replay_start, w.swa_block_table,
+        w.swa_cache.block_size, None, w.comp_cache.block_size, w.window, 4, w.topk_local)
+    got = out_wide.cpu().numpy()
+    _assert_same(got[:, 2:2 + w.window + 8], want, "strided sparse_indices")
+    assert np.all(got[:, :2] == -7) and np.all(got[:, 2 + w.window + 8:] == -7)
+    _assert_same(lens.cpu().numpy(), want_lens, "strided lens")
+
+
+# ---- gathers -------------------------------------------------------------------------
+
+@pytest.mark.parametrize("D,rope,ue8m0", [(512, 64, True), (128, 0, True), (512, 64, False),
+                                          (256, 128, True), (64, 0, False)])
+def test_fp8_gather_random_records(cuda_device, D, rope, ue8m0):
+    """Arbitrary record bytes (UE8M0: no NaN codes; scales 2^-127..2^127, so
+    products hit bf16 subnormals and infinities); indices with -1 and
+    out-of-range slots; ragged rows x columns; output as a strided view."""
+    rng = np.random.default_rng(D * 3 + rope)
+    bs, pages = 16, 9
+    rec = oracle.fp8_record_bytes(D, rope, ue8m0)
+    geom = synthetic.CacheGeom(pages, bs, (bs * rec + 15) // 16 * 16)
+    if ue8m0:
+        host = synthetic.random_cache_bytes(21, geom)
+    else:  # fp32 scales: fill through the oracle insert so scales are finite
+        host = np.zeros((geom.num_pages, geom.page_stride), np.uint8)
+        rows = torch.from_numpy(rng.standard_normal((pages * bs, D)).astype(np.float32) * 4).to(
+            torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        oracle.quantize_and_insert_k_cache(rows, np.arange(pages * bs, dtype=np.int64), host,
+                                           bs, D, rope, False)
+    R, Cc = 37, 19
+    idx = rng.integers(-1, pages * bs, size=(R, Cc)).astype(np.int32)
+    idx[0, :] = -1
+    idx[1, 3] = pages * bs
+    idx[2, 4] = 2**31 - 1
+    out = torch.full((R, Cc + 2, D), 7, dtype=torch.bfloat16, device=cuda_device)
+    ops.dequantize_and_gather_k_cache(out[:, 1:Cc + 1, :], torch.from_numpy(host).to(cuda_device),
+                                      _dev_i32(idx, cuda_device), bs, rope_dim=rope,
+                                      is_ue8m0=ue8m0)
+    want = oracle.dequantize_and_gather_k_cache(host, bs, 0, D, rope, idx, is_ue8m0=ue8m0)
+    got = _u16(out)
+    _assert_same(got[:, 1:Cc + 1], want, f"fp8 gather D={D}")
+    seven = np.uint16(torch.tensor(7.0, dtype=torch.bfloat16).view(torch.int16).item())
+    assert np.all(got[:, 0] == seven) and np.all(got[:, Cc + 1] == seven)
+
+
+@pytest.mark.parametrize("D", [32, 64, 128, 256, 512, 1024])
+def test_mxfp4_gather_random_records(cuda_device, D):
+    rng = np.random.default_rng(D + 5)
+    bs, pages = 8, 11
+    rec = D // 2 + D // 32
+    geom = synthetic.CacheGeom(pages, bs, (bs * rec + 15) // 16 * 16)
+    host = rng.integers(0, 256, size=(geom.num_pages, geom.page_stride), dtype=np.uint8)
+    R, Cc = 23, 31
+    idx = rng.integers(-1, pages * bs + 3, size=(R, Cc)).astype(np.int32)
+    out = torch.empty((R, Cc, D), dtype=torch.bfloat16, device=cuda_device)
+    ops.dequantize_and_gather_k_cache(out, torch.from_numpy(host).to(cuda_device),
+                                      _dev_i32(idx, cuda_device), bs, record=ops.PSK_REC_MXFP4)
+    want = oracle.dequantize_and_gather_k_cache(host, bs, 1, D, 0, idx)
+    _assert_same(_u16(out), want, f"mxfp4 gather D={D}")
+
+
+# ---- the whole step, at full size, as the benchmark launches it -----------------------
+
+SAMPLE = {"tiny": None, "decode": None, "prefill": 48, "mixed": 48, "mxfp4": None}
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "mixed", "mxfp4"])
+def test_pipeline_step_matches_oracle(cuda_device, name):
+    w = synthetic.make(name)
+    host = {}
+    for i, cname in enumerate(("swa_cache", "comp_cache", "index_cache")):
+        g = getattr(w, cname)
+        host[cname] = None if g is None else synthetic.random_cache_bytes(50 + i, g)
+    p = Pipeline(w, cuda_device)
+    for cname, arr in host.items():
+        if arr is not None:
+            getattr(p, cname).copy_(torch.from_numpy(arr))
+    p.step()
+    torch.cuda.synchronize()
+    toks = None
+    if SAMPLE[name]:
+        rng = np.random.default_rng(99)
+        toks = np.unique(np.concatenate([[0, w.num_tokens - 1],
+                                         rng.integers(0, w.num_tokens, SAMPLE[name])]))
+    ref = run_step(w, host["swa_cache"], host["comp_cache"], host["index_cache"], toks)
+    for cname, arr in host.items():
+        if arr is not None:
+            _assert_same(getattr(p, cname).cpu().numpy(), arr, f"{name} {cname}")
+    if w.has_fp8:
+        _assert_same(p.sparse_indices.cpu().numpy(), ref["sparse_indices"], f"{name} indices")
+        _assert_same(p.lens.cpu().numpy(), ref["lens"], f"{name} lens")
+        g = p.gathered if toks is None else p.gathered[torch.from_numpy(toks).to(cuda_device)]
+        _assert_same(_u16(g), ref["gathered"], f"{name} gathered rows")
+    _assert_same(p.global_topk.cpu().numpy(), ref["global_topk"], f"{name} global top-k")
+    _assert_same(p.global_lens.cpu().numpy(), ref["global_lens"], f"{name} global lens")
+    gi = p.gathered_index if toks is None else p.gathered_index[torch.from_numpy(toks).to(cuda_device)]
+    _assert_same(_u16(gi), ref["gathered_index"], f"{name} gathered mxfp4 rows")
+    assert int(p.err.item()) == ref["err"] == 0
+    del p
