@@ -114,7 +114,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -182,18 +182,28 @@ def time_oracle(w, budget_s: float, max_rows: int = 80000):
     return n * steps / spent, desc
 
 
+def _graph_events_supported(torch) -> bool:
+    import inspect
+    try:
+        return "external" in inspect.signature(torch.cuda.Event.__new__).parameters
+    except (TypeError, ValueError):
+        return False
+
+
 # ---- main ------------------------------------------------------------------------------
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="decode",
                     choices=["tiny", "decode", "prefill", "mixed", "mxfp4"])
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--eager", action="store_true",
+                    help="launch the step eagerly instead of replaying a CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -239,28 +249,60 @@ def main():
 
     visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x]
     clocks = ClockSampler(visible[local_rank] if local_rank < len(visible) else str(local_rank))
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
-          for _ in range(args.steps)]
+    graph = None
+    if not args.eager and _graph_events_supported(torch):
+        # Capture the step once: kernels run back to back on the GPU (no host
+        # launch gaps), with an event node between consecutive kernels.
+        evs = [torch.cuda.Event(enable_timing=True, external=True)
+               for _ in range(len(launches) + 1)]
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            p.step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            evs[0].record()
+            for i, (_, launch) in enumerate(launches):
+                launch()
+                evs[i + 1].record()
+        for _ in range(args.warmup):
+            flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
     t_wall0 = time.perf_counter()
-    for s in range(args.steps):
-        flush.zero_()
-        ev[s][0].record(stream)
-        for i, (_, launch) in enumerate(launches):
-            launch()
-            ev[s][i + 1].record(stream)
-    torch.cuda.synchronize(dev)
+    step_ms, kern_ms = [], {n: [] for n in names}
+    if graph is not None:
+        for s in range(args.steps):
+            flush.zero_()
+            graph.replay()
+            torch.cuda.synchronize(dev)
+            step_ms.append(evs[0].elapsed_time(evs[-1]))
+            for i, n in enumerate(names):
+                kern_ms[n].append(evs[i].elapsed_time(evs[i + 1]))
+    else:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
+              for _ in range(args.steps)]
+        for s in range(args.steps):
+            flush.zero_()
+            ev[s][0].record(stream)
+            for i, (_, launch) in enumerate(launches):
+                launch()
+                ev[s][i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        step_ms = [ev[s][0].elapsed_time(ev[s][-1]) for s in range(args.steps)]
+        for i, n in enumerate(names):
+            kern_ms[n] = [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)]
     t_wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
     if dist:
         dist.barrier()
 
-    step_ms = [ev[s][0].elapsed_time(ev[s][-1]) for s in range(args.steps)]
-    kern_ms = {n: [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)]
-               for i, n in enumerate(names)}
     ms_per_step = statistics.mean(step_ms)
     if dist:
         t = torch.tensor([ms_per_step], device=dev)
@@ -306,7 +348,8 @@ def main():
                                f"head_dim {w.head_dim} (rope {w.rope_dim}), window {w.window}, "
                                f"top-k {w.topk}, ratio {w.compress_ratio}",
                    "seed": w.seed, "l2": "flushed before every step (512 MiB memset)",
-                   "parallelism": f"dp{world} (independent batch per GPU)"},
+                   "parallelism": f"dp{world} (independent batch per GPU)",
+                   "launch": "cuda graph of the step" if graph is not None else "eager"},
         "roofline": roof,
         "kernels": kernels,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT,

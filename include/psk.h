@@ -86,6 +86,17 @@ const char* psk_last_error(void);
 int32_t psk_abi_version(void);
 
 /*
+ * psk_device_wait_timeouts -- diagnostic of the pipelined kernels.
+ * Kernels that wait on shared-memory barriers (the TMA-fed gather) bound every
+ * wait to 2 s of wall time; a wait that expires is counted in a per-device
+ * counter, the kernel stops its remaining work instead of hanging, and the
+ * output of that launch is incomplete.  This call copies the current device's
+ * counter (0 in normal operation) into *count.  Synchronous (it waits for the
+ * device); returns PSK_ERR_CUDA if the copy fails.
+ */
+psk_status psk_device_wait_timeouts(uint32_t* count);
+
+/*
  * quantize_and_insert_k_cache -- block-scaled FP8 quantize + paged insert.
  * [VLLM] quantize_and_insert_k_cache; math of [OPS] _fp8_ds_mla_cache_rows.
  *
@@ -95,7 +106,7 @@ int32_t psk_abi_version(void);
  *                more (data-parallel padding) rows.
  *   slot_mapping int64 [num_tokens]; -1 (any negative) = skip the token.
  *   k_cache      uint8 [num_pages, page_stride] fp8_ds_mla pages (written).
- *   head_dim     multiple of 64 in [64, 1024]; rope_dim multiple of 64 in
+ *   head_dim     one of 64, 128, 256, 512, 1024; rope_dim multiple of 64 in
  *                [0, head_dim); the rope dims are the last rope_dim of each row
  *                and are stored verbatim (the caller has already rotated them).
  *   is_ue8m0     1: per 64-block e = ceil(log2(max(amax, 1e-4) / 448)) exactly,
@@ -121,7 +132,7 @@ psk_status quantize_and_insert_k_cache(
  *   index_k      bf16 [num_tokens, >= head_dim], row stride k_row_stride.
  *   slot_mapping int64 [num_tokens]; negative = skip.
  *   cache        uint8 [num_pages, page_stride] MXFP4 pages (written).
- *   head_dim     multiple of 32 in [32, 1024].
+ *   head_dim     one of 32, 64, 128, 256, 512, 1024.
  *   Per 32-block: e = ceil(log2(max(amax, 1e-4) / 6)) (the pages print no
  *   writer rule; this is E8M0 = ceil-pow2(amax / 6)), scale byte
  *   clamp(e + 127, 0, 254), codes RNE-E2M1 of x * 2^-e, saturating at 6.

@@ -31,6 +31,7 @@ _I32 = ctypes.c_int32
 SIGNATURES = {
     "psk_last_error": (ctypes.c_char_p, []),
     "psk_abi_version": (_I32, []),
+    "psk_device_wait_timeouts": (_I32, [_P]),
     "quantize_and_insert_k_cache": (
         _I32, [_P, _I64, _P, _I64, _P, _I64, _I64, _I32, _I32, _I32, _I32, _P, _P]),
     "write_indexer_mxfp4_cache": (
@@ -94,6 +95,13 @@ def call(name: str, *args) -> None:
 def status(name: str, *args) -> int:
     """Call an entry point and return its raw status code."""
     return getattr(lib(), name)(*args)
+
+
+def device_wait_timeouts() -> int:
+    """Expired in-kernel waits on the current device (0 in normal operation)."""
+    v = ctypes.c_uint32(0)
+    call("psk_device_wait_timeouts", ctypes.addressof(v))
+    return int(v.value)
 
 
 def last_error() -> str:

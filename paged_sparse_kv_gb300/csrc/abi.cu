@@ -77,6 +77,11 @@ const char* psk_last_error(void) { return g_last_error.c_str(); }
 
 int32_t psk_abi_version(void) { return 1; }
 
+psk_status psk_device_wait_timeouts(uint32_t* count) {
+    CHECK(count != nullptr, "count must be non-null");
+    return cuda_status(psk::read_wait_timeouts(count), "reading the wait-timeout counter");
+}
+
 psk_status quantize_and_insert_k_cache(const void* k, int64_t k_row_stride,
                                        const int64_t* slot_mapping, int64_t num_tokens,
                                        uint8_t* k_cache, int64_t num_pages, int64_t page_stride,

@@ -50,90 +50,181 @@ __device__ __forceinline__ RowAddr row_of(const GatherParams& p, int64_t it, int
     return a;
 }
 
-template <int D, bool UE8M0, int UNROLL>
-__global__ void __launch_bounds__(kThreads)
-gather_fp8_kernel(GatherParams p) {
+// ---- fp8_ds_mla: warp-specialised TMA pipeline ------------------------------------
+//
+// Warp 0 (producer) walks tiles of kRowsPerTile consecutive (t, j) items: its
+// lanes load the tile's slot ids with one coalesced load, then each lane issues
+// a 1-D bulk copy (cp.async.bulk) of its row's data record and of the 16-byte
+// aligned chunk holding the row's scales into stage s of a kStages-deep
+// shared-memory ring, completing on the stage's `full` mbarrier
+// (expect_tx = bytes of the valid rows).  The kConsumerWarps consumer warps
+// wait on `full`, dequantize rows out of shared memory, stream them to global
+// memory, and release the stage on its `empty` mbarrier.  The producer runs up
+// to kStages tiles ahead, so each SM keeps tens of KB of row reads in flight
+// without spending registers on them.  Every wait is bounded (2 s): on expiry
+// the thread counts a timeout in g_wait_timeouts and stops; the producer
+// always drains the copies it issued before it exits.
+
+constexpr int kStages = 4;
+constexpr int kRowsPerTile = 16;
+constexpr int kConsumerWarps = 8;
+constexpr int kTmaThreads = kWarp * (1 + kConsumerWarps);
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ unsigned int g_wait_timeouts = 0;
+
+__device__ __forceinline__ void item_to_tj(int64_t item, int32_t cols, bool small, int64_t& t,
+                                           int32_t& j) {
+    if (small) {
+        const uint32_t ui = (uint32_t)item, uc = (uint32_t)cols;
+        const uint32_t q = ui / uc;
+        t = q;
+        j = (int32_t)(ui - q * uc);
+    } else {
+        t = item / cols;
+        j = (int32_t)(item - t * cols);
+    }
+}
+
+template <int D, bool UE8M0>
+__global__ void __launch_bounds__(kTmaThreads)
+gather_fp8_tma_kernel(GatherParams p, int slot_bytes) {
     constexpr int CHUNKS = D / 8;
     constexpr int LANES = CHUNKS < kWarp ? CHUNKS : kWarp;
     constexpr int CPL = CHUNKS / LANES;
+    constexpr int GPW = kWarp / LANES;
     constexpr int NBLK = D / 64;
     constexpr int SDIM = UE8M0 ? NBLK : 4 * NBLK;
 
-    const int lane = threadIdx.x & 31;
-    const int gl = lane % LANES;
-    const int64_t gid = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / LANES;
-    const int64_t ngroups = (int64_t)gridDim.x * kThreads / LANES;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kRowsPerTile * slot_bytes);
+    uint64_t* empty = full + kStages;
+    int32_t* slots = reinterpret_cast<int32_t*>(empty + kStages);
+
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int64_t items = p.rows * (int64_t)p.cols;
+    const int64_t tiles = (items + kRowsPerTile - 1) / kRowsPerTile;
     const int64_t capacity = p.num_pages * (int64_t)p.block_size;
     const bool small = items <= 0xFFFFFFFFll;
     const int nope = D - p.rope_dim;
-    const int64_t ts = nope + 2 * p.rope_dim;
+    const int ts = nope + 2 * p.rope_dim;
+    const int bs = p.block_size;
 
-    for (int64_t it0 = gid * UNROLL; it0 < items; it0 += ngroups * UNROLL) {
-        RowAddr ra[UNROLL];
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const int64_t it = it0 + u;
-            if (it < items) {
-                ra[u] = row_of(p, it, capacity, small);
-            } else {
-                ra[u].t = -1;
-                ra[u].slot = -1;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        int i = 0;
+        bool ok = true;
+        for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++i) {
+            const int s = i % kStages;
+            if (i >= kStages && !mbar_wait_bounded(&empty[s], ((i / kStages) - 1) & 1, kWaitLimitNs)) {
+                ok = false;
+                break;
+            }
+            const int64_t item = tile * kRowsPerTile + lane;
+            int32_t slot = -1;
+            if (lane < kRowsPerTile && item < items) {
+                int64_t t;
+                int32_t j;
+                item_to_tj(item, p.cols, small, t, j);
+                const int32_t raw = __ldg(p.idx + t * p.idx_stride + j);
+                slot = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
+            }
+            uint32_t bytes = 0;
+            const uint8_t* src_data = nullptr;
+            const uint8_t* src_scl = nullptr;
+            uint32_t scl_bytes = 0;
+            if (slot >= 0) {
+                const int32_t page = slot / bs;
+                const int32_t off = slot - page * bs;
+                const uint8_t* base = p.cache + (int64_t)page * p.page_stride;
+                src_data = base + (int64_t)off * ts;
+                const uintptr_t a = reinterpret_cast<uintptr_t>(base + (int64_t)bs * ts + (int64_t)off * SDIM);
+                const uintptr_t a0 = a & ~(uintptr_t)15, a1 = (a + SDIM + 15) & ~(uintptr_t)15;
+                src_scl = reinterpret_cast<const uint8_t*>(a0);
+                scl_bytes = (uint32_t)(a1 - a0);
+                bytes = (uint32_t)ts + scl_bytes;
+            }
+            const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, bytes);
+            if (lane < kRowsPerTile) slots[s * kRowsPerTile + lane] = slot;
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], total);
+            __syncwarp();
+            if (slot >= 0) {
+                uint8_t* dst = ring + (size_t)(s * kRowsPerTile + lane) * slot_bytes;
+                bulk_g2s(dst, src_data, (uint32_t)ts, &full[s]);
+                bulk_g2s(dst + ts, src_scl, scl_bytes, &full[s]);
             }
         }
-        uint4 raw[UNROLL][CPL];
-        float sc[UNROLL][CPL];
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            if (ra[u].slot < 0) continue;
-            const int64_t page = ra[u].slot / p.block_size;
-            const int64_t off = ra[u].slot - page * p.block_size;
-            const uint8_t* base = p.cache + page * p.page_stride;
-            const uint8_t* data = base + off * ts;
-            const uint8_t* scl = base + (int64_t)p.block_size * ts + off * SDIM;
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) {
-                const int c = gl + i * LANES;
-                if (8 * c < nope) {
-                    const uint2 w = ld_nc_v2(data + 8 * c);
-                    raw[u][i] = make_uint4(w.x, w.y, 0u, 0u);
-                    if constexpr (UE8M0) {
-                        sc[u][i] = ue8m0_scale(ld_nc_u8(scl + c / 8));
-                    } else {
-                        sc[u][i] = __uint_as_float(ld_nc_u32(scl + 4 * (c / 8)));
-                    }
-                } else {
-                    raw[u][i] = ld_nc_v4(data + 16 * c - nope);
-                    sc[u][i] = 0.0f;
-                }
+        if (!ok && lane == 0) atomicAdd(&g_wait_timeouts, 1u);
+        // Drain: the last phase issued on every stage must land before exit.
+        if (lane == 0) {
+            for (int s = 0; s < kStages && s < i; ++s) {
+                const int last = s + ((i - 1 - s) / kStages) * kStages;
+                if (!mbar_wait_bounded(&full[s], (last / kStages) & 1, kWaitLimitNs))
+                    atomicAdd(&g_wait_timeouts, 1u);
             }
         }
+        return;
+    }
+
+    const int cw = warp - 1;
+    const int grp = lane / LANES, gl = lane % LANES;
+    int i = 0;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++i) {
+        const int s = i % kStages;
+        if (!mbar_wait_bounded(&full[s], (i / kStages) & 1, kWaitLimitNs)) {
+            if (lane == 0) atomicAdd(&g_wait_timeouts, 1u);
+            return;
+        }
+        for (int r = cw * GPW + grp; r < kRowsPerTile; r += kConsumerWarps * GPW) {
+            const int64_t item = tile * kRowsPerTile + r;
+            if (item >= items) break;
+            const int32_t slot = slots[s * kRowsPerTile + r];
+            int64_t t;
+            int32_t j;
+            item_to_tj(item, p.cols, small, t, j);
+            uint16_t* orow = p.out + t * p.out_stride_t + (int64_t)j * p.out_stride_j;
+            const uint8_t* srow = ring + (size_t)(s * kRowsPerTile + r) * slot_bytes;
+            const int soff = slot >= 0 ? (int)(((int64_t)(slot % bs) * SDIM) & 15) : 0;
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            if (ra[u].t < 0) continue;
-            uint16_t* orow = p.out + ra[u].t * p.out_stride_t + (int64_t)ra[u].j * p.out_stride_j;
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) {
-                const int c = gl + i * LANES;
+            for (int ci = 0; ci < CPL; ++ci) {
+                const int c = gl + ci * LANES;
                 uint4 o;
-                if (ra[u].slot < 0) {
+                if (slot < 0) {
                     o = make_uint4(0u, 0u, 0u, 0u);
                 } else if (8 * c < nope) {
-                    const float s = sc[u][i];
-                    const uint32_t h0 = cvt_e4m3x2_to_f16x2(raw[u][i].x & 0xFFFFu);
-                    const uint32_t h1 = cvt_e4m3x2_to_f16x2(raw[u][i].x >> 16);
-                    const uint32_t h2 = cvt_e4m3x2_to_f16x2(raw[u][i].y & 0xFFFFu);
-                    const uint32_t h3 = cvt_e4m3x2_to_f16x2(raw[u][i].y >> 16);
-                    o.x = pack_bf16x2(__fmul_rn(f16_lo(h0), s), __fmul_rn(f16_hi(h0), s));
-                    o.y = pack_bf16x2(__fmul_rn(f16_lo(h1), s), __fmul_rn(f16_hi(h1), s));
-                    o.z = pack_bf16x2(__fmul_rn(f16_lo(h2), s), __fmul_rn(f16_hi(h2), s));
-                    o.w = pack_bf16x2(__fmul_rn(f16_lo(h3), s), __fmul_rn(f16_hi(h3), s));
+                    const uint2 w = lds_v2(srow + 8 * c);
+                    float sc;
+                    if constexpr (UE8M0) {
+                        sc = ue8m0_scale(lds_u8(srow + ts + soff + c / 8));
+                    } else {
+                        sc = __uint_as_float(lds_u32(srow + ts + soff + 4 * (c / 8)));
+                    }
+                    const uint32_t h0 = cvt_e4m3x2_to_f16x2(w.x & 0xFFFFu);
+                    const uint32_t h1 = cvt_e4m3x2_to_f16x2(w.x >> 16);
+                    const uint32_t h2 = cvt_e4m3x2_to_f16x2(w.y & 0xFFFFu);
+                    const uint32_t h3 = cvt_e4m3x2_to_f16x2(w.y >> 16);
+                    o.x = pack_bf16x2(__fmul_rn(f16_lo(h0), sc), __fmul_rn(f16_hi(h0), sc));
+                    o.y = pack_bf16x2(__fmul_rn(f16_lo(h1), sc), __fmul_rn(f16_hi(h1), sc));
+                    o.z = pack_bf16x2(__fmul_rn(f16_lo(h2), sc), __fmul_rn(f16_hi(h2), sc));
+                    o.w = pack_bf16x2(__fmul_rn(f16_lo(h3), sc), __fmul_rn(f16_hi(h3), sc));
                 } else {
-                    o = raw[u][i];
+                    o = lds_v4(srow + 16 * c - nope);
                 }
                 st_stream_v4(orow + 8 * c, o);
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
     }
 }
 
@@ -222,12 +313,29 @@ int64_t persistent_blocks(K kernel, int64_t groups_needed, int lanes) {
 
 template <int D, bool UE8M0>
 cudaError_t gather_fp8_dispatch(const GatherParams& p, cudaStream_t stream) {
-    constexpr int UNROLL = 2;
-    constexpr int LANES = (D / 8) < kWarp ? (D / 8) : kWarp;
+    const int ts = D - p.rope_dim + 2 * p.rope_dim;
+    constexpr int SDIM = UE8M0 ? D / 64 : 4 * (D / 64);
+    // data record + the 16-byte chunks covering the scales, rounded to 16
+    const int slot_bytes = (ts + ((SDIM + 15) / 16 + 1) * 16 + 15) / 16 * 16;
+    const size_t smem = (size_t)kStages * kRowsPerTile * slot_bytes +
+                        2 * kStages * sizeof(uint64_t) + kStages * kRowsPerTile * sizeof(int32_t);
+    auto kern = gather_fp8_tma_kernel<D, UE8M0>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             200 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTmaThreads, smem) !=
+            cudaSuccess || per_sm < 1)
+        per_sm = 1;
     const int64_t items = p.rows * (int64_t)p.cols;
-    auto kern = gather_fp8_kernel<D, UE8M0, UNROLL>;
-    const int64_t blocks = persistent_blocks(kern, (items + UNROLL - 1) / UNROLL, LANES);
-    kern<<<(unsigned)blocks, kThreads, 0, stream>>>(p);
+    const int64_t tiles = (items + kRowsPerTile - 1) / kRowsPerTile;
+    int64_t blocks = (int64_t)sm_count() * per_sm;
+    if (blocks > tiles) blocks = tiles;
+    kern<<<(unsigned)blocks, kTmaThreads, smem, stream>>>(p, slot_bytes);
     return cudaGetLastError();
 }
 
@@ -243,6 +351,10 @@ cudaError_t gather_mxfp4_dispatch(const GatherParams& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t read_wait_timeouts(uint32_t* count) {
+    return cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(uint32_t));
+}
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
     if (p.record == 0) {

@@ -84,4 +84,7 @@ struct GatherParams {
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
 
+// Number of bounded in-kernel waits that expired on the current device.
+cudaError_t read_wait_timeouts(uint32_t* count);
+
 }  // namespace psk

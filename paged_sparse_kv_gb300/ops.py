@@ -46,8 +46,12 @@ def _pages(cache: torch.Tensor):
 
 
 def _rows(t: torch.Tensor, name: str):
-    if t.dim() != 2 or t.stride(1) != 1:
-        raise ValueError(f"{name} must be 2-D with unit inner stride")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if t.numel() == 0:
+        return t.shape[1]
+    if t.stride(1) != 1 and t.shape[1] > 1:
+        raise ValueError(f"{name} must have unit inner stride")
     return t.stride(0)
 
 
