@@ -190,6 +190,59 @@ def _graph_events_supported(torch) -> bool:
         return False
 
 
+def kernel_source_hash() -> str:
+    """sha1 over the CUDA sources (sorted by name); identifies the kernel build
+    a recorded ncu capture belongs to."""
+    import glob
+    import hashlib
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "paged_sparse_kv_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(os.path.basename(f).encode())
+            h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
+def recorded_traffic(config: str, kernel: str):
+    """DRAM bytes (read + write) per launch from profiles/traffic.txt, or None
+    when no capture exists for this kernel build."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == config and \
+                parts[1] == kernel and parts[3] == src:
+            return int(parts[2])
+    return None
+
+
+def _instrumented(p, names, evs):
+    """The step serialised on the current stream, an event before each kernel."""
+    L = dict(p.launches())
+    evs[0].record()
+    for i, n in enumerate(names):
+        L[n]()
+        evs[i + 1].record()
+
+
+def _capture(torch, dev, stream, fn):
+    """Capture fn() into a CUDA graph (after one eager run on a side stream)."""
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        fn()
+    stream.wait_stream(side)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize(dev)
+    return g
+
+
 # ---- main ------------------------------------------------------------------------------
 
 def main():
@@ -198,7 +251,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="decode",
-                    choices=["tiny", "decode", "prefill", "mixed", "mxfp4"])
+                    choices=["tiny", "decode", "prefill", "mixed", "mxfp4", "prefill_small"])
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
@@ -228,8 +281,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    maker = synthetic.MAKERS[args.config]
-    w = maker(synthetic.BASE_SEED + synthetic.CONFIG_NAMES.index(args.config) + 1000 * rank)
+    w = synthetic.make(args.config, seed_offset=1000 * rank)
     p = Pipeline(w, dev)
     p.fill_caches_with_quantized_rows(seed=4321 + rank)
     launches = p.launches()
@@ -239,7 +291,7 @@ def main():
 
     for _ in range(args.warmup):
         flush.zero_()
-        p.step()
+        p.step(concurrent=True)
     torch.cuda.synchronize(dev)
 
     outputs = {"global_topk": p.global_topk.cpu().numpy()}
@@ -249,55 +301,77 @@ def main():
 
     visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x]
     clocks = ClockSampler(visible[local_rank] if local_rank < len(visible) else str(local_rank))
-    graph = None
-    if not args.eager and _graph_events_supported(torch):
-        # Capture the step once: kernels run back to back on the GPU (no host
-        # launch gaps), with an event node between consecutive kernels.
-        evs = [torch.cuda.Event(enable_timing=True, external=True)
-               for _ in range(len(launches) + 1)]
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            p.step()
-        stream.wait_stream(side)
-        torch.cuda.synchronize(dev)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            evs[0].record()
-            for i, (_, launch) in enumerate(launches):
-                launch()
-                evs[i + 1].record()
+    use_graph = not args.eager and _graph_events_supported(torch)
+
+    # (1) Per-kernel breakdown, untimed: the step serialised on one stream with
+    # an event between consecutive kernels.  Each figure includes the cost of
+    # the event node in front of the kernel.
+    kern_ms = {n: [] for n in names}
+    if use_graph:
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(names) + 1)]
+        g_ser = _capture(torch, dev, stream, lambda: _instrumented(p, names, evs))
+        for _ in range(max(5, min(args.steps, 30))):
+            flush.zero_()
+            g_ser.replay()
+            torch.cuda.synchronize(dev)
+            for i, n in enumerate(names):
+                kern_ms[n].append(evs[i].elapsed_time(evs[i + 1]))
+        del g_ser
+    else:
+        for _ in range(max(5, min(args.steps, 30))):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+            flush.zero_()
+            _instrumented(p, names, evs)
+            torch.cuda.synchronize(dev)
+            for i, n in enumerate(names):
+                kern_ms[n].append(evs[i].elapsed_time(evs[i + 1]))
+    top = max(names, key=lambda n: statistics.mean(kern_ms[n]))
+
+    # (2) Timed region: K steps.  Each step replays the concurrent step (three
+    # streams) as a CUDA graph with no event inside, timed by events on either
+    # side (-> value); then, after another L2 flush, an instrumented replay of
+    # the same step with events around the dominant kernel on its own stream
+    # (-> roofline).  Event nodes inside a graph cost a few microseconds each,
+    # so they are kept out of the replay that gives the step time.
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    k_pre = torch.cuda.Event(enable_timing=True, external=use_graph)
+    k_post = torch.cuda.Event(enable_timing=True, external=use_graph)
+    hooks = {top: (lambda: k_pre.record(), lambda: k_post.record())}
+    g_plain = g_inst = None
+    if use_graph:
+        g_plain = _capture(torch, dev, stream, lambda: p.step(concurrent=True))
+        g_inst = _capture(torch, dev, stream, lambda: p.step(concurrent=True, hooks=hooks))
         for _ in range(args.warmup):
             flush.zero_()
-            graph.replay()
+            g_plain.replay()
+            flush.zero_()
+            g_inst.replay()
         torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
     t_wall0 = time.perf_counter()
-    step_ms, kern_ms = [], {n: [] for n in names}
-    if graph is not None:
-        for s in range(args.steps):
-            flush.zero_()
-            graph.replay()
-            torch.cuda.synchronize(dev)
-            step_ms.append(evs[0].elapsed_time(evs[-1]))
-            for i, n in enumerate(names):
-                kern_ms[n].append(evs[i].elapsed_time(evs[i + 1]))
-    else:
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
-              for _ in range(args.steps)]
-        for s in range(args.steps):
-            flush.zero_()
-            ev[s][0].record(stream)
-            for i, (_, launch) in enumerate(launches):
-                launch()
-                ev[s][i + 1].record(stream)
+    step_ms, top_ms = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        t_start.record(stream)
+        if g_plain is not None:
+            g_plain.replay()
+        else:
+            p.step(concurrent=True)
+        t_end.record(stream)
+        flush.zero_()
+        if g_inst is not None:
+            g_inst.replay()
+        else:
+            p.step(concurrent=True, hooks=hooks)
+        k_post.synchronize()
         torch.cuda.synchronize(dev)
-        step_ms = [ev[s][0].elapsed_time(ev[s][-1]) for s in range(args.steps)]
-        for i, n in enumerate(names):
-            kern_ms[n] = [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)]
+        step_ms.append(t_start.elapsed_time(t_end))
+        top_ms.append(k_pre.elapsed_time(k_post))
+    torch.cuda.synchronize(dev)
     t_wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
     if dist:
@@ -323,22 +397,19 @@ def main():
     for n in names:
         mean_ms = statistics.mean(kern_ms[n])
         gbs = alg[n] / (mean_ms / 1e3) / 1e9
-        kernels[n] = {"us": round(mean_ms * 1e3, 2), "alg_bytes": int(alg[n]),
-                      "GBps": round(gbs, 1), "frac_measured": round(gbs / peak, 3),
-                      "frac_nominal_8TBps": round(gbs / NOMINAL_HBM_GBS, 3),
-                      "share": round(mean_ms / ms_per_step, 3)}
-    top = max(names, key=lambda n: kernels[n]["us"])
-    roof = {"kernel": top, "bound": "hbm", "achieved": kernels[top]["GBps"], "peak": peak,
-            "peak_kind": peak_kind, "unit": "GB/s",
-            "frac": round(kernels[top]["GBps"] / peak, 3), "traffic": None}
-    traffic_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(traffic_path):
-        try:
-            tr = json.load(open(traffic_path)).get(args.config, {}).get(top)
-            roof["traffic"] = tr
-        except Exception:
-            pass
-
+        kernels[n] = {"us_serial_with_event_node": round(mean_ms * 1e3, 2),
+                      "alg_bytes": int(alg[n]), "GBps": round(gbs, 1),
+                      "frac_measured": round(gbs / peak, 3),
+                      "frac_nominal_8TBps": round(gbs / NOMINAL_HBM_GBS, 3)}
+    top_mean = statistics.mean(top_ms)
+    achieved = alg[top] / (top_mean / 1e3) / 1e9
+    roof = {"kernel": top, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 3),
+            "traffic": None, "us_per_launch": round(top_mean * 1e3, 2),
+            "alg_bytes_per_launch": int(alg[top]),
+            "frac_nominal_8TBps": round(achieved / NOMINAL_HBM_GBS, 3)}
+    roof["traffic"] = recorded_traffic(args.config, top)
+    step_bytes = sum(alg.values())
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -349,13 +420,19 @@ def main():
                                f"top-k {w.topk}, ratio {w.compress_ratio}",
                    "seed": w.seed, "l2": "flushed before every step (512 MiB memset)",
                    "parallelism": f"dp{world} (independent batch per GPU)",
-                   "launch": "cuda graph of the step" if graph is not None else "eager"},
+                   "launch": ("cuda graph of the step on three streams" if g_plain is not None
+                              else "eager, three streams"),
+                   "timing": "value: events around an un-instrumented graph replay of each "
+                             "step; roofline: events around the dominant kernel in a second, "
+                             "instrumented replay of the same step after each timed step"},
         "roofline": roof,
         "kernels": kernels,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e["ms_per_step"], 4)},
-        "gpu_launches": len(launches) * args.steps,
+        "gpu_launches": 2 * len(launches) * args.steps,
+        "step_alg_bytes": int(step_bytes),
+        "step_GBps": round(step_bytes / (ms_per_step / 1e3) / 1e9, 1),
         "clocks": clk,
         "wall_s_timed_region": round(t_wall, 4),
     }
@@ -387,7 +464,7 @@ def run_e2e(p, args, dev, flush):
         t0 = time.perf_counter()
         for d, h in zip(ins, h_in):
             d.copy_(h, non_blocking=True)
-        p.step()
+        p.step(concurrent=True)
         for h, d in zip(h_out, outs):
             h.copy_(d, non_blocking=True)
         torch.cuda.synchronize(dev)
@@ -404,7 +481,7 @@ def run_reference(args, rank, world):
     from oracle.pipeline import run_step
     from paged_sparse_kv_gb300 import synthetic
     oracle.build()
-    w = synthetic.MAKERS[args.config]()
+    w = synthetic.make(args.config)
     caches = _oracle_state(w)
     toks, n = _oracle_sample_tokens(w, 80000)
     for _ in range(args.warmup):

@@ -5,21 +5,17 @@
 // read_deepseek_v4_indexer_mxfp4_cache (MXFP4); index form of vLLM
 // deepseek_v41 ops dequantize_and_gather_k_cache.
 //
-// Design (HBM-bound: ~584 B read + 1024 B written per fp8 row):
-//  * A group of LANES lanes owns one output row (one (token, column) pair);
-//    every lane owns 16-byte output chunks (8 bf16), so a 512-dim row is one
-//    coalesced 512-byte store instruction per half row, issued as a streaming
-//    (evict-first) store so the gathered output does not push reused cache
-//    rows out of L2.
-//  * The fp8 record is read as 8-byte chunks (nope) and 16-byte chunks (rope)
-//    straight from the page; the scale byte of each 64-block is a broadcast
-//    load within the block's lanes.
-//  * Decode: cvt.rn.f16x2.e4m3x2 (exact), binary32 multiply by the
-//    power-of-two scale, cvt.rn.bf16x2.f32.
-//  * Each group handles UNROLL rows per step with every load issued first;
-//    the grid is a persistent multiple of the SM count and groups stride
-//    over the flattened (row, column) space.
-//  * Invalid slots (negative or beyond the cache) produce zero rows.
+// Two kernels:
+//  * fp8_ds_mla records (584 B per 512-dim row): a warp-specialised pipeline
+//    that moves records into shared memory with 1-D bulk copies (TMA) and
+//    dequantizes from there (details above the kernel).
+//  * MXFP4 records (68 B per 128-dim row): batched plain loads.
+// Both write each output row as 16-byte chunks, one warp store instruction
+// covering 512 contiguous bytes, issued as streaming (evict-first) stores so
+// the gathered output does not push reused cache rows out of L2.  Decode is
+// exact: cvt.rn.f16x2.{e4m3x2,e2m1x2}, a binary32 multiply by the scale, and
+// cvt.rn.bf16x2.f32.  Invalid slots (negative or beyond the cache) give zero
+// rows.
 #include "launch.h"
 #include "psk_common.cuh"
 
@@ -27,28 +23,6 @@ namespace psk {
 namespace {
 
 constexpr int kThreads = 256;
-
-struct RowAddr {
-    int64_t t;
-    int32_t j;
-    int64_t slot;  // -1 = zero row
-};
-
-__device__ __forceinline__ RowAddr row_of(const GatherParams& p, int64_t it, int64_t capacity,
-                                          bool small) {
-    RowAddr a;
-    if (small) {
-        const uint32_t ui = (uint32_t)it, uc = (uint32_t)p.cols;
-        a.t = ui / uc;
-        a.j = (int32_t)(ui - (uint32_t)a.t * uc);
-    } else {
-        a.t = it / p.cols;
-        a.j = (int32_t)(it - a.t * p.cols);
-    }
-    const int32_t s = __ldg(p.idx + a.t * p.idx_stride + a.j);
-    a.slot = (s < 0 || (int64_t)s >= capacity) ? -1 : s;
-    return a;
-}
 
 // ---- fp8_ds_mla: warp-specialised TMA pipeline ------------------------------------
 //
@@ -100,7 +74,8 @@ gather_fp8_tma_kernel(GatherParams p, int slot_bytes) {
     uint8_t* ring = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kRowsPerTile * slot_bytes);
     uint64_t* empty = full + kStages;
-    int32_t* slots = reinterpret_cast<int32_t*>(empty + kStages);
+    int64_t* outoff = reinterpret_cast<int64_t*>(empty + kStages);   // [kStages][kRowsPerTile]
+    int32_t* slots = reinterpret_cast<int32_t*>(outoff + kStages * kRowsPerTile);
 
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int64_t items = p.rows * (int64_t)p.cols;
@@ -119,49 +94,77 @@ gather_fp8_tma_kernel(GatherParams p, int slot_bytes) {
         mbar_fence_init();
     }
     __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
 
     if (warp == 0) {
+        // Producer.  Lanes 0-15 and 16-31 load the slot ids of two tiles per
+        // load instruction; each round covers kLoadTiles tiles, so the ring
+        // fills after one index-load latency instead of one per tile.
+        constexpr int kLoadTiles = 4;
+        const int half = lane >> 4, r = lane & 15;
         int i = 0;
         bool ok = true;
-        for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++i) {
-            const int s = i % kStages;
-            if (i >= kStages && !mbar_wait_bounded(&empty[s], ((i / kStages) - 1) & 1, kWaitLimitNs)) {
-                ok = false;
-                break;
+        for (int64_t base = blockIdx.x; base < tiles && ok; base += (int64_t)kLoadTiles * gridDim.x) {
+            int32_t slot[kLoadTiles / 2];
+            int64_t oof[kLoadTiles / 2];
+#pragma unroll
+            for (int q = 0; q < kLoadTiles / 2; ++q) {
+                const int64_t tile = base + (int64_t)(2 * q + half) * gridDim.x;
+                const int64_t item = tile * kRowsPerTile + r;
+                slot[q] = -1;
+                oof[q] = 0;
+                if (tile < tiles && item < items) {
+                    int64_t t;
+                    int32_t j;
+                    item_to_tj(item, p.cols, small, t, j);
+                    const int32_t raw = __ldg(p.idx + t * p.idx_stride + j);
+                    slot[q] = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
+                    oof[q] = t * p.out_stride_t + (int64_t)j * p.out_stride_j;
+                }
             }
-            const int64_t item = tile * kRowsPerTile + lane;
-            int32_t slot = -1;
-            if (lane < kRowsPerTile && item < items) {
-                int64_t t;
-                int32_t j;
-                item_to_tj(item, p.cols, small, t, j);
-                const int32_t raw = __ldg(p.idx + t * p.idx_stride + j);
-                slot = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
-            }
-            uint32_t bytes = 0;
-            const uint8_t* src_data = nullptr;
-            const uint8_t* src_scl = nullptr;
-            uint32_t scl_bytes = 0;
-            if (slot >= 0) {
-                const int32_t page = slot / bs;
-                const int32_t off = slot - page * bs;
-                const uint8_t* base = p.cache + (int64_t)page * p.page_stride;
-                src_data = base + (int64_t)off * ts;
-                const uintptr_t a = reinterpret_cast<uintptr_t>(base + (int64_t)bs * ts + (int64_t)off * SDIM);
-                const uintptr_t a0 = a & ~(uintptr_t)15, a1 = (a + SDIM + 15) & ~(uintptr_t)15;
-                src_scl = reinterpret_cast<const uint8_t*>(a0);
-                scl_bytes = (uint32_t)(a1 - a0);
-                bytes = (uint32_t)ts + scl_bytes;
-            }
-            const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, bytes);
-            if (lane < kRowsPerTile) slots[s * kRowsPerTile + lane] = slot;
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], total);
-            __syncwarp();
-            if (slot >= 0) {
-                uint8_t* dst = ring + (size_t)(s * kRowsPerTile + lane) * slot_bytes;
-                bulk_g2s(dst, src_data, (uint32_t)ts, &full[s]);
-                bulk_g2s(dst + ts, src_scl, scl_bytes, &full[s]);
+#pragma unroll
+            for (int k = 0; k < kLoadTiles; ++k) {
+                const int64_t tile = base + (int64_t)k * gridDim.x;
+                if (tile >= tiles) break;
+                const int s = i % kStages;
+                if (i >= kStages && !mbar_wait_bounded(&empty[s], ((i / kStages) - 1) & 1, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                const bool mine = half == (k & 1);
+                const int32_t sl = mine ? slot[k / 2] : -1;
+                uint32_t bytes = 0;
+                const uint8_t* src_data = nullptr;
+                const uint8_t* src_scl = nullptr;
+                uint32_t scl_bytes = 0;
+                int32_t soff = -1;
+                if (sl >= 0) {
+                    const int32_t page = sl / bs;
+                    const int32_t off = sl - page * bs;
+                    const uint8_t* pbase = p.cache + (int64_t)page * p.page_stride;
+                    src_data = pbase + (int64_t)off * ts;
+                    const uintptr_t a = reinterpret_cast<uintptr_t>(pbase + (int64_t)bs * ts + (int64_t)off * SDIM);
+                    const uintptr_t a0 = a & ~(uintptr_t)15, a1 = (a + SDIM + 15) & ~(uintptr_t)15;
+                    src_scl = reinterpret_cast<const uint8_t*>(a0);
+                    scl_bytes = (uint32_t)(a1 - a0);
+                    soff = (int32_t)(a - a0);
+                    bytes = (uint32_t)ts + scl_bytes;
+                }
+                const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, bytes);
+                if (mine) {
+                    slots[s * kRowsPerTile + r] = soff;  // -1: zero row
+                    outoff[s * kRowsPerTile + r] = oof[k / 2];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], total);
+                __syncwarp();
+                if (sl >= 0) {
+                    uint8_t* dst = ring + (size_t)(s * kRowsPerTile + r) * slot_bytes;
+                    bulk_g2s(dst, src_data, (uint32_t)ts, &full[s]);
+                    bulk_g2s(dst + ts, src_scl, scl_bytes, &full[s]);
+                }
+                ++i;
             }
         }
         if (!ok && lane == 0) atomicAdd(&g_wait_timeouts, 1u);
@@ -188,18 +191,14 @@ gather_fp8_tma_kernel(GatherParams p, int slot_bytes) {
         for (int r = cw * GPW + grp; r < kRowsPerTile; r += kConsumerWarps * GPW) {
             const int64_t item = tile * kRowsPerTile + r;
             if (item >= items) break;
-            const int32_t slot = slots[s * kRowsPerTile + r];
-            int64_t t;
-            int32_t j;
-            item_to_tj(item, p.cols, small, t, j);
-            uint16_t* orow = p.out + t * p.out_stride_t + (int64_t)j * p.out_stride_j;
+            const int32_t soff = slots[s * kRowsPerTile + r];  // scale offset, -1 = zero row
+            uint16_t* orow = p.out + outoff[s * kRowsPerTile + r];
             const uint8_t* srow = ring + (size_t)(s * kRowsPerTile + r) * slot_bytes;
-            const int soff = slot >= 0 ? (int)(((int64_t)(slot % bs) * SDIM) & 15) : 0;
 #pragma unroll
             for (int ci = 0; ci < CPL; ++ci) {
                 const int c = gl + ci * LANES;
                 uint4 o;
-                if (slot < 0) {
+                if (soff < 0) {
                     o = make_uint4(0u, 0u, 0u, 0u);
                 } else if (8 * c < nope) {
                     const uint2 w = lds_v2(srow + 8 * c);
@@ -228,64 +227,89 @@ gather_fp8_tma_kernel(GatherParams p, int slot_bytes) {
     }
 }
 
-template <int D, int UNROLL>
+// ---- MXFP4: batched loads -----------------------------------------------------------
+//
+// A 68-byte record is too small for a bulk copy to pay off, so this gather
+// uses plain loads arranged for memory-level parallelism: a warp takes a
+// batch of STEPS * GPW consecutive (t, j) items, loads their slot ids with one
+// coalesced load, then issues every record load of the batch (a 4-byte word of
+// packed E2M1 values and the scale byte per lane, for each item) before it
+// converts and stores anything.
+template <int D>
 __global__ void __launch_bounds__(kThreads)
 gather_mxfp4_kernel(GatherParams p) {
     constexpr int CHUNKS = D / 8;
     constexpr int LANES = CHUNKS < kWarp ? CHUNKS : kWarp;
     constexpr int CPL = CHUNKS / LANES;
+    constexpr int GPW = kWarp / LANES;
+    constexpr int STEPS = (kWarp / GPW) < 8 ? (kWarp / GPW) : 8;
+    constexpr int BATCH = STEPS * GPW;  // <= 32 items, one slot id per lane
     constexpr int VB = D / 2, SB = D / 32;
 
     const int lane = threadIdx.x & 31;
-    const int gl = lane % LANES;
-    const int64_t gid = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / LANES;
-    const int64_t ngroups = (int64_t)gridDim.x * kThreads / LANES;
+    const int grp = lane / LANES, gl = lane % LANES;
+    const int64_t warp_id = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / kWarp;
+    const int64_t nwarps = (int64_t)gridDim.x * kThreads / kWarp;
     const int64_t items = p.rows * (int64_t)p.cols;
     const int64_t capacity = p.num_pages * (int64_t)p.block_size;
     const bool small = items <= 0xFFFFFFFFll;
+    pdl_wait();
+    pdl_launch_dependents();
 
-    for (int64_t it0 = gid * UNROLL; it0 < items; it0 += ngroups * UNROLL) {
-        RowAddr ra[UNROLL];
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const int64_t it = it0 + u;
-            if (it < items) {
-                ra[u] = row_of(p, it, capacity, small);
+    for (int64_t b0 = warp_id * BATCH; b0 < items; b0 += nwarps * BATCH) {
+        // slot id and output offset of item b0 + lane
+        int32_t my_slot = -1;
+        int64_t my_off = -1;
+        if (lane < BATCH && b0 + lane < items) {
+            const int64_t item = b0 + lane;
+            int64_t t;
+            int32_t j;
+            if (small) {
+                const uint32_t q = (uint32_t)item / (uint32_t)p.cols;
+                t = q;
+                j = (int32_t)((uint32_t)item - q * (uint32_t)p.cols);
             } else {
-                ra[u].t = -1;
-                ra[u].slot = -1;
+                t = item / p.cols;
+                j = (int32_t)(item - t * p.cols);
+            }
+            const int32_t raw = __ldg(p.idx + t * p.idx_stride + j);
+            my_slot = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
+            my_off = t * p.out_stride_t + (int64_t)j * p.out_stride_j;
+        }
+        uint32_t raw[STEPS][CPL];
+        uint32_t scl[STEPS][CPL];
+        int32_t slot[STEPS];
+#pragma unroll
+        for (int st = 0; st < STEPS; ++st) {
+            slot[st] = __shfl_sync(0xFFFFFFFFu, my_slot, st * GPW + grp);
+            if (slot[st] >= 0) {
+                const int32_t page = slot[st] / p.block_size;
+                const int32_t off = slot[st] - page * p.block_size;
+                const uint8_t* base = p.cache + (int64_t)page * p.page_stride;
+                const uint8_t* vals = base + (int64_t)off * VB;
+                const uint8_t* sc = base + (int64_t)p.block_size * VB + (int64_t)off * SB;
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) {
+                    const int c = gl + i * LANES;
+                    raw[st][i] = ld_nc_u32(vals + 4 * c);
+                    scl[st][i] = ld_nc_u8(sc + c / 4);
+                }
             }
         }
-        uint32_t raw[UNROLL][CPL];
-        float sc[UNROLL][CPL];
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            if (ra[u].slot < 0) continue;
-            const int64_t page = ra[u].slot / p.block_size;
-            const int64_t off = ra[u].slot - page * p.block_size;
-            const uint8_t* base = p.cache + page * p.page_stride;
-            const uint8_t* vals = base + off * VB;
-            const uint8_t* scl = base + (int64_t)p.block_size * VB + off * SB;
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) {
-                const int c = gl + i * LANES;
-                raw[u][i] = ld_nc_u32(vals + 4 * c);
-                sc[u][i] = ue8m0_scale(ld_nc_u8(scl + c / 4));
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            if (ra[u].t < 0) continue;
-            uint16_t* orow = p.out + ra[u].t * p.out_stride_t + (int64_t)ra[u].j * p.out_stride_j;
+        for (int st = 0; st < STEPS; ++st) {
+            const int64_t off = __shfl_sync(0xFFFFFFFFu, my_off, st * GPW + grp);
+            if (off < 0) continue;
+            uint16_t* orow = p.out + off;
 #pragma unroll
             for (int i = 0; i < CPL; ++i) {
                 const int c = gl + i * LANES;
                 uint4 o;
-                if (ra[u].slot < 0) {
+                if (slot[st] < 0) {
                     o = make_uint4(0u, 0u, 0u, 0u);
                 } else {
-                    const float s = sc[u][i];
-                    const uint32_t w = raw[u][i];
+                    const float s = ue8m0_scale(scl[st][i]);
+                    const uint32_t w = raw[st][i];
                     uint32_t r[4];
 #pragma unroll
                     for (int b = 0; b < 4; ++b) {
@@ -318,7 +342,8 @@ cudaError_t gather_fp8_dispatch(const GatherParams& p, cudaStream_t stream) {
     // data record + the 16-byte chunks covering the scales, rounded to 16
     const int slot_bytes = (ts + ((SDIM + 15) / 16 + 1) * 16 + 15) / 16 * 16;
     const size_t smem = (size_t)kStages * kRowsPerTile * slot_bytes +
-                        2 * kStages * sizeof(uint64_t) + kStages * kRowsPerTile * sizeof(int32_t);
+                        2 * kStages * sizeof(uint64_t) +
+                        kStages * kRowsPerTile * (sizeof(int64_t) + sizeof(int32_t));
     auto kern = gather_fp8_tma_kernel<D, UE8M0>;
     static bool attr_set = false;
     if (!attr_set) {
@@ -335,19 +360,19 @@ cudaError_t gather_fp8_dispatch(const GatherParams& p, cudaStream_t stream) {
     const int64_t tiles = (items + kRowsPerTile - 1) / kRowsPerTile;
     int64_t blocks = (int64_t)sm_count() * per_sm;
     if (blocks > tiles) blocks = tiles;
-    kern<<<(unsigned)blocks, kTmaThreads, smem, stream>>>(p, slot_bytes);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kTmaThreads), smem, stream, p, slot_bytes);
 }
 
 template <int D>
 cudaError_t gather_mxfp4_dispatch(const GatherParams& p, cudaStream_t stream) {
-    constexpr int UNROLL = 4;
     constexpr int LANES = (D / 8) < kWarp ? (D / 8) : kWarp;
+    constexpr int GPW = kWarp / LANES;
+    constexpr int STEPS = (kWarp / GPW) < 8 ? (kWarp / GPW) : 8;
     const int64_t items = p.rows * (int64_t)p.cols;
-    auto kern = gather_mxfp4_kernel<D, UNROLL>;
-    const int64_t blocks = persistent_blocks(kern, (items + UNROLL - 1) / UNROLL, LANES);
-    kern<<<(unsigned)blocks, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    auto kern = gather_mxfp4_kernel<D>;
+    const int64_t batches = (items + STEPS * GPW - 1) / (STEPS * GPW);
+    const int64_t blocks = persistent_blocks(kern, batches, kWarp);
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace

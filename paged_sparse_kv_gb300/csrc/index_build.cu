@@ -167,6 +167,8 @@ __global__ void __launch_bounds__(kThreads) index_build_kernel(IndexParams p) {
     const int64_t t0 = (int64_t)blockIdx.x * p.tokens_per_cta;
     int64_t t1 = t0 + p.tokens_per_cta;
     if (t1 > p.num_tokens) t1 = p.num_tokens;
+    pdl_wait();
+    pdl_launch_dependents();
 
     // Stage the compressed block-table row when the tile is one request.
     int32_t staged = -1;
@@ -228,14 +230,9 @@ cudaError_t launch_index_build(IndexParams p, bool has_swa, cudaStream_t stream)
     const bool vec = ((reinterpret_cast<uintptr_t>(p.out) & 15) == 0) && (p.out_stride % 4 == 0) &&
                      ((reinterpret_cast<uintptr_t>(p.topk_local) & 15) == 0) &&
                      (p.topk_stride % 4 == 0) && (!has_swa || p.window % 4 == 0);
-    if (has_swa) {
-        if (vec) index_build_kernel<true, true><<<(unsigned)blocks, kThreads, smem, stream>>>(p);
-        else index_build_kernel<true, false><<<(unsigned)blocks, kThreads, smem, stream>>>(p);
-    } else {
-        if (vec) index_build_kernel<false, true><<<(unsigned)blocks, kThreads, smem, stream>>>(p);
-        else index_build_kernel<false, false><<<(unsigned)blocks, kThreads, smem, stream>>>(p);
-    }
-    return cudaGetLastError();
+    auto kern = has_swa ? (vec ? index_build_kernel<true, true> : index_build_kernel<true, false>)
+                        : (vec ? index_build_kernel<false, true> : index_build_kernel<false, false>);
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p);
 }
 
 }  // namespace psk

@@ -85,6 +85,8 @@ fp8_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
     const int64_t tok0 = gid * UNROLL;
     const int nope = D - rope;
     const int64_t ts = nope + 2 * rope;
+    pdl_wait();
+    pdl_launch_dependents();
 
     uint4 v[UNROLL][CPL];
     int64_t s[UNROLL];
@@ -183,6 +185,8 @@ mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
         LANES == 32 ? 0xFFFFFFFFu : (((1u << LANES) - 1u) << (grp * LANES));
     const int64_t gid = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / LANES;
     const int64_t tok0 = gid * UNROLL;
+    pdl_wait();
+    pdl_launch_dependents();
 
     uint4 v[UNROLL][CPL];
     int64_t s[UNROLL];
@@ -249,11 +253,10 @@ cudaError_t fp8_insert_dispatch(const InsertParams& p, cudaStream_t stream) {
     const int64_t groups = (p.num_tokens + UNROLL - 1) / UNROLL;
     const int64_t threads = groups * LANES;
     const int64_t blocks = (threads + kThreads - 1) / kThreads;
-    fp8_insert_kernel<D, UE8M0, UNROLL><<<(unsigned)blocks, kThreads, 0, stream>>>(
-        static_cast<const uint16_t*>(p.k), p.k_row_stride, p.slots, p.num_tokens, p.cache,
-        p.num_pages * (int64_t)p.block_size, p.page_stride, p.block_size, p.rope_dim,
-        p.err_count);
-    return cudaGetLastError();
+    return launch_pdl(fp8_insert_kernel<D, UE8M0, UNROLL>, dim3((unsigned)blocks), dim3(kThreads),
+                      0, stream, static_cast<const uint16_t*>(p.k), p.k_row_stride, p.slots,
+                      p.num_tokens, p.cache, p.num_pages * (int64_t)p.block_size,
+                      p.page_stride, p.block_size, p.rope_dim, p.err_count);
 }
 
 template <int D>
@@ -263,10 +266,10 @@ cudaError_t mxfp4_insert_dispatch(const InsertParams& p, cudaStream_t stream) {
     const int64_t groups = (p.num_tokens + UNROLL - 1) / UNROLL;
     const int64_t threads = groups * LANES;
     const int64_t blocks = (threads + kThreads - 1) / kThreads;
-    mxfp4_insert_kernel<D, UNROLL><<<(unsigned)blocks, kThreads, 0, stream>>>(
-        static_cast<const uint16_t*>(p.k), p.k_row_stride, p.slots, p.num_tokens, p.cache,
-        p.num_pages * (int64_t)p.block_size, p.page_stride, p.block_size, p.err_count);
-    return cudaGetLastError();
+    return launch_pdl(mxfp4_insert_kernel<D, UNROLL>, dim3((unsigned)blocks), dim3(kThreads), 0,
+                      stream, static_cast<const uint16_t*>(p.k), p.k_row_stride, p.slots,
+                      p.num_tokens, p.cache, p.num_pages * (int64_t)p.block_size,
+                      p.page_stride, p.block_size, p.err_count);
 }
 
 }  // namespace

@@ -149,6 +149,18 @@ __device__ __forceinline__ float clamp_sym(float v, float lim) {
     return v > lim ? lim : (v < -lim ? -lim : v);
 }
 
+// ---- programmatic dependent launch ------------------------------------------------
+//
+// Every libpsk kernel is launched with programmatic stream serialisation, so
+// it may start while the previous kernel on the stream is still finishing.
+// pdl_wait() blocks until that kernel has completed and its writes are
+// visible; every kernel calls it before its first global-memory access.
+// pdl_launch_dependents() lets the next kernel on the stream begin launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- integer helpers ---------------------------------------------------------------
 
 __host__ __device__ __forceinline__ int log2_if_pow2(int x) {
@@ -188,14 +200,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One try_wait; the thread may be suspended in hardware (up to the hint, in
+// ns) until the phase completes, so a waiting warp does not spin on issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
         : "memory");
     return ok != 0;
 }
@@ -212,9 +226,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
                                                   uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 

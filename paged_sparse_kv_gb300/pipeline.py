@@ -13,6 +13,19 @@ A step runs every hot-path row over one batch, in this order:
 
 Workloads without an FP8 part (the MXFP4 indexer workload) run 2, 5 and 6.
 All buffers are allocated once here; ``step()`` only launches kernels.
+
+``step(concurrent=True)`` runs the three independent chains of the step on
+three streams (fork/join with events; the same dependencies as the serial
+order):
+
+  stream M:  combine_topk_swa_indices -> gather[topk]
+  stream A:  quantize_and_insert_k_cache -> (wait for the index build) -> gather[swa]
+  stream B:  compute_global_topk_indices_and_lens -> write_indexer_mxfp4_cache
+             -> gather[mxfp4]
+
+Decode-sized kernels fill only part of the GPU, so overlapping the chains
+shortens the step to its critical path.  Capturing ``step(concurrent=True)``
+in a CUDA graph keeps the fork/join structure.
 """
 from __future__ import annotations
 
@@ -148,6 +161,51 @@ class Pipeline:
             record=ops.PSK_REC_MXFP4)))
         return L
 
-    def step(self) -> None:
-        for _, launch in self.launches():
-            launch()
+    def step(self, concurrent: bool = False, hooks: Optional[dict] = None) -> None:
+        """Launch one step.  ``hooks`` maps a kernel name to a pair of callables
+        run on that kernel's stream just before and just after its launch
+        (used to bracket one kernel with timing events)."""
+        L = dict(self.launches())
+        hooks = hooks or {}
+
+        def run(name):
+            pre, post = hooks.get(name, (None, None))
+            if pre:
+                pre()
+            L[name]()
+            if post:
+                post()
+
+        if not concurrent:
+            for name in L:
+                run(name)
+            return
+        main = torch.cuda.current_stream(self.dev)
+        if not hasattr(self, "_side"):
+            self._side = (torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev))
+        sa, sb = self._side
+        fork = torch.cuda.Event()
+        fork.record(main)
+        sa.wait_event(fork)
+        sb.wait_event(fork)
+        with torch.cuda.stream(sb):
+            run("compute_global_topk_indices_and_lens")
+            if "write_indexer_mxfp4_cache" in L:
+                run("write_indexer_mxfp4_cache")
+            run("dequantize_and_gather_k_cache[mxfp4]")
+            done_b = torch.cuda.Event()
+            done_b.record(sb)
+        if self.w.has_fp8:
+            with torch.cuda.stream(sa):
+                run("quantize_and_insert_k_cache")
+            run("combine_topk_swa_indices")
+            built = torch.cuda.Event()
+            built.record(main)
+            with torch.cuda.stream(sa):
+                sa.wait_event(built)
+                run("dequantize_and_gather_k_cache[swa]")
+                done_a = torch.cuda.Event()
+                done_a.record(sa)
+            run("dequantize_and_gather_k_cache[topk]")
+            main.wait_event(done_a)
+        main.wait_event(done_b)

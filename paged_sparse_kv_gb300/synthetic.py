@@ -218,10 +218,10 @@ def make_decode(seed: int = BASE_SEED + 1) -> Workload:
         index_cache=CacheGeom(comp_pages, bs, bs * mxfp4_record_bytes(128)))
 
 
-def make_prefill(seed: int = BASE_SEED + 2) -> Workload:
+def make_prefill(seed: int = BASE_SEED + 2, num_reqs: int = 4) -> Workload:
     rng = np.random.default_rng(seed)
     gen = torch.Generator().manual_seed(seed)
-    R, Q, bs, D, rope, W, K, ratio = 4, 4096, 64, 512, 64, 128, 512, 4
+    R, Q, bs, D, rope, W, K, ratio = num_reqs, 4096, 64, 512, 64, 128, 512, 4
     T = R * Q
     lens = np.full(R, Q, dtype=np.int32)
     qsl = (np.arange(R + 1) * Q).astype(np.int32)
@@ -238,7 +238,7 @@ def make_prefill(seed: int = BASE_SEED + 2) -> Workload:
     topk = np.stack([_distinct_topk(rng, K, int(p + 1) // ratio, K) for p in pos])
     geom = CacheGeom(1024, bs, bs * fp8_record_bytes(D, rope))
     return Workload(
-        name="prefill", seed=seed, head_dim=D, rope_dim=rope, index_head_dim=128,
+        name="prefill" if num_reqs == 4 else f"prefill_{num_reqs}req", seed=seed, head_dim=D, rope_dim=rope, index_head_dim=128,
         window=W, compress_ratio=ratio, topk=K,
         k=_randn_bf16(gen, T, D, outlier_frac=0.01, outlier_scale=20.0),
         insert_slots=insert,
@@ -333,12 +333,22 @@ def make_mxfp4(seed: int = BASE_SEED + 4) -> Workload:
         has_fp8=False)
 
 
+def make_prefill_small(seed: int = BASE_SEED + 5) -> Workload:
+    """One request of the prefill workload (4096 new tokens): the same kernels
+    at a quarter of the size, small enough for a full profiler capture."""
+    return make_prefill(seed, num_reqs=1)
+
+
 MAKERS = {"tiny": make_tiny, "decode": make_decode, "prefill": make_prefill,
-          "mixed": make_mixed, "mxfp4": make_mxfp4}
+          "mixed": make_mixed, "mxfp4": make_mxfp4, "prefill_small": make_prefill_small}
+DEFAULT_SEEDS = {"tiny": BASE_SEED + 0, "decode": BASE_SEED + 1, "prefill": BASE_SEED + 2,
+                 "mixed": BASE_SEED + 3, "mxfp4": BASE_SEED + 4, "prefill_small": BASE_SEED + 5}
 
 
-def make(name: str) -> Workload:
-    return MAKERS[name]()
+def make(name: str, seed_offset: int = 0) -> Workload:
+    """The named workload, drawn from its seed (plus seed_offset, e.g. one
+    independent batch per GPU)."""
+    return MAKERS[name](DEFAULT_SEEDS[name] + seed_offset)
 
 
 def random_cache_bytes(seed: int, geom: CacheGeom) -> np.ndarray:

@@ -353,8 +353,13 @@ def test_mxfp4_gather_random_records(cuda_device, D):
 SAMPLE = {"tiny": None, "decode": None, "prefill": 48, "mixed": 48, "mxfp4": None}
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "mixed", "mxfp4"])
-def test_pipeline_step_matches_oracle(cuda_device, name):
+@pytest.mark.parametrize("name,mode", [("tiny", "serial"), ("decode", "serial"),
+                                       ("prefill", "serial"), ("mixed", "serial"),
+                                       ("mxfp4", "serial"), ("tiny", "graph"),
+                                       ("decode", "graph"), ("mixed", "concurrent")])
+def test_pipeline_step_matches_oracle(cuda_device, name, mode):
+    """The whole step at full size, launched the way the benchmark launches it
+    (serial, three concurrent streams, or a CUDA graph of the concurrent step)."""
     w = synthetic.make(name)
     host = {}
     for i, cname in enumerate(("swa_cache", "comp_cache", "index_cache")):
@@ -364,7 +369,22 @@ def test_pipeline_step_matches_oracle(cuda_device, name):
     for cname, arr in host.items():
         if arr is not None:
             getattr(p, cname).copy_(torch.from_numpy(arr))
-    p.step()
+    if mode == "serial":
+        p.step()
+    elif mode == "concurrent":
+        p.step(concurrent=True)
+    else:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(cuda_device)
+        side.wait_stream(torch.cuda.current_stream(cuda_device))
+        with torch.cuda.graph(g, stream=side):
+            p.step(concurrent=True)
+        torch.cuda.synchronize()
+        # capture launched nothing: the caches still hold the initial bytes
+        for cname, arr in host.items():
+            if arr is not None:
+                _assert_same(getattr(p, cname).cpu().numpy(), arr, f"{name} {cname} untouched")
+        g.replay()
     torch.cuda.synchronize()
     toks = None
     if SAMPLE[name]:
