@@ -79,6 +79,14 @@ def _load():
         "oracle_dequantize_and_gather_k_cache": (
             None, [_P, _I64, _I64, _P, _I64, _I64, _I32, _I32, _I32, _I32, _I32,
                    _P, _I64, _I64, _I32]),
+        "oracle_dequantize_and_gather_k_cache_ranges": (
+            None, [_P, _I64, _I64, _I64, _P, _I64, _I64, _I32, _I32, _I32, _I32, _I32,
+                   _P, _P, _P, _I64, _I32, _P, _I32, _I64]),
+        "oracle_combine_topk_swa_workspace_indices": (
+            None, [_P, _P, _P, _P, _I32, _I64, _I32, _I32, _P, _I64, _I32, _I64, _I64,
+                   _P, _P, _I64, _P]),
+        "oracle_indexer_mxfp4_paged_gather": (
+            None, [_P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _I32, _P, _I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -246,3 +254,59 @@ def dequantize_and_gather_k_cache(cache, block_size, record, head_dim, rope_dim,
         cache.shape[1], block_size, record, head_dim, rope_dim, int(bool(is_ue8m0)),
         _ptr(indices), cols, rows, cols)
     return out
+
+
+def dequantize_and_gather_k_cache_ranges(out, cache, block_size, record, head_dim, rope_dim,
+                                         seq_lens, gather_lens, block_table, offset,
+                                         base_offsets=None, is_ue8m0=True) -> np.ndarray:
+    """Range-form gather into ``out`` (uint16 [R, rows, head_dim], updated in place)."""
+    seq_lens = _as(seq_lens, np.int32)
+    gather_lens = _as(gather_lens, np.int32)
+    block_table = _as(block_table, np.int32)
+    base_offsets = _as(base_offsets, np.int32)
+    assert out.dtype == np.uint16 and out.ndim == 3 and out.flags["C_CONTIGUOUS"]
+    assert cache.dtype == np.uint8 and cache.ndim == 2 and cache.flags["C_CONTIGUOUS"]
+    R, rows, D = out.shape
+    assert D == head_dim and seq_lens.shape[0] == R
+    _load().oracle_dequantize_and_gather_k_cache_ranges(
+        _ptr(out), rows * D, D, rows, _ptr(cache), cache.shape[0], cache.shape[1], block_size,
+        record, head_dim, rope_dim, int(bool(is_ue8m0)), _ptr(seq_lens), _ptr(gather_lens),
+        _ptr(block_table), block_table.shape[1], block_table.shape[1], _ptr(base_offsets), R,
+        offset)
+    return out
+
+
+def combine_topk_swa_workspace_indices(query_start_loc, seq_lens, gather_lens, token_to_req,
+                                       window, compress_ratio, topk_local, workspace_width,
+                                       compressed_base, is_valid_token=None):
+    query_start_loc = _as(query_start_loc, np.int32)
+    seq_lens = _as(seq_lens, np.int32)
+    gather_lens = _as(gather_lens, np.int32)
+    token_to_req = _as(token_to_req, np.int32)
+    topk_local = _as(topk_local, np.int32)
+    if is_valid_token is not None:
+        is_valid_token = np.ascontiguousarray(is_valid_token).astype(np.uint8)
+    T, K = topk_local.shape
+    P = (K + 3) // 4 * 4
+    out = np.empty((T, window + P), dtype=np.int32)
+    lens = np.empty((T,), dtype=np.int32)
+    _load().oracle_combine_topk_swa_workspace_indices(
+        _ptr(query_start_loc), _ptr(seq_lens), _ptr(gather_lens), _ptr(token_to_req),
+        seq_lens.shape[0], T, window, compress_ratio, _ptr(topk_local), K, K, workspace_width,
+        compressed_base, _ptr(is_valid_token), _ptr(out), window + P, _ptr(lens))
+    return out, lens
+
+
+def indexer_mxfp4_paged_gather(cache, block_size, head_dim, block_table, cu_seq_lens):
+    """Raw MXFP4 rows over per-request ranges: (values [N, D/2], scales [N, D/32])."""
+    block_table = _as(block_table, np.int32)
+    cu_seq_lens = _as(cu_seq_lens, np.int32)
+    assert cache.dtype == np.uint8 and cache.ndim == 2 and cache.flags["C_CONTIGUOUS"]
+    n = int(cu_seq_lens[-1])
+    values = np.empty((n, head_dim // 2), dtype=np.uint8)
+    scales = np.empty((n, head_dim // 32), dtype=np.uint8)
+    _load().oracle_indexer_mxfp4_paged_gather(
+        _ptr(values), _ptr(scales), _ptr(cache), cache.shape[0], cache.shape[1], block_size,
+        head_dim, _ptr(block_table), block_table.shape[1], block_table.shape[1],
+        _ptr(cu_seq_lens), cu_seq_lens.shape[0] - 1)
+    return values, scales

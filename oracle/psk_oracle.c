@@ -548,3 +548,142 @@ void oracle_dequantize_and_gather_k_cache(
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Prefill workspace path: range gather, workspace indices, raw MXFP4 gather  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Range form of the gather ([VLLM] dequantize_and_gather_k_cache(out, k_cache,
+ * seq_lens, gather_lens, block_table, block_size, offset); called twice per
+ * layer by [BE] _prefill_workspace, compressed rows at offset 0 and window rows
+ * at offset compressed_base).  For request r, with g = gather_lens[r] (or
+ * seq_lens[r] when gather_lens is NULL), row i in [0, g) is position
+ * p = seq_lens[r] - g + i, mapped through the request's block-table row, and
+ * goes to out[r][offset + i] (dequantized as in the index form; a missing page
+ * gives a zero row).  Rows outside [offset, offset + g), and rows at or beyond
+ * out_rows, are not written.
+ */
+void oracle_dequantize_and_gather_k_cache_ranges(
+    uint16_t* out, int64_t out_stride_r, int64_t out_stride_i, int64_t out_rows,
+    const uint8_t* cache, int64_t num_pages, int64_t page_stride,
+    int32_t block_size, int32_t record, int32_t head_dim, int32_t rope_dim,
+    int32_t is_ue8m0, const int32_t* seq_lens, const int32_t* gather_lens,
+    const int32_t* block_table, int64_t bt_stride, int32_t bt_width,
+    const int32_t* base_offsets, int32_t num_reqs, int64_t offset) {
+    for (int32_t r = 0; r < num_reqs; ++r) {
+        const int64_t seq = seq_lens[r];
+        const int64_t g = gather_lens ? gather_lens[r] : seq;
+        const int64_t base = base_offsets ? base_offsets[r] : 0;
+        for (int64_t i = 0; i < g; ++i) {
+            if (offset + i < 0 || offset + i >= out_rows) continue;
+            const int64_t p = seq - g + i;
+            const int32_t s = slot_of(block_table + (int64_t)r * bt_stride, bt_width, base,
+                                      block_size, p);
+            /* one row through the index-form gather of that slot */
+            oracle_dequantize_and_gather_k_cache(
+                out + r * out_stride_r + (offset + i) * out_stride_i, 0, 0, cache, num_pages,
+                page_stride, block_size, record, head_dim, rope_dim, is_ue8m0, &s, 1, 1, 1);
+        }
+    }
+}
+
+/*
+ * Workspace-relative form of the fused index build (TokenSpeed's
+ * combine_topk_swa_indices as called by [BE] _prefill_workspace with
+ * workspace_width and compressed_base).  Request r's workspace rows start at
+ * r * workspace_width: its compressed entries 0 .. floor(seq_lens[r] / ratio) - 1
+ * at rows 0.., its gathered window positions g0 .. seq_lens[r] - 1 at rows
+ * compressed_base.., with g0 = seq_lens[r] - gather_lens[r].  For token t at
+ * pos (as in the global-slot builder):
+ *   columns [0, W): position lo + c, lo = max(pos - W + 1, 0), maps to row
+ *     r*ww + compressed_base + (p - g0) when g0 <= p <= pos, else -1;
+ *   columns [W, W + topk): local index l maps to r*ww + l when
+ *     0 <= l < floor(seq_lens[r] / ratio), else -1;
+ *   padding to W + roundup(topk, 4): -1;  lens = entries >= 0.
+ * Same column layout as the global-slot builder (a reading: the kernel body is
+ * not printed).  A padding token is all -1 with lens 0.
+ */
+void oracle_combine_topk_swa_workspace_indices(
+    const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* gather_lens, const int32_t* token_to_req, int32_t num_reqs,
+    int64_t num_tokens, int32_t window, int32_t compress_ratio,
+    const int32_t* topk_local, int64_t topk_stride, int32_t topk,
+    int64_t workspace_width, int64_t compressed_base,
+    const uint8_t* is_valid_token, int32_t* indices, int64_t out_stride,
+    int32_t* lens) {
+    const int32_t padded = (topk + 3) / 4 * 4;
+    const int32_t width = window + padded;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int32_t* row = indices + t * out_stride;
+        const int32_t r = token_to_req[t];
+        const int ok = (is_valid_token ? is_valid_token[t] != 0 : 1) &&
+                       r >= 0 && r < num_reqs;
+        if (!ok) {
+            for (int32_t c = 0; c < width; ++c) row[c] = -1;
+            lens[t] = 0;
+            continue;
+        }
+        const int64_t qstart = query_start_loc[r];
+        const int64_t qlen = (int64_t)query_start_loc[r + 1] - qstart;
+        const int64_t seq = seq_lens[r];
+        const int64_t pos = seq - qlen + (t - qstart);
+        const int64_t g0 = seq - gather_lens[r];
+        const int64_t lc = seq / compress_ratio;
+        const int64_t rbase = (int64_t)r * workspace_width;
+        int64_t lo = pos - window + 1;
+        if (lo < 0) lo = 0;
+        int32_t count = 0;
+        for (int32_t c = 0; c < window; ++c) {
+            const int64_t p = lo + c;
+            int64_t v = -1;
+            if (p <= pos && p >= g0) v = rbase + compressed_base + (p - g0);
+            if (v > INT32_MAX) v = -1;
+            row[c] = (int32_t)v;
+            if (v >= 0) ++count;
+        }
+        for (int32_t j = 0; j < topk; ++j) {
+            const int64_t l = topk_local[t * topk_stride + j];
+            int64_t v = (l >= 0 && l < lc) ? rbase + l : -1;
+            if (v > INT32_MAX) v = -1;
+            row[window + j] = (int32_t)v;
+            if (v >= 0) ++count;
+        }
+        for (int32_t j = topk; j < padded; ++j) row[window + j] = -1;
+        lens[t] = count;
+    }
+}
+
+/*
+ * Raw (packed) gather of MXFP4 indexer keys over per-request ranges
+ * ([MDL] _deepseek_v4_gather_paged_indexer_mxfp4_cache -> indexer_mxfp4_paged_gather):
+ * output row cu_seq_lens[r] + i (i < cu_seq_lens[r+1] - cu_seq_lens[r]) holds the
+ * head_dim/2 value bytes and head_dim/32 scale bytes of local position i of
+ * request r, copied unchanged; a position without a page gives zero bytes.
+ */
+void oracle_indexer_mxfp4_paged_gather(
+    uint8_t* values_out, uint8_t* scales_out, const uint8_t* cache,
+    int64_t num_pages, int64_t page_stride, int32_t block_size,
+    int32_t head_dim, const int32_t* block_table, int64_t bt_stride,
+    int32_t bt_width, const int32_t* cu_seq_lens, int32_t num_reqs) {
+    const int64_t vb = head_dim / 2, sb = head_dim / 32;
+    const int64_t capacity = num_pages * (int64_t)block_size;
+    for (int32_t r = 0; r < num_reqs; ++r) {
+        for (int64_t row = cu_seq_lens[r]; row < cu_seq_lens[r + 1]; ++row) {
+            const int64_t i = row - cu_seq_lens[r];
+            const int32_t s = slot_of(block_table + (int64_t)r * bt_stride, bt_width, 0,
+                                      block_size, i);
+            uint8_t* vo = values_out + row * vb;
+            uint8_t* so = scales_out + row * sb;
+            if (s < 0 || s >= capacity) {
+                memset(vo, 0, (size_t)vb);
+                memset(so, 0, (size_t)sb);
+                continue;
+            }
+            const int64_t page = s / block_size, off = s % block_size;
+            const uint8_t* base = cache + page * page_stride;
+            memcpy(vo, base + off * vb, (size_t)vb);
+            memcpy(so, base + (int64_t)block_size * vb + off * sb, (size_t)sb);
+        }
+    }
+}

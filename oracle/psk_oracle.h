@@ -80,6 +80,30 @@ void oracle_dequantize_and_gather_k_cache(
     int32_t is_ue8m0, const int32_t* indices, int64_t idx_stride, int64_t rows,
     int32_t cols);
 
+/* ---- range-form gather, workspace indices, raw MXFP4 gather ---- */
+void oracle_dequantize_and_gather_k_cache_ranges(
+    uint16_t* out, int64_t out_stride_r, int64_t out_stride_i, int64_t out_rows,
+    const uint8_t* cache, int64_t num_pages, int64_t page_stride,
+    int32_t block_size, int32_t record, int32_t head_dim, int32_t rope_dim,
+    int32_t is_ue8m0, const int32_t* seq_lens, const int32_t* gather_lens,
+    const int32_t* block_table, int64_t bt_stride, int32_t bt_width,
+    const int32_t* base_offsets, int32_t num_reqs, int64_t offset);
+
+void oracle_combine_topk_swa_workspace_indices(
+    const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* gather_lens, const int32_t* token_to_req, int32_t num_reqs,
+    int64_t num_tokens, int32_t window, int32_t compress_ratio,
+    const int32_t* topk_local, int64_t topk_stride, int32_t topk,
+    int64_t workspace_width, int64_t compressed_base,
+    const uint8_t* is_valid_token, int32_t* indices, int64_t out_stride,
+    int32_t* lens);
+
+void oracle_indexer_mxfp4_paged_gather(
+    uint8_t* values_out, uint8_t* scales_out, const uint8_t* cache,
+    int64_t num_pages, int64_t page_stride, int32_t block_size,
+    int32_t head_dim, const int32_t* block_table, int64_t bt_stride,
+    int32_t bt_width, const int32_t* cu_seq_lens, int32_t num_reqs);
+
 #ifdef __cplusplus
 }
 #endif

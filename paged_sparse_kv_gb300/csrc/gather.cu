@@ -15,7 +15,7 @@
 // the gathered output does not push reused cache rows out of L2.  Decode is
 // exact: cvt.rn.f16x2.{e4m3x2,e2m1x2}, a binary32 multiply by the scale, and
 // cvt.rn.bf16x2.f32.  Invalid slots (negative or beyond the cache) give zero
-// rows.
+// rows.  The scale multiply is one packed mul.rn.f32x2 per pair of elements.
 #include "launch.h"
 #include "psk_common.cuh"
 
@@ -208,14 +208,11 @@ gather_fp8_tma_kernel(GatherParams p, int slot_bytes) {
                     } else {
                         sc = __uint_as_float(lds_u32(srow + ts + soff + 4 * (c / 8)));
                     }
-                    const uint32_t h0 = cvt_e4m3x2_to_f16x2(w.x & 0xFFFFu);
-                    const uint32_t h1 = cvt_e4m3x2_to_f16x2(w.x >> 16);
-                    const uint32_t h2 = cvt_e4m3x2_to_f16x2(w.y & 0xFFFFu);
-                    const uint32_t h3 = cvt_e4m3x2_to_f16x2(w.y >> 16);
-                    o.x = pack_bf16x2(__fmul_rn(f16_lo(h0), sc), __fmul_rn(f16_hi(h0), sc));
-                    o.y = pack_bf16x2(__fmul_rn(f16_lo(h1), sc), __fmul_rn(f16_hi(h1), sc));
-                    o.z = pack_bf16x2(__fmul_rn(f16_lo(h2), sc), __fmul_rn(f16_hi(h2), sc));
-                    o.w = pack_bf16x2(__fmul_rn(f16_lo(h3), sc), __fmul_rn(f16_hi(h3), sc));
+                    const uint64_t s2 = splat_f32x2(sc);
+                    o.x = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x & 0xFFFFu), s2);
+                    o.y = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x >> 16), s2);
+                    o.z = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y & 0xFFFFu), s2);
+                    o.w = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y >> 16), s2);
                 } else {
                     o = lds_v4(srow + 16 * c - nope);
                 }
@@ -308,15 +305,12 @@ gather_mxfp4_kernel(GatherParams p) {
                 if (slot[st] < 0) {
                     o = make_uint4(0u, 0u, 0u, 0u);
                 } else {
-                    const float s = ue8m0_scale(scl[st][i]);
+                    const uint64_t s2 = splat_f32x2(ue8m0_scale(scl[st][i]));
                     const uint32_t w = raw[st][i];
-                    uint32_t r[4];
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        const uint32_t h = cvt_e2m1x2_to_f16x2((w >> (8 * b)) & 0xFFu);
-                        r[b] = pack_bf16x2(__fmul_rn(f16_lo(h), s), __fmul_rn(f16_hi(h), s));
-                    }
-                    o = make_uint4(r[0], r[1], r[2], r[3]);
+                    o.x = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(w & 0xFFu), s2);
+                    o.y = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((w >> 8) & 0xFFu), s2);
+                    o.z = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((w >> 16) & 0xFFu), s2);
+                    o.w = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(w >> 24), s2);
                 }
                 st_stream_v4(orow + 8 * c, o);
             }

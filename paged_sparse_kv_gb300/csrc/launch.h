@@ -81,6 +81,7 @@ struct IndexParams {
     int32_t tokens_per_cta;
     int32_t warps_per_token;
     int32_t stage_comp;  // entries of the compressed row staged in shared memory
+    int32_t stage_swa;   // entries of the SWA row staged in shared memory
 };
 
 // has_swa = true: the fused window + top-k build; false: top-k mapping only.

@@ -144,6 +144,27 @@ __device__ __forceinline__ float f16_hi(uint32_t h2) {
     return f;
 }
 
+// Two f16 (packed) times a binary32 scale pair {s, s}, rounded to packed bf16:
+// each half widened to binary32 exactly, one packed multiply (mul.rn.f32x2,
+// IEEE round-to-nearest per element, subnormals kept), then cvt.rn.bf16x2.
+__device__ __forceinline__ uint32_t scale_f16x2_to_bf16x2(uint32_t h2, uint64_t s2) {
+    const float lo = f16_lo(h2), hi = f16_hi(h2);
+    uint32_t r;
+    asm("{\n\t.reg .b64 x, y;\n\t.reg .b32 a, b;\n\t"
+        "mov.b64 x, {%1, %2};\n\t"
+        "mul.rn.f32x2 y, x, %3;\n\t"
+        "mov.b64 {a, b}, y;\n\t"
+        "cvt.rn.bf16x2.f32 %0, b, a;\n\t}"
+        : "=r"(r)
+        : "f"(lo), "f"(hi), "l"(s2));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t splat_f32x2(float s) {
+    const uint64_t b = __float_as_uint(s);
+    return (b << 32) | b;
+}
+
 // Clamp to [-lim, lim] keeping NaN and the sign of zero.
 __device__ __forceinline__ float clamp_sym(float v, float lim) {
     return v > lim ? lim : (v < -lim ? -lim : v);
