@@ -96,6 +96,33 @@ def algorithmic_bytes(p, outputs) -> dict:
     return res
 
 
+def workspace_algorithmic_bytes(p) -> dict:
+    """Compulsory bytes of the prefill workspace step's launches."""
+    from paged_sparse_kv_gb300.pipeline import workspace_geometry
+    w = p.w
+    g = workspace_geometry(w)
+    D = w.head_dim
+    rec = D - w.rope_dim + 2 * w.rope_dim + D // 64
+    T, K, R = w.num_tokens, w.topk, w.num_reqs
+    res = {}
+    ins = w.insert_slots
+    res["quantize_and_insert_k_cache"] = int((ins >= 0).sum()) * (2 * D + rec) + ins.size * 8
+    ins = w.index_insert_slots
+    Di = w.index_head_dim
+    res["write_indexer_mxfp4_cache"] = int((ins >= 0).sum()) * (2 * Di + Di // 2 + Di // 32) + \
+        ins.size * 8
+    cb = g["compressed_base"]
+    rows_c = int(np.minimum(g["compressed_lens"], cb).sum())
+    rows_w = int(np.minimum(g["gather_lens"], g["workspace_width"] - cb).sum())
+    res["dequantize_and_gather_k_cache_ranges[compressed]"] = rows_c * (rec + 2 * D) + R * 8
+    res["dequantize_and_gather_k_cache_ranges[swa]"] = rows_w * (rec + 2 * D) + R * 12
+    P = w.padded_topk
+    res["combine_topk_swa_workspace_indices"] = T * (4 * K + 4 * (w.window + P) + 8) + R * 16
+    n_raw = int(g["cu_compressed"][-1])
+    res["indexer_mxfp4_paged_gather"] = n_raw * 2 * (Di // 2 + Di // 32) + (R + 1) * 4
+    return res
+
+
 # ---- clocks sampled during the timed region --------------------------------------------
 
 class ClockSampler:
@@ -166,10 +193,22 @@ def _oracle_sample_tokens(w, max_rows: int):
     return np.linspace(0, w.num_tokens - 1, n).astype(np.int64), n
 
 
-def time_oracle(w, budget_s: float, max_rows: int = 80000):
+def time_oracle(w, budget_s: float, max_rows: int = 80000, path: str = "index"):
     """Run oracle steps until budget_s of CPU work; returns (tokens/s, desc)."""
-    from oracle.pipeline import run_step
+    from oracle.pipeline import run_step, run_workspace_step
     caches = _oracle_state(w)
+    if path == "workspace":
+        from paged_sparse_kv_gb300.pipeline import workspace_geometry
+        geom = workspace_geometry(w)
+        steps, spent = 0, 0.0
+        while spent < budget_s or steps == 0:
+            t0 = time.perf_counter()
+            run_workspace_step(w, geom, caches["swa_cache"], caches["comp_cache"],
+                               caches["index_cache"])
+            spent += time.perf_counter() - t0
+            steps += 1
+        return (w.num_tokens * steps / spent,
+                f"{steps} oracle steps of the {w.name} batch on the workspace path")
     toks, n = _oracle_sample_tokens(w, max_rows)
     steps, spent = 0, 0.0
     while spent < budget_s or steps == 0:
@@ -219,9 +258,9 @@ def recorded_traffic(config: str, kernel: str):
     return None
 
 
-def _instrumented(p, names, evs):
+def _instrumented(launches, names, evs):
     """The step serialised on the current stream, an event before each kernel."""
-    L = dict(p.launches())
+    L = dict(launches)
     evs[0].record()
     for i, n in enumerate(names):
         L[n]()
@@ -255,6 +294,9 @@ def main():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--path", default="index", choices=["index", "workspace"],
+                    help="index: the index-keyed gather into [T, W+P, D]; workspace: the "
+                         "prefill workspace path (range gathers + workspace indices)")
     ap.add_argument("--eager", action="store_true",
                     help="launch the step eagerly instead of replaying a CUDA graph")
     args = ap.parse_args()
@@ -284,20 +326,26 @@ def main():
     w = synthetic.make(args.config, seed_offset=1000 * rank)
     p = Pipeline(w, dev)
     p.fill_caches_with_quantized_rows(seed=4321 + rank)
-    launches = p.launches()
+    path = args.path
+    if path == "workspace" and not w.has_fp8:
+        raise SystemExit("the workspace path needs a workload with an FP8 part")
+    launches = p.workspace_launches() if path == "workspace" else p.launches()
     names = [n for n, _ in launches]
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
         flush.zero_()
-        p.step(concurrent=True)
+        p.step(concurrent=True, path=path)
     torch.cuda.synchronize(dev)
 
-    outputs = {"global_topk": p.global_topk.cpu().numpy()}
-    if w.has_fp8:
-        outputs["sparse_indices"] = p.sparse_indices.cpu().numpy()
-    alg = algorithmic_bytes(p, outputs)
+    if path == "workspace":
+        alg = workspace_algorithmic_bytes(p)
+    else:
+        outputs = {"global_topk": p.global_topk.cpu().numpy()}
+        if w.has_fp8:
+            outputs["sparse_indices"] = p.sparse_indices.cpu().numpy()
+        alg = algorithmic_bytes(p, outputs)
 
     visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x]
     clocks = ClockSampler(visible[local_rank] if local_rank < len(visible) else str(local_rank))
@@ -309,7 +357,7 @@ def main():
     kern_ms = {n: [] for n in names}
     if use_graph:
         evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(names) + 1)]
-        g_ser = _capture(torch, dev, stream, lambda: _instrumented(p, names, evs))
+        g_ser = _capture(torch, dev, stream, lambda: _instrumented(launches, names, evs))
         for _ in range(max(5, min(args.steps, 30))):
             flush.zero_()
             g_ser.replay()
@@ -321,7 +369,7 @@ def main():
         for _ in range(max(5, min(args.steps, 30))):
             evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
             flush.zero_()
-            _instrumented(p, names, evs)
+            _instrumented(launches, names, evs)
             torch.cuda.synchronize(dev)
             for i, n in enumerate(names):
                 kern_ms[n].append(evs[i].elapsed_time(evs[i + 1]))
@@ -340,8 +388,9 @@ def main():
     hooks = {top: (lambda: k_pre.record(), lambda: k_post.record())}
     g_plain = g_inst = None
     if use_graph:
-        g_plain = _capture(torch, dev, stream, lambda: p.step(concurrent=True))
-        g_inst = _capture(torch, dev, stream, lambda: p.step(concurrent=True, hooks=hooks))
+        g_plain = _capture(torch, dev, stream, lambda: p.step(concurrent=True, path=path))
+        g_inst = _capture(torch, dev, stream,
+                          lambda: p.step(concurrent=True, hooks=hooks, path=path))
         for _ in range(args.warmup):
             flush.zero_()
             g_plain.replay()
@@ -360,13 +409,13 @@ def main():
         if g_plain is not None:
             g_plain.replay()
         else:
-            p.step(concurrent=True)
+            p.step(concurrent=True, path=path)
         t_end.record(stream)
         flush.zero_()
         if g_inst is not None:
             g_inst.replay()
         else:
-            p.step(concurrent=True, hooks=hooks)
+            p.step(concurrent=True, hooks=hooks, path=path)
         k_post.synchronize()
         torch.cuda.synchronize(dev)
         step_ms.append(t_start.elapsed_time(t_end))
@@ -385,7 +434,7 @@ def main():
     value = w.num_tokens * world / (ms_per_step / 1e3)
 
     # ---- end to end through the public API with host buffers ----
-    e2e = run_e2e(p, args, dev, flush)
+    e2e = run_e2e(p, args, dev, flush, path)
     if dist:
         t = torch.tensor([e2e["ms_per_step"]], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -418,6 +467,7 @@ def main():
         "config": {"workload": f"{w.name}: {w.num_reqs} requests, {w.num_tokens} query tokens, "
                                f"head_dim {w.head_dim} (rope {w.rope_dim}), window {w.window}, "
                                f"top-k {w.topk}, ratio {w.compress_ratio}",
+                   "path": path,
                    "seed": w.seed, "l2": "flushed before every step (512 MiB memset)",
                    "parallelism": f"dp{world} (independent batch per GPU)",
                    "launch": ("cuda graph of the step on three streams" if g_plain is not None
@@ -437,7 +487,7 @@ def main():
         "wall_s_timed_region": round(t_wall, 4),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, desc = time_oracle(w, args.cpu_budget)
+        v, desc = time_oracle(w, args.cpu_budget, path=path)
         line["cpu_baseline"] = {"value": round(v, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": desc}
     if rank == 0:
@@ -446,13 +496,16 @@ def main():
         dist.destroy_process_group()
 
 
-def run_e2e(p, args, dev, flush):
+def run_e2e(p, args, dev, flush, path="index"):
     """The step through the public API with pinned host inputs and outputs."""
     import torch
     ins = [t for t in (p.k, p.insert_slots, p.index_k, p.index_insert_slots, p.qsl, p.seq_lens,
                        p.t2r, p.replay, p.topk) if t is not None]
-    outs = [t for t in (p.sparse_indices, p.lens, p.gathered, p.global_topk, p.global_lens,
-                        p.gathered_index) if t is not None]
+    if path == "workspace":
+        outs = [p.ws, p.ws_indices, p.ws_lens, p.raw_values, p.raw_scales]
+    else:
+        outs = [t for t in (p.sparse_indices, p.lens, p.gathered, p.global_topk, p.global_lens,
+                            p.gathered_index) if t is not None]
     h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in ins]
     h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
@@ -464,7 +517,7 @@ def run_e2e(p, args, dev, flush):
         t0 = time.perf_counter()
         for d, h in zip(ins, h_in):
             d.copy_(h, non_blocking=True)
-        p.step(concurrent=True)
+        p.step(concurrent=True, path=path)
         for h, d in zip(h_out, outs):
             h.copy_(d, non_blocking=True)
         torch.cuda.synchronize(dev)

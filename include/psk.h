@@ -245,6 +245,85 @@ psk_status dequantize_and_gather_k_cache(
     int32_t is_ue8m0, const int32_t* indices, int64_t idx_stride, int64_t rows,
     int32_t cols, psk_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Prefill workspace path (TokenSpeed backends/deepseek_v4.py, _prefill_workspace) */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * dequantize_and_gather_k_cache_ranges -- range-form dequantize + gather.
+ * [VLLM] dequantize_and_gather_k_cache(out, k_cache, seq_lens, gather_lens,
+ * block_table, block_size, offset); [BE] _prefill_workspace calls it for the
+ * compressed cache (offset 0, gather_lens NULL) and the SWA cache (offset
+ * compressed_base, gather_lens = query_lens + min(prefix, W - 1)).
+ *
+ *   out          bf16 [num_reqs, out_rows, head_dim]; row i of request r starts
+ *                at out + r*out_stride_r + i*out_stride_i (elements, multiples
+ *                of 8).
+ *   For request r, g = gather_lens[r] (seq_lens[r] when gather_lens is NULL):
+ *   row i in [0, g) is position seq_lens[r] - g + i, mapped through
+ *   block_table[r] (logical page position/block_size - base_offsets[r]) and
+ *   written, dequantized as dequantize_and_gather_k_cache does, to out row
+ *   offset + i; a position without a page gives a zero row.  Rows at or beyond
+ *   out_rows, and rows of out outside [offset, offset + g), are not written.
+ *   record must be PSK_REC_FP8_DS_MLA (PSK_ERR_UNSUPPORTED otherwise).
+ *   Requires 0 <= offset <= out_rows and out_rows - offset <= INT32_MAX.
+ */
+psk_status dequantize_and_gather_k_cache_ranges(
+    void* out, int64_t out_stride_r, int64_t out_stride_i, int64_t out_rows,
+    const uint8_t* cache, int64_t num_pages, int64_t page_stride,
+    int32_t block_size, psk_record record, int32_t head_dim, int32_t rope_dim,
+    int32_t is_ue8m0, const int32_t* seq_lens, const int32_t* gather_lens,
+    const int32_t* block_table, int64_t bt_stride, int32_t bt_width,
+    const int32_t* base_offsets, int32_t num_reqs, int64_t offset,
+    psk_stream_t stream);
+
+/*
+ * combine_topk_swa_workspace_indices -- workspace-relative fused index build.
+ * TokenSpeed's combine_topk_swa_indices(topk_indices, query_start_loc,
+ * seq_lens, gather_lens, window_size, compress_ratio, topk, workspace_width,
+ * compressed_base) as [BE] _prefill_workspace calls it.
+ *
+ *   Request r's workspace rows start at r * workspace_width: its compressed
+ *   entries 0 .. seq_lens[r]/compress_ratio - 1 at rows 0.., and its gathered
+ *   positions g0 = seq_lens[r] - gather_lens[r] .. seq_lens[r] - 1 at rows
+ *   compressed_base...  For token t at pos (as combine_topk_swa_indices):
+ *   columns [0, W): position max(pos - W + 1, 0) + c -> row
+ *     r*ww + compressed_base + (p - g0) when g0 <= p <= pos, else -1;
+ *   columns [W, W + topk): local index l -> r*ww + l when
+ *     0 <= l < seq_lens[r] / compress_ratio, else -1;
+ *   remaining columns up to W + roundup(topk, 4): -1;  lens = entries >= 0.
+ *   The column layout is that of combine_topk_swa_indices (the pages do not
+ *   print this kernel).  Padding tokens: all -1, lens 0.
+ */
+psk_status combine_topk_swa_workspace_indices(
+    const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* gather_lens, const int32_t* token_to_req, int32_t num_reqs,
+    int64_t num_tokens, int32_t window, int32_t compress_ratio,
+    const int32_t* topk_local, int64_t topk_stride, int32_t topk,
+    int64_t workspace_width, int64_t compressed_base,
+    const uint8_t* is_valid_token, int32_t* indices, int64_t out_stride,
+    int32_t* lens, psk_stream_t stream);
+
+/*
+ * indexer_mxfp4_paged_gather -- raw (packed) MXFP4 rows over request ranges.
+ * [MDL] _deepseek_v4_gather_paged_indexer_mxfp4_cache (for the indexer's
+ * score GEMM, which reads the packed E2M1 values and E8M0 scales).
+ *
+ *   values_out   uint8 [total_rows, head_dim/2]; scales_out uint8
+ *                [total_rows, head_dim/32] (4-byte aligned rows).
+ *   cu_seq_lens  int32 [num_reqs + 1], non-decreasing, cu[0] = 0 and
+ *                cu[num_reqs] = total_rows.
+ *   Row cu[r] + i holds the record bytes of local position i of request r
+ *   through block_table[r] (no base offset), unchanged; a position without a
+ *   page gives zero bytes.
+ */
+psk_status indexer_mxfp4_paged_gather(
+    uint8_t* values_out, uint8_t* scales_out, const uint8_t* cache,
+    int64_t num_pages, int64_t page_stride, int32_t block_size, int32_t head_dim,
+    const int32_t* block_table, int64_t bt_stride, int32_t bt_width,
+    const int32_t* cu_seq_lens, int32_t num_reqs, int64_t total_rows,
+    psk_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,8 +13,10 @@ from typing import Optional, Sequence
 import numpy as np
 
 from . import (REC_FP8_DS_MLA, REC_MXFP4, combine_topk_swa_indices,
-               compute_global_topk_indices_and_lens, dequantize_and_gather_k_cache,
-               quantize_and_insert_k_cache, write_indexer_mxfp4_cache)
+               combine_topk_swa_workspace_indices, compute_global_topk_indices_and_lens,
+               dequantize_and_gather_k_cache, dequantize_and_gather_k_cache_ranges,
+               indexer_mxfp4_paged_gather, quantize_and_insert_k_cache,
+               write_indexer_mxfp4_cache)
 
 
 def run_step(w, swa_cache: Optional[np.ndarray], comp_cache: Optional[np.ndarray],
@@ -52,4 +54,34 @@ def run_step(w, swa_cache: Optional[np.ndarray], comp_cache: Optional[np.ndarray
     res["gathered_index"] = dequantize_and_gather_k_cache(
         index_cache, w.index_cache.block_size, REC_MXFP4, w.index_head_dim, 0,
         np.ascontiguousarray(rows))
+    return res
+
+
+def run_workspace_step(w, geom: dict, swa_cache, comp_cache, index_cache) -> dict:
+    """The prefill workspace step (``geom`` = the workspace geometry of the
+    batch: gather_lens, compressed_lens, compressed_base, workspace_width,
+    cu_compressed).  Caches are updated in place."""
+    res: dict = {"err": 0}
+    res["err"] += quantize_and_insert_k_cache(
+        w.k, w.insert_slots, swa_cache, w.swa_cache.block_size, w.head_dim, w.rope_dim)
+    res["err"] += write_indexer_mxfp4_cache(
+        w.index_k, w.index_insert_slots, index_cache, w.index_cache.block_size,
+        w.index_head_dim)
+    cb, ww = geom["compressed_base"], geom["workspace_width"]
+    table = w.comp_block_table if w.comp_block_table is not None else w.swa_block_table
+    comp_part = np.zeros((w.num_reqs, cb, w.head_dim), np.uint16)
+    dequantize_and_gather_k_cache_ranges(comp_part, comp_cache, w.comp_cache.block_size,
+                                         REC_FP8_DS_MLA, w.head_dim, w.rope_dim,
+                                         geom["compressed_lens"], None, table, 0)
+    ws = np.zeros((w.num_reqs, ww, w.head_dim), np.uint16)
+    dequantize_and_gather_k_cache_ranges(ws, swa_cache, w.swa_cache.block_size, REC_FP8_DS_MLA,
+                                         w.head_dim, w.rope_dim, w.seq_lens,
+                                         geom["gather_lens"], w.swa_block_table, cb)
+    res["workspace_compressed"] = comp_part
+    res["workspace_window"] = ws[:, cb:]
+    res["ws_indices"], res["ws_lens"] = combine_topk_swa_workspace_indices(
+        w.query_start_loc, w.seq_lens, geom["gather_lens"], w.token_to_req, w.window,
+        w.compress_ratio, w.topk_local, ww, cb, is_valid_token=w.is_valid_token)
+    res["raw_values"], res["raw_scales"] = indexer_mxfp4_paged_gather(
+        index_cache, w.index_cache.block_size, w.index_head_dim, table, geom["cu_compressed"])
     return res

@@ -46,6 +46,14 @@ SIGNATURES = {
     "dequantize_and_gather_k_cache": (
         _I32, [_P, _I64, _I64, _P, _I64, _I64, _I32, _I32, _I32, _I32, _I32, _P, _I64, _I64,
                _I32, _P]),
+    "dequantize_and_gather_k_cache_ranges": (
+        _I32, [_P, _I64, _I64, _I64, _P, _I64, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P, _P,
+               _I64, _I32, _P, _I32, _I64, _P]),
+    "combine_topk_swa_workspace_indices": (
+        _I32, [_P, _P, _P, _P, _I32, _I64, _I32, _I32, _P, _I64, _I32, _I64, _I64, _P, _P, _I64,
+               _P, _P]),
+    "indexer_mxfp4_paged_gather": (
+        _I32, [_P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _I32, _P, _I32, _I64, _P]),
 }
 
 _lib = None

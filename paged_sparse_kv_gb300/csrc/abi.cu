@@ -293,6 +293,103 @@ psk_status dequantize_and_gather_k_cache(void* out, int64_t out_stride_t, int64_
                        "dequantize_and_gather_k_cache launch");
 }
 
+psk_status dequantize_and_gather_k_cache_ranges(
+    void* out, int64_t out_stride_r, int64_t out_stride_i, int64_t out_rows, const uint8_t* cache,
+    int64_t num_pages, int64_t page_stride, int32_t block_size, psk_record record,
+    int32_t head_dim, int32_t rope_dim, int32_t is_ue8m0, const int32_t* seq_lens,
+    const int32_t* gather_lens, const int32_t* block_table, int64_t bt_stride, int32_t bt_width,
+    const int32_t* base_offsets, int32_t num_reqs, int64_t offset, psk_stream_t stream) {
+    if (record != PSK_REC_FP8_DS_MLA)
+        return fail(PSK_ERR_UNSUPPORTED, "the range form gathers fp8_ds_mla records only");
+    CHECK(is_ue8m0 == 0 || is_ue8m0 == 1, "is_ue8m0 must be 0 or 1");
+    CHECK(fp8_head_dim_ok(head_dim), "head_dim must be one of 64, 128, 256, 512, 1024 (got %d)",
+          head_dim);
+    CHECK(rope_dim >= 0 && rope_dim < head_dim && rope_dim % 64 == 0,
+          "rope_dim must be a multiple of 64 in [0, head_dim) (got %d)", rope_dim);
+    psk_status st = check_cache(cache, num_pages, page_stride, block_size,
+                                fp8_record_bytes(head_dim, rope_dim, is_ue8m0));
+    if (st != PSK_OK) return st;
+    CHECK(num_reqs >= 0, "num_reqs must be >= 0");
+    CHECK(offset >= 0 && out_rows >= offset, "need 0 <= offset <= out_rows");
+    CHECK(out_rows - offset <= INT32_MAX, "out_rows - offset must fit in int32");
+    CHECK(bt_width >= 0 && bt_stride >= bt_width, "need 0 <= bt_width <= bt_stride");
+    if (num_reqs == 0 || out_rows == offset) return ok();
+    CHECK(out && seq_lens, "out and seq_lens must be non-null");
+    CHECK(bt_width == 0 || block_table, "block_table must be non-null");
+    CHECK(aligned(out, 16), "out must be 16-byte aligned");
+    CHECK(out_stride_r >= 0 && out_stride_i >= 0 && out_stride_r % 8 == 0 && out_stride_i % 8 == 0,
+          "output strides must be non-negative multiples of 8 elements");
+    CHECK(aligned(seq_lens, 4) && aligned(gather_lens, 4) && aligned(block_table, 4) &&
+              aligned(base_offsets, 4),
+          "int32 arrays must be 4-byte aligned");
+    psk::RangeParams p{static_cast<uint16_t*>(out), out_stride_r, out_stride_i, out_rows, offset,
+                       cache, num_pages, page_stride, block_size, head_dim, rope_dim, is_ue8m0,
+                       seq_lens, gather_lens, block_table, bt_stride, bt_width, base_offsets,
+                       num_reqs};
+    return cuda_status(psk::launch_gather_ranges(p, reinterpret_cast<cudaStream_t>(stream)),
+                       "dequantize_and_gather_k_cache_ranges launch");
+}
+
+psk_status combine_topk_swa_workspace_indices(
+    const int32_t* query_start_loc, const int32_t* seq_lens, const int32_t* gather_lens,
+    const int32_t* token_to_req, int32_t num_reqs, int64_t num_tokens, int32_t window,
+    int32_t compress_ratio, const int32_t* topk_local, int64_t topk_stride, int32_t topk,
+    int64_t workspace_width, int64_t compressed_base, const uint8_t* is_valid_token,
+    int32_t* indices, int64_t out_stride, int32_t* lens, psk_stream_t stream) {
+    CHECK(num_tokens >= 0, "num_tokens must be >= 0");
+    CHECK(window >= 0 && topk >= 0, "window and topk must be >= 0");
+    CHECK(compress_ratio >= 1, "compress_ratio must be >= 1");
+    CHECK(workspace_width >= 0 && compressed_base >= 0,
+          "workspace_width and compressed_base must be >= 0");
+    const int64_t cols = (int64_t)window + ((int64_t)topk + 3) / 4 * 4;
+    CHECK(cols <= INT32_MAX, "window + padded topk overflows int32");
+    CHECK(topk_stride >= topk, "topk_stride must be >= topk");
+    CHECK(out_stride >= cols, "out_stride must be >= window + roundup(topk, 4)");
+    if (num_tokens == 0) return ok();
+    CHECK(num_reqs >= 1, "num_reqs must be >= 1");
+    CHECK(query_start_loc && seq_lens && gather_lens && token_to_req && indices && lens,
+          "query_start_loc, seq_lens, gather_lens, token_to_req, indices and lens must be non-null");
+    CHECK(topk == 0 || topk_local, "topk_local must be non-null");
+    CHECK(aligned(query_start_loc, 4) && aligned(seq_lens, 4) && aligned(gather_lens, 4) &&
+              aligned(token_to_req, 4) && aligned(topk_local, 4) && aligned(indices, 4) &&
+              aligned(lens, 4),
+          "int32 arrays must be 4-byte aligned");
+    psk::WorkspaceIndexParams p{query_start_loc, seq_lens, gather_lens, token_to_req, num_reqs,
+                                num_tokens, window, compress_ratio, topk_local, topk_stride,
+                                topk, workspace_width, compressed_base, is_valid_token, indices,
+                                out_stride, lens};
+    return cuda_status(psk::launch_workspace_indices(p, reinterpret_cast<cudaStream_t>(stream)),
+                       "combine_topk_swa_workspace_indices launch");
+}
+
+psk_status indexer_mxfp4_paged_gather(uint8_t* values_out, uint8_t* scales_out,
+                                      const uint8_t* cache, int64_t num_pages,
+                                      int64_t page_stride, int32_t block_size, int32_t head_dim,
+                                      const int32_t* block_table, int64_t bt_stride,
+                                      int32_t bt_width, const int32_t* cu_seq_lens,
+                                      int32_t num_reqs, int64_t total_rows,
+                                      psk_stream_t stream) {
+    CHECK(mxfp4_head_dim_ok(head_dim),
+          "head_dim must be one of 32, 64, 128, 256, 512, 1024 (got %d)", head_dim);
+    psk_status st = check_cache(cache, num_pages, page_stride, block_size,
+                                head_dim / 2 + head_dim / 32);
+    if (st != PSK_OK) return st;
+    CHECK(total_rows >= 0 && num_reqs >= 0, "total_rows and num_reqs must be >= 0");
+    CHECK(bt_width >= 0 && bt_stride >= bt_width, "need 0 <= bt_width <= bt_stride");
+    if (total_rows == 0) return ok();
+    CHECK(num_reqs >= 1, "num_reqs must be >= 1 when total_rows > 0");
+    CHECK(values_out && scales_out && cu_seq_lens, "outputs and cu_seq_lens must be non-null");
+    CHECK(bt_width == 0 || block_table, "block_table must be non-null");
+    CHECK(aligned(values_out, 4) && aligned(scales_out, 4) && aligned(cu_seq_lens, 4) &&
+              aligned(block_table, 4),
+          "values_out, scales_out and int32 arrays must be 4-byte aligned");
+    psk::RawGatherParams p{values_out, scales_out, cache, num_pages, page_stride, block_size,
+                           head_dim, block_table, bt_stride, bt_width, cu_seq_lens, num_reqs,
+                           total_rows};
+    return cuda_status(psk::launch_mxfp4_raw_gather(p, reinterpret_cast<cudaStream_t>(stream)),
+                       "indexer_mxfp4_paged_gather launch");
+}
+
 }  // extern "C"
 
 namespace psk {

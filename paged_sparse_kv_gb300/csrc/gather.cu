@@ -60,9 +60,30 @@ __device__ __forceinline__ void item_to_tj(int64_t item, int32_t cols, bool smal
     }
 }
 
-template <int D, bool UE8M0>
+// Where each item's slot comes from: the index matrix (INDEX form) or a
+// request's position range through its block-table row (RANGE form).
+struct ItemSource {
+    GatherParams g;      // index form (and cache geometry for both forms)
+    RangeParams r;       // range form
+};
+
+// Slot of position p through one table row (the block-table rule), or -1.
+__device__ __forceinline__ int32_t table_slot(const int32_t* row, int32_t width, int64_t base,
+                                              int32_t bs, int64_t p) {
+    if (p < 0) return -1;
+    const int64_t q = p / bs;
+    const int64_t lp = q - base;
+    if (lp < 0 || lp >= width) return -1;
+    const int32_t page = __ldg(row + lp);
+    if (page < 0) return -1;
+    const int64_t s = (int64_t)page * bs + (p - q * bs);
+    return s > 0x7FFFFFFFll ? -1 : (int32_t)s;
+}
+
+template <int D, bool UE8M0, bool RANGE>
 __global__ void __launch_bounds__(kTmaThreads)
-gather_fp8_tma_kernel(GatherParams p, int slot_bytes) {
+gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
+    const GatherParams& p = src.g;
     constexpr int CHUNKS = D / 8;
     constexpr int LANES = CHUNKS < kWarp ? CHUNKS : kWarp;
     constexpr int CPL = CHUNKS / LANES;
@@ -78,10 +99,13 @@ gather_fp8_tma_kernel(GatherParams p, int slot_bytes) {
     int32_t* slots = reinterpret_cast<int32_t*>(outoff + kStages * kRowsPerTile);
 
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    const int64_t items = p.rows * (int64_t)p.cols;
+    // INDEX form: items = rows x cols of the index matrix.  RANGE form:
+    // items = num_reqs x span, span = out_rows - offset rows per request.
+    const int64_t span = RANGE ? src.r.out_rows - src.r.offset : (int64_t)p.cols;
+    const int64_t items = RANGE ? (int64_t)src.r.num_reqs * span : p.rows * (int64_t)p.cols;
     const int64_t tiles = (items + kRowsPerTile - 1) / kRowsPerTile;
     const int64_t capacity = p.num_pages * (int64_t)p.block_size;
-    const bool small = items <= 0xFFFFFFFFll;
+    const bool small = items <= 0xFFFFFFFFll && span <= 0x7FFFFFFFll;
     const int nope = D - p.rope_dim;
     const int ts = nope + 2 * p.rope_dim;
     const int bs = p.block_size;
@@ -117,10 +141,28 @@ gather_fp8_tma_kernel(GatherParams p, int slot_bytes) {
                 if (tile < tiles && item < items) {
                     int64_t t;
                     int32_t j;
-                    item_to_tj(item, p.cols, small, t, j);
-                    const int32_t raw = __ldg(p.idx + t * p.idx_stride + j);
-                    slot[q] = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
-                    oof[q] = t * p.out_stride_t + (int64_t)j * p.out_stride_j;
+                    item_to_tj(item, (int32_t)span, small, t, j);
+                    if (RANGE) {
+                        // t = request, j = row within the request's span
+                        const int64_t seq = __ldg(src.r.seq_lens + t);
+                        const int64_t g = src.r.gather_lens ? __ldg(src.r.gather_lens + t) : seq;
+                        if (j < g) {
+                            const int64_t base = src.r.base_offsets ? __ldg(src.r.base_offsets + t) : 0;
+                            const int32_t raw = table_slot(src.r.block_table + t * src.r.bt_stride,
+                                                           src.r.bt_width, base, p.block_size,
+                                                           seq - g + j);
+                            slot[q] = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
+                            oof[q] = t * src.r.out_stride_r + (src.r.offset + j) * src.r.out_stride_i;
+                        } else {
+                            slot[q] = -2;  // outside the gathered range: not written
+                        }
+                    } else {
+                        const int32_t raw = __ldg(p.idx + t * p.idx_stride + j);
+                        slot[q] = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
+                        oof[q] = t * p.out_stride_t + (int64_t)j * p.out_stride_j;
+                    }
+                } else {
+                    slot[q] = -2;
                 }
             }
 #pragma unroll
@@ -133,7 +175,7 @@ gather_fp8_tma_kernel(GatherParams p, int slot_bytes) {
                     break;
                 }
                 const bool mine = half == (k & 1);
-                const int32_t sl = mine ? slot[k / 2] : -1;
+                const int32_t sl = mine ? slot[k / 2] : -2;
                 uint32_t bytes = 0;
                 const uint8_t* src_data = nullptr;
                 const uint8_t* src_scl = nullptr;
@@ -153,7 +195,7 @@ gather_fp8_tma_kernel(GatherParams p, int slot_bytes) {
                 }
                 const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, bytes);
                 if (mine) {
-                    slots[s * kRowsPerTile + r] = soff;  // -1: zero row
+                    slots[s * kRowsPerTile + r] = sl == -2 ? -2 : soff;  // -1 zero row, -2 skip
                     outoff[s * kRowsPerTile + r] = oof[k / 2];
                 }
                 __syncwarp();
@@ -192,6 +234,7 @@ gather_fp8_tma_kernel(GatherParams p, int slot_bytes) {
             const int64_t item = tile * kRowsPerTile + r;
             if (item >= items) break;
             const int32_t soff = slots[s * kRowsPerTile + r];  // scale offset, -1 = zero row
+            if (soff == -2) continue;                           // not written
             uint16_t* orow = p.out + outoff[s * kRowsPerTile + r];
             const uint8_t* srow = ring + (size_t)(s * kRowsPerTile + r) * slot_bytes;
 #pragma unroll
@@ -329,16 +372,16 @@ int64_t persistent_blocks(K kernel, int64_t groups_needed, int lanes) {
     return need < full ? need : full;
 }
 
-template <int D, bool UE8M0>
-cudaError_t gather_fp8_dispatch(const GatherParams& p, cudaStream_t stream) {
-    const int ts = D - p.rope_dim + 2 * p.rope_dim;
+template <int D, bool UE8M0, bool RANGE>
+cudaError_t gather_fp8_dispatch(const ItemSource& src, int64_t items, cudaStream_t stream) {
+    const int ts = D - src.g.rope_dim + 2 * src.g.rope_dim;
     constexpr int SDIM = UE8M0 ? D / 64 : 4 * (D / 64);
     // data record + the 16-byte chunks covering the scales, rounded to 16
     const int slot_bytes = (ts + ((SDIM + 15) / 16 + 1) * 16 + 15) / 16 * 16;
     const size_t smem = (size_t)kStages * kRowsPerTile * slot_bytes +
                         2 * kStages * sizeof(uint64_t) +
                         kStages * kRowsPerTile * (sizeof(int64_t) + sizeof(int32_t));
-    auto kern = gather_fp8_tma_kernel<D, UE8M0>;
+    auto kern = gather_fp8_tma_kernel<D, UE8M0, RANGE>;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -350,11 +393,24 @@ cudaError_t gather_fp8_dispatch(const GatherParams& p, cudaStream_t stream) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTmaThreads, smem) !=
             cudaSuccess || per_sm < 1)
         per_sm = 1;
-    const int64_t items = p.rows * (int64_t)p.cols;
     const int64_t tiles = (items + kRowsPerTile - 1) / kRowsPerTile;
     int64_t blocks = (int64_t)sm_count() * per_sm;
     if (blocks > tiles) blocks = tiles;
-    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kTmaThreads), smem, stream, p, slot_bytes);
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kTmaThreads), smem, stream, src,
+                      slot_bytes);
+}
+
+template <bool RANGE>
+cudaError_t fp8_by_dim(const ItemSource& src, int64_t items, cudaStream_t stream) {
+    const bool ue = src.g.is_ue8m0 != 0;
+    switch (src.g.head_dim) {
+        case 64: return ue ? gather_fp8_dispatch<64, true, RANGE>(src, items, stream) : gather_fp8_dispatch<64, false, RANGE>(src, items, stream);
+        case 128: return ue ? gather_fp8_dispatch<128, true, RANGE>(src, items, stream) : gather_fp8_dispatch<128, false, RANGE>(src, items, stream);
+        case 256: return ue ? gather_fp8_dispatch<256, true, RANGE>(src, items, stream) : gather_fp8_dispatch<256, false, RANGE>(src, items, stream);
+        case 512: return ue ? gather_fp8_dispatch<512, true, RANGE>(src, items, stream) : gather_fp8_dispatch<512, false, RANGE>(src, items, stream);
+        case 1024: return ue ? gather_fp8_dispatch<1024, true, RANGE>(src, items, stream) : gather_fp8_dispatch<1024, false, RANGE>(src, items, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 template <int D>
@@ -377,15 +433,9 @@ cudaError_t read_wait_timeouts(uint32_t* count) {
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
     if (p.record == 0) {
-        const bool ue = p.is_ue8m0 != 0;
-        switch (p.head_dim) {
-            case 64: return ue ? gather_fp8_dispatch<64, true>(p, stream) : gather_fp8_dispatch<64, false>(p, stream);
-            case 128: return ue ? gather_fp8_dispatch<128, true>(p, stream) : gather_fp8_dispatch<128, false>(p, stream);
-            case 256: return ue ? gather_fp8_dispatch<256, true>(p, stream) : gather_fp8_dispatch<256, false>(p, stream);
-            case 512: return ue ? gather_fp8_dispatch<512, true>(p, stream) : gather_fp8_dispatch<512, false>(p, stream);
-            case 1024: return ue ? gather_fp8_dispatch<1024, true>(p, stream) : gather_fp8_dispatch<1024, false>(p, stream);
-            default: return cudaErrorInvalidValue;
-        }
+        ItemSource src{};
+        src.g = p;
+        return fp8_by_dim<false>(src, p.rows * (int64_t)p.cols, stream);
     }
     switch (p.head_dim) {
         case 32: return gather_mxfp4_dispatch<32>(p, stream);
@@ -394,6 +444,109 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
         case 256: return gather_mxfp4_dispatch<256>(p, stream);
         case 512: return gather_mxfp4_dispatch<512>(p, stream);
         case 1024: return gather_mxfp4_dispatch<1024>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gather_ranges(const RangeParams& r, cudaStream_t stream) {
+    ItemSource src{};
+    src.r = r;
+    src.g.out = r.out;
+    src.g.cache = r.cache;
+    src.g.num_pages = r.num_pages;
+    src.g.page_stride = r.page_stride;
+    src.g.block_size = r.block_size;
+    src.g.record = 0;
+    src.g.head_dim = r.head_dim;
+    src.g.rope_dim = r.rope_dim;
+    src.g.is_ue8m0 = r.is_ue8m0;
+    return fp8_by_dim<true>(src, (int64_t)r.num_reqs * (r.out_rows - r.offset), stream);
+}
+
+// ---- raw MXFP4 paged gather ----------------------------------------------------------
+//
+// TokenSpeed models/deepseek_v4.py, _deepseek_v4_gather_paged_indexer_mxfp4_cache
+// (indexer_mxfp4_paged_gather): packed records copied unchanged, request r's
+// local positions 0.. to output rows cu_seq_lens[r]..  A group of D/8 lanes
+// (at most 32) owns one row: each lane copies 4 value bytes, lane 0 the scale
+// bytes.  A row finds its request by binary search over cu_seq_lens.
+template <int D>
+__global__ void __launch_bounds__(kThreads) mxfp4_raw_gather_kernel(RawGatherParams p) {
+    constexpr int CHUNKS = D / 8;  // 4 value bytes per chunk
+    constexpr int LANES = CHUNKS < kWarp ? CHUNKS : kWarp;
+    constexpr int CPL = CHUNKS / LANES;
+    constexpr int VB = D / 2, SB = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int gl = lane % LANES;
+    const int64_t gid = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / LANES;
+    const int64_t ngroups = (int64_t)gridDim.x * kThreads / LANES;
+    const int64_t capacity = p.num_pages * (int64_t)p.block_size;
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int64_t row = gid; row < p.total_rows; row += ngroups) {
+        // last request r with cu_seq_lens[r] <= row
+        int lo = 0, hi = p.num_reqs;  // invariant: cu[lo] <= row (when valid)
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) / 2;
+            if ((int64_t)__ldg(p.cu_seq_lens + mid) <= row) lo = mid; else hi = mid;
+        }
+        const int64_t start = __ldg(p.cu_seq_lens + lo), end = __ldg(p.cu_seq_lens + lo + 1);
+        int32_t s = -1;
+        if (row >= start && row < end) {
+            const int64_t i = row - start;
+            const int64_t lp = i / p.block_size;
+            if (lp < p.bt_width) {
+                const int32_t page = __ldg(p.block_table + (int64_t)lo * p.bt_stride + lp);
+                if (page >= 0) {
+                    const int64_t sl = (int64_t)page * p.block_size + (i - lp * p.block_size);
+                    if (sl < capacity) s = (int32_t)sl;
+                }
+            }
+        }
+        uint8_t* vo = p.values_out + row * VB;
+        uint8_t* so = p.scales_out + row * SB;
+        if (s < 0) {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) *reinterpret_cast<uint32_t*>(vo + 4 * (gl + c * LANES)) = 0u;
+            if (gl == 0) for (int b = 0; b < SB; ++b) so[b] = 0;
+            continue;
+        }
+        const int32_t page = s / p.block_size, off = s - page * p.block_size;
+        const uint8_t* base = p.cache + (int64_t)page * p.page_stride;
+        const uint8_t* vals = base + (int64_t)off * VB;
+        const uint8_t* scl = base + (int64_t)p.block_size * VB + (int64_t)off * SB;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            const int k = gl + c * LANES;
+            *reinterpret_cast<uint32_t*>(vo + 4 * k) = ld_nc_u32(vals + 4 * k);
+        }
+        if (gl == 0) {
+            if (SB % 4 == 0) {
+                for (int b = 0; b < SB; b += 4)
+                    *reinterpret_cast<uint32_t*>(so + b) = ld_nc_u32(scl + b);
+            } else {
+                for (int b = 0; b < SB; ++b) so[b] = (uint8_t)ld_nc_u8(scl + b);
+            }
+        }
+    }
+}
+
+template <int D>
+cudaError_t raw_dispatch(const RawGatherParams& p, cudaStream_t stream) {
+    constexpr int LANES = (D / 8) < kWarp ? (D / 8) : kWarp;
+    auto kern = mxfp4_raw_gather_kernel<D>;
+    const int64_t blocks = persistent_blocks(kern, p.total_rows, LANES);
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p);
+}
+
+cudaError_t launch_mxfp4_raw_gather(const RawGatherParams& p, cudaStream_t stream) {
+    switch (p.head_dim) {
+        case 32: return raw_dispatch<32>(p, stream);
+        case 64: return raw_dispatch<64>(p, stream);
+        case 128: return raw_dispatch<128>(p, stream);
+        case 256: return raw_dispatch<256>(p, stream);
+        case 512: return raw_dispatch<512>(p, stream);
+        case 1024: return raw_dispatch<1024>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

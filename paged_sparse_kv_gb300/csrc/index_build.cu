@@ -278,7 +278,124 @@ __global__ void __launch_bounds__(kThreads) index_build_kernel(IndexParams p) {
     }
 }
 
+// ---- workspace-relative form ------------------------------------------------------
+//
+// TokenSpeed's combine_topk_swa_indices as the prefill workspace path calls it
+// (backends/deepseek_v4.py, _prefill_workspace): request r's rows start at
+// r * workspace_width, compressed entries at rows 0.., the gathered window
+// positions g0 = seq - gather_len .. seq - 1 at rows compressed_base...  No
+// table look-ups: every column is arithmetic on the token's metadata.
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceIndexParams p,
+                                                                   int tokens_per_cta, int wpt) {
+    __shared__ int s_cnt[kWarps];
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int64_t t0 = (int64_t)blockIdx.x * tokens_per_cta;
+    int64_t t1 = t0 + tokens_per_cta;
+    if (t1 > p.num_tokens) t1 = p.num_tokens;
+    const int tpp = kWarps / wpt, tslot = warp / wpt, slice = warp % wpt;
+    const int first = slice * kWarp + lane, stride = wpt * kWarp;
+    const int W = p.window;
+    const int P = (p.topk + 3) / 4 * 4;
+    const int cols = W + P;
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int64_t tb = t0; tb < t1; tb += tpp) {
+        const int64_t t = tb + tslot;
+        int cnt = 0;
+        if (t < t1) {
+            int32_t* out = p.out + t * p.out_stride;
+            const int32_t r = __ldg(p.t2r + t);
+            const bool ok = (p.valid == nullptr || __ldg(p.valid + t) != 0) && r >= 0 &&
+                            r < p.num_reqs;
+            int64_t pos = 0, lo = 0, g0 = 0, lc = 0, rbase = 0;
+            if (ok) {
+                const int64_t qs = __ldg(p.qsl + r), qe = __ldg(p.qsl + r + 1);
+                const int64_t seq = __ldg(p.seq_lens + r);
+                pos = seq - (qe - qs) + (t - qs);
+                g0 = seq - __ldg(p.gather_lens + r);
+                lc = seq / p.compress_ratio;
+                rbase = (int64_t)r * p.workspace_width;
+                lo = pos - W + 1;
+                if (lo < 0) lo = 0;
+            }
+            const int32_t* tk = p.topk_local + t * p.topk_stride;
+            auto col = [&](int c, int l_in) -> int {
+                if (!ok) return -1;
+                int64_t v = -1;
+                if (c < W) {
+                    const int64_t ps = lo + c;
+                    if (ps <= pos && ps >= g0) v = rbase + p.compressed_base + (ps - g0);
+                } else if (c - W < p.topk) {
+                    if (l_in >= 0 && l_in < lc) v = rbase + l_in;
+                }
+                return v > 0x7FFFFFFFll ? -1 : (int)v;
+            };
+            if (VEC) {
+                const int nq = cols / 4;
+                for (int q = first; q < nq; q += stride) {
+                    const int c0 = 4 * q;
+                    int4 l = make_int4(-1, -1, -1, -1);
+                    if (ok && c0 >= W) {
+                        const int j0 = c0 - W;
+                        if (j0 + 3 < p.topk) {
+                            l = __ldg(reinterpret_cast<const int4*>(tk + j0));
+                        } else {
+                            l.x = j0 < p.topk ? __ldg(tk + j0) : -1;
+                            l.y = j0 + 1 < p.topk ? __ldg(tk + j0 + 1) : -1;
+                            l.z = j0 + 2 < p.topk ? __ldg(tk + j0 + 2) : -1;
+                        }
+                    }
+                    const int4 v = make_int4(col(c0, l.x), col(c0 + 1, l.y), col(c0 + 2, l.z),
+                                             col(c0 + 3, l.w));
+                    cnt += (v.x >= 0) + (v.y >= 0) + (v.z >= 0) + (v.w >= 0);
+                    *reinterpret_cast<int4*>(out + c0) = v;
+                }
+            } else {
+                for (int c = first; c < cols; c += stride) {
+                    const int l = (ok && c >= W && c - W < p.topk) ? __ldg(tk + (c - W)) : -1;
+                    const int v = col(c, l);
+                    cnt += v >= 0;
+                    out[c] = v;
+                }
+            }
+        }
+        cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+        if (wpt == 1) {
+            if (lane == 0 && t < t1) p.lens[t] = cnt;
+        } else {
+            if (lane == 0) s_cnt[warp] = cnt;
+            __syncthreads();
+            if (slice == 0 && lane == 0 && t < t1) {
+                int sum = 0;
+                for (int i = 0; i < wpt; ++i) sum += s_cnt[warp + i];
+                p.lens[t] = sum;
+            }
+            __syncthreads();
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_workspace_indices(const WorkspaceIndexParams& p, cudaStream_t stream) {
+    const int sms = sm_count();
+    const int64_t T = p.num_tokens;
+    int wpt = 1;
+    while (wpt < kWarps && T * wpt < (int64_t)sms * 16) wpt *= 2;
+    const int tpp = kWarps / wpt;
+    int64_t passes = T / ((int64_t)tpp * 2 * sms);
+    if (passes < 1) passes = 1;
+    if (passes > 8) passes = 8;
+    const int tokens_per_cta = (int)(tpp * passes);
+    const int64_t blocks = (T + tokens_per_cta - 1) / tokens_per_cta;
+    const bool vec = ((reinterpret_cast<uintptr_t>(p.out) & 15) == 0) && (p.out_stride % 4 == 0) &&
+                     ((reinterpret_cast<uintptr_t>(p.topk_local) & 15) == 0) &&
+                     (p.topk_stride % 4 == 0) && (p.window % 4 == 0);
+    auto kern = vec ? workspace_index_kernel<true> : workspace_index_kernel<false>;
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p, tokens_per_cta,
+                      wpt);
+}
 
 cudaError_t launch_index_build(IndexParams p, bool has_swa, cudaStream_t stream) {
     const int sms = sm_count();

@@ -107,6 +107,73 @@ struct GatherParams {
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
 
+// Range form: per request r, rows i < out_rows - offset; g = gather_lens[r]
+// (or seq_lens[r]); row i < g is position seq_lens[r] - g + i -> out row
+// offset + i; rows i >= g are not written.
+struct RangeParams {
+    uint16_t* out;
+    int64_t out_stride_r;
+    int64_t out_stride_i;
+    int64_t out_rows;
+    int64_t offset;
+    const uint8_t* cache;
+    int64_t num_pages;
+    int64_t page_stride;
+    int32_t block_size;
+    int32_t head_dim;
+    int32_t rope_dim;
+    int32_t is_ue8m0;
+    const int32_t* seq_lens;
+    const int32_t* gather_lens;
+    const int32_t* block_table;
+    int64_t bt_stride;
+    int32_t bt_width;
+    const int32_t* base_offsets;
+    int32_t num_reqs;
+};
+
+cudaError_t launch_gather_ranges(const RangeParams& p, cudaStream_t stream);
+
+struct WorkspaceIndexParams {
+    const int32_t* qsl;
+    const int32_t* seq_lens;
+    const int32_t* gather_lens;
+    const int32_t* t2r;
+    int32_t num_reqs;
+    int64_t num_tokens;
+    int32_t window;
+    int32_t compress_ratio;
+    const int32_t* topk_local;
+    int64_t topk_stride;
+    int32_t topk;
+    int64_t workspace_width;
+    int64_t compressed_base;
+    const uint8_t* valid;
+    int32_t* out;
+    int64_t out_stride;
+    int32_t* lens;
+};
+
+cudaError_t launch_workspace_indices(const WorkspaceIndexParams& p, cudaStream_t stream);
+
+struct RawGatherParams {
+    uint8_t* values_out;
+    uint8_t* scales_out;
+    const uint8_t* cache;
+    int64_t num_pages;
+    int64_t page_stride;
+    int32_t block_size;
+    int32_t head_dim;
+    const int32_t* block_table;
+    int64_t bt_stride;
+    int32_t bt_width;
+    const int32_t* cu_seq_lens;
+    int32_t num_reqs;
+    int64_t total_rows;
+};
+
+cudaError_t launch_mxfp4_raw_gather(const RawGatherParams& p, cudaStream_t stream);
+
 // Number of bounded in-kernel waits that expired on the current device.
 cudaError_t read_wait_timeouts(uint32_t* count);
 

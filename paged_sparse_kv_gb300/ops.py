@@ -175,3 +175,76 @@ def dequantize_and_gather_k_cache(out: torch.Tensor, cache: torch.Tensor,
               rope_dim if record == PSK_REC_FP8_DS_MLA else 0, int(bool(is_ue8m0)),
               _ptr(indices), _rows(indices, "indices"), T, C, _stream(out.device))
     return out
+
+
+# ---- prefill workspace path ------------------------------------------------------------
+
+def dequantize_and_gather_k_cache_ranges(out: torch.Tensor, cache: torch.Tensor,
+                                         seq_lens: torch.Tensor,
+                                         gather_lens: Optional[torch.Tensor],
+                                         block_table: torch.Tensor, block_size: int,
+                                         offset: int, *, rope_dim: int = 64,
+                                         is_ue8m0: bool = True,
+                                         base_offsets: Optional[torch.Tensor] = None
+                                         ) -> torch.Tensor:
+    """Range-form gather into ``out`` [R, rows, D] bf16 (a workspace); see psk.h."""
+    _need_cuda(out, cache, seq_lens, gather_lens, block_table, base_offsets)
+    _need(out, torch.bfloat16, "out")
+    if out.dim() != 3 or out.stride(2) != 1:
+        raise ValueError("out must be [R, rows, D] with unit inner stride")
+    for t, n in ((seq_lens, "seq_lens"), (block_table, "block_table")):
+        _need(t, torch.int32, n)
+    num_pages, page_stride = _pages(cache)
+    _abi.call("dequantize_and_gather_k_cache_ranges", _ptr(out), out.stride(0), out.stride(1),
+              out.shape[1], _ptr(cache), num_pages, page_stride, block_size,
+              PSK_REC_FP8_DS_MLA, out.shape[2], rope_dim, int(bool(is_ue8m0)), _ptr(seq_lens),
+              _ptr(gather_lens), _ptr(block_table), _rows(block_table, "block_table"),
+              block_table.shape[1], _ptr(base_offsets), seq_lens.shape[0], offset,
+              _stream(out.device))
+    return out
+
+
+def combine_topk_swa_workspace_indices(topk_indices: torch.Tensor,
+                                       query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
+                                       gather_lens: torch.Tensor, token_to_req: torch.Tensor,
+                                       window_size: int, compress_ratio: int,
+                                       workspace_width: int, compressed_base: int, *,
+                                       is_valid_token: Optional[torch.Tensor] = None,
+                                       out: Optional[torch.Tensor] = None,
+                                       lens: Optional[torch.Tensor] = None):
+    """Workspace-relative index build; returns (indices [T, W + roundup4(K)], lens [T])."""
+    _need_cuda(topk_indices, query_start_loc, seq_lens, gather_lens, token_to_req,
+               is_valid_token)
+    dev = topk_indices.device
+    T, K = topk_indices.shape
+    width = window_size + (K + 3) // 4 * 4
+    if out is None:
+        out = torch.empty((T, width), dtype=torch.int32, device=dev)
+    if lens is None:
+        lens = torch.empty((T,), dtype=torch.int32, device=dev)
+    valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
+    _abi.call("combine_topk_swa_workspace_indices", _ptr(query_start_loc), _ptr(seq_lens),
+              _ptr(gather_lens), _ptr(token_to_req), seq_lens.shape[0], T, window_size,
+              compress_ratio, _ptr(topk_indices), _rows(topk_indices, "topk_indices"), K,
+              workspace_width, compressed_base, _ptr(valid), _ptr(out), _rows(out, "out"),
+              _ptr(lens), _stream(dev))
+    return out, lens
+
+
+def indexer_mxfp4_paged_gather(cache: torch.Tensor, block_table: torch.Tensor,
+                               cu_seq_lens: torch.Tensor, block_size: int, head_dim: int,
+                               total_rows: int, values_out: Optional[torch.Tensor] = None,
+                               scales_out: Optional[torch.Tensor] = None):
+    """Raw MXFP4 rows over request ranges; returns (values [N, D/2], scales [N, D/32]) uint8."""
+    _need_cuda(cache, block_table, cu_seq_lens)
+    dev = cache.device
+    if values_out is None:
+        values_out = torch.empty((total_rows, head_dim // 2), dtype=torch.uint8, device=dev)
+    if scales_out is None:
+        scales_out = torch.empty((total_rows, head_dim // 32), dtype=torch.uint8, device=dev)
+    num_pages, page_stride = _pages(cache)
+    _abi.call("indexer_mxfp4_paged_gather", _ptr(values_out), _ptr(scales_out), _ptr(cache),
+              num_pages, page_stride, block_size, head_dim, _ptr(block_table),
+              _rows(block_table, "block_table"), block_table.shape[1], _ptr(cu_seq_lens),
+              cu_seq_lens.shape[0] - 1, total_rows, _stream(dev))
+    return values_out, scales_out

@@ -26,6 +26,18 @@ order):
 Decode-sized kernels fill only part of the GPU, so overlapping the chains
 shortens the step to its critical path.  Capturing ``step(concurrent=True)``
 in a CUDA graph keeps the fork/join structure.
+
+``path="workspace"`` is the prefill path of TokenSpeed's backend
+(``_prefill_workspace``): the compressed rows of every request (range form,
+offset 0) and its window rows (offset ``compressed_base``) are gathered into a
+per-request bf16 workspace, the index build emits workspace-relative rows,
+and the indexer's packed MXFP4 keys of every compressed entry are gathered
+raw:
+
+  stream M:  dequantize_and_gather_k_cache_ranges[compressed] ->
+             combine_topk_swa_workspace_indices
+  stream A:  quantize_and_insert_k_cache -> dequantize_and_gather_k_cache_ranges[swa]
+  stream B:  write_indexer_mxfp4_cache -> indexer_mxfp4_paged_gather
 """
 from __future__ import annotations
 
@@ -99,6 +111,58 @@ class Pipeline:
         self.global_lens = torch.empty((T,), dtype=torch.int32, device=dev)
         self.gathered_index = torch.empty((T, K, w.index_head_dim), dtype=torch.bfloat16,
                                           device=dev)
+        self.ws = None
+
+    def alloc_workspace(self) -> None:
+        """Workspace geometry and buffers of the prefill workspace path, from
+        the batch metadata on the host (as the backend sizes them)."""
+        w, dev = self.w, self.dev
+        g = workspace_geometry(w)
+        self.ws_glen = _dev_i32(g["gather_lens"], dev)
+        self.ws_lc = _dev_i32(g["compressed_lens"], dev)
+        self.ws_cu = _dev_i32(g["cu_compressed"], dev)
+        self.ws_cb, self.ws_width = g["compressed_base"], g["workspace_width"]
+        self.ws_rows_raw = int(g["cu_compressed"][-1])
+        self.ws = torch.empty((w.num_reqs, self.ws_width, w.head_dim), dtype=torch.bfloat16,
+                              device=dev)
+        self.ws_indices = torch.empty((w.num_tokens, self.cols), dtype=torch.int32, device=dev)
+        self.ws_lens = torch.empty((w.num_tokens,), dtype=torch.int32, device=dev)
+        self.raw_values = torch.empty((self.ws_rows_raw, w.index_head_dim // 2),
+                                      dtype=torch.uint8, device=dev)
+        self.raw_scales = torch.empty((self.ws_rows_raw, w.index_head_dim // 32),
+                                      dtype=torch.uint8, device=dev)
+
+    def workspace_launches(self) -> list[tuple[str, Callable[[], None]]]:
+        """The prefill workspace step as (kernel name, launch) pairs, in order."""
+        w = self.w
+        if self.ws is None:
+            self.alloc_workspace()
+        comp_table = self.comp_bt if self.comp_bt is not None else self.swa_bt
+        return [
+            ("quantize_and_insert_k_cache", lambda: ops.quantize_and_insert_k_cache(
+                self.k, self.swa_cache, self.insert_slots, w.swa_cache.block_size,
+                rope_dim=w.rope_dim, err_count=self.err)),
+            ("write_indexer_mxfp4_cache", lambda: ops.write_indexer_mxfp4_cache(
+                self.index_k, self.index_cache, self.index_insert_slots,
+                w.index_cache.block_size, err_count=self.err)),
+            ("dequantize_and_gather_k_cache_ranges[compressed]",
+             lambda: ops.dequantize_and_gather_k_cache_ranges(
+                 self.ws[:, :self.ws_cb], self.comp_cache, self.ws_lc, None, comp_table,
+                 w.comp_cache.block_size, 0, rope_dim=w.rope_dim)),
+            ("dequantize_and_gather_k_cache_ranges[swa]",
+             lambda: ops.dequantize_and_gather_k_cache_ranges(
+                 self.ws, self.swa_cache, self.seq_lens, self.ws_glen, self.swa_bt,
+                 w.swa_cache.block_size, self.ws_cb, rope_dim=w.rope_dim)),
+            ("combine_topk_swa_workspace_indices",
+             lambda: ops.combine_topk_swa_workspace_indices(
+                 self.topk, self.qsl, self.seq_lens, self.ws_glen, self.t2r, w.window,
+                 w.compress_ratio, self.ws_width, self.ws_cb, is_valid_token=self.valid,
+                 out=self.ws_indices, lens=self.ws_lens)),
+            ("indexer_mxfp4_paged_gather", lambda: ops.indexer_mxfp4_paged_gather(
+                self.index_cache, comp_table, self.ws_cu, w.index_cache.block_size,
+                w.index_head_dim, self.ws_rows_raw, values_out=self.raw_values,
+                scales_out=self.raw_scales)),
+        ]
 
     # the indexer cache follows the compressed table
     @property
@@ -161,10 +225,13 @@ class Pipeline:
             record=ops.PSK_REC_MXFP4)))
         return L
 
-    def step(self, concurrent: bool = False, hooks: Optional[dict] = None) -> None:
+    def step(self, concurrent: bool = False, hooks: Optional[dict] = None,
+             path: str = "index") -> None:
         """Launch one step.  ``hooks`` maps a kernel name to a pair of callables
         run on that kernel's stream just before and just after its launch
         (used to bracket one kernel with timing events)."""
+        if path == "workspace":
+            return self._workspace_step(concurrent, hooks or {})
         L = dict(self.launches())
         hooks = hooks or {}
 
@@ -209,3 +276,58 @@ class Pipeline:
             run("dequantize_and_gather_k_cache[topk]")
             main.wait_event(done_a)
         main.wait_event(done_b)
+
+    def _workspace_step(self, concurrent: bool, hooks: dict) -> None:
+        L = dict(self.workspace_launches())
+
+        def run(name):
+            pre, post = hooks.get(name, (None, None))
+            if pre:
+                pre()
+            L[name]()
+            if post:
+                post()
+
+        if not concurrent:
+            for name in L:
+                run(name)
+            return
+        main = torch.cuda.current_stream(self.dev)
+        if not hasattr(self, "_side"):
+            self._side = (torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev))
+        sa, sb = self._side
+        fork = torch.cuda.Event()
+        fork.record(main)
+        sa.wait_event(fork)
+        sb.wait_event(fork)
+        with torch.cuda.stream(sb):
+            run("write_indexer_mxfp4_cache")
+            run("indexer_mxfp4_paged_gather")
+            done_b = torch.cuda.Event()
+            done_b.record(sb)
+        with torch.cuda.stream(sa):
+            run("quantize_and_insert_k_cache")
+            run("dequantize_and_gather_k_cache_ranges[swa]")
+            done_a = torch.cuda.Event()
+            done_a.record(sa)
+        run("dequantize_and_gather_k_cache_ranges[compressed]")
+        run("combine_topk_swa_workspace_indices")
+        main.wait_event(done_a)
+        main.wait_event(done_b)
+
+
+def workspace_geometry(w: Workload) -> dict:
+    """Per-request gather lengths and the workspace shape of the prefill path
+    (TokenSpeed backends/deepseek_v4.py, _prefill_workspace): gather_lens =
+    query_lens + min(prefix, W - 1); compressed_lens = seq_lens // ratio;
+    compressed_base = max compressed length; workspace_width = compressed_base +
+    max gather length; cu_compressed = prefix sums of compressed_lens."""
+    seq = w.seq_lens.astype(np.int64)
+    qlen = np.diff(w.query_start_loc).astype(np.int64)
+    glen = qlen + np.minimum(seq - qlen, max(w.window - 1, 0))
+    lc = seq // w.compress_ratio
+    cb = int(lc.max()) if lc.size else 0
+    return {"gather_lens": glen.astype(np.int32), "compressed_lens": lc.astype(np.int32),
+            "compressed_base": cb,
+            "workspace_width": max(1, cb + (int(glen.max()) if glen.size else 0)),
+            "cu_compressed": np.concatenate([[0], np.cumsum(lc)]).astype(np.int32)}

@@ -157,3 +157,60 @@ def test_error_message_is_thread_local(psk_lib):
     th.join()
     assert seen["msg"] == ""
     assert "is_ue8m0" in _abi.last_error()
+
+
+def _ranges(**kw):
+    a = dict(out=A, osr=8 * 512, osi=512, rows=8, cache=B, num_pages=8, page_stride=64 * 584,
+             bs=64, rec=0, D=512, rope=64, ue=1, seq=C, glen=None, bt=C + 4096, bts=4, btw=4,
+             base=None, R=2, off=0)
+    a.update(kw)
+    return _abi.status("dequantize_and_gather_k_cache_ranges", a["out"], a["osr"], a["osi"],
+                       a["rows"], a["cache"], a["num_pages"], a["page_stride"], a["bs"], a["rec"],
+                       a["D"], a["rope"], a["ue"], a["seq"], a["glen"], a["bt"], a["bts"],
+                       a["btw"], a["base"], a["R"], a["off"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(off=9), dict(off=-1), dict(out=None), dict(seq=None),
+                                dict(osi=4), dict(out=A + 2), dict(btw=5), dict(D=100),
+                                dict(page_stride=100), dict(R=-1)])
+def test_range_gather_rejects_bad_arguments(psk_lib, kw):
+    assert _ranges(**kw) == INV
+
+
+def test_range_gather_rejects_mxfp4_record(psk_lib):
+    assert _ranges(rec=1) == _abi.PSK_ERR_UNSUPPORTED
+
+
+def test_range_gather_zero_work_ok(psk_lib):
+    assert _ranges(R=0, out=None, seq=None) == OK
+    assert _ranges(off=8, out=None) == OK
+
+
+def _wsidx(**kw):
+    a = dict(qsl=A, seq=A + 256, glen=A + 512, t2r=A + 768, R=2, n=3, W=8, ratio=4, topk=B,
+             ts=8, K=8, ww=100, cb=10, valid=None, out=C, os=16, lens=C + 4096)
+    a.update(kw)
+    return _abi.status("combine_topk_swa_workspace_indices", a["qsl"], a["seq"], a["glen"],
+                       a["t2r"], a["R"], a["n"], a["W"], a["ratio"], a["topk"], a["ts"], a["K"],
+                       a["ww"], a["cb"], a["valid"], a["out"], a["os"], a["lens"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(os=15), dict(ratio=0), dict(glen=None), dict(W=-1),
+                                dict(ww=-1), dict(R=0), dict(lens=None), dict(ts=4)])
+def test_workspace_indices_reject_bad_arguments(psk_lib, kw):
+    assert _wsidx(**kw) == INV
+
+
+def _raw(**kw):
+    a = dict(v=A, s=A + 4096, cache=B, num_pages=4, page_stride=64 * 68, bs=64, D=128, bt=C,
+             bts=2, btw=2, cu=C + 256, R=2, n=100)
+    a.update(kw)
+    return _abi.status("indexer_mxfp4_paged_gather", a["v"], a["s"], a["cache"], a["num_pages"],
+                       a["page_stride"], a["bs"], a["D"], a["bt"], a["bts"], a["btw"], a["cu"],
+                       a["R"], a["n"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(D=96), dict(v=None), dict(cu=None), dict(R=0),
+                                dict(s=A + 4098), dict(n=-1), dict(page_stride=64 * 68 - 16)])
+def test_mxfp4_raw_gather_rejects_bad_arguments(psk_lib, kw):
+    assert _raw(**kw) == INV
