@@ -28,6 +28,20 @@
 namespace psk {
 namespace {
 
+// Launch-shape constants (overridable at build time for tuning sweeps).
+#ifndef PSK_INDEX_BATCH
+#define PSK_INDEX_BATCH 4
+#endif
+#ifndef PSK_WS_INDEX_BATCH
+#define PSK_WS_INDEX_BATCH 4
+#endif
+#ifndef PSK_INDEX_MAX_PASSES
+#define PSK_INDEX_MAX_PASSES 1
+#endif
+#ifndef PSK_WS_INDEX_MAX_PASSES
+#define PSK_WS_INDEX_MAX_PASSES 2
+#endif
+
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / kWarp;
 constexpr int kMaxStagedEntries = 4096;  // 16 KB of int32 page ids per staged row
@@ -35,14 +49,27 @@ constexpr int kMaxStagedEntries = 4096;  // 16 KB of int32 page ids per staged r
 struct TableRow {
     const int32_t* row;  // global row, or shared copy
     int32_t width;
-    int64_t base;
+    int32_t base;
     int32_t bs;
     int32_t shift;  // log2(bs) or -1
+    int32_t maxp;   // INT32_MAX / bs: largest page whose slots can fit in int32
+    int32_t maxrem; // INT32_MAX % bs
 };
 
-// Slot of logical position p (p >= 0) through one block-table row, or -1.
-__device__ __forceinline__ int32_t map_slot(const TableRow& tr, bool shared, int64_t p) {
-    int64_t q, rem;
+__device__ __forceinline__ void table_limits(TableRow& tr) {
+    tr.maxp = INT_MAX / tr.bs;
+    tr.maxrem = INT_MAX % tr.bs;
+}
+
+// Slot of logical position p (0 <= p <= INT32_MAX) through one block-table
+// row, or -1: logical page p / bs - base outside [0, width), a negative page,
+// or a slot beyond INT32_MAX.  All 32-bit: q - base is formed modulo 2^32 and
+// tested as unsigned against width; it wraps only when the true logical page
+// is >= 2^31 (q >= 0, base >= -2^31), and then the wrapped value is negative,
+// i.e. rejected, as the true one would be.
+template <bool SHARED>
+__device__ __forceinline__ int32_t map_slot(const TableRow& tr, int32_t p) {
+    int32_t q, rem;
     if (tr.shift >= 0) {
         q = p >> tr.shift;
         rem = p & ((1 << tr.shift) - 1);
@@ -50,12 +77,11 @@ __device__ __forceinline__ int32_t map_slot(const TableRow& tr, bool shared, int
         q = p / tr.bs;
         rem = p - q * tr.bs;
     }
-    const int64_t lp = q - tr.base;
-    if (lp < 0 || lp >= tr.width) return -1;
-    const int32_t page = shared ? tr.row[lp] : __ldg(tr.row + lp);
-    if (page < 0) return -1;
-    const int64_t s = (int64_t)page * tr.bs + rem;
-    return s > INT_MAX ? -1 : (int32_t)s;
+    const uint32_t lp = (uint32_t)q - (uint32_t)tr.base;
+    if (lp >= (uint32_t)tr.width) return -1;
+    const int32_t page = SHARED ? tr.row[lp] : __ldg(tr.row + lp);
+    if ((uint32_t)page > (uint32_t)tr.maxp || (page == tr.maxp && rem > tr.maxrem)) return -1;
+    return page * tr.bs + rem;
 }
 
 // Per-token values that depend on its request (second memory round trip).
@@ -63,7 +89,7 @@ struct TokMeta {
     int32_t r;
     bool ok;
     int64_t pos, lo;
-    int64_t swa_base, comp_base;
+    int32_t swa_base, comp_base;
 };
 
 template <bool HAS_SWA>
@@ -97,12 +123,12 @@ __device__ __forceinline__ int4 load_topk_quad(const IndexParams& p, const int32
 }
 
 // Writes token t's row and returns this lane's count of valid entries.
-// `pre` is the top-k quad of column group `first`, loaded in advance (VEC).
-template <bool HAS_SWA, bool VEC>
+// `pre` holds the lane's first batch of top-k quads, loaded in advance (VEC).
+// STAGED: the token's table rows are in shared memory (else read through L1).
+template <bool HAS_SWA, bool VEC, bool STAGED>
 __device__ __forceinline__ int build_row(const IndexParams& p, int64_t t, const TokMeta& m,
-                                         int first, int stride, int4 pre, bool swa_s,
-                                         bool comp_s, const int32_t* s_swa,
-                                         const int32_t* s_comp) {
+                                         int first, int stride, const int4 (&pre)[PSK_INDEX_BATCH],
+                                         const int32_t* s_swa, const int32_t* s_comp) {
     int32_t* out = p.out + t * p.out_stride;
     if (!m.ok) {
         if (VEC) {
@@ -121,49 +147,68 @@ __device__ __forceinline__ int build_row(const IndexParams& p, int64_t t, const 
         return 0;
     }
     TableRow comp;
-    comp.row = comp_s ? s_comp : p.comp_bt + (int64_t)m.r * p.comp_stride;
+    comp.row = STAGED ? s_comp : p.comp_bt + (int64_t)m.r * p.comp_stride;
     comp.width = p.comp_width;
     comp.base = m.comp_base;
     comp.bs = p.comp_bs;
     comp.shift = p.comp_shift;
+    table_limits(comp);
     TableRow swa;
     if (HAS_SWA) {
-        swa.row = swa_s ? s_swa : p.swa_bt + (int64_t)m.r * p.swa_stride;
+        swa.row = STAGED ? s_swa : p.swa_bt + (int64_t)m.r * p.swa_stride;
         swa.width = p.swa_width;
         swa.base = m.swa_base;
         swa.bs = p.swa_bs;
         swa.shift = p.swa_shift;
+        table_limits(swa);
     }
     const int32_t* tk = p.topk_local + t * p.topk_stride;
     const int W = HAS_SWA ? p.window : 0;
 
     int cnt = 0;
     if (VEC) {
+        // Quads are processed in batches of kBatch per lane: every top-k load
+        // of a batch is issued before any of them is used.
+        constexpr int kBatch = PSK_INDEX_BATCH;
         const int nq = (p.out_cols + 3) / 4;
-        for (int q = first; q < nq; q += stride) {
-            const int c0 = 4 * q;
-            int v[4];
-            if (HAS_SWA && c0 < W) {
+        for (int qb = first; qb < nq; qb += kBatch * stride) {
+            int4 L[kBatch];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int64_t ps = m.lo + c0 + e;
-                    v[e] = ps <= m.pos ? map_slot(swa, swa_s, ps) : -1;
-                }
-            } else {
-                const int4 w = (q == first) ? pre : load_topk_quad(p, tk, c0 - W);
-                v[0] = w.x >= 0 ? map_slot(comp, comp_s, w.x) : -1;
-                v[1] = w.y >= 0 ? map_slot(comp, comp_s, w.y) : -1;
-                v[2] = w.z >= 0 ? map_slot(comp, comp_s, w.z) : -1;
-                v[3] = w.w >= 0 ? map_slot(comp, comp_s, w.w) : -1;
+            for (int u = 0; u < kBatch; ++u) {
+                const int q = qb + u * stride;
+                const int c0 = 4 * q;
+                L[u] = make_int4(-1, -1, -1, -1);
+                if (qb == first) L[u] = pre[u];
+                else if (q < nq && c0 >= W) L[u] = load_topk_quad(p, tk, c0 - W);
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) cnt += v[e] >= 0;
-            if (c0 + 3 < p.out_cols) {
-                *reinterpret_cast<int4*>(out + c0) = make_int4(v[0], v[1], v[2], v[3]);
-            } else {
-                out[c0] = v[0];
-                if (c0 + 1 < p.out_cols) out[c0 + 1] = v[1];
-                if (c0 + 2 < p.out_cols) out[c0 + 2] = v[2];
+            for (int u = 0; u < kBatch; ++u) {
+                const int q = qb + u * stride;
+                if (q >= nq) break;
+                const int c0 = 4 * q;
+                int v[4];
+                if (HAS_SWA && c0 < W) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int64_t ps = m.lo + c0 + e;
+                        v[e] = ps <= m.pos ? map_slot<STAGED>(swa, (int32_t)ps) : -1;
+                    }
+                } else {
+                    const int4 w = L[u];
+                    v[0] = w.x >= 0 ? map_slot<STAGED>(comp, w.x) : -1;
+                    v[1] = w.y >= 0 ? map_slot<STAGED>(comp, w.y) : -1;
+                    v[2] = w.z >= 0 ? map_slot<STAGED>(comp, w.z) : -1;
+                    v[3] = w.w >= 0 ? map_slot<STAGED>(comp, w.w) : -1;
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) cnt += v[e] >= 0;
+                if (c0 + 3 < p.out_cols) {
+                    *reinterpret_cast<int4*>(out + c0) = make_int4(v[0], v[1], v[2], v[3]);
+                } else {
+                    out[c0] = v[0];
+                    if (c0 + 1 < p.out_cols) out[c0 + 1] = v[1];
+                    if (c0 + 2 < p.out_cols) out[c0 + 2] = v[2];
+                }
             }
         }
     } else {
@@ -171,17 +216,31 @@ __device__ __forceinline__ int build_row(const IndexParams& p, int64_t t, const 
             int v;
             if (HAS_SWA && c < W) {
                 const int64_t ps = m.lo + c;
-                v = ps <= m.pos ? map_slot(swa, swa_s, ps) : -1;
+                v = ps <= m.pos ? map_slot<STAGED>(swa, (int32_t)ps) : -1;
             } else {
                 const int j = c - W;
                 const int l = j < p.topk ? __ldg(tk + j) : -1;
-                v = l >= 0 ? map_slot(comp, comp_s, l) : -1;
+                v = l >= 0 ? map_slot<STAGED>(comp, l) : -1;
             }
             cnt += v >= 0;
             out[c] = v;
         }
     }
     return cnt;
+}
+
+// Loads the lane's first batch of top-k quads of token t (depends on t only).
+template <bool VEC>
+__device__ __forceinline__ void load_first_batch(const IndexParams& p, int64_t t, int64_t t1,
+                                                 int first, int stride, int W,
+                                                 int4 (&pre)[PSK_INDEX_BATCH]) {
+#pragma unroll
+    for (int u = 0; u < PSK_INDEX_BATCH; ++u) {
+        const int c0 = 4 * (first + u * stride);
+        pre[u] = make_int4(-1, -1, -1, -1);
+        if (VEC && t < t1 && c0 >= W && c0 < p.out_cols)
+            pre[u] = load_topk_quad(p, p.topk_local + t * p.topk_stride, c0 - W);
+    }
 }
 
 // Copies `n` table entries to shared memory, 4 loads in flight per thread.
@@ -202,7 +261,7 @@ __device__ __forceinline__ void stage_row(int32_t* dst, const int32_t* src, int 
 }
 
 template <bool HAS_SWA, bool VEC>
-__global__ void __launch_bounds__(kThreads) index_build_kernel(IndexParams p) {
+__global__ void __launch_bounds__(kThreads, 3) index_build_kernel(IndexParams p) {
     extern __shared__ int32_t s_tab[];  // [stage_comp] compressed row, then [stage_swa] SWA row
     __shared__ int s_cnt[kWarps];
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
@@ -224,23 +283,22 @@ __global__ void __launch_bounds__(kThreads) index_build_kernel(IndexParams p) {
     const int32_t r1 = __ldg(p.t2r + t1 - 1);
     const int64_t tf = t0 + tslot;  // this warp's first token
     int32_t rf = -1;
-    int4 pre = make_int4(-1, -1, -1, -1);
-    if (tf < t1) {
-        rf = __ldg(p.t2r + tf);
-        if (VEC && 4 * first >= W && 4 * first < p.out_cols)
-            pre = load_topk_quad(p, p.topk_local + tf * p.topk_stride, 4 * first - W);
-    }
+    int4 pre[PSK_INDEX_BATCH];
+    if (tf < t1) rf = __ldg(p.t2r + tf);
+    load_first_batch<VEC>(p, tf, t1, first, stride, W, pre);
     // Round 2: the first token's request metadata and, when the tile is one
     // request, its block-table rows into shared memory.
     TokMeta mf;
     if (tf < t1) mf = load_meta<HAS_SWA>(p, tf, rf);
-    const int32_t staged = (r0 == r1 && r0 >= 0 && r0 < p.num_reqs) ? r0 : -1;
-    const bool comp_s = staged >= 0 && p.stage_comp > 0;
-    const bool swa_s = HAS_SWA && staged >= 0 && p.stage_swa > 0;
+    // Stage only when every row the tile needs fits (p.stage_* > 0 exactly then).
+    const bool fits = p.stage_comp > 0 && (!HAS_SWA || p.stage_swa > 0);
+    const int32_t staged = (fits && r0 == r1 && r0 >= 0 && r0 < p.num_reqs) ? r0 : -1;
     int32_t* s_comp = s_tab;
     int32_t* s_swa = s_tab + p.stage_comp;
-    if (comp_s) stage_row(s_comp, p.comp_bt + (int64_t)staged * p.comp_stride, p.stage_comp);
-    if (swa_s) stage_row(s_swa, p.swa_bt + (int64_t)staged * p.swa_stride, p.stage_swa);
+    if (staged >= 0) {
+        stage_row(s_comp, p.comp_bt + (int64_t)staged * p.comp_stride, p.stage_comp);
+        if (HAS_SWA) stage_row(s_swa, p.swa_bt + (int64_t)staged * p.swa_stride, p.stage_swa);
+    }
     __syncthreads();
 
     for (int64_t tb = t0; tb < t1; tb += tpp) {
@@ -248,19 +306,16 @@ __global__ void __launch_bounds__(kThreads) index_build_kernel(IndexParams p) {
         int cnt = 0;
         if (t < t1) {
             TokMeta m;
-            int4 q0;
             if (tb == t0) {
                 m = mf;
-                q0 = pre;
             } else {
                 m = load_meta<HAS_SWA>(p, t, __ldg(p.t2r + t));
-                q0 = (VEC && 4 * first >= W && 4 * first < p.out_cols)
-                         ? load_topk_quad(p, p.topk_local + t * p.topk_stride, 4 * first - W)
-                         : make_int4(-1, -1, -1, -1);
+                load_first_batch<VEC>(p, t, t1, first, stride, W, pre);
             }
-            const bool same = m.r == staged;
-            cnt = build_row<HAS_SWA, VEC>(p, t, m, first, stride, q0, swa_s && same,
-                                          comp_s && same, s_swa, s_comp);
+            if (staged >= 0 && m.r == staged)
+                cnt = build_row<HAS_SWA, VEC, true>(p, t, m, first, stride, pre, s_swa, s_comp);
+            else
+                cnt = build_row<HAS_SWA, VEC, false>(p, t, m, first, stride, pre, s_swa, s_comp);
         }
         cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
         if (wpt == 1) {
@@ -306,6 +361,28 @@ __global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceInde
         if (t < t1) {
             int32_t* out = p.out + t * p.out_stride;
             const int32_t r = __ldg(p.t2r + t);
+            const int32_t* tk = p.topk_local + t * p.topk_stride;
+            // The first batch of top-k quads depends only on t: issue it now.
+            constexpr int kPre = PSK_WS_INDEX_BATCH;
+            int4 Lpre[kPre];
+            if (VEC) {
+#pragma unroll
+                for (int u = 0; u < kPre; ++u) {
+                    const int q = first + u * stride;
+                    const int c0 = 4 * q;
+                    Lpre[u] = make_int4(-1, -1, -1, -1);
+                    if (q < cols / 4 && c0 >= W) {
+                        const int j0 = c0 - W;
+                        if (j0 + 3 < p.topk) {
+                            Lpre[u] = __ldg(reinterpret_cast<const int4*>(tk + j0));
+                        } else {
+                            Lpre[u].x = j0 < p.topk ? __ldg(tk + j0) : -1;
+                            Lpre[u].y = j0 + 1 < p.topk ? __ldg(tk + j0 + 1) : -1;
+                            Lpre[u].z = j0 + 2 < p.topk ? __ldg(tk + j0 + 2) : -1;
+                        }
+                    }
+                }
+            }
             const bool ok = (p.valid == nullptr || __ldg(p.valid + t) != 0) && r >= 0 &&
                             r < p.num_reqs;
             int64_t pos = 0, lo = 0, g0 = 0, lc = 0, rbase = 0;
@@ -319,7 +396,6 @@ __global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceInde
                 lo = pos - W + 1;
                 if (lo < 0) lo = 0;
             }
-            const int32_t* tk = p.topk_local + t * p.topk_stride;
             auto col = [&](int c, int l_in) -> int {
                 if (!ok) return -1;
                 int64_t v = -1;
@@ -332,24 +408,39 @@ __global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceInde
                 return v > 0x7FFFFFFFll ? -1 : (int)v;
             };
             if (VEC) {
+                constexpr int kBatch = PSK_WS_INDEX_BATCH;
                 const int nq = cols / 4;
-                for (int q = first; q < nq; q += stride) {
-                    const int c0 = 4 * q;
-                    int4 l = make_int4(-1, -1, -1, -1);
-                    if (ok && c0 >= W) {
-                        const int j0 = c0 - W;
-                        if (j0 + 3 < p.topk) {
-                            l = __ldg(reinterpret_cast<const int4*>(tk + j0));
-                        } else {
-                            l.x = j0 < p.topk ? __ldg(tk + j0) : -1;
-                            l.y = j0 + 1 < p.topk ? __ldg(tk + j0 + 1) : -1;
-                            l.z = j0 + 2 < p.topk ? __ldg(tk + j0 + 2) : -1;
+                for (int qb = first; qb < nq; qb += kBatch * stride) {
+                    int4 L[kBatch];
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) {
+                        const int q = qb + u * stride;
+                        const int c0 = 4 * q;
+                        L[u] = make_int4(-1, -1, -1, -1);
+                        if (qb == first) {
+                            L[u] = Lpre[u];
+                        } else if (q < nq && c0 >= W) {
+                            const int j0 = c0 - W;
+                            if (j0 + 3 < p.topk) {
+                                L[u] = __ldg(reinterpret_cast<const int4*>(tk + j0));
+                            } else {
+                                L[u].x = j0 < p.topk ? __ldg(tk + j0) : -1;
+                                L[u].y = j0 + 1 < p.topk ? __ldg(tk + j0 + 1) : -1;
+                                L[u].z = j0 + 2 < p.topk ? __ldg(tk + j0 + 2) : -1;
+                            }
                         }
                     }
-                    const int4 v = make_int4(col(c0, l.x), col(c0 + 1, l.y), col(c0 + 2, l.z),
-                                             col(c0 + 3, l.w));
-                    cnt += (v.x >= 0) + (v.y >= 0) + (v.z >= 0) + (v.w >= 0);
-                    *reinterpret_cast<int4*>(out + c0) = v;
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) {
+                        const int q = qb + u * stride;
+                        if (q >= nq) break;
+                        const int c0 = 4 * q;
+                        const int4 l = L[u];
+                        const int4 v = make_int4(col(c0, l.x), col(c0 + 1, l.y), col(c0 + 2, l.z),
+                                                 col(c0 + 3, l.w));
+                        cnt += (v.x >= 0) + (v.y >= 0) + (v.z >= 0) + (v.w >= 0);
+                        *reinterpret_cast<int4*>(out + c0) = v;
+                    }
                 }
             } else {
                 for (int c = first; c < cols; c += stride) {
@@ -386,7 +477,7 @@ cudaError_t launch_workspace_indices(const WorkspaceIndexParams& p, cudaStream_t
     const int tpp = kWarps / wpt;
     int64_t passes = T / ((int64_t)tpp * 2 * sms);
     if (passes < 1) passes = 1;
-    if (passes > 8) passes = 8;
+    if (passes > PSK_WS_INDEX_MAX_PASSES) passes = PSK_WS_INDEX_MAX_PASSES;
     const int tokens_per_cta = (int)(tpp * passes);
     const int64_t blocks = (T + tokens_per_cta - 1) / tokens_per_cta;
     const bool vec = ((reinterpret_cast<uintptr_t>(p.out) & 15) == 0) && (p.out_stride % 4 == 0) &&
@@ -408,11 +499,12 @@ cudaError_t launch_index_build(IndexParams p, bool has_swa, cudaStream_t stream)
     const int tpp = kWarps / wpt;
     int64_t passes = T / ((int64_t)tpp * 2 * sms);
     if (passes < 1) passes = 1;
-    if (passes > 8) passes = 8;
+    if (passes > PSK_INDEX_MAX_PASSES) passes = PSK_INDEX_MAX_PASSES;
     p.warps_per_token = wpt;
     p.tokens_per_cta = (int32_t)(tpp * passes);
     p.stage_comp = (p.comp_width > 0 && p.comp_width <= kMaxStagedEntries) ? p.comp_width : 0;
     p.stage_swa = (has_swa && p.swa_width > 0 && p.swa_width <= kMaxStagedEntries) ? p.swa_width : 0;
+    if (p.stage_comp == 0 || (has_swa && p.stage_swa == 0)) p.stage_comp = p.stage_swa = 0;
     const int64_t blocks = (T + p.tokens_per_cta - 1) / p.tokens_per_cta;
     const size_t smem = (size_t)(p.stage_comp + p.stage_swa) * sizeof(int32_t);
 

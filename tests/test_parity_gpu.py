@@ -406,3 +406,35 @@ def test_pipeline_step_matches_oracle(cuda_device, name, mode):
     _assert_same(_u16(gi), ref["gathered_index"], f"{name} gathered mxfp4 rows")
     assert int(p.err.item()) == ref["err"] == 0
     del p
+
+
+@pytest.mark.parametrize("bs", [1, 3, 64])
+def test_index_build_int32_extremes(cuda_device, bs):
+    """Base offsets at the int32 limits, pages whose slots straddle INT32_MAX,
+    local indices near INT32_MAX: the 32-bit device arithmetic must agree with
+    the oracle's 64-bit arithmetic."""
+    rng = np.random.default_rng(bs)
+    imax = 2**31 - 1
+    maxp = imax // bs
+    R, width, T, K = 3, 6, 24, 12
+    table = rng.choice(np.array([maxp, maxp - 1, maxp + 1 if maxp + 1 <= imax else maxp, 0, 5, -1,
+                                 imax], np.int64), size=(R, width)).astype(np.int32)
+    base = np.array([-2**31, imax, 0], np.int32)
+    t2r = rng.integers(0, R, size=T).astype(np.int32)
+    cand = np.array([0, bs - 1, bs, imax, imax - 1, imax - bs, -1, 7], np.int64)
+    topk = rng.choice(cand, size=(T, K)).astype(np.int32)
+    # positions that reach logical pages 0.. of each base: p = (lp + base) * bs + o
+    for r in range(R):
+        lo = (int(base[r]) * bs) if base[r] >= 0 else 0
+        for j in range(0, K, 3):
+            rows = np.nonzero(t2r == r)[0]
+            if rows.size and 0 <= lo <= imax - width * bs:
+                topk[rows, j] = lo + int(rng.integers(0, width * bs))
+    d = cuda_device
+    out, lens = ops.compute_global_topk_indices_and_lens(
+        _dev_i32(topk, d), _dev_i32(t2r, d), _dev_i32(table, d), bs,
+        base_offsets=_dev_i32(base, d))
+    want, wl = oracle.compute_global_topk_indices_and_lens(topk, t2r, table, bs, base_offsets=base)
+    _assert_same(out.cpu().numpy(), want, "extreme global top-k")
+    _assert_same(lens.cpu().numpy(), wl, "extreme lens")
+    assert (want >= 0).any()
