@@ -69,14 +69,15 @@ struct ItemSource {
 
 // Slot of position p through one table row (the block-table rule), or -1.
 __device__ __forceinline__ int32_t table_slot(const int32_t* row, int32_t width, int64_t base,
-                                              int32_t bs, int64_t p) {
+                                              int32_t bs, int32_t shift, int64_t p) {
     if (p < 0) return -1;
-    const int64_t q = p / bs;
+    int64_t rem;
+    const int64_t q = div_block(p, bs, shift, rem);
     const int64_t lp = q - base;
     if (lp < 0 || lp >= width) return -1;
     const int32_t page = __ldg(row + lp);
     if (page < 0) return -1;
-    const int64_t s = (int64_t)page * bs + (p - q * bs);
+    const int64_t s = (int64_t)page * bs + rem;
     return s > 0x7FFFFFFFll ? -1 : (int32_t)s;
 }
 
@@ -150,7 +151,7 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
                             const int64_t base = src.r.base_offsets ? __ldg(src.r.base_offsets + t) : 0;
                             const int32_t raw = table_slot(src.r.block_table + t * src.r.bt_stride,
                                                            src.r.bt_width, base, p.block_size,
-                                                           seq - g + j);
+                                                           p.block_shift, seq - g + j);
                             slot[q] = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
                             oof[q] = t * src.r.out_stride_r + (src.r.offset + j) * src.r.out_stride_i;
                         } else {
@@ -182,8 +183,8 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
                 uint32_t scl_bytes = 0;
                 int32_t soff = -1;
                 if (sl >= 0) {
-                    const int32_t page = sl / bs;
-                    const int32_t off = sl - page * bs;
+                    int32_t off;
+                    const int32_t page = div_block32(sl, bs, p.block_shift, off);
                     const uint8_t* pbase = p.cache + (int64_t)page * p.page_stride;
                     src_data = pbase + (int64_t)off * ts;
                     const uintptr_t a = reinterpret_cast<uintptr_t>(pbase + (int64_t)bs * ts + (int64_t)off * SDIM);
@@ -323,8 +324,8 @@ gather_mxfp4_kernel(GatherParams p) {
         for (int st = 0; st < STEPS; ++st) {
             slot[st] = __shfl_sync(0xFFFFFFFFu, my_slot, st * GPW + grp);
             if (slot[st] >= 0) {
-                const int32_t page = slot[st] / p.block_size;
-                const int32_t off = slot[st] - page * p.block_size;
+                int32_t off;
+                const int32_t page = div_block32(slot[st], p.block_size, p.block_shift, off);
                 const uint8_t* base = p.cache + (int64_t)page * p.page_stride;
                 const uint8_t* vals = base + (int64_t)off * VB;
                 const uint8_t* sc = base + (int64_t)p.block_size * VB + (int64_t)off * SB;
@@ -431,7 +432,9 @@ cudaError_t read_wait_timeouts(uint32_t* count) {
     return cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(uint32_t));
 }
 
-cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
+cudaError_t launch_gather(const GatherParams& params, cudaStream_t stream) {
+    GatherParams p = params;
+    p.block_shift = log2_if_pow2(p.block_size);
     if (p.record == 0) {
         ItemSource src{};
         src.g = p;
@@ -456,6 +459,7 @@ cudaError_t launch_gather_ranges(const RangeParams& r, cudaStream_t stream) {
     src.g.num_pages = r.num_pages;
     src.g.page_stride = r.page_stride;
     src.g.block_size = r.block_size;
+    src.g.block_shift = log2_if_pow2(r.block_size);
     src.g.record = 0;
     src.g.head_dim = r.head_dim;
     src.g.rope_dim = r.rope_dim;
@@ -494,11 +498,12 @@ __global__ void __launch_bounds__(kThreads) mxfp4_raw_gather_kernel(RawGatherPar
         int32_t s = -1;
         if (row >= start && row < end) {
             const int64_t i = row - start;
-            const int64_t lp = i / p.block_size;
+            int64_t rem;
+            const int64_t lp = div_block(i, p.block_size, p.block_shift, rem);
             if (lp < p.bt_width) {
                 const int32_t page = __ldg(p.block_table + (int64_t)lo * p.bt_stride + lp);
                 if (page >= 0) {
-                    const int64_t sl = (int64_t)page * p.block_size + (i - lp * p.block_size);
+                    const int64_t sl = (int64_t)page * p.block_size + rem;
                     if (sl < capacity) s = (int32_t)sl;
                 }
             }
@@ -511,7 +516,8 @@ __global__ void __launch_bounds__(kThreads) mxfp4_raw_gather_kernel(RawGatherPar
             if (gl == 0) for (int b = 0; b < SB; ++b) so[b] = 0;
             continue;
         }
-        const int32_t page = s / p.block_size, off = s - page * p.block_size;
+        int32_t off;
+        const int32_t page = div_block32(s, p.block_size, p.block_shift, off);
         const uint8_t* base = p.cache + (int64_t)page * p.page_stride;
         const uint8_t* vals = base + (int64_t)off * VB;
         const uint8_t* scl = base + (int64_t)p.block_size * VB + (int64_t)off * SB;
@@ -539,7 +545,9 @@ cudaError_t raw_dispatch(const RawGatherParams& p, cudaStream_t stream) {
     return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p);
 }
 
-cudaError_t launch_mxfp4_raw_gather(const RawGatherParams& p, cudaStream_t stream) {
+cudaError_t launch_mxfp4_raw_gather(const RawGatherParams& params, cudaStream_t stream) {
+    RawGatherParams p = params;
+    p.block_shift = log2_if_pow2(p.block_size);
     switch (p.head_dim) {
         case 32: return raw_dispatch<32>(p, stream);
         case 64: return raw_dispatch<64>(p, stream);

@@ -12,7 +12,10 @@
 //  * A quant block is 8 chunks (FP8, 64 dims) or 4 chunks (MXFP4, 32 dims),
 //    held by 8 or 4 consecutive lanes: its amax is a 3- or 2-step
 //    __shfl_xor reduction.
-//  * Exponents are read off the binary32 bits of amax / max_code (no log2).
+//  * amax is a 16-bit unsigned max over the bf16 magnitude bits, and the
+//    scale exponent ceil(log2(amax / max_code)) is read off amax's own bits
+//    (exact for bf16 amax; no divide, no log2); scaling is a packed
+//    mul.rn.f32x2 per pair.
 //  * Codes are packed with cvt.rn.satfinite.{e4m3x2,e2m1x2}.f32 and stored as
 //    8-byte (FP8) / 4-byte (MXFP4) words: a group's stores of one record are
 //    contiguous and coalesce; the rope tail moves as untouched 16-byte chunks.
@@ -70,7 +73,7 @@ __global__ void __launch_bounds__(kThreads)
 fp8_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
                   const int64_t* __restrict__ slots, int64_t n,
                   uint8_t* __restrict__ cache, int64_t capacity, int64_t page_stride,
-                  int32_t bs, int32_t rope, int32_t* __restrict__ err) {
+                  int32_t bs, int32_t shift, int32_t rope, int32_t* __restrict__ err) {
     constexpr int CHUNKS = D / 8;
     constexpr int LANES = CHUNKS < kWarp ? CHUNKS : kWarp;
     constexpr int CPL = CHUNKS / LANES;
@@ -110,8 +113,8 @@ fp8_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
             if (gl == 0 && err) atomicAdd(err, 1);
             continue;
         }
-        const int64_t page = sl / bs;
-        const int64_t off = sl - page * bs;
+        int64_t off;
+        const int64_t page = div_block(sl, bs, shift, off);
         uint8_t* base = cache + page * page_stride;
         uint8_t* data = base + off * ts;
         uint8_t* scl = base + (int64_t)bs * ts + off * SDIM;
@@ -123,21 +126,26 @@ fp8_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
             const uint4 w = v[u][i];
             float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                           bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-            float am = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(x[j]));
-            am = fmaxf(am, __shfl_xor_sync(gmask, am, 1));
-            am = fmaxf(am, __shfl_xor_sync(gmask, am, 2));
-            am = fmaxf(am, __shfl_xor_sync(gmask, am, 4));
+            uint32_t amb = absmax_bf16x8_bits(w);
+            amb = max(amb, __shfl_xor_sync(gmask, amb, 1));
+            amb = max(amb, __shfl_xor_sync(gmask, amb, 2));
+            amb = max(amb, __shfl_xor_sync(gmask, amb, 4));
+            const float am = __uint_as_float(amb << 16);
             if (8 * c < nope) {  // uniform over the block's 8 lanes
                 float y[8];
                 if constexpr (UE8M0) {
                     const float a = fmaxf(am, 1.0e-4f);
-                    const int e = ceil_log2_pos(__fdiv_rn(a, 448.0f));
+                    const int e = ceil_log2_div_const(a, 0x600000u, 8);  // / 448
                     const int b = min(max(e + 127, 0), 255);
-                    const float pw = exp2_int(-e);
+                    const uint64_t pw2 = splat_f32x2(exp2_int(-e));
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) y[j] = clamp_sym(__fmul_rn(x[j], pw), 448.0f);
+                    for (int j = 0; j < 8; j += 2) {
+                        y[j] = x[j];
+                        y[j + 1] = x[j + 1];
+                        mul2_rn(y[j], y[j + 1], pw2);
+                        y[j] = clamp_sym(y[j], 448.0f);
+                        y[j + 1] = clamp_sym(y[j + 1], 448.0f);
+                    }
                     sb[i] = (uint32_t)b;
                 } else {
                     const float a = fmaxf(am, 1.0e-12f);
@@ -172,7 +180,7 @@ __global__ void __launch_bounds__(kThreads)
 mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
                     const int64_t* __restrict__ slots, int64_t n,
                     uint8_t* __restrict__ cache, int64_t capacity, int64_t page_stride,
-                    int32_t bs, int32_t* __restrict__ err) {
+                    int32_t bs, int32_t shift, int32_t* __restrict__ err) {
     constexpr int CHUNKS = D / 8;
     constexpr int LANES = CHUNKS < kWarp ? CHUNKS : kWarp;
     constexpr int CPL = CHUNKS / LANES;
@@ -210,8 +218,8 @@ mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
             if (gl == 0 && err) atomicAdd(err, 1);
             continue;
         }
-        const int64_t page = sl / bs;
-        const int64_t off = sl - page * bs;
+        int64_t off;
+        const int64_t page = div_block(sl, bs, shift, off);
         uint8_t* base = cache + page * page_stride;
         uint8_t* vals = base + off * VB;
         uint8_t* scl = base + (int64_t)bs * VB + off * SB;
@@ -223,21 +231,19 @@ mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
             const uint4 w = v[u][i];
             float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                           bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-            float am = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(x[j]));
-            am = fmaxf(am, __shfl_xor_sync(gmask, am, 1));
-            am = fmaxf(am, __shfl_xor_sync(gmask, am, 2));
-            const float a = fmaxf(am, 1.0e-4f);
-            const int e = ceil_log2_pos(__fdiv_rn(a, 6.0f));
+            uint32_t amb = absmax_bf16x8_bits(w);
+            amb = max(amb, __shfl_xor_sync(gmask, amb, 1));
+            amb = max(amb, __shfl_xor_sync(gmask, amb, 2));
+            const float a = fmaxf(__uint_as_float(amb << 16), 1.0e-4f);
+            const int e = ceil_log2_div_const(a, 0x400000u, 2);  // / 6
             const int b = min(max(e + 127, 0), 254);
-            const float pw = exp2_int(-e);
+            const uint64_t pw2 = splat_f32x2(exp2_int(-e));
             uint32_t word = 0;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint32_t byte =
-                    cvt_e2m1x2(__fmul_rn(x[2 * j], pw), __fmul_rn(x[2 * j + 1], pw));
-                word |= (byte & 0xFFu) << (8 * j);
+                float lo = x[2 * j], hi = x[2 * j + 1];
+                mul2_rn(lo, hi, pw2);
+                word |= (cvt_e2m1x2(lo, hi) & 0xFFu) << (8 * j);
             }
             *reinterpret_cast<uint32_t*>(vals + 4 * c) = word;
             sb[i] = (uint32_t)b;
@@ -256,7 +262,8 @@ cudaError_t fp8_insert_dispatch(const InsertParams& p, cudaStream_t stream) {
     return launch_pdl(fp8_insert_kernel<D, UE8M0, UNROLL>, dim3((unsigned)blocks), dim3(kThreads),
                       0, stream, static_cast<const uint16_t*>(p.k), p.k_row_stride, p.slots,
                       p.num_tokens, p.cache, p.num_pages * (int64_t)p.block_size,
-                      p.page_stride, p.block_size, p.rope_dim, p.err_count);
+                      p.page_stride, p.block_size, log2_if_pow2(p.block_size), p.rope_dim,
+                      p.err_count);
 }
 
 template <int D>
@@ -269,7 +276,7 @@ cudaError_t mxfp4_insert_dispatch(const InsertParams& p, cudaStream_t stream) {
     return launch_pdl(mxfp4_insert_kernel<D, UNROLL>, dim3((unsigned)blocks), dim3(kThreads), 0,
                       stream, static_cast<const uint16_t*>(p.k), p.k_row_stride, p.slots,
                       p.num_tokens, p.cache, p.num_pages * (int64_t)p.block_size,
-                      p.page_stride, p.block_size, p.err_count);
+                      p.page_stride, p.block_size, log2_if_pow2(p.block_size), p.err_count);
 }
 
 }  // namespace

@@ -103,6 +103,7 @@ struct GatherParams {
     int64_t idx_stride;
     int64_t rows;
     int32_t cols;
+    int32_t block_shift;  // log2(block_size) or -1; set by the launcher
 };
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
@@ -170,6 +171,7 @@ struct RawGatherParams {
     const int32_t* cu_seq_lens;
     int32_t num_reqs;
     int64_t total_rows;
+    int32_t block_shift;  // log2(block_size) or -1; set by the launcher
 };
 
 cudaError_t launch_mxfp4_raw_gather(const RawGatherParams& p, cudaStream_t stream);

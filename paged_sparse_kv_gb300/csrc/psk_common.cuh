@@ -89,6 +89,43 @@ __device__ __forceinline__ int ceil_log2_pos(float q) {
     return e + ((b & 0x7FFFFFu) != 0u ? 1 : 0);
 }
 
+// ceil(log2(RN(a / c))) for c = cs * 2^cx with significand cs (mantissa bits
+// cs_mant), without dividing.  Write a = s * 2^x, s in [1, 2).  Then
+// a / c <= 2^k  <=>  s <= cs * 2^(k + cx - x), so the exact answer is
+// x - cx + (s > cs).  It equals the answer for the rounded quotient RN(a / c)
+// whenever a / c is either exactly a power of two or farther than half an ulp
+// from every power of two.  For c = 448 = 1.75 * 2^8 and c = 6 = 1.5 * 2^2 that
+// holds for every a with an 8-bit significand (a bf16 block amax: a / c is a
+// power of two exactly when s = cs, and otherwise at least ~0.4% away) and for
+// the 1e-4 floor.  a must be positive and normal; +inf gives 128 (as the
+// quotient inf would).
+__device__ __forceinline__ int ceil_log2_div_const(float a, uint32_t cs_mant, int cx) {
+    const uint32_t b = __float_as_uint(a);
+    if (b >= 0x7F800000u) return 128;
+    const int x = (int)(b >> 23) - 127;
+    return x - cx + ((b & 0x7FFFFFu) > cs_mant ? 1 : 0);
+}
+
+// Largest |x| of eight bf16 values (packed in a uint4) as the bf16 bit pattern
+// of the magnitude, zero-extended: for non-negative finite values the bit order
+// is the numeric order, so a 16-bit unsigned max is exact.
+__device__ __forceinline__ uint32_t absmax_bf16x8_bits(uint4 w) {
+    uint32_t m = __vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, w.z & 0x7FFF7FFFu);
+    m = __vmaxu2(m, w.w & 0x7FFF7FFFu);
+    return max(m & 0xFFFFu, m >> 16);
+}
+
+// {lo, hi} * {s, s} in one packed multiply (IEEE RN per element, no flush).
+__device__ __forceinline__ void mul2_rn(float& lo, float& hi, uint64_t s2) {
+    asm("{\n\t.reg .b64 x, y;\n\t"
+        "mov.b64 x, {%0, %1};\n\t"
+        "mul.rn.f32x2 y, x, %2;\n\t"
+        "mov.b64 {%0, %1}, y;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "l"(s2));
+}
+
 // Decode of a UE8M0 byte: 2^(b - 127) as binary32 (b = 255 -> +inf).
 __device__ __forceinline__ float ue8m0_scale(uint32_t b) {
     return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
@@ -189,6 +226,35 @@ __host__ __device__ __forceinline__ int log2_if_pow2(int x) {
     int s = 0;
     while ((1 << s) < x) ++s;
     return s;
+}
+
+// Quotient and remainder of v >= 0 by a page's block size bs.  shift =
+// log2_if_pow2(bs), computed once on the host: a shift and a mask when bs is
+// a power of two, else a 32-bit divide while v fits in 32 bits, else a 64-bit
+// one (an emulated 64-bit divide costs dozens of instructions per call).
+__device__ __forceinline__ int64_t div_block(int64_t v, int32_t bs, int32_t shift, int64_t& rem) {
+    if (shift >= 0) {
+        rem = v & (int64_t)(bs - 1);
+        return v >> shift;
+    }
+    if ((uint64_t)v <= 0xFFFFFFFFull) {
+        const uint32_t q = (uint32_t)v / (uint32_t)bs;
+        rem = (int64_t)((uint32_t)v - q * (uint32_t)bs);
+        return (int64_t)q;
+    }
+    const int64_t q = v / bs;
+    rem = v - q * bs;
+    return q;
+}
+
+__device__ __forceinline__ int32_t div_block32(int32_t v, int32_t bs, int32_t shift, int32_t& rem) {
+    if (shift >= 0) {
+        rem = v & (bs - 1);
+        return v >> shift;
+    }
+    const uint32_t q = (uint32_t)v / (uint32_t)bs;
+    rem = (int32_t)((uint32_t)v - q * (uint32_t)bs);
+    return (int32_t)q;
 }
 
 }  // namespace psk

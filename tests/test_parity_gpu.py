@@ -141,13 +141,15 @@ def test_mxfp4_insert_matches_oracle(cuda_device, name):
     assert int(err.item()) == n_err
 
 
+@pytest.mark.parametrize("bs", [16, 12])
 @pytest.mark.parametrize("D,rope,ue8m0", [(64, 0, True), (128, 0, True), (256, 128, True),
                                           (512, 64, False), (1024, 64, True)])
-def test_fp8_insert_shapes_strides_and_skips(cuda_device, D, rope, ue8m0):
+def test_fp8_insert_shapes_strides_and_skips(cuda_device, D, rope, ue8m0, bs):
     """Ragged token count, a k with extra rows and a wider row stride,
-    negative and out-of-range slots (counted), all head_dim variants."""
+    negative and out-of-range slots (counted), all head_dim variants; a
+    power-of-two and an odd block size."""
     rng = np.random.default_rng(D + rope)
-    N, bs, pages = 203, 16, 20
+    N, pages = 203, 20
     rows = rng.standard_normal((N + 5, D + 24)).astype(np.float32) * 3
     k = torch.from_numpy(rows).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     slots = rng.permutation(pages * bs)[:N].astype(np.int64)
@@ -168,10 +170,11 @@ def test_fp8_insert_shapes_strides_and_skips(cuda_device, D, rope, ue8m0):
     assert int(err.item()) == n_err == 2
 
 
+@pytest.mark.parametrize("bs", [8, 7])
 @pytest.mark.parametrize("D", [32, 64, 128, 256, 512, 1024])
-def test_mxfp4_insert_shapes_and_skips(cuda_device, D):
+def test_mxfp4_insert_shapes_and_skips(cuda_device, D, bs):
     rng = np.random.default_rng(D)
-    N, bs, pages = 77, 8, 12
+    N, pages = 77, 12
     rows = rng.standard_normal((N, D)).astype(np.float32)
     rows[5] = 0.0
     k = torch.from_numpy(rows).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
@@ -298,14 +301,15 @@ def test_index_build_strided_views(cuda_device):
 
 # ---- gathers -------------------------------------------------------------------------
 
+@pytest.mark.parametrize("bs", [16, 5])
 @pytest.mark.parametrize("D,rope,ue8m0", [(512, 64, True), (128, 0, True), (512, 64, False),
                                           (256, 128, True), (64, 0, False)])
-def test_fp8_gather_random_records(cuda_device, D, rope, ue8m0):
+def test_fp8_gather_random_records(cuda_device, D, rope, ue8m0, bs):
     """Arbitrary record bytes (UE8M0: no NaN codes; scales 2^-127..2^127, so
     products hit bf16 subnormals and infinities); indices with -1 and
     out-of-range slots; ragged rows x columns; output as a strided view."""
     rng = np.random.default_rng(D * 3 + rope)
-    bs, pages = 16, 9
+    pages = 9
     rec = oracle.fp8_record_bytes(D, rope, ue8m0)
     geom = synthetic.CacheGeom(pages, bs, (bs * rec + 15) // 16 * 16)
     if ue8m0:
@@ -332,10 +336,11 @@ def test_fp8_gather_random_records(cuda_device, D, rope, ue8m0):
     assert np.all(got[:, 0] == seven) and np.all(got[:, Cc + 1] == seven)
 
 
+@pytest.mark.parametrize("bs", [8, 3])
 @pytest.mark.parametrize("D", [32, 64, 128, 256, 512, 1024])
-def test_mxfp4_gather_random_records(cuda_device, D):
+def test_mxfp4_gather_random_records(cuda_device, D, bs):
     rng = np.random.default_rng(D + 5)
-    bs, pages = 8, 11
+    pages = 11
     rec = D // 2 + D // 32
     geom = synthetic.CacheGeom(pages, bs, (bs * rec + 15) // 16 * 16)
     host = rng.integers(0, 256, size=(geom.num_pages, geom.page_stride), dtype=np.uint8)

@@ -37,7 +37,7 @@ def _free():
 @pytest.mark.parametrize("seed", range(16))
 def test_range_gather_fuzz(cuda_device, seed):
     rng = np.random.default_rng(500 + seed)
-    bs = int(rng.choice([1, 2, 4, 16, 64]))
+    bs = int(rng.choice([1, 2, 3, 4, 5, 16, 64]))
     D, rope = [(128, 0), (512, 64), (256, 64)][seed % 3]
     ue8m0 = bool(seed % 4)
     R, width, pages = int(rng.integers(1, 5)), 7, 13
@@ -148,10 +148,11 @@ def test_prefill_workspace_full_size(cuda_device):
     assert np.array_equal(_u16(ws), want)
 
 
+@pytest.mark.parametrize("bs", [8, 6])
 @pytest.mark.parametrize("D", [64, 128, 256])
-def test_mxfp4_raw_gather_fuzz(cuda_device, D):
+def test_mxfp4_raw_gather_fuzz(cuda_device, D, bs):
     rng = np.random.default_rng(D)
-    bs, pages, R = 8, 17, 5
+    pages, R = 17, 5
     rec = D // 2 + D // 32
     geom = synthetic.CacheGeom(pages, bs, (bs * rec + 15) // 16 * 16)
     cache = rng.integers(0, 256, size=(pages, geom.page_stride), dtype=np.uint8)
