@@ -175,6 +175,15 @@ fp8_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
     }
 }
 
+// Lanes per token of the MXFP4 insert: two 16-byte chunks per lane where the
+// row allows it (halving the per-token slot, address and branch work of one
+// chunk per lane), at least the 4 lanes of one 32-element block.
+template <int D>
+__host__ __device__ constexpr int mxfp4_lanes() {
+    constexpr int half = D / 16;
+    return half < 4 ? 4 : (half > kWarp ? kWarp : half);
+}
+
 template <int D, int UNROLL>
 __global__ void __launch_bounds__(kThreads)
 mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
@@ -182,10 +191,10 @@ mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
                     uint8_t* __restrict__ cache, int64_t capacity, int64_t page_stride,
                     int32_t bs, int32_t shift, int32_t* __restrict__ err) {
     constexpr int CHUNKS = D / 8;
-    constexpr int LANES = CHUNKS < kWarp ? CHUNKS : kWarp;
+    constexpr int LANES = mxfp4_lanes<D>();
     constexpr int CPL = CHUNKS / LANES;
     constexpr int VB = D / 2;   // value bytes per token
-    constexpr int SB = D / 32;  // scale bytes per token
+    static_assert(CPL * LANES == CHUNKS && LANES % 4 == 0, "a block spans 4 lanes");
 
     const int lane = threadIdx.x & 31;
     const int grp = lane / LANES, gl = lane % LANES;
@@ -222,9 +231,8 @@ mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
         const int64_t page = div_block(sl, bs, shift, off);
         uint8_t* base = cache + page * page_stride;
         uint8_t* vals = base + off * VB;
-        uint8_t* scl = base + (int64_t)bs * VB + off * SB;
+        uint8_t* scl = base + (int64_t)bs * VB + off * (D / 32);
 
-        uint32_t sb[CPL];
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
             const int c = gl + i * LANES;
@@ -236,7 +244,6 @@ mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
             amb = max(amb, __shfl_xor_sync(gmask, amb, 2));
             const float a = fmaxf(__uint_as_float(amb << 16), 1.0e-4f);
             const int e = ceil_log2_div_const(a, 0x400000u, 2);  // / 6
-            const int b = min(max(e + 127, 0), 254);
             const uint64_t pw2 = splat_f32x2(exp2_int(-e));
             uint32_t word = 0;
 #pragma unroll
@@ -246,9 +253,9 @@ mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
                 word |= (cvt_e2m1x2(lo, hi) & 0xFFu) << (8 * j);
             }
             *reinterpret_cast<uint32_t*>(vals + 4 * c) = word;
-            sb[i] = (uint32_t)b;
+            // the block's first lane writes its scale byte
+            if ((gl & 3) == 0) scl[c / 4] = (uint8_t)min(max(e + 127, 0), 254);
         }
-        store_scale_bytes<LANES, CPL, 4>(sb, gmask, grp, gl, scl);
     }
 }
 
@@ -269,7 +276,7 @@ cudaError_t fp8_insert_dispatch(const InsertParams& p, cudaStream_t stream) {
 template <int D>
 cudaError_t mxfp4_insert_dispatch(const InsertParams& p, cudaStream_t stream) {
     constexpr int UNROLL = 2;
-    constexpr int LANES = (D / 8) < kWarp ? (D / 8) : kWarp;
+    constexpr int LANES = mxfp4_lanes<D>();
     const int64_t groups = (p.num_tokens + UNROLL - 1) / UNROLL;
     const int64_t threads = groups * LANES;
     const int64_t blocks = (threads + kThreads - 1) / kThreads;
