@@ -41,6 +41,9 @@ namespace {
 #ifndef PSK_WS_INDEX_MAX_PASSES
 #define PSK_WS_INDEX_MAX_PASSES 2
 #endif
+#ifndef PSK_INDEX_MIN_CTAS
+#define PSK_INDEX_MIN_CTAS 3
+#endif
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / kWarp;
@@ -51,44 +54,58 @@ struct TableRow {
     int32_t width;
     int32_t base;
     int32_t bs;
-    int32_t shift;  // log2(bs) or -1
+    int32_t shift;  // log2(bs) (POW2 kernels)
     int32_t maxp;   // INT32_MAX / bs: largest page whose slots can fit in int32
     int32_t maxrem; // INT32_MAX % bs
 };
-
-__device__ __forceinline__ void table_limits(TableRow& tr) {
-    tr.maxp = INT_MAX / tr.bs;
-    tr.maxrem = INT_MAX % tr.bs;
-}
 
 // Slot of logical position p (0 <= p <= INT32_MAX) through one block-table
 // row, or -1: logical page p / bs - base outside [0, width), a negative page,
 // or a slot beyond INT32_MAX.  All 32-bit: q - base is formed modulo 2^32 and
 // tested as unsigned against width; it wraps only when the true logical page
 // is >= 2^31 (q >= 0, base >= -2^31), and then the wrapped value is negative,
-// i.e. rejected, as the true one would be.
-template <bool SHARED>
+// i.e. rejected, as the true one would be.  POW2 (bs = 2^shift): a page
+// p <= maxp = INT32_MAX >> shift gives page * bs + rem <= INT32_MAX for every
+// rem < bs, so one unsigned compare rejects both negative and too-large pages.
+template <bool SHARED, bool POW2>
 __device__ __forceinline__ int32_t map_slot(const TableRow& tr, int32_t p) {
     int32_t q, rem;
-    if (tr.shift >= 0) {
+    if (POW2) {
         q = p >> tr.shift;
-        rem = p & ((1 << tr.shift) - 1);
+        rem = p & (tr.bs - 1);
     } else {
-        q = p / tr.bs;
+        q = (int32_t)((uint32_t)p / (uint32_t)tr.bs);
         rem = p - q * tr.bs;
     }
     const uint32_t lp = (uint32_t)q - (uint32_t)tr.base;
     if (lp >= (uint32_t)tr.width) return -1;
     const int32_t page = SHARED ? tr.row[lp] : __ldg(tr.row + lp);
+    if (POW2) return (uint32_t)page > (uint32_t)tr.maxp ? -1 : ((page << tr.shift) | rem);
     if ((uint32_t)page > (uint32_t)tr.maxp || (page == tr.maxp && rem > tr.maxrem)) return -1;
     return page * tr.bs + rem;
 }
 
+// The same rule for any position p >= 0 (window positions past INT32_MAX,
+// which only metadata whose tokens lie outside their request's query range
+// can produce).
+__device__ __forceinline__ int32_t map_slot_wide(const TableRow& tr, int64_t p) {
+    const int64_t q = p / tr.bs;
+    const int64_t lp = q - tr.base;
+    if (lp < 0 || lp >= tr.width) return -1;
+    const int32_t page = __ldg(tr.row + lp);  // a global row
+    if (page < 0) return -1;
+    const int64_t s = (int64_t)page * tr.bs + (p - q * tr.bs);
+    return s > 0x7FFFFFFFll ? -1 : (int32_t)s;
+}
+
 // Per-token values that depend on its request (second memory round trip).
+// Window columns c < nwin hold positions lo + c <= pos.
 struct TokMeta {
     int32_t r;
     bool ok;
-    int64_t pos, lo;
+    bool wide;  // pos > INT32_MAX: window slots through map_slot_wide
+    int32_t nwin;
+    int64_t lo;
     int32_t swa_base, comp_base;
 };
 
@@ -97,7 +114,9 @@ __device__ __forceinline__ TokMeta load_meta(const IndexParams& p, int64_t t, in
     TokMeta m;
     m.r = r;
     m.ok = (p.valid == nullptr || __ldg(p.valid + t) != 0) && r >= 0 && r < p.num_reqs;
-    m.pos = m.lo = 0;
+    m.lo = 0;
+    m.nwin = 0;
+    m.wide = false;
     m.swa_base = m.comp_base = 0;
     if (!m.ok) return m;
     m.comp_base = p.comp_base ? __ldg(p.comp_base + r) : 0;
@@ -105,12 +124,15 @@ __device__ __forceinline__ TokMeta load_meta(const IndexParams& p, int64_t t, in
         m.swa_base = p.swa_base ? __ldg(p.swa_base + r) : 0;
         const int64_t qs = __ldg(p.qsl + r);
         const int64_t qe = __ldg(p.qsl + r + 1);
-        m.pos = (int64_t)__ldg(p.seq_lens + r) - (qe - qs) + (t - qs);
-        int64_t lo = m.pos - p.window + 1;
+        const int64_t pos = (int64_t)__ldg(p.seq_lens + r) - (qe - qs) + (t - qs);
+        int64_t lo = pos - p.window + 1;
         const int64_t rs = p.replay ? (int64_t)__ldg(p.replay + r) : 0;
         if (rs > lo) lo = rs;
         if (lo < 0) lo = 0;
         m.lo = lo;
+        const int64_t n = pos - lo + 1;  // <= window
+        m.nwin = n > 0 ? (int32_t)n : 0;
+        m.wide = pos > 0x7FFFFFFFll;
     }
     return m;
 }
@@ -122,10 +144,35 @@ __device__ __forceinline__ int4 load_topk_quad(const IndexParams& p, const int32
                      j0 + 2 < p.topk ? __ldg(tk + j0 + 2) : -1, -1);
 }
 
+// Token t's row when its window positions pass INT32_MAX: one column per
+// lane step, window slots through the 64-bit rule, both rows in global memory.
+template <bool POW2>
+__device__ __noinline__ int build_row_wide(const IndexParams& p, int64_t t, const TokMeta& m,
+                                           int first, int stride, TableRow swa, TableRow comp) {
+    int32_t* out = p.out + t * p.out_stride;
+    const int32_t* tk = p.topk_local + t * p.topk_stride;
+    swa.row = p.swa_bt + (int64_t)m.r * p.swa_stride;
+    comp.row = p.comp_bt + (int64_t)m.r * p.comp_stride;
+    int cnt = 0;
+    for (int c = first; c < p.out_cols; c += stride) {
+        int v;
+        if (c < p.window) {
+            v = c < m.nwin ? map_slot_wide(swa, m.lo + c) : -1;
+        } else {
+            const int j = c - p.window;
+            const int l = j < p.topk ? __ldg(tk + j) : -1;
+            v = l >= 0 ? map_slot<false, POW2>(comp, l) : -1;
+        }
+        cnt += v >= 0;
+        out[c] = v;
+    }
+    return cnt;
+}
+
 // Writes token t's row and returns this lane's count of valid entries.
 // `pre` holds the lane's first batch of top-k quads, loaded in advance (VEC).
 // STAGED: the token's table rows are in shared memory (else read through L1).
-template <bool HAS_SWA, bool VEC, bool STAGED>
+template <bool HAS_SWA, bool VEC, bool POW2, bool STAGED>
 __device__ __forceinline__ int build_row(const IndexParams& p, int64_t t, const TokMeta& m,
                                          int first, int stride, const int4 (&pre)[PSK_INDEX_BATCH],
                                          const int32_t* s_swa, const int32_t* s_comp) {
@@ -152,7 +199,8 @@ __device__ __forceinline__ int build_row(const IndexParams& p, int64_t t, const 
     comp.base = m.comp_base;
     comp.bs = p.comp_bs;
     comp.shift = p.comp_shift;
-    table_limits(comp);
+    comp.maxp = p.comp_maxp;
+    comp.maxrem = p.comp_maxrem;
     TableRow swa;
     if (HAS_SWA) {
         swa.row = STAGED ? s_swa : p.swa_bt + (int64_t)m.r * p.swa_stride;
@@ -160,10 +208,12 @@ __device__ __forceinline__ int build_row(const IndexParams& p, int64_t t, const 
         swa.base = m.swa_base;
         swa.bs = p.swa_bs;
         swa.shift = p.swa_shift;
-        table_limits(swa);
+        swa.maxp = p.swa_maxp;
+        swa.maxrem = p.swa_maxrem;
     }
     const int32_t* tk = p.topk_local + t * p.topk_stride;
     const int W = HAS_SWA ? p.window : 0;
+    if (HAS_SWA && m.wide) return build_row_wide<POW2>(p, t, m, first, stride, swa, comp);
 
     int cnt = 0;
     if (VEC) {
@@ -188,17 +238,16 @@ __device__ __forceinline__ int build_row(const IndexParams& p, int64_t t, const 
                 const int c0 = 4 * q;
                 int v[4];
                 if (HAS_SWA && c0 < W) {
+                    const int32_t lo = (int32_t)m.lo;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int64_t ps = m.lo + c0 + e;
-                        v[e] = ps <= m.pos ? map_slot<STAGED>(swa, (int32_t)ps) : -1;
-                    }
+                    for (int e = 0; e < 4; ++e)
+                        v[e] = c0 + e < m.nwin ? map_slot<STAGED, POW2>(swa, lo + c0 + e) : -1;
                 } else {
                     const int4 w = L[u];
-                    v[0] = w.x >= 0 ? map_slot<STAGED>(comp, w.x) : -1;
-                    v[1] = w.y >= 0 ? map_slot<STAGED>(comp, w.y) : -1;
-                    v[2] = w.z >= 0 ? map_slot<STAGED>(comp, w.z) : -1;
-                    v[3] = w.w >= 0 ? map_slot<STAGED>(comp, w.w) : -1;
+                    v[0] = w.x >= 0 ? map_slot<STAGED, POW2>(comp, w.x) : -1;
+                    v[1] = w.y >= 0 ? map_slot<STAGED, POW2>(comp, w.y) : -1;
+                    v[2] = w.z >= 0 ? map_slot<STAGED, POW2>(comp, w.z) : -1;
+                    v[3] = w.w >= 0 ? map_slot<STAGED, POW2>(comp, w.w) : -1;
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) cnt += v[e] >= 0;
@@ -215,12 +264,11 @@ __device__ __forceinline__ int build_row(const IndexParams& p, int64_t t, const 
         for (int c = first; c < p.out_cols; c += stride) {
             int v;
             if (HAS_SWA && c < W) {
-                const int64_t ps = m.lo + c;
-                v = ps <= m.pos ? map_slot<STAGED>(swa, (int32_t)ps) : -1;
+                v = c < m.nwin ? map_slot<STAGED, POW2>(swa, (int32_t)m.lo + c) : -1;
             } else {
                 const int j = c - W;
                 const int l = j < p.topk ? __ldg(tk + j) : -1;
-                v = l >= 0 ? map_slot<STAGED>(comp, l) : -1;
+                v = l >= 0 ? map_slot<STAGED, POW2>(comp, l) : -1;
             }
             cnt += v >= 0;
             out[c] = v;
@@ -260,8 +308,8 @@ __device__ __forceinline__ void stage_row(int32_t* dst, const int32_t* src, int 
     }
 }
 
-template <bool HAS_SWA, bool VEC>
-__global__ void __launch_bounds__(kThreads, 3) index_build_kernel(IndexParams p) {
+template <bool HAS_SWA, bool VEC, bool POW2>
+__global__ void __launch_bounds__(kThreads, PSK_INDEX_MIN_CTAS) index_build_kernel(IndexParams p) {
     extern __shared__ int32_t s_tab[];  // [stage_comp] compressed row, then [stage_swa] SWA row
     __shared__ int s_cnt[kWarps];
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
@@ -313,9 +361,9 @@ __global__ void __launch_bounds__(kThreads, 3) index_build_kernel(IndexParams p)
                 load_first_batch<VEC>(p, t, t1, first, stride, W, pre);
             }
             if (staged >= 0 && m.r == staged)
-                cnt = build_row<HAS_SWA, VEC, true>(p, t, m, first, stride, pre, s_swa, s_comp);
+                cnt = build_row<HAS_SWA, VEC, POW2, true>(p, t, m, first, stride, pre, s_swa, s_comp);
             else
-                cnt = build_row<HAS_SWA, VEC, false>(p, t, m, first, stride, pre, s_swa, s_comp);
+                cnt = build_row<HAS_SWA, VEC, POW2, false>(p, t, m, first, stride, pre, s_swa, s_comp);
         }
         cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
         if (wpt == 1) {
@@ -508,11 +556,25 @@ cudaError_t launch_index_build(IndexParams p, bool has_swa, cudaStream_t stream)
     const int64_t blocks = (T + p.tokens_per_cta - 1) / p.tokens_per_cta;
     const size_t smem = (size_t)(p.stage_comp + p.stage_swa) * sizeof(int32_t);
 
+    p.comp_maxp = INT_MAX / p.comp_bs;
+    p.comp_maxrem = INT_MAX % p.comp_bs;
+    if (has_swa) {
+        p.swa_maxp = INT_MAX / p.swa_bs;
+        p.swa_maxrem = INT_MAX % p.swa_bs;
+    }
+
     const bool vec = ((reinterpret_cast<uintptr_t>(p.out) & 15) == 0) && (p.out_stride % 4 == 0) &&
                      ((reinterpret_cast<uintptr_t>(p.topk_local) & 15) == 0) &&
                      (p.topk_stride % 4 == 0) && (!has_swa || p.window % 4 == 0);
-    auto kern = has_swa ? (vec ? index_build_kernel<true, true> : index_build_kernel<true, false>)
-                        : (vec ? index_build_kernel<false, true> : index_build_kernel<false, false>);
+    const bool pow2 = p.comp_shift >= 0 && (!has_swa || p.swa_shift >= 0);
+    void (*kern)(IndexParams);
+    if (has_swa) {
+        if (vec) kern = pow2 ? index_build_kernel<true, true, true> : index_build_kernel<true, true, false>;
+        else kern = pow2 ? index_build_kernel<true, false, true> : index_build_kernel<true, false, false>;
+    } else {
+        if (vec) kern = pow2 ? index_build_kernel<false, true, true> : index_build_kernel<false, true, false>;
+        else kern = pow2 ? index_build_kernel<false, false, true> : index_build_kernel<false, false, false>;
+    }
     return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p);
 }
 

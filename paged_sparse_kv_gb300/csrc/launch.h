@@ -82,6 +82,8 @@ struct IndexParams {
     int32_t warps_per_token;
     int32_t stage_comp;  // entries of the compressed row staged in shared memory
     int32_t stage_swa;   // entries of the SWA row staged in shared memory
+    int32_t swa_maxp, swa_maxrem;    // INT32_MAX / swa_bs, INT32_MAX % swa_bs
+    int32_t comp_maxp, comp_maxrem;  // the same for comp_bs
 };
 
 // has_swa = true: the fused window + top-k build; false: top-k mapping only.
