@@ -11,7 +11,8 @@ U[1024, 8192], head_dim 512 = 448 fp8 + 64 bf16 rope, page 64, window 128,
 top-k 512).
 
 Timing: W untimed warm-up steps, then K steps, each preceded by an L2 flush
-(a 512 MiB memset, outside the timed events) and bracketed by CUDA events on
+(a 512 MiB memset, then a 256 MiB read so no dirty line of the memset is left
+to write back; outside the timed events) and bracketed by CUDA events on
 the launching stream; per-kernel events give each kernel's average duration.
 `value` is query tokens per second over all ranks (weak scaling: every rank
 runs its own full batch).  `e2e` repeats the step through the public API with
@@ -331,11 +332,11 @@ def main():
         raise SystemExit("the workspace path needs a workload with an FP8 part")
     launches = p.workspace_launches() if path == "workspace" else p.launches()
     names = [n for n, _ in launches]
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         p.step(concurrent=True, path=path)
     torch.cuda.synchronize(dev)
 
@@ -359,7 +360,7 @@ def main():
         evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(names) + 1)]
         g_ser = _capture(torch, dev, stream, lambda: _instrumented(launches, names, evs))
         for _ in range(max(5, min(args.steps, 30))):
-            flush.zero_()
+            flush()
             g_ser.replay()
             torch.cuda.synchronize(dev)
             for i, n in enumerate(names):
@@ -368,7 +369,7 @@ def main():
     else:
         for _ in range(max(5, min(args.steps, 30))):
             evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
-            flush.zero_()
+            flush()
             _instrumented(launches, names, evs)
             torch.cuda.synchronize(dev)
             for i, n in enumerate(names):
@@ -392,9 +393,9 @@ def main():
         g_inst = _capture(torch, dev, stream,
                           lambda: p.step(concurrent=True, hooks=hooks, path=path))
         for _ in range(args.warmup):
-            flush.zero_()
+            flush()
             g_plain.replay()
-            flush.zero_()
+            flush()
             g_inst.replay()
         torch.cuda.synchronize(dev)
     if dist:
@@ -404,14 +405,14 @@ def main():
     t_wall0 = time.perf_counter()
     step_ms, top_ms = [], []
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         t_start.record(stream)
         if g_plain is not None:
             g_plain.replay()
         else:
             p.step(concurrent=True, path=path)
         t_end.record(stream)
-        flush.zero_()
+        flush()
         if g_inst is not None:
             g_inst.replay()
         else:
@@ -468,7 +469,8 @@ def main():
                                f"head_dim {w.head_dim} (rope {w.rope_dim}), window {w.window}, "
                                f"top-k {w.topk}, ratio {w.compress_ratio}",
                    "path": path,
-                   "seed": w.seed, "l2": "flushed before every step (512 MiB memset)",
+                   "seed": w.seed, "l2": ("flushed before every step: 512 MiB memset, then a 256 MiB read so "
+                         "the lines left in L2 are clean"),
                    "parallelism": f"dp{world} (independent batch per GPU)",
                    "launch": ("cuda graph of the step on three streams" if g_plain is not None
                               else "eager, three streams"),
@@ -496,6 +498,21 @@ def main():
         dist.destroy_process_group()
 
 
+class L2Flush:
+    """Evicts the step's data from L2 (129 MB) between timed steps: a 512 MiB
+    memset, then a 256 MiB read of another buffer.  After the memset alone L2
+    would hold dirty lines whose write-back the next step would pay for; the
+    read replaces them with clean ones."""
+
+    def __init__(self, torch, dev):
+        self.w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.amax()
+
+
 def run_e2e(p, args, dev, flush, path="index"):
     """The step through the public API with pinned host inputs and outputs."""
     import torch
@@ -512,7 +529,7 @@ def run_e2e(p, args, dev, flush, path="index"):
     d2h = sum(t.numel() * t.element_size() for t in h_out)
     times = []
     for s in range(args.warmup + args.steps):
-        flush.zero_()
+        flush()
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         for d, h in zip(ins, h_in):

@@ -87,11 +87,12 @@ int32_t psk_abi_version(void);
 
 /*
  * psk_device_wait_timeouts -- diagnostic of the pipelined kernels.
- * Kernels that wait on shared-memory barriers (the TMA-fed gather) bound every
- * wait to 2 s of wall time; a wait that expires is counted in a per-device
- * counter, the kernel stops its remaining work instead of hanging, and the
- * output of that launch is incomplete.  This call copies the current device's
- * counter (0 in normal operation) into *count.  Synchronous (it waits for the
+ * Kernels that wait on shared-memory barriers (the TMA-fed gather and the
+ * index builders that stage top-k rows by bulk copies) bound every wait to
+ * 2 s of wall time; a wait that expires is counted in a per-device counter,
+ * the kernel stops its remaining work instead of hanging, and the output of
+ * that launch is incomplete.  This call copies the current device's count
+ * (the sum over those kernels; 0 in normal operation) into *count.  Synchronous (it waits for the
  * device); returns PSK_ERR_CUDA if the copy fails.
  */
 psk_status psk_device_wait_timeouts(uint32_t* count);

@@ -79,7 +79,13 @@ int32_t psk_abi_version(void) { return 1; }
 
 psk_status psk_device_wait_timeouts(uint32_t* count) {
     CHECK(count != nullptr, "count must be non-null");
-    return cuda_status(psk::read_wait_timeouts(count), "reading the wait-timeout counter");
+    uint32_t gather = 0, index = 0;
+    psk_status st = cuda_status(psk::read_wait_timeouts(&gather), "reading the wait-timeout counter");
+    if (st != PSK_OK) return st;
+    st = cuda_status(psk::read_index_wait_timeouts(&index), "reading the wait-timeout counter");
+    if (st != PSK_OK) return st;
+    *count = gather + index;
+    return PSK_OK;
 }
 
 psk_status quantize_and_insert_k_cache(const void* k, int64_t k_row_stride,

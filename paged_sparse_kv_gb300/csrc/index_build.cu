@@ -44,10 +44,19 @@ namespace {
 #ifndef PSK_INDEX_MIN_CTAS
 #define PSK_INDEX_MIN_CTAS 3
 #endif
+#ifndef PSK_INDEX_TMA_MIN_CTAS
+#define PSK_INDEX_TMA_MIN_CTAS 4
+#endif
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / kWarp;
 constexpr int kMaxStagedEntries = 4096;  // 16 KB of int32 page ids per staged row
+constexpr int kMaxTopkStageBytes = 64 * 1024;  // top-k rows of one CTA in shared memory
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Waits on the top-k staging barrier that gave up (2 s without the copies
+// landing); the rows of that CTA are left unwritten.
+__device__ unsigned int g_index_wait_timeouts = 0;
 
 struct TableRow {
     const int32_t* row;  // global row, or shared copy
@@ -277,6 +286,77 @@ __device__ __forceinline__ int build_row(const IndexParams& p, int64_t t, const 
     return cnt;
 }
 
+// Token t's row from its top-k row staged in shared memory (s_row; the TMA
+// kernels: VEC layout, topk % 4 == 0, so a quad is all top-k or all past it).
+template <bool HAS_SWA, bool POW2, bool STAGED>
+__device__ __forceinline__ int build_row_smem(const IndexParams& p, int64_t t, const TokMeta& m,
+                                              int first, int stride, const int32_t* s_row,
+                                              const int32_t* s_swa, const int32_t* s_comp) {
+    int32_t* out = p.out + t * p.out_stride;
+    const int nq = p.out_cols / 4;
+    if (!m.ok) {
+        for (int q = first; q < nq; q += stride)
+            *reinterpret_cast<int4*>(out + 4 * q) = make_int4(-1, -1, -1, -1);
+        return 0;
+    }
+    TableRow comp;
+    comp.row = STAGED ? s_comp : p.comp_bt + (int64_t)m.r * p.comp_stride;
+    comp.width = p.comp_width;
+    comp.base = m.comp_base;
+    comp.bs = p.comp_bs;
+    comp.shift = p.comp_shift;
+    comp.maxp = p.comp_maxp;
+    comp.maxrem = p.comp_maxrem;
+    TableRow swa;
+    if (HAS_SWA) {
+        swa.row = STAGED ? s_swa : p.swa_bt + (int64_t)m.r * p.swa_stride;
+        swa.width = p.swa_width;
+        swa.base = m.swa_base;
+        swa.bs = p.swa_bs;
+        swa.shift = p.swa_shift;
+        swa.maxp = p.swa_maxp;
+        swa.maxrem = p.swa_maxrem;
+    }
+    const int W = HAS_SWA ? p.window : 0;
+    if (HAS_SWA && m.wide) return build_row_wide<POW2>(p, t, m, first, stride, swa, comp);
+    int cnt = 0;
+#pragma unroll 2
+    for (int q = first; q < nq; q += stride) {
+        const int c0 = 4 * q;
+        int v[4];
+        if (HAS_SWA && c0 < W) {
+            const int32_t lo = (int32_t)m.lo;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                v[e] = c0 + e < m.nwin ? map_slot<STAGED, POW2>(swa, lo + c0 + e) : -1;
+        } else {
+            const int j0 = c0 - W;
+            const int4 w = j0 < p.topk ? *reinterpret_cast<const int4*>(s_row + j0)
+                                       : make_int4(-1, -1, -1, -1);
+            v[0] = w.x >= 0 ? map_slot<STAGED, POW2>(comp, w.x) : -1;
+            v[1] = w.y >= 0 ? map_slot<STAGED, POW2>(comp, w.y) : -1;
+            v[2] = w.z >= 0 ? map_slot<STAGED, POW2>(comp, w.z) : -1;
+            v[3] = w.w >= 0 ? map_slot<STAGED, POW2>(comp, w.w) : -1;
+        }
+        cnt += (v[0] >= 0) + (v[1] >= 0) + (v[2] >= 0) + (v[3] >= 0);
+        *reinterpret_cast<int4*>(out + c0) = make_int4(v[0], v[1], v[2], v[3]);
+    }
+    return cnt;
+}
+
+// Thread 0 of the CTA: one bulk copy per token row t0..t1-1 of topk_local
+// into `dst` (rows of `words` int32), all completing on `bar`.  Returns the
+// bytes expected.  Every address and size is a multiple of 16 bytes (16-byte
+// aligned topk_local, topk_stride and topk multiples of 4).
+__device__ __forceinline__ void stage_topk_rows(int32_t* dst, const int32_t* topk_local,
+                                                int64_t topk_stride, int words, int64_t t0,
+                                                int64_t t1, uint64_t* bar) {
+    const uint32_t bytes = (uint32_t)words * 4u;
+    mbar_arrive_expect_tx(bar, bytes * (uint32_t)(t1 - t0));
+    for (int64_t t = t0; t < t1; ++t)
+        bulk_g2s(dst + (t - t0) * words, topk_local + t * topk_stride, bytes, bar);
+}
+
 // Loads the lane's first batch of top-k quads of token t (depends on t only).
 template <bool VEC>
 __device__ __forceinline__ void load_first_batch(const IndexParams& p, int64_t t, int64_t t1,
@@ -308,10 +388,14 @@ __device__ __forceinline__ void stage_row(int32_t* dst, const int32_t* src, int 
     }
 }
 
-template <bool HAS_SWA, bool VEC, bool POW2>
-__global__ void __launch_bounds__(kThreads, PSK_INDEX_MIN_CTAS) index_build_kernel(IndexParams p) {
-    extern __shared__ int32_t s_tab[];  // [stage_comp] compressed row, then [stage_swa] SWA row
+template <bool HAS_SWA, bool VEC, bool POW2, bool TMA>
+__global__ void __launch_bounds__(kThreads, TMA ? PSK_INDEX_TMA_MIN_CTAS : PSK_INDEX_MIN_CTAS)
+index_build_kernel(IndexParams p) {
+    // Dynamic shared memory: [TMA: tokens_per_cta top-k rows][compressed
+    // table row][SWA table row].
+    extern __shared__ __align__(16) int32_t s_dyn[];
     __shared__ int s_cnt[kWarps];
+    __shared__ __align__(8) uint64_t s_bar;
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int64_t t0 = (int64_t)blockIdx.x * p.tokens_per_cta;
     int64_t t1 = t0 + p.tokens_per_cta;
@@ -323,17 +407,29 @@ __global__ void __launch_bounds__(kThreads, PSK_INDEX_MIN_CTAS) index_build_kern
     const int first = slice * kWarp + lane;
     const int stride = wpt * kWarp;
     const int W = HAS_SWA ? p.window : 0;
+    const bool copy_topk = TMA && p.topk > 0;
+    int32_t* s_topk = s_dyn;
+    int32_t* s_comp = s_dyn + (TMA ? p.tokens_per_cta * p.topk : 0);
+    int32_t* s_swa = s_comp + p.stage_comp;
+    if (TMA && threadIdx.x == 0) {
+        mbar_init(&s_bar, 1);
+        mbar_fence_init();
+    }
+    if (TMA) __syncthreads();
     pdl_wait();
     pdl_launch_dependents();
 
-    // Round 1: loads that depend only on token indices.
+    // Round 1: loads that depend only on token indices (TMA: the CTA's
+    // top-k rows, in flight while the metadata arrives).
+    if (copy_topk && threadIdx.x == 0)
+        stage_topk_rows(s_topk, p.topk_local, p.topk_stride, p.topk, t0, t1, &s_bar);
     const int32_t r0 = __ldg(p.t2r + t0);
     const int32_t r1 = __ldg(p.t2r + t1 - 1);
     const int64_t tf = t0 + tslot;  // this warp's first token
     int32_t rf = -1;
     int4 pre[PSK_INDEX_BATCH];
     if (tf < t1) rf = __ldg(p.t2r + tf);
-    load_first_batch<VEC>(p, tf, t1, first, stride, W, pre);
+    if (!TMA) load_first_batch<VEC>(p, tf, t1, first, stride, W, pre);
     // Round 2: the first token's request metadata and, when the tile is one
     // request, its block-table rows into shared memory.
     TokMeta mf;
@@ -341,37 +437,48 @@ __global__ void __launch_bounds__(kThreads, PSK_INDEX_MIN_CTAS) index_build_kern
     // Stage only when every row the tile needs fits (p.stage_* > 0 exactly then).
     const bool fits = p.stage_comp > 0 && (!HAS_SWA || p.stage_swa > 0);
     const int32_t staged = (fits && r0 == r1 && r0 >= 0 && r0 < p.num_reqs) ? r0 : -1;
-    int32_t* s_comp = s_tab;
-    int32_t* s_swa = s_tab + p.stage_comp;
     if (staged >= 0) {
         stage_row(s_comp, p.comp_bt + (int64_t)staged * p.comp_stride, p.stage_comp);
         if (HAS_SWA) stage_row(s_swa, p.swa_bt + (int64_t)staged * p.swa_stride, p.stage_swa);
     }
     __syncthreads();
+    bool rows_ok = true;
+    if (copy_topk) {
+        rows_ok = mbar_wait_bounded(&s_bar, 0, kWaitLimitNs);
+        if (!rows_ok && lane == 0) atomicAdd(&g_index_wait_timeouts, 1u);
+    }
 
     for (int64_t tb = t0; tb < t1; tb += tpp) {
         const int64_t t = tb + tslot;
         int cnt = 0;
-        if (t < t1) {
+        if (t < t1 && rows_ok) {
             TokMeta m;
             if (tb == t0) {
                 m = mf;
             } else {
                 m = load_meta<HAS_SWA>(p, t, __ldg(p.t2r + t));
-                load_first_batch<VEC>(p, t, t1, first, stride, W, pre);
+                if (!TMA) load_first_batch<VEC>(p, t, t1, first, stride, W, pre);
             }
-            if (staged >= 0 && m.r == staged)
-                cnt = build_row<HAS_SWA, VEC, POW2, true>(p, t, m, first, stride, pre, s_swa, s_comp);
-            else
-                cnt = build_row<HAS_SWA, VEC, POW2, false>(p, t, m, first, stride, pre, s_swa, s_comp);
+            if (TMA) {
+                const int32_t* s_row = s_topk + (t - t0) * p.topk;
+                if (staged >= 0 && m.r == staged)
+                    cnt = build_row_smem<HAS_SWA, POW2, true>(p, t, m, first, stride, s_row, s_swa, s_comp);
+                else
+                    cnt = build_row_smem<HAS_SWA, POW2, false>(p, t, m, first, stride, s_row, s_swa, s_comp);
+            } else {
+                if (staged >= 0 && m.r == staged)
+                    cnt = build_row<HAS_SWA, VEC, POW2, true>(p, t, m, first, stride, pre, s_swa, s_comp);
+                else
+                    cnt = build_row<HAS_SWA, VEC, POW2, false>(p, t, m, first, stride, pre, s_swa, s_comp);
+            }
         }
         cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
         if (wpt == 1) {
-            if (lane == 0 && t < t1) p.lens[t] = cnt;
+            if (lane == 0 && t < t1 && rows_ok) p.lens[t] = cnt;
         } else {
             if (lane == 0) s_cnt[warp] = cnt;
             __syncthreads();
-            if (slice == 0 && lane == 0 && t < t1) {
+            if (slice == 0 && lane == 0 && t < t1 && rows_ok) {
                 int sum = 0;
                 for (int i = 0; i < wpt; ++i) sum += s_cnt[warp + i];
                 p.lens[t] = sum;
@@ -379,6 +486,9 @@ __global__ void __launch_bounds__(kThreads, PSK_INDEX_MIN_CTAS) index_build_kern
             __syncthreads();
         }
     }
+    // A CTA whose wait gave up must not retire with copies still landing in
+    // its shared memory: one more bounded wait.
+    if (copy_topk && !rows_ok && threadIdx.x == 0) mbar_wait_bounded(&s_bar, 0, kWaitLimitNs);
 }
 
 // ---- workspace-relative form ------------------------------------------------------
@@ -388,10 +498,32 @@ __global__ void __launch_bounds__(kThreads, PSK_INDEX_MIN_CTAS) index_build_kern
 // r * workspace_width, compressed entries at rows 0.., the gathered window
 // positions g0 = seq - gather_len .. seq - 1 at rows compressed_base...  No
 // table look-ups: every column is arithmetic on the token's metadata.
-template <bool VEC>
+// Workspace row of column c (top-k entry l_in for c >= W) for a token with
+// the given metadata, or -1.
+struct WsMeta {
+    bool ok;
+    int64_t pos, lo, g0, lc, rbase;
+};
+
+__device__ __forceinline__ int ws_col(const WorkspaceIndexParams& p, const WsMeta& m, int c,
+                                      int l_in) {
+    if (!m.ok) return -1;
+    int64_t v = -1;
+    if (c < p.window) {
+        const int64_t ps = m.lo + c;
+        if (ps <= m.pos && ps >= m.g0) v = m.rbase + p.compressed_base + (ps - m.g0);
+    } else if (c - p.window < p.topk) {
+        if (l_in >= 0 && l_in < m.lc) v = m.rbase + l_in;
+    }
+    return v > 0x7FFFFFFFll ? -1 : (int)v;
+}
+
+template <bool VEC, bool TMA>
 __global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceIndexParams p,
                                                                    int tokens_per_cta, int wpt) {
+    extern __shared__ __align__(16) int32_t s_dyn[];  // TMA: the CTA's top-k rows
     __shared__ int s_cnt[kWarps];
+    __shared__ __align__(8) uint64_t s_bar;
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int64_t t0 = (int64_t)blockIdx.x * tokens_per_cta;
     int64_t t1 = t0 + tokens_per_cta;
@@ -401,19 +533,29 @@ __global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceInde
     const int W = p.window;
     const int P = (p.topk + 3) / 4 * 4;
     const int cols = W + P;
+    const bool copy_topk = TMA && p.topk > 0;
+    if (TMA && threadIdx.x == 0) {
+        mbar_init(&s_bar, 1);
+        mbar_fence_init();
+    }
+    if (TMA) __syncthreads();
     pdl_wait();
     pdl_launch_dependents();
+    if (copy_topk && threadIdx.x == 0)
+        stage_topk_rows(s_dyn, p.topk_local, p.topk_stride, p.topk, t0, t1, &s_bar);
+    bool rows_ok = true;
     for (int64_t tb = t0; tb < t1; tb += tpp) {
         const int64_t t = tb + tslot;
-        int cnt = 0;
+        const int32_t* tk = p.topk_local + t * p.topk_stride;
+        // The first batch of top-k quads depends only on t: issue it first.
+        constexpr int kPre = PSK_WS_INDEX_BATCH;
+        int4 Lpre[kPre];
+        WsMeta m;
+        m.ok = false;
+        m.pos = m.lo = m.g0 = m.lc = m.rbase = 0;
         if (t < t1) {
-            int32_t* out = p.out + t * p.out_stride;
             const int32_t r = __ldg(p.t2r + t);
-            const int32_t* tk = p.topk_local + t * p.topk_stride;
-            // The first batch of top-k quads depends only on t: issue it now.
-            constexpr int kPre = PSK_WS_INDEX_BATCH;
-            int4 Lpre[kPre];
-            if (VEC) {
+            if (VEC && !TMA) {
 #pragma unroll
                 for (int u = 0; u < kPre; ++u) {
                     const int q = first + u * stride;
@@ -431,31 +573,41 @@ __global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceInde
                     }
                 }
             }
-            const bool ok = (p.valid == nullptr || __ldg(p.valid + t) != 0) && r >= 0 &&
-                            r < p.num_reqs;
-            int64_t pos = 0, lo = 0, g0 = 0, lc = 0, rbase = 0;
-            if (ok) {
+            m.ok = (p.valid == nullptr || __ldg(p.valid + t) != 0) && r >= 0 && r < p.num_reqs;
+            if (m.ok) {
                 const int64_t qs = __ldg(p.qsl + r), qe = __ldg(p.qsl + r + 1);
                 const int64_t seq = __ldg(p.seq_lens + r);
-                pos = seq - (qe - qs) + (t - qs);
-                g0 = seq - __ldg(p.gather_lens + r);
-                lc = seq / p.compress_ratio;
-                rbase = (int64_t)r * p.workspace_width;
-                lo = pos - W + 1;
-                if (lo < 0) lo = 0;
+                m.pos = seq - (qe - qs) + (t - qs);
+                m.g0 = seq - __ldg(p.gather_lens + r);
+                m.lc = seq / p.compress_ratio;
+                m.rbase = (int64_t)r * p.workspace_width;
+                m.lo = m.pos - W + 1;
+                if (m.lo < 0) m.lo = 0;
             }
-            auto col = [&](int c, int l_in) -> int {
-                if (!ok) return -1;
-                int64_t v = -1;
-                if (c < W) {
-                    const int64_t ps = lo + c;
-                    if (ps <= pos && ps >= g0) v = rbase + p.compressed_base + (ps - g0);
-                } else if (c - W < p.topk) {
-                    if (l_in >= 0 && l_in < lc) v = rbase + l_in;
+        }
+        if (copy_topk && tb == t0) {
+            rows_ok = mbar_wait_bounded(&s_bar, 0, kWaitLimitNs);
+            if (!rows_ok && lane == 0) atomicAdd(&g_index_wait_timeouts, 1u);
+        }
+        int cnt = 0;
+        if (t < t1 && rows_ok) {
+            int32_t* out = p.out + t * p.out_stride;
+            if (TMA) {
+                const int32_t* s_row = s_dyn + (t - t0) * p.topk;
+                const int nq = cols / 4;
+#pragma unroll 2
+                for (int q = first; q < nq; q += stride) {
+                    const int c0 = 4 * q;
+                    const int j0 = c0 - W;
+                    const int4 l = (j0 >= 0 && j0 < p.topk)
+                                       ? *reinterpret_cast<const int4*>(s_row + j0)
+                                       : make_int4(-1, -1, -1, -1);
+                    const int4 v = make_int4(ws_col(p, m, c0, l.x), ws_col(p, m, c0 + 1, l.y),
+                                             ws_col(p, m, c0 + 2, l.z), ws_col(p, m, c0 + 3, l.w));
+                    cnt += (v.x >= 0) + (v.y >= 0) + (v.z >= 0) + (v.w >= 0);
+                    *reinterpret_cast<int4*>(out + c0) = v;
                 }
-                return v > 0x7FFFFFFFll ? -1 : (int)v;
-            };
-            if (VEC) {
+            } else if (VEC) {
                 constexpr int kBatch = PSK_WS_INDEX_BATCH;
                 const int nq = cols / 4;
                 for (int qb = first; qb < nq; qb += kBatch * stride) {
@@ -484,16 +636,16 @@ __global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceInde
                         if (q >= nq) break;
                         const int c0 = 4 * q;
                         const int4 l = L[u];
-                        const int4 v = make_int4(col(c0, l.x), col(c0 + 1, l.y), col(c0 + 2, l.z),
-                                                 col(c0 + 3, l.w));
+                        const int4 v = make_int4(ws_col(p, m, c0, l.x), ws_col(p, m, c0 + 1, l.y),
+                                                 ws_col(p, m, c0 + 2, l.z), ws_col(p, m, c0 + 3, l.w));
                         cnt += (v.x >= 0) + (v.y >= 0) + (v.z >= 0) + (v.w >= 0);
                         *reinterpret_cast<int4*>(out + c0) = v;
                     }
                 }
             } else {
                 for (int c = first; c < cols; c += stride) {
-                    const int l = (ok && c >= W && c - W < p.topk) ? __ldg(tk + (c - W)) : -1;
-                    const int v = col(c, l);
+                    const int l = (m.ok && c >= W && c - W < p.topk) ? __ldg(tk + (c - W)) : -1;
+                    const int v = ws_col(p, m, c, l);
                     cnt += v >= 0;
                     out[c] = v;
                 }
@@ -501,11 +653,11 @@ __global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceInde
         }
         cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
         if (wpt == 1) {
-            if (lane == 0 && t < t1) p.lens[t] = cnt;
+            if (lane == 0 && t < t1 && rows_ok) p.lens[t] = cnt;
         } else {
             if (lane == 0) s_cnt[warp] = cnt;
             __syncthreads();
-            if (slice == 0 && lane == 0 && t < t1) {
+            if (slice == 0 && lane == 0 && t < t1 && rows_ok) {
                 int sum = 0;
                 for (int i = 0; i < wpt; ++i) sum += s_cnt[warp + i];
                 p.lens[t] = sum;
@@ -513,9 +665,22 @@ __global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceInde
             __syncthreads();
         }
     }
+    if (copy_topk && !rows_ok && threadIdx.x == 0) mbar_wait_bounded(&s_bar, 0, kWaitLimitNs);
+}
+
+// Raises a kernel's dynamic shared-memory limit when a launch needs more than
+// the default 48 KB (once per kernel and size class).
+template <typename Kern>
+cudaError_t allow_dynamic_smem(Kern kern, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
 }  // namespace
+
+cudaError_t read_index_wait_timeouts(uint32_t* count) {
+    return cudaMemcpyFromSymbol(count, g_index_wait_timeouts, sizeof(uint32_t));
+}
 
 cudaError_t launch_workspace_indices(const WorkspaceIndexParams& p, cudaStream_t stream) {
     const int sms = sm_count();
@@ -523,16 +688,23 @@ cudaError_t launch_workspace_indices(const WorkspaceIndexParams& p, cudaStream_t
     int wpt = 1;
     while (wpt < kWarps && T * wpt < (int64_t)sms * 16) wpt *= 2;
     const int tpp = kWarps / wpt;
-    int64_t passes = T / ((int64_t)tpp * 2 * sms);
-    if (passes < 1) passes = 1;
-    if (passes > PSK_WS_INDEX_MAX_PASSES) passes = PSK_WS_INDEX_MAX_PASSES;
-    const int tokens_per_cta = (int)(tpp * passes);
-    const int64_t blocks = (T + tokens_per_cta - 1) / tokens_per_cta;
     const bool vec = ((reinterpret_cast<uintptr_t>(p.out) & 15) == 0) && (p.out_stride % 4 == 0) &&
                      ((reinterpret_cast<uintptr_t>(p.topk_local) & 15) == 0) &&
                      (p.topk_stride % 4 == 0) && (p.window % 4 == 0);
-    auto kern = vec ? workspace_index_kernel<true> : workspace_index_kernel<false>;
-    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p, tokens_per_cta,
+    // Staged top-k rows: one pass of tpp tokens per CTA, whole 16-byte quads.
+    const bool tma = vec && p.topk % 4 == 0 && (int64_t)tpp * p.topk * 4 <= kMaxTopkStageBytes;
+    int64_t passes = T / ((int64_t)tpp * 2 * sms);
+    if (passes < 1) passes = 1;
+    if (passes > PSK_WS_INDEX_MAX_PASSES) passes = PSK_WS_INDEX_MAX_PASSES;
+    if (tma) passes = 1;
+    const int tokens_per_cta = (int)(tpp * passes);
+    const int64_t blocks = (T + tokens_per_cta - 1) / tokens_per_cta;
+    const size_t smem = tma ? (size_t)tokens_per_cta * p.topk * sizeof(int32_t) : 0;
+    auto kern = tma ? workspace_index_kernel<true, true>
+                    : (vec ? workspace_index_kernel<true, false> : workspace_index_kernel<false, false>);
+    const cudaError_t e = allow_dynamic_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p, tokens_per_cta,
                       wpt);
 }
 
@@ -554,8 +726,6 @@ cudaError_t launch_index_build(IndexParams p, bool has_swa, cudaStream_t stream)
     p.stage_swa = (has_swa && p.swa_width > 0 && p.swa_width <= kMaxStagedEntries) ? p.swa_width : 0;
     if (p.stage_comp == 0 || (has_swa && p.stage_swa == 0)) p.stage_comp = p.stage_swa = 0;
     const int64_t blocks = (T + p.tokens_per_cta - 1) / p.tokens_per_cta;
-    const size_t smem = (size_t)(p.stage_comp + p.stage_swa) * sizeof(int32_t);
-
     p.comp_maxp = INT_MAX / p.comp_bs;
     p.comp_maxrem = INT_MAX % p.comp_bs;
     if (has_swa) {
@@ -566,15 +736,28 @@ cudaError_t launch_index_build(IndexParams p, bool has_swa, cudaStream_t stream)
     const bool vec = ((reinterpret_cast<uintptr_t>(p.out) & 15) == 0) && (p.out_stride % 4 == 0) &&
                      ((reinterpret_cast<uintptr_t>(p.topk_local) & 15) == 0) &&
                      (p.topk_stride % 4 == 0) && (!has_swa || p.window % 4 == 0);
+    // Top-k rows staged by bulk copies: whole 16-byte quads, at most
+    // kMaxTopkStageBytes per CTA.
+    const bool tma = vec && p.topk % 4 == 0 &&
+                     (int64_t)p.tokens_per_cta * p.topk * 4 <= kMaxTopkStageBytes;
     const bool pow2 = p.comp_shift >= 0 && (!has_swa || p.swa_shift >= 0);
-    void (*kern)(IndexParams);
-    if (has_swa) {
-        if (vec) kern = pow2 ? index_build_kernel<true, true, true> : index_build_kernel<true, true, false>;
-        else kern = pow2 ? index_build_kernel<true, false, true> : index_build_kernel<true, false, false>;
-    } else {
-        if (vec) kern = pow2 ? index_build_kernel<false, true, true> : index_build_kernel<false, true, false>;
-        else kern = pow2 ? index_build_kernel<false, false, true> : index_build_kernel<false, false, false>;
-    }
+    const size_t smem =
+        ((tma ? (size_t)p.tokens_per_cta * p.topk : 0) + p.stage_comp + p.stage_swa) *
+        sizeof(int32_t);
+    using Kern = void (*)(IndexParams);
+    // [has_swa][pow2][mode: 0 scalar, 1 vector, 2 vector + staged top-k rows]
+    static const Kern kTable[2][2][3] = {
+        {{index_build_kernel<false, false, false, false>, index_build_kernel<false, true, false, false>,
+          index_build_kernel<false, true, false, true>},
+         {index_build_kernel<false, false, true, false>, index_build_kernel<false, true, true, false>,
+          index_build_kernel<false, true, true, true>}},
+        {{index_build_kernel<true, false, false, false>, index_build_kernel<true, true, false, false>,
+          index_build_kernel<true, true, false, true>},
+         {index_build_kernel<true, false, true, false>, index_build_kernel<true, true, true, false>,
+          index_build_kernel<true, true, true, true>}}};
+    const Kern kern = kTable[has_swa][pow2][tma ? 2 : (vec ? 1 : 0)];
+    const cudaError_t e = allow_dynamic_smem(kern, smem);
+    if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p);
 }
 

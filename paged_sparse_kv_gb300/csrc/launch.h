@@ -179,6 +179,7 @@ struct RawGatherParams {
 cudaError_t launch_mxfp4_raw_gather(const RawGatherParams& p, cudaStream_t stream);
 
 // Number of bounded in-kernel waits that expired on the current device.
-cudaError_t read_wait_timeouts(uint32_t* count);
+cudaError_t read_wait_timeouts(uint32_t* count);        // gather kernels
+cudaError_t read_index_wait_timeouts(uint32_t* count);  // index builders
 
 }  // namespace psk
