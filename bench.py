@@ -230,27 +230,41 @@ def _graph_events_supported(torch) -> bool:
         return False
 
 
-def kernel_source_hash() -> str:
-    """sha1 over the CUDA sources (sorted by name); identifies the kernel build
-    a recorded ncu capture belongs to."""
-    import glob
+# CUDA source file of each timed entry point (plus the shared headers).
+KERNEL_SOURCES = {
+    "quantize_and_insert_k_cache": "insert.cu",
+    "write_indexer_mxfp4_cache": "insert.cu",
+    "combine_topk_swa_indices": "index_build.cu",
+    "compute_global_topk_indices_and_lens": "index_build.cu",
+    "combine_topk_swa_workspace_indices": "index_build.cu",
+    "dequantize_and_gather_k_cache": "gather.cu",
+    "dequantize_and_gather_k_cache_ranges": "gather.cu",
+    "indexer_mxfp4_paged_gather": "gather.cu",
+}
+SHARED_SOURCES = ("psk_common.cuh", "launch.h")
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """sha1 over the CUDA sources a timed kernel is built from (its .cu file
+    and the shared headers); identifies the build a recorded ncu capture
+    belongs to."""
     import hashlib
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "paged_sparse_kv_gb300", "csrc")
-    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(os.path.basename(f).encode())
-            h.update(open(f, "rb").read())
+    base = kernel.split("[")[0]
+    for f in sorted((KERNEL_SOURCES[base],) + SHARED_SOURCES):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()
 
 
 def recorded_traffic(config: str, kernel: str):
     """DRAM bytes (read + write) per launch from profiles/traffic.txt, or None
-    when no capture exists for this kernel build."""
+    when no capture exists for the current build of this kernel."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(kernel)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#") and parts[0] == config and \
