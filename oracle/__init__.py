@@ -87,6 +87,15 @@ def _load():
                    _P, _P, _I64, _P]),
         "oracle_indexer_mxfp4_paged_gather": (
             None, [_P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _I32, _P, _I32]),
+        "oracle_decode_swa_indices_and_lens": (
+            None, [_P, _P, _P, _I32, _I64, _P, _I64, _I32, _P, _I32, _I32, _P, _P, _I64, _P]),
+        "oracle_compute_dense_compressed_indices_and_lens": (
+            None, [_P, _I64, _P, _I32, _P, _I64, _I32, _P, _I32, _I32, _I32, _P, _P, _I64,
+                   _P]),
+        "oracle_build_dense_prefill_local_compressed_indices": (
+            None, [_P, _I64, _I32, _I32, _P, _I64]),
+        "oracle_combine_dense_swa_indices": (
+            None, [_P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64, _P, _I64, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -310,3 +319,74 @@ def indexer_mxfp4_paged_gather(cache, block_size, head_dim, block_table, cu_seq_
         head_dim, _ptr(block_table), block_table.shape[1], block_table.shape[1],
         _ptr(cu_seq_lens), cu_seq_lens.shape[0] - 1)
     return values, scales
+
+
+# ---- dense builders -------------------------------------------------------------------
+
+def decode_swa_indices_and_lens(query_start_loc, seq_lens, token_to_req, block_table,
+                                block_size, window, base_offsets=None, is_valid_token=None):
+    """Window-only indices [T, window] + lens of the decode SWA precompute."""
+    query_start_loc = _as(query_start_loc, np.int32)
+    seq_lens = _as(seq_lens, np.int32)
+    token_to_req = _as(token_to_req, np.int32)
+    block_table = _as(block_table, np.int32)
+    base_offsets = _as(base_offsets, np.int32)
+    if is_valid_token is not None:
+        is_valid_token = np.ascontiguousarray(is_valid_token).astype(np.uint8)
+    T = token_to_req.shape[0]
+    out = np.empty((T, window), dtype=np.int32)
+    lens = np.empty((T,), dtype=np.int32)
+    _load().oracle_decode_swa_indices_and_lens(
+        _ptr(query_start_loc), _ptr(seq_lens), _ptr(token_to_req), seq_lens.shape[0], T,
+        _ptr(block_table), block_table.shape[1], block_table.shape[1], _ptr(base_offsets),
+        block_size, window, _ptr(is_valid_token), _ptr(out), window, _ptr(lens))
+    return out, lens
+
+
+def compute_dense_compressed_indices_and_lens(positions, token_to_req, block_table, block_size,
+                                              compress_ratio, width, num_reqs=None,
+                                              base_offsets=None, is_valid_token=None):
+    """Every visible compressed entry's slot [T, width] + lens (HCA decode)."""
+    positions = _as(positions, np.int64)
+    token_to_req = _as(token_to_req, np.int32)
+    block_table = _as(block_table, np.int32)
+    base_offsets = _as(base_offsets, np.int32)
+    if is_valid_token is not None:
+        is_valid_token = np.ascontiguousarray(is_valid_token).astype(np.uint8)
+    T = positions.shape[0]
+    R = block_table.shape[0] if num_reqs is None else num_reqs
+    out = np.empty((T, width), dtype=np.int32)
+    lens = np.empty((T,), dtype=np.int32)
+    _load().oracle_compute_dense_compressed_indices_and_lens(
+        _ptr(positions), T, _ptr(token_to_req), R, _ptr(block_table), block_table.shape[1],
+        block_table.shape[1], _ptr(base_offsets), block_size, compress_ratio, width,
+        _ptr(is_valid_token), _ptr(out), width, _ptr(lens))
+    return out, lens
+
+
+def build_dense_prefill_local_compressed_indices(positions, compress_ratio, width):
+    """Request-local dense compressed indices [T, width]."""
+    positions = _as(positions, np.int64)
+    T = positions.shape[0]
+    out = np.empty((T, width), dtype=np.int32)
+    _load().oracle_build_dense_prefill_local_compressed_indices(
+        _ptr(positions), T, compress_ratio, width, _ptr(out), width)
+    return out
+
+
+def combine_dense_swa_indices(positions, token_to_req, seq_lens, gather_lens, window,
+                              workspace_width, compressed_base=0):
+    """Window-only workspace indices [T, window] + lens (layers without a
+    compressed cache)."""
+    positions = _as(positions, np.int64)
+    token_to_req = _as(token_to_req, np.int32)
+    seq_lens = _as(seq_lens, np.int32)
+    gather_lens = _as(gather_lens, np.int32)
+    T = positions.shape[0]
+    out = np.empty((T, window), dtype=np.int32)
+    lens = np.empty((T,), dtype=np.int32)
+    _load().oracle_combine_dense_swa_indices(
+        _ptr(positions), _ptr(token_to_req), _ptr(seq_lens), _ptr(gather_lens),
+        seq_lens.shape[0], T, window, workspace_width, compressed_base, _ptr(out), window,
+        _ptr(lens))
+    return out, lens

@@ -687,3 +687,163 @@ void oracle_indexer_mxfp4_paged_gather(
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Dense builders: decode SWA indices, HCA dense compressed indices, dense   */
+/* prefill local indices, SWA-only workspace combine                        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [OPS] deepseek_v4_decode_swa_indices_and_lens as [BE]
+ * _update_decode_swa_metadata calls it (query_start_loc, seq_lens,
+ * token_to_req_indices, block_table, block_table_base_offsets, window_size,
+ * block_size, is_valid_token -> indices [T, window_size], lens [T]).  The body
+ * is not printed; read as the window part of the fused builder: the token's
+ * position from the metadata ([BE] _decode_positions_from_metadata), window
+ * [max(pos - window + 1, 0), pos] left-aligned, oldest first; each position's
+ * slot through the SWA table (minus the request's base logical page) or -1;
+ * lens = entries >= 0; a padding token (is_valid_token 0, or a request index
+ * outside [0, num_reqs)) is all -1 with lens 0.  The call passes no
+ * replay_start, so none bounds the window.
+ */
+void oracle_decode_swa_indices_and_lens(
+    const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* token_to_req, int32_t num_reqs, int64_t num_tokens,
+    const int32_t* block_table, int64_t bt_stride, int32_t bt_width,
+    const int32_t* base_offsets, int32_t block_size, int32_t window,
+    const uint8_t* is_valid_token, int32_t* indices, int64_t out_stride,
+    int32_t* lens) {
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int32_t* row = indices + t * out_stride;
+        const int32_t r = token_to_req[t];
+        const int ok = (is_valid_token ? is_valid_token[t] != 0 : 1) &&
+                       r >= 0 && r < num_reqs;
+        int32_t count = 0;
+        if (!ok) {
+            for (int32_t c = 0; c < window; ++c) row[c] = -1;
+            lens[t] = 0;
+            continue;
+        }
+        const int64_t qstart = query_start_loc[r];
+        const int64_t qlen = (int64_t)query_start_loc[r + 1] - qstart;
+        const int64_t pos = (int64_t)seq_lens[r] - qlen + (t - qstart);
+        int64_t lo = pos - window + 1;
+        if (lo < 0) lo = 0;
+        const int32_t* trow = block_table + (int64_t)r * bt_stride;
+        const int64_t base = base_offsets ? base_offsets[r] : 0;
+        for (int32_t c = 0; c < window; ++c) {
+            const int64_t p = lo + c;
+            const int32_t v = p <= pos ? slot_of(trow, bt_width, base, block_size, p) : -1;
+            row[c] = v;
+            if (v >= 0) ++count;
+        }
+        lens[t] = count;
+    }
+}
+
+/*
+ * [BE] _decode_compressed_attention_indices_and_lens for a compress ratio other
+ * than 4 (printed in full): token t of request r at positions[t] sees
+ * n = clamp(floor((positions[t] + 1) / ratio), 0, width) compressed entries;
+ * column j < width holds the slot of compressed entry j through the compressed
+ * table row (logical page j / bs minus the request's base logical page) when
+ * j < n and that page exists, else -1; lens[t] = n -- the count of visible
+ * entries, including any whose page is missing, as printed -- and 0 for a
+ * padding token (is_valid_token 0; and, a reading shared with the other
+ * builders, a request index outside [0, num_reqs), whose row is all -1).
+ * Slots beyond INT32_MAX are -1 (the builders' common reading).
+ */
+void oracle_compute_dense_compressed_indices_and_lens(
+    const int64_t* positions, int64_t num_tokens, const int32_t* token_to_req,
+    int32_t num_reqs, const int32_t* block_table, int64_t bt_stride,
+    int32_t bt_width, const int32_t* base_offsets, int32_t block_size,
+    int32_t compress_ratio, int32_t width, const uint8_t* is_valid_token,
+    int32_t* indices, int64_t out_stride, int32_t* lens) {
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int32_t* row = indices + t * out_stride;
+        const int32_t r = token_to_req[t];
+        const int ok = (is_valid_token ? is_valid_token[t] != 0 : 1) &&
+                       r >= 0 && r < num_reqs;
+        if (!ok) {
+            for (int32_t j = 0; j < width; ++j) row[j] = -1;
+            lens[t] = 0;
+            continue;
+        }
+        /* floor division of pos + 1 by the ratio, then the clamp to [0, width] */
+        const int64_t num = positions[t] + 1;
+        int64_t n = num >= 0 ? num / compress_ratio
+                             : -((-num + compress_ratio - 1) / compress_ratio);
+        if (n < 0) n = 0;
+        if (n > width) n = width;
+        const int32_t* trow = block_table + (int64_t)r * bt_stride;
+        const int64_t base = base_offsets ? base_offsets[r] : 0;
+        for (int32_t j = 0; j < width; ++j)
+            row[j] = j < n ? slot_of(trow, bt_width, base, block_size, j) : -1;
+        lens[t] = (int32_t)n;
+    }
+}
+
+/*
+ * [OPS] deepseek_v4_build_dense_prefill_local_compressed_indices(positions,
+ * compress_ratio, width, out) as [BE] _dense_prefill_local_compressed_indices
+ * calls it on the HCA prefill workspace path: the body is not printed; read as
+ * the request-local form of the dense decode rule, out[t][j] = j for
+ * j < min(floor((positions[t] + 1) / ratio), width), else -1.  The rows are the
+ * top-k input of the workspace-relative combine.
+ */
+void oracle_build_dense_prefill_local_compressed_indices(
+    const int64_t* positions, int64_t num_tokens, int32_t compress_ratio,
+    int32_t width, int32_t* out, int64_t out_stride) {
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int64_t num = positions[t] + 1;
+        int64_t n = num >= 0 ? num / compress_ratio
+                             : -((-num + compress_ratio - 1) / compress_ratio);
+        if (n < 0) n = 0;
+        if (n > width) n = width;
+        for (int32_t j = 0; j < width; ++j) out[t * out_stride + j] = j < n ? j : -1;
+    }
+}
+
+/*
+ * [OPS] deepseek_v4_combine_dense_swa_indices as [BE] _prefill_workspace calls
+ * it for layers without a compressed cache (compress_ratio <= 1, where the
+ * compressed lengths are all zero and compressed_base is 0); the body is not
+ * printed.  Read as the window columns of the workspace-relative combine with
+ * the token's position given: column c < window holds position
+ * p = lo + c, lo = max(positions[t] - window + 1, 0), as workspace row
+ * r * workspace_width + compressed_base + (p - g0) when g0 <= p <= positions[t],
+ * g0 = seq_lens[r] - gather_lens[r], else -1 (rows beyond INT32_MAX: -1);
+ * lens = entries >= 0; a request index outside [0, num_reqs) gives an all -1
+ * row with lens 0.
+ */
+void oracle_combine_dense_swa_indices(
+    const int64_t* positions, const int32_t* token_to_req,
+    const int32_t* seq_lens, const int32_t* gather_lens, int32_t num_reqs,
+    int64_t num_tokens, int32_t window, int64_t workspace_width,
+    int64_t compressed_base, int32_t* indices, int64_t out_stride,
+    int32_t* lens) {
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int32_t* row = indices + t * out_stride;
+        const int32_t r = token_to_req[t];
+        if (r < 0 || r >= num_reqs) {
+            for (int32_t c = 0; c < window; ++c) row[c] = -1;
+            lens[t] = 0;
+            continue;
+        }
+        const int64_t pos = positions[t];
+        const int64_t g0 = (int64_t)seq_lens[r] - gather_lens[r];
+        const int64_t rbase = (int64_t)r * workspace_width;
+        int64_t lo = pos - window + 1;
+        if (lo < 0) lo = 0;
+        int32_t count = 0;
+        for (int32_t c = 0; c < window; ++c) {
+            const int64_t p = lo + c;
+            int64_t v = -1;
+            if (p <= pos && p >= g0) v = rbase + compressed_base + (p - g0);
+            if (v > INT32_MAX) v = -1;
+            row[c] = (int32_t)v;
+            if (v >= 0) ++count;
+        }
+        lens[t] = count;
+    }
+}

@@ -104,6 +104,33 @@ void oracle_indexer_mxfp4_paged_gather(
     int32_t head_dim, const int32_t* block_table, int64_t bt_stride,
     int32_t bt_width, const int32_t* cu_seq_lens, int32_t num_reqs);
 
+/* ---- dense builders ---- */
+void oracle_decode_swa_indices_and_lens(
+    const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* token_to_req, int32_t num_reqs, int64_t num_tokens,
+    const int32_t* block_table, int64_t bt_stride, int32_t bt_width,
+    const int32_t* base_offsets, int32_t block_size, int32_t window,
+    const uint8_t* is_valid_token, int32_t* indices, int64_t out_stride,
+    int32_t* lens);
+
+void oracle_compute_dense_compressed_indices_and_lens(
+    const int64_t* positions, int64_t num_tokens, const int32_t* token_to_req,
+    int32_t num_reqs, const int32_t* block_table, int64_t bt_stride,
+    int32_t bt_width, const int32_t* base_offsets, int32_t block_size,
+    int32_t compress_ratio, int32_t width, const uint8_t* is_valid_token,
+    int32_t* indices, int64_t out_stride, int32_t* lens);
+
+void oracle_build_dense_prefill_local_compressed_indices(
+    const int64_t* positions, int64_t num_tokens, int32_t compress_ratio,
+    int32_t width, int32_t* out, int64_t out_stride);
+
+void oracle_combine_dense_swa_indices(
+    const int64_t* positions, const int32_t* token_to_req,
+    const int32_t* seq_lens, const int32_t* gather_lens, int32_t num_reqs,
+    int64_t num_tokens, int32_t window, int64_t workspace_width,
+    int64_t compressed_base, int32_t* indices, int64_t out_stride,
+    int32_t* lens);
+
 #ifdef __cplusplus
 }
 #endif
