@@ -97,6 +97,27 @@ def algorithmic_bytes(p, outputs) -> dict:
     return res
 
 
+def dense_algorithmic_bytes(p, outputs) -> dict:
+    """Compulsory bytes of the dense (no top-k) decode step's launches."""
+    w = p.w
+    T, R, W, Wd = w.num_tokens, w.num_reqs, w.window, w.dense_width
+    rec = w.head_dim - w.rope_dim + 2 * w.rope_dim + w.head_dim // 64
+    ins = w.insert_slots
+    res = {"quantize_and_insert_k_cache": int((ins >= 0).sum()) * (2 * w.head_dim + rec) +
+           ins.size * 8}
+    # token -> request + lens; per request qsl pair and seq_len, and the table row
+    res["decode_swa_indices_and_lens"] = (T * (4 * W + 4 + 4) + R * 12 +
+                                          R * w.swa_block_table.shape[1] * 4)
+    # position (8) + token -> request + lens per token, and the table row
+    res["compute_dense_compressed_indices_and_lens"] = (T * (4 * Wd + 8 + 4 + 4) +
+                                                        R * w.comp_block_table.shape[1] * 4)
+    for part, cols in (("swa", outputs["swa_indices"]), ("compressed", outputs["dense_indices"])):
+        distinct = np.unique(cols[cols >= 0]).size
+        res[f"dequantize_and_gather_k_cache[{part}]"] = (distinct * rec + cols.size * 4 +
+                                                         cols.size * 2 * w.head_dim)
+    return res
+
+
 def workspace_algorithmic_bytes(p) -> dict:
     """Compulsory bytes of the prefill workspace step's launches."""
     from paged_sparse_kv_gb300.pipeline import workspace_geometry
@@ -196,8 +217,17 @@ def _oracle_sample_tokens(w, max_rows: int):
 
 def time_oracle(w, budget_s: float, max_rows: int = 80000, path: str = "index"):
     """Run oracle steps until budget_s of CPU work; returns (tokens/s, desc)."""
-    from oracle.pipeline import run_step, run_workspace_step
+    from oracle.pipeline import run_dense_step, run_step, run_workspace_step
     caches = _oracle_state(w)
+    if path == "dense":
+        steps, spent = 0, 0.0
+        while spent < budget_s or steps == 0:
+            t0 = time.perf_counter()
+            run_dense_step(w, caches["swa_cache"], caches["comp_cache"])
+            spent += time.perf_counter() - t0
+            steps += 1
+        return (w.num_tokens * steps / spent,
+                f"{steps} oracle steps of the {w.name} batch on the dense path")
     if path == "workspace":
         from paged_sparse_kv_gb300.pipeline import workspace_geometry
         geom = workspace_geometry(w)
@@ -237,6 +267,10 @@ KERNEL_SOURCES = {
     "combine_topk_swa_indices": "index_build.cu",
     "compute_global_topk_indices_and_lens": "index_build.cu",
     "combine_topk_swa_workspace_indices": "index_build.cu",
+    "decode_swa_indices_and_lens": "index_build.cu",
+    "compute_dense_compressed_indices_and_lens": "index_build.cu",
+    "build_dense_prefill_local_compressed_indices": "index_build.cu",
+    "combine_dense_swa_indices": "index_build.cu",
     "dequantize_and_gather_k_cache": "gather.cu",
     "dequantize_and_gather_k_cache_ranges": "gather.cu",
     "indexer_mxfp4_paged_gather": "gather.cu",
@@ -305,13 +339,16 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="decode",
-                    choices=["tiny", "decode", "prefill", "mixed", "mxfp4", "prefill_small"])
+                    choices=["tiny", "decode", "prefill", "mixed", "mxfp4", "prefill_small",
+                             "decode_hca"])
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--path", default="index", choices=["index", "workspace"],
+    ap.add_argument("--path", default="index", choices=["index", "workspace", "dense"],
                     help="index: the index-keyed gather into [T, W+P, D]; workspace: the "
-                         "prefill workspace path (range gathers + workspace indices)")
+                         "prefill workspace path (range gathers + workspace indices); dense: "
+                         "the no-top-k decode step of a heavily compressed layer (the "
+                         "decode_hca workload always takes it)")
     ap.add_argument("--eager", action="store_true",
                     help="launch the step eagerly instead of replaying a CUDA graph")
     args = ap.parse_args()
@@ -341,10 +378,13 @@ def main():
     w = synthetic.make(args.config, seed_offset=1000 * rank)
     p = Pipeline(w, dev)
     p.fill_caches_with_quantized_rows(seed=4321 + rank)
-    path = args.path
+    path = "dense" if w.dense_width > 0 else args.path
     if path == "workspace" and not w.has_fp8:
         raise SystemExit("the workspace path needs a workload with an FP8 part")
-    launches = p.workspace_launches() if path == "workspace" else p.launches()
+    if path == "dense" and w.dense_width <= 0:
+        raise SystemExit("the dense path needs a workload with dense compressed entries")
+    launches = {"workspace": p.workspace_launches, "dense": p.dense_launches,
+                "index": p.launches}[path]()
     names = [n for n, _ in launches]
     flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
@@ -356,6 +396,9 @@ def main():
 
     if path == "workspace":
         alg = workspace_algorithmic_bytes(p)
+    elif path == "dense":
+        alg = dense_algorithmic_bytes(p, {"swa_indices": p.swa_indices.cpu().numpy(),
+                                          "dense_indices": p.dense_indices.cpu().numpy()})
     else:
         outputs = {"global_topk": p.global_topk.cpu().numpy()}
         if w.has_fp8:
@@ -534,6 +577,10 @@ def run_e2e(p, args, dev, flush, path="index"):
                        p.t2r, p.replay, p.topk) if t is not None]
     if path == "workspace":
         outs = [p.ws, p.ws_indices, p.ws_lens, p.raw_values, p.raw_scales]
+    elif path == "dense":
+        ins = [t for t in (p.k, p.insert_slots, p.qsl, p.seq_lens, p.t2r, p.positions)
+               if t is not None]
+        outs = [p.swa_indices, p.swa_lens, p.dense_indices, p.dense_lens, p.dense_gathered]
     else:
         outs = [t for t in (p.sparse_indices, p.lens, p.gathered, p.global_topk, p.global_lens,
                             p.gathered_index) if t is not None]
@@ -557,34 +604,51 @@ def run_e2e(p, args, dev, flush, path="index"):
     return {"ms_per_step": statistics.mean(times) * 1e3, "h2d": h2d, "d2h": d2h}
 
 
+def _oracle_step(w, path: str, caches):
+    """(one oracle step as a callable, tokens it covers, description) for a path."""
+    from oracle.pipeline import run_dense_step, run_step, run_workspace_step
+    if path == "dense":
+        return (lambda: run_dense_step(w, caches["swa_cache"], caches["comp_cache"]),
+                w.num_tokens, f"oracle step of the {w.name} batch (dense path) per timed step")
+    if path == "workspace":
+        from paged_sparse_kv_gb300.pipeline import workspace_geometry
+        geom = workspace_geometry(w)
+        return (lambda: run_workspace_step(w, geom, caches["swa_cache"], caches["comp_cache"],
+                                           caches["index_cache"]),
+                w.num_tokens,
+                f"oracle step of the {w.name} batch (workspace path) per timed step")
+    toks, n = _oracle_sample_tokens(w, 80000)
+    return (lambda: run_step(w, caches["swa_cache"], caches["comp_cache"],
+                             caches["index_cache"], toks),
+            n, f"oracle step of the {w.name} batch per timed step; gathers over {n} of "
+               f"{w.num_tokens} tokens")
+
+
 def run_reference(args, rank, world):
     """Reference arm: the CPU oracle, timed on this host's cores."""
     if rank != 0:
         return
     import oracle
-    from oracle.pipeline import run_step
     from paged_sparse_kv_gb300 import synthetic
     oracle.build()
     w = synthetic.make(args.config)
-    caches = _oracle_state(w)
-    toks, n = _oracle_sample_tokens(w, 80000)
+    path = "dense" if w.dense_width > 0 else args.path
+    step, n, desc = _oracle_step(w, path, _oracle_state(w))
     for _ in range(args.warmup):
-        run_step(w, caches["swa_cache"], caches["comp_cache"], caches["index_cache"], toks)
+        step()
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        run_step(w, caches["swa_cache"], caches["comp_cache"], caches["index_cache"], toks)
+        step()
         times.append(time.perf_counter() - t0)
     ms = statistics.mean(times) * 1e3
     value = n / (ms / 1e3)
-    desc = (f"oracle step of the {w.name} batch per timed step; gathers over {n} of "
-            f"{w.num_tokens} tokens")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16/fp8/fp4", "data": "synthetic",
-        "config": {"workload": w.name, "seed": w.seed},
+        "config": {"workload": w.name, "seed": w.seed, "path": path},
         "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,

@@ -325,6 +325,101 @@ psk_status indexer_mxfp4_paged_gather(
     const int32_t* cu_seq_lens, int32_t num_reqs, int64_t total_rows,
     psk_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Dense builders (TokenSpeed backends/deepseek_v4.py: decode SWA precompute, */
+/* HCA dense compressed indices, SWA-only workspace combine)                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * decode_swa_indices_and_lens -- window-only slot indices of decode tokens.
+ * TokenSpeed deepseek_v4_decode_swa_indices_and_lens as [BE]
+ * _update_decode_swa_metadata calls it (query_start_loc, seq_lens,
+ * token_to_req_indices, block_table, block_table_base_offsets, window_size,
+ * block_size, is_valid_token).  The kernel is not printed: read as the window
+ * columns of combine_topk_swa_indices with no top-k and no replay_start.
+ *
+ *   out_indices  int32 [num_tokens, window], row stride out_stride (>= window):
+ *                column c holds the slot of position lo + c, lo =
+ *                max(pos - window + 1, 0), through block_table[r] (logical
+ *                page position/block_size - base_offsets[r]), or -1 past pos
+ *                or where the page is missing / the slot exceeds INT32_MAX.
+ *   out_lens     int32 [num_tokens]: entries >= 0.  Padding tokens
+ *                (is_valid_token 0 or a request index outside [0, num_reqs)):
+ *                all -1, lens 0.
+ *   pos = seq_lens[r] - query_len[r] + (t - query_start_loc[r]).
+ */
+psk_status decode_swa_indices_and_lens(
+    const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* token_to_req, int32_t num_reqs, int64_t num_tokens,
+    const int32_t* block_table, int64_t bt_stride, int32_t bt_width,
+    const int32_t* base_offsets, int32_t block_size, int32_t window,
+    const uint8_t* is_valid_token, int32_t* out_indices, int64_t out_stride,
+    int32_t* out_lens, psk_stream_t stream);
+
+/*
+ * compute_dense_compressed_indices_and_lens -- every visible compressed entry
+ * of a decode token (the HCA layers).  [BE]
+ * _decode_compressed_attention_indices_and_lens for a compress ratio other
+ * than 4 (printed in full).
+ *
+ *   positions    int64 [num_tokens] token positions (8-byte aligned).
+ *   n(t)         = clamp(floor((positions[t] + 1) / compress_ratio), 0, width).
+ *   out_indices  int32 [num_tokens, width], row stride out_stride (>= width):
+ *                column j holds, for j < n(t), the slot of compressed entry j
+ *                through block_table[r] (logical page j/block_size -
+ *                base_offsets[r]) or -1 where that page is missing; -1 for
+ *                j >= n(t).
+ *   out_lens     int32 [num_tokens]: n(t) -- the count of visible entries,
+ *                including those whose page is missing, as the pages print
+ *                it -- and 0 for a padding token (is_valid_token 0, or a
+ *                request index outside [0, num_reqs), whose row is all -1).
+ *   width        the caller's dense width (the pages round
+ *                ceil(context_len / ratio) up to an alignment).
+ */
+psk_status compute_dense_compressed_indices_and_lens(
+    const int64_t* positions, int64_t num_tokens, const int32_t* token_to_req,
+    int32_t num_reqs, const int32_t* block_table, int64_t bt_stride,
+    int32_t bt_width, const int32_t* base_offsets, int32_t block_size,
+    int32_t compress_ratio, int32_t width, const uint8_t* is_valid_token,
+    int32_t* out_indices, int64_t out_stride, int32_t* out_lens,
+    psk_stream_t stream);
+
+/*
+ * build_dense_prefill_local_compressed_indices -- request-local dense
+ * compressed indices of prefill tokens (the HCA prefill workspace's top-k
+ * input).  TokenSpeed deepseek_v4_build_dense_prefill_local_compressed_indices
+ * (positions, compress_ratio, width, out) as [BE]
+ * _dense_prefill_local_compressed_indices calls it; the kernel is not printed:
+ * read as out[t][j] = j for j < clamp(floor((positions[t] + 1) / ratio), 0,
+ * width), else -1.  out: int32 [num_tokens, width], row stride out_stride.
+ */
+psk_status build_dense_prefill_local_compressed_indices(
+    const int64_t* positions, int64_t num_tokens, int32_t compress_ratio,
+    int32_t width, int32_t* out, int64_t out_stride, psk_stream_t stream);
+
+/*
+ * combine_dense_swa_indices -- workspace-relative window indices of layers
+ * without a compressed cache (compress_ratio <= 1).  TokenSpeed
+ * deepseek_v4_combine_dense_swa_indices as [BE] _prefill_workspace calls it
+ * (its compressed lengths are then all zero); the kernel is not printed: read
+ * as the window columns of combine_topk_swa_workspace_indices with the token's
+ * position given.
+ *
+ *   indices  int32 [num_tokens, window], row stride out_stride (>= window):
+ *            column c holds position p = max(positions[t] - window + 1, 0) + c
+ *            as workspace row r*workspace_width + compressed_base + (p - g0)
+ *            when g0 <= p <= positions[t], g0 = seq_lens[r] - gather_lens[r];
+ *            else -1 (also for rows beyond INT32_MAX).
+ *   lens     int32 [num_tokens]: entries >= 0.  A request index outside
+ *            [0, num_reqs) gives an all -1 row with lens 0.
+ */
+psk_status combine_dense_swa_indices(
+    const int64_t* positions, const int32_t* token_to_req,
+    const int32_t* seq_lens, const int32_t* gather_lens, int32_t num_reqs,
+    int64_t num_tokens, int32_t window, int64_t workspace_width,
+    int64_t compressed_base, int32_t* indices, int64_t out_stride,
+    int32_t* lens, psk_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

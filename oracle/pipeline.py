@@ -13,7 +13,8 @@ from typing import Optional, Sequence
 import numpy as np
 
 from . import (REC_FP8_DS_MLA, REC_MXFP4, combine_topk_swa_indices,
-               combine_topk_swa_workspace_indices, compute_global_topk_indices_and_lens,
+               combine_topk_swa_workspace_indices, compute_dense_compressed_indices_and_lens,
+               compute_global_topk_indices_and_lens, decode_swa_indices_and_lens,
                dequantize_and_gather_k_cache, dequantize_and_gather_k_cache_ranges,
                indexer_mxfp4_paged_gather, quantize_and_insert_k_cache,
                write_indexer_mxfp4_cache)
@@ -84,4 +85,25 @@ def run_workspace_step(w, geom: dict, swa_cache, comp_cache, index_cache) -> dic
         w.compress_ratio, w.topk_local, ww, cb, is_valid_token=w.is_valid_token)
     res["raw_values"], res["raw_scales"] = indexer_mxfp4_paged_gather(
         index_cache, w.index_cache.block_size, w.index_head_dim, table, geom["cu_compressed"])
+    return res
+
+
+def run_dense_step(w, swa_cache, comp_cache) -> dict:
+    """The dense (no top-k) decode step: FP8 insert, window-only slot indices,
+    every visible compressed entry's slot, and the two-part gather into
+    [T, W + dense_width, D].  Caches are updated in place."""
+    res: dict = {"err": 0}
+    res["err"] += quantize_and_insert_k_cache(
+        w.k, w.insert_slots, swa_cache, w.swa_cache.block_size, w.head_dim, w.rope_dim)
+    res["swa_indices"], res["swa_lens"] = decode_swa_indices_and_lens(
+        w.query_start_loc, w.seq_lens, w.token_to_req, w.swa_block_table,
+        w.swa_cache.block_size, w.window, is_valid_token=w.is_valid_token)
+    res["dense_indices"], res["dense_lens"] = compute_dense_compressed_indices_and_lens(
+        w.positions, w.token_to_req, w.comp_block_table, w.comp_cache.block_size,
+        w.compress_ratio, w.dense_width, num_reqs=w.num_reqs, is_valid_token=w.is_valid_token)
+    g_swa = dequantize_and_gather_k_cache(swa_cache, w.swa_cache.block_size, REC_FP8_DS_MLA,
+                                          w.head_dim, w.rope_dim, res["swa_indices"])
+    g_cmp = dequantize_and_gather_k_cache(comp_cache, w.comp_cache.block_size, REC_FP8_DS_MLA,
+                                          w.head_dim, w.rope_dim, res["dense_indices"])
+    res["gathered"] = np.concatenate([g_swa, g_cmp], axis=1)
     return res

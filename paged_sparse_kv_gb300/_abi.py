@@ -54,6 +54,14 @@ SIGNATURES = {
                _P, _P]),
     "indexer_mxfp4_paged_gather": (
         _I32, [_P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _I32, _P, _I32, _I64, _P]),
+    "decode_swa_indices_and_lens": (
+        _I32, [_P, _P, _P, _I32, _I64, _P, _I64, _I32, _P, _I32, _I32, _P, _P, _I64, _P, _P]),
+    "compute_dense_compressed_indices_and_lens": (
+        _I32, [_P, _I64, _P, _I32, _P, _I64, _I32, _P, _I32, _I32, _I32, _P, _P, _I64, _P, _P]),
+    "build_dense_prefill_local_compressed_indices": (
+        _I32, [_P, _I64, _I32, _I32, _P, _I64, _P]),
+    "combine_dense_swa_indices": (
+        _I32, [_P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64, _P, _I64, _P, _P]),
 }
 
 _lib = None

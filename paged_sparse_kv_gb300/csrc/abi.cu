@@ -75,7 +75,7 @@ extern "C" {
 
 const char* psk_last_error(void) { return g_last_error.c_str(); }
 
-int32_t psk_abi_version(void) { return 1; }
+int32_t psk_abi_version(void) { return 2; }
 
 psk_status psk_device_wait_timeouts(uint32_t* count) {
     CHECK(count != nullptr, "count must be non-null");
@@ -363,7 +363,7 @@ psk_status combine_topk_swa_workspace_indices(
     psk::WorkspaceIndexParams p{query_start_loc, seq_lens, gather_lens, token_to_req, num_reqs,
                                 num_tokens, window, compress_ratio, topk_local, topk_stride,
                                 topk, workspace_width, compressed_base, is_valid_token, indices,
-                                out_stride, lens};
+                                out_stride, lens, nullptr};
     return cuda_status(psk::launch_workspace_indices(p, reinterpret_cast<cudaStream_t>(stream)),
                        "combine_topk_swa_workspace_indices launch");
 }
@@ -394,6 +394,134 @@ psk_status indexer_mxfp4_paged_gather(uint8_t* values_out, uint8_t* scales_out,
                            total_rows};
     return cuda_status(psk::launch_mxfp4_raw_gather(p, reinterpret_cast<cudaStream_t>(stream)),
                        "indexer_mxfp4_paged_gather launch");
+}
+
+psk_status decode_swa_indices_and_lens(
+    const int32_t* query_start_loc, const int32_t* seq_lens, const int32_t* token_to_req,
+    int32_t num_reqs, int64_t num_tokens, const int32_t* block_table, int64_t bt_stride,
+    int32_t bt_width, const int32_t* base_offsets, int32_t block_size, int32_t window,
+    const uint8_t* is_valid_token, int32_t* out_indices, int64_t out_stride, int32_t* out_lens,
+    psk_stream_t stream) {
+    CHECK(num_tokens >= 0, "num_tokens must be >= 0");
+    CHECK(window >= 0, "window must be >= 0");
+    CHECK(block_size >= 1, "block_size must be >= 1");
+    CHECK(bt_width >= 0 && bt_stride >= bt_width, "need 0 <= bt_width <= bt_stride");
+    CHECK(out_stride >= window, "out_stride must be >= window");
+    if (num_tokens == 0) return ok();
+    CHECK(num_reqs >= 1, "num_reqs must be >= 1");
+    CHECK(query_start_loc && seq_lens && token_to_req && out_indices && out_lens,
+          "query_start_loc, seq_lens, token_to_req, out_indices and out_lens must be non-null");
+    CHECK(bt_width == 0 || block_table, "block_table must be non-null");
+    CHECK(aligned(query_start_loc, 4) && aligned(seq_lens, 4) && aligned(token_to_req, 4) &&
+              aligned(block_table, 4) && aligned(base_offsets, 4) && aligned(out_indices, 4) &&
+              aligned(out_lens, 4),
+          "int32 arrays must be 4-byte aligned");
+    psk::IndexParams p{};
+    p.qsl = query_start_loc;
+    p.seq_lens = seq_lens;
+    p.t2r = token_to_req;
+    p.replay = nullptr;
+    p.num_reqs = num_reqs;
+    p.num_tokens = num_tokens;
+    p.swa_bt = p.comp_bt = block_table;
+    p.swa_stride = p.comp_stride = bt_stride;
+    p.swa_width = p.comp_width = bt_width;
+    p.swa_base = p.comp_base = base_offsets;
+    p.swa_bs = p.comp_bs = block_size;
+    p.swa_shift = p.comp_shift = psk::log2_if_pow2(block_size);
+    p.window = window;
+    p.topk = 0;
+    p.out_cols = window;
+    p.topk_local = nullptr;
+    p.topk_stride = 0;
+    p.valid = is_valid_token;
+    p.out = out_indices;
+    p.out_stride = out_stride;
+    p.lens = out_lens;
+    return cuda_status(psk::launch_index_build(p, true, reinterpret_cast<cudaStream_t>(stream)),
+                       "decode_swa_indices_and_lens launch");
+}
+
+psk_status compute_dense_compressed_indices_and_lens(
+    const int64_t* positions, int64_t num_tokens, const int32_t* token_to_req, int32_t num_reqs,
+    const int32_t* block_table, int64_t bt_stride, int32_t bt_width, const int32_t* base_offsets,
+    int32_t block_size, int32_t compress_ratio, int32_t width, const uint8_t* is_valid_token,
+    int32_t* out_indices, int64_t out_stride, int32_t* out_lens, psk_stream_t stream) {
+    CHECK(num_tokens >= 0, "num_tokens must be >= 0");
+    CHECK(width >= 0, "width must be >= 0");
+    CHECK(compress_ratio >= 1, "compress_ratio must be >= 1");
+    CHECK(block_size >= 1, "block_size must be >= 1");
+    CHECK(bt_width >= 0 && bt_stride >= bt_width, "need 0 <= bt_width <= bt_stride");
+    CHECK(out_stride >= width, "out_stride must be >= width");
+    if (num_tokens == 0) return ok();
+    CHECK(num_reqs >= 1, "num_reqs must be >= 1");
+    CHECK(positions && token_to_req && out_lens,
+          "positions, token_to_req and out_lens must be non-null");
+    CHECK(width == 0 || out_indices, "out_indices must be non-null");
+    CHECK(bt_width == 0 || block_table, "block_table must be non-null");
+    CHECK(aligned(positions, 8), "positions must be 8-byte aligned");
+    CHECK(aligned(token_to_req, 4) && aligned(block_table, 4) && aligned(base_offsets, 4) &&
+              aligned(out_indices, 4) && aligned(out_lens, 4),
+          "int32 arrays must be 4-byte aligned");
+    CHECK(num_tokens <= ((int64_t)INT32_MAX * 256) / (width > 0 ? width : 1),
+          "num_tokens x width is too large");
+    psk::DenseParams p{positions, num_tokens, token_to_req, num_reqs, block_table, bt_stride,
+                       bt_width, base_offsets, block_size, compress_ratio, width, is_valid_token,
+                       out_indices, out_stride, out_lens};
+    return cuda_status(psk::launch_dense_indices(p, true, reinterpret_cast<cudaStream_t>(stream)),
+                       "compute_dense_compressed_indices_and_lens launch");
+}
+
+psk_status build_dense_prefill_local_compressed_indices(const int64_t* positions,
+                                                        int64_t num_tokens,
+                                                        int32_t compress_ratio, int32_t width,
+                                                        int32_t* out, int64_t out_stride,
+                                                        psk_stream_t stream) {
+    CHECK(num_tokens >= 0, "num_tokens must be >= 0");
+    CHECK(width >= 0, "width must be >= 0");
+    CHECK(compress_ratio >= 1, "compress_ratio must be >= 1");
+    CHECK(out_stride >= width, "out_stride must be >= width");
+    if (num_tokens == 0 || width == 0) return ok();
+    CHECK(positions && out, "positions and out must be non-null");
+    CHECK(aligned(positions, 8), "positions must be 8-byte aligned");
+    CHECK(aligned(out, 4), "out must be 4-byte aligned");
+    CHECK(num_tokens <= ((int64_t)INT32_MAX * 256) / width, "num_tokens x width is too large");
+    psk::DenseParams p{};
+    p.positions = positions;
+    p.num_tokens = num_tokens;
+    p.ratio = compress_ratio;
+    p.width = width;
+    p.bs = 1;
+    p.out = out;
+    p.out_stride = out_stride;
+    return cuda_status(psk::launch_dense_indices(p, false, reinterpret_cast<cudaStream_t>(stream)),
+                       "build_dense_prefill_local_compressed_indices launch");
+}
+
+psk_status combine_dense_swa_indices(const int64_t* positions, const int32_t* token_to_req,
+                                     const int32_t* seq_lens, const int32_t* gather_lens,
+                                     int32_t num_reqs, int64_t num_tokens, int32_t window,
+                                     int64_t workspace_width, int64_t compressed_base,
+                                     int32_t* indices, int64_t out_stride, int32_t* lens,
+                                     psk_stream_t stream) {
+    CHECK(num_tokens >= 0, "num_tokens must be >= 0");
+    CHECK(window >= 0, "window must be >= 0");
+    CHECK(workspace_width >= 0 && compressed_base >= 0,
+          "workspace_width and compressed_base must be >= 0");
+    CHECK(out_stride >= window, "out_stride must be >= window");
+    if (num_tokens == 0) return ok();
+    CHECK(num_reqs >= 1, "num_reqs must be >= 1");
+    CHECK(positions && token_to_req && seq_lens && gather_lens && indices && lens,
+          "positions, token_to_req, seq_lens, gather_lens, indices and lens must be non-null");
+    CHECK(aligned(positions, 8), "positions must be 8-byte aligned");
+    CHECK(aligned(token_to_req, 4) && aligned(seq_lens, 4) && aligned(gather_lens, 4) &&
+              aligned(indices, 4) && aligned(lens, 4),
+          "int32 arrays must be 4-byte aligned");
+    psk::WorkspaceIndexParams p{nullptr, seq_lens, gather_lens, token_to_req, num_reqs,
+                                num_tokens, window, 1, nullptr, 0, 0, workspace_width,
+                                compressed_base, nullptr, indices, out_stride, lens, positions};
+    return cuda_status(psk::launch_workspace_indices(p, reinterpret_cast<cudaStream_t>(stream)),
+                       "combine_dense_swa_indices launch");
 }
 
 }  // extern "C"

@@ -20,6 +20,7 @@
 //  * lens is a warp reduction (__reduce_add_sync) of per-lane valid counts,
 //    combined across the warps of a token in shared memory when a token is
 //    split over several warps (small batches: every SM gets work).
+#include <algorithm>
 #include <climits>
 
 #include "launch.h"
@@ -575,9 +576,13 @@ __global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceInde
             }
             m.ok = (p.valid == nullptr || __ldg(p.valid + t) != 0) && r >= 0 && r < p.num_reqs;
             if (m.ok) {
-                const int64_t qs = __ldg(p.qsl + r), qe = __ldg(p.qsl + r + 1);
                 const int64_t seq = __ldg(p.seq_lens + r);
-                m.pos = seq - (qe - qs) + (t - qs);
+                if (p.positions) {
+                    m.pos = __ldg(p.positions + t);
+                } else {
+                    const int64_t qs = __ldg(p.qsl + r), qe = __ldg(p.qsl + r + 1);
+                    m.pos = seq - (qe - qs) + (t - qs);
+                }
                 m.g0 = seq - __ldg(p.gather_lens + r);
                 m.lc = seq / p.compress_ratio;
                 m.rbase = (int64_t)r * p.workspace_width;
@@ -668,6 +673,70 @@ __global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceInde
     if (copy_topk && !rows_ok && threadIdx.x == 0) mbar_wait_bounded(&s_bar, 0, kWaitLimitNs);
 }
 
+// ---- dense builders -------------------------------------------------------------------
+//
+// HCA decode (TokenSpeed backends/deepseek_v4.py,
+// _decode_compressed_attention_indices_and_lens for a ratio other than 4) and
+// the HCA prefill workspace's request-local form
+// (_dense_prefill_local_compressed_indices): token t sees
+// n = clamp(floor((pos + 1) / ratio), 0, width) compressed entries.  Every
+// entry is arithmetic on the position, so one thread owns one 16-byte quad of
+// one row (VEC) or one column; lens (= n, the global form) is written by the
+// row's first thread.  No reduction, no shared memory.
+
+// floor((pos + 1) / ratio) clamped to [0, width].
+__device__ __forceinline__ int32_t visible_entries(int64_t pos, int32_t ratio, int32_t width) {
+    const int64_t num = pos + 1;
+    if (num <= 0) return 0;
+    const int64_t n = num <= 0xFFFFFFFFll ? (int64_t)((uint32_t)num / (uint32_t)ratio)
+                                          : num / ratio;
+    return n < width ? (int32_t)n : width;
+}
+
+template <bool GLOBAL, bool VEC, bool POW2>
+__global__ void __launch_bounds__(kThreads) dense_index_kernel(DenseParams p, TableRow tr0) {
+    // at least one thread per row: it writes lens even when width is 0
+    const int per_row = max(VEC ? (p.width + 3) / 4 : p.width, 1);
+    const int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t t = g <= 0xFFFFFFFFll ? (int64_t)((uint32_t)g / (uint32_t)per_row) : g / per_row;
+    const int q = (int)(g - t * per_row);
+    pdl_wait();
+    pdl_launch_dependents();
+    if (t >= p.num_tokens) return;
+    int32_t* out = p.out + t * p.out_stride;
+    const int c0 = VEC ? 4 * q : q;
+    constexpr int E = VEC ? 4 : 1;
+    int v[4] = {-1, -1, -1, -1};
+    if (GLOBAL) {
+        const int32_t r = __ldg(p.t2r + t);
+        const bool ok = (p.valid == nullptr || __ldg(p.valid + t) != 0) && r >= 0 &&
+                        r < p.num_reqs;
+        int32_t n = 0;
+        if (ok) {
+            n = visible_entries(__ldg(p.positions + t), p.ratio, p.width);
+            TableRow tr = tr0;
+            tr.row = p.bt + (int64_t)r * p.bt_stride;
+            tr.base = p.base ? __ldg(p.base + r) : 0;
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                if (c0 + e < n) v[e] = map_slot<false, POW2>(tr, c0 + e);
+        }
+        if (q == 0) p.lens[t] = n;
+    } else {
+        const int32_t n = visible_entries(__ldg(p.positions + t), p.ratio, p.width);
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            if (c0 + e < n) v[e] = c0 + e;
+    }
+    if (VEC && c0 + 3 < p.width) {
+        *reinterpret_cast<int4*>(out + c0) = make_int4(v[0], v[1], v[2], v[3]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            if (c0 + e < p.width) out[c0 + e] = v[e];
+    }
+}
+
 // Raises a kernel's dynamic shared-memory limit when a launch needs more than
 // the default 48 KB (once per kernel and size class).
 template <typename Kern>
@@ -680,6 +749,29 @@ cudaError_t allow_dynamic_smem(Kern kern, size_t bytes) {
 
 cudaError_t read_index_wait_timeouts(uint32_t* count) {
     return cudaMemcpyFromSymbol(count, g_index_wait_timeouts, sizeof(uint32_t));
+}
+
+cudaError_t launch_dense_indices(const DenseParams& p, bool global, cudaStream_t stream) {
+    const bool vec = ((reinterpret_cast<uintptr_t>(p.out) & 15) == 0) && (p.out_stride % 4 == 0);
+    const int64_t per_row = std::max<int64_t>(vec ? (p.width + 3) / 4 : p.width, 1);
+    const int64_t threads = p.num_tokens * per_row;
+    const int64_t blocks = (threads + kThreads - 1) / kThreads;
+    TableRow tr{};
+    tr.width = p.bt_width;
+    tr.bs = p.bs;
+    tr.shift = log2_if_pow2(p.bs);
+    tr.maxp = INT_MAX / p.bs;
+    tr.maxrem = INT_MAX % p.bs;
+    const bool pow2 = tr.shift >= 0;
+    using Kern = void (*)(DenseParams, TableRow);
+    // [global][vec][pow2]
+    static const Kern kTable[2][2][2] = {
+        {{dense_index_kernel<false, false, false>, dense_index_kernel<false, false, true>},
+         {dense_index_kernel<false, true, false>, dense_index_kernel<false, true, true>}},
+        {{dense_index_kernel<true, false, false>, dense_index_kernel<true, false, true>},
+         {dense_index_kernel<true, true, false>, dense_index_kernel<true, true, true>}}};
+    return launch_pdl(kTable[global][vec][pow2], dim3((unsigned)blocks), dim3(kThreads), 0,
+                      stream, p, tr);
 }
 
 cudaError_t launch_workspace_indices(const WorkspaceIndexParams& p, cudaStream_t stream) {

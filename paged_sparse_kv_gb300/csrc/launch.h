@@ -155,9 +155,34 @@ struct WorkspaceIndexParams {
     int32_t* out;
     int64_t out_stride;
     int32_t* lens;
+    const int64_t* positions;  // non-null: token positions given (qsl unused)
 };
 
 cudaError_t launch_workspace_indices(const WorkspaceIndexParams& p, cudaStream_t stream);
+
+// Dense builders: every visible compressed entry of a token (HCA decode:
+// slots through the table + lens; prefill: request-local entry numbers).
+struct DenseParams {
+    const int64_t* positions;
+    int64_t num_tokens;
+    const int32_t* t2r;      // global form only
+    int32_t num_reqs;
+    const int32_t* bt;       // global form only
+    int64_t bt_stride;
+    int32_t bt_width;
+    const int32_t* base;
+    int32_t bs;
+    int32_t ratio;
+    int32_t width;
+    const uint8_t* valid;
+    int32_t* out;
+    int64_t out_stride;
+    int32_t* lens;           // global form only
+};
+
+// global = true: compute_dense_compressed_indices_and_lens; false:
+// build_dense_prefill_local_compressed_indices.
+cudaError_t launch_dense_indices(const DenseParams& p, bool global, cudaStream_t stream);
 
 struct RawGatherParams {
     uint8_t* values_out;

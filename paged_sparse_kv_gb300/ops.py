@@ -248,3 +248,93 @@ def indexer_mxfp4_paged_gather(cache: torch.Tensor, block_table: torch.Tensor,
               _rows(block_table, "block_table"), block_table.shape[1], _ptr(cu_seq_lens),
               cu_seq_lens.shape[0] - 1, total_rows, _stream(dev))
     return values_out, scales_out
+
+
+# ---- dense builders ---------------------------------------------------------------------
+
+def decode_swa_indices_and_lens(query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
+                                token_to_req: torch.Tensor, block_table: torch.Tensor,
+                                block_size: int, window_size: int, *,
+                                base_offsets: Optional[torch.Tensor] = None,
+                                is_valid_token: Optional[torch.Tensor] = None,
+                                out: Optional[torch.Tensor] = None,
+                                lens: Optional[torch.Tensor] = None):
+    """Window-only slot indices of decode tokens; returns (indices [T, W], lens [T])."""
+    _need_cuda(query_start_loc, seq_lens, token_to_req, block_table, base_offsets,
+               is_valid_token)
+    dev = token_to_req.device
+    T = token_to_req.shape[0]
+    if out is None:
+        out = torch.empty((T, window_size), dtype=torch.int32, device=dev)
+    if lens is None:
+        lens = torch.empty((T,), dtype=torch.int32, device=dev)
+    valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
+    _abi.call("decode_swa_indices_and_lens", _ptr(query_start_loc), _ptr(seq_lens),
+              _ptr(token_to_req), seq_lens.shape[0], T, _ptr(block_table),
+              _rows(block_table, "block_table"), block_table.shape[1], _ptr(base_offsets),
+              block_size, window_size, _ptr(valid), _ptr(out), _rows(out, "out"), _ptr(lens),
+              _stream(dev))
+    return out, lens
+
+
+def compute_dense_compressed_indices_and_lens(positions: torch.Tensor,
+                                              token_to_req: torch.Tensor,
+                                              block_table: torch.Tensor, block_size: int,
+                                              compress_ratio: int, width: int, *,
+                                              num_reqs: Optional[int] = None,
+                                              base_offsets: Optional[torch.Tensor] = None,
+                                              is_valid_token: Optional[torch.Tensor] = None,
+                                              out: Optional[torch.Tensor] = None,
+                                              lens: Optional[torch.Tensor] = None):
+    """Slots of every visible compressed entry; returns (indices [T, width], lens [T])."""
+    _need_cuda(positions, token_to_req, block_table, base_offsets, is_valid_token)
+    _need(positions, torch.int64, "positions")
+    dev = positions.device
+    T = positions.shape[0]
+    if out is None:
+        out = torch.empty((T, width), dtype=torch.int32, device=dev)
+    if lens is None:
+        lens = torch.empty((T,), dtype=torch.int32, device=dev)
+    valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
+    R = block_table.shape[0] if num_reqs is None else num_reqs
+    _abi.call("compute_dense_compressed_indices_and_lens", _ptr(positions), T,
+              _ptr(token_to_req), R, _ptr(block_table), _rows(block_table, "block_table"),
+              block_table.shape[1], _ptr(base_offsets), block_size, compress_ratio, width,
+              _ptr(valid), _ptr(out), _rows(out, "out"), _ptr(lens), _stream(dev))
+    return out, lens
+
+
+def build_dense_prefill_local_compressed_indices(positions: torch.Tensor, compress_ratio: int,
+                                                 width: int, *,
+                                                 out: Optional[torch.Tensor] = None):
+    """Request-local dense compressed indices [T, width] (j, or -1 past the visible count)."""
+    _need_cuda(positions)
+    _need(positions, torch.int64, "positions")
+    dev = positions.device
+    T = positions.shape[0]
+    if out is None:
+        out = torch.empty((T, width), dtype=torch.int32, device=dev)
+    _abi.call("build_dense_prefill_local_compressed_indices", _ptr(positions), T,
+              compress_ratio, width, _ptr(out), _rows(out, "out"), _stream(dev))
+    return out
+
+
+def combine_dense_swa_indices(positions: torch.Tensor, token_to_req: torch.Tensor,
+                              seq_lens: torch.Tensor, gather_lens: torch.Tensor,
+                              window_size: int, workspace_width: int, compressed_base: int = 0,
+                              *, out: Optional[torch.Tensor] = None,
+                              lens: Optional[torch.Tensor] = None):
+    """Workspace-relative window indices of layers without a compressed cache;
+    returns (indices [T, W], lens [T])."""
+    _need_cuda(positions, token_to_req, seq_lens, gather_lens)
+    _need(positions, torch.int64, "positions")
+    dev = positions.device
+    T = positions.shape[0]
+    if out is None:
+        out = torch.empty((T, window_size), dtype=torch.int32, device=dev)
+    if lens is None:
+        lens = torch.empty((T,), dtype=torch.int32, device=dev)
+    _abi.call("combine_dense_swa_indices", _ptr(positions), _ptr(token_to_req), _ptr(seq_lens),
+              _ptr(gather_lens), seq_lens.shape[0], T, window_size, workspace_width,
+              compressed_base, _ptr(out), _rows(out, "out"), _ptr(lens), _stream(dev))
+    return out, lens

@@ -38,6 +38,14 @@ raw:
              combine_topk_swa_workspace_indices
   stream A:  quantize_and_insert_k_cache -> dequantize_and_gather_k_cache_ranges[swa]
   stream B:  write_indexer_mxfp4_cache -> indexer_mxfp4_paged_gather
+
+``path="dense"`` is the decode step of a heavily compressed attention layer
+(no top-k; TokenSpeed's decode SWA precompute and
+``_decode_compressed_attention_indices_and_lens`` for a ratio other than 4):
+
+  stream M:  decode_swa_indices_and_lens -> (wait for the insert) -> gather[swa]
+  stream A:  quantize_and_insert_k_cache
+  stream B:  compute_dense_compressed_indices_and_lens -> gather[compressed]
 """
 from __future__ import annotations
 
@@ -164,6 +172,45 @@ class Pipeline:
                 scales_out=self.raw_scales)),
         ]
 
+    def alloc_dense(self) -> None:
+        """Buffers of the dense (no top-k) decode step."""
+        w, dev = self.w, self.dev
+        T, W, Wd = w.num_tokens, w.window, w.dense_width
+        self.positions = _dev_i64(w.positions, dev)
+        self.swa_indices = torch.empty((T, W), dtype=torch.int32, device=dev)
+        self.swa_lens = torch.empty((T,), dtype=torch.int32, device=dev)
+        self.dense_indices = torch.empty((T, Wd), dtype=torch.int32, device=dev)
+        self.dense_lens = torch.empty((T,), dtype=torch.int32, device=dev)
+        self.dense_gathered = torch.empty((T, W + Wd, w.head_dim), dtype=torch.bfloat16,
+                                          device=dev)
+
+    def dense_launches(self) -> list[tuple[str, Callable[[], None]]]:
+        """The dense decode step as (kernel name, launch) pairs, in order."""
+        w = self.w
+        if getattr(self, "dense_indices", None) is None:
+            self.alloc_dense()
+        W = w.window
+        return [
+            ("quantize_and_insert_k_cache", lambda: ops.quantize_and_insert_k_cache(
+                self.k, self.swa_cache, self.insert_slots, w.swa_cache.block_size,
+                rope_dim=w.rope_dim, err_count=self.err)),
+            ("decode_swa_indices_and_lens", lambda: ops.decode_swa_indices_and_lens(
+                self.qsl, self.seq_lens, self.t2r, self.swa_bt, w.swa_cache.block_size, W,
+                is_valid_token=self.valid, out=self.swa_indices, lens=self.swa_lens)),
+            ("compute_dense_compressed_indices_and_lens",
+             lambda: ops.compute_dense_compressed_indices_and_lens(
+                 self.positions, self.t2r, self.comp_bt, w.comp_cache.block_size,
+                 w.compress_ratio, w.dense_width, is_valid_token=self.valid,
+                 out=self.dense_indices, lens=self.dense_lens)),
+            ("dequantize_and_gather_k_cache[swa]", lambda: ops.dequantize_and_gather_k_cache(
+                self.dense_gathered[:, :W, :], self.swa_cache, self.swa_indices,
+                w.swa_cache.block_size, rope_dim=w.rope_dim)),
+            ("dequantize_and_gather_k_cache[compressed]",
+             lambda: ops.dequantize_and_gather_k_cache(
+                 self.dense_gathered[:, W:, :], self.comp_cache, self.dense_indices,
+                 w.comp_cache.block_size, rope_dim=w.rope_dim)),
+        ]
+
     # the indexer cache follows the compressed table
     @property
     def index_table(self) -> torch.Tensor:
@@ -232,6 +279,8 @@ class Pipeline:
         (used to bracket one kernel with timing events)."""
         if path == "workspace":
             return self._workspace_step(concurrent, hooks or {})
+        if path == "dense":
+            return self._dense_step(concurrent, hooks or {})
         L = dict(self.launches())
         hooks = hooks or {}
 
@@ -313,6 +362,44 @@ class Pipeline:
         run("dequantize_and_gather_k_cache_ranges[compressed]")
         run("combine_topk_swa_workspace_indices")
         main.wait_event(done_a)
+        main.wait_event(done_b)
+
+
+    def _dense_step(self, concurrent: bool, hooks: dict) -> None:
+        L = dict(self.dense_launches())
+
+        def run(name):
+            pre, post = hooks.get(name, (None, None))
+            if pre:
+                pre()
+            L[name]()
+            if post:
+                post()
+
+        if not concurrent:
+            for name in L:
+                run(name)
+            return
+        main = torch.cuda.current_stream(self.dev)
+        if not hasattr(self, "_side"):
+            self._side = (torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev))
+        sa, sb = self._side
+        fork = torch.cuda.Event()
+        fork.record(main)
+        sa.wait_event(fork)
+        sb.wait_event(fork)
+        with torch.cuda.stream(sb):
+            run("compute_dense_compressed_indices_and_lens")
+            run("dequantize_and_gather_k_cache[compressed]")
+            done_b = torch.cuda.Event()
+            done_b.record(sb)
+        with torch.cuda.stream(sa):
+            run("quantize_and_insert_k_cache")
+            inserted = torch.cuda.Event()
+            inserted.record(sa)
+        run("decode_swa_indices_and_lens")
+        main.wait_event(inserted)
+        run("dequantize_and_gather_k_cache[swa]")
         main.wait_event(done_b)
 
 

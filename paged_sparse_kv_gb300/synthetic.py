@@ -24,8 +24,13 @@ measure on no public dataset, so every input here is synthetic:
 * ``mxfp4``   1,048,576 indexer-key rows [*, 128] into a 1,048,576-slot MXFP4
               cache (random-permutation slot mapping); 128 decode tokens at
               context 131072, top-k 2048 over 32768 compressed entries.
+* ``decode_hca`` the decode batch of a layer with heavily compressed attention
+              (compress ratio 128, no indexer): 64 requests x 1 token, context
+              U[1024, 8192], window 128, every visible compressed entry
+              (dense width 64 = 8192 / 128).
 
-Seeds are ``20261202 + index`` in the order above.
+Seeds are ``20261202 + index`` in the order above (``prefill_small`` +5,
+``decode_hca`` +6).
 """
 from __future__ import annotations
 
@@ -80,6 +85,9 @@ class Workload:
     index_cache: Optional[CacheGeom]
     # which steps the workload runs
     has_fp8: bool = True
+    # dense builders: token positions and the dense compressed width (0: none)
+    positions: Optional[np.ndarray] = None  # int64 [T]
+    dense_width: int = 0
 
     @property
     def num_tokens(self) -> int:
@@ -339,10 +347,45 @@ def make_prefill_small(seed: int = BASE_SEED + 5) -> Workload:
     return make_prefill(seed, num_reqs=1)
 
 
+def make_decode_hca(seed: int = BASE_SEED + 6) -> Workload:
+    """Decode batch of a heavily compressed (ratio 128) attention layer: no
+    top-k and no indexer; each token attends to its window and to every
+    compressed entry its position has completed."""
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator().manual_seed(seed)
+    R, bs, D, rope, W, ratio, ctx = 64, 64, 512, 64, 128, 128, 8192
+    L = rng.integers(1024, ctx, size=R, endpoint=True).astype(np.int32)
+    pos = L.astype(np.int64) - 1
+    swa_counts = [(int(x) + bs - 1) // bs for x in L]
+    swa_pages = int(sum(swa_counts))
+    swa_table = _tables_from_page_counts(rng, swa_counts, swa_pages, max(swa_counts))
+    Lc = (pos + 1) // ratio
+    comp_counts = [max(1, (int(c) + bs - 1) // bs) for c in Lc]
+    comp_pages = int(sum(comp_counts))
+    comp_table = _tables_from_page_counts(rng, comp_counts, comp_pages, max(comp_counts))
+    insert = np.array([_page_slots(swa_table[r], bs)[pos[r]] for r in range(R)], dtype=np.int64)
+    width = (ctx + ratio - 1) // ratio
+    return Workload(
+        name="decode_hca", seed=seed, head_dim=D, rope_dim=rope, index_head_dim=128,
+        window=W, compress_ratio=ratio, topk=0,
+        k=_randn_bf16(gen, R, D), insert_slots=insert,
+        index_k=None, index_insert_slots=None,
+        query_start_loc=np.arange(R + 1, dtype=np.int32), seq_lens=L,
+        token_to_req=np.arange(R, dtype=np.int32),
+        replay_start=np.zeros(R, dtype=np.int32), is_valid_token=None,
+        swa_block_table=swa_table, comp_block_table=comp_table,
+        topk_local=np.zeros((R, 0), dtype=np.int32),
+        swa_cache=CacheGeom(swa_pages, bs, bs * fp8_record_bytes(D, rope)),
+        comp_cache=CacheGeom(comp_pages, bs, bs * fp8_record_bytes(D, rope)),
+        index_cache=None, positions=pos, dense_width=width)
+
+
 MAKERS = {"tiny": make_tiny, "decode": make_decode, "prefill": make_prefill,
-          "mixed": make_mixed, "mxfp4": make_mxfp4, "prefill_small": make_prefill_small}
+          "mixed": make_mixed, "mxfp4": make_mxfp4, "prefill_small": make_prefill_small,
+          "decode_hca": make_decode_hca}
 DEFAULT_SEEDS = {"tiny": BASE_SEED + 0, "decode": BASE_SEED + 1, "prefill": BASE_SEED + 2,
-                 "mixed": BASE_SEED + 3, "mxfp4": BASE_SEED + 4, "prefill_small": BASE_SEED + 5}
+                 "mixed": BASE_SEED + 3, "mxfp4": BASE_SEED + 4, "prefill_small": BASE_SEED + 5,
+                 "decode_hca": BASE_SEED + 6}
 
 
 def make(name: str, seed_offset: int = 0) -> Workload:

@@ -214,3 +214,80 @@ def _raw(**kw):
                                 dict(s=A + 4098), dict(n=-1), dict(page_stride=64 * 68 - 16)])
 def test_mxfp4_raw_gather_rejects_bad_arguments(psk_lib, kw):
     assert _raw(**kw) == INV
+
+
+def _dswa(**kw):
+    a = dict(qsl=A, seq=A + 256, t2r=A + 512, R=2, n=3, bt=B, bts=4, btw=4, base=None, bs=16,
+             W=8, valid=None, out=C, os=8, lens=C + 4096)
+    a.update(kw)
+    return _abi.status("decode_swa_indices_and_lens", a["qsl"], a["seq"], a["t2r"], a["R"], a["n"],
+                       a["bt"], a["bts"], a["btw"], a["base"], a["bs"], a["W"], a["valid"],
+                       a["out"], a["os"], a["lens"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(W=-1), dict(bs=0), dict(btw=5), dict(os=7), dict(R=0),
+                                dict(qsl=None), dict(out=None), dict(lens=None), dict(bt=None),
+                                dict(out=C + 2), dict(n=-1)])
+def test_decode_swa_rejects_bad_arguments(psk_lib, kw):
+    assert _dswa(**kw) == INV
+
+
+def test_decode_swa_zero_tokens_ok(psk_lib):
+    assert _dswa(n=0, qsl=None, out=None, lens=None) == OK
+
+
+def _dense(**kw):
+    a = dict(pos=A, n=3, t2r=A + 256, R=2, bt=B, bts=4, btw=4, base=None, bs=16, ratio=128,
+             width=64, valid=None, out=C, os=64, lens=C + 8192)
+    a.update(kw)
+    return _abi.status("compute_dense_compressed_indices_and_lens", a["pos"], a["n"], a["t2r"],
+                       a["R"], a["bt"], a["bts"], a["btw"], a["base"], a["bs"], a["ratio"],
+                       a["width"], a["valid"], a["out"], a["os"], a["lens"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(width=-1), dict(ratio=0), dict(bs=0), dict(os=63),
+                                dict(btw=5), dict(R=0), dict(pos=None), dict(pos=A + 4),
+                                dict(out=None), dict(lens=None), dict(t2r=None), dict(n=-2)])
+def test_dense_compressed_rejects_bad_arguments(psk_lib, kw):
+    assert _dense(**kw) == INV
+
+
+def test_dense_compressed_zero_tokens_ok(psk_lib):
+    assert _dense(n=0, pos=None, out=None, lens=None) == OK
+
+
+def _local(**kw):
+    a = dict(pos=A, n=3, ratio=128, width=64, out=C, os=64)
+    a.update(kw)
+    return _abi.status("build_dense_prefill_local_compressed_indices", a["pos"], a["n"],
+                       a["ratio"], a["width"], a["out"], a["os"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(width=-1), dict(ratio=0), dict(os=63), dict(pos=None),
+                                dict(out=None), dict(pos=A + 4), dict(out=C + 2), dict(n=-1)])
+def test_dense_local_rejects_bad_arguments(psk_lib, kw):
+    assert _local(**kw) == INV
+
+
+def test_dense_local_zero_work_ok(psk_lib):
+    assert _local(n=0, pos=None, out=None) == OK
+    assert _local(width=0, os=0, pos=None, out=None) == OK
+
+
+def _dswa_ws(**kw):
+    a = dict(pos=A, t2r=A + 256, seq=A + 512, glen=A + 768, R=2, n=3, W=8, ww=100, cb=10, out=C,
+             os=8, lens=C + 4096)
+    a.update(kw)
+    return _abi.status("combine_dense_swa_indices", a["pos"], a["t2r"], a["seq"], a["glen"],
+                       a["R"], a["n"], a["W"], a["ww"], a["cb"], a["out"], a["os"], a["lens"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(W=-1), dict(ww=-1), dict(cb=-1), dict(os=7), dict(R=0),
+                                dict(pos=None), dict(glen=None), dict(out=None), dict(lens=None),
+                                dict(pos=A + 4), dict(seq=A + 514)])
+def test_dense_swa_rejects_bad_arguments(psk_lib, kw):
+    assert _dswa_ws(**kw) == INV
+
+
+def test_dense_swa_zero_tokens_ok(psk_lib):
+    assert _dswa_ws(n=0, pos=None, out=None, lens=None) == OK
