@@ -260,33 +260,36 @@ def _graph_events_supported(torch) -> bool:
         return False
 
 
-# CUDA source file of each timed entry point (plus the shared headers).
+# CUDA sources of each timed entry point: its kernel file and that family's
+# header (plus the shared headers).
+_FAMILY = {"insert": ("insert.cu", "insert.h"), "index": ("index_build.cu", "index_build.h"),
+           "gather": ("gather.cu", "gather.h")}
 KERNEL_SOURCES = {
-    "quantize_and_insert_k_cache": "insert.cu",
-    "write_indexer_mxfp4_cache": "insert.cu",
-    "combine_topk_swa_indices": "index_build.cu",
-    "compute_global_topk_indices_and_lens": "index_build.cu",
-    "combine_topk_swa_workspace_indices": "index_build.cu",
-    "decode_swa_indices_and_lens": "index_build.cu",
-    "compute_dense_compressed_indices_and_lens": "index_build.cu",
-    "build_dense_prefill_local_compressed_indices": "index_build.cu",
-    "combine_dense_swa_indices": "index_build.cu",
-    "dequantize_and_gather_k_cache": "gather.cu",
-    "dequantize_and_gather_k_cache_ranges": "gather.cu",
-    "indexer_mxfp4_paged_gather": "gather.cu",
+    "quantize_and_insert_k_cache": _FAMILY["insert"],
+    "write_indexer_mxfp4_cache": _FAMILY["insert"],
+    "combine_topk_swa_indices": _FAMILY["index"],
+    "compute_global_topk_indices_and_lens": _FAMILY["index"],
+    "combine_topk_swa_workspace_indices": _FAMILY["index"],
+    "decode_swa_indices_and_lens": _FAMILY["index"],
+    "compute_dense_compressed_indices_and_lens": _FAMILY["index"],
+    "build_dense_prefill_local_compressed_indices": _FAMILY["index"],
+    "combine_dense_swa_indices": _FAMILY["index"],
+    "dequantize_and_gather_k_cache": _FAMILY["gather"],
+    "dequantize_and_gather_k_cache_ranges": _FAMILY["gather"],
+    "indexer_mxfp4_paged_gather": _FAMILY["gather"],
 }
 SHARED_SOURCES = ("psk_common.cuh", "launch.h")
 
 
 def kernel_source_hash(kernel: str) -> str:
-    """sha1 over the CUDA sources a timed kernel is built from (its .cu file
-    and the shared headers); identifies the build a recorded ncu capture
-    belongs to."""
+    """sha1 over the CUDA sources a timed kernel is built from (its .cu file,
+    its family's header and the shared headers); identifies the build a
+    recorded ncu capture belongs to."""
     import hashlib
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "paged_sparse_kv_gb300", "csrc")
     base = kernel.split("[")[0]
-    for f in sorted((KERNEL_SOURCES[base],) + SHARED_SOURCES):
+    for f in sorted(KERNEL_SOURCES[base] + SHARED_SOURCES):
         h.update(f.encode())
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()

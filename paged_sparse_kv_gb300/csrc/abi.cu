@@ -10,6 +10,9 @@
 #include <cstring>
 #include <string>
 
+#include "gather.h"
+#include "index_build.h"
+#include "insert.h"
 #include "launch.h"
 #include "psk.h"
 #include "psk_common.cuh"

@@ -16,7 +16,7 @@
 // exact: cvt.rn.f16x2.{e4m3x2,e2m1x2}, a binary32 multiply by the scale, and
 // cvt.rn.bf16x2.f32.  Invalid slots (negative or beyond the cache) give zero
 // rows.  The scale multiply is one packed mul.rn.f32x2 per pair of elements.
-#include "launch.h"
+#include "gather.h"
 #include "psk_common.cuh"
 
 namespace psk {

@@ -1,0 +1,80 @@
+// gather.h -- parameters and launchers of the dequantize-and-gather kernels (internal).
+#pragma once
+
+#include "launch.h"
+
+namespace psk {
+
+struct GatherParams {
+    uint16_t* out;
+    int64_t out_stride_t;
+    int64_t out_stride_j;
+    const uint8_t* cache;
+    int64_t num_pages;
+    int64_t page_stride;
+    int32_t block_size;
+    int32_t record;
+    int32_t head_dim;
+    int32_t rope_dim;
+    int32_t is_ue8m0;
+    const int32_t* idx;
+    int64_t idx_stride;
+    int64_t rows;
+    int32_t cols;
+    int32_t block_shift;  // log2(block_size) or -1; set by the launcher
+};
+
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
+
+// Range form: per request r, rows i < out_rows - offset; g = gather_lens[r]
+// (or seq_lens[r]); row i < g is position seq_lens[r] - g + i -> out row
+// offset + i; rows i >= g are not written.
+struct RangeParams {
+    uint16_t* out;
+    int64_t out_stride_r;
+    int64_t out_stride_i;
+    int64_t out_rows;
+    int64_t offset;
+    const uint8_t* cache;
+    int64_t num_pages;
+    int64_t page_stride;
+    int32_t block_size;
+    int32_t head_dim;
+    int32_t rope_dim;
+    int32_t is_ue8m0;
+    const int32_t* seq_lens;
+    const int32_t* gather_lens;
+    const int32_t* block_table;
+    int64_t bt_stride;
+    int32_t bt_width;
+    const int32_t* base_offsets;
+    int32_t num_reqs;
+};
+
+cudaError_t launch_gather_ranges(const RangeParams& p, cudaStream_t stream);
+
+struct RawGatherParams {
+    uint8_t* values_out;
+    uint8_t* scales_out;
+    const uint8_t* cache;
+    int64_t num_pages;
+    int64_t page_stride;
+    int32_t block_size;
+    int32_t head_dim;
+    const int32_t* block_table;
+    int64_t bt_stride;
+    int32_t bt_width;
+    const int32_t* cu_seq_lens;
+    int32_t num_reqs;
+    int64_t total_rows;
+    int32_t block_shift;  // log2(block_size) or -1; set by the launcher
+};
+
+cudaError_t launch_mxfp4_raw_gather(const RawGatherParams& p, cudaStream_t stream);
+
+// Number of bounded in-kernel waits that expired on the current device.
+
+// Count of expired bounded waits in the gather kernels.
+cudaError_t read_wait_timeouts(uint32_t* count);
+
+}  // namespace psk

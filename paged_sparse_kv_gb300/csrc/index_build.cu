@@ -23,7 +23,7 @@
 #include <algorithm>
 #include <climits>
 
-#include "launch.h"
+#include "index_build.h"
 #include "psk_common.cuh"
 
 namespace psk {

@@ -23,7 +23,7 @@
 //    written with a single aligned store.
 //  * Each group handles UNROLL tokens with all loads issued before any use,
 //    so enough bytes are in flight to cover HBM latency.
-#include "launch.h"
+#include "insert.h"
 #include "psk_common.cuh"
 
 namespace psk {
