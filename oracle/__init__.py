@@ -26,6 +26,7 @@ GCC_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
 
 REC_FP8_DS_MLA = 0
 REC_MXFP4 = 1
+REC_FP8_INDEXER = 2
 
 
 def build(force: bool = False) -> str:
@@ -96,6 +97,11 @@ def _load():
             None, [_P, _I64, _I32, _I32, _P, _I64]),
         "oracle_combine_dense_swa_indices": (
             None, [_P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64, _P, _I64, _P]),
+        "oracle_write_indexer_fp8_cache": (
+            _I64, [_P, _I64, _P, _I64, _P, _I64, _I64, _I32, _I32]),
+        "oracle_indexer_k_norm_rope_store": (
+            _I64, [_P, _I64, _P, _P, _I64, _I64, _P, ctypes.c_float, _P, _I64, _I32, _I32, _P,
+                   _I64, _I64, _I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -390,3 +396,37 @@ def combine_dense_swa_indices(positions, token_to_req, seq_lens, gather_lens, wi
         seq_lens.shape[0], T, window, workspace_width, compressed_base, _ptr(out), window,
         _ptr(lens))
     return out, lens
+
+
+# ---- indexer-key variants -------------------------------------------------------------
+
+def fp8_indexer_record_bytes(head_dim: int) -> int:
+    """head_dim e4m3 bytes + one binary32 scale."""
+    return head_dim + 4
+
+
+def write_indexer_fp8_cache(k, slots, cache, block_size, head_dim) -> int:
+    """FP8 indexer records (per-token power-of-two binary32 scale); returns the
+    count of out-of-range slots."""
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    slots = _as(slots, np.int64)
+    assert cache.dtype == np.uint8 and cache.ndim == 2 and cache.flags["C_CONTIGUOUS"]
+    return _load().oracle_write_indexer_fp8_cache(
+        _ptr(k), k.shape[1], _ptr(slots), slots.shape[0], _ptr(cache), cache.shape[0],
+        cache.shape[1], block_size, head_dim)
+
+
+def indexer_k_norm_rope_store(k_pre, positions, cos_sin_cache, rms_norm_weight, rms_norm_eps,
+                              slots, compress_ratio, record, cache, block_size) -> int:
+    """k_norm -> RoPE -> quant -> paged store of 128-dim indexer keys (record
+    REC_MXFP4 or REC_FP8_INDEXER); returns the count of skipped-and-counted rows."""
+    k_pre = np.ascontiguousarray(k_pre, dtype=np.uint16)
+    positions = _as(positions, np.int64)
+    cs = np.ascontiguousarray(cos_sin_cache, dtype=np.float32)
+    wt = np.ascontiguousarray(rms_norm_weight, dtype=np.float32)
+    slots = _as(slots, np.int64)
+    assert cache.dtype == np.uint8 and cache.ndim == 2 and cache.flags["C_CONTIGUOUS"]
+    return _load().oracle_indexer_k_norm_rope_store(
+        _ptr(k_pre), k_pre.shape[1], _ptr(positions), _ptr(cs), cs.shape[1], cs.shape[0],
+        _ptr(wt), float(rms_norm_eps), _ptr(slots), slots.shape[0], compress_ratio, record,
+        _ptr(cache), cache.shape[0], cache.shape[1], block_size)

@@ -493,6 +493,8 @@ void oracle_combine_topk_swa_indices(
  *               rope dims -> the stored bf16 bit patterns.
  *   MXFP4:      dim d -> bf16(e2m1(nibble d) * 2^(scale[d/32] - 127)), nibble
  *               d is the low half of byte d/2 for even d, the high half for odd.
+ *   FP8 indexer (record 2, [OPS] write_deepseek_v4_indexer_fp8_cache):
+ *               dim d -> bf16(e4m3(byte d) * scale_f32).
  * Products are formed in binary32 and rounded once more to bf16.
  */
 void oracle_dequantize_and_gather_k_cache(
@@ -534,7 +536,7 @@ void oracle_dequantize_and_gather_k_cache(
                     const uint8_t* p = data + nope + 2 * (int64_t)(d - nope);
                     o[d] = (uint16_t)(p[0] | (p[1] << 8));
                 }
-            } else {
+            } else if (record == 1) {
                 const int64_t vbytes = head_dim / 2, sbytes = head_dim / 32;
                 const uint8_t* vals = base + off * vbytes;
                 const uint8_t* scl = base + (int64_t)block_size * vbytes + off * sbytes;
@@ -544,6 +546,13 @@ void oracle_dequantize_and_gather_k_cache(
                     float f = oracle_e2m1_decode(nib) * pow2f((int)scl[d / 32] - 127);
                     o[d] = oracle_bf16_from_f32(f);
                 }
+            } else {
+                /* FP8 indexer record: head_dim e4m3 bytes, one binary32 scale */
+                const uint8_t* vals = base + off * head_dim;
+                float sc;
+                memcpy(&sc, base + (int64_t)block_size * head_dim + off * 4, 4);
+                for (int32_t d = 0; d < head_dim; ++d)
+                    o[d] = oracle_bf16_from_f32(oracle_e4m3_decode(vals[d]) * sc);
             }
         }
     }
@@ -846,4 +855,179 @@ void oracle_combine_dense_swa_indices(
         }
         lens[t] = count;
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Indexer-key variants: the FP8 indexer record and indexer_k_norm_rope_store */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Per-row FP8 quantization with one power-of-two binary32 scale ([OPS]
+ * _fp8_e4m3_pow2_bytes and _write_deepseek_v4_indexer_fp8_cache_capturable):
+ * scale = 2^ceil(log2(max(amax / 448, 1e-10))) -- the quotient is floored, not
+ * amax; the ceiling is taken exactly on the binary32 quotient, as for the
+ * UE8M0 record -- and code = e4m3(clamp(x / scale, -448, 448)).  Returns the
+ * scale.
+ */
+static float fp8_pow2_row(const float* x, int32_t n, uint8_t* codes) {
+    float amax = 0.0f;
+    for (int32_t i = 0; i < n; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    float q = amax / 448.0f;
+    if (q < 1.0e-10f) q = 1.0e-10f;
+    const float scale = pow2f(oracle_ceil_log2(q));
+    for (int32_t i = 0; i < n; ++i) {
+        float v = x[i] / scale;
+        if (v > 448.0f) v = 448.0f;
+        if (v < -448.0f) v = -448.0f;
+        codes[i] = oracle_e4m3_encode(v);
+    }
+    return scale;
+}
+
+/*
+ * Per-32-block MXFP4 quantization of binary32 values, the rule of
+ * oracle_write_indexer_mxfp4_cache: e = ceil(log2(max(amax, 1e-4) / 6)), scale
+ * byte clamp(e + 127, 0, 254), code = e2m1(x * 2^-e), even element in the low
+ * nibble.
+ */
+static void mxfp4_row(const float* x, int32_t n, uint8_t* vals, uint8_t* scl) {
+    for (int32_t b = 0; b < n / 32; ++b) {
+        float amax = 0.0f;
+        for (int j = 0; j < 32; ++j) {
+            float a = fabsf(x[b * 32 + j]);
+            if (a > amax) amax = a;
+        }
+        float a = (amax < 1.0e-4f) ? 1.0e-4f : amax;
+        int32_t e = oracle_ceil_log2(a / 6.0f);
+        int32_t byte = e + 127;
+        if (byte < 0) byte = 0;
+        if (byte > 254) byte = 254;
+        scl[b] = (uint8_t)byte;
+        float p = pow2f(-e);
+        for (int j = 0; j < 32; j += 2) {
+            uint8_t lo = oracle_e2m1_encode(x[b * 32 + j] * p);
+            uint8_t hi = oracle_e2m1_encode(x[b * 32 + j + 1] * p);
+            vals[(b * 32 + j) / 2] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
+/*
+ * [OPS] write_deepseek_v4_indexer_fp8_cache: FP8 indexer keys in the
+ * "[values | fp32 scale]" page layout.  Page: [block_size x head_dim e4m3
+ * bytes][block_size x 4-byte little-endian binary32 scales]; token off of a
+ * page at off * head_dim and block_size * head_dim + off * 4.  Slots < 0 are
+ * skipped; slots >= capacity are skipped and counted (returned).
+ */
+int64_t oracle_write_indexer_fp8_cache(
+    const uint16_t* k, int64_t k_row_stride, const int64_t* slot_mapping,
+    int64_t num_tokens, uint8_t* cache, int64_t num_pages,
+    int64_t page_stride, int32_t block_size, int32_t head_dim) {
+    const int64_t capacity = num_pages * (int64_t)block_size;
+    int64_t errors = 0;
+    float x[1024];
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        const int64_t s = slot_mapping[i];
+        if (s < 0) continue;
+        if (s >= capacity) {
+            ++errors;
+            continue;
+        }
+        const int64_t page = s / block_size, off = s % block_size;
+        uint8_t* base = cache + page * page_stride;
+        for (int32_t d = 0; d < head_dim; ++d) x[d] = oracle_bf16_to_f32(k[i * k_row_stride + d]);
+        const float scale = fp8_pow2_row(x, head_dim, base + off * head_dim);
+        memcpy(base + (int64_t)block_size * head_dim + off * 4, &scale, 4);
+    }
+    return errors;
+}
+
+/* Pairwise (recursive halving) binary32 sum of v[0..n), n a power of two. */
+static float pairwise_sum(const float* v, int32_t n) {
+    if (n == 1) return v[0];
+    return pairwise_sum(v, n / 2) + pairwise_sum(v + n / 2, n / 2);
+}
+
+/*
+ * [VLLM] indexer_k_norm_rope_store(k_pre, positions, cos_sin_cache,
+ * rms_norm_weight, rms_norm_eps, k_cache, kv_slot_mapping, compress_ratio,
+ * use_fp4_cache): k_norm -> RoPE -> quant -> paged store of 128-dim indexer
+ * keys (64 RoPE dims).  The kernel is not printed; the stages follow the
+ * pages' torch forms of the same steps:
+ *   emission: token t writes a key when kv_slot_mapping[t] >= 0 and it closes
+ *     its compress group, (positions[t] + 1) % ratio == 0 (the valid_token rule
+ *     of [OPS] _compress_v4_state_windows_capturable; "only group-boundary rows
+ *     are read");
+ *   RMSNorm ([OPS] _compress_v4_state_windows_capturable), binary32:
+ *     variance = (sum of x_d * x_d) / 128 with the sum taken pairwise
+ *     (recursive halving in index order -- a reading: no order is printed);
+ *     r = binary32 rounding of 1 / sqrt(variance + eps) with the square root
+ *     and the quotient in binary64 (a reading: the printed rsqrt is a binary32
+ *     library call of unstated accuracy); y_d = (x_d * r) * weight_d;
+ *   RoPE ([OPS] _apply_gptj_rope_tail_rows, GPT-J pairs on the last 64 dims):
+ *     for i < 32, e = y[64 + 2i], o = y[65 + 2i], c = cs[p][i], s = cs[p][32 + i]:
+ *     y[64 + 2i] = e*c - o*s, y[65 + 2i] = e*s + o*c (each product and sum
+ *     rounded to binary32), at the group's first position
+ *     p = floor(positions[t] / ratio) * ratio (the compressed_positions of
+ *     [OPS] deepseek_v4_csa_indexer_cache_insert);
+ *   quant + store: record 1 = the MXFP4 record, record 2 = the FP8 indexer
+ *     record, at kv_slot_mapping[t].
+ * Slots >= capacity and RoPE rows p outside [0, max_pos) are skipped and
+ * counted (returned).
+ */
+int64_t oracle_indexer_k_norm_rope_store(
+    const uint16_t* k_pre, int64_t k_row_stride, const int64_t* positions,
+    const float* cos_sin_cache, int64_t cs_stride, int64_t max_pos,
+    const float* rms_norm_weight, float rms_norm_eps,
+    const int64_t* slot_mapping, int64_t num_tokens, int32_t compress_ratio,
+    int32_t record, uint8_t* cache, int64_t num_pages, int64_t page_stride,
+    int32_t block_size) {
+    const int32_t D = 128, R = 64, nope = D - R;
+    const int64_t capacity = num_pages * (int64_t)block_size;
+    int64_t errors = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int64_t s = slot_mapping[t];
+        if (s < 0) continue;
+        const int64_t pos = positions[t];
+        /* group boundary: (pos + 1) mod ratio == 0 (floor modulus) */
+        int64_t m = (pos + 1) % compress_ratio;
+        if (m < 0) m += compress_ratio;
+        if (m != 0) continue;
+        /* floor(pos / ratio) * ratio */
+        int64_t q = pos / compress_ratio;
+        if (pos % compress_ratio != 0 && pos < 0) q -= 1;
+        const int64_t p = q * compress_ratio;
+        if (s >= capacity || p < 0 || p >= max_pos) {
+            ++errors;
+            continue;
+        }
+        float x[128], sq[128], y[128];
+        for (int32_t d = 0; d < D; ++d) {
+            x[d] = oracle_bf16_to_f32(k_pre[t * k_row_stride + d]);
+            sq[d] = x[d] * x[d];
+        }
+        const float variance = pairwise_sum(sq, D) / 128.0f;
+        const float r = (float)(1.0 / sqrt((double)(variance + rms_norm_eps)));
+        for (int32_t d = 0; d < D; ++d) y[d] = (x[d] * r) * rms_norm_weight[d];
+        const float* cs = cos_sin_cache + p * cs_stride;
+        for (int32_t i = 0; i < R / 2; ++i) {
+            const float e = y[nope + 2 * i], o = y[nope + 2 * i + 1];
+            const float c = cs[i], sn = cs[R / 2 + i];
+            const float ec = e * c, os = o * sn, es = e * sn, oc = o * c;
+            y[nope + 2 * i] = ec - os;
+            y[nope + 2 * i + 1] = es + oc;
+        }
+        const int64_t page = s / block_size, off = s % block_size;
+        uint8_t* base = cache + page * page_stride;
+        if (record == 1) {
+            mxfp4_row(y, D, base + off * (D / 2), base + (int64_t)block_size * (D / 2) + off * (D / 32));
+        } else {
+            const float scale = fp8_pow2_row(y, D, base + off * D);
+            memcpy(base + (int64_t)block_size * D + off * 4, &scale, 4);
+        }
+    }
+    return errors;
 }

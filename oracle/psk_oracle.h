@@ -13,7 +13,10 @@
  * library cast, brute-force enumeration of windows and slots, hand-worked
  * golden records, invariants).  One function has a weaker pin and is marked
  * "parity unpinned" where it is defined: the fp32-scale FP8 record
- * (is_ue8m0 = 0), whose rule no page prints.
+ * (is_ue8m0 = 0), whose rule no page prints.  indexer_k_norm_rope_store takes
+ * two readings (pairwise summation, binary64 reciprocal square root) that fix
+ * the rounding of steps the pages leave open; its pins check the arithmetic
+ * against closed forms, not a printed result.
  */
 #ifndef PSK_ORACLE_H
 #define PSK_ORACLE_H
@@ -130,6 +133,20 @@ void oracle_combine_dense_swa_indices(
     int64_t num_tokens, int32_t window, int64_t workspace_width,
     int64_t compressed_base, int32_t* indices, int64_t out_stride,
     int32_t* lens);
+
+/* ---- indexer-key variants ---- */
+int64_t oracle_write_indexer_fp8_cache(
+    const uint16_t* k, int64_t k_row_stride, const int64_t* slot_mapping,
+    int64_t num_tokens, uint8_t* cache, int64_t num_pages,
+    int64_t page_stride, int32_t block_size, int32_t head_dim);
+
+int64_t oracle_indexer_k_norm_rope_store(
+    const uint16_t* k_pre, int64_t k_row_stride, const int64_t* positions,
+    const float* cos_sin_cache, int64_t cs_stride, int64_t max_pos,
+    const float* rms_norm_weight, float rms_norm_eps,
+    const int64_t* slot_mapping, int64_t num_tokens, int32_t compress_ratio,
+    int32_t record, uint8_t* cache, int64_t num_pages, int64_t page_stride,
+    int32_t block_size);
 
 #ifdef __cplusplus
 }
