@@ -76,7 +76,8 @@ typedef enum psk_status {
 
 typedef enum psk_record {
     PSK_REC_FP8_DS_MLA = 0,
-    PSK_REC_MXFP4 = 1
+    PSK_REC_MXFP4 = 1,
+    PSK_REC_FP8_INDEXER = 2
 } psk_record;
 
 /* Message describing the calling thread's most recent error ("" if none). */
@@ -222,8 +223,9 @@ psk_status combine_topk_swa_indices(
 /*
  * dequantize_and_gather_k_cache -- index-keyed dequantize + gather.
  * Index form of [VLLM] dequantize_and_gather_k_cache; per-row math of [OPS]
- * dequantize_deepseek_v4_fp8_ds_mla_cache (record 0) and
- * read_deepseek_v4_indexer_mxfp4_cache (record 1).
+ * dequantize_deepseek_v4_fp8_ds_mla_cache (record 0),
+ * read_deepseek_v4_indexer_mxfp4_cache (record 1) and the FP8 indexer record
+ * of write_deepseek_v4_indexer_fp8_cache (record 2).
  *
  *   out          bf16; row (t, j) starts at out + t*out_stride_t + j*out_stride_j
  *                (elements, multiples of 8) and holds head_dim values.
@@ -232,8 +234,10 @@ psk_status combine_topk_swa_indices(
  *   For s = indices[t][j]: s < 0 or s >= num_pages * block_size gives an
  *   all-zero row.  Otherwise, fp8_ds_mla: nope dim d = bf16(e4m3 * 2^(scale-127))
  *   (or * fp32 scale when is_ue8m0 = 0), rope dims copied bit for bit; MXFP4:
- *   dim d = bf16(e2m1 * 2^(scale-127)).  Products are formed in binary32 and
- *   rounded to bf16 (for UE8M0 scales the product is exact).
+ *   dim d = bf16(e2m1 * 2^(scale-127)); FP8 indexer: dim d = bf16(e4m3 *
+ *   scale_f32).  Products are formed in binary32 and rounded to bf16 (for
+ *   power-of-two scales the product is exact).  MXFP4 and FP8 indexer records
+ *   take head_dim in {32, 64, ..., 1024} and rope_dim 0.
  *   To gather the window columns from the SWA cache and the top-k columns from
  *   the compressed cache, make two calls on column ranges of one index matrix
  *   and one output (pointer offsets + strides), as a k_cache / extra_k_cache
@@ -419,6 +423,63 @@ psk_status combine_dense_swa_indices(
     int64_t num_tokens, int32_t window, int64_t workspace_width,
     int64_t compressed_base, int32_t* indices, int64_t out_stride,
     int32_t* lens, psk_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Indexer-key variants: the FP8 indexer record and the fused k_norm ->      */
+/* RoPE -> quant -> store of indexer keys                                    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * write_indexer_fp8_cache -- FP8 indexer keys in the "[values | fp32 scale]"
+ * page layout.  TokenSpeed write_deepseek_v4_indexer_fp8_cache and its
+ * capturable form; the rule of _fp8_e4m3_pow2_bytes.
+ *
+ *   index_k   bf16 [num_tokens, head_dim], row stride k_row_stride (elements,
+ *             multiple of 8; 16-byte aligned).
+ *   Per token: scale = 2^ceil(log2(max(amax / 448, 1e-10))) (the exact ceiling
+ *   of the binary32 quotient), code = e4m3(clamp(x / scale, +-448)).
+ *   Page: [block_size x head_dim e4m3 bytes][block_size x 4-byte binary32
+ *   scales]; page_stride >= block_size * (head_dim + 4), a multiple of 16.
+ *   Slots < 0 are skipped; slots >= num_pages * block_size are skipped and
+ *   counted in *err_count (optional).  head_dim in {32, 64, ..., 1024}.
+ */
+psk_status write_indexer_fp8_cache(
+    const void* index_k, int64_t k_row_stride, const int64_t* slot_mapping,
+    int64_t num_tokens, uint8_t* cache, int64_t num_pages, int64_t page_stride,
+    int32_t block_size, int32_t head_dim, int32_t* err_count, psk_stream_t stream);
+
+/*
+ * indexer_k_norm_rope_store -- k_norm -> RoPE -> quant -> paged store of
+ * 128-dim indexer keys.  [VLLM] indexer_k_norm_rope_store(k_pre, positions,
+ * cos_sin_cache, rms_norm_weight, rms_norm_eps, k_cache, kv_slot_mapping,
+ * compress_ratio, use_fp4_cache); its kernel is not printed, so each stage
+ * follows the pages' torch form of it.
+ *
+ *   k_pre            bf16 [num_tokens, 128], row stride k_row_stride (elements,
+ *                    multiple of 4; 8-byte aligned).
+ *   positions        int64 [num_tokens].
+ *   cos_sin_cache    binary32 [max_pos, cs_stride]: 32 cos then 32 sin (GPT-J).
+ *   rms_norm_weight  binary32 [128], 16-byte aligned.
+ *   Token t writes a key at kv_slot_mapping[t] when that slot is >= 0 and
+ *   (positions[t] + 1) % compress_ratio == 0 (it closes its group; other rows
+ *   are not read).  Key: x = k_pre[t] in binary32; variance = pairwise sum of
+ *   x_d^2 (recursive halving in index order) / 128; r = binary32 rounding of
+ *   1 / sqrt(variance + rms_norm_eps) evaluated in binary64; y = (x * r) * w;
+ *   then GPT-J RoPE on dims 64..127 (pair i: y[64+2i], y[65+2i] rotated by
+ *   cos_sin_cache[p][i], [p][32+i], p = floor(pos / ratio) * ratio), every
+ *   product and sum rounded to binary32 without contraction; then the MXFP4
+ *   record (record = PSK_REC_MXFP4, 68-byte keys) or the FP8 indexer record
+ *   (PSK_REC_FP8_INDEXER, 132-byte keys), as the two writers above quantize.
+ *   Slots >= capacity and RoPE rows p outside [0, max_pos) are skipped and
+ *   counted in *err_count (optional).
+ */
+psk_status indexer_k_norm_rope_store(
+    const void* k_pre, int64_t k_row_stride, const int64_t* positions,
+    const float* cos_sin_cache, int64_t cs_stride, int64_t max_pos,
+    const float* rms_norm_weight, float rms_norm_eps,
+    const int64_t* kv_slot_mapping, int64_t num_tokens, int32_t compress_ratio,
+    psk_record record, uint8_t* k_cache, int64_t num_pages, int64_t page_stride,
+    int32_t block_size, int32_t* err_count, psk_stream_t stream);
 
 #ifdef __cplusplus
 }

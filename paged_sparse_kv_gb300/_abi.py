@@ -20,6 +20,7 @@ PSK_ERR_UNSUPPORTED = 2
 PSK_ERR_CUDA = 3
 PSK_REC_FP8_DS_MLA = 0
 PSK_REC_MXFP4 = 1
+PSK_REC_FP8_INDEXER = 2
 
 STATUS_NAMES = {0: "PSK_OK", 1: "PSK_ERR_INVALID_ARGUMENT", 2: "PSK_ERR_UNSUPPORTED",
                 3: "PSK_ERR_CUDA"}
@@ -62,6 +63,11 @@ SIGNATURES = {
         _I32, [_P, _I64, _I32, _I32, _P, _I64, _P]),
     "combine_dense_swa_indices": (
         _I32, [_P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64, _P, _I64, _P, _P]),
+    "write_indexer_fp8_cache": (
+        _I32, [_P, _I64, _P, _I64, _P, _I64, _I64, _I32, _I32, _P, _P]),
+    "indexer_k_norm_rope_store": (
+        _I32, [_P, _I64, _P, _P, _I64, _I64, _P, ctypes.c_float, _P, _I64, _I32, _I32, _P, _I64,
+               _I64, _I32, _P, _P]),
 }
 
 _lib = None

@@ -268,10 +268,16 @@ psk_status dequantize_and_gather_k_cache(void* out, int64_t out_stride_t, int64_
                                          int64_t idx_stride, int64_t rows, int32_t cols,
                                          psk_stream_t stream) {
     CHECK(rows >= 0 && cols >= 0, "rows and cols must be >= 0");
-    CHECK(record == PSK_REC_FP8_DS_MLA || record == PSK_REC_MXFP4, "unknown record %d",
-          (int)record);
+    CHECK(record == PSK_REC_FP8_DS_MLA || record == PSK_REC_MXFP4 ||
+              record == PSK_REC_FP8_INDEXER,
+          "unknown record %d", (int)record);
     int64_t rec_bytes;
-    if (record == PSK_REC_FP8_DS_MLA) {
+    if (record == PSK_REC_FP8_INDEXER) {
+        CHECK(mxfp4_head_dim_ok(head_dim),
+              "head_dim must be one of 32, 64, 128, 256, 512, 1024 (got %d)", head_dim);
+        CHECK(rope_dim == 0, "rope_dim must be 0 for the FP8 indexer record");
+        rec_bytes = head_dim + 4;
+    } else if (record == PSK_REC_FP8_DS_MLA) {
         CHECK(is_ue8m0 == 0 || is_ue8m0 == 1, "is_ue8m0 must be 0 or 1");
         CHECK(fp8_head_dim_ok(head_dim),
               "head_dim must be one of 64, 128, 256, 512, 1024 (got %d)", head_dim);
@@ -525,6 +531,66 @@ psk_status combine_dense_swa_indices(const int64_t* positions, const int32_t* to
                                 compressed_base, nullptr, indices, out_stride, lens, positions};
     return cuda_status(psk::launch_workspace_indices(p, reinterpret_cast<cudaStream_t>(stream)),
                        "combine_dense_swa_indices launch");
+}
+
+psk_status write_indexer_fp8_cache(const void* index_k, int64_t k_row_stride,
+                                   const int64_t* slot_mapping, int64_t num_tokens,
+                                   uint8_t* cache, int64_t num_pages, int64_t page_stride,
+                                   int32_t block_size, int32_t head_dim, int32_t* err_count,
+                                   psk_stream_t stream) {
+    CHECK(num_tokens >= 0, "num_tokens must be >= 0");
+    CHECK(mxfp4_head_dim_ok(head_dim),
+          "head_dim must be one of 32, 64, 128, 256, 512, 1024 (got %d)", head_dim);
+    psk_status st = check_cache(cache, num_pages, page_stride, block_size, head_dim + 4);
+    if (st != PSK_OK) return st;
+    if (num_tokens == 0) return ok();
+    CHECK(index_k != nullptr && slot_mapping != nullptr,
+          "index_k and slot_mapping must be non-null");
+    CHECK(aligned(index_k, 16), "index_k must be 16-byte aligned");
+    CHECK(k_row_stride >= head_dim && k_row_stride % 8 == 0,
+          "k_row_stride must be >= head_dim and a multiple of 8 elements");
+    CHECK(aligned(slot_mapping, 8), "slot_mapping must be 8-byte aligned");
+    CHECK(err_count == nullptr || aligned(err_count, 4), "err_count must be 4-byte aligned");
+    psk::InsertParams p{index_k, k_row_stride, slot_mapping, num_tokens, cache, num_pages,
+                        page_stride, block_size, head_dim, 0, 1, err_count};
+    return cuda_status(psk::launch_fp8_indexer_insert(p, reinterpret_cast<cudaStream_t>(stream)),
+                       "write_indexer_fp8_cache launch");
+}
+
+psk_status indexer_k_norm_rope_store(const void* k_pre, int64_t k_row_stride,
+                                     const int64_t* positions, const float* cos_sin_cache,
+                                     int64_t cs_stride, int64_t max_pos,
+                                     const float* rms_norm_weight, float rms_norm_eps,
+                                     const int64_t* kv_slot_mapping, int64_t num_tokens,
+                                     int32_t compress_ratio, psk_record record,
+                                     uint8_t* k_cache, int64_t num_pages, int64_t page_stride,
+                                     int32_t block_size, int32_t* err_count,
+                                     psk_stream_t stream) {
+    CHECK(num_tokens >= 0, "num_tokens must be >= 0");
+    CHECK(record == PSK_REC_MXFP4 || record == PSK_REC_FP8_INDEXER,
+          "record must be PSK_REC_MXFP4 or PSK_REC_FP8_INDEXER (got %d)", (int)record);
+    CHECK(compress_ratio >= 1, "compress_ratio must be >= 1");
+    CHECK(max_pos >= 0 && cs_stride >= 64, "need max_pos >= 0 and cs_stride >= 64");
+    psk_status st = check_cache(k_cache, num_pages, page_stride, block_size,
+                                record == PSK_REC_MXFP4 ? 68 : 132);
+    if (st != PSK_OK) return st;
+    if (num_tokens == 0) return ok();
+    CHECK(k_pre && positions && cos_sin_cache && rms_norm_weight && kv_slot_mapping,
+          "k_pre, positions, cos_sin_cache, rms_norm_weight and kv_slot_mapping must be non-null");
+    CHECK(aligned(k_pre, 8) && k_row_stride >= 128 && k_row_stride % 4 == 0,
+          "k_pre must be 8-byte aligned with a row stride >= 128 and a multiple of 4 elements");
+    CHECK(aligned(positions, 8) && aligned(kv_slot_mapping, 8),
+          "positions and kv_slot_mapping must be 8-byte aligned");
+    CHECK(aligned(cos_sin_cache, 4), "cos_sin_cache must be 4-byte aligned");
+    CHECK(aligned(rms_norm_weight, 16), "rms_norm_weight must be 16-byte aligned");
+    CHECK(err_count == nullptr || aligned(err_count, 4), "err_count must be 4-byte aligned");
+    CHECK(num_tokens <= INT64_MAX / 32, "num_tokens is too large");
+    psk::NormRopeParams p{static_cast<const uint16_t*>(k_pre), k_row_stride, positions,
+                          cos_sin_cache, cs_stride, max_pos, rms_norm_weight, rms_norm_eps,
+                          kv_slot_mapping, num_tokens, compress_ratio, (int32_t)record, k_cache,
+                          num_pages, page_stride, block_size, err_count};
+    return cuda_status(psk::launch_norm_rope_store(p, reinterpret_cast<cudaStream_t>(stream)),
+                       "indexer_k_norm_rope_store launch");
 }
 
 }  // extern "C"

@@ -268,24 +268,28 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
     }
 }
 
-// ---- MXFP4: batched loads -----------------------------------------------------------
+// ---- small records (MXFP4, FP8 indexer): batched loads --------------------------------
 //
-// A 68-byte record is too small for a bulk copy to pay off, so this gather
-// uses plain loads arranged for memory-level parallelism: a warp takes a
-// batch of STEPS * GPW consecutive (t, j) items, loads their slot ids with one
-// coalesced load, then issues every record load of the batch (a 4-byte word of
-// packed E2M1 values and the scale byte per lane, for each item) before it
-// converts and stores anything.
-template <int D>
+// A 68-byte MXFP4 record (or a 132-byte FP8 indexer record at head_dim 128)
+// is too small for a bulk copy to pay off, so this gather uses plain loads
+// arranged for memory-level parallelism: a warp takes a batch of STEPS * GPW
+// consecutive (t, j) items, loads their slot ids with one coalesced load, then
+// issues every record load of the batch (per lane and item: 4 bytes of packed
+// E2M1 values and their scale byte, or 8 e4m3 bytes and the row's binary32
+// scale) before it converts and stores anything.
+// REC 1: MXFP4 (TokenSpeed read_deepseek_v4_indexer_mxfp4_cache); REC 2: the
+// FP8 indexer record (write_deepseek_v4_indexer_fp8_cache's layout).
+template <int D, int REC>
 __global__ void __launch_bounds__(kThreads)
-gather_mxfp4_kernel(GatherParams p) {
+gather_small_kernel(GatherParams p) {
     constexpr int CHUNKS = D / 8;
     constexpr int LANES = CHUNKS < kWarp ? CHUNKS : kWarp;
     constexpr int CPL = CHUNKS / LANES;
     constexpr int GPW = kWarp / LANES;
     constexpr int STEPS = (kWarp / GPW) < 8 ? (kWarp / GPW) : 8;
     constexpr int BATCH = STEPS * GPW;  // <= 32 items, one slot id per lane
-    constexpr int VB = D / 2, SB = D / 32;
+    constexpr int VB = REC == 1 ? D / 2 : D;    // value bytes per token
+    constexpr int SB = REC == 1 ? D / 32 : 4;   // scale bytes per token
 
     const int lane = threadIdx.x & 31;
     const int grp = lane / LANES, gl = lane % LANES;
@@ -317,8 +321,8 @@ gather_mxfp4_kernel(GatherParams p) {
             my_slot = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
             my_off = t * p.out_stride_t + (int64_t)j * p.out_stride_j;
         }
-        uint32_t raw[STEPS][CPL];
-        uint32_t scl[STEPS][CPL];
+        uint2 raw[STEPS][CPL];     // REC 1: .x = 4 value bytes; REC 2: 8 e4m3 bytes
+        uint32_t scl[STEPS][CPL];  // REC 1: scale byte; REC 2: binary32 scale bits
         int32_t slot[STEPS];
 #pragma unroll
         for (int st = 0; st < STEPS; ++st) {
@@ -332,8 +336,13 @@ gather_mxfp4_kernel(GatherParams p) {
 #pragma unroll
                 for (int i = 0; i < CPL; ++i) {
                     const int c = gl + i * LANES;
-                    raw[st][i] = ld_nc_u32(vals + 4 * c);
-                    scl[st][i] = ld_nc_u8(sc + c / 4);
+                    if constexpr (REC == 1) {
+                        raw[st][i].x = ld_nc_u32(vals + 4 * c);
+                        scl[st][i] = ld_nc_u8(sc + c / 4);
+                    } else {
+                        raw[st][i] = ld_nc_v2(vals + 8 * c);
+                        scl[st][i] = ld_nc_u32(sc);
+                    }
                 }
             }
         }
@@ -348,13 +357,20 @@ gather_mxfp4_kernel(GatherParams p) {
                 uint4 o;
                 if (slot[st] < 0) {
                     o = make_uint4(0u, 0u, 0u, 0u);
-                } else {
+                } else if constexpr (REC == 1) {
                     const uint64_t s2 = splat_f32x2(ue8m0_scale(scl[st][i]));
-                    const uint32_t w = raw[st][i];
+                    const uint32_t w = raw[st][i].x;
                     o.x = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(w & 0xFFu), s2);
                     o.y = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((w >> 8) & 0xFFu), s2);
                     o.z = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((w >> 16) & 0xFFu), s2);
                     o.w = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(w >> 24), s2);
+                } else {
+                    const uint64_t s2 = splat_f32x2(__uint_as_float(scl[st][i]));
+                    const uint2 w = raw[st][i];
+                    o.x = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x & 0xFFFFu), s2);
+                    o.y = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x >> 16), s2);
+                    o.z = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y & 0xFFFFu), s2);
+                    o.w = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y >> 16), s2);
                 }
                 st_stream_v4(orow + 8 * c, o);
             }
@@ -414,16 +430,29 @@ cudaError_t fp8_by_dim(const ItemSource& src, int64_t items, cudaStream_t stream
     }
 }
 
-template <int D>
-cudaError_t gather_mxfp4_dispatch(const GatherParams& p, cudaStream_t stream) {
+template <int D, int REC>
+cudaError_t gather_small_dispatch(const GatherParams& p, cudaStream_t stream) {
     constexpr int LANES = (D / 8) < kWarp ? (D / 8) : kWarp;
     constexpr int GPW = kWarp / LANES;
     constexpr int STEPS = (kWarp / GPW) < 8 ? (kWarp / GPW) : 8;
     const int64_t items = p.rows * (int64_t)p.cols;
-    auto kern = gather_mxfp4_kernel<D>;
+    auto kern = gather_small_kernel<D, REC>;
     const int64_t batches = (items + STEPS * GPW - 1) / (STEPS * GPW);
     const int64_t blocks = persistent_blocks(kern, batches, kWarp);
     return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p);
+}
+
+template <int REC>
+cudaError_t gather_small_by_dim(const GatherParams& p, cudaStream_t stream) {
+    switch (p.head_dim) {
+        case 32: return gather_small_dispatch<32, REC>(p, stream);
+        case 64: return gather_small_dispatch<64, REC>(p, stream);
+        case 128: return gather_small_dispatch<128, REC>(p, stream);
+        case 256: return gather_small_dispatch<256, REC>(p, stream);
+        case 512: return gather_small_dispatch<512, REC>(p, stream);
+        case 1024: return gather_small_dispatch<1024, REC>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -440,15 +469,7 @@ cudaError_t launch_gather(const GatherParams& params, cudaStream_t stream) {
         src.g = p;
         return fp8_by_dim<false>(src, p.rows * (int64_t)p.cols, stream);
     }
-    switch (p.head_dim) {
-        case 32: return gather_mxfp4_dispatch<32>(p, stream);
-        case 64: return gather_mxfp4_dispatch<64>(p, stream);
-        case 128: return gather_mxfp4_dispatch<128>(p, stream);
-        case 256: return gather_mxfp4_dispatch<256>(p, stream);
-        case 512: return gather_mxfp4_dispatch<512>(p, stream);
-        case 1024: return gather_mxfp4_dispatch<1024>(p, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    return p.record == 1 ? gather_small_by_dim<1>(p, stream) : gather_small_by_dim<2>(p, stream);
 }
 
 cudaError_t launch_gather_ranges(const RangeParams& r, cudaStream_t stream) {

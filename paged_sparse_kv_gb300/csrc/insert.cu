@@ -259,6 +259,183 @@ mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
     }
 }
 
+// ---- FP8 indexer record --------------------------------------------------------------
+//
+// TokenSpeed write_deepseek_v4_indexer_fp8_cache (the "[values | fp32 scale]"
+// page layout) with the rule of _fp8_e4m3_pow2_bytes: one power-of-two
+// binary32 scale per token, 2^ceil(log2(max(amax / 448, 1e-10))) -- the
+// quotient is floored, not amax -- and codes e4m3(x / scale), computed as
+// x * 2^-e (the same single rounding of the same exact value).  Lanes as the
+// MXFP4 insert; the row amax is an integer shuffle-max over the token's lanes.
+template <int D, int UNROLL>
+__global__ void __launch_bounds__(kThreads)
+fp8_indexer_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
+                          const int64_t* __restrict__ slots, int64_t n,
+                          uint8_t* __restrict__ cache, int64_t capacity, int64_t page_stride,
+                          int32_t bs, int32_t shift, int32_t* __restrict__ err) {
+    constexpr int CHUNKS = D / 8;
+    constexpr int LANES = mxfp4_lanes<D>();
+    constexpr int CPL = CHUNKS / LANES;
+    static_assert(CPL * LANES == CHUNKS, "whole chunks per lane");
+
+    const int lane = threadIdx.x & 31;
+    const int grp = lane / LANES, gl = lane % LANES;
+    const unsigned gmask =
+        LANES == 32 ? 0xFFFFFFFFu : (((1u << LANES) - 1u) << (grp * LANES));
+    const int64_t gid = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / LANES;
+    const int64_t tok0 = gid * UNROLL;
+    pdl_wait();
+    pdl_launch_dependents();
+
+    uint4 v[UNROLL][CPL];
+    int64_t s[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+        const int64_t t = tok0 + u;
+        s[u] = -1;
+        if (t < n) {
+            s[u] = __ldg(slots + t);
+            const uint16_t* row = k + t * k_row_stride;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) v[u][i] = ld_stream_v4(row + 8 * (gl + i * LANES));
+        }
+    }
+
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+        const int64_t sl = s[u];
+        if (sl < 0) continue;
+        if (sl >= capacity) {
+            if (gl == 0 && err) atomicAdd(err, 1);
+            continue;
+        }
+        int64_t off;
+        const int64_t page = div_block(sl, bs, shift, off);
+        uint8_t* base = cache + page * page_stride;
+        uint8_t* vals = base + off * D;
+
+        uint32_t amb = 0;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) amb = max(amb, absmax_bf16x8_bits(v[u][i]));
+#pragma unroll
+        for (int m = 1; m < LANES; m <<= 1) amb = max(amb, __shfl_xor_sync(gmask, amb, m));
+        const float q = fmaxf(__fdiv_rn(__uint_as_float(amb << 16), 448.0f), 1.0e-10f);
+        const int e = ceil_log2_pos(q);
+        const uint64_t pw2 = splat_f32x2(exp2_int(-e));
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            const int c = gl + i * LANES;
+            const uint4 w = v[u][i];
+            float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                          bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) mul2_rn(x[j], x[j + 1], pw2);
+            uint2 q8;
+            q8.x = cvt_e4m3x2(x[0], x[1]) | (cvt_e4m3x2(x[2], x[3]) << 16);
+            q8.y = cvt_e4m3x2(x[4], x[5]) | (cvt_e4m3x2(x[6], x[7]) << 16);
+            st_v2(vals + 8 * c, q8);
+        }
+        if (gl == 0)
+            *reinterpret_cast<float*>(base + (int64_t)bs * D + off * 4) = exp2_int(e);
+    }
+}
+
+// ---- indexer_k_norm_rope_store ---------------------------------------------------------
+//
+// vLLM deepseek_v41 ops, indexer_k_norm_rope_store: k_norm -> RoPE -> quant ->
+// paged store of 128-dim indexer keys.  One warp per token; lane l holds dims
+// 4l..4l+3 (one 8-byte load).
+//  * Emission: slot >= 0 and the token closes its compress group,
+//    (pos + 1) % ratio == 0 (TokenSpeed _compress_v4_state_windows_capturable's
+//    valid_token rule).
+//  * RMSNorm in binary32, every operation rounded once (no contraction): the
+//    sum of squares is a pairwise sum -- (s0 + s1) + (s2 + s3) in the lane,
+//    then xor-shuffles over 1, 2, 4, 8, 16 lanes, i.e. recursive halving of
+//    the index range; variance = sum / 128; r = binary32 of 1 / sqrt(variance
+//    + eps) with the square root and the quotient in IEEE binary64;
+//    y = (x * r) * weight.
+//  * GPT-J RoPE (TokenSpeed _apply_gptj_rope_tail_rows) on dims 64..127 (lanes
+//    16..31: two pairs each) at the cos_sin row of the group's first position
+//    floor(pos / ratio) * ratio.
+//  * MXFP4 record (8-lane blocks) or FP8 indexer record (row amax), with the
+//    inserts' rules.
+template <bool FP4>
+__global__ void __launch_bounds__(kThreads) norm_rope_store_kernel(NormRopeParams p,
+                                                                   int32_t shift) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / kWarp;
+    pdl_wait();
+    pdl_launch_dependents();
+    if (t >= p.num_tokens) return;
+    const int64_t sl = __ldg(p.slots + t);
+    if (sl < 0) return;
+    const int64_t pos = __ldg(p.positions + t);
+    int64_t rem = (pos + 1) % p.ratio;
+    if (rem < 0) rem += p.ratio;
+    if (rem != 0) return;  // not a group boundary: the row is not read
+    int64_t grp = pos / p.ratio;
+    if (pos % p.ratio != 0 && pos < 0) grp -= 1;
+    const int64_t prow = grp * p.ratio;
+    const int64_t capacity = p.num_pages * (int64_t)p.block_size;
+    if (sl >= capacity || prow < 0 || prow >= p.max_pos) {
+        if (lane == 0 && p.err_count) atomicAdd(p.err_count, 1);
+        return;
+    }
+
+    const uint2 kw = ld_nc_v2(p.k + t * p.k_row_stride + 4 * lane);
+    float y[4] = {bf16_lo(kw.x), bf16_hi(kw.x), bf16_lo(kw.y), bf16_hi(kw.y)};
+    float ss = __fadd_rn(__fadd_rn(__fmul_rn(y[0], y[0]), __fmul_rn(y[1], y[1])),
+                         __fadd_rn(__fmul_rn(y[2], y[2]), __fmul_rn(y[3], y[3])));
+#pragma unroll
+    for (int m = 1; m < kWarp; m <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, m));
+    const float variance = __fdiv_rn(ss, 128.0f);
+    const float r =
+        __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn((double)__fadd_rn(variance, p.eps))));
+    const float4 wv = __ldg(reinterpret_cast<const float4*>(p.weight) + lane);
+    y[0] = __fmul_rn(__fmul_rn(y[0], r), wv.x);
+    y[1] = __fmul_rn(__fmul_rn(y[1], r), wv.y);
+    y[2] = __fmul_rn(__fmul_rn(y[2], r), wv.z);
+    y[3] = __fmul_rn(__fmul_rn(y[3], r), wv.w);
+    if (lane >= 16) {
+        const float* cs = p.cos_sin + prow * p.cs_stride;
+        const int i0 = 2 * lane - 32;  // pair index of dims 4l, 4l + 1
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float c = __ldg(cs + i0 + h), sn = __ldg(cs + 32 + i0 + h);
+            const float e = y[2 * h], o = y[2 * h + 1];
+            y[2 * h] = __fsub_rn(__fmul_rn(e, c), __fmul_rn(o, sn));
+            y[2 * h + 1] = __fadd_rn(__fmul_rn(e, sn), __fmul_rn(o, c));
+        }
+    }
+
+    int64_t off;
+    const int64_t page = div_block(sl, p.block_size, shift, off);
+    uint8_t* base = p.cache + page * p.page_stride;
+    float a = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
+    if constexpr (FP4) {
+#pragma unroll
+        for (int m = 1; m < 8; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, m));
+        const int e = ceil_log2_pos(__fdiv_rn(fmaxf(a, 1.0e-4f), 6.0f));
+        const float pw = exp2_int(-e);
+        const uint32_t lo = cvt_e2m1x2(__fmul_rn(y[0], pw), __fmul_rn(y[1], pw)) & 0xFFu;
+        const uint32_t hi = cvt_e2m1x2(__fmul_rn(y[2], pw), __fmul_rn(y[3], pw)) & 0xFFu;
+        *reinterpret_cast<uint16_t*>(base + off * 64 + 2 * lane) = (uint16_t)(lo | (hi << 8));
+        if ((lane & 7) == 0)
+            base[(int64_t)p.block_size * 64 + off * 4 + lane / 8] =
+                (uint8_t)min(max(e + 127, 0), 254);
+    } else {
+#pragma unroll
+        for (int m = 1; m < kWarp; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, m));
+        const int e = ceil_log2_pos(fmaxf(__fdiv_rn(a, 448.0f), 1.0e-10f));
+        const float pw = exp2_int(-e);
+        const uint32_t q = cvt_e4m3x2(__fmul_rn(y[0], pw), __fmul_rn(y[1], pw)) |
+                           (cvt_e4m3x2(__fmul_rn(y[2], pw), __fmul_rn(y[3], pw)) << 16);
+        *reinterpret_cast<uint32_t*>(base + off * 128 + 4 * lane) = q;
+        if (lane == 0)
+            *reinterpret_cast<float*>(base + (int64_t)p.block_size * 128 + off * 4) = exp2_int(e);
+    }
+}
+
 template <int D, bool UE8M0>
 cudaError_t fp8_insert_dispatch(const InsertParams& p, cudaStream_t stream) {
     constexpr int UNROLL = 2;
@@ -286,7 +463,40 @@ cudaError_t mxfp4_insert_dispatch(const InsertParams& p, cudaStream_t stream) {
                       p.page_stride, p.block_size, log2_if_pow2(p.block_size), p.err_count);
 }
 
+template <int D>
+cudaError_t fp8_indexer_insert_dispatch(const InsertParams& p, cudaStream_t stream) {
+    constexpr int UNROLL = 2;
+    constexpr int LANES = mxfp4_lanes<D>();
+    const int64_t groups = (p.num_tokens + UNROLL - 1) / UNROLL;
+    const int64_t threads = groups * LANES;
+    const int64_t blocks = (threads + kThreads - 1) / kThreads;
+    return launch_pdl(fp8_indexer_insert_kernel<D, UNROLL>, dim3((unsigned)blocks),
+                      dim3(kThreads), 0, stream, static_cast<const uint16_t*>(p.k),
+                      p.k_row_stride, p.slots, p.num_tokens, p.cache,
+                      p.num_pages * (int64_t)p.block_size, p.page_stride, p.block_size,
+                      log2_if_pow2(p.block_size), p.err_count);
+}
+
 }  // namespace
+
+cudaError_t launch_fp8_indexer_insert(const InsertParams& p, cudaStream_t stream) {
+    switch (p.head_dim) {
+        case 32: return fp8_indexer_insert_dispatch<32>(p, stream);
+        case 64: return fp8_indexer_insert_dispatch<64>(p, stream);
+        case 128: return fp8_indexer_insert_dispatch<128>(p, stream);
+        case 256: return fp8_indexer_insert_dispatch<256>(p, stream);
+        case 512: return fp8_indexer_insert_dispatch<512>(p, stream);
+        case 1024: return fp8_indexer_insert_dispatch<1024>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_norm_rope_store(const NormRopeParams& p, cudaStream_t stream) {
+    const int64_t blocks = (p.num_tokens * kWarp + kThreads - 1) / kThreads;
+    const int32_t shift = log2_if_pow2(p.block_size);
+    auto kern = p.record == 1 ? norm_rope_store_kernel<true> : norm_rope_store_kernel<false>;
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p, shift);
+}
 
 cudaError_t launch_fp8_insert(const InsertParams& p, cudaStream_t stream) {
     const bool ue = p.is_ue8m0 != 0;

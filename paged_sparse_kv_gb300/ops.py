@@ -16,7 +16,7 @@ from typing import Optional
 import torch
 
 from . import _abi
-from ._abi import PSK_REC_FP8_DS_MLA, PSK_REC_MXFP4, PskError  # noqa: F401
+from ._abi import PSK_REC_FP8_DS_MLA, PSK_REC_FP8_INDEXER, PSK_REC_MXFP4, PskError  # noqa: F401
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -338,3 +338,43 @@ def combine_dense_swa_indices(positions: torch.Tensor, token_to_req: torch.Tenso
               _ptr(gather_lens), seq_lens.shape[0], T, window_size, workspace_width,
               compressed_base, _ptr(out), _rows(out, "out"), _ptr(lens), _stream(dev))
     return out, lens
+
+
+# ---- indexer-key variants -------------------------------------------------------------
+
+def write_indexer_fp8_cache(index_k: torch.Tensor, cache: torch.Tensor, slot_mapping: torch.Tensor,
+                            block_size: int, *, err_count: Optional[torch.Tensor] = None) -> None:
+    """FP8 indexer keys ([values | binary32 power-of-two scale] pages)."""
+    _need_cuda(index_k, cache, slot_mapping, err_count)
+    _need(index_k, torch.bfloat16, "index_k")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    num_pages, page_stride = _pages(cache)
+    _abi.call("write_indexer_fp8_cache", _ptr(index_k), _rows(index_k, "index_k"),
+              _ptr(slot_mapping), slot_mapping.shape[0], _ptr(cache), num_pages, page_stride,
+              block_size, index_k.shape[1], _ptr(err_count), _stream(index_k.device))
+
+
+def indexer_k_norm_rope_store(k_pre: torch.Tensor, positions: torch.Tensor,
+                              cos_sin_cache: torch.Tensor, rms_norm_weight: torch.Tensor,
+                              rms_norm_eps: float, k_cache: torch.Tensor,
+                              kv_slot_mapping: torch.Tensor, compress_ratio: int,
+                              use_fp4_cache: bool, block_size: int, *,
+                              err_count: Optional[torch.Tensor] = None) -> None:
+    """k_norm -> GPT-J RoPE -> MXFP4 / FP8 indexer record -> paged store of
+    128-dim indexer keys (the vLLM op's argument names)."""
+    _need_cuda(k_pre, positions, cos_sin_cache, rms_norm_weight, k_cache, kv_slot_mapping,
+               err_count)
+    _need(k_pre, torch.bfloat16, "k_pre")
+    _need(positions, torch.int64, "positions")
+    _need(cos_sin_cache, torch.float32, "cos_sin_cache")
+    _need(rms_norm_weight, torch.float32, "rms_norm_weight")
+    _need(kv_slot_mapping, torch.int64, "kv_slot_mapping")
+    if k_pre.dim() != 2 or k_pre.shape[1] != 128:
+        raise ValueError("k_pre must be [num_tokens, 128]")
+    num_pages, page_stride = _pages(k_cache)
+    record = PSK_REC_MXFP4 if use_fp4_cache else PSK_REC_FP8_INDEXER
+    _abi.call("indexer_k_norm_rope_store", _ptr(k_pre), _rows(k_pre, "k_pre"), _ptr(positions),
+              _ptr(cos_sin_cache), _rows(cos_sin_cache, "cos_sin_cache"), cos_sin_cache.shape[0],
+              _ptr(rms_norm_weight.contiguous()), float(rms_norm_eps), _ptr(kv_slot_mapping),
+              kv_slot_mapping.shape[0], compress_ratio, record, _ptr(k_cache), num_pages,
+              page_stride, block_size, _ptr(err_count), _stream(k_pre.device))

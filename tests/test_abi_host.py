@@ -291,3 +291,52 @@ def test_dense_swa_rejects_bad_arguments(psk_lib, kw):
 
 def test_dense_swa_zero_tokens_ok(psk_lib):
     assert _dswa_ws(n=0, pos=None, out=None, lens=None) == OK
+
+
+def _fp8i(**kw):
+    a = dict(k=A, ks=128, slots=B, n=4, cache=C, num_pages=8, page_stride=64 * 132, bs=64,
+             D=128, err=None)
+    a.update(kw)
+    return _abi.status("write_indexer_fp8_cache", a["k"], a["ks"], a["slots"], a["n"], a["cache"],
+                       a["num_pages"], a["page_stride"], a["bs"], a["D"], a["err"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(D=48), dict(D=16), dict(page_stride=64 * 132 - 16),
+                                dict(cache=C + 4), dict(k=None), dict(k=A + 8), dict(ks=120),
+                                dict(n=-5), dict(slots=B + 4), dict(err=B + 2)])
+def test_fp8_indexer_insert_rejects_bad_arguments(psk_lib, kw):
+    assert _fp8i(**kw) == INV
+
+
+def test_fp8_indexer_insert_zero_tokens_ok(psk_lib):
+    assert _fp8i(n=0, k=None, slots=None) == OK
+
+
+def test_fp8_indexer_gather_record_checks(psk_lib):
+    assert _gather(rec=2, D=128, rope=0, page_stride=64 * 132, rows=0, out=None, idx=None) == OK
+    assert _gather(rec=2, D=128, rope=64, page_stride=64 * 132) == INV
+    assert _gather(rec=2, D=128, rope=0, page_stride=64 * 132 - 16) == INV
+    assert _gather(rec=3, D=128, rope=0) == INV
+
+
+def _nrs(**kw):
+    a = dict(k=A, ks=128, pos=B, cs=C, css=64, maxp=4096, w=A + 4096, eps=1e-6, slots=B + 4096,
+             n=4, ratio=4, rec=1, cache=C + 65536, num_pages=8, page_stride=64 * 68, bs=64,
+             err=None)
+    a.update(kw)
+    return _abi.status("indexer_k_norm_rope_store", a["k"], a["ks"], a["pos"], a["cs"], a["css"],
+                       a["maxp"], a["w"], a["eps"], a["slots"], a["n"], a["ratio"], a["rec"],
+                       a["cache"], a["num_pages"], a["page_stride"], a["bs"], a["err"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(rec=0), dict(rec=3), dict(ratio=0), dict(css=32),
+                                dict(maxp=-1), dict(ks=126), dict(ks=100), dict(k=A + 2),
+                                dict(pos=B + 4), dict(w=A + 4100), dict(cs=C + 2),
+                                dict(page_stride=64 * 68 - 16), dict(rec=2, page_stride=64 * 68),
+                                dict(k=None), dict(slots=None), dict(n=-1), dict(err=B + 1)])
+def test_norm_rope_store_rejects_bad_arguments(psk_lib, kw):
+    assert _nrs(**kw) == INV
+
+
+def test_norm_rope_store_zero_tokens_ok(psk_lib):
+    assert _nrs(n=0, k=None, pos=None) == OK

@@ -1,0 +1,162 @@
+"""GPU parity for the indexer-key variants: the FP8 indexer record (writer and
+reader through dequantize_and_gather_k_cache) and indexer_k_norm_rope_store,
+byte for byte against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_sparse_kv_gb300 import ops, synthetic
+from test_parity_gpu import _assert_same, _bf16_dev, _exhaustive_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _i64(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int64)).to(dev)
+
+
+def _u16(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def test_fp8_indexer_insert_exhaustive_codes(cuda_device):
+    """Every finite bf16 value under every scale exponent from below the
+    1e-10 quotient floor (2^-40) to 2^120, one 32-dim row per lead."""
+    rows = _exhaustive_rows(448.0, -40, 120, 32, 1)
+    N, bs = rows.shape[0], 64
+    pages = (N + bs - 1) // bs
+    host = np.zeros((pages, bs * 36), np.uint8)
+    slots = np.arange(N, dtype=np.int64)
+    dev_cache = torch.from_numpy(host).to(cuda_device)
+    ops.write_indexer_fp8_cache(_bf16_dev(rows, cuda_device), dev_cache, _i64(slots, cuda_device),
+                                bs)
+    oracle.write_indexer_fp8_cache(rows, slots, host, bs, 32)
+    assert N > 100000
+    _assert_same(dev_cache.cpu().numpy(), host, "exhaustive fp8 indexer codes")
+
+
+@pytest.mark.parametrize("bs", [64, 7])
+@pytest.mark.parametrize("D", [32, 64, 128, 256, 512, 1024])
+def test_fp8_indexer_insert_shapes_and_skips(cuda_device, D, bs):
+    rng = np.random.default_rng(D + bs)
+    N, pages = 97, 20
+    x = (rng.standard_normal((N, D + 8)) * np.exp(rng.uniform(-8, 8, size=(N, 1)))).astype(
+        np.float32)
+    x[4] = 0.0
+    k = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    slots = rng.permutation(pages * bs)[:N].astype(np.int64)
+    slots[::6] = -1
+    slots[5] = pages * bs + 3
+    stride = (bs * (D + 4) + 15) // 16 * 16
+    host = synthetic.random_cache_bytes(9, synthetic.CacheGeom(pages, bs, stride))
+    dev_cache = torch.from_numpy(host).to(cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    kd = _bf16_dev(k, cuda_device)
+    ops.write_indexer_fp8_cache(kd[:, :D], dev_cache, _i64(slots, cuda_device), bs, err_count=err)
+    n_err = oracle.write_indexer_fp8_cache(np.ascontiguousarray(k[:, :D]), slots, host, bs, D)
+    _assert_same(dev_cache.cpu().numpy(), host, f"fp8 indexer insert D={D}")
+    assert int(err.item()) == n_err == 1
+
+
+@pytest.mark.parametrize("bs", [8, 5])
+@pytest.mark.parametrize("D", [32, 128, 512])
+def test_fp8_indexer_gather_random_records(cuda_device, D, bs):
+    """Arbitrary e4m3 bytes (no NaN codes) with power-of-two and arbitrary
+    finite binary32 scales; -1 and out-of-range indices give zero rows."""
+    rng = np.random.default_rng(3 * D + bs)
+    pages = 9
+    stride = (bs * (D + 4) + 15) // 16 * 16
+    host = synthetic.random_cache_bytes(31, synthetic.CacheGeom(pages, bs, stride))
+    for s in range(pages * bs):
+        page, off = divmod(s, bs)
+        e = int(rng.integers(-60, 60))
+        v = np.float32(np.ldexp(1.0, e)) * (np.float32(rng.uniform(0.5, 2)) if s % 2 else 1)
+        host[page, bs * D + off * 4: bs * D + off * 4 + 4] = np.frombuffer(
+            np.float32(v).tobytes(), np.uint8)
+    R, C = 21, 17
+    idx = rng.integers(-1, pages * bs + 2, size=(R, C)).astype(np.int32)
+    out = torch.full((R, C, D), 3, dtype=torch.bfloat16, device=cuda_device)
+    ops.dequantize_and_gather_k_cache(out, torch.from_numpy(host).to(cuda_device),
+                                      torch.from_numpy(idx).to(cuda_device), bs,
+                                      record=ops.PSK_REC_FP8_INDEXER)
+    want = oracle.dequantize_and_gather_k_cache(host, bs, 2, D, 0, idx)
+    _assert_same(_u16(out), want, f"fp8 indexer gather D={D}")
+
+
+def _gptj_table(max_pos, dtype=np.float32):
+    theta = 10000.0 ** (-np.arange(32) / 32.0)
+    ang = np.arange(max_pos)[:, None] * theta[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(dtype)
+
+
+@pytest.mark.parametrize("fp4", [True, False])
+@pytest.mark.parametrize("ratio", [1, 2, 4])
+@pytest.mark.parametrize("bs", [64, 3])
+def test_norm_rope_store_fuzz(cuda_device, fp4, ratio, bs):
+    rng = np.random.default_rng(100 * ratio + bs + fp4)
+    N, pages, max_pos = 1500, 40, 4096
+    x = rng.standard_normal((N, 136)).astype(np.float32)
+    out = rng.random((N, 136)) < 0.01
+    x[out] *= 20.0
+    x *= np.exp(rng.uniform(-6, 6, size=(N, 1))).astype(np.float32)
+    x[7] = 0.0
+    k = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    pos = rng.integers(-3, max_pos + 40, size=N).astype(np.int64)
+    slots = rng.permutation(pages * bs)[:N].astype(np.int64) if pages * bs >= N else \
+        rng.integers(0, pages * bs, size=N).astype(np.int64)
+    slots[::9] = -1
+    if pages * bs < N:  # distinct slots among the tokens that write
+        emit = np.nonzero(slots >= 0)[0]
+        slots[emit] = -1
+        keep = emit[: pages * bs]
+        slots[keep] = rng.permutation(pages * bs)[: keep.size]
+    # two counted skips: a slot beyond the cache and a RoPE row beyond max_pos,
+    # both on group boundaries
+    pos[11], slots[11] = 5 * ratio - 1, pages * bs + 1
+    pos[13], slots[13] = max_pos + ratio - 1, pages * bs + 2
+    cs = _gptj_table(max_pos)
+    w = rng.uniform(0.25, 4.0, size=128).astype(np.float32)
+    eps = 1e-6
+    rec = 68 if fp4 else 132
+    stride = (bs * rec + 15) // 16 * 16
+    host = synthetic.random_cache_bytes(5, synthetic.CacheGeom(pages, bs, stride))
+    d = cuda_device
+    dev_cache = torch.from_numpy(host).to(d)
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    kd = _bf16_dev(k, d)
+    ops.indexer_k_norm_rope_store(kd[:, :128], _i64(pos, d), torch.from_numpy(cs).to(d),
+                                  torch.from_numpy(w).to(d), eps, dev_cache, _i64(slots, d), ratio,
+                                  fp4, bs, err_count=err)
+    n_err = oracle.indexer_k_norm_rope_store(np.ascontiguousarray(k[:, :128]), pos, cs, w, eps,
+                                             slots, ratio, 1 if fp4 else 2, host, bs)
+    _assert_same(dev_cache.cpu().numpy(), host, f"norm rope store fp4={fp4} ratio={ratio}")
+    assert int(err.item()) == n_err and n_err >= 2
+
+
+def test_norm_rope_store_prefill_size(cuda_device):
+    """The prefill batch's 16384 tokens at ratio 4 (a key per 4 tokens) into the
+    MXFP4 and FP8 indexer caches, strided k_pre and a padded cos_sin table."""
+    w_ = synthetic.make("prefill")
+    d = cuda_device
+    qlen = np.diff(w_.query_start_loc)
+    pos = np.concatenate([np.arange(s - q, s) for s, q in zip(w_.seq_lens, qlen)]).astype(np.int64)
+    rng = np.random.default_rng(77)
+    k = torch.from_numpy(rng.standard_normal((pos.size, 256)).astype(np.float32)).to(
+        torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    cs = np.zeros((4096, 72), np.float32)
+    cs[:, :64] = _gptj_table(4096)
+    wt = rng.uniform(0.5, 2.0, size=128).astype(np.float32)
+    for fp4 in (True, False):
+        bs, rec = 64, (68 if fp4 else 132)
+        pages = w_.index_cache.num_pages
+        host = np.zeros((pages, bs * rec), np.uint8)
+        slots = w_.index_insert_slots
+        dev_cache = torch.from_numpy(host).to(d)
+        kd = _bf16_dev(k, d)
+        ops.indexer_k_norm_rope_store(kd[:, 64:192], _i64(pos, d), torch.from_numpy(cs).to(d),
+                                      torch.from_numpy(wt).to(d), 1e-6, dev_cache, _i64(slots, d),
+                                      4, fp4, bs)
+        oracle.indexer_k_norm_rope_store(np.ascontiguousarray(k[:, 64:192]), pos, cs[:, :64], wt,
+                                         1e-6, slots, 4, 1 if fp4 else 2, host, bs)
+        _assert_same(dev_cache.cpu().numpy(), host, f"prefill norm rope store fp4={fp4}")
