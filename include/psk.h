@@ -463,8 +463,8 @@ psk_status write_indexer_fp8_cache(
  *   Token t writes a key at kv_slot_mapping[t] when that slot is >= 0 and
  *   (positions[t] + 1) % compress_ratio == 0 (it closes its group; other rows
  *   are not read).  Key: x = k_pre[t] in binary32; variance = pairwise sum of
- *   x_d^2 (recursive halving in index order) / 128; r = binary32 rounding of
- *   1 / sqrt(variance + rms_norm_eps) evaluated in binary64; y = (x * r) * w;
+ *   x_d^2 (recursive halving in index order) / 128; r = 1 / sqrt(variance +
+ *   rms_norm_eps) as IEEE binary32 square root then division; y = (x * r) * w;
  *   then GPT-J RoPE on dims 64..127 (pair i: y[64+2i], y[65+2i] rotated by
  *   cos_sin_cache[p][i], [p][32+i], p = floor(pos / ratio) * ratio), every
  *   product and sum rounded to binary32 without contraction; then the MXFP4

@@ -16,8 +16,10 @@ from . import (REC_FP8_DS_MLA, REC_MXFP4, combine_topk_swa_indices,
                combine_topk_swa_workspace_indices, compute_dense_compressed_indices_and_lens,
                compute_global_topk_indices_and_lens, decode_swa_indices_and_lens,
                dequantize_and_gather_k_cache, dequantize_and_gather_k_cache_ranges,
-               indexer_mxfp4_paged_gather, quantize_and_insert_k_cache,
-               write_indexer_mxfp4_cache)
+               indexer_k_norm_rope_store, indexer_mxfp4_paged_gather,
+               quantize_and_insert_k_cache, write_indexer_fp8_cache, write_indexer_mxfp4_cache)
+
+REC_FP8_INDEXER = 2
 
 
 def run_step(w, swa_cache: Optional[np.ndarray], comp_cache: Optional[np.ndarray],
@@ -106,4 +108,31 @@ def run_dense_step(w, swa_cache, comp_cache) -> dict:
     g_cmp = dequantize_and_gather_k_cache(comp_cache, w.comp_cache.block_size, REC_FP8_DS_MLA,
                                           w.head_dim, w.rope_dim, res["dense_indices"])
     res["gathered"] = np.concatenate([g_swa, g_cmp], axis=1)
+    return res
+
+
+def run_indexer_step(w, variant: str, cache, inputs: dict, sample_tokens=None) -> dict:
+    """The indexer step with the FP8 indexer record ("fp8") or the fused
+    norm-RoPE-MXFP4 store ("store") as the key writer; ``cache`` is that
+    writer's cache (updated in place); ``inputs`` holds positions, cos_sin,
+    weight and eps for "store"."""
+    res: dict = {}
+    bs = w.index_cache.block_size
+    if variant == "fp8":
+        res["err"] = write_indexer_fp8_cache(w.index_k, w.index_insert_slots, cache, bs,
+                                             w.index_head_dim)
+        rec = REC_FP8_INDEXER
+    else:
+        res["err"] = indexer_k_norm_rope_store(
+            w.index_k, inputs["positions"], inputs["cos_sin"], inputs["weight"], inputs["eps"],
+            w.index_insert_slots, 1, REC_MXFP4, cache, bs)
+        rec = REC_MXFP4
+    table = w.comp_block_table if w.comp_block_table is not None else w.swa_block_table
+    gt, gl = compute_global_topk_indices_and_lens(w.topk_local, w.token_to_req, table, bs,
+                                                  is_valid_token=w.is_valid_token)
+    res["global_topk"], res["global_lens"] = gt, gl
+    toks = None if sample_tokens is None else np.asarray(sample_tokens, dtype=np.int64)
+    rows = gt if toks is None else gt[toks]
+    res["gathered_index"] = dequantize_and_gather_k_cache(cache, bs, rec, w.index_head_dim, 0,
+                                                          np.ascontiguousarray(rows))
     return res

@@ -964,8 +964,8 @@ static float pairwise_sum(const float* v, int32_t n) {
  *   RMSNorm ([OPS] _compress_v4_state_windows_capturable), binary32:
  *     variance = (sum of x_d * x_d) / 128 with the sum taken pairwise
  *     (recursive halving in index order -- a reading: no order is printed);
- *     r = binary32 rounding of 1 / sqrt(variance + eps) with the square root
- *     and the quotient in binary64 (a reading: the printed rsqrt is a binary32
+ *     r = 1 / sqrt(variance + eps) as an IEEE binary32 square root followed
+ *     by an IEEE binary32 division (a reading: the printed rsqrt is a binary32
  *     library call of unstated accuracy); y_d = (x_d * r) * weight_d;
  *   RoPE ([OPS] _apply_gptj_rope_tail_rows, GPT-J pairs on the last 64 dims):
  *     for i < 32, e = y[64 + 2i], o = y[65 + 2i], c = cs[p][i], s = cs[p][32 + i]:
@@ -1010,7 +1010,7 @@ int64_t oracle_indexer_k_norm_rope_store(
             sq[d] = x[d] * x[d];
         }
         const float variance = pairwise_sum(sq, D) / 128.0f;
-        const float r = (float)(1.0 / sqrt((double)(variance + rms_norm_eps)));
+        const float r = 1.0f / sqrtf(variance + rms_norm_eps);
         for (int32_t d = 0; d < D; ++d) y[d] = (x[d] * r) * rms_norm_weight[d];
         const float* cs = cos_sin_cache + p * cs_stride;
         for (int32_t i = 0; i < R / 2; ++i) {

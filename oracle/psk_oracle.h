@@ -14,7 +14,7 @@
  * golden records, invariants).  One function has a weaker pin and is marked
  * "parity unpinned" where it is defined: the fp32-scale FP8 record
  * (is_ue8m0 = 0), whose rule no page prints.  indexer_k_norm_rope_store takes
- * two readings (pairwise summation, binary64 reciprocal square root) that fix
+ * two readings (pairwise summation, IEEE binary32 square root then division) that fix
  * the rounding of steps the pages leave open; its pins check the arithmetic
  * against closed forms, not a printed result.
  */
