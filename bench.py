@@ -118,6 +118,30 @@ def dense_algorithmic_bytes(p, outputs) -> dict:
     return res
 
 
+def indexer_algorithmic_bytes(p, variant: str, outputs) -> dict:
+    """Compulsory bytes of the indexer_fp8 / indexer_store steps."""
+    w = p.w
+    T, K, R, D = w.num_tokens, w.topk, w.num_reqs, w.index_head_dim
+    ins = w.index_insert_slots
+    nv = int((ins >= 0).sum())
+    comp_tab = w.comp_block_table if w.comp_block_table is not None else w.swa_block_table
+    res = {"compute_global_topk_indices_and_lens": T * (8 * K + 8) + R * comp_tab.shape[1] * 4}
+    gt = outputs["global_topk"]
+    distinct = np.unique(gt[gt >= 0]).size
+    if variant == "fp8":
+        res["write_indexer_fp8_cache"] = nv * (2 * D + D + 4) + ins.size * 8
+        res["dequantize_and_gather_k_cache[fp8_indexer]"] = (distinct * (D + 4) + gt.size * 4 +
+                                                             gt.size * 2 * D)
+    else:
+        n = ins.size
+        rows = min(n, p.INDEXER_MAX_POS)  # distinct RoPE rows read
+        res["indexer_k_norm_rope_store"] = (nv * (2 * D + D // 2 + D // 32) + n * 16 +
+                                            rows * 64 * 4 + D * 4)
+        res["dequantize_and_gather_k_cache[mxfp4]"] = (distinct * (D // 2 + D // 32) +
+                                                       gt.size * 4 + gt.size * 2 * D)
+    return res
+
+
 def workspace_algorithmic_bytes(p) -> dict:
     """Compulsory bytes of the prefill workspace step's launches."""
     from paged_sparse_kv_gb300.pipeline import workspace_geometry
@@ -215,41 +239,16 @@ def _oracle_sample_tokens(w, max_rows: int):
     return np.linspace(0, w.num_tokens - 1, n).astype(np.int64), n
 
 
-def time_oracle(w, budget_s: float, max_rows: int = 80000, path: str = "index"):
+def time_oracle(w, budget_s: float, path: str = "index"):
     """Run oracle steps until budget_s of CPU work; returns (tokens/s, desc)."""
-    from oracle.pipeline import run_dense_step, run_step, run_workspace_step
-    caches = _oracle_state(w)
-    if path == "dense":
-        steps, spent = 0, 0.0
-        while spent < budget_s or steps == 0:
-            t0 = time.perf_counter()
-            run_dense_step(w, caches["swa_cache"], caches["comp_cache"])
-            spent += time.perf_counter() - t0
-            steps += 1
-        return (w.num_tokens * steps / spent,
-                f"{steps} oracle steps of the {w.name} batch on the dense path")
-    if path == "workspace":
-        from paged_sparse_kv_gb300.pipeline import workspace_geometry
-        geom = workspace_geometry(w)
-        steps, spent = 0, 0.0
-        while spent < budget_s or steps == 0:
-            t0 = time.perf_counter()
-            run_workspace_step(w, geom, caches["swa_cache"], caches["comp_cache"],
-                               caches["index_cache"])
-            spent += time.perf_counter() - t0
-            steps += 1
-        return (w.num_tokens * steps / spent,
-                f"{steps} oracle steps of the {w.name} batch on the workspace path")
-    toks, n = _oracle_sample_tokens(w, max_rows)
+    step, n, desc = _oracle_step(w, path, _oracle_state(w))
     steps, spent = 0, 0.0
     while spent < budget_s or steps == 0:
         t0 = time.perf_counter()
-        run_step(w, caches["swa_cache"], caches["comp_cache"], caches["index_cache"], toks)
+        step()
         spent += time.perf_counter() - t0
         steps += 1
-    desc = (f"{steps} oracle steps of the {w.name} batch; gathers over {n} of "
-            f"{w.num_tokens} tokens (value scaled to tokens whose rows were gathered)")
-    return n * steps / spent, desc
+    return n * steps / spent, f"{steps} x [{desc}] in {spent:.1f} s"
 
 
 def _graph_events_supported(torch) -> bool:
@@ -267,6 +266,8 @@ _FAMILY = {"insert": ("insert.cu", "insert.h"), "index": ("index_build.cu", "ind
 KERNEL_SOURCES = {
     "quantize_and_insert_k_cache": _FAMILY["insert"],
     "write_indexer_mxfp4_cache": _FAMILY["insert"],
+    "write_indexer_fp8_cache": _FAMILY["insert"],
+    "indexer_k_norm_rope_store": _FAMILY["insert"],
     "combine_topk_swa_indices": _FAMILY["index"],
     "compute_global_topk_indices_and_lens": _FAMILY["index"],
     "combine_topk_swa_workspace_indices": _FAMILY["index"],
@@ -300,6 +301,8 @@ def recorded_traffic(config: str, kernel: str):
     when no capture exists for the current build of this kernel."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
+        return None
+    if kernel.split("[")[0] not in KERNEL_SOURCES:
         return None
     src = kernel_source_hash(kernel)
     for line in open(path):
@@ -347,11 +350,14 @@ def main():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--path", default="index", choices=["index", "workspace", "dense"],
+    ap.add_argument("--path", default="index",
+                    choices=["index", "workspace", "dense", "indexer_fp8", "indexer_store"],
                     help="index: the index-keyed gather into [T, W+P, D]; workspace: the "
                          "prefill workspace path (range gathers + workspace indices); dense: "
                          "the no-top-k decode step of a heavily compressed layer (the "
-                         "decode_hca workload always takes it)")
+                         "decode_hca workload always takes it); indexer_fp8 / indexer_store: "
+                         "the mxfp4 workload's step with the FP8 indexer record or the fused "
+                         "norm-RoPE store as the key writer")
     ap.add_argument("--eager", action="store_true",
                     help="launch the step eagerly instead of replaying a CUDA graph")
     args = ap.parse_args()
@@ -386,8 +392,13 @@ def main():
         raise SystemExit("the workspace path needs a workload with an FP8 part")
     if path == "dense" and w.dense_width <= 0:
         raise SystemExit("the dense path needs a workload with dense compressed entries")
-    launches = {"workspace": p.workspace_launches, "dense": p.dense_launches,
-                "index": p.launches}[path]()
+    if path.startswith("indexer_") and (w.index_k is None or w.index_head_dim != 128):
+        raise SystemExit("the indexer paths need 128-dim indexer keys")
+    if path.startswith("indexer_"):
+        launches = p.indexer_launches(path.split("_")[1])
+    else:
+        launches = {"workspace": p.workspace_launches, "dense": p.dense_launches,
+                    "index": p.launches}[path]()
     names = [n for n, _ in launches]
     flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
@@ -402,6 +413,9 @@ def main():
     elif path == "dense":
         alg = dense_algorithmic_bytes(p, {"swa_indices": p.swa_indices.cpu().numpy(),
                                           "dense_indices": p.dense_indices.cpu().numpy()})
+    elif path.startswith("indexer_"):
+        alg = indexer_algorithmic_bytes(p, path.split("_")[1],
+                                        {"global_topk": p.global_topk.cpu().numpy()})
     else:
         outputs = {"global_topk": p.global_topk.cpu().numpy()}
         if w.has_fp8:
@@ -584,6 +598,11 @@ def run_e2e(p, args, dev, flush, path="index"):
         ins = [t for t in (p.k, p.insert_slots, p.qsl, p.seq_lens, p.t2r, p.positions)
                if t is not None]
         outs = [p.swa_indices, p.swa_lens, p.dense_indices, p.dense_lens, p.dense_gathered]
+    elif path.startswith("indexer_"):
+        ins = [p.index_k, p.index_insert_slots, p.topk, p.t2r]
+        if path == "indexer_store":
+            ins.append(p.ix_positions)
+        outs = [p.global_topk, p.global_lens, p.gathered_index]
     else:
         outs = [t for t in (p.sparse_indices, p.lens, p.gathered, p.global_topk, p.global_lens,
                             p.gathered_index) if t is not None]
@@ -609,7 +628,22 @@ def run_e2e(p, args, dev, flush, path="index"):
 
 def _oracle_step(w, path: str, caches):
     """(one oracle step as a callable, tokens it covers, description) for a path."""
-    from oracle.pipeline import run_dense_step, run_step, run_workspace_step
+    from oracle.pipeline import run_dense_step, run_indexer_step, run_step, run_workspace_step
+    if path.startswith("indexer_"):
+        from paged_sparse_kv_gb300 import synthetic
+        from paged_sparse_kv_gb300.pipeline import Pipeline
+        variant = path.split("_")[1]
+        n = w.index_k.shape[0]
+        inputs = {"positions": np.arange(n, dtype=np.int64) % Pipeline.INDEXER_MAX_POS,
+                  "cos_sin": synthetic.gptj_cos_sin(Pipeline.INDEXER_MAX_POS),
+                  "weight": synthetic.norm_weight(w.seed), "eps": 1e-6}
+        g = w.index_cache
+        cache = (np.zeros((g.num_pages, g.block_size * 132), np.uint8) if variant == "fp8"
+                 else caches["index_cache"])
+        toks, nt = _oracle_sample_tokens(w, 80000)
+        return (lambda: run_indexer_step(w, variant, cache, inputs, toks), nt,
+                f"oracle step of the {w.name} batch ({path} path) per timed step; gathers over "
+                f"{nt} of {w.num_tokens} tokens")
     if path == "dense":
         return (lambda: run_dense_step(w, caches["swa_cache"], caches["comp_cache"]),
                 w.num_tokens, f"oracle step of the {w.name} batch (dense path) per timed step")

@@ -456,7 +456,7 @@ psk_status write_indexer_fp8_cache(
  * follows the pages' torch form of it.
  *
  *   k_pre            bf16 [num_tokens, 128], row stride k_row_stride (elements,
- *                    multiple of 4; 8-byte aligned).
+ *                    multiple of 8; 16-byte aligned).
  *   positions        int64 [num_tokens].
  *   cos_sin_cache    binary32 [max_pos, cs_stride]: 32 cos then 32 sin (GPT-J).
  *   rms_norm_weight  binary32 [128], 16-byte aligned.

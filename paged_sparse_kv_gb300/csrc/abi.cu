@@ -577,8 +577,8 @@ psk_status indexer_k_norm_rope_store(const void* k_pre, int64_t k_row_stride,
     if (num_tokens == 0) return ok();
     CHECK(k_pre && positions && cos_sin_cache && rms_norm_weight && kv_slot_mapping,
           "k_pre, positions, cos_sin_cache, rms_norm_weight and kv_slot_mapping must be non-null");
-    CHECK(aligned(k_pre, 8) && k_row_stride >= 128 && k_row_stride % 4 == 0,
-          "k_pre must be 8-byte aligned with a row stride >= 128 and a multiple of 4 elements");
+    CHECK(aligned(k_pre, 16) && k_row_stride >= 128 && k_row_stride % 8 == 0,
+          "k_pre must be 16-byte aligned with a row stride >= 128 and a multiple of 8 elements");
     CHECK(aligned(positions, 8) && aligned(kv_slot_mapping, 8),
           "positions and kv_slot_mapping must be 8-byte aligned");
     CHECK(aligned(cos_sin_cache, 4), "cos_sin_cache must be 4-byte aligned");

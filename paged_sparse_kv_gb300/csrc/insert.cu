@@ -343,97 +343,256 @@ fp8_indexer_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
 // ---- indexer_k_norm_rope_store ---------------------------------------------------------
 //
 // vLLM deepseek_v41 ops, indexer_k_norm_rope_store: k_norm -> RoPE -> quant ->
-// paged store of 128-dim indexer keys.  One warp per token; lane l holds dims
-// 4l..4l+3 (one 8-byte load).
+// paged store of 128-dim indexer keys.  Eight lanes per key, four keys per
+// warp; lane g holds the chunk A = dims [8g, 8g + 8) of the un-rotated half
+// and the chunk B = dims [64 + 8g, 64 + 8g + 8) of the RoPE half, so every
+// lane rotates four pairs.
 //  * Emission: slot >= 0 and the token closes its compress group,
 //    (pos + 1) % ratio == 0 (TokenSpeed _compress_v4_state_windows_capturable's
-//    valid_token rule).
+//    valid_token rule); other rows are not read (except that with ratio 1,
+//    where every row with a slot writes, the row is loaded with the slot).
 //  * RMSNorm in binary32, every operation rounded once (no contraction): the
-//    sum of squares is a pairwise sum -- (s0 + s1) + (s2 + s3) in the lane,
-//    then xor-shuffles over 1, 2, 4, 8, 16 lanes, i.e. recursive halving of
-//    the index range; variance = sum / 128; r = binary32 of 1 / sqrt(variance
-//    + eps) with the square root and the quotient in IEEE binary64;
-//    y = (x * r) * weight.
-//  * GPT-J RoPE (TokenSpeed _apply_gptj_rope_tail_rows) on dims 64..127 (lanes
-//    16..31: two pairs each) at the cos_sin row of the group's first position
-//    floor(pos / ratio) * ratio.
-//  * MXFP4 record (8-lane blocks) or FP8 indexer record (row amax), with the
-//    inserts' rules.
-template <bool FP4>
-__global__ void __launch_bounds__(kThreads) norm_rope_store_kernel(NormRopeParams p,
-                                                                   int32_t shift) {
-    const int lane = threadIdx.x & 31;
-    const int64_t t = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / kWarp;
-    pdl_wait();
-    pdl_launch_dependents();
-    if (t >= p.num_tokens) return;
-    const int64_t sl = __ldg(p.slots + t);
-    if (sl < 0) return;
-    const int64_t pos = __ldg(p.positions + t);
-    int64_t rem = (pos + 1) % p.ratio;
-    if (rem < 0) rem += p.ratio;
-    if (rem != 0) return;  // not a group boundary: the row is not read
-    int64_t grp = pos / p.ratio;
-    if (pos % p.ratio != 0 && pos < 0) grp -= 1;
-    const int64_t prow = grp * p.ratio;
-    const int64_t capacity = p.num_pages * (int64_t)p.block_size;
-    if (sl >= capacity || prow < 0 || prow >= p.max_pos) {
-        if (lane == 0 && p.err_count) atomicAdd(p.err_count, 1);
-        return;
-    }
+//    sum of squares is a pairwise sum (recursive halving of the index range):
+//    each half of the row is a tree over its eight 8-dim chunks -- a 3-level
+//    tree in the lane, then xor-shuffles over 1, 2, 4 lanes -- and the sum is
+//    the two halves' sum.  variance = sum * 2^-7 (= sum / 128 exactly);
+//    r = 1 / sqrt(variance + eps) as an IEEE binary32 square root then an IEEE
+//    reciprocal (= the IEEE quotient 1 / s); y = (x * r) * weight.
+//  * GPT-J RoPE (TokenSpeed _apply_gptj_rope_tail_rows) on chunk B at the
+//    cos_sin row of the group's first position floor(pos / ratio) * ratio.
+//  * MXFP4 record (a 32-block is one chunk of four lanes) or FP8 indexer record
+//    (row amax), with the inserts' rules; the scale exponents are read off the
+//    binary32 amax without dividing (exact for any normal binary32 amax, as
+//    for bf16: see ceil_log2_div_const).
+// Keys of a warp that do not write still take part in every shuffle.
+// One key's state between the stages of the kernel below.
+struct NormRopeKey {
+    bool act;
+    int64_t sl, pos, prow;
+    uint4 ka, kb;     // chunks A and B of the bf16 row
+    float c4[4], s4[4];
+};
 
-    const uint2 kw = ld_nc_v2(p.k + t * p.k_row_stride + 4 * lane);
-    float y[4] = {bf16_lo(kw.x), bf16_hi(kw.x), bf16_lo(kw.y), bf16_hi(kw.y)};
-    float ss = __fadd_rn(__fadd_rn(__fmul_rn(y[0], y[0]), __fmul_rn(y[1], y[1])),
-                         __fadd_rn(__fmul_rn(y[2], y[2]), __fmul_rn(y[3], y[3])));
-#pragma unroll
-    for (int m = 1; m < kWarp; m <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, m));
-    const float variance = __fdiv_rn(ss, 128.0f);
-    const float r =
-        __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn((double)__fadd_rn(variance, p.eps))));
-    const float4 wv = __ldg(reinterpret_cast<const float4*>(p.weight) + lane);
-    y[0] = __fmul_rn(__fmul_rn(y[0], r), wv.x);
-    y[1] = __fmul_rn(__fmul_rn(y[1], r), wv.y);
-    y[2] = __fmul_rn(__fmul_rn(y[2], r), wv.z);
-    y[3] = __fmul_rn(__fmul_rn(y[3], r), wv.w);
-    if (lane >= 16) {
-        const float* cs = p.cos_sin + prow * p.cs_stride;
-        const int i0 = 2 * lane - 32;  // pair index of dims 4l, 4l + 1
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float c = __ldg(cs + i0 + h), sn = __ldg(cs + 32 + i0 + h);
-            const float e = y[2 * h], o = y[2 * h + 1];
-            y[2 * h] = __fsub_rn(__fmul_rn(e, c), __fmul_rn(o, sn));
-            y[2 * h + 1] = __fadd_rn(__fmul_rn(e, sn), __fmul_rn(o, c));
+// Round trip 1: the slot and the position; with ratio 1 (EVERY_ROW: every row
+// with a slot writes) the key row too.
+template <bool EVERY_ROW>
+__device__ __forceinline__ void nrs_load(const NormRopeParams& p, int64_t t, int gl,
+                                         NormRopeKey& k) {
+    k.act = t < p.num_tokens;
+    k.sl = -1;
+    k.pos = k.prow = 0;
+    k.ka = k.kb = make_uint4(0u, 0u, 0u, 0u);
+    if (k.act) {
+        k.sl = __ldg(p.slots + t);
+        k.pos = __ldg(p.positions + t);
+        if (EVERY_ROW) {
+            const uint16_t* row = p.k + t * p.k_row_stride + 8 * gl;
+            k.ka = ld_stream_v4(row);
+            k.kb = ld_stream_v4(row + 64);
         }
     }
+}
 
-    int64_t off;
-    const int64_t page = div_block(sl, p.block_size, shift, off);
-    uint8_t* base = p.cache + page * p.page_stride;
-    float a = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
-    if constexpr (FP4) {
-#pragma unroll
-        for (int m = 1; m < 8; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, m));
-        const int e = ceil_log2_pos(__fdiv_rn(fmaxf(a, 1.0e-4f), 6.0f));
-        const float pw = exp2_int(-e);
-        const uint32_t lo = cvt_e2m1x2(__fmul_rn(y[0], pw), __fmul_rn(y[1], pw)) & 0xFFu;
-        const uint32_t hi = cvt_e2m1x2(__fmul_rn(y[2], pw), __fmul_rn(y[3], pw)) & 0xFFu;
-        *reinterpret_cast<uint16_t*>(base + off * 64 + 2 * lane) = (uint16_t)(lo | (hi << 8));
-        if ((lane & 7) == 0)
-            base[(int64_t)p.block_size * 64 + off * 4 + lane / 8] =
-                (uint8_t)min(max(e + 127, 0), 254);
-    } else {
-#pragma unroll
-        for (int m = 1; m < kWarp; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, m));
-        const int e = ceil_log2_pos(fmaxf(__fdiv_rn(a, 448.0f), 1.0e-10f));
-        const float pw = exp2_int(-e);
-        const uint32_t q = cvt_e4m3x2(__fmul_rn(y[0], pw), __fmul_rn(y[1], pw)) |
-                           (cvt_e4m3x2(__fmul_rn(y[2], pw), __fmul_rn(y[3], pw)) << 16);
-        *reinterpret_cast<uint32_t*>(base + off * 128 + 4 * lane) = q;
-        if (lane == 0)
-            *reinterpret_cast<float*>(base + (int64_t)p.block_size * 128 + off * 4) = exp2_int(e);
+// The emission rule and range checks, then round trip 2: the key row (unless
+// already loaded) and chunk B's four cos and four sin values.
+template <bool EVERY_ROW, bool CS_VEC>
+__device__ __forceinline__ void nrs_resolve(const NormRopeParams& p, int64_t t, int gl,
+                                            NormRopeKey& k) {
+    k.act = k.act && k.sl >= 0;
+    if (k.act) {
+        const int64_t pos = k.pos;
+        const uint32_t ratio = (uint32_t)p.ratio;
+        bool boundary;
+        if (pos >= 0 && pos < 0xFFFFFFFFll) {
+            const uint32_t q = (uint32_t)pos / ratio;
+            boundary = (uint32_t)pos - q * ratio == ratio - 1u;
+            k.prow = (int64_t)q * ratio;
+        } else {
+            int64_t rem = (pos + 1) % p.ratio;
+            if (rem < 0) rem += p.ratio;
+            boundary = rem == 0;
+            int64_t grp = pos / p.ratio;
+            if (pos % p.ratio != 0 && pos < 0) grp -= 1;
+            k.prow = grp * p.ratio;
+        }
+        k.act = boundary;
+        if (k.act && (k.sl >= p.num_pages * (int64_t)p.block_size || k.prow < 0 ||
+                      k.prow >= p.max_pos)) {
+            if (gl == 0 && p.err_count) atomicAdd(p.err_count, 1);
+            k.act = false;
+        }
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        k.c4[j] = 1.0f;
+        k.s4[j] = 0.0f;
+    }
+    if (k.act) {
+        if (!EVERY_ROW) {
+            const uint16_t* row = p.k + t * p.k_row_stride + 8 * gl;
+            k.ka = ld_stream_v4(row);
+            k.kb = ld_stream_v4(row + 64);
+        }
+        const float* cs = p.cos_sin + k.prow * p.cs_stride + 4 * gl;
+        if (CS_VEC) {
+            const float4 cv = __ldg(reinterpret_cast<const float4*>(cs));
+            const float4 sv = __ldg(reinterpret_cast<const float4*>(cs + 32));
+            k.c4[0] = cv.x; k.c4[1] = cv.y; k.c4[2] = cv.z; k.c4[3] = cv.w;
+            k.s4[0] = sv.x; k.s4[1] = sv.y; k.s4[2] = sv.z; k.s4[3] = sv.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                k.c4[j] = __ldg(cs + j);
+                k.s4[j] = __ldg(cs + 32 + j);
+            }
+        }
+    }
+}
+
+// Norm, RoPE, quantize and store one key (every lane of the warp takes part
+// in the shuffles).
+template <bool FP4>
+__device__ __forceinline__ void nrs_compute_store(const NormRopeParams& p, int32_t shift, int gl,
+                                                  const NormRopeKey& k) {
+    constexpr int LPT = 8;
+    const bool act = k.act;
+    float ya[8], yb[8];
+    {
+        const uint32_t wa[4] = {k.ka.x, k.ka.y, k.ka.z, k.ka.w};
+        const uint32_t wb[4] = {k.kb.x, k.kb.y, k.kb.z, k.kb.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ya[2 * i] = act ? bf16_lo(wa[i]) : 0.0f;
+            ya[2 * i + 1] = act ? bf16_hi(wa[i]) : 0.0f;
+            yb[2 * i] = act ? bf16_lo(wb[i]) : 0.0f;
+            yb[2 * i + 1] = act ? bf16_hi(wb[i]) : 0.0f;
+        }
+    }
+    // pairwise sum of squares of each chunk (8 -> 4 -> 2 -> 1), then over the
+    // half's eight chunks (lanes), then the two halves
+    float sa[4], sb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        sa[i] = __fadd_rn(__fmul_rn(ya[2 * i], ya[2 * i]), __fmul_rn(ya[2 * i + 1], ya[2 * i + 1]));
+        sb[i] = __fadd_rn(__fmul_rn(yb[2 * i], yb[2 * i]), __fmul_rn(yb[2 * i + 1], yb[2 * i + 1]));
+    }
+    float ha = __fadd_rn(__fadd_rn(sa[0], sa[1]), __fadd_rn(sa[2], sa[3]));
+    float hb = __fadd_rn(__fadd_rn(sb[0], sb[1]), __fadd_rn(sb[2], sb[3]));
+#pragma unroll
+    for (int m = 1; m < LPT; m <<= 1) {
+        ha = __fadd_rn(ha, __shfl_xor_sync(0xFFFFFFFFu, ha, m));
+        hb = __fadd_rn(hb, __shfl_xor_sync(0xFFFFFFFFu, hb, m));
+    }
+    const float variance = __fmul_rn(__fadd_rn(ha, hb), 0.0078125f);
+    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(variance, p.eps)));
+    const float4* wv = reinterpret_cast<const float4*>(p.weight) + 2 * gl;
+    const float4 w0 = __ldg(wv), w1 = __ldg(wv + 1), w2 = __ldg(wv + 16), w3 = __ldg(wv + 17);
+    const float wa8[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const float wb8[8] = {w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        ya[i] = __fmul_rn(__fmul_rn(ya[i], r), wa8[i]);
+        yb[i] = __fmul_rn(__fmul_rn(yb[i], r), wb8[i]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float e = yb[2 * j], o = yb[2 * j + 1];
+        yb[2 * j] = __fsub_rn(__fmul_rn(e, k.c4[j]), __fmul_rn(o, k.s4[j]));
+        yb[2 * j + 1] = __fadd_rn(__fmul_rn(e, k.s4[j]), __fmul_rn(o, k.c4[j]));
+    }
+
+    float aa = 0.0f, ab = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        aa = fmaxf(aa, fabsf(ya[i]));
+        ab = fmaxf(ab, fabsf(yb[i]));
+    }
+    int64_t off = 0;
+    uint8_t* base = p.cache;
+    if (act) {
+        const int64_t page = div_block(k.sl, p.block_size, shift, off);
+        base = p.cache + page * p.page_stride;
+    }
+    if constexpr (FP4) {
+        // 32-blocks: chunk A of lanes 0-3 / 4-7 (blocks 0, 1), chunk B (blocks 2, 3)
+#pragma unroll
+        for (int m = 1; m < 4; m <<= 1) {
+            aa = fmaxf(aa, __shfl_xor_sync(0xFFFFFFFFu, aa, m));
+            ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, m));
+        }
+        const int ea = ceil_log2_div_const(fmaxf(aa, 1.0e-4f), 0x400000u, 2);  // / 6
+        const int eb = ceil_log2_div_const(fmaxf(ab, 1.0e-4f), 0x400000u, 2);
+        const uint64_t pa = splat_f32x2(exp2_int(-ea)), pb = splat_f32x2(exp2_int(-eb));
+        uint32_t qa = 0u, qb = 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float a0 = ya[2 * j], a1 = ya[2 * j + 1], b0 = yb[2 * j], b1 = yb[2 * j + 1];
+            mul2_rn(a0, a1, pa);
+            mul2_rn(b0, b1, pb);
+            qa |= (cvt_e2m1x2(a0, a1) & 0xFFu) << (8 * j);
+            qb |= (cvt_e2m1x2(b0, b1) & 0xFFu) << (8 * j);
+        }
+        if (act) {
+            uint8_t* vals = base + off * 64;
+            *reinterpret_cast<uint32_t*>(vals + 4 * gl) = qa;
+            *reinterpret_cast<uint32_t*>(vals + 32 + 4 * gl) = qb;
+            if ((gl & 3) == 0) {
+                uint8_t* scl = base + (int64_t)p.block_size * 64 + off * 4 + gl / 4;
+                scl[0] = (uint8_t)min(max(ea + 127, 0), 254);
+                scl[2] = (uint8_t)min(max(eb + 127, 0), 254);
+            }
+        }
+    } else {
+        float a = fmaxf(aa, ab);
+#pragma unroll
+        for (int m = 1; m < LPT; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, m));
+        // max(a / 448, 1e-10) then ceil(log2): the floor's exponent is -33
+        const int e = max(ceil_log2_div_const(a, 0x600000u, 8), -33);
+        const uint64_t pw = splat_f32x2(exp2_int(-e));
+        uint32_t qa[2], qb[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float a0 = ya[4 * h], a1 = ya[4 * h + 1], a2 = ya[4 * h + 2], a3 = ya[4 * h + 3];
+            float b0 = yb[4 * h], b1 = yb[4 * h + 1], b2 = yb[4 * h + 2], b3 = yb[4 * h + 3];
+            mul2_rn(a0, a1, pw);
+            mul2_rn(a2, a3, pw);
+            mul2_rn(b0, b1, pw);
+            mul2_rn(b2, b3, pw);
+            qa[h] = cvt_e4m3x2(a0, a1) | (cvt_e4m3x2(a2, a3) << 16);
+            qb[h] = cvt_e4m3x2(b0, b1) | (cvt_e4m3x2(b2, b3) << 16);
+        }
+        if (act) {
+            uint8_t* vals = base + off * 128;
+            *reinterpret_cast<uint2*>(vals + 8 * gl) = make_uint2(qa[0], qa[1]);
+            *reinterpret_cast<uint2*>(vals + 64 + 8 * gl) = make_uint2(qb[0], qb[1]);
+            if (gl == 0)
+                *reinterpret_cast<float*>(base + (int64_t)p.block_size * 128 + off * 4) = exp2_int(e);
+        }
+    }
+}
+
+#ifndef PSK_NORM_ROPE_UNROLL
+#define PSK_NORM_ROPE_UNROLL 2
+#endif
+
+// U keys per 8-lane group: all of the keys' first-round loads are issued
+// before any is used, then all second-round loads, then the arithmetic.
+template <bool FP4, bool EVERY_ROW, bool CS_VEC, int U>
+__global__ void __launch_bounds__(kThreads) norm_rope_store_kernel(NormRopeParams p,
+                                                                   int32_t shift) {
+    constexpr int LPT = 8;  // lanes per key
+    const int gl = (threadIdx.x & 31) % LPT;
+    const int64_t g = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / LPT;
+    const int64_t ngroups = (int64_t)gridDim.x * kThreads / LPT;
+    pdl_wait();
+    pdl_launch_dependents();
+    NormRopeKey k[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) nrs_load<EVERY_ROW>(p, g + u * ngroups, gl, k[u]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) nrs_resolve<EVERY_ROW, CS_VEC>(p, g + u * ngroups, gl, k[u]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) nrs_compute_store<FP4>(p, shift, gl, k[u]);
 }
 
 template <int D, bool UE8M0>
@@ -492,9 +651,21 @@ cudaError_t launch_fp8_indexer_insert(const InsertParams& p, cudaStream_t stream
 }
 
 cudaError_t launch_norm_rope_store(const NormRopeParams& p, cudaStream_t stream) {
-    const int64_t blocks = (p.num_tokens * kWarp + kThreads - 1) / kThreads;
+    constexpr int U = PSK_NORM_ROPE_UNROLL;
+    // 8 lanes per key, U keys per lane group (keys g, g + G, ... for G groups)
+    const int64_t groups = (p.num_tokens + U - 1) / U;
+    const int64_t blocks = (groups * 8 + kThreads - 1) / kThreads;
     const int32_t shift = log2_if_pow2(p.block_size);
-    auto kern = p.record == 1 ? norm_rope_store_kernel<true> : norm_rope_store_kernel<false>;
+    const bool every = p.ratio == 1;
+    const bool cs_vec = (reinterpret_cast<uintptr_t>(p.cos_sin) & 15) == 0 && p.cs_stride % 4 == 0;
+    using Kern = void (*)(NormRopeParams, int32_t);
+    // [fp4][every row][vector cos/sin]
+    static const Kern kTable[2][2][2] = {
+        {{norm_rope_store_kernel<false, false, false, U>, norm_rope_store_kernel<false, false, true, U>},
+         {norm_rope_store_kernel<false, true, false, U>, norm_rope_store_kernel<false, true, true, U>}},
+        {{norm_rope_store_kernel<true, false, false, U>, norm_rope_store_kernel<true, false, true, U>},
+         {norm_rope_store_kernel<true, true, false, U>, norm_rope_store_kernel<true, true, true, U>}}};
+    const Kern kern = kTable[p.record == 1][every][cs_vec];
     return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p, shift);
 }
 

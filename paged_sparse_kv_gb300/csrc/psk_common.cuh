@@ -96,9 +96,13 @@ __device__ __forceinline__ int ceil_log2_pos(float q) {
 // whenever a / c is either exactly a power of two or farther than half an ulp
 // from every power of two.  For c = 448 = 1.75 * 2^8 and c = 6 = 1.5 * 2^2 that
 // holds for every a with an 8-bit significand (a bf16 block amax: a / c is a
-// power of two exactly when s = cs, and otherwise at least ~0.4% away) and for
-// the 1e-4 floor.  a must be positive and normal; +inf gives 128 (as the
-// quotient inf would).
+// power of two exactly when s = cs, and otherwise at least ~0.4% away), for
+// the 1e-4 floor, and for every normal binary32 a: the significands next to
+// cs are cs +- 2^-23, whose quotients s / cs lie at least 2^-23 / 1.75 above 1
+// (more than the half ulp 2^-24 above 1) or below 1 (more than the half ulp
+// 2^-25 below 1), so RN(a / c) is a power of two exactly when s = cs and is
+// on the same side of it as a / c otherwise (the quotient must stay normal).
+// a must be positive and normal; +inf gives 128 (as the quotient inf would).
 __device__ __forceinline__ int ceil_log2_div_const(float a, uint32_t cs_mant, int cx) {
     const uint32_t b = __float_as_uint(a);
     if (b >= 0x7F800000u) return 128;

@@ -39,6 +39,16 @@ raw:
   stream A:  quantize_and_insert_k_cache -> dequantize_and_gather_k_cache_ranges[swa]
   stream B:  write_indexer_mxfp4_cache -> indexer_mxfp4_paged_gather
 
+``path="indexer_fp8"`` and ``path="indexer_store"`` are the indexer step of
+the MXFP4 workload with the other key writers: the FP8 indexer record
+(write_indexer_fp8_cache, read back as record 2) and the fused k_norm -> RoPE
+-> MXFP4 store (indexer_k_norm_rope_store, ratio 1, positions cycling through
+a 131072-row GPT-J table):
+
+  stream A:  <key writer>
+  stream B:  compute_global_topk_indices_and_lens
+  join:      gather of the top-k keys
+
 ``path="dense"`` is the decode step of a heavily compressed attention layer
 (no top-k; TokenSpeed's decode SWA precompute and
 ``_decode_compressed_attention_indices_and_lens`` for a ratio other than 4):
@@ -211,6 +221,53 @@ class Pipeline:
                  w.comp_cache.block_size, rope_dim=w.rope_dim)),
         ]
 
+    INDEXER_MAX_POS = 131072
+
+    def alloc_indexer(self) -> None:
+        """Buffers of the indexer_fp8 / indexer_store steps."""
+        from . import synthetic
+        w, dev = self.w, self.dev
+        g = w.index_cache
+        n = w.index_k.shape[0]
+        self.fp8i_cache = torch.zeros((g.num_pages, g.block_size * 132), dtype=torch.uint8,
+                                      device=dev)
+        self.ix_positions = torch.arange(n, dtype=torch.int64, device=dev) % self.INDEXER_MAX_POS
+        self.ix_cos_sin = torch.from_numpy(synthetic.gptj_cos_sin(self.INDEXER_MAX_POS)).to(dev)
+        self.ix_weight = torch.from_numpy(synthetic.norm_weight(w.seed)).to(dev)
+        self.ix_eps = 1e-6
+
+    def indexer_launches(self, variant: str) -> list[tuple[str, Callable[[], None]]]:
+        """The indexer step with the FP8 indexer record ("fp8") or the fused
+        norm-RoPE-MXFP4 store ("store") as the key writer."""
+        w = self.w
+        if getattr(self, "fp8i_cache", None) is None:
+            self.alloc_indexer()
+        bs = w.index_cache.block_size
+        topk = ("compute_global_topk_indices_and_lens",
+                lambda: ops.compute_global_topk_indices_and_lens(
+                    self.topk, self.t2r, self.index_table, bs, self.valid,
+                    out=self.global_topk, lens=self.global_lens))
+        if variant == "fp8":
+            return [
+                ("write_indexer_fp8_cache", lambda: ops.write_indexer_fp8_cache(
+                    self.index_k, self.fp8i_cache, self.index_insert_slots, bs,
+                    err_count=self.err)),
+                topk,
+                ("dequantize_and_gather_k_cache[fp8_indexer]",
+                 lambda: ops.dequantize_and_gather_k_cache(
+                     self.gathered_index, self.fp8i_cache, self.global_topk, bs,
+                     record=ops.PSK_REC_FP8_INDEXER)),
+            ]
+        return [
+            ("indexer_k_norm_rope_store", lambda: ops.indexer_k_norm_rope_store(
+                self.index_k, self.ix_positions, self.ix_cos_sin, self.ix_weight, self.ix_eps,
+                self.index_cache, self.index_insert_slots, 1, True, bs, err_count=self.err)),
+            topk,
+            ("dequantize_and_gather_k_cache[mxfp4]", lambda: ops.dequantize_and_gather_k_cache(
+                self.gathered_index, self.index_cache, self.global_topk, bs,
+                record=ops.PSK_REC_MXFP4)),
+        ]
+
     # the indexer cache follows the compressed table
     @property
     def index_table(self) -> torch.Tensor:
@@ -281,6 +338,8 @@ class Pipeline:
             return self._workspace_step(concurrent, hooks or {})
         if path == "dense":
             return self._dense_step(concurrent, hooks or {})
+        if path in ("indexer_fp8", "indexer_store"):
+            return self._indexer_step(concurrent, hooks or {}, path.split("_")[1])
         L = dict(self.launches())
         hooks = hooks or {}
 
@@ -364,6 +423,43 @@ class Pipeline:
         main.wait_event(done_a)
         main.wait_event(done_b)
 
+
+    def _indexer_step(self, concurrent: bool, hooks: dict, variant: str) -> None:
+        L = self.indexer_launches(variant)
+        names = [n for n, _ in L]
+        fns = dict(L)
+
+        def run(name):
+            pre, post = hooks.get(name, (None, None))
+            if pre:
+                pre()
+            fns[name]()
+            if post:
+                post()
+
+        if not concurrent:
+            for name in names:
+                run(name)
+            return
+        main = torch.cuda.current_stream(self.dev)
+        if not hasattr(self, "_side"):
+            self._side = (torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev))
+        sa, sb = self._side
+        fork = torch.cuda.Event()
+        fork.record(main)
+        sa.wait_event(fork)
+        sb.wait_event(fork)
+        with torch.cuda.stream(sb):
+            run(names[1])
+            done_b = torch.cuda.Event()
+            done_b.record(sb)
+        with torch.cuda.stream(sa):
+            run(names[0])
+            done_a = torch.cuda.Event()
+            done_a.record(sa)
+        main.wait_event(done_a)
+        main.wait_event(done_b)
+        run(names[2])
 
     def _dense_step(self, concurrent: bool, hooks: dict) -> None:
         L = dict(self.dense_launches())

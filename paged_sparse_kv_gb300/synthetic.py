@@ -394,6 +394,21 @@ def make(name: str, seed_offset: int = 0) -> Workload:
     return MAKERS[name](DEFAULT_SEEDS[name] + seed_offset)
 
 
+def gptj_cos_sin(max_pos: int, rope_dim: int = 64, base: float = 10000.0) -> np.ndarray:
+    """A RoPE table [max_pos, rope_dim] in binary32, GPT-J layout (rope_dim/2
+    cosines, then rope_dim/2 sines) with the usual inverse-frequency ladder:
+    the input a model's RoPE instance would hand the indexer-key store."""
+    half = rope_dim // 2
+    theta = base ** (-np.arange(half, dtype=np.float64) / half)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * theta[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def norm_weight(seed: int, dim: int = 128) -> np.ndarray:
+    """A k_norm weight vector [dim] in binary32, U[0.5, 2]."""
+    return np.random.default_rng(seed).uniform(0.5, 2.0, size=dim).astype(np.float32)
+
+
 def random_cache_bytes(seed: int, geom: CacheGeom) -> np.ndarray:
     """A cache filled with seeded random bytes, none of them 0x7F or 0xFF (the
     E4M3 NaN codes), so that every record decodes to finite or infinite

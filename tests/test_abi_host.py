@@ -330,7 +330,7 @@ def _nrs(**kw):
 
 
 @pytest.mark.parametrize("kw", [dict(rec=0), dict(rec=3), dict(ratio=0), dict(css=32),
-                                dict(maxp=-1), dict(ks=126), dict(ks=100), dict(k=A + 2),
+                                dict(maxp=-1), dict(ks=126), dict(ks=132), dict(k=A + 8),
                                 dict(pos=B + 4), dict(w=A + 4100), dict(cs=C + 2),
                                 dict(page_stride=64 * 68 - 16), dict(rec=2, page_stride=64 * 68),
                                 dict(k=None), dict(slots=None), dict(n=-1), dict(err=B + 1)])

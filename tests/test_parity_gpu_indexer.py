@@ -90,10 +90,11 @@ def _gptj_table(max_pos, dtype=np.float32):
     return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(dtype)
 
 
+@pytest.mark.parametrize("cs_pad", [0, 3])
 @pytest.mark.parametrize("fp4", [True, False])
 @pytest.mark.parametrize("ratio", [1, 2, 4])
 @pytest.mark.parametrize("bs", [64, 3])
-def test_norm_rope_store_fuzz(cuda_device, fp4, ratio, bs):
+def test_norm_rope_store_fuzz(cuda_device, fp4, ratio, bs, cs_pad):
     rng = np.random.default_rng(100 * ratio + bs + fp4)
     N, pages, max_pos = 1500, 40, 4096
     x = rng.standard_normal((N, 136)).astype(np.float32)
@@ -116,6 +117,8 @@ def test_norm_rope_store_fuzz(cuda_device, fp4, ratio, bs):
     pos[11], slots[11] = 5 * ratio - 1, pages * bs + 1
     pos[13], slots[13] = max_pos + ratio - 1, pages * bs + 2
     cs = _gptj_table(max_pos)
+    cs_dev = np.zeros((max_pos, 64 + cs_pad), np.float32)  # stride 67: scalar cos/sin loads
+    cs_dev[:, :64] = cs
     w = rng.uniform(0.25, 4.0, size=128).astype(np.float32)
     eps = 1e-6
     rec = 68 if fp4 else 132
@@ -125,7 +128,7 @@ def test_norm_rope_store_fuzz(cuda_device, fp4, ratio, bs):
     dev_cache = torch.from_numpy(host).to(d)
     err = torch.zeros(1, dtype=torch.int32, device=d)
     kd = _bf16_dev(k, d)
-    ops.indexer_k_norm_rope_store(kd[:, :128], _i64(pos, d), torch.from_numpy(cs).to(d),
+    ops.indexer_k_norm_rope_store(kd[:, :128], _i64(pos, d), torch.from_numpy(cs_dev).to(d),
                                   torch.from_numpy(w).to(d), eps, dev_cache, _i64(slots, d), ratio,
                                   fp4, bs, err_count=err)
     n_err = oracle.indexer_k_norm_rope_store(np.ascontiguousarray(k[:, :128]), pos, cs, w, eps,
@@ -160,3 +163,37 @@ def test_norm_rope_store_prefill_size(cuda_device):
         oracle.indexer_k_norm_rope_store(np.ascontiguousarray(k[:, 64:192]), pos, cs[:, :64], wt,
                                          1e-6, slots, 4, 1 if fp4 else 2, host, bs)
         _assert_same(dev_cache.cpu().numpy(), host, f"prefill norm rope store fp4={fp4}")
+
+
+@pytest.mark.parametrize("path", ["indexer_fp8", "indexer_store"])
+def test_indexer_steps_match_oracle(cuda_device, path):
+    """The indexer steps of the 1,048,576-key workload as the benchmark launches
+    them (concurrent streams): every cache byte, the global top-k and lens, and
+    the gathered keys of a sample of tokens, against the oracle."""
+    from oracle.pipeline import run_indexer_step
+    from paged_sparse_kv_gb300.pipeline import Pipeline
+    w = synthetic.make("mxfp4")
+    p = Pipeline(w, cuda_device)
+    variant = path.split("_")[1]
+    p.indexer_launches(variant)
+    g = w.index_cache
+    if variant == "fp8":
+        host = np.zeros((g.num_pages, g.block_size * 132), np.uint8)
+        dev_cache = p.fp8i_cache
+    else:
+        host = synthetic.random_cache_bytes(44, g)
+        dev_cache = p.index_cache
+    dev_cache.copy_(torch.from_numpy(host))
+    p.step(concurrent=True, path=path)
+    torch.cuda.synchronize(cuda_device)
+    n = w.index_k.shape[0]
+    inputs = {"positions": np.arange(n, dtype=np.int64) % Pipeline.INDEXER_MAX_POS,
+              "cos_sin": synthetic.gptj_cos_sin(Pipeline.INDEXER_MAX_POS),
+              "weight": synthetic.norm_weight(w.seed), "eps": 1e-6}
+    toks = np.arange(0, w.num_tokens, 9)
+    want = run_indexer_step(w, variant, host, inputs, toks)
+    _assert_same(dev_cache.cpu().numpy(), host, f"{path} cache")
+    assert np.array_equal(p.global_topk.cpu().numpy(), want["global_topk"])
+    assert np.array_equal(p.global_lens.cpu().numpy(), want["global_lens"])
+    _assert_same(_u16(p.gathered_index)[toks], want["gathered_index"], f"{path} gathered")
+    assert int(p.err.item()) == want["err"] == 0
