@@ -282,17 +282,27 @@ KERNEL_SOURCES = {
 SHARED_SOURCES = ("psk_common.cuh", "launch.h")
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and with whitespace runs collapsed, so
+    that editing a comment does not mark a kernel as changed."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel: str) -> str:
-    """sha1 over the CUDA sources a timed kernel is built from (its .cu file,
-    its family's header and the shared headers); identifies the build a
-    recorded ncu capture belongs to."""
+    """sha1 over the code (comments and whitespace dropped) of the CUDA
+    sources a timed kernel is built from: its .cu file, its family's header
+    and the shared headers.  Identifies the build a recorded ncu capture
+    belongs to."""
     import hashlib
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "paged_sparse_kv_gb300", "csrc")
     base = kernel.split("[")[0]
     for f in sorted(KERNEL_SOURCES[base] + SHARED_SOURCES):
         h.update(f.encode())
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()
 
 
