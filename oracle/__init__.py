@@ -99,6 +99,13 @@ def _load():
             None, [_P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64, _P, _I64, _P]),
         "oracle_write_indexer_fp8_cache": (
             _I64, [_P, _I64, _P, _I64, _P, _I64, _I64, _I32, _I32]),
+        "oracle_exp_cw": (ctypes.c_float, [ctypes.c_float]),
+        "oracle_exp_cw_array": (None, [_P, _P, _I64]),
+        "oracle_save_compressor_state": (
+            _I64, [_P, _P, _I64, _P, _I32, _P, _P, _I64, _I32, _P, _I64, _I32]),
+        "oracle_compress_kv_cache_insert": (
+            _I64, [_P, _I64, _I32, _I32, _P, _P, _P, _P, _I64, _I32, _P, _I32, _I64, _I32, _I32,
+                   _I32, _I32, _P, ctypes.c_float, _P, _I64, _I64, _P, _I64, _I64, _I32, _P]),
         "oracle_indexer_k_norm_rope_store": (
             _I64, [_P, _I64, _P, _P, _I64, _I64, _P, ctypes.c_float, _P, _I64, _I32, _I32, _P,
                    _I64, _I64, _I32]),
@@ -430,3 +437,57 @@ def indexer_k_norm_rope_store(k_pre, positions, cos_sin_cache, rms_norm_weight, 
         _ptr(k_pre), k_pre.shape[1], _ptr(positions), _ptr(cs), cs.shape[1], cs.shape[0],
         _ptr(wt), float(rms_norm_eps), _ptr(slots), slots.shape[0], compress_ratio, record,
         _ptr(cache), cache.shape[0], cache.shape[1], block_size)
+
+
+# ---- compressed-KV producer -------------------------------------------------------------
+
+def exp_cw(x) -> np.ndarray:
+    """The oracle's binary32 exp (Cody-Waite reduction + Taylor polynomial)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    _load().oracle_exp_cw_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def save_compressor_state(kv, score, ape, slots, positions, compress_ratio, state_cache,
+                          block_size) -> int:
+    """state[slot] = [kv, score + ape[pos % ratio]]; state_cache float32
+    [pages, block_size, 2 * state_width] updated in place."""
+    kv = np.ascontiguousarray(kv, dtype=np.float32)
+    score = np.ascontiguousarray(score, dtype=np.float32)
+    ape = np.ascontiguousarray(ape, dtype=np.float32)
+    slots = _as(slots, np.int64)
+    positions = _as(positions, np.int64)
+    assert state_cache.dtype == np.float32 and state_cache.flags["C_CONTIGUOUS"]
+    sw = kv.shape[1]
+    assert state_cache.shape[1:] == (block_size, 2 * sw)
+    return _load().oracle_save_compressor_state(
+        _ptr(kv), _ptr(score), sw, _ptr(ape), sw, _ptr(slots), _ptr(positions),
+        slots.shape[0], compress_ratio, _ptr(state_cache), state_cache.shape[0], block_size)
+
+
+def compress_kv_cache_insert(state_cache, token_to_req, positions, state_slots, block_table,
+                             state_block_size, rms_norm_weight, rms_norm_eps, cos_sin_cache,
+                             kv_cache, kv_slots, kv_block_size, compress_ratio, overlap,
+                             num_reqs=None, base_offsets=None, head_dim=512) -> int:
+    """The compressed-KV producer: window softmax pooling of the state, RMSNorm,
+    GPT-J RoPE of the tail, fp8_ds_mla insert.  Returns the counted skips."""
+    assert state_cache.dtype == np.float32 and state_cache.flags["C_CONTIGUOUS"]
+    token_to_req = _as(token_to_req, np.int32)
+    positions = _as(positions, np.int64)
+    state_slots = _as(state_slots, np.int64)
+    block_table = _as(block_table, np.int32)
+    base_offsets = _as(base_offsets, np.int32)
+    wt = np.ascontiguousarray(rms_norm_weight, dtype=np.float32)
+    cs = np.ascontiguousarray(cos_sin_cache, dtype=np.float32)
+    kv_slots = _as(kv_slots, np.int64)
+    assert kv_cache.dtype == np.uint8 and kv_cache.ndim == 2 and kv_cache.flags["C_CONTIGUOUS"]
+    sw = state_cache.shape[2] // 2
+    R = block_table.shape[0] if num_reqs is None else num_reqs
+    return _load().oracle_compress_kv_cache_insert(
+        _ptr(state_cache), state_cache.shape[0], state_block_size, sw, _ptr(token_to_req),
+        _ptr(positions), _ptr(state_slots), _ptr(block_table), block_table.shape[1],
+        block_table.shape[1], _ptr(base_offsets), R, positions.shape[0], compress_ratio,
+        int(bool(overlap)), head_dim, cs.shape[1], _ptr(wt), float(rms_norm_eps), _ptr(cs),
+        cs.shape[1], cs.shape[0], _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1],
+        kv_block_size, _ptr(kv_slots))

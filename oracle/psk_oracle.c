@@ -1031,3 +1031,201 @@ int64_t oracle_indexer_k_norm_rope_store(
     }
     return errors;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Compressed-KV producer: compressor state, window pooling, record insert   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * exp of a binary32, by Cody and Waite's argument reduction (Cody & Waite,
+ * "Software Manual for the Elementary Functions", 1980) and the Taylor series:
+ *   k = nearest integer to x / ln 2 (x * 1.44269504, rounded to even);
+ *   r = x - k*ln2_hi - k*ln2_lo with ln2_hi = 0.693145751953125 (16 significant
+ *       bits, so k*ln2_hi is exact for |k| <= 256) and ln2_lo = ln 2 - ln2_hi,
+ *       each step one fused multiply-add;
+ *   exp(r) = 1 + r + r^2/2! + ... + r^7/7! by Horner with fused multiply-adds
+ *       (|r| <= 0.347: the first omitted term is below 6e-9 relative);
+ *   result = p * 2^k, as one multiply by a normal power of two (two when 2^k
+ *       is not normal, so a subnormal result is rounded once).
+ * Every operation is an IEEE binary32 one, so the kernels evaluate the same
+ * sequence to the same bits.  Pinned against the C library's exp within 2 ulp.
+ */
+float oracle_exp_cw(float x) {
+    if (isnan(x)) return x;
+    if (x > 88.7228f) return INFINITY;
+    if (x < -103.98f) return 0.0f;
+    const float k = rintf(x * 1.44269504f);
+    float r = fmaf(-k, 0.693145751953125f, x);
+    r = fmaf(-k, 1.42860677e-06f, r);
+    float p = 1.98412698e-04f;            /* 1/7! */
+    p = fmaf(p, r, 1.38888889e-03f);      /* 1/6! */
+    p = fmaf(p, r, 8.33333333e-03f);      /* 1/5! */
+    p = fmaf(p, r, 4.16666667e-02f);      /* 1/4! */
+    p = fmaf(p, r, 1.66666667e-01f);      /* 1/3! */
+    p = fmaf(p, r, 0.5f);                 /* 1/2! */
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    const int ki = (int)k;
+    if (ki < -126) return (p * pow2f(ki + 64)) * pow2f(-64);
+    if (ki > 127) return (p * pow2f(ki - 1)) * 2.0f;
+    return p * pow2f(ki);
+}
+
+/*
+ * [OPS] save_deepseek_v4_compressor_state: the compressor's residual state of
+ * each token, [kv_state | score_state] (each state_width binary32 values), in a
+ * paged cache [pages, block_size, 2 * state_width] at the token's state slot;
+ * the score state "includes the APE row selected by position % compress_ratio".
+ * The kernel is not printed; read as state[slot] = [kv[t], score[t] + ape[pos %
+ * ratio]] (binary32 adds).  Slots < 0 are skipped; slots beyond the cache are
+ * skipped and counted.
+ */
+int64_t oracle_save_compressor_state(
+    const float* kv, const float* score, int64_t in_stride, const float* ape,
+    int32_t state_width, const int64_t* slot_mapping, const int64_t* positions,
+    int64_t num_tokens, int32_t compress_ratio, float* state_cache, int64_t num_pages,
+    int32_t block_size) {
+    const int64_t capacity = num_pages * (int64_t)block_size;
+    int64_t errors = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int64_t s = slot_mapping[t];
+        if (s < 0) continue;
+        if (s >= capacity) {
+            ++errors;
+            continue;
+        }
+        int64_t a = positions[t] % compress_ratio;
+        if (a < 0) a += compress_ratio;
+        float* row = state_cache + s * 2 * (int64_t)state_width;
+        for (int32_t d = 0; d < state_width; ++d) {
+            row[d] = kv[t * in_stride + d];
+            row[state_width + d] = score[t * in_stride + d] + ape[a * state_width + d];
+        }
+    }
+    return errors;
+}
+
+/*
+ * [OPS] deepseek_v4_csa_compress_kv_cache_insert (compress_ratio 4, overlap) and
+ * deepseek_v4_hca_compress_kv_cache_insert (128, no overlap), whose torch form is
+ * _compress_v4_state_windows_capturable then _write_fp8_ds_mla_cache_rows_capturable
+ * (_fp8_ds_mla_cache_rows):
+ *   emission: token t writes when its state slot and kv_slot_mapping[t] are >= 0
+ *     and (pos + 1) % ratio == 0;
+ *   window: the window = (overlap ? 2 : 1) * ratio positions pos - window + 1 + j;
+ *     position p is present when p >= 0, its logical page floor(p / bs) - base[r]
+ *     lies in [0, width) and the table entry is >= 0; its state row is
+ *     state[entry * bs + p % bs];
+ *   head_dim values per row: the kv slice and the score slice at column offset
+ *     head_dim for j >= ratio under overlap (the newer positions take the second
+ *     slice), else 0;
+ *   pooling per column d: scores of absent positions are -1e30 and their kv 0;
+ *     m = max_j s_j; e_j = exp(s_j - m); sum = e_0 + e_1 + ... (ascending j);
+ *     w_j = e_j / sum; c_d = kv_0 w_0 + kv_1 w_1 + ... (ascending j; each product
+ *     and sum rounded) -- the order is a reading (none is printed); exp is
+ *     oracle_exp_cw;
+ *   RMSNorm as indexer_k_norm_rope_store's (pairwise sum of squares / head_dim,
+ *     IEEE sqrt then division, (c * r) * weight);
+ *   record: the fp8_ds_mla insert of the bf16 row [bf16(normed) on the nope dims |
+ *     bf16(GPT-J RoPE of the binary32 normed tail at floor(pos / ratio) * ratio)],
+ *     i.e. oracle_quantize_and_insert_k_cache's UE8M0 rule (as
+ *     _fp8_ds_mla_cache_rows quantises normed.to(bf16)).
+ * Slots beyond a cache and RoPE rows outside [0, max_pos) are skipped and counted.
+ */
+int64_t oracle_compress_kv_cache_insert(
+    const float* state_cache, int64_t state_num_pages, int32_t state_block_size,
+    int32_t state_width, const int32_t* token_to_req, const int64_t* positions,
+    const int64_t* state_slot_mapping, const int32_t* block_table, int64_t bt_stride,
+    int32_t bt_width, const int32_t* base_offsets, int32_t num_reqs, int64_t num_tokens,
+    int32_t compress_ratio, int32_t overlap, int32_t head_dim, int32_t rope_dim,
+    const float* rms_norm_weight, float rms_norm_eps, const float* cos_sin_cache,
+    int64_t cs_stride, int64_t max_pos, uint8_t* kv_cache, int64_t kv_num_pages,
+    int64_t kv_page_stride, int32_t kv_block_size, const int64_t* kv_slot_mapping) {
+    const int32_t window = (overlap ? 2 : 1) * compress_ratio;
+    const int64_t state_cap = state_num_pages * (int64_t)state_block_size;
+    const int64_t kv_cap = kv_num_pages * (int64_t)kv_block_size;
+    const int32_t nope = head_dim - rope_dim;
+    int64_t errors = 0;
+    float c[1024], sq[1024], y[1024];
+    int64_t rowidx[256];
+    uint16_t bf[1024];
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        if (state_slot_mapping[t] < 0 || kv_slot_mapping[t] < 0) continue;
+        const int64_t pos = positions[t];
+        int64_t m = (pos + 1) % compress_ratio;
+        if (m < 0) m += compress_ratio;
+        if (m != 0) continue;
+        int64_t q = pos / compress_ratio;
+        if (pos % compress_ratio != 0 && pos < 0) q -= 1;
+        const int64_t prow = q * compress_ratio;
+        const int32_t r = token_to_req[t];
+        if (kv_slot_mapping[t] >= kv_cap || prow < 0 || prow >= max_pos || r < 0 ||
+            r >= num_reqs) {
+            ++errors;
+            continue;
+        }
+        /* the window's state rows (-1: absent) */
+        const int64_t base = base_offsets ? base_offsets[r] : 0;
+        for (int32_t j = 0; j < window; ++j) {
+            const int64_t p = pos - window + 1 + j;
+            rowidx[j] = -1;
+            if (p < 0) continue;
+            const int64_t lp = p / state_block_size - base;
+            if (lp < 0 || lp >= bt_width) continue;
+            const int32_t entry = block_table[(int64_t)r * bt_stride + lp];
+            if (entry < 0) continue;
+            const int64_t srow = (int64_t)entry * state_block_size + p % state_block_size;
+            if (srow >= state_cap) continue;
+            rowidx[j] = srow;
+        }
+        /* softmax pooling per column */
+        for (int32_t d = 0; d < head_dim; ++d) {
+            float s[256], kvv[256];
+            for (int32_t j = 0; j < window; ++j) {
+                const int32_t off = (overlap && j >= compress_ratio) ? head_dim : 0;
+                if (rowidx[j] < 0) {
+                    s[j] = -1.0e30f;
+                    kvv[j] = 0.0f;
+                } else {
+                    const float* row = state_cache + rowidx[j] * 2 * (int64_t)state_width;
+                    kvv[j] = row[off + d];
+                    s[j] = row[state_width + off + d];
+                }
+            }
+            float mx = s[0];
+            for (int32_t j = 1; j < window; ++j)
+                if (s[j] > mx) mx = s[j];
+            float sum = 0.0f;
+            for (int32_t j = 0; j < window; ++j) sum = sum + oracle_exp_cw(s[j] - mx);
+            float acc = 0.0f;
+            for (int32_t j = 0; j < window; ++j) {
+                const float w = oracle_exp_cw(s[j] - mx) / sum;
+                acc = acc + kvv[j] * w;
+            }
+            c[d] = acc;
+        }
+        /* RMSNorm */
+        for (int32_t d = 0; d < head_dim; ++d) sq[d] = c[d] * c[d];
+        const float variance = pairwise_sum(sq, head_dim) / (float)head_dim;
+        const float rr = 1.0f / sqrtf(variance + rms_norm_eps);
+        for (int32_t d = 0; d < head_dim; ++d) y[d] = (c[d] * rr) * rms_norm_weight[d];
+        /* bf16 row: the nope dims rounded as they are, the tail after GPT-J RoPE */
+        for (int32_t d = 0; d < nope; ++d) bf[d] = oracle_bf16_from_f32(y[d]);
+        const float* cs = cos_sin_cache + prow * cs_stride;
+        for (int32_t i = 0; i < rope_dim / 2; ++i) {
+            const float e = y[nope + 2 * i], o = y[nope + 2 * i + 1];
+            const float cc = cs[i], sn = cs[rope_dim / 2 + i];
+            const float ec = e * cc, os = o * sn, es = e * sn, oc = o * cc;
+            bf[nope + 2 * i] = oracle_bf16_from_f32(ec - os);
+            bf[nope + 2 * i + 1] = oracle_bf16_from_f32(es + oc);
+        }
+        errors += oracle_quantize_and_insert_k_cache(bf, head_dim, kv_slot_mapping + t, 1,
+                                                     kv_cache, kv_num_pages, kv_page_stride,
+                                                     kv_block_size, head_dim, rope_dim, 1);
+    }
+    return errors;
+}
+
+void oracle_exp_cw_array(const float* x, float* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_exp_cw(x[i]);
+}

@@ -148,6 +148,26 @@ int64_t oracle_indexer_k_norm_rope_store(
     int32_t record, uint8_t* cache, int64_t num_pages, int64_t page_stride,
     int32_t block_size);
 
+/* ---- compressed-KV producer ---- */
+float oracle_exp_cw(float x);
+void oracle_exp_cw_array(const float* x, float* out, int64_t n);
+
+int64_t oracle_save_compressor_state(
+    const float* kv, const float* score, int64_t in_stride, const float* ape,
+    int32_t state_width, const int64_t* slot_mapping, const int64_t* positions,
+    int64_t num_tokens, int32_t compress_ratio, float* state_cache, int64_t num_pages,
+    int32_t block_size);
+
+int64_t oracle_compress_kv_cache_insert(
+    const float* state_cache, int64_t state_num_pages, int32_t state_block_size,
+    int32_t state_width, const int32_t* token_to_req, const int64_t* positions,
+    const int64_t* state_slot_mapping, const int32_t* block_table, int64_t bt_stride,
+    int32_t bt_width, const int32_t* base_offsets, int32_t num_reqs, int64_t num_tokens,
+    int32_t compress_ratio, int32_t overlap, int32_t head_dim, int32_t rope_dim,
+    const float* rms_norm_weight, float rms_norm_eps, const float* cos_sin_cache,
+    int64_t cs_stride, int64_t max_pos, uint8_t* kv_cache, int64_t kv_num_pages,
+    int64_t kv_page_stride, int32_t kv_block_size, const int64_t* kv_slot_mapping);
+
 #ifdef __cplusplus
 }
 #endif
