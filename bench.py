@@ -142,6 +142,33 @@ def indexer_algorithmic_bytes(p, variant: str, outputs) -> dict:
     return res
 
 
+def compressor_algorithmic_bytes(p) -> dict:
+    """Compulsory bytes of the compressor step: per layer the state write (kv
+    and score read, the state row written, plus slot and position), and the
+    compressed insert (every distinct window position's state slices once,
+    the record written, per-token metadata)."""
+    w = p.w
+    res = {}
+    for c in p.comp_layers:
+        h = c["host"]
+        r, sw, ov = h["ratio"], h["state_width"], h["overlap"]
+        T = w.num_tokens
+        nv = int((h["state_slots"] >= 0).sum())
+        res[f"save_compressor_state[{r}]"] = nv * (2 * sw * 4 * 2) + T * 16 + r * sw * 4
+        pos, t2r = h["positions"], w.token_to_req
+        emit = (h["state_slots"] >= 0) & (h["kv_slots"] >= 0) & ((pos + 1) % r == 0)
+        window = (2 if ov else 1) * r
+        seen = set()
+        for t in np.nonzero(emit)[0]:
+            for q in range(int(pos[t]) - window + 1, int(pos[t]) + 1):
+                if q >= 0:
+                    seen.add((int(t2r[t]), q))
+        # each present position's kv and score slices: all of a 2*sw row
+        res[f"compress_kv_cache_insert[{r}]"] = (len(seen) * 2 * sw * 4 + int(emit.sum()) * 584 +
+                                                 T * 24)
+    return res
+
+
 def workspace_algorithmic_bytes(p) -> dict:
     """Compulsory bytes of the prefill workspace step's launches."""
     from paged_sparse_kv_gb300.pipeline import workspace_geometry
@@ -262,12 +289,14 @@ def _graph_events_supported(torch) -> bool:
 # CUDA sources of each timed entry point: its kernel file and that family's
 # header (plus the shared headers).
 _FAMILY = {"insert": ("insert.cu", "insert.h"), "index": ("index_build.cu", "index_build.h"),
-           "gather": ("gather.cu", "gather.h")}
+           "gather": ("gather.cu", "gather.h"), "compressor": ("compressor.cu", "compressor.h")}
 KERNEL_SOURCES = {
     "quantize_and_insert_k_cache": _FAMILY["insert"],
     "write_indexer_mxfp4_cache": _FAMILY["insert"],
     "write_indexer_fp8_cache": _FAMILY["insert"],
     "indexer_k_norm_rope_store": _FAMILY["insert"],
+    "save_compressor_state": _FAMILY["compressor"],
+    "compress_kv_cache_insert": _FAMILY["compressor"],
     "combine_topk_swa_indices": _FAMILY["index"],
     "compute_global_topk_indices_and_lens": _FAMILY["index"],
     "combine_topk_swa_workspace_indices": _FAMILY["index"],
@@ -361,13 +390,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--path", default="index",
-                    choices=["index", "workspace", "dense", "indexer_fp8", "indexer_store"],
+                    choices=["index", "workspace", "dense", "indexer_fp8", "indexer_store",
+                             "compressor"],
                     help="index: the index-keyed gather into [T, W+P, D]; workspace: the "
                          "prefill workspace path (range gathers + workspace indices); dense: "
                          "the no-top-k decode step of a heavily compressed layer (the "
                          "decode_hca workload always takes it); indexer_fp8 / indexer_store: "
                          "the mxfp4 workload's step with the FP8 indexer record or the fused "
-                         "norm-RoPE store as the key writer")
+                         "norm-RoPE store as the key writer; compressor: the compressed-KV "
+                         "producer (ratio 4 and 128 layers) of a prefill batch")
     ap.add_argument("--eager", action="store_true",
                     help="launch the step eagerly instead of replaying a CUDA graph")
     args = ap.parse_args()
@@ -404,8 +435,12 @@ def main():
         raise SystemExit("the dense path needs a workload with dense compressed entries")
     if path.startswith("indexer_") and (w.index_k is None or w.index_head_dim != 128):
         raise SystemExit("the indexer paths need 128-dim indexer keys")
+    if path == "compressor" and not w.has_fp8:
+        raise SystemExit("the compressor path needs a workload with an FP8 part")
     if path.startswith("indexer_"):
         launches = p.indexer_launches(path.split("_")[1])
+    elif path == "compressor":
+        launches = p.compressor_launches()
     else:
         launches = {"workspace": p.workspace_launches, "dense": p.dense_launches,
                     "index": p.launches}[path]()
@@ -426,6 +461,8 @@ def main():
     elif path.startswith("indexer_"):
         alg = indexer_algorithmic_bytes(p, path.split("_")[1],
                                         {"global_topk": p.global_topk.cpu().numpy()})
+    elif path == "compressor":
+        alg = compressor_algorithmic_bytes(p)
     else:
         outputs = {"global_topk": p.global_topk.cpu().numpy()}
         if w.has_fp8:
@@ -608,6 +645,10 @@ def run_e2e(p, args, dev, flush, path="index"):
         ins = [t for t in (p.k, p.insert_slots, p.qsl, p.seq_lens, p.t2r, p.positions)
                if t is not None]
         outs = [p.swa_indices, p.swa_lens, p.dense_indices, p.dense_lens, p.dense_gathered]
+    elif path == "compressor":
+        ins = [t for c in p.comp_layers for t in (c["kv"], c["score"], c["positions"],
+                                                  c["state_slots"], c["kv_slots"])]
+        outs = [c["kv_cache"] for c in p.comp_layers]
     elif path.startswith("indexer_"):
         ins = [p.index_k, p.index_insert_slots, p.topk, p.t2r]
         if path == "indexer_store":
@@ -638,7 +679,17 @@ def run_e2e(p, args, dev, flush, path="index"):
 
 def _oracle_step(w, path: str, caches):
     """(one oracle step as a callable, tokens it covers, description) for a path."""
-    from oracle.pipeline import run_dense_step, run_indexer_step, run_step, run_workspace_step
+    from oracle.pipeline import (run_compressor_step, run_dense_step, run_indexer_step,
+                                 run_step, run_workspace_step)
+    if path == "compressor":
+        from paged_sparse_kv_gb300 import synthetic
+        layers = [synthetic.compressor_inputs(w, r, 777 + i) for i, r in enumerate((4, 128))]
+        states = [np.zeros((c["state_pages"], c["state_bs"], 2 * c["state_width"]), np.float32)
+                  for c in layers]
+        kvc = [np.zeros((c["kv_geom"].num_pages, c["kv_geom"].page_stride), np.uint8)
+               for c in layers]
+        return (lambda: run_compressor_step(w, layers, states, kvc), w.num_tokens,
+                f"oracle step of the {w.name} batch (compressor path) per timed step")
     if path.startswith("indexer_"):
         from paged_sparse_kv_gb300 import synthetic
         from paged_sparse_kv_gb300.pipeline import Pipeline

@@ -481,6 +481,70 @@ psk_status indexer_k_norm_rope_store(
     psk_record record, uint8_t* k_cache, int64_t num_pages, int64_t page_stride,
     int32_t block_size, int32_t* err_count, psk_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Compressed-KV producer (TokenSpeed deepseek_v4_ops.py)                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * save_compressor_state -- the compressor's residual state of each token.
+ * TokenSpeed save_deepseek_v4_compressor_state: "[kv_state, score_state], each
+ * with width coff * head_dim; score state includes the APE row selected by
+ * position % compress_ratio".  The kernel is not printed: read as
+ * state[slot] = [kv[t], score[t] + ape[pos % ratio]] (binary32 adds).
+ *
+ *   kv, score    binary32 [num_tokens, in_stride] (16-byte aligned, in_stride a
+ *                multiple of 4 >= state_width).
+ *   ape          binary32 [compress_ratio, state_width].
+ *   state_cache  binary32 [num_pages, block_size, 2 * state_width] (16-byte
+ *                aligned); row = slot.
+ *   Slots < 0 are skipped; slots >= num_pages * block_size are skipped and
+ *   counted in *err_count (optional).
+ */
+psk_status save_compressor_state(
+    const float* kv, const float* score, int64_t in_stride, const float* ape,
+    int32_t state_width, const int64_t* slot_mapping, const int64_t* positions,
+    int64_t num_tokens, int32_t compress_ratio, float* state_cache, int64_t num_pages,
+    int32_t block_size, int32_t* err_count, psk_stream_t stream);
+
+/*
+ * compress_kv_cache_insert -- the compressed KV row of every token that closes
+ * a compress group, window-pooled from the compressor state, normalised,
+ * rotated and inserted as an fp8_ds_mla record (512 dims = 448 + 64 RoPE).
+ * TokenSpeed deepseek_v4_csa_compress_kv_cache_insert (compress_ratio 4,
+ * overlap 1) and deepseek_v4_hca_compress_kv_cache_insert (128, overlap 0),
+ * whose torch form is _compress_v4_state_windows_capturable followed by
+ * _write_fp8_ds_mla_cache_rows_capturable.
+ *
+ *   Token t writes when state_slot_mapping[t] and kv_slot_mapping[t] are >= 0
+ *   and (pos + 1) % ratio == 0.  Its window is the W = (overlap ? 2 : 1) *
+ *   ratio positions pos - W + 1 + j (W <= 256); position p is present when
+ *   p >= 0 and block_table[r][p / state_block_size - base_offsets[r]] (index in
+ *   [0, bt_width)) is >= 0; its state row is entry * state_block_size + p %
+ *   state_block_size.  Column d of window row j: kv = row[off + d], score =
+ *   row[state_width + off + d], off = 512 for j >= ratio under overlap (the
+ *   newer positions take the second slice), else 0; absent rows score -1e30
+ *   with kv 0.  Per column: m = max_j score; e_j = exp(score_j - m); sum =
+ *   e_0 + e_1 + ...; c_d = kv_0 (e_0 / sum) + kv_1 (e_1 / sum) + ... (window
+ *   order; binary32, no contraction; exp by Cody-Waite reduction and the Taylor
+ *   series to r^7/7!, the oracle's sequence).  Then RMSNorm as
+ *   indexer_k_norm_rope_store's (pairwise sum of squares / 512, IEEE sqrt then
+ *   reciprocal, (c * r) * weight), GPT-J RoPE of dims 448..511 at
+ *   floor(pos / ratio) * ratio, and the fp8_ds_mla record of the bf16 row
+ *   (quantize_and_insert_k_cache's UE8M0 rule) at kv_slot_mapping[t].
+ *   Slots beyond the kv cache, RoPE rows outside [0, max_pos) and request
+ *   indices outside [0, num_reqs) are skipped and counted in *err_count.
+ */
+psk_status compress_kv_cache_insert(
+    const float* state_cache, int64_t state_num_pages, int32_t state_block_size,
+    int32_t state_width, const int32_t* token_to_req, const int64_t* positions,
+    const int64_t* state_slot_mapping, const int32_t* block_table, int64_t bt_stride,
+    int32_t bt_width, const int32_t* base_offsets, int32_t num_reqs, int64_t num_tokens,
+    int32_t compress_ratio, int32_t overlap, const float* rms_norm_weight,
+    float rms_norm_eps, const float* cos_sin_cache, int64_t cs_stride, int64_t max_pos,
+    uint8_t* kv_cache, int64_t kv_num_pages, int64_t kv_page_stride,
+    int32_t kv_block_size, const int64_t* kv_slot_mapping, int32_t* err_count,
+    psk_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,7 +16,8 @@ from . import (REC_FP8_DS_MLA, REC_MXFP4, combine_topk_swa_indices,
                combine_topk_swa_workspace_indices, compute_dense_compressed_indices_and_lens,
                compute_global_topk_indices_and_lens, decode_swa_indices_and_lens,
                dequantize_and_gather_k_cache, dequantize_and_gather_k_cache_ranges,
-               indexer_k_norm_rope_store, indexer_mxfp4_paged_gather,
+               compress_kv_cache_insert, indexer_k_norm_rope_store, indexer_mxfp4_paged_gather,
+               save_compressor_state,
                quantize_and_insert_k_cache, write_indexer_fp8_cache, write_indexer_mxfp4_cache)
 
 REC_FP8_INDEXER = 2
@@ -135,4 +136,19 @@ def run_indexer_step(w, variant: str, cache, inputs: dict, sample_tokens=None) -
     rows = gt if toks is None else gt[toks]
     res["gathered_index"] = dequantize_and_gather_k_cache(cache, bs, rec, w.index_head_dim, 0,
                                                           np.ascontiguousarray(rows))
+    return res
+
+
+def run_compressor_step(w, layers, states, kv_caches, eps: float = 1e-6) -> dict:
+    """The compressor step: for each layer (compressor_inputs of a ratio), save
+    the state of every token, then insert the compressed rows of the tokens
+    that close a group.  ``states`` and ``kv_caches`` are updated in place."""
+    res: dict = {"err": 0}
+    for c, st, kvc in zip(layers, states, kv_caches):
+        res["err"] += save_compressor_state(c["kv"], c["score"], c["ape"], c["state_slots"],
+                                            c["positions"], c["ratio"], st, c["state_bs"])
+        res["err"] += compress_kv_cache_insert(
+            st, w.token_to_req, c["positions"], c["state_slots"], c["state_table"], c["state_bs"],
+            c["weight"], eps, c["cos_sin"], kvc, c["kv_slots"], c["kv_geom"].block_size,
+            c["ratio"], c["overlap"])
     return res

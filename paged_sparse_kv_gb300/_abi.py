@@ -65,6 +65,11 @@ SIGNATURES = {
         _I32, [_P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64, _P, _I64, _P, _P]),
     "write_indexer_fp8_cache": (
         _I32, [_P, _I64, _P, _I64, _P, _I64, _I64, _I32, _I32, _P, _P]),
+    "save_compressor_state": (
+        _I32, [_P, _P, _I64, _P, _I32, _P, _P, _I64, _I32, _P, _I64, _I32, _P, _P]),
+    "compress_kv_cache_insert": (
+        _I32, [_P, _I64, _I32, _I32, _P, _P, _P, _P, _I64, _I32, _P, _I32, _I64, _I32, _I32, _P,
+               ctypes.c_float, _P, _I64, _I64, _P, _I64, _I64, _I32, _P, _P, _P]),
     "indexer_k_norm_rope_store": (
         _I32, [_P, _I64, _P, _P, _I64, _I64, _P, ctypes.c_float, _P, _I64, _I32, _I32, _P, _I64,
                _I64, _I32, _P, _P]),

@@ -10,6 +10,7 @@
 #include <cstring>
 #include <string>
 
+#include "compressor.h"
 #include "gather.h"
 #include "index_build.h"
 #include "insert.h"
@@ -591,6 +592,82 @@ psk_status indexer_k_norm_rope_store(const void* k_pre, int64_t k_row_stride,
                           num_pages, page_stride, block_size, err_count};
     return cuda_status(psk::launch_norm_rope_store(p, reinterpret_cast<cudaStream_t>(stream)),
                        "indexer_k_norm_rope_store launch");
+}
+
+psk_status save_compressor_state(const float* kv, const float* score, int64_t in_stride,
+                                 const float* ape, int32_t state_width,
+                                 const int64_t* slot_mapping, const int64_t* positions,
+                                 int64_t num_tokens, int32_t compress_ratio, float* state_cache,
+                                 int64_t num_pages, int32_t block_size, int32_t* err_count,
+                                 psk_stream_t stream) {
+    CHECK(num_tokens >= 0, "num_tokens must be >= 0");
+    CHECK(state_width > 0 && state_width % 4 == 0, "state_width must be a positive multiple of 4");
+    CHECK(compress_ratio >= 1, "compress_ratio must be >= 1");
+    CHECK(num_pages >= 1 && block_size >= 1, "num_pages and block_size must be >= 1");
+    CHECK(state_cache != nullptr && aligned(state_cache, 16), "state_cache must be 16-byte aligned");
+    if (num_tokens == 0) return ok();
+    CHECK(kv && score && ape && slot_mapping && positions,
+          "kv, score, ape, slot_mapping and positions must be non-null");
+    CHECK(in_stride >= state_width && in_stride % 4 == 0,
+          "in_stride must be >= state_width and a multiple of 4");
+    CHECK(aligned(kv, 16) && aligned(score, 16) && aligned(ape, 16),
+          "kv, score and ape must be 16-byte aligned");
+    CHECK(aligned(slot_mapping, 8) && aligned(positions, 8),
+          "slot_mapping and positions must be 8-byte aligned");
+    CHECK(err_count == nullptr || aligned(err_count, 4), "err_count must be 4-byte aligned");
+    CHECK(num_tokens <= INT64_MAX / 32, "num_tokens is too large");
+    psk::SaveStateParams p{kv, score, in_stride, ape, state_width, slot_mapping, positions,
+                           num_tokens, compress_ratio, state_cache, num_pages, block_size,
+                           err_count};
+    return cuda_status(psk::launch_save_compressor_state(p, reinterpret_cast<cudaStream_t>(stream)),
+                       "save_compressor_state launch");
+}
+
+psk_status compress_kv_cache_insert(
+    const float* state_cache, int64_t state_num_pages, int32_t state_block_size,
+    int32_t state_width, const int32_t* token_to_req, const int64_t* positions,
+    const int64_t* state_slot_mapping, const int32_t* block_table, int64_t bt_stride,
+    int32_t bt_width, const int32_t* base_offsets, int32_t num_reqs, int64_t num_tokens,
+    int32_t compress_ratio, int32_t overlap, const float* rms_norm_weight, float rms_norm_eps,
+    const float* cos_sin_cache, int64_t cs_stride, int64_t max_pos, uint8_t* kv_cache,
+    int64_t kv_num_pages, int64_t kv_page_stride, int32_t kv_block_size,
+    const int64_t* kv_slot_mapping, int32_t* err_count, psk_stream_t stream) {
+    CHECK(num_tokens >= 0, "num_tokens must be >= 0");
+    CHECK(overlap == 0 || overlap == 1, "overlap must be 0 or 1");
+    CHECK(compress_ratio >= 1 && (overlap ? 2 : 1) * (int64_t)compress_ratio <= 256,
+          "the window ((overlap ? 2 : 1) * compress_ratio) must be in [1, 256]");
+    CHECK(state_width == (overlap ? 2 : 1) * 512,
+          "state_width must be 512 (1024 with overlap) for 512-dim keys");
+    CHECK(state_num_pages >= 1 && state_block_size >= 1, "state pages and block size must be >= 1");
+    CHECK(bt_width >= 0 && bt_stride >= bt_width, "need 0 <= bt_width <= bt_stride");
+    CHECK(max_pos >= 0 && cs_stride >= 64, "need max_pos >= 0 and cs_stride >= 64");
+    psk_status st = check_cache(kv_cache, kv_num_pages, kv_page_stride, kv_block_size,
+                                fp8_record_bytes(512, 64, 1));
+    if (st != PSK_OK) return st;
+    if (num_tokens == 0) return ok();
+    CHECK(num_reqs >= 1, "num_reqs must be >= 1");
+    CHECK(state_cache && token_to_req && positions && state_slot_mapping && rms_norm_weight &&
+              cos_sin_cache && kv_slot_mapping,
+          "state_cache, token_to_req, positions, state_slot_mapping, rms_norm_weight, "
+          "cos_sin_cache and kv_slot_mapping must be non-null");
+    CHECK(bt_width == 0 || block_table, "block_table must be non-null");
+    CHECK(aligned(state_cache, 16) && aligned(rms_norm_weight, 16),
+          "state_cache and rms_norm_weight must be 16-byte aligned");
+    CHECK(aligned(positions, 8) && aligned(state_slot_mapping, 8) && aligned(kv_slot_mapping, 8),
+          "positions and slot mappings must be 8-byte aligned");
+    CHECK(aligned(token_to_req, 4) && aligned(block_table, 4) && aligned(base_offsets, 4) &&
+              aligned(cos_sin_cache, 4),
+          "int32 arrays and cos_sin_cache must be 4-byte aligned");
+    CHECK(err_count == nullptr || aligned(err_count, 4), "err_count must be 4-byte aligned");
+    CHECK(num_tokens <= 0x7FFFFFFFll, "num_tokens must fit a grid");
+    psk::CompressParams p{state_cache, state_num_pages, state_block_size, state_width,
+                          token_to_req, positions, state_slot_mapping, block_table, bt_stride,
+                          bt_width, base_offsets, num_reqs, num_tokens, compress_ratio, overlap,
+                          rms_norm_weight, rms_norm_eps, cos_sin_cache, cs_stride, max_pos,
+                          kv_cache, kv_num_pages, kv_page_stride, kv_block_size, kv_slot_mapping,
+                          err_count};
+    return cuda_status(psk::launch_compress_kv_insert(p, reinterpret_cast<cudaStream_t>(stream)),
+                       "compress_kv_cache_insert launch");
 }
 
 }  // extern "C"

@@ -378,3 +378,63 @@ def indexer_k_norm_rope_store(k_pre: torch.Tensor, positions: torch.Tensor,
               _ptr(rms_norm_weight.contiguous()), float(rms_norm_eps), _ptr(kv_slot_mapping),
               kv_slot_mapping.shape[0], compress_ratio, record, _ptr(k_cache), num_pages,
               page_stride, block_size, _ptr(err_count), _stream(k_pre.device))
+
+
+# ---- compressed-KV producer -------------------------------------------------------------
+
+def save_compressor_state(kv: torch.Tensor, score: torch.Tensor, ape: torch.Tensor,
+                          state_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                          positions: torch.Tensor, block_size: int, compress_ratio: int, *,
+                          err_count: Optional[torch.Tensor] = None) -> None:
+    """state[slot] = [kv, score + ape[pos % ratio]] into the binary32 state cache
+    [pages, block_size, 2 * state_width]."""
+    _need_cuda(kv, score, ape, state_cache, slot_mapping, positions, err_count)
+    for t, n in ((kv, "kv"), (score, "score"), (ape, "ape"), (state_cache, "state_cache")):
+        _need(t, torch.float32, n)
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _need(positions, torch.int64, "positions")
+    if kv.stride() != score.stride():
+        raise ValueError("kv and score must share a layout")
+    sw = kv.shape[1]
+    if state_cache.dim() != 3 or state_cache.shape[1] != block_size or \
+            state_cache.shape[2] != 2 * sw or not state_cache.is_contiguous():
+        raise ValueError("state_cache must be contiguous [pages, block_size, 2 * state_width]")
+    _abi.call("save_compressor_state", _ptr(kv), _ptr(score), _rows(kv, "kv"),
+              _ptr(ape.contiguous()), sw, _ptr(slot_mapping), _ptr(positions),
+              slot_mapping.shape[0], compress_ratio, _ptr(state_cache), state_cache.shape[0],
+              block_size, _ptr(err_count), _stream(kv.device))
+
+
+def compress_kv_cache_insert(state_cache: torch.Tensor, token_to_req_indices: torch.Tensor,
+                             positions: torch.Tensor, compressor_slot_mapping: torch.Tensor,
+                             block_table: torch.Tensor, compressor_block_size: int,
+                             rms_norm_weight: torch.Tensor, rms_norm_eps: float,
+                             cos_sin_cache: torch.Tensor, kv_cache_2d: torch.Tensor,
+                             kv_slot_mapping: torch.Tensor, kv_cache_block_size: int,
+                             compress_ratio: int, *, overlap: Optional[bool] = None,
+                             block_table_base_offsets: Optional[torch.Tensor] = None,
+                             err_count: Optional[torch.Tensor] = None) -> None:
+    """Window-pooled, normalised, rotated fp8_ds_mla rows of the compressed KV
+    cache (ratio 4 with overlap = the CSA insert, ratio 128 = the HCA insert)."""
+    _need_cuda(state_cache, token_to_req_indices, positions, compressor_slot_mapping,
+               block_table, rms_norm_weight, cos_sin_cache, kv_cache_2d, kv_slot_mapping,
+               block_table_base_offsets, err_count)
+    _need(state_cache, torch.float32, "state_cache")
+    _need(positions, torch.int64, "positions")
+    _need(rms_norm_weight, torch.float32, "rms_norm_weight")
+    _need(cos_sin_cache, torch.float32, "cos_sin_cache")
+    if overlap is None:
+        overlap = compress_ratio == 4
+    if state_cache.dim() != 3 or not state_cache.is_contiguous():
+        raise ValueError("state_cache must be contiguous [pages, block_size, 2 * state_width]")
+    num_pages, page_stride = _pages(kv_cache_2d)
+    _abi.call("compress_kv_cache_insert", _ptr(state_cache), state_cache.shape[0],
+              compressor_block_size, state_cache.shape[2] // 2, _ptr(token_to_req_indices),
+              _ptr(positions), _ptr(compressor_slot_mapping), _ptr(block_table),
+              _rows(block_table, "block_table"), block_table.shape[1],
+              _ptr(block_table_base_offsets), block_table.shape[0], positions.shape[0],
+              compress_ratio, int(bool(overlap)), _ptr(rms_norm_weight.contiguous()),
+              float(rms_norm_eps), _ptr(cos_sin_cache), _rows(cos_sin_cache, "cos_sin_cache"),
+              cos_sin_cache.shape[0], _ptr(kv_cache_2d), num_pages, page_stride,
+              kv_cache_block_size, _ptr(kv_slot_mapping), _ptr(err_count),
+              _stream(state_cache.device))

@@ -49,6 +49,12 @@ a 131072-row GPT-J table):
   stream B:  compute_global_topk_indices_and_lens
   join:      gather of the top-k keys
 
+``path="compressor"`` is the compressed-KV producer of a prefill batch for a
+ratio-4 (overlapping window) and a ratio-128 layer, one per stream:
+
+  stream A:  save_compressor_state[4] -> compress_kv_cache_insert[4]
+  stream B:  save_compressor_state[128] -> compress_kv_cache_insert[128]
+
 ``path="dense"`` is the decode step of a heavily compressed attention layer
 (no top-k; TokenSpeed's decode SWA precompute and
 ``_decode_compressed_attention_indices_and_lens`` for a ratio other than 4):
@@ -221,6 +227,51 @@ class Pipeline:
                  w.comp_cache.block_size, rope_dim=w.rope_dim)),
         ]
 
+    COMPRESSOR_EPS = 1e-6
+
+    def alloc_compressor(self, seed: int = 777) -> None:
+        """Inputs and caches of the compressor step (ratio 4 and 128 layers)."""
+        from . import synthetic
+        w, dev = self.w, self.dev
+        self.comp_layers = []
+        for i, ratio in enumerate((4, 128)):
+            c = synthetic.compressor_inputs(w, ratio, seed + i)
+            g = c["kv_geom"]
+            d = {"host": c, "ratio": ratio, "overlap": c["overlap"],
+                 "kv": torch.from_numpy(c["kv"]).to(dev),
+                 "score": torch.from_numpy(c["score"]).to(dev),
+                 "ape": torch.from_numpy(c["ape"]).to(dev),
+                 "positions": _dev_i64(c["positions"], dev),
+                 "state_slots": _dev_i64(c["state_slots"], dev),
+                 "state_table": _dev_i32(c["state_table"], dev),
+                 "state": torch.zeros((c["state_pages"], c["state_bs"], 2 * c["state_width"]),
+                                      dtype=torch.float32, device=dev),
+                 "kv_slots": _dev_i64(c["kv_slots"], dev),
+                 "kv_cache": (self.comp_cache if ratio == 4 else
+                              torch.zeros((g.num_pages, g.page_stride), dtype=torch.uint8,
+                                          device=dev)),
+                 "weight": torch.from_numpy(c["weight"]).to(dev),
+                 "cos_sin": torch.from_numpy(c["cos_sin"]).to(dev)}
+            self.comp_layers.append(d)
+
+    def compressor_launches(self) -> list[tuple[str, Callable[[], None]]]:
+        """The compressor step as (kernel name, launch) pairs, in order."""
+        w = self.w
+        if getattr(self, "comp_layers", None) is None:
+            self.alloc_compressor()
+        L = []
+        for c in self.comp_layers:
+            r = c["ratio"]
+            L.append((f"save_compressor_state[{r}]", lambda c=c: ops.save_compressor_state(
+                c["kv"], c["score"], c["ape"], c["state"], c["state_slots"], c["positions"],
+                c["state"].shape[1], c["ratio"], err_count=self.err)))
+            L.append((f"compress_kv_cache_insert[{r}]", lambda c=c: ops.compress_kv_cache_insert(
+                c["state"], self.t2r, c["positions"], c["state_slots"], c["state_table"],
+                c["state"].shape[1], c["weight"], self.COMPRESSOR_EPS, c["cos_sin"],
+                c["kv_cache"], c["kv_slots"], 64, c["ratio"], overlap=c["overlap"],
+                err_count=self.err)))
+        return L
+
     INDEXER_MAX_POS = 131072
 
     def alloc_indexer(self) -> None:
@@ -340,6 +391,8 @@ class Pipeline:
             return self._dense_step(concurrent, hooks or {})
         if path in ("indexer_fp8", "indexer_store"):
             return self._indexer_step(concurrent, hooks or {}, path.split("_")[1])
+        if path == "compressor":
+            return self._compressor_step(concurrent, hooks or {})
         L = dict(self.launches())
         hooks = hooks or {}
 
@@ -460,6 +513,38 @@ class Pipeline:
         main.wait_event(done_a)
         main.wait_event(done_b)
         run(names[2])
+
+    def _compressor_step(self, concurrent: bool, hooks: dict) -> None:
+        L = self.compressor_launches()
+        fns = dict(L)
+
+        def run(name):
+            pre, post = hooks.get(name, (None, None))
+            if pre:
+                pre()
+            fns[name]()
+            if post:
+                post()
+
+        if not concurrent:
+            for name, _ in L:
+                run(name)
+            return
+        main = torch.cuda.current_stream(self.dev)
+        if not hasattr(self, "_side"):
+            self._side = (torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev))
+        sa, _ = self._side
+        fork = torch.cuda.Event()
+        fork.record(main)
+        sa.wait_event(fork)
+        with torch.cuda.stream(sa):
+            run("save_compressor_state[128]")
+            run("compress_kv_cache_insert[128]")
+            done = torch.cuda.Event()
+            done.record(sa)
+        run("save_compressor_state[4]")
+        run("compress_kv_cache_insert[4]")
+        main.wait_event(done)
 
     def _dense_step(self, concurrent: bool, hooks: dict) -> None:
         L = dict(self.dense_launches())

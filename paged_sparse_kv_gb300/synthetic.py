@@ -409,6 +409,49 @@ def norm_weight(seed: int, dim: int = 128) -> np.ndarray:
     return np.random.default_rng(seed).uniform(0.5, 2.0, size=dim).astype(np.float32)
 
 
+def compressor_inputs(w: Workload, ratio: int, seed: int) -> dict:
+    """Inputs of one compressor layer for a batch (compress ratio 4 with the
+    overlapping window -- state width 1024 -- or 128 without -- 512): the
+    binary32 kv and score projections N(0,1) and N(0,3), the APE rows
+    N(0, 0.5) and the norm weight.  The state cache is paged by position like
+    the SWA cache, so its table and each token's state slot are the SWA ones;
+    ratio 4 writes its rows at the compressed-entry slots the indexer keys use
+    (floor(pos / 4) through the compressed table), ratio 128 at slots of its
+    own small cache (entry floor(pos / 128), one page per 64 entries)."""
+    overlap = ratio == 4
+    sw = (2 if overlap else 1) * 512
+    T = w.num_tokens
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator().manual_seed(seed)
+    kv = torch.randn(T, sw, generator=gen).numpy()
+    score = (torch.randn(T, sw, generator=gen) * 3.0).numpy()
+    ape = (torch.randn(ratio, sw, generator=gen) * 0.5).numpy()
+    qlen = np.diff(w.query_start_loc).astype(np.int64)
+    pos = np.concatenate([np.arange(s - q, s) for s, q in zip(w.seq_lens.astype(np.int64), qlen)])
+    if overlap:
+        kv_slots = np.asarray(w.index_insert_slots, np.int64)
+        kv_table = w.comp_block_table if w.comp_block_table is not None else w.swa_block_table
+        kv_geom = w.comp_cache
+    else:
+        n_ent = (w.seq_lens.astype(np.int64) + ratio - 1) // ratio
+        per = int((n_ent.max() + 63) // 64)
+        pages = w.num_reqs * per
+        kv_table = rng.permutation(pages).astype(np.int32).reshape(w.num_reqs, per)
+        kv_slots = np.full(T, -1, np.int64)
+        for t in range(T):
+            if (pos[t] + 1) % ratio == 0:
+                e = pos[t] // ratio
+                r = w.token_to_req[t]
+                kv_slots[t] = int(kv_table[r, e // 64]) * 64 + e % 64
+        kv_geom = CacheGeom(pages, 64, 64 * fp8_record_bytes(512, 64))
+    return {"ratio": ratio, "overlap": overlap, "state_width": sw, "kv": kv, "score": score,
+            "ape": ape, "positions": pos.astype(np.int64), "state_slots": w.insert_slots,
+            "state_table": w.swa_block_table, "state_bs": w.swa_cache.block_size,
+            "state_pages": w.swa_cache.num_pages, "kv_slots": kv_slots, "kv_table": kv_table,
+            "kv_geom": kv_geom, "weight": norm_weight(seed, 512),
+            "cos_sin": gptj_cos_sin(int(w.seq_lens.max()))}
+
+
 def random_cache_bytes(seed: int, geom: CacheGeom) -> np.ndarray:
     """A cache filled with seeded random bytes, none of them 0x7F or 0xFF (the
     E4M3 NaN codes), so that every record decodes to finite or infinite

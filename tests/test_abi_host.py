@@ -340,3 +340,44 @@ def test_norm_rope_store_rejects_bad_arguments(psk_lib, kw):
 
 def test_norm_rope_store_zero_tokens_ok(psk_lib):
     assert _nrs(n=0, k=None, pos=None) == OK
+
+
+def _save(**kw):
+    a = dict(kv=A, sc=A + 65536, ins=1024, ape=B, sw=1024, slots=B + 65536, pos=C, n=4, ratio=4,
+             st=C + 65536, pages=4, bs=16, err=None)
+    a.update(kw)
+    return _abi.status("save_compressor_state", a["kv"], a["sc"], a["ins"], a["ape"], a["sw"],
+                       a["slots"], a["pos"], a["n"], a["ratio"], a["st"], a["pages"], a["bs"],
+                       a["err"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(sw=0), dict(sw=1022), dict(ratio=0), dict(pages=0),
+                                dict(st=None), dict(st=C + 65544), dict(kv=None), dict(ins=1020),
+                                dict(ins=1026), dict(kv=A + 4), dict(slots=B + 65540), dict(n=-1)])
+def test_save_state_rejects_bad_arguments(psk_lib, kw):
+    assert _save(**kw) == INV
+
+
+def _cmp(**kw):
+    a = dict(st=A, spages=8, sbs=16, sw=1024, t2r=B, pos=B + 4096, ss=B + 8192, bt=C, bts=4,
+             btw=4, base=None, R=2, n=4, ratio=4, ov=1, w=C + 4096, eps=1e-6, cs=C + 8192,
+             css=64, maxp=4096, kv=A + 1048576, kpages=8, kps=64 * 584, kbs=64, ks=B + 12288,
+             err=None)
+    a.update(kw)
+    return _abi.status("compress_kv_cache_insert", a["st"], a["spages"], a["sbs"], a["sw"],
+                       a["t2r"], a["pos"], a["ss"], a["bt"], a["bts"], a["btw"], a["base"],
+                       a["R"], a["n"], a["ratio"], a["ov"], a["w"], a["eps"], a["cs"], a["css"],
+                       a["maxp"], a["kv"], a["kpages"], a["kps"], a["kbs"], a["ks"], a["err"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(ov=2), dict(ratio=0), dict(ratio=129, ov=1),
+                                dict(ratio=300, ov=0, sw=512), dict(sw=512), dict(ov=0),
+                                dict(spages=0), dict(btw=5), dict(css=32), dict(maxp=-1),
+                                dict(kps=64 * 584 - 16), dict(R=0), dict(st=None), dict(st=A + 4),
+                                dict(w=C + 4100), dict(pos=B + 4100), dict(n=-1)])
+def test_compress_rejects_bad_arguments(psk_lib, kw):
+    assert _cmp(**kw) == INV
+
+
+def test_compress_zero_tokens_ok(psk_lib):
+    assert _cmp(n=0, st=None, t2r=None) == OK
