@@ -306,6 +306,8 @@ KERNEL_SOURCES = {
     "combine_dense_swa_indices": _FAMILY["index"],
     "dequantize_and_gather_k_cache": _FAMILY["gather"],
     "dequantize_and_gather_k_cache_ranges": _FAMILY["gather"],
+    "dequantize_and_gather_k_cache_topk": _FAMILY["gather"],
+    "dequantize_and_gather_k_cache_window": _FAMILY["gather"],
     "indexer_mxfp4_paged_gather": _FAMILY["gather"],
 }
 SHARED_SOURCES = ("psk_common.cuh", "launch.h")
@@ -390,8 +392,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--path", default="index",
-                    choices=["index", "workspace", "dense", "indexer_fp8", "indexer_store",
-                             "compressor"],
+                    choices=["index", "fused", "workspace", "dense", "indexer_fp8",
+                             "indexer_store", "compressor"],
                     help="index: the index-keyed gather into [T, W+P, D]; workspace: the "
                          "prefill workspace path (range gathers + workspace indices); dense: "
                          "the no-top-k decode step of a heavily compressed layer (the "
@@ -443,7 +445,7 @@ def main():
         launches = p.compressor_launches()
     else:
         launches = {"workspace": p.workspace_launches, "dense": p.dense_launches,
-                    "index": p.launches}[path]()
+                    "index": p.launches, "fused": p.fused_launches}[path]()
     names = [n for n, _ in launches]
     flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
@@ -468,6 +470,18 @@ def main():
         if w.has_fp8:
             outputs["sparse_indices"] = p.sparse_indices.cpu().numpy()
         alg = algorithmic_bytes(p, outputs)
+        if path == "fused":
+            # the fused gathers move the same rows; the top-k forms read a top-k
+            # entry per item where the index form read a slot id, the window form
+            # reads per-token metadata instead of its index columns
+            alg["dequantize_and_gather_k_cache_topk[mxfp4]"] = alg.pop(
+                "dequantize_and_gather_k_cache[mxfp4]")
+            if w.has_fp8:
+                alg["dequantize_and_gather_k_cache_topk[topk]"] = alg.pop(
+                    "dequantize_and_gather_k_cache[topk]")
+                alg["dequantize_and_gather_k_cache_window[swa]"] = (
+                    alg.pop("dequantize_and_gather_k_cache[swa]") -
+                    w.num_tokens * w.window * 4 + w.num_tokens * 16)
 
     visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x]
     clocks = ClockSampler(visible[local_rank] if local_rank < len(visible) else str(local_rank))

@@ -545,6 +545,52 @@ psk_status compress_kv_cache_insert(
     int32_t kv_block_size, const int64_t* kv_slot_mapping, int32_t* err_count,
     psk_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Fused gathers: the slots computed in the gather (no index matrix)          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * dequantize_and_gather_k_cache_topk -- the top-k columns of a token gathered
+ * straight from its local top-k indices.  Output identical to
+ * compute_global_topk_indices_and_lens (table, base offsets, padding tokens)
+ * followed by dequantize_and_gather_k_cache over that matrix, in one launch
+ * with no index matrix in between (the pages' decode path maps local top-k to
+ * global slots, [BE] _decode_compressed_attention_indices_and_lens, then the
+ * attention reads those rows; here the rows are dequantised directly).
+ *
+ *   out           bf16 rows (t, j) at out + t*out_stride_t + j*out_stride_j,
+ *                 j < topk (elements, multiples of 8).
+ *   topk_local    int32 [num_tokens, topk_stride].
+ *   record        any of the three; fp8_ds_mla with UE8M0 scales.
+ *   Arguments as in compute_global_topk_indices_and_lens and
+ *   dequantize_and_gather_k_cache.
+ */
+psk_status dequantize_and_gather_k_cache_topk(
+    void* out, int64_t out_stride_t, int64_t out_stride_j, const uint8_t* cache,
+    int64_t num_pages, int64_t page_stride, int32_t block_size, psk_record record,
+    int32_t head_dim, int32_t rope_dim, const int32_t* topk_local, int64_t topk_stride,
+    int64_t num_tokens, int32_t topk, const int32_t* token_to_req,
+    const int32_t* block_table, int64_t bt_stride, int32_t bt_width, int32_t num_reqs,
+    const int32_t* base_offsets, const uint8_t* is_valid_token, psk_stream_t stream);
+
+/*
+ * dequantize_and_gather_k_cache_window -- the window columns of a token
+ * gathered straight from its position.  Output identical to the window
+ * columns [0, window) of combine_topk_swa_indices (position from the
+ * metadata, window [max(replay_start, pos - window + 1, 0), pos] left-aligned,
+ * the SWA table and base offsets, padding tokens) followed by
+ * dequantize_and_gather_k_cache over them, in one launch.  fp8_ds_mla records
+ * with UE8M0 scales; out rows (t, c), c < window, as above.
+ */
+psk_status dequantize_and_gather_k_cache_window(
+    void* out, int64_t out_stride_t, int64_t out_stride_j, const uint8_t* cache,
+    int64_t num_pages, int64_t page_stride, int32_t block_size, int32_t head_dim,
+    int32_t rope_dim, const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* token_to_req, const int32_t* replay_start, int32_t num_reqs,
+    int64_t num_tokens, const int32_t* block_table, int64_t bt_stride, int32_t bt_width,
+    const int32_t* base_offsets, int32_t window, const uint8_t* is_valid_token,
+    psk_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

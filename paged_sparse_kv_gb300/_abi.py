@@ -65,6 +65,12 @@ SIGNATURES = {
         _I32, [_P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64, _P, _I64, _P, _P]),
     "write_indexer_fp8_cache": (
         _I32, [_P, _I64, _P, _I64, _P, _I64, _I64, _I32, _I32, _P, _P]),
+    "dequantize_and_gather_k_cache_topk": (
+        _I32, [_P, _I64, _I64, _P, _I64, _I64, _I32, _I32, _I32, _I32, _P, _I64, _I64, _I32, _P, _P,
+               _I64, _I32, _I32, _P, _P, _P]),
+    "dequantize_and_gather_k_cache_window": (
+        _I32, [_P, _I64, _I64, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _I32, _I64, _P,
+               _I64, _I32, _P, _I32, _P, _P]),
     "save_compressor_state": (
         _I32, [_P, _P, _I64, _P, _I32, _P, _P, _I64, _I32, _P, _I64, _I32, _P, _P]),
     "compress_kv_cache_insert": (

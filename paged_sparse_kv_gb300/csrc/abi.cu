@@ -670,6 +670,90 @@ psk_status compress_kv_cache_insert(
                        "compress_kv_cache_insert launch");
 }
 
+psk_status dequantize_and_gather_k_cache_topk(
+    void* out, int64_t out_stride_t, int64_t out_stride_j, const uint8_t* cache,
+    int64_t num_pages, int64_t page_stride, int32_t block_size, psk_record record,
+    int32_t head_dim, int32_t rope_dim, const int32_t* topk_local, int64_t topk_stride,
+    int64_t num_tokens, int32_t topk, const int32_t* token_to_req, const int32_t* block_table,
+    int64_t bt_stride, int32_t bt_width, int32_t num_reqs, const int32_t* base_offsets,
+    const uint8_t* is_valid_token, psk_stream_t stream) {
+    CHECK(num_tokens >= 0 && topk >= 0, "num_tokens and topk must be >= 0");
+    CHECK(record == PSK_REC_FP8_DS_MLA || record == PSK_REC_MXFP4 ||
+              record == PSK_REC_FP8_INDEXER,
+          "unknown record %d", (int)record);
+    int64_t rec_bytes;
+    if (record == PSK_REC_FP8_DS_MLA) {
+        CHECK(fp8_head_dim_ok(head_dim),
+              "head_dim must be one of 64, 128, 256, 512, 1024 (got %d)", head_dim);
+        CHECK(rope_dim >= 0 && rope_dim < head_dim && rope_dim % 64 == 0,
+              "rope_dim must be a multiple of 64 in [0, head_dim) (got %d)", rope_dim);
+        rec_bytes = fp8_record_bytes(head_dim, rope_dim, 1);
+    } else {
+        CHECK(mxfp4_head_dim_ok(head_dim),
+              "head_dim must be one of 32, 64, 128, 256, 512, 1024 (got %d)", head_dim);
+        CHECK(rope_dim == 0, "rope_dim must be 0 for this record");
+        rec_bytes = record == PSK_REC_MXFP4 ? head_dim / 2 + head_dim / 32 : head_dim + 4;
+    }
+    psk_status st = check_cache(cache, num_pages, page_stride, block_size, rec_bytes);
+    if (st != PSK_OK) return st;
+    CHECK(topk_stride >= topk, "topk_stride must be >= topk");
+    CHECK(bt_width >= 0 && bt_stride >= bt_width, "need 0 <= bt_width <= bt_stride");
+    if (num_tokens == 0 || topk == 0) return ok();
+    CHECK(num_reqs >= 1, "num_reqs must be >= 1");
+    CHECK(out && topk_local && token_to_req, "out, topk_local and token_to_req must be non-null");
+    CHECK(bt_width == 0 || block_table, "block_table must be non-null");
+    CHECK(aligned(out, 16), "out must be 16-byte aligned");
+    CHECK(out_stride_t >= 0 && out_stride_j >= 0 && out_stride_t % 8 == 0 && out_stride_j % 8 == 0,
+          "output strides must be non-negative multiples of 8 elements");
+    CHECK(aligned(topk_local, 4) && aligned(token_to_req, 4) && aligned(block_table, 4) &&
+              aligned(base_offsets, 4),
+          "int32 arrays must be 4-byte aligned");
+    psk::GatherParams p{static_cast<uint16_t*>(out), out_stride_t, out_stride_j, cache,
+                        num_pages, page_stride, block_size, (int32_t)record, head_dim,
+                        rope_dim, 1, nullptr, 0, num_tokens, topk};
+    psk::TopkSource tk{topk_local, topk_stride, token_to_req, is_valid_token, num_reqs,
+                       block_table, bt_stride, bt_width, base_offsets};
+    return cuda_status(psk::launch_gather_topk(p, tk, reinterpret_cast<cudaStream_t>(stream)),
+                       "dequantize_and_gather_k_cache_topk launch");
+}
+
+psk_status dequantize_and_gather_k_cache_window(
+    void* out, int64_t out_stride_t, int64_t out_stride_j, const uint8_t* cache,
+    int64_t num_pages, int64_t page_stride, int32_t block_size, int32_t head_dim,
+    int32_t rope_dim, const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* token_to_req, const int32_t* replay_start, int32_t num_reqs,
+    int64_t num_tokens, const int32_t* block_table, int64_t bt_stride, int32_t bt_width,
+    const int32_t* base_offsets, int32_t window, const uint8_t* is_valid_token,
+    psk_stream_t stream) {
+    CHECK(num_tokens >= 0 && window >= 0, "num_tokens and window must be >= 0");
+    CHECK(fp8_head_dim_ok(head_dim),
+          "head_dim must be one of 64, 128, 256, 512, 1024 (got %d)", head_dim);
+    CHECK(rope_dim >= 0 && rope_dim < head_dim && rope_dim % 64 == 0,
+          "rope_dim must be a multiple of 64 in [0, head_dim) (got %d)", rope_dim);
+    psk_status st = check_cache(cache, num_pages, page_stride, block_size,
+                                fp8_record_bytes(head_dim, rope_dim, 1));
+    if (st != PSK_OK) return st;
+    CHECK(bt_width >= 0 && bt_stride >= bt_width, "need 0 <= bt_width <= bt_stride");
+    if (num_tokens == 0 || window == 0) return ok();
+    CHECK(num_reqs >= 1, "num_reqs must be >= 1");
+    CHECK(out && query_start_loc && seq_lens && token_to_req,
+          "out, query_start_loc, seq_lens and token_to_req must be non-null");
+    CHECK(bt_width == 0 || block_table, "block_table must be non-null");
+    CHECK(aligned(out, 16), "out must be 16-byte aligned");
+    CHECK(out_stride_t >= 0 && out_stride_j >= 0 && out_stride_t % 8 == 0 && out_stride_j % 8 == 0,
+          "output strides must be non-negative multiples of 8 elements");
+    CHECK(aligned(query_start_loc, 4) && aligned(seq_lens, 4) && aligned(token_to_req, 4) &&
+              aligned(replay_start, 4) && aligned(block_table, 4) && aligned(base_offsets, 4),
+          "int32 arrays must be 4-byte aligned");
+    psk::GatherParams p{static_cast<uint16_t*>(out), out_stride_t, out_stride_j, cache,
+                        num_pages, page_stride, block_size, 0, head_dim, rope_dim, 1, nullptr, 0,
+                        num_tokens, window};
+    psk::WindowSource wn{query_start_loc, seq_lens, token_to_req, replay_start, is_valid_token,
+                         num_reqs, block_table, bt_stride, bt_width, base_offsets};
+    return cuda_status(psk::launch_gather_window(p, wn, reinterpret_cast<cudaStream_t>(stream)),
+                       "dequantize_and_gather_k_cache_window launch");
+}
+
 }  // extern "C"
 
 namespace psk {

@@ -60,11 +60,17 @@ __device__ __forceinline__ void item_to_tj(int64_t item, int32_t cols, bool smal
     }
 }
 
-// Where each item's slot comes from: the index matrix (INDEX form) or a
-// request's position range through its block-table row (RANGE form).
+// Where each item's slot comes from: the index matrix (INDEX form), a
+// request's position range through its block-table row (RANGE form), a
+// token's local top-k index through its request's table (TOPK form) or a
+// token's window position through the SWA table (WINDOW form).
+enum : int { kSrcIndex = 0, kSrcRange = 1, kSrcTopk = 2, kSrcWindow = 3 };
+
 struct ItemSource {
-    GatherParams g;      // index form (and cache geometry for both forms)
+    GatherParams g;      // index form (and cache geometry and output for every form)
     RangeParams r;       // range form
+    TopkSource tk;       // top-k form
+    WindowSource wn;     // window form
 };
 
 // Slot of position p through one table row (the block-table rule), or -1.
@@ -81,7 +87,45 @@ __device__ __forceinline__ int32_t table_slot(const int32_t* row, int32_t width,
     return s > 0x7FFFFFFFll ? -1 : (int32_t)s;
 }
 
-template <int D, bool UE8M0, bool RANGE>
+// Slot of item (t, j) of the TOPK form: the compute_global_topk_indices_and_lens
+// rule (padding token or -1 entry -> -1) then the gather's capacity check.
+// The token's request, validity and top-k entry are loaded together.
+__device__ __forceinline__ int32_t topk_item_slot(const TopkSource& s, int32_t bs, int32_t shift,
+                                                  int64_t capacity, int64_t t, int32_t j) {
+    const int32_t r = __ldg(s.t2r + t);
+    const bool valid = s.valid == nullptr || __ldg(s.valid + t) != 0;
+    const int32_t l = __ldg(s.topk_local + t * s.topk_stride + j);
+    if (!valid || r < 0 || r >= s.num_reqs || l < 0) return -1;
+    const int64_t base = s.base ? __ldg(s.base + r) : 0;
+    const int32_t raw = table_slot(s.bt + (int64_t)r * s.bt_stride, s.bt_width, base, bs, shift, l);
+    return (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
+}
+
+// Slot of window column c of token t (the WINDOW form): the window rule of
+// combine_topk_swa_indices -- position from the request's metadata, window
+// [max(replay_start, pos - W + 1, 0), pos], left-aligned -- then the gather's
+// capacity check.
+__device__ __forceinline__ int32_t window_item_slot(const WindowSource& s, int32_t W, int32_t bs,
+                                                    int32_t shift, int64_t capacity, int64_t t,
+                                                    int32_t c) {
+    const int32_t r = __ldg(s.t2r + t);
+    const bool valid = s.valid == nullptr || __ldg(s.valid + t) != 0;
+    if (!valid || r < 0 || r >= s.num_reqs) return -1;
+    const int64_t qs = __ldg(s.qsl + r), qe = __ldg(s.qsl + r + 1);
+    const int64_t seq = __ldg(s.seq_lens + r);
+    const int64_t rs = s.replay ? (int64_t)__ldg(s.replay + r) : 0;
+    const int64_t base = s.base ? __ldg(s.base + r) : 0;
+    const int64_t pos = seq - (qe - qs) + (t - qs);
+    int64_t lo = pos - W + 1;
+    if (rs > lo) lo = rs;
+    if (lo < 0) lo = 0;
+    const int64_t p = lo + c;
+    if (p > pos) return -1;
+    const int32_t raw = table_slot(s.bt + (int64_t)r * s.bt_stride, s.bt_width, base, bs, shift, p);
+    return (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
+}
+
+template <int D, bool UE8M0, int SRC>
 __global__ void __launch_bounds__(kTmaThreads)
 gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
     const GatherParams& p = src.g;
@@ -102,6 +146,7 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     // INDEX form: items = rows x cols of the index matrix.  RANGE form:
     // items = num_reqs x span, span = out_rows - offset rows per request.
+    constexpr bool RANGE = SRC == kSrcRange;
     const int64_t span = RANGE ? src.r.out_rows - src.r.offset : (int64_t)p.cols;
     const int64_t items = RANGE ? (int64_t)src.r.num_reqs * span : p.rows * (int64_t)p.cols;
     const int64_t tiles = (items + kRowsPerTile - 1) / kRowsPerTile;
@@ -158,8 +203,15 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
                             slot[q] = -2;  // outside the gathered range: not written
                         }
                     } else {
-                        const int32_t raw = __ldg(p.idx + t * p.idx_stride + j);
-                        slot[q] = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
+                        if (SRC == kSrcTopk) {
+                            slot[q] = topk_item_slot(src.tk, bs, p.block_shift, capacity, t, j);
+                        } else if (SRC == kSrcWindow) {
+                            slot[q] = window_item_slot(src.wn, p.cols, bs, p.block_shift, capacity,
+                                                       t, j);
+                        } else {
+                            const int32_t raw = __ldg(p.idx + t * p.idx_stride + j);
+                            slot[q] = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
+                        }
                         oof[q] = t * p.out_stride_t + (int64_t)j * p.out_stride_j;
                     }
                 } else {
@@ -279,9 +331,9 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
 // scale) before it converts and stores anything.
 // REC 1: MXFP4 (TokenSpeed read_deepseek_v4_indexer_mxfp4_cache); REC 2: the
 // FP8 indexer record (write_deepseek_v4_indexer_fp8_cache's layout).
-template <int D, int REC>
+template <int D, int REC, int SRC>
 __global__ void __launch_bounds__(kThreads)
-gather_small_kernel(GatherParams p) {
+gather_small_kernel(GatherParams p, TopkSource tk) {
     constexpr int CHUNKS = D / 8;
     constexpr int LANES = CHUNKS < kWarp ? CHUNKS : kWarp;
     constexpr int CPL = CHUNKS / LANES;
@@ -317,8 +369,12 @@ gather_small_kernel(GatherParams p) {
                 t = item / p.cols;
                 j = (int32_t)(item - t * p.cols);
             }
-            const int32_t raw = __ldg(p.idx + t * p.idx_stride + j);
-            my_slot = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
+            if (SRC == kSrcTopk) {
+                my_slot = topk_item_slot(tk, p.block_size, p.block_shift, capacity, t, j);
+            } else {
+                const int32_t raw = __ldg(p.idx + t * p.idx_stride + j);
+                my_slot = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
+            }
             my_off = t * p.out_stride_t + (int64_t)j * p.out_stride_j;
         }
         uint2 raw[STEPS][CPL];     // REC 1: .x = 4 value bytes; REC 2: 8 e4m3 bytes
@@ -389,7 +445,7 @@ int64_t persistent_blocks(K kernel, int64_t groups_needed, int lanes) {
     return need < full ? need : full;
 }
 
-template <int D, bool UE8M0, bool RANGE>
+template <int D, bool UE8M0, int SRC>
 cudaError_t gather_fp8_dispatch(const ItemSource& src, int64_t items, cudaStream_t stream) {
     const int ts = D - src.g.rope_dim + 2 * src.g.rope_dim;
     constexpr int SDIM = UE8M0 ? D / 64 : 4 * (D / 64);
@@ -398,7 +454,7 @@ cudaError_t gather_fp8_dispatch(const ItemSource& src, int64_t items, cudaStream
     const size_t smem = (size_t)kStages * kRowsPerTile * slot_bytes +
                         2 * kStages * sizeof(uint64_t) +
                         kStages * kRowsPerTile * (sizeof(int64_t) + sizeof(int32_t));
-    auto kern = gather_fp8_tma_kernel<D, UE8M0, RANGE>;
+    auto kern = gather_fp8_tma_kernel<D, UE8M0, SRC>;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -417,40 +473,48 @@ cudaError_t gather_fp8_dispatch(const ItemSource& src, int64_t items, cudaStream
                       slot_bytes);
 }
 
-template <bool RANGE>
+template <int SRC>
 cudaError_t fp8_by_dim(const ItemSource& src, int64_t items, cudaStream_t stream) {
     const bool ue = src.g.is_ue8m0 != 0;
+    if (SRC >= kSrcTopk && !ue) return cudaErrorInvalidValue;  // fused forms: UE8M0 only
     switch (src.g.head_dim) {
-        case 64: return ue ? gather_fp8_dispatch<64, true, RANGE>(src, items, stream) : gather_fp8_dispatch<64, false, RANGE>(src, items, stream);
-        case 128: return ue ? gather_fp8_dispatch<128, true, RANGE>(src, items, stream) : gather_fp8_dispatch<128, false, RANGE>(src, items, stream);
-        case 256: return ue ? gather_fp8_dispatch<256, true, RANGE>(src, items, stream) : gather_fp8_dispatch<256, false, RANGE>(src, items, stream);
-        case 512: return ue ? gather_fp8_dispatch<512, true, RANGE>(src, items, stream) : gather_fp8_dispatch<512, false, RANGE>(src, items, stream);
-        case 1024: return ue ? gather_fp8_dispatch<1024, true, RANGE>(src, items, stream) : gather_fp8_dispatch<1024, false, RANGE>(src, items, stream);
+#define PSK_FP8_CASE(DIM)                                                                  \
+        case DIM:                                                                          \
+            if constexpr (SRC >= kSrcTopk) return gather_fp8_dispatch<DIM, true, SRC>(src, items, stream); \
+            else return ue ? gather_fp8_dispatch<DIM, true, SRC>(src, items, stream)       \
+                           : gather_fp8_dispatch<DIM, false, SRC>(src, items, stream);
+        PSK_FP8_CASE(64)
+        PSK_FP8_CASE(128)
+        PSK_FP8_CASE(256)
+        PSK_FP8_CASE(512)
+        PSK_FP8_CASE(1024)
+#undef PSK_FP8_CASE
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <int D, int REC>
-cudaError_t gather_small_dispatch(const GatherParams& p, cudaStream_t stream) {
+template <int D, int REC, int SRC>
+cudaError_t gather_small_dispatch(const GatherParams& p, const TopkSource& tk,
+                                  cudaStream_t stream) {
     constexpr int LANES = (D / 8) < kWarp ? (D / 8) : kWarp;
     constexpr int GPW = kWarp / LANES;
     constexpr int STEPS = (kWarp / GPW) < 8 ? (kWarp / GPW) : 8;
     const int64_t items = p.rows * (int64_t)p.cols;
-    auto kern = gather_small_kernel<D, REC>;
+    auto kern = gather_small_kernel<D, REC, SRC>;
     const int64_t batches = (items + STEPS * GPW - 1) / (STEPS * GPW);
     const int64_t blocks = persistent_blocks(kern, batches, kWarp);
-    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p);
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p, tk);
 }
 
-template <int REC>
-cudaError_t gather_small_by_dim(const GatherParams& p, cudaStream_t stream) {
+template <int REC, int SRC>
+cudaError_t gather_small_by_dim(const GatherParams& p, const TopkSource& tk, cudaStream_t stream) {
     switch (p.head_dim) {
-        case 32: return gather_small_dispatch<32, REC>(p, stream);
-        case 64: return gather_small_dispatch<64, REC>(p, stream);
-        case 128: return gather_small_dispatch<128, REC>(p, stream);
-        case 256: return gather_small_dispatch<256, REC>(p, stream);
-        case 512: return gather_small_dispatch<512, REC>(p, stream);
-        case 1024: return gather_small_dispatch<1024, REC>(p, stream);
+        case 32: return gather_small_dispatch<32, REC, SRC>(p, tk, stream);
+        case 64: return gather_small_dispatch<64, REC, SRC>(p, tk, stream);
+        case 128: return gather_small_dispatch<128, REC, SRC>(p, tk, stream);
+        case 256: return gather_small_dispatch<256, REC, SRC>(p, tk, stream);
+        case 512: return gather_small_dispatch<512, REC, SRC>(p, tk, stream);
+        case 1024: return gather_small_dispatch<1024, REC, SRC>(p, tk, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -467,9 +531,36 @@ cudaError_t launch_gather(const GatherParams& params, cudaStream_t stream) {
     if (p.record == 0) {
         ItemSource src{};
         src.g = p;
-        return fp8_by_dim<false>(src, p.rows * (int64_t)p.cols, stream);
+        return fp8_by_dim<kSrcIndex>(src, p.rows * (int64_t)p.cols, stream);
     }
-    return p.record == 1 ? gather_small_by_dim<1>(p, stream) : gather_small_by_dim<2>(p, stream);
+    const TopkSource none{};
+    return p.record == 1 ? gather_small_by_dim<1, kSrcIndex>(p, none, stream)
+                         : gather_small_by_dim<2, kSrcIndex>(p, none, stream);
+}
+
+cudaError_t launch_gather_topk(const GatherParams& params, const TopkSource& tk,
+                               cudaStream_t stream) {
+    GatherParams p = params;
+    p.block_shift = log2_if_pow2(p.block_size);
+    if (p.record == 0) {
+        ItemSource src{};
+        src.g = p;
+        src.tk = tk;
+        return fp8_by_dim<kSrcTopk>(src, p.rows * (int64_t)p.cols, stream);
+    }
+    return p.record == 1 ? gather_small_by_dim<1, kSrcTopk>(p, tk, stream)
+                         : gather_small_by_dim<2, kSrcTopk>(p, tk, stream);
+}
+
+cudaError_t launch_gather_window(const GatherParams& params, const WindowSource& wn,
+                                 cudaStream_t stream) {
+    GatherParams p = params;
+    p.block_shift = log2_if_pow2(p.block_size);
+    if (p.record != 0) return cudaErrorInvalidValue;
+    ItemSource src{};
+    src.g = p;
+    src.wn = wn;
+    return fp8_by_dim<kSrcWindow>(src, p.rows * (int64_t)p.cols, stream);
 }
 
 cudaError_t launch_gather_ranges(const RangeParams& r, cudaStream_t stream) {
@@ -485,7 +576,7 @@ cudaError_t launch_gather_ranges(const RangeParams& r, cudaStream_t stream) {
     src.g.head_dim = r.head_dim;
     src.g.rope_dim = r.rope_dim;
     src.g.is_ue8m0 = r.is_ue8m0;
-    return fp8_by_dim<true>(src, (int64_t)r.num_reqs * (r.out_rows - r.offset), stream);
+    return fp8_by_dim<kSrcRange>(src, (int64_t)r.num_reqs * (r.out_rows - r.offset), stream);
 }
 
 // ---- raw MXFP4 paged gather ----------------------------------------------------------

@@ -74,6 +74,40 @@ cudaError_t launch_mxfp4_raw_gather(const RawGatherParams& p, cudaStream_t strea
 
 // Number of bounded in-kernel waits that expired on the current device.
 
+// Slots computed in the gather itself (no index matrix): the top-k columns of
+// a token (a local top-k index through the request's table, the
+// compute_global_topk_indices_and_lens rule) or its window columns (the
+// window rule of combine_topk_swa_indices through the SWA table).
+struct TopkSource {
+    const int32_t* topk_local;  // [rows, topk_stride]
+    int64_t topk_stride;
+    const int32_t* t2r;
+    const uint8_t* valid;       // nullable
+    int32_t num_reqs;
+    const int32_t* bt;
+    int64_t bt_stride;
+    int32_t bt_width;
+    const int32_t* base;        // nullable
+};
+
+struct WindowSource {
+    const int32_t* qsl;
+    const int32_t* seq_lens;
+    const int32_t* t2r;
+    const int32_t* replay;      // nullable
+    const uint8_t* valid;       // nullable
+    int32_t num_reqs;
+    const int32_t* bt;
+    int64_t bt_stride;
+    int32_t bt_width;
+    const int32_t* base;        // nullable
+};
+
+// p.idx is unused: rows = tokens, cols = topk (or window); out as in p.
+cudaError_t launch_gather_topk(const GatherParams& p, const TopkSource& s, cudaStream_t stream);
+cudaError_t launch_gather_window(const GatherParams& p, const WindowSource& s,
+                                 cudaStream_t stream);
+
 // Count of expired bounded waits in the gather kernels.
 cudaError_t read_wait_timeouts(uint32_t* count);
 

@@ -438,3 +438,60 @@ def compress_kv_cache_insert(state_cache: torch.Tensor, token_to_req_indices: to
               cos_sin_cache.shape[0], _ptr(kv_cache_2d), num_pages, page_stride,
               kv_cache_block_size, _ptr(kv_slot_mapping), _ptr(err_count),
               _stream(state_cache.device))
+
+
+# ---- fused gathers ------------------------------------------------------------------------
+
+def dequantize_and_gather_k_cache_topk(out: torch.Tensor, cache: torch.Tensor,
+                                       topk_indices: torch.Tensor,
+                                       token_to_req_indices: torch.Tensor,
+                                       block_table: torch.Tensor, block_size: int, *,
+                                       record: int = PSK_REC_FP8_DS_MLA, rope_dim: int = 64,
+                                       num_reqs: Optional[int] = None,
+                                       base_offsets: Optional[torch.Tensor] = None,
+                                       is_valid_token: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """out[t, j] = the row of topk_indices[t, j] mapped through the request's table
+    (= compute_global_topk_indices_and_lens + dequantize_and_gather_k_cache)."""
+    _need_cuda(out, cache, topk_indices, token_to_req_indices, block_table, base_offsets,
+               is_valid_token)
+    _need(out, torch.bfloat16, "out")
+    T, K = topk_indices.shape
+    if out.dim() != 3 or out.shape[0] != T or out.shape[1] != K or out.stride(2) != 1:
+        raise ValueError("out must be [T, K, D] with unit inner stride")
+    num_pages, page_stride = _pages(cache)
+    valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
+    R = block_table.shape[0] if num_reqs is None else num_reqs
+    _abi.call("dequantize_and_gather_k_cache_topk", _ptr(out), out.stride(0), out.stride(1),
+              _ptr(cache), num_pages, page_stride, block_size, record, out.shape[2],
+              rope_dim if record == PSK_REC_FP8_DS_MLA else 0, _ptr(topk_indices),
+              _rows(topk_indices, "topk_indices"), T, K, _ptr(token_to_req_indices),
+              _ptr(block_table), _rows(block_table, "block_table"), block_table.shape[1], R,
+              _ptr(base_offsets), _ptr(valid), _stream(out.device))
+    return out
+
+
+def dequantize_and_gather_k_cache_window(out: torch.Tensor, cache: torch.Tensor,
+                                         query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
+                                         token_to_req: torch.Tensor,
+                                         replay_start: Optional[torch.Tensor],
+                                         block_table: torch.Tensor, block_size: int,
+                                         window_size: int, *, rope_dim: int = 64,
+                                         base_offsets: Optional[torch.Tensor] = None,
+                                         is_valid_token: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """out[t, c] = the row of window column c of token t (= the window columns of
+    combine_topk_swa_indices + dequantize_and_gather_k_cache)."""
+    _need_cuda(out, cache, query_start_loc, seq_lens, token_to_req, replay_start, block_table,
+               base_offsets, is_valid_token)
+    _need(out, torch.bfloat16, "out")
+    T = token_to_req.shape[0]
+    if out.dim() != 3 or out.shape[0] != T or out.shape[1] != window_size or out.stride(2) != 1:
+        raise ValueError("out must be [T, window, D] with unit inner stride")
+    num_pages, page_stride = _pages(cache)
+    valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
+    _abi.call("dequantize_and_gather_k_cache_window", _ptr(out), out.stride(0), out.stride(1),
+              _ptr(cache), num_pages, page_stride, block_size, out.shape[2], rope_dim,
+              _ptr(query_start_loc), _ptr(seq_lens), _ptr(token_to_req), _ptr(replay_start),
+              seq_lens.shape[0], T, _ptr(block_table), _rows(block_table, "block_table"),
+              block_table.shape[1], _ptr(base_offsets), window_size, _ptr(valid),
+              _stream(out.device))
+    return out

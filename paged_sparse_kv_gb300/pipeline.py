@@ -27,6 +27,16 @@ Decode-sized kernels fill only part of the GPU, so overlapping the chains
 shortens the step to its critical path.  Capturing ``step(concurrent=True)``
 in a CUDA graph keeps the fork/join structure.
 
+``path="fused"`` produces the same outputs with gathers that compute their
+own slots (the window rule through the SWA table, the local top-k through the
+compressed / indexer table), so no gather waits for an index build; the index
+builders still run for their outputs (sparse_indices, lens, the global top-k):
+
+  stream M:  gather_topk[topk]  (issued first)
+  stream A:  quantize_and_insert_k_cache -> gather_window[swa]
+  stream B:  write_indexer_mxfp4_cache -> gather_topk[mxfp4]
+  stream C:  combine_topk_swa_indices -> compute_global_topk_indices_and_lens
+
 ``path="workspace"`` is the prefill path of TokenSpeed's backend
 (``_prefill_workspace``): the compressed rows of every request (range form,
 offset 0) and its window rows (offset ``compressed_base``) are gathered into a
@@ -129,6 +139,9 @@ class Pipeline:
             self.lens = torch.empty((T,), dtype=torch.int32, device=dev)
             self.gathered = torch.empty((T, self.cols, w.head_dim), dtype=torch.bfloat16,
                                         device=dev)
+            # the padding columns (sparse_indices -1) gather as zero rows; the
+            # fused top-k gather writes only the K real columns
+            self.gathered[:, w.window + K:].zero_()
         else:
             self.sparse_indices = self.lens = self.gathered = None
         self.global_topk = torch.empty((T, K), dtype=torch.int32, device=dev)
@@ -380,6 +393,79 @@ class Pipeline:
             record=ops.PSK_REC_MXFP4)))
         return L
 
+    def fused_launches(self) -> list[tuple[str, Callable[[], None]]]:
+        """The fused step as (kernel name, launch) pairs, in serial order."""
+        w = self.w
+        base = dict(self.launches())
+        L: list[tuple[str, Callable[[], None]]] = []
+        for name in ("quantize_and_insert_k_cache", "write_indexer_mxfp4_cache",
+                     "combine_topk_swa_indices", "compute_global_topk_indices_and_lens"):
+            if name in base:
+                L.append((name, base[name]))
+        if w.has_fp8:
+            W = w.window
+            L.append(("dequantize_and_gather_k_cache_window[swa]",
+                      lambda: ops.dequantize_and_gather_k_cache_window(
+                          self.gathered[:, :W, :], self.swa_cache, self.qsl, self.seq_lens,
+                          self.t2r, self.replay, self.swa_bt, w.swa_cache.block_size, W,
+                          rope_dim=w.rope_dim, is_valid_token=self.valid)))
+            comp_table = self.comp_bt if self.comp_bt is not None else self.swa_bt
+            L.append(("dequantize_and_gather_k_cache_topk[topk]",
+                      lambda: ops.dequantize_and_gather_k_cache_topk(
+                          self.gathered[:, W:W + w.topk, :], self.comp_cache, self.topk, self.t2r,
+                          comp_table, w.comp_cache.block_size, rope_dim=w.rope_dim,
+                          num_reqs=w.num_reqs, is_valid_token=self.valid)))
+        L.append(("dequantize_and_gather_k_cache_topk[mxfp4]",
+                  lambda: ops.dequantize_and_gather_k_cache_topk(
+                      self.gathered_index, self.index_cache, self.topk, self.t2r,
+                      self.index_table, w.index_cache.block_size, record=ops.PSK_REC_MXFP4,
+                      num_reqs=w.num_reqs, is_valid_token=self.valid)))
+        return L
+
+    def _fused_step(self, concurrent: bool, hooks: dict) -> None:
+        L = self.fused_launches()
+        fns = dict(L)
+
+        def run(name):
+            if name not in fns:
+                return
+            pre, post = hooks.get(name, (None, None))
+            if pre:
+                pre()
+            fns[name]()
+            if post:
+                post()
+
+        if not concurrent:
+            for name, _ in L:
+                run(name)
+            return
+        main = torch.cuda.current_stream(self.dev)
+        if not hasattr(self, "_side3"):
+            self._side3 = tuple(torch.cuda.Stream(self.dev) for _ in range(3))
+        sa, sb, sc = self._side3
+        fork = torch.cuda.Event()
+        fork.record(main)
+        # the longest gather is issued first so that its CTAs are resident
+        # before the side chains take SMs
+        run("dequantize_and_gather_k_cache_topk[topk]")
+        done = []
+        for st, names in ((sa, ("quantize_and_insert_k_cache",
+                                "dequantize_and_gather_k_cache_window[swa]")),
+                          (sb, ("write_indexer_mxfp4_cache",
+                                "dequantize_and_gather_k_cache_topk[mxfp4]")),
+                          (sc, ("combine_topk_swa_indices",
+                                "compute_global_topk_indices_and_lens"))):
+            st.wait_event(fork)
+            with torch.cuda.stream(st):
+                for n in names:
+                    run(n)
+                ev = torch.cuda.Event()
+                ev.record(st)
+                done.append(ev)
+        for ev in done:
+            main.wait_event(ev)
+
     def step(self, concurrent: bool = False, hooks: Optional[dict] = None,
              path: str = "index") -> None:
         """Launch one step.  ``hooks`` maps a kernel name to a pair of callables
@@ -387,6 +473,8 @@ class Pipeline:
         (used to bracket one kernel with timing events)."""
         if path == "workspace":
             return self._workspace_step(concurrent, hooks or {})
+        if path == "fused":
+            return self._fused_step(concurrent, hooks or {})
         if path == "dense":
             return self._dense_step(concurrent, hooks or {})
         if path in ("indexer_fp8", "indexer_store"):

@@ -381,3 +381,59 @@ def test_compress_rejects_bad_arguments(psk_lib, kw):
 
 def test_compress_zero_tokens_ok(psk_lib):
     assert _cmp(n=0, st=None, t2r=None) == OK
+
+
+def _gather_topk(**kw):
+    a = dict(out=A, ost=512 * 512, osj=512, cache=B, num_pages=8, page_stride=64 * 584, bs=64,
+             rec=0, D=512, rope=64, tk=C, tks=512, T=4, K=512, t2r=C + 4096, bt=C + 8192,
+             bts=16, btw=16, R=2, base=None, valid=None)
+    a.update(kw)
+    return _abi.status("dequantize_and_gather_k_cache_topk", a["out"], a["ost"], a["osj"],
+                       a["cache"], a["num_pages"], a["page_stride"], a["bs"], a["rec"], a["D"],
+                       a["rope"], a["tk"], a["tks"], a["T"], a["K"], a["t2r"], a["bt"],
+                       a["bts"], a["btw"], a["R"], a["base"], a["valid"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(rec=3), dict(D=100), dict(rope=16), dict(out=A + 8),
+                                dict(osj=4), dict(ost=-8), dict(tks=100), dict(tk=None),
+                                dict(t2r=None), dict(bt=None), dict(out=None), dict(T=-1),
+                                dict(K=-1), dict(R=0), dict(bts=8), dict(btw=-1),
+                                dict(page_stride=1000), dict(rec=1, D=128, rope=64),
+                                dict(rec=1, D=48, rope=0), dict(rec=2, D=64, rope=0,
+                                                                page_stride=100),
+                                dict(tk=C + 2), dict(base=C + 1), dict(cache=None)])
+def test_gather_topk_rejects_bad_arguments(psk_lib, kw):
+    assert _gather_topk(**kw) == INV
+
+
+def test_gather_topk_zero_work_ok(psk_lib):
+    assert _gather_topk(T=0, out=None, tk=None, t2r=None) == OK
+    assert _gather_topk(K=0, tks=0, out=None, tk=None, t2r=None) == OK
+    # an empty table needs no pointer: every slot resolves to -1
+    assert _gather_topk(T=0, btw=0, bt=None) == OK
+
+
+def _gather_window(**kw):
+    a = dict(out=A, ost=128 * 512, osj=512, cache=B, num_pages=8, page_stride=64 * 584, bs=64,
+             D=512, rope=64, qsl=C, seq=C + 64, t2r=C + 128, replay=None, R=2, T=4,
+             bt=C + 8192, bts=16, btw=16, base=None, W=128, valid=None)
+    a.update(kw)
+    return _abi.status("dequantize_and_gather_k_cache_window", a["out"], a["ost"], a["osj"],
+                       a["cache"], a["num_pages"], a["page_stride"], a["bs"], a["D"], a["rope"],
+                       a["qsl"], a["seq"], a["t2r"], a["replay"], a["R"], a["T"], a["bt"],
+                       a["bts"], a["btw"], a["base"], a["W"], a["valid"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(D=100), dict(rope=16), dict(D=128, rope=128),
+                                dict(out=A + 8), dict(osj=4), dict(ost=-8), dict(qsl=None),
+                                dict(seq=None), dict(t2r=None), dict(bt=None), dict(out=None),
+                                dict(T=-1), dict(W=-1), dict(R=0), dict(bts=8),
+                                dict(page_stride=1000), dict(replay=C + 2), dict(seq=C + 1),
+                                dict(cache=None)])
+def test_gather_window_rejects_bad_arguments(psk_lib, kw):
+    assert _gather_window(**kw) == INV
+
+
+def test_gather_window_zero_work_ok(psk_lib):
+    assert _gather_window(T=0, out=None, qsl=None, seq=None, t2r=None) == OK
+    assert _gather_window(W=0, out=None, qsl=None, seq=None, t2r=None) == OK

@@ -443,3 +443,98 @@ def test_index_build_int32_extremes(cuda_device, bs):
     _assert_same(out.cpu().numpy(), want, "extreme global top-k")
     _assert_same(lens.cpu().numpy(), wl, "extreme lens")
     assert (want >= 0).any()
+
+
+# ---- fused gathers (slots computed in the gather) ---------------------------------------
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fused_gathers_match_two_step_oracle(cuda_device, seed):
+    """gather_topk == compute_global_topk + gather and gather_window == the
+    window columns of combine + gather, on random metadata (padding tokens,
+    requests out of range, base offsets, replay_start, -1 table entries and
+    top-k entries, odd page sizes) for the three records."""
+    rng = np.random.default_rng(7000 + seed)
+    d = cuda_device
+    bs = int(rng.choice([1, 4, 5, 16, 64]))
+    R = int(rng.integers(1, 5))
+    qlen = rng.integers(0, 6, size=R)
+    seq = (qlen + rng.integers(0, 40 * bs // 4 + 8, size=R)).astype(np.int32)
+    qsl = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+    T = int(qsl[-1])
+    if T == 0:
+        return
+    t2r = np.repeat(np.arange(R), qlen).astype(np.int32)
+    t2r[rng.random(T) < 0.1] = R
+    valid = None if rng.random() < 0.5 else (rng.random(T) < 0.85)
+    replay = None if rng.random() < 0.5 else rng.integers(0, 6, size=R).astype(np.int32)
+    width, pages = 12, 30
+    table = rng.integers(-1, pages, size=(R, width)).astype(np.int32)
+    base = None if rng.random() < 0.5 else rng.integers(0, 2, size=R).astype(np.int32)
+    K, W = int(rng.choice([4, 16, 20])), int(rng.choice([4, 8, 12]))
+    topk = rng.integers(-1, width * bs + 3, size=(T, K)).astype(np.int32)
+    for rec, D, rope in ((0, 512, 64), (0, 128, 0), (1, 128, 0), (2, 64, 0)):
+        rb = oracle.fp8_record_bytes(D, rope, True) if rec == 0 else (
+            D // 2 + D // 32 if rec == 1 else D + 4)
+        geom = synthetic.CacheGeom(pages, bs, (bs * rb + 15) // 16 * 16)
+        host = synthetic.random_cache_bytes(17 + rec, geom)
+        if rec == 2:  # finite binary32 scales
+            for s_ in range(pages * bs):
+                pg, off = divmod(s_, bs)
+                host[pg, bs * D + off * 4: bs * D + off * 4 + 4] = np.frombuffer(
+                    np.float32(2.0 ** int(rng.integers(-20, 20))).tobytes(), np.uint8)
+        dev_cache = torch.from_numpy(host).to(d)
+        gt, _ = oracle.compute_global_topk_indices_and_lens(topk, t2r, table, bs, base_offsets=base,
+                                                            is_valid_token=valid)
+        want = oracle.dequantize_and_gather_k_cache(host, bs, rec, D, rope, gt)
+        out = torch.full((T, K + 1, D), 5, dtype=torch.bfloat16, device=d)
+        ops.dequantize_and_gather_k_cache_topk(
+            out[:, 1:], dev_cache, _dev_i32(topk, d), _dev_i32(t2r, d), _dev_i32(table, d), bs,
+            record=rec, rope_dim=rope, num_reqs=R, base_offsets=_dev_i32(base, d),
+            is_valid_token=None if valid is None else torch.from_numpy(valid.astype(np.uint8)).to(d))
+        _assert_same(_u16(out[:, 1:]), want, f"fused topk gather rec={rec} D={D}")
+        if rec != 0:
+            continue
+        si, _ = oracle.combine_topk_swa_indices(qsl, seq, t2r, replay, table, bs, table, bs, W, 4,
+                                                np.zeros((T, 0), np.int32), swa_base_offsets=base,
+                                                is_valid_token=valid)
+        want = oracle.dequantize_and_gather_k_cache(host, bs, 0, D, rope, np.ascontiguousarray(si[:, :W]))
+        outw = torch.empty((T, W, D), dtype=torch.bfloat16, device=d)
+        ops.dequantize_and_gather_k_cache_window(
+            outw, dev_cache, _dev_i32(qsl, d), _dev_i32(seq, d), _dev_i32(t2r, d),
+            _dev_i32(replay, d), _dev_i32(table, d), bs, W, rope_dim=rope,
+            base_offsets=_dev_i32(base, d),
+            is_valid_token=None if valid is None else torch.from_numpy(valid.astype(np.uint8)).to(d))
+        _assert_same(_u16(outw), want, f"fused window gather D={D}")
+
+
+@pytest.mark.parametrize("name,mode", [("decode", "graph"), ("tiny", "serial"),
+                                       ("mixed", "concurrent"), ("mxfp4", "graph")])
+def test_fused_step_matches_index_step(cuda_device, name, mode):
+    """The fused step's outputs equal the index step's (itself pinned against
+    the oracle): same caches, indices, lens and gathered rows."""
+    from paged_sparse_kv_gb300.pipeline import Pipeline
+    w = synthetic.make(name)
+    outs = []
+    for path in ("index", "fused"):
+        p = Pipeline(w, cuda_device)
+        for cname, geom in (("swa_cache", w.swa_cache), ("comp_cache", w.comp_cache),
+                            ("index_cache", w.index_cache)):
+            if geom is not None:
+                getattr(p, cname).copy_(torch.from_numpy(synthetic.random_cache_bytes(91, geom)))
+        if mode == "graph":
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(cuda_device)
+            side.wait_stream(torch.cuda.current_stream(cuda_device))
+            with torch.cuda.graph(g, stream=side):
+                p.step(concurrent=True, path=path)
+            g.replay()
+        else:
+            p.step(concurrent=(mode == "concurrent"), path=path)
+        torch.cuda.synchronize(cuda_device)
+        outs.append([t.cpu() for t in (p.sparse_indices, p.lens, p.gathered, p.global_topk,
+                                       p.global_lens, p.gathered_index, p.swa_cache,
+                                       p.index_cache) if t is not None])
+        del p
+        torch.cuda.empty_cache()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
