@@ -42,6 +42,9 @@ namespace {
 #ifndef PSK_WS_INDEX_MAX_PASSES
 #define PSK_WS_INDEX_MAX_PASSES 2
 #endif
+#ifndef PSK_INDEX_SB_UNROLL
+#define PSK_INDEX_SB_UNROLL 1
+#endif
 #ifndef PSK_INDEX_MIN_CTAS
 #define PSK_INDEX_MIN_CTAS 3
 #endif
@@ -51,6 +54,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / kWarp;
+constexpr int kSbUnroll = PSK_INDEX_SB_UNROLL;
 constexpr int kMaxStagedEntries = 4096;  // 16 KB of int32 page ids per staged row
 constexpr int kMaxTopkStageBytes = 64 * 1024;  // top-k rows of one CTA in shared memory
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -345,6 +349,116 @@ __device__ __forceinline__ int build_row_smem(const IndexParams& p, int64_t t, c
     return cnt;
 }
 
+// ---- slot-base tables (power-of-two pages, the CTA's request staged) ---------------
+//
+// A staged table row held as slot bases: entry i is page_i << shift, or -1
+// when page_i is negative or its slots would pass INT32_MAX (page > maxp), and
+// one more entry, at index width, is -1.  A position p then maps to
+// base[i] | (p & (bs - 1)) with i = (p >> shift) - table_base when p lies in
+// the row's position range, else to base[width] = -1: -1 | rem stays -1.
+__device__ __forceinline__ void stage_slot_bases(int32_t* dst, const int32_t* src, int n,
+                                                 int shift, int32_t maxp) {
+    for (int i0 = threadIdx.x; i0 <= n; i0 += 4 * kThreads) {
+        int32_t v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kThreads;
+            v[u] = i < n ? __ldg(src + i) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kThreads;
+            if (i <= n) dst[i] = (uint32_t)v[u] > (uint32_t)maxp ? -1 : (v[u] << shift);
+        }
+    }
+}
+
+// The positions [lo, lo + span) that one staged row maps: its pages'
+// positions, clipped to [0, 2^31) and to [clip_lo, clip_hi).
+struct SbRange {
+    uint32_t lo;    // first mapped position
+    uint32_t span;  // number of mapped positions (0: none)
+    int32_t base;   // table base offset (logical page of entry 0)
+};
+
+__device__ __forceinline__ SbRange sb_range(int32_t base, int32_t width, int shift,
+                                            int64_t clip_lo, int64_t clip_hi) {
+    int64_t lo = (int64_t)base << shift;
+    int64_t hi = lo + ((int64_t)width << shift);
+    if (lo < clip_lo) lo = clip_lo;
+    if (hi > clip_hi) hi = clip_hi;
+    if (lo < 0) lo = 0;
+    if (hi > 0x80000000ll) hi = 0x80000000ll;
+    SbRange r;
+    r.lo = hi > lo ? (uint32_t)lo : 0u;
+    r.span = hi > lo ? (uint32_t)(hi - lo) : 0u;
+    r.base = base;
+    return r;
+}
+
+// Slot of position p through a slot-base row (see above): one unsigned range
+// test, one shared load, one OR.  Positions below lo (negative ones included)
+// wrap to >= span.  In range, p >= 0 and (p >> shift) - base lies in [0, width).
+__device__ __forceinline__ int32_t sb_slot(const int32_t* sb, const SbRange& r, int width,
+                                           int shift, int32_t mask, int32_t p) {
+    const bool in = (uint32_t)p - r.lo < r.span;
+    const int i = in ? (int)(((uint32_t)p >> shift) - (uint32_t)r.base) : width;
+    return sb[i] | (p & mask);
+}
+
+// Token t's row (window columns then top-k columns) through the CTA's staged
+// slot-base rows; the top-k row is in shared memory (s_row).  The same values
+// as build_row_smem with the tables staged.
+template <bool HAS_SWA>
+__device__ __forceinline__ int build_row_sb(const IndexParams& p, int64_t t, const TokMeta& m,
+                                            int first, int stride, const int32_t* s_row,
+                                            const int32_t* s_swa, const int32_t* s_comp) {
+    int32_t* out = p.out + t * p.out_stride;
+    const int nq = p.out_cols / 4;
+    if (!m.ok) {
+        for (int q = first; q < nq; q += stride)
+            *reinterpret_cast<int4*>(out + 4 * q) = make_int4(-1, -1, -1, -1);
+        return 0;
+    }
+    const int W = HAS_SWA ? p.window : 0;
+    const int cshift = p.comp_shift;
+    const int32_t cmask = p.comp_bs - 1;
+    const SbRange cr = sb_range(m.comp_base, p.comp_width, cshift, 0, 0x80000000ll);
+    SbRange wr{};
+    int sshift = 0;
+    int32_t smask = 0;
+    if (HAS_SWA) {
+        sshift = p.swa_shift;
+        smask = p.swa_bs - 1;
+        // window column c holds position lo + c for c < nwin
+        wr = sb_range(m.swa_base, p.swa_width, sshift, m.lo, m.lo + m.nwin);
+    }
+    int invalid = 0;  // minus the count of valid entries written by this lane
+    int cols = 0;
+#pragma unroll kSbUnroll
+    for (int q = first; q < nq; q += stride) {
+        const int c0 = 4 * q;
+        int v[4];
+        if (HAS_SWA && c0 < W) {
+            // m.lo <= INT32_MAX (not a wide token); columns past nwin wrap out of range
+            const uint32_t pos0 = (uint32_t)m.lo + (uint32_t)c0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                v[e] = sb_slot(s_swa, wr, p.swa_width, sshift, smask, (int32_t)(pos0 + (uint32_t)e));
+        } else {
+            const int4 w = *reinterpret_cast<const int4*>(s_row + (c0 - W));
+            v[0] = sb_slot(s_comp, cr, p.comp_width, cshift, cmask, w.x);
+            v[1] = sb_slot(s_comp, cr, p.comp_width, cshift, cmask, w.y);
+            v[2] = sb_slot(s_comp, cr, p.comp_width, cshift, cmask, w.z);
+            v[3] = sb_slot(s_comp, cr, p.comp_width, cshift, cmask, w.w);
+        }
+        invalid += (v[0] >> 31) + (v[1] >> 31) + (v[2] >> 31) + (v[3] >> 31);
+        cols += 4;
+        *reinterpret_cast<int4*>(out + c0) = make_int4(v[0], v[1], v[2], v[3]);
+    }
+    return cols + invalid;
+}
+
 // Thread 0 of the CTA: one bulk copy per token row t0..t1-1 of topk_local
 // into `dst` (rows of `words` int32), all completing on `bar`.  Returns the
 // bytes expected.  Every address and size is a multiple of 16 bytes (16-byte
@@ -393,7 +507,9 @@ template <bool HAS_SWA, bool VEC, bool POW2, bool TMA>
 __global__ void __launch_bounds__(kThreads, TMA ? PSK_INDEX_TMA_MIN_CTAS : PSK_INDEX_MIN_CTAS)
 index_build_kernel(IndexParams p) {
     // Dynamic shared memory: [TMA: tokens_per_cta top-k rows][compressed
-    // table row][SWA table row].
+    // table row + 1][SWA table row + 1].  With staged top-k rows and
+    // power-of-two pages the table rows are held as slot bases.
+    constexpr bool SB = TMA && POW2;
     extern __shared__ __align__(16) int32_t s_dyn[];
     __shared__ int s_cnt[kWarps];
     __shared__ __align__(8) uint64_t s_bar;
@@ -411,7 +527,7 @@ index_build_kernel(IndexParams p) {
     const bool copy_topk = TMA && p.topk > 0;
     int32_t* s_topk = s_dyn;
     int32_t* s_comp = s_dyn + (TMA ? p.tokens_per_cta * p.topk : 0);
-    int32_t* s_swa = s_comp + p.stage_comp;
+    int32_t* s_swa = s_comp + p.stage_comp + 1;
     if (TMA && threadIdx.x == 0) {
         mbar_init(&s_bar, 1);
         mbar_fence_init();
@@ -438,7 +554,13 @@ index_build_kernel(IndexParams p) {
     // Stage only when every row the tile needs fits (p.stage_* > 0 exactly then).
     const bool fits = p.stage_comp > 0 && (!HAS_SWA || p.stage_swa > 0);
     const int32_t staged = (fits && r0 == r1 && r0 >= 0 && r0 < p.num_reqs) ? r0 : -1;
-    if (staged >= 0) {
+    if (staged >= 0 && SB) {
+        stage_slot_bases(s_comp, p.comp_bt + (int64_t)staged * p.comp_stride, p.stage_comp,
+                         p.comp_shift, p.comp_maxp);
+        if (HAS_SWA)
+            stage_slot_bases(s_swa, p.swa_bt + (int64_t)staged * p.swa_stride, p.stage_swa,
+                             p.swa_shift, p.swa_maxp);
+    } else if (staged >= 0) {
         stage_row(s_comp, p.comp_bt + (int64_t)staged * p.comp_stride, p.stage_comp);
         if (HAS_SWA) stage_row(s_swa, p.swa_bt + (int64_t)staged * p.swa_stride, p.stage_swa);
     }
@@ -462,7 +584,10 @@ index_build_kernel(IndexParams p) {
             }
             if (TMA) {
                 const int32_t* s_row = s_topk + (t - t0) * p.topk;
-                if (staged >= 0 && m.r == staged)
+                // (a wide token's row reads global tables only)
+                if (staged >= 0 && m.r == staged && SB && !m.wide)
+                    cnt = build_row_sb<HAS_SWA>(p, t, m, first, stride, s_row, s_swa, s_comp);
+                else if (staged >= 0 && m.r == staged)
                     cnt = build_row_smem<HAS_SWA, POW2, true>(p, t, m, first, stride, s_row, s_swa, s_comp);
                 else
                     cnt = build_row_smem<HAS_SWA, POW2, false>(p, t, m, first, stride, s_row, s_swa, s_comp);
@@ -834,7 +959,7 @@ cudaError_t launch_index_build(IndexParams p, bool has_swa, cudaStream_t stream)
                      (int64_t)p.tokens_per_cta * p.topk * 4 <= kMaxTopkStageBytes;
     const bool pow2 = p.comp_shift >= 0 && (!has_swa || p.swa_shift >= 0);
     const size_t smem =
-        ((tma ? (size_t)p.tokens_per_cta * p.topk : 0) + p.stage_comp + p.stage_swa) *
+        ((tma ? (size_t)p.tokens_per_cta * p.topk : 0) + p.stage_comp + 1 + p.stage_swa + 1) *
         sizeof(int32_t);
     using Kern = void (*)(IndexParams);
     // [has_swa][pow2][mode: 0 scalar, 1 vector, 2 vector + staged top-k rows]

@@ -445,6 +445,64 @@ def test_index_build_int32_extremes(cuda_device, bs):
     assert (want >= 0).any()
 
 
+@pytest.mark.parametrize("bs", [1, 16, 64])
+@pytest.mark.parametrize("base", [-3, 0, 2])
+def test_index_build_staged_tables_large_batch(cuda_device, bs, base):
+    """Batches large enough for one warp per token and 8 tokens per CTA, one
+    request per CTA (tables staged in shared memory): negative and positive
+    base offsets, -1 pages and pages whose slots pass INT32_MAX, top-k entries
+    below, inside and past each table's range, replay_start, invalid tokens;
+    one request with positions near INT32_MAX."""
+    rng = np.random.default_rng(100 * bs + base + 7)
+    imax = 2**31 - 1
+    maxp = imax // bs
+    R, width, K, W = 3, 24, 16, 8
+    qlen = np.array([1500, 1200, 40], np.int64)
+    seq = np.array([1500 + 300, 1200 + 5, imax - 3], np.int64)
+    qsl = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+    T = int(qsl[-1])
+    t2r = np.repeat(np.arange(R), qlen).astype(np.int32)
+    valid = (rng.random(T) < 0.9).astype(np.uint8)
+    replay = np.array([0, 600, 0], np.int32)
+    pages = rng.integers(-1, 50, size=(R, width)).astype(np.int64)
+    pages[rng.random(pages.shape) < 0.1] = maxp
+    if maxp + 1 <= imax:
+        pages[rng.random(pages.shape) < 0.05] = maxp + 1
+    table = pages.astype(np.int32)
+    swa_table = rng.integers(-1, 50, size=(R, width)).astype(np.int32)
+    bases = np.array([base, base + 1, 0], np.int32)
+    # the third request's window lives at logical pages near imax // bs
+    swa_base = np.array([base, base, (imax - 3 - 2 * W) // bs], np.int32)
+    lo = np.maximum(bases.astype(np.int64) * bs, 0)
+    topk = np.empty((T, K), np.int64)
+    for r in range(R):
+        rows = t2r == r
+        span = width * bs
+        topk[rows] = rng.integers(lo[r] - bs, lo[r] + span + bs, size=(int(rows.sum()), K))
+    topk[rng.random(topk.shape) < 0.1] = -1
+    topk[rng.random(topk.shape) < 0.02] = imax
+    topk = np.clip(topk, -1, imax).astype(np.int32)
+    d = cuda_device
+    si, lens = ops.combine_topk_swa_indices(
+        _dev_i32(qsl, d), _dev_i32(seq.astype(np.int32), d), _dev_i32(t2r, d), _dev_i32(replay, d),
+        _dev_i32(swa_table, d), bs, _dev_i32(table, d), bs, W, 4, _dev_i32(topk, d),
+        swa_base_offsets=_dev_i32(swa_base, d), compressed_base_offsets=_dev_i32(bases, d),
+        is_valid_token=torch.from_numpy(valid).to(d), num_tokens=T)
+    want, want_lens = oracle.combine_topk_swa_indices(
+        qsl, seq.astype(np.int32), t2r, replay, swa_table, bs, table, bs, W, 4, topk,
+        swa_base_offsets=swa_base, comp_base_offsets=bases, is_valid_token=valid)
+    _assert_same(si.cpu().numpy(), want, "staged combine")
+    _assert_same(lens.cpu().numpy(), want_lens, "staged combine lens")
+    assert (want[:, :W] >= 0).any() and (want[:, W:] >= 0).any()
+    out, gl = ops.compute_global_topk_indices_and_lens(
+        _dev_i32(topk, d), _dev_i32(t2r, d), _dev_i32(table, d), bs,
+        torch.from_numpy(valid).to(d), base_offsets=_dev_i32(bases, d))
+    want_g, want_gl = oracle.compute_global_topk_indices_and_lens(
+        topk, t2r, table, bs, base_offsets=bases, is_valid_token=valid)
+    _assert_same(out.cpu().numpy(), want_g, "staged global top-k")
+    _assert_same(gl.cpu().numpy(), want_gl, "staged global lens")
+
+
 # ---- fused gathers (slots computed in the gather) ---------------------------------------
 
 @pytest.mark.parametrize("seed", range(12))
