@@ -88,8 +88,9 @@ int32_t psk_abi_version(void);
 
 /*
  * psk_device_wait_timeouts -- diagnostic of the pipelined kernels.
- * Kernels that wait on shared-memory barriers (the TMA-fed gather and the
- * index builders that stage top-k rows by bulk copies) bound every wait to
+ * Kernels that wait on shared-memory barriers (the TMA-fed gather, the
+ * index builders that stage top-k rows by bulk copies and the long-window
+ * compressed-row kernel of compress_kv_cache_insert) bound every wait to
  * 2 s of wall time; a wait that expires is counted in a per-device counter,
  * the kernel stops its remaining work instead of hanging, and the output of
  * that launch is incomplete.  This call copies the current device's count

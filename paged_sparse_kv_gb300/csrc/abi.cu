@@ -83,12 +83,14 @@ int32_t psk_abi_version(void) { return 2; }
 
 psk_status psk_device_wait_timeouts(uint32_t* count) {
     CHECK(count != nullptr, "count must be non-null");
-    uint32_t gather = 0, index = 0;
+    uint32_t gather = 0, index = 0, compress = 0;
     psk_status st = cuda_status(psk::read_wait_timeouts(&gather), "reading the wait-timeout counter");
     if (st != PSK_OK) return st;
     st = cuda_status(psk::read_index_wait_timeouts(&index), "reading the wait-timeout counter");
     if (st != PSK_OK) return st;
-    *count = gather + index;
+    st = cuda_status(psk::read_compress_wait_timeouts(&compress), "reading the wait-timeout counter");
+    if (st != PSK_OK) return st;
+    *count = gather + index + compress;
     return PSK_OK;
 }
 

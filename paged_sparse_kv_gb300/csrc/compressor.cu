@@ -355,7 +355,342 @@ __global__ void __launch_bounds__(THREADS) compress_kernel(CompressParams p, int
     }
 }
 
+// ---- long windows: a cluster of CTAs per token ----------------------------------------
+//
+// For windows of more than 8 rows (HCA: 128).  A cluster of kSlices CTAs
+// owns one writing token at a time; CTA k of the cluster owns columns
+// [64k, 64k + 64), one thread per column.  Its slice of every window row
+// (score and kv, 256 bytes each) is bulk-copied into shared memory in one
+// round, counted by one mbarrier, and the three softmax passes run from shared
+// memory in window order, each exp kept in place of its score for the
+// weighted pass.  The RMSNorm's pairwise sum of squares is completed across
+// the cluster: each CTA's 64-column partial (a subtree of the pairwise tree)
+// goes to its shared memory, a cluster barrier, then every CTA reads the eight
+// partials through distributed shared memory and adds them in the tree's
+// order.  CTA k < 7 writes FP8 block k of the record; CTA 7 the RoPE tail and
+// the unused scale slot.
+constexpr int kSliceCols = 64;
+constexpr int kSlices = kHead / kSliceCols;  // CTAs per cluster
+constexpr int kColThreads = 4;                 // threads per column
+constexpr int kClusterThreads = kSliceCols * kColThreads;
+constexpr int kScanWarps = kClusterThreads / kWarp;  // chunks scanned per round
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Bulk-copy waits that gave up (2 s); the CTA stops copying and leaves its
+// remaining rows unwritten.
+__device__ unsigned int g_compress_wait_timeouts = 0;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster; orders prior shared-memory
+// accesses before the peers' later ones.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The float at `local`'s offset in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// its later bulk copies into shared memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Column c of the slice through the window, by the kColThreads threads of
+// the column: thread q of it owns the contiguous rows [q W / n, (q + 1) W / n).
+//  * max: part 0 folds from row 0 as the oracle does (a NaN there stays), the
+//    other parts from -inf, and the parts combine in order with the same
+//    strict comparison -- the oracle's first maximum (NaNs skipped);
+//  * each part's exps replace its scores, then one thread of the column sums
+//    them in window order;
+//  * each part's kv * (exp / sum) products replace the exps, then one thread
+//    sums them in window order.
+// Returns the pooled value in part 0's thread (0 in the others).  Every
+// thread of the CTA calls it (it holds CTA barriers).
+__device__ __forceinline__ float slice_pool(float* s_sc, const float* s_kv, float* s_mx,
+                                            float* s_sum, int window, int c, int q) {
+    constexpr int U = 8;
+    const int j0 = q * window / kColThreads, j1 = (q + 1) * window / kColThreads;
+    float mx = q == 0 ? s_sc[c] : __int_as_float(0xFF800000);
+#pragma unroll 8
+    for (int j = (q == 0 ? 1 : j0); j < j1; ++j) {
+        const float v = s_sc[j * kSliceCols + c];
+        mx = v > mx ? v : mx;
+    }
+    s_mx[q * kSliceCols + c] = mx;
+    __syncthreads();
+    mx = s_mx[c];
+#pragma unroll
+    for (int k = 1; k < kColThreads; ++k) {
+        const float v = s_mx[k * kSliceCols + c];
+        mx = v > mx ? v : mx;
+    }
+    int j = j0;
+    for (; j + U <= j1; j += U) {
+        float e[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) e[u] = cw_exp(__fsub_rn(s_sc[(j + u) * kSliceCols + c], mx));
+#pragma unroll
+        for (int u = 0; u < U; ++u) s_sc[(j + u) * kSliceCols + c] = e[u];
+    }
+    for (; j < j1; ++j) s_sc[j * kSliceCols + c] = cw_exp(__fsub_rn(s_sc[j * kSliceCols + c], mx));
+    __syncthreads();
+    if (q == 0) {
+        float sum = 0.0f;
+#pragma unroll 8
+        for (int k = 0; k < window; ++k) sum = __fadd_rn(sum, s_sc[k * kSliceCols + c]);
+        s_sum[c] = sum;
+    }
+    __syncthreads();
+    const float sum = s_sum[c];
+    j = j0;
+    for (; j + U <= j1; j += U) {
+        float pr[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            pr[u] = __fmul_rn(s_kv[(j + u) * kSliceCols + c],
+                              __fdiv_rn(s_sc[(j + u) * kSliceCols + c], sum));
+#pragma unroll
+        for (int u = 0; u < U; ++u) s_sc[(j + u) * kSliceCols + c] = pr[u];
+    }
+    for (; j < j1; ++j)
+        s_sc[j * kSliceCols + c] =
+            __fmul_rn(s_kv[j * kSliceCols + c], __fdiv_rn(s_sc[j * kSliceCols + c], sum));
+    __syncthreads();
+    float acc = 0.0f;
+    if (q == 0) {
+#pragma unroll 8
+        for (int k = 0; k < window; ++k) acc = __fadd_rn(acc, s_sc[k * kSliceCols + c]);
+    }
+    return acc;
+}
+
+// Warp 0: the writing tokens among c0 .. c0 + 31 into s_list (ascending),
+// their number into s_count; skips counted when `count_errors`.
+__device__ __forceinline__ void scan_chunk(const CompressParams& p, int64_t c0, bool count_errors,
+                                           int64_t* s_list, int* s_count) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = c0 + lane;
+    bool emit = false;
+    if (t < p.num_tokens) {
+        const int64_t ss = __ldg(p.state_slots + t), ks = __ldg(p.kv_slots + t);
+        const int64_t pos = __ldg(p.positions + t);
+        if (ss >= 0 && ks >= 0) {
+            int64_t rem = (pos + 1) % p.ratio;
+            if (rem < 0) rem += p.ratio;
+            if (rem == 0) {
+                int64_t grp = pos / p.ratio;
+                if (pos % p.ratio != 0 && pos < 0) grp -= 1;
+                const int64_t prow = grp * p.ratio;
+                const int32_t r = __ldg(p.t2r + t);
+                if (ks >= p.kv_pages * (int64_t)p.kv_bs || prow < 0 || prow >= p.max_pos ||
+                    r < 0 || r >= p.num_reqs) {
+                    if (count_errors && p.err_count) atomicAdd(p.err_count, 1);
+                } else {
+                    emit = true;
+                }
+            }
+        }
+    }
+    const unsigned mask = __ballot_sync(0xFFFFFFFFu, emit);
+    if (emit) s_list[__popc(mask & ((1u << lane) - 1u))] = t;
+    if (lane == 0) *s_count = __popc(mask);
+}
+
+// State row of window entry j of token t (-1: absent), as the oracle forms it.
+__device__ __forceinline__ int64_t window_row(const CompressParams& p, int64_t pos, int32_t r,
+                                              int64_t base, int window, int j) {
+    const int64_t ps = pos - window + 1 + j;
+    if (ps < 0) return -1;
+    const int64_t lp = ps / p.state_bs - base;
+    if (lp < 0 || lp >= p.bt_width) return -1;
+    const int32_t entry = __ldg(p.bt + (int64_t)r * p.bt_stride + lp);
+    if (entry < 0) return -1;
+    const int64_t sr = (int64_t)entry * p.state_bs + ps % p.state_bs;
+    return sr < p.state_pages * (int64_t)p.state_bs ? sr : -1;
+}
+
+// Column col0 + tid of the normalised row into token t's record: CTA k < 7
+// FP8 block k (amax over the block's 64 bf16 values, the UE8M0 exponent),
+// CTA 7 the GPT-J RoPE tail as bf16 and the unused scale slot.  The branch is
+// uniform over the CTA.  Nothing is stored when `skip`.
+__device__ __forceinline__ void slice_epilogue(const CompressParams& p, int32_t kv_shift, int64_t t,
+                                               int64_t pos, uint32_t rank, float y,
+                                               uint32_t* s_amax, bool owner, bool skip) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    skip = skip || !owner;  // threads 0..63 (warps 0 and 1) own the columns
+    const int64_t ks = __ldg(p.kv_slots + t);
+    int64_t off;
+    const int64_t page = div_block(ks, p.kv_bs, kv_shift, off);
+    constexpr int kTS = kNope + 2 * kRope;  // 576 data bytes per token
+    uint8_t* pbase = p.kv_cache + page * p.kv_page_stride;
+    uint8_t* data = pbase + off * kTS;
+    uint8_t* scl = pbase + (int64_t)p.kv_bs * kTS + off * (kHead / 64);
+    if ((int)rank < kNope / kSliceCols) {
+        const uint32_t b = pack_bf16x2(y, 0.0f) & 0xFFFFu;
+        uint32_t amb = b & 0x7FFFu;
+#pragma unroll
+        for (int m = 1; m < kWarp; m <<= 1) amb = max(amb, __shfl_xor_sync(0xFFFFFFFFu, amb, m));
+        if (owner && lane == 0) s_amax[warp] = amb;
+        __syncthreads();
+        amb = max(s_amax[0], s_amax[1]);
+        const float a = fmaxf(__uint_as_float(amb << 16), 1.0e-4f);
+        const int e = ceil_log2_div_const(a, 0x600000u, 8);  // / 448
+        const uint32_t q = cvt_e4m3x2(__fmul_rn(__uint_as_float(b << 16), exp2_int(-e)), 0.0f) & 0xFFu;
+        if (!skip) {
+            data[kSliceCols * rank + tid] = (uint8_t)q;
+            if (tid == 0) scl[rank] = (uint8_t)min(max(e + 127, 0), 255);
+        }
+    } else {  // GPT-J RoPE at the group's first position: pairs (2i, 2i + 1) of the tail
+        int64_t grp = pos / p.ratio;
+        if (pos % p.ratio != 0 && pos < 0) grp -= 1;
+        const float* cs = p.cos_sin + grp * p.ratio * p.cs_stride;
+        const float other = __shfl_xor_sync(0xFFFFFFFFu, y, 1);
+        const bool odd = tid & 1;
+        const float ev = odd ? other : y, od = odd ? y : other;
+        const int i = (tid & (kSliceCols - 1)) >> 1;
+        const float c = __ldg(cs + i), sn = __ldg(cs + kRope / 2 + i);
+        const float v = odd ? __fadd_rn(__fmul_rn(ev, sn), __fmul_rn(od, c))
+                            : __fsub_rn(__fmul_rn(ev, c), __fmul_rn(od, sn));
+        if (!skip) {
+            *reinterpret_cast<uint16_t*>(data + kNope + 2 * tid) = (uint16_t)(pack_bf16x2(v, 0.0f) & 0xFFFFu);
+            if (tid == 0) scl[kNope / 64] = 0;  // the unused scale slot
+        }
+    }
+}
+
+__global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kClusterThreads)
+compress_cluster_kernel(CompressParams p, int32_t kv_shift) {
+    // [window][64] scores (then exps, then products), [window][64] kv
+    extern __shared__ __align__(16) float s_dyn[];
+    __shared__ float s_mx[kColThreads * kSliceCols];
+    __shared__ float s_sum[kSliceCols];
+    __shared__ float s_part[kSliceCols / kWarp];
+    __shared__ float s_ssq[2];  // this CTA's partial, by token parity (read by the cluster)
+    __shared__ uint32_t s_amax[kSliceCols / kWarp];
+    __shared__ int s_nrows[kScanWarps];
+    __shared__ int64_t s_list[kScanWarps * kWarp];
+    __shared__ int s_count[kScanWarps];
+    __shared__ __align__(8) uint64_t s_bar;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = tid % kSliceCols, q = tid / kSliceCols;  // column, part of the window
+    const bool owner = q == 0;  // threads 0..63: the column's sums, RMSNorm and record
+    const uint32_t rank = cluster_ctarank();
+    const int col0 = kSliceCols * (int)rank;
+    const int window = (p.overlap ? 2 : 1) * p.ratio;
+    float* s_sc = s_dyn;
+    float* s_kv = s_dyn + window * kSliceCols;
+    if (tid == 0) {
+        mbar_init(&s_bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t nclusters = gridDim.x / kSlices;
+    const int64_t cl = blockIdx.x / kSlices;
+    int tok = 0;        // tokens begun by this CTA (mbarrier phase and s_ssq parity)
+    bool dead = false;  // a copy wait gave up: no further copies or waits
+    int dead_tok = 0;   // the token whose wait gave up
+    // The cluster's chunks are cl, cl + nclusters, ...; each round, warp w
+    // scans the round's w-th.  Every CTA of the cluster scans the same chunks;
+    // rank 0 counts the skips.
+    for (int64_t i0 = 0; (cl + i0 * nclusters) * kWarp < p.num_tokens; i0 += kScanWarps) {
+        scan_chunk(p, (cl + (i0 + warp) * nclusters) * kWarp, rank == 0, s_list + warp * kWarp,
+                   &s_count[warp]);
+        __syncthreads();
+        for (int w = 0; w < kScanWarps; ++w) {
+            const int nw = s_count[w];
+            for (int i = 0; i < nw; ++i, ++tok) {
+                const int64_t t = s_list[w * kWarp + i];
+                const int64_t pos = __ldg(p.positions + t);
+                const int32_t r = __ldg(p.t2r + t);
+                const int64_t base = p.base ? __ldg(p.base + r) : 0;
+                // this CTA's slices of the window rows: bulk copies, absent rows filled
+                int nrows = 0;
+                if (!dead) {
+                    fence_proxy_async_smem();
+                    for (int j = tid; j < window; j += kClusterThreads) {
+                        const int64_t row = window_row(p, pos, r, base, window, j);
+                        if (row >= 0) {
+                            const int off = (p.overlap && j >= p.ratio) ? kHead : 0;
+                            const float* src = p.state + row * 2 * (int64_t)p.state_width + off + col0;
+                            bulk_g2s(s_kv + j * kSliceCols, src, kSliceCols * 4, &s_bar);
+                            bulk_g2s(s_sc + j * kSliceCols, src + p.state_width, kSliceCols * 4, &s_bar);
+                            ++nrows;
+                        } else {
+                            for (int k = 0; k < kSliceCols; ++k) {
+                                s_sc[j * kSliceCols + k] = -1.0e30f;
+                                s_kv[j * kSliceCols + k] = 0.0f;
+                            }
+                        }
+                    }
+                }
+                nrows = __reduce_add_sync(0xFFFFFFFFu, nrows);
+                if (lane == 0) s_nrows[warp] = nrows;
+                __syncthreads();
+                if (!dead && tid == 0) {
+                    int total = 0;
+                    for (int k = 0; k < kScanWarps; ++k) total += s_nrows[k];
+                    mbar_arrive_expect_tx(&s_bar, (uint32_t)total * 2u * kSliceCols * 4u);
+                }
+                const bool landed =
+                    dead ? false : mbar_wait_bounded(&s_bar, (uint32_t)(tok & 1), kWaitLimitNs);
+                if (!dead && !__syncthreads_and(landed)) {
+                    if (tid == 0) atomicAdd(&g_compress_wait_timeouts, 1u);
+                    dead = true;
+                    dead_tok = tok;
+                }
+                // pooling, then this CTA's part of the pairwise sum of squares
+                const float acc = dead ? 0.0f : slice_pool(s_sc, s_kv, s_mx, s_sum, window, c, q);
+                float ssq = __fmul_rn(acc, acc);
+#pragma unroll
+                for (int m = 1; m < kWarp; m <<= 1)
+                    ssq = __fadd_rn(ssq, __shfl_xor_sync(0xFFFFFFFFu, ssq, m));
+                if (owner && lane == 0) s_part[warp] = ssq;
+                __syncthreads();
+                if (tid == 0) s_ssq[tok & 1] = __fadd_rn(s_part[0], s_part[1]);
+                cluster_sync_all();
+                float part[kSlices];
+#pragma unroll
+                for (int k = 0; k < kSlices; ++k) part[k] = ld_cluster_f32(&s_ssq[tok & 1], (uint32_t)k);
+#pragma unroll
+                for (int h = kSlices / 2; h >= 1; h >>= 1)
+#pragma unroll
+                    for (int k = 0; k < h; ++k) part[k] = __fadd_rn(part[2 * k], part[2 * k + 1]);
+                const float variance = __fmul_rn(part[0], 1.0f / kHead);  // exact: a power of two
+                const float rr = __frcp_rn(__fsqrt_rn(__fadd_rn(variance, p.eps)));
+                const float y = __fmul_rn(__fmul_rn(acc, rr), __ldg(p.weight + col0 + c));
+                slice_epilogue(p, kv_shift, t, pos, rank, y, s_amax, owner, dead);
+                __syncthreads();  // the slices are read before the next token's copies
+            }
+        }
+        __syncthreads();  // every thread has read s_count / s_list before the next scan
+    }
+    // no CTA leaves while a peer may read its partial; copies of a CTA whose
+    // wait gave up are waited for (bounded) before it retires
+    cluster_sync_all();
+    if (dead && tid == 0) mbar_wait_bounded(&s_bar, (uint32_t)(dead_tok & 1), kWaitLimitNs);
+}
+
 }  // namespace
+
+cudaError_t read_compress_wait_timeouts(uint32_t* count) {
+    return cudaMemcpyFromSymbol(count, g_compress_wait_timeouts, sizeof(uint32_t));
+}
 
 cudaError_t launch_save_compressor_state(const SaveStateParams& p, cudaStream_t stream) {
     const int64_t blocks = (p.num_tokens * kWarp + kThreads - 1) / kThreads;
@@ -378,8 +713,29 @@ cudaError_t launch_compress_kv_insert(const CompressParams& p, cudaStream_t stre
         auto kern = compress_kernel<128, true>;
         return launch_pdl(kern, grid_for(kern, 128), dim3(128), 0, stream, p, shift);
     }
-    auto kern = compress_kernel<512, false>;
-    return launch_pdl(kern, grid_for(kern, 512), dim3(512), 0, stream, p, shift);
+    // longer windows: clusters of kSlices CTAs, as many as can be resident
+    auto kern = compress_cluster_kernel;
+    const size_t smem = (size_t)window * kSliceCols * 2 * sizeof(float);
+    static bool attr_set = false;
+    if (!attr_set) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)(kMaxWindow * kSliceCols * 2 * sizeof(float)));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kSlices);
+    cfg.blockDim = dim3(kClusterThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess || max_clusters < 1)
+        max_clusters = 1;
+    const int64_t per_round = (int64_t)kScanWarps;
+    const int64_t want = (chunks + per_round - 1) / per_round;
+    const int64_t clusters = want < max_clusters ? want : max_clusters;
+    return launch_pdl(kern, dim3((unsigned)(clusters * kSlices)), dim3(kClusterThreads), smem, stream,
+                      p, shift);
 }
 
 }  // namespace psk

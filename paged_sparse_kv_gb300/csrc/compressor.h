@@ -54,4 +54,7 @@ struct CompressParams {
 
 cudaError_t launch_compress_kv_insert(const CompressParams& p, cudaStream_t stream);
 
+// Copies of the long-window kernel whose bounded wait gave up.
+cudaError_t read_compress_wait_timeouts(uint32_t* count);
+
 }  // namespace psk
