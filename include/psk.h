@@ -100,6 +100,19 @@ int32_t psk_abi_version(void);
 psk_status psk_device_wait_timeouts(uint32_t* count);
 
 /*
+ * psk_device_wait_selftest -- exercises the failure path of those bounded
+ * waits (the pages have no counterpart; a diagnostic of this library).  One
+ * thread of a one-warp kernel waits on a shared-memory barrier that nothing
+ * completes; after limit_ns (1e3 .. 1e9 ns) of wall time the wait gives up,
+ * the expiry is counted as in the pipelined kernels (psk_device_wait_timeouts
+ * rises by one when the kernel has run) and the kernel returns normally, so the
+ * context and the stream stay usable.  Asynchronous on `stream`.  Errors:
+ * PSK_ERR_INVALID_ARGUMENT for a limit outside the range, PSK_ERR_CUDA if the
+ * launch fails.
+ */
+psk_status psk_device_wait_selftest(uint64_t limit_ns, psk_stream_t stream);
+
+/*
  * quantize_and_insert_k_cache -- block-scaled FP8 quantize + paged insert.
  * [VLLM] quantize_and_insert_k_cache; math of [OPS] _fp8_ds_mla_cache_rows.
  *

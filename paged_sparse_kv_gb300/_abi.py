@@ -33,6 +33,7 @@ SIGNATURES = {
     "psk_last_error": (ctypes.c_char_p, []),
     "psk_abi_version": (_I32, []),
     "psk_device_wait_timeouts": (_I32, [_P]),
+    "psk_device_wait_selftest": (_I32, [ctypes.c_uint64, _P]),
     "quantize_and_insert_k_cache": (
         _I32, [_P, _I64, _P, _I64, _P, _I64, _I64, _I32, _I32, _I32, _I32, _P, _P]),
     "write_indexer_mxfp4_cache": (

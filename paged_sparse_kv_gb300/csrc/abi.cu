@@ -79,7 +79,7 @@ extern "C" {
 
 const char* psk_last_error(void) { return g_last_error.c_str(); }
 
-int32_t psk_abi_version(void) { return 2; }
+int32_t psk_abi_version(void) { return 3; }
 
 psk_status psk_device_wait_timeouts(uint32_t* count) {
     CHECK(count != nullptr, "count must be non-null");
@@ -92,6 +92,12 @@ psk_status psk_device_wait_timeouts(uint32_t* count) {
     if (st != PSK_OK) return st;
     *count = gather + index + compress;
     return PSK_OK;
+}
+
+psk_status psk_device_wait_selftest(uint64_t limit_ns, psk_stream_t stream) {
+    CHECK(limit_ns >= 1000 && limit_ns <= 1000000000ull, "limit_ns must be in [1e3, 1e9]");
+    return cuda_status(psk::launch_wait_selftest(limit_ns, reinterpret_cast<cudaStream_t>(stream)),
+                       "psk_device_wait_selftest launch");
 }
 
 psk_status quantize_and_insert_k_cache(const void* k, int64_t k_row_stride,

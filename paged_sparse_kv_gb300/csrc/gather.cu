@@ -519,10 +519,26 @@ cudaError_t gather_small_by_dim(const GatherParams& p, const TopkSource& tk, cud
     }
 }
 
+// Failure-path check of the bounded wait: one thread waits on a barrier that
+// nothing completes, gives up after limit_ns and counts the expiry exactly as
+// the pipelined kernels do; the kernel then returns normally.
+__global__ void wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    if (!mbar_wait_bounded(&bar, 0, limit_ns)) atomicAdd(&g_wait_timeouts, 1u);
+}
+
 }  // namespace
 
 cudaError_t read_wait_timeouts(uint32_t* count) {
     return cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(uint32_t));
+}
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, kWarp, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gather(const GatherParams& params, cudaStream_t stream) {

@@ -111,4 +111,7 @@ cudaError_t launch_gather_window(const GatherParams& p, const WindowSource& s,
 // Count of expired bounded waits in the gather kernels.
 cudaError_t read_wait_timeouts(uint32_t* count);
 
+// One bounded wait on a barrier nothing completes (counted when it expires).
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
+
 }  // namespace psk

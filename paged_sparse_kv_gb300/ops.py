@@ -495,3 +495,13 @@ def dequantize_and_gather_k_cache_window(out: torch.Tensor, cache: torch.Tensor,
               block_table.shape[1], _ptr(base_offsets), window_size, _ptr(valid),
               _stream(out.device))
     return out
+
+
+def device_wait_timeouts() -> int:
+    """Expired in-kernel bounded waits on the current device (0 in normal operation)."""
+    return _abi.device_wait_timeouts()
+
+
+def device_wait_selftest(limit_ns: int, device: torch.device) -> None:
+    """Launch one bounded wait that nothing completes (counted when it expires)."""
+    _abi.call("psk_device_wait_selftest", int(limit_ns), _stream(device))

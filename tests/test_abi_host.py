@@ -437,3 +437,8 @@ def test_gather_window_rejects_bad_arguments(psk_lib, kw):
 def test_gather_window_zero_work_ok(psk_lib):
     assert _gather_window(T=0, out=None, qsl=None, seq=None, t2r=None) == OK
     assert _gather_window(W=0, out=None, qsl=None, seq=None, t2r=None) == OK
+
+
+@pytest.mark.parametrize("limit", [0, 999, 10**9 + 1, 2**63])
+def test_wait_selftest_rejects_bad_limit(psk_lib, limit):
+    assert _abi.status("psk_device_wait_selftest", limit, None) == INV
