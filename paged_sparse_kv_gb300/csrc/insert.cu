@@ -404,8 +404,14 @@ __device__ __forceinline__ void nrs_resolve(const NormRopeParams& p, int64_t t, 
         const uint32_t ratio = (uint32_t)p.ratio;
         bool boundary;
         if (pos >= 0 && pos < 0xFFFFFFFFll) {
-            const uint32_t q = (uint32_t)pos / ratio;
-            boundary = (uint32_t)pos - q * ratio == ratio - 1u;
+            uint32_t q;
+            if (p.ratio_shift >= 0) {  // power-of-two ratio: shift and mask
+                q = (uint32_t)pos >> p.ratio_shift;
+                boundary = ((uint32_t)pos & (ratio - 1u)) == ratio - 1u;
+            } else {
+                q = (uint32_t)pos / ratio;
+                boundary = (uint32_t)pos - q * ratio == ratio - 1u;
+            }
             k.prow = (int64_t)q * ratio;
         } else {
             int64_t rem = (pos + 1) % p.ratio;
@@ -456,16 +462,18 @@ __device__ __forceinline__ void nrs_compute_store(const NormRopeParams& p, int32
                                                   const NormRopeKey& k) {
     constexpr int LPT = 8;
     const bool act = k.act;
+    // (an inactive key's values are whatever was loaded: its lanes reduce only
+    // among themselves and store nothing)
     float ya[8], yb[8];
     {
         const uint32_t wa[4] = {k.ka.x, k.ka.y, k.ka.z, k.ka.w};
         const uint32_t wb[4] = {k.kb.x, k.kb.y, k.kb.z, k.kb.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            ya[2 * i] = act ? bf16_lo(wa[i]) : 0.0f;
-            ya[2 * i + 1] = act ? bf16_hi(wa[i]) : 0.0f;
-            yb[2 * i] = act ? bf16_lo(wb[i]) : 0.0f;
-            yb[2 * i + 1] = act ? bf16_hi(wb[i]) : 0.0f;
+            ya[2 * i] = bf16_lo(wa[i]);
+            ya[2 * i + 1] = bf16_hi(wa[i]);
+            yb[2 * i] = bf16_lo(wb[i]);
+            yb[2 * i + 1] = bf16_hi(wb[i]);
         }
     }
     // pairwise sum of squares of each chunk (8 -> 4 -> 2 -> 1), then over the
@@ -666,7 +674,9 @@ cudaError_t launch_norm_rope_store(const NormRopeParams& p, cudaStream_t stream)
         {{norm_rope_store_kernel<true, false, false, U>, norm_rope_store_kernel<true, false, true, U>},
          {norm_rope_store_kernel<true, true, false, U>, norm_rope_store_kernel<true, true, true, U>}}};
     const Kern kern = kTable[p.record == 1][every][cs_vec];
-    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p, shift);
+    NormRopeParams q = p;
+    q.ratio_shift = log2_if_pow2(p.ratio);
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, q, shift);
 }
 
 cudaError_t launch_fp8_insert(const InsertParams& p, cudaStream_t stream) {

@@ -45,6 +45,7 @@ struct NormRopeParams {
     int64_t page_stride;
     int32_t block_size;
     int32_t* err_count;
+    int32_t ratio_shift;      // log2(ratio) for a power-of-two ratio, else -1 (launcher)
 };
 
 cudaError_t launch_norm_rope_store(const NormRopeParams& p, cudaStream_t stream);

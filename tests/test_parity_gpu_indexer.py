@@ -92,7 +92,7 @@ def _gptj_table(max_pos, dtype=np.float32):
 
 @pytest.mark.parametrize("cs_pad", [0, 3])
 @pytest.mark.parametrize("fp4", [True, False])
-@pytest.mark.parametrize("ratio", [1, 2, 4])
+@pytest.mark.parametrize("ratio", [1, 2, 3, 4])
 @pytest.mark.parametrize("bs", [64, 3])
 def test_norm_rope_store_fuzz(cuda_device, fp4, ratio, bs, cs_pad):
     rng = np.random.default_rng(100 * ratio + bs + fp4)
@@ -115,7 +115,8 @@ def test_norm_rope_store_fuzz(cuda_device, fp4, ratio, bs, cs_pad):
     # two counted skips: a slot beyond the cache and a RoPE row beyond max_pos,
     # both on group boundaries
     pos[11], slots[11] = 5 * ratio - 1, pages * bs + 1
-    pos[13], slots[13] = max_pos + ratio - 1, pages * bs + 2
+    # the first group-closing position whose RoPE row floor(p / ratio) * ratio >= max_pos
+    pos[13], slots[13] = (-(-max_pos // ratio) + 1) * ratio - 1, pages * bs + 2
     cs = _gptj_table(max_pos)
     cs_dev = np.zeros((max_pos, 64 + cs_pad), np.float32)  # stride 67: scalar cos/sin loads
     cs_dev[:, :64] = cs
