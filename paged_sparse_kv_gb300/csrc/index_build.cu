@@ -45,6 +45,9 @@ namespace {
 #ifndef PSK_INDEX_SB_UNROLL
 #define PSK_INDEX_SB_UNROLL 1
 #endif
+#ifndef PSK_INDEX_WARPS_PER_SM
+#define PSK_INDEX_WARPS_PER_SM 16  // split a token over warps below this many token-warps per SM
+#endif
 #ifndef PSK_INDEX_MIN_CTAS
 #define PSK_INDEX_MIN_CTAS 3
 #endif
@@ -930,7 +933,7 @@ cudaError_t launch_index_build(IndexParams p, bool has_swa, cudaStream_t stream)
     const int64_t T = p.num_tokens;
     // Split a token over several warps when the batch is too small to fill
     // every SM with one warp per token.
-    const int64_t want_warps = (int64_t)sms * 16;
+    const int64_t want_warps = (int64_t)sms * PSK_INDEX_WARPS_PER_SM;
     int wpt = 1;
     while (wpt < kWarps && T * wpt < want_warps) wpt *= 2;
     const int tpp = kWarps / wpt;
