@@ -308,6 +308,7 @@ KERNEL_SOURCES = {
     "dequantize_and_gather_k_cache_ranges": _FAMILY["gather"],
     "dequantize_and_gather_k_cache_topk": _FAMILY["gather"],
     "dequantize_and_gather_k_cache_window": _FAMILY["gather"],
+    "dequantize_and_gather_k_cache_pair": _FAMILY["gather"],
     "indexer_mxfp4_paged_gather": _FAMILY["gather"],
 }
 SHARED_SOURCES = ("psk_common.cuh", "launch.h")
@@ -470,6 +471,11 @@ def main():
         if w.has_fp8:
             outputs["sparse_indices"] = p.sparse_indices.cpu().numpy()
         alg = algorithmic_bytes(p, outputs)
+        if path == "index" and "dequantize_and_gather_k_cache_pair" in names:
+            # one launch over both column ranges: the two parts' bytes
+            alg["dequantize_and_gather_k_cache_pair"] = (
+                alg.pop("dequantize_and_gather_k_cache[swa]") +
+                alg.pop("dequantize_and_gather_k_cache[topk]"))
         if path == "fused":
             # the fused gathers move the same rows; the top-k forms read a top-k
             # entry per item where the index form read a slot id, the window form

@@ -605,6 +605,32 @@ psk_status dequantize_and_gather_k_cache_window(
     const int32_t* base_offsets, int32_t window, const uint8_t* is_valid_token,
     psk_stream_t stream);
 
+/*
+ * dequantize_and_gather_k_cache_pair -- one index matrix read against two
+ * fp8_ds_mla caches of the same record format: columns j < split take their
+ * slots in cache_a, columns j >= split in cache_b.  This is how the decode
+ * attention reads the combined matrix of combine_topk_swa_indices against
+ * the SWA cache (window columns) and the compressed cache (top-k columns),
+ * [BE] forward_deepseek_v4_decode (k_cache with extra_k_cache); the output
+ * equals dequantize_and_gather_k_cache over columns [0, split) of cache_a and
+ * over columns [split, cols) of cache_b, in one launch.  UE8M0 scales; each
+ * cache has its own pages, page stride and block size; slots outside a cache
+ * give zero rows as in dequantize_and_gather_k_cache.
+ *
+ *   out      bf16 rows (t, j) at out + t*out_stride_t + j*out_stride_j,
+ *            j < cols (elements, multiples of 8; 16-byte aligned).
+ *   indices  int32 [rows, idx_stride], idx_stride >= cols.
+ *   split    0 <= split <= cols.
+ *   Errors: PSK_ERR_INVALID_ARGUMENT as dequantize_and_gather_k_cache, for
+ *   either cache; PSK_ERR_CUDA if the launch fails.
+ */
+psk_status dequantize_and_gather_k_cache_pair(
+    void* out, int64_t out_stride_t, int64_t out_stride_j, const uint8_t* cache_a,
+    int64_t num_pages_a, int64_t page_stride_a, int32_t block_size_a, const uint8_t* cache_b,
+    int64_t num_pages_b, int64_t page_stride_b, int32_t block_size_b, int32_t head_dim,
+    int32_t rope_dim, const int32_t* indices, int64_t idx_stride, int64_t rows, int32_t cols,
+    int32_t split, psk_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

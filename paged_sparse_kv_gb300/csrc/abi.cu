@@ -79,7 +79,7 @@ extern "C" {
 
 const char* psk_last_error(void) { return g_last_error.c_str(); }
 
-int32_t psk_abi_version(void) { return 3; }
+int32_t psk_abi_version(void) { return 4; }
 
 psk_status psk_device_wait_timeouts(uint32_t* count) {
     CHECK(count != nullptr, "count must be non-null");
@@ -760,6 +760,40 @@ psk_status dequantize_and_gather_k_cache_window(
                          num_reqs, block_table, bt_stride, bt_width, base_offsets};
     return cuda_status(psk::launch_gather_window(p, wn, reinterpret_cast<cudaStream_t>(stream)),
                        "dequantize_and_gather_k_cache_window launch");
+}
+
+psk_status dequantize_and_gather_k_cache_pair(
+    void* out, int64_t out_stride_t, int64_t out_stride_j, const uint8_t* cache_a,
+    int64_t num_pages_a, int64_t page_stride_a, int32_t block_size_a, const uint8_t* cache_b,
+    int64_t num_pages_b, int64_t page_stride_b, int32_t block_size_b, int32_t head_dim,
+    int32_t rope_dim, const int32_t* indices, int64_t idx_stride, int64_t rows, int32_t cols,
+    int32_t split, psk_stream_t stream) {
+    CHECK(rows >= 0 && cols >= 0, "rows and cols must be >= 0");
+    CHECK(split >= 0 && split <= cols, "need 0 <= split <= cols");
+    CHECK(fp8_head_dim_ok(head_dim),
+          "head_dim must be one of 64, 128, 256, 512, 1024 (got %d)", head_dim);
+    CHECK(rope_dim >= 0 && rope_dim < head_dim && rope_dim % 64 == 0,
+          "rope_dim must be a multiple of 64 in [0, head_dim) (got %d)", rope_dim);
+    const int64_t rec_bytes = fp8_record_bytes(head_dim, rope_dim, 1);
+    psk_status st = check_cache(cache_a, num_pages_a, page_stride_a, block_size_a, rec_bytes);
+    if (st != PSK_OK) return st;
+    st = check_cache(cache_b, num_pages_b, page_stride_b, block_size_b, rec_bytes);
+    if (st != PSK_OK) return st;
+    CHECK(idx_stride >= cols, "idx_stride must be >= cols");
+    if (rows == 0 || cols == 0) return ok();
+    CHECK(out != nullptr && indices != nullptr, "out and indices must be non-null");
+    CHECK(aligned(out, 16), "out must be 16-byte aligned");
+    CHECK(out_stride_t >= 0 && out_stride_j >= 0 && out_stride_t % 8 == 0 &&
+              out_stride_j % 8 == 0,
+          "output strides must be non-negative multiples of 8 elements");
+    CHECK(aligned(indices, 4), "indices must be 4-byte aligned");
+    CHECK(rows <= INT64_MAX / cols, "rows * cols overflows");
+    psk::GatherParams p{static_cast<uint16_t*>(out), out_stride_t, out_stride_j, cache_a,
+                        num_pages_a, page_stride_a, block_size_a, 0, head_dim, rope_dim, 1,
+                        indices, idx_stride, rows, cols};
+    psk::PairSource pr{cache_b, num_pages_b, page_stride_b, block_size_b, -1, split};
+    return cuda_status(psk::launch_gather_pair(p, pr, reinterpret_cast<cudaStream_t>(stream)),
+                       "dequantize_and_gather_k_cache_pair launch");
 }
 
 }  // extern "C"

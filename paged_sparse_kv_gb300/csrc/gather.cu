@@ -64,13 +64,14 @@ __device__ __forceinline__ void item_to_tj(int64_t item, int32_t cols, bool smal
 // request's position range through its block-table row (RANGE form), a
 // token's local top-k index through its request's table (TOPK form) or a
 // token's window position through the SWA table (WINDOW form).
-enum : int { kSrcIndex = 0, kSrcRange = 1, kSrcTopk = 2, kSrcWindow = 3 };
+enum : int { kSrcIndex = 0, kSrcRange = 1, kSrcTopk = 2, kSrcWindow = 3, kSrcPair = 4 };
 
 struct ItemSource {
     GatherParams g;      // index form (and cache geometry and output for every form)
     RangeParams r;       // range form
     TopkSource tk;       // top-k form
     WindowSource wn;     // window form
+    PairSource pr;       // pair form: index form over two caches split by column
 };
 
 // Slot of position p through one table row (the block-table rule), or -1.
@@ -151,6 +152,7 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
     const int64_t items = RANGE ? (int64_t)src.r.num_reqs * span : p.rows * (int64_t)p.cols;
     const int64_t tiles = (items + kRowsPerTile - 1) / kRowsPerTile;
     const int64_t capacity = p.num_pages * (int64_t)p.block_size;
+    const int64_t capacity2 = SRC == kSrcPair ? src.pr.num_pages * (int64_t)src.pr.block_size : 0;
     const bool small = items <= 0xFFFFFFFFll && span <= 0x7FFFFFFFll;
     const int nope = D - p.rope_dim;
     const int ts = nope + 2 * p.rope_dim;
@@ -178,12 +180,14 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
         for (int64_t base = blockIdx.x; base < tiles && ok; base += (int64_t)kLoadTiles * gridDim.x) {
             int32_t slot[kLoadTiles / 2];
             int64_t oof[kLoadTiles / 2];
+            bool second[kLoadTiles / 2];  // PAIR form: the item reads the second cache
 #pragma unroll
             for (int q = 0; q < kLoadTiles / 2; ++q) {
                 const int64_t tile = base + (int64_t)(2 * q + half) * gridDim.x;
                 const int64_t item = tile * kRowsPerTile + r;
                 slot[q] = -1;
                 oof[q] = 0;
+                second[q] = false;
                 if (tile < tiles && item < items) {
                     int64_t t;
                     int32_t j;
@@ -208,6 +212,11 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
                         } else if (SRC == kSrcWindow) {
                             slot[q] = window_item_slot(src.wn, p.cols, bs, p.block_shift, capacity,
                                                        t, j);
+                        } else if (SRC == kSrcPair) {
+                            second[q] = j >= src.pr.split;
+                            const int64_t cap = second[q] ? capacity2 : capacity;
+                            const int32_t raw = __ldg(p.idx + t * p.idx_stride + j);
+                            slot[q] = (raw >= 0 && (int64_t)raw < cap) ? raw : -1;
                         } else {
                             const int32_t raw = __ldg(p.idx + t * p.idx_stride + j);
                             slot[q] = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
@@ -235,11 +244,14 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
                 uint32_t scl_bytes = 0;
                 int32_t soff = -1;
                 if (sl >= 0) {
+                    const bool sec = SRC == kSrcPair && mine && second[k / 2];
+                    const int32_t cbs = sec ? src.pr.block_size : bs;
                     int32_t off;
-                    const int32_t page = div_block32(sl, bs, p.block_shift, off);
-                    const uint8_t* pbase = p.cache + (int64_t)page * p.page_stride;
+                    const int32_t page = div_block32(sl, cbs, sec ? src.pr.block_shift : p.block_shift, off);
+                    const uint8_t* pbase = (sec ? src.pr.cache : p.cache) +
+                                           (int64_t)page * (sec ? src.pr.page_stride : p.page_stride);
                     src_data = pbase + (int64_t)off * ts;
-                    const uintptr_t a = reinterpret_cast<uintptr_t>(pbase + (int64_t)bs * ts + (int64_t)off * SDIM);
+                    const uintptr_t a = reinterpret_cast<uintptr_t>(pbase + (int64_t)cbs * ts + (int64_t)off * SDIM);
                     const uintptr_t a0 = a & ~(uintptr_t)15, a1 = (a + SDIM + 15) & ~(uintptr_t)15;
                     src_scl = reinterpret_cast<const uint8_t*>(a0);
                     scl_bytes = (uint32_t)(a1 - a0);
@@ -577,6 +589,18 @@ cudaError_t launch_gather_window(const GatherParams& params, const WindowSource&
     src.g = p;
     src.wn = wn;
     return fp8_by_dim<kSrcWindow>(src, p.rows * (int64_t)p.cols, stream);
+}
+
+cudaError_t launch_gather_pair(const GatherParams& params, const PairSource& pr,
+                               cudaStream_t stream) {
+    GatherParams p = params;
+    p.block_shift = log2_if_pow2(p.block_size);
+    if (p.record != 0) return cudaErrorInvalidValue;
+    ItemSource src{};
+    src.g = p;
+    src.pr = pr;
+    src.pr.block_shift = log2_if_pow2(pr.block_size);
+    return fp8_by_dim<kSrcPair>(src, p.rows * (int64_t)p.cols, stream);
 }
 
 cudaError_t launch_gather_ranges(const RangeParams& r, cudaStream_t stream) {

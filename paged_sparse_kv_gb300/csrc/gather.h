@@ -104,6 +104,18 @@ struct WindowSource {
 };
 
 // p.idx is unused: rows = tokens, cols = topk (or window); out as in p.
+// Two caches of one record format read through one index matrix: columns
+// j >= split take their slots in this cache, columns j < split in GatherParams'.
+struct PairSource {
+    const uint8_t* cache;
+    int64_t num_pages;
+    int64_t page_stride;
+    int32_t block_size;
+    int32_t block_shift;  // set by the launcher
+    int32_t split;
+};
+
+cudaError_t launch_gather_pair(const GatherParams& p, const PairSource& s, cudaStream_t stream);
 cudaError_t launch_gather_topk(const GatherParams& p, const TopkSource& s, cudaStream_t stream);
 cudaError_t launch_gather_window(const GatherParams& p, const WindowSource& s,
                                  cudaStream_t stream);

@@ -505,3 +505,23 @@ def device_wait_timeouts() -> int:
 def device_wait_selftest(limit_ns: int, device: torch.device) -> None:
     """Launch one bounded wait that nothing completes (counted when it expires)."""
     _abi.call("psk_device_wait_selftest", int(limit_ns), _stream(device))
+
+
+def dequantize_and_gather_k_cache_pair(out: torch.Tensor, cache_a: torch.Tensor, block_size_a: int,
+                                       cache_b: torch.Tensor, block_size_b: int,
+                                       indices: torch.Tensor, split: int, *,
+                                       rope_dim: int = 64) -> torch.Tensor:
+    """out[t, j] = row indices[t, j] of cache_a for j < split, of cache_b for
+    j >= split (fp8_ds_mla, UE8M0)."""
+    _need_cuda(out, cache_a, cache_b, indices)
+    _need(out, torch.bfloat16, "out")
+    R, C = indices.shape
+    if out.dim() != 3 or out.shape[0] != R or out.shape[1] != C or out.stride(2) != 1:
+        raise ValueError("out must be [rows, cols, D] with unit inner stride")
+    np_a, ps_a = _pages(cache_a)
+    np_b, ps_b = _pages(cache_b)
+    _abi.call("dequantize_and_gather_k_cache_pair", _ptr(out), out.stride(0), out.stride(1),
+              _ptr(cache_a), np_a, ps_a, block_size_a, _ptr(cache_b), np_b, ps_b, block_size_b,
+              out.shape[2], rope_dim, _ptr(indices), _rows(indices, "indices"), R, C, split,
+              _stream(out.device))
+    return out

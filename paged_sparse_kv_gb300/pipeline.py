@@ -5,9 +5,11 @@ A step runs every hot-path row over one batch, in this order:
   1. quantize_and_insert_k_cache   new K rows -> SWA cache (FP8 fp8_ds_mla)
   2. write_indexer_mxfp4_cache     new indexer keys -> indexer cache (MXFP4)
   3. combine_topk_swa_indices      window + top-k -> sparse_indices, lens
-  4. dequantize_and_gather_k_cache window columns from the SWA cache and
-                                   top-k columns from the compressed cache
-                                   (two launches into one [T, W+P, D] output)
+  4. dequantize_and_gather_k_cache(_pair)  window columns from the SWA cache,
+                                   top-k columns from the compressed cache,
+                                   into one [T, W+P, D] output: one pair launch
+                                   for index matrices of at most 2^20 items,
+                                   else two launches on column ranges
   5. compute_global_topk_indices_and_lens  top-k -> indexer-cache slots
   6. dequantize_and_gather_k_cache those slots from the MXFP4 indexer cache
 
@@ -18,8 +20,10 @@ All buffers are allocated once here; ``step()`` only launches kernels.
 three streams (fork/join with events; the same dependencies as the serial
 order):
 
-  stream M:  combine_topk_swa_indices -> gather[topk]
-  stream A:  quantize_and_insert_k_cache -> (wait for the index build) -> gather[swa]
+  stream M:  combine_topk_swa_indices -> (wait for the insert) -> gather_pair
+  stream A:  quantize_and_insert_k_cache
+  (two launches: stream M gathers the top-k columns after the build, stream A
+  the window columns after the insert and the build)
   stream B:  compute_global_topk_indices_and_lens -> write_indexer_mxfp4_cache
              -> gather[mxfp4]
 
@@ -134,6 +138,10 @@ class Pipeline:
 
         T, K = w.num_tokens, w.topk
         self.cols = w.window + w.padded_topk
+        # Decode-sized index matrices are gathered by one launch over both
+        # caches; larger ones by two column-range launches on two streams,
+        # which overlap better (measured on the prefill and mixed batches).
+        self.gather_as_pair = T * self.cols <= self.PAIR_MAX_ITEMS
         if w.has_fp8:
             self.sparse_indices = torch.empty((T, self.cols), dtype=torch.int32, device=dev)
             self.lens = torch.empty((T,), dtype=torch.int32, device=dev)
@@ -285,6 +293,7 @@ class Pipeline:
                 err_count=self.err)))
         return L
 
+    PAIR_MAX_ITEMS = 1 << 20
     INDEXER_MAX_POS = 131072
 
     def alloc_indexer(self) -> None:
@@ -379,12 +388,17 @@ class Pipeline:
                 w.swa_cache.block_size, self.comp_bt, w.comp_cache.block_size, W,
                 w.compress_ratio, self.topk, is_valid_token=self.valid,
                 out=self.sparse_indices, lens=self.lens)))
-            L.append(("dequantize_and_gather_k_cache[swa]", lambda: ops.dequantize_and_gather_k_cache(
-                self.gathered[:, :W, :], self.swa_cache, self.sparse_indices[:, :W],
-                w.swa_cache.block_size, rope_dim=w.rope_dim)))
-            L.append(("dequantize_and_gather_k_cache[topk]", lambda: ops.dequantize_and_gather_k_cache(
-                self.gathered[:, W:, :], self.comp_cache, self.sparse_indices[:, W:],
-                w.comp_cache.block_size, rope_dim=w.rope_dim)))
+            if self.gather_as_pair:
+                L.append(("dequantize_and_gather_k_cache_pair", lambda: ops.dequantize_and_gather_k_cache_pair(
+                    self.gathered, self.swa_cache, w.swa_cache.block_size, self.comp_cache,
+                    w.comp_cache.block_size, self.sparse_indices, W, rope_dim=w.rope_dim)))
+            else:
+                L.append(("dequantize_and_gather_k_cache[swa]", lambda: ops.dequantize_and_gather_k_cache(
+                    self.gathered[:, :W, :], self.swa_cache, self.sparse_indices[:, :W],
+                    w.swa_cache.block_size, rope_dim=w.rope_dim)))
+                L.append(("dequantize_and_gather_k_cache[topk]", lambda: ops.dequantize_and_gather_k_cache(
+                    self.gathered[:, W:, :], self.comp_cache, self.sparse_indices[:, W:],
+                    w.comp_cache.block_size, rope_dim=w.rope_dim)))
         L.append(("compute_global_topk_indices_and_lens", lambda: ops.compute_global_topk_indices_and_lens(
             self.topk, self.t2r, self.index_table, w.index_cache.block_size, self.valid,
             out=self.global_topk, lens=self.global_lens)))
@@ -514,16 +528,22 @@ class Pipeline:
         if self.w.has_fp8:
             with torch.cuda.stream(sa):
                 run("quantize_and_insert_k_cache")
+                inserted = torch.cuda.Event()
+                inserted.record(sa)
             run("combine_topk_swa_indices")
-            built = torch.cuda.Event()
-            built.record(main)
-            with torch.cuda.stream(sa):
-                sa.wait_event(built)
-                run("dequantize_and_gather_k_cache[swa]")
-                done_a = torch.cuda.Event()
-                done_a.record(sa)
-            run("dequantize_and_gather_k_cache[topk]")
-            main.wait_event(done_a)
+            if self.gather_as_pair:
+                main.wait_event(inserted)
+                run("dequantize_and_gather_k_cache_pair")
+            else:
+                built = torch.cuda.Event()
+                built.record(main)
+                with torch.cuda.stream(sa):
+                    sa.wait_event(built)
+                    run("dequantize_and_gather_k_cache[swa]")
+                    done_a = torch.cuda.Event()
+                    done_a.record(sa)
+                run("dequantize_and_gather_k_cache[topk]")
+                main.wait_event(done_a)
         main.wait_event(done_b)
 
     def _workspace_step(self, concurrent: bool, hooks: dict) -> None:

@@ -442,3 +442,27 @@ def test_gather_window_zero_work_ok(psk_lib):
 @pytest.mark.parametrize("limit", [0, 999, 10**9 + 1, 2**63])
 def test_wait_selftest_rejects_bad_limit(psk_lib, limit):
     assert _abi.status("psk_device_wait_selftest", limit, None) == INV
+
+
+def _gather_pair(**kw):
+    a = dict(out=A, ost=640 * 512, osj=512, ca=B, npa=8, psa=64 * 584, bsa=64, cb=B + 4096,
+             npb=4, psb=16 * 592, bsb=16, D=512, rope=64, idx=C, ids=640, rows=4, cols=640,
+             split=128)
+    a.update(kw)
+    return _abi.status("dequantize_and_gather_k_cache_pair", a["out"], a["ost"], a["osj"], a["ca"],
+                       a["npa"], a["psa"], a["bsa"], a["cb"], a["npb"], a["psb"], a["bsb"], a["D"],
+                       a["rope"], a["idx"], a["ids"], a["rows"], a["cols"], a["split"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(D=100), dict(rope=16), dict(out=A + 8), dict(osj=4),
+                                dict(ost=-8), dict(ids=100), dict(idx=None), dict(out=None),
+                                dict(rows=-1), dict(split=-1), dict(split=641),
+                                dict(psa=1000), dict(psb=16 * 500), dict(ca=None), dict(cb=None),
+                                dict(cb=B + 8), dict(npb=0), dict(bsb=0)])
+def test_gather_pair_rejects_bad_arguments(psk_lib, kw):
+    assert _gather_pair(**kw) == INV
+
+
+def test_gather_pair_zero_work_ok(psk_lib):
+    assert _gather_pair(rows=0, out=None, idx=None) == OK
+    assert _gather_pair(cols=0, ids=0, split=0, out=None, idx=None) == OK

@@ -503,6 +503,39 @@ def test_index_build_staged_tables_large_batch(cuda_device, bs, base):
     _assert_same(gl.cpu().numpy(), want_gl, "staged global lens")
 
 
+@pytest.mark.parametrize("split_kind", ["zero", "mid", "all"])
+@pytest.mark.parametrize("D,rope", [(512, 64), (128, 0)])
+def test_pair_gather_matches_two_range_gathers(cuda_device, split_kind, D, rope):
+    """One index matrix over two caches (different pages, strides and page
+    sizes): columns < split from cache A, the rest from cache B; slots past
+    either cache's capacity give zero rows; strided output."""
+    rng = np.random.default_rng(D + {"zero": 0, "mid": 1, "all": 2}[split_kind])
+    rec = oracle.fp8_record_bytes(D, rope, True)
+    ga = synthetic.CacheGeom(9, 16, (16 * rec + 15) // 16 * 16 + 32)
+    gb = synthetic.CacheGeom(13, 5, (5 * rec + 15) // 16 * 16)
+    ha = synthetic.random_cache_bytes(31, ga)
+    hb = synthetic.random_cache_bytes(32, gb)
+    R, Cc = 37, 21
+    split = {"zero": 0, "mid": 8, "all": Cc}[split_kind]
+    cap_a, cap_b = 9 * 16, 13 * 5
+    idx = rng.integers(-1, max(cap_a, cap_b) + 4, size=(R, Cc)).astype(np.int32)
+    idx[0, :] = -1
+    idx[1, :] = cap_b  # valid in A, past B
+    idx[2, :] = cap_a  # past A (and B)
+    d = cuda_device
+    out = torch.full((R, Cc + 2, D), 3, dtype=torch.bfloat16, device=d)
+    ops.dequantize_and_gather_k_cache_pair(out[:, 1:Cc + 1], torch.from_numpy(ha).to(d), 16,
+                                           torch.from_numpy(hb).to(d), 5,
+                                           _dev_i32(idx, d), split, rope_dim=rope)
+    got = _u16(out)
+    want_a = oracle.dequantize_and_gather_k_cache(ha, 16, 0, D, rope, np.ascontiguousarray(idx[:, :split]))
+    want_b = oracle.dequantize_and_gather_k_cache(hb, 5, 0, D, rope, np.ascontiguousarray(idx[:, split:]))
+    _assert_same(got[:, 1:1 + split], want_a, "pair gather, cache A columns")
+    _assert_same(got[:, 1 + split:Cc + 1], want_b, "pair gather, cache B columns")
+    three = np.uint16(torch.tensor(3.0, dtype=torch.bfloat16).view(torch.int16).item())
+    assert np.all(got[:, 0] == three) and np.all(got[:, Cc + 1] == three)
+
+
 # ---- fused gathers (slots computed in the gather) ---------------------------------------
 
 @pytest.mark.parametrize("seed", range(12))
