@@ -266,6 +266,38 @@ def _oracle_sample_tokens(w, max_rows: int):
     return np.linspace(0, w.num_tokens - 1, n).astype(np.int64), n
 
 
+def host_description() -> dict:
+    """The host the oracle is timed on: its processor and logical core count."""
+    cpu = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model", "Hardware"):
+            for line in info.splitlines():
+                if line.split(":")[0].strip() == key and ":" in line:
+                    cpu = line.split(":", 1)[1].strip()
+                    break
+            if cpu:
+                break
+        if not cpu:  # Arm: the implementer and part numbers
+            impl = part = ""
+            for line in info.splitlines():
+                k = line.split(":")[0].strip()
+                if k == "CPU implementer" and not impl:
+                    impl = line.split(":", 1)[1].strip()
+                if k == "CPU part" and not part:
+                    part = line.split(":", 1)[1].strip()
+            names = {("0x41", "0xd4f"): "Arm Neoverse V2", ("0x41", "0xd40"): "Arm Neoverse V1",
+                     ("0x41", "0xd0c"): "Arm Neoverse N1"}
+            if impl or part:
+                cpu = names.get((impl, part), f"implementer {impl} part {part}")
+    except OSError:
+        pass
+    import platform
+    return {"cpu": cpu or platform.processor() or platform.machine(),
+            "arch": platform.machine(), "nproc": os.cpu_count()}
+
+
 def time_oracle(w, budget_s: float, path: str = "index"):
     """Run oracle steps until budget_s of CPU work; returns (tokens/s, desc)."""
     step, n, desc = _oracle_step(w, path, _oracle_state(w))
@@ -568,6 +600,22 @@ def main():
     if dist:
         dist.barrier()
 
+    # Back to back: the step graph replayed n times with no flush between (warm
+    # L2), timed by one pair of events -- the latency-bound steps' throughput
+    # when steps follow each other; reported beside the flushed per-step value.
+    b2b = None
+    if g_plain is not None:
+        n_b2b = 20
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        flush()
+        b0.record(stream)
+        for _ in range(n_b2b):
+            g_plain.replay()
+        b1.record(stream)
+        torch.cuda.synchronize(dev)
+        b2b = {"ms_per_step": round(b0.elapsed_time(b1) / n_b2b, 5), "steps": n_b2b,
+               "note": "step graph replayed back to back, no L2 flush between"}
     ms_per_step = statistics.mean(step_ms)
     if dist:
         t = torch.tensor([ms_per_step], device=dev)
@@ -630,11 +678,12 @@ def main():
         "step_GBps": round(step_bytes / (ms_per_step / 1e3) / 1e9, 1),
         "clocks": clk,
         "wall_s_timed_region": round(t_wall, 4),
+        "back_to_back": b2b,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, desc = time_oracle(w, args.cpu_budget, path=path)
         line["cpu_baseline"] = {"value": round(v, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": desc}
+                                "sample": desc, "host": host_description()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -787,6 +836,7 @@ def run_reference(args, rank, world):
         "vs_baseline": None, "dtype": "bf16/fp8/fp4", "data": "synthetic",
         "config": {"workload": w.name, "seed": w.seed, "path": path},
         "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "host": host_description(),
                          "sample": desc},
         "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
