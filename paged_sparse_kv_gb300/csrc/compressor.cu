@@ -81,14 +81,13 @@ __global__ void __launch_bounds__(kThreads) save_state_kernel(SaveStateParams p)
 
 // ---- compressed rows ------------------------------------------------------------------
 //
-// One CTA per token.  THREADS = 128 (four columns per thread; windows of at
-// most 8 rows are loaded into registers in one round trip) or 512 (one column
-// per thread, the window streamed with loads issued eight rows ahead) -- the
-// latter for long windows, which have few tokens to spread over the GPU.
-// Every column's softmax is computed by one thread in window order, so the
-// split of columns does not change any result.  The normalised row goes
-// through shared memory to a common epilogue: 128 threads, four dims each
-// (RoPE on the tail, bf16, the fp8_ds_mla record).
+// Windows of at most 8 rows (CSA: ratio 4, overlapping): one CTA of 128
+// threads per token, four columns per thread, the whole window loaded into
+// registers in one round trip.  Every column's softmax is computed by one
+// thread in window order, so the split of columns does not change any result.
+// The normalised row goes through shared memory to the epilogue: 128 threads,
+// four dims each (RoPE on the tail, bf16, the fp8_ds_mla record).  Longer
+// windows take the cluster kernel further below.
 constexpr int kMaxWindow = 256;
 constexpr int kHead = 512;
 constexpr int kRope = 64;
@@ -122,12 +121,12 @@ __device__ __forceinline__ void load_slice(const CompressParams& p, int64_t row,
 }
 
 // One token's compressed row (the whole CTA; every thread calls it).
-template <int THREADS, bool REGS>
+template <int THREADS>
 __device__ __forceinline__ void compress_token(const CompressParams& p, int32_t kv_shift, int64_t t,
                                                int64_t* s_row, float* s_part, float* s_y) {
     constexpr int CPT = kHead / THREADS;  // columns per thread
     constexpr int NW = THREADS / kWarp;
-    constexpr int WREG = 8;               // window rows held in registers (REGS)
+    constexpr int WREG = 8;               // window rows held in registers
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t ks = __ldg(p.kv_slots + t);
     const int64_t pos = __ldg(p.positions + t);
@@ -162,7 +161,7 @@ __device__ __forceinline__ void compress_token(const CompressParams& p, int32_t 
         sum[e] = 0.0f;
         acc[e] = 0.0f;
     }
-    if (REGS) {
+    {
         // the whole window (<= 8 rows) in registers: one round of loads
         float sv[WREG][CPT], kv[WREG][CPT];
 #pragma unroll
@@ -190,47 +189,6 @@ __device__ __forceinline__ void compress_token(const CompressParams& p, int32_t 
 #pragma unroll
                 for (int e = 0; e < CPT; ++e)
                     acc[e] = __fadd_rn(acc[e], __fmul_rn(kv[j][e], __fdiv_rn(ex[j][e], sum[e])));
-    } else {
-        // streamed: three passes, U rows' loads issued before their use
-        constexpr int U = 8;
-        for (int j0 = 0; j0 < window; j0 += U) {
-            float sv[U][CPT], kd[U][CPT];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (j0 + u < window) load_slice<CPT>(p, s_row[j0 + u], j0 + u, col, sv[u], kd[u], false);
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (j0 + u < window)
-#pragma unroll
-                    for (int e = 0; e < CPT; ++e)
-                        mx[e] = (j0 + u == 0) ? sv[u][e] : (sv[u][e] > mx[e] ? sv[u][e] : mx[e]);
-        }
-        for (int j0 = 0; j0 < window; j0 += U) {
-            float sv[U][CPT], kd[U][CPT];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (j0 + u < window) load_slice<CPT>(p, s_row[j0 + u], j0 + u, col, sv[u], kd[u], false);
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (j0 + u < window)
-#pragma unroll
-                    for (int e = 0; e < CPT; ++e)
-                        sum[e] = __fadd_rn(sum[e], cw_exp(__fsub_rn(sv[u][e], mx[e])));
-        }
-        for (int j0 = 0; j0 < window; j0 += U) {
-            float sv[U][CPT], kd[U][CPT];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (j0 + u < window) load_slice<CPT>(p, s_row[j0 + u], j0 + u, col, sv[u], kd[u], true);
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (j0 + u < window)
-#pragma unroll
-                    for (int e = 0; e < CPT; ++e) {
-                        const float w = __fdiv_rn(cw_exp(__fsub_rn(sv[u][e], mx[e])), sum[e]);
-                        acc[e] = __fadd_rn(acc[e], __fmul_rn(kd[u][e], w));
-                    }
-        }
     }
 
     // RMSNorm: pairwise sum of squares over the 512 columns -- in the thread
@@ -301,12 +259,12 @@ __device__ __forceinline__ void compress_token(const CompressParams& p, int32_t 
     }
 }
 
-// Persistent CTAs: each scans contiguous 32-token chunks (warp 0: one
+// Persistent CTAs: each scans contiguous CHUNK-token chunks (warp 0: one
 // coalesced read of the chunk's slots and positions, a ballot of the tokens
 // that write, counted skips), lists the writing tokens in ascending order in
 // shared memory, and processes them one at a time with the whole CTA -- most
 // tokens of a batch do not close a group, so no CTA is spent on them.
-template <int THREADS, bool REGS>
+template <int THREADS, int CHUNK>
 __global__ void __launch_bounds__(THREADS) compress_kernel(CompressParams p, int32_t kv_shift) {
     __shared__ int64_t s_row[kMaxWindow];
     __shared__ float s_part[THREADS / kWarp];
@@ -316,12 +274,12 @@ __global__ void __launch_bounds__(THREADS) compress_kernel(CompressParams p, int
     const int tid = threadIdx.x, lane = tid & 31;
     pdl_wait();
     pdl_launch_dependents();
-    for (int64_t c0 = (int64_t)blockIdx.x * kWarp; c0 < p.num_tokens;
-         c0 += (int64_t)gridDim.x * kWarp) {
+    for (int64_t c0 = (int64_t)blockIdx.x * CHUNK; c0 < p.num_tokens;
+         c0 += (int64_t)gridDim.x * CHUNK) {
         if (tid < kWarp) {
             const int64_t t = c0 + lane;
             bool emit = false;
-            if (t < p.num_tokens) {
+            if (lane < CHUNK && t < p.num_tokens) {
                 const int64_t ss = __ldg(p.state_slots + t), ks = __ldg(p.kv_slots + t);
                 const int64_t pos = __ldg(p.positions + t);
                 if (ss >= 0 && ks >= 0) {
@@ -348,7 +306,7 @@ __global__ void __launch_bounds__(THREADS) compress_kernel(CompressParams p, int
         __syncthreads();
         const int n = s_count;
         for (int i = 0; i < n; ++i) {
-            compress_token<THREADS, REGS>(p, kv_shift, s_list[i], s_row, s_part, s_y);
+            compress_token<THREADS>(p, kv_shift, s_list[i], s_row, s_part, s_y);
             __syncthreads();
         }
         __syncthreads();  // every thread has read s_count / s_list before the next scan
@@ -701,17 +659,19 @@ cudaError_t launch_compress_kv_insert(const CompressParams& p, cudaStream_t stre
     const int window = (p.overlap ? 2 : 1) * p.ratio;
     const int32_t shift = log2_if_pow2(p.kv_bs);
     const int64_t chunks = (p.num_tokens + kWarp - 1) / kWarp;
-    auto grid_for = [&](auto kern, int threads) {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) !=
-                cudaSuccess || per_sm < 1)
-            per_sm = 1;
-        const int64_t full = (int64_t)sm_count() * per_sm;
-        return dim3((unsigned)(chunks < full ? chunks : full));
-    };
     if (window <= 8) {
-        auto kern = compress_kernel<128, true>;
-        return launch_pdl(kern, grid_for(kern, 128), dim3(128), 0, stream, p, shift);
+        // 32-token chunks (16-token chunks, which fill every resident CTA
+        // slot, measured slower: twice the scans)
+        constexpr int kChunk = 32;
+        auto kern = compress_kernel<128, kChunk>;
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, 0) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        const int64_t nchunks = (p.num_tokens + kChunk - 1) / kChunk;
+        const int64_t full = (int64_t)sm_count() * per_sm;
+        return launch_pdl(kern, dim3((unsigned)(nchunks < full ? nchunks : full)), dim3(128), 0,
+                          stream, p, shift);
     }
     // longer windows: clusters of kSlices CTAs, as many as can be resident
     auto kern = compress_cluster_kernel;
