@@ -16,14 +16,14 @@ A step runs every hot-path row over one batch, in this order:
 Workloads without an FP8 part (the MXFP4 indexer workload) run 2, 5 and 6.
 All buffers are allocated once here; ``step()`` only launches kernels.
 
-``step(concurrent=True)`` runs the three independent chains of the step on
-three streams (fork/join with events; the same dependencies as the serial
-order):
+``step(concurrent=True)`` runs the independent chains of the step on two
+streams (three with the two-launch gather), fork/join with events, with the
+same dependencies as the serial order:
 
-  stream M:  combine_topk_swa_indices -> (wait for the insert) -> gather_pair
-  stream A:  quantize_and_insert_k_cache
-  (two launches: stream M gathers the top-k columns after the build, stream A
-  the window columns after the insert and the build)
+  stream M:  quantize_and_insert_k_cache -> combine_topk_swa_indices -> gather_pair
+             (one PDL chain: each kernel waits for its predecessor's grid)
+  (two launches: stream A runs quantize_and_insert_k_cache and then the window
+  columns after the build, stream M the build and then the top-k columns)
   stream B:  compute_global_topk_indices_and_lens -> write_indexer_mxfp4_cache
              -> gather[mxfp4]
 
@@ -525,25 +525,26 @@ class Pipeline:
             run("dequantize_and_gather_k_cache[mxfp4]")
             done_b = torch.cuda.Event()
             done_b.record(sb)
-        if self.w.has_fp8:
+        if self.w.has_fp8 and self.gather_as_pair:
+            # one programmatic (PDL) chain: each kernel waits for its
+            # predecessor's grid before its first global access, so the gather
+            # sees the insert's rows through the index build
+            run("quantize_and_insert_k_cache")
+            run("combine_topk_swa_indices")
+            run("dequantize_and_gather_k_cache_pair")
+        elif self.w.has_fp8:
             with torch.cuda.stream(sa):
                 run("quantize_and_insert_k_cache")
-                inserted = torch.cuda.Event()
-                inserted.record(sa)
             run("combine_topk_swa_indices")
-            if self.gather_as_pair:
-                main.wait_event(inserted)
-                run("dequantize_and_gather_k_cache_pair")
-            else:
-                built = torch.cuda.Event()
-                built.record(main)
-                with torch.cuda.stream(sa):
-                    sa.wait_event(built)
-                    run("dequantize_and_gather_k_cache[swa]")
-                    done_a = torch.cuda.Event()
-                    done_a.record(sa)
-                run("dequantize_and_gather_k_cache[topk]")
-                main.wait_event(done_a)
+            built = torch.cuda.Event()
+            built.record(main)
+            with torch.cuda.stream(sa):
+                sa.wait_event(built)
+                run("dequantize_and_gather_k_cache[swa]")
+                done_a = torch.cuda.Event()
+                done_a.record(sa)
+            run("dequantize_and_gather_k_cache[topk]")
+            main.wait_event(done_a)
         main.wait_event(done_b)
 
     def _workspace_step(self, concurrent: bool, hooks: dict) -> None:
