@@ -424,10 +424,12 @@ def main():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--path", default="index",
-                    choices=["index", "fused", "workspace", "dense", "indexer_fp8",
+    ap.add_argument("--path", default="auto",
+                    choices=["auto", "index", "fused", "workspace", "dense", "indexer_fp8",
                              "indexer_store", "compressor"],
-                    help="index: the index-keyed gather into [T, W+P, D]; workspace: the "
+                    help="auto: fused for index matrices of up to 2^20 items (latency-bound "
+                         "batches), else index; "
+                         "index: the index-keyed gather into [T, W+P, D]; workspace: the "
                          "prefill workspace path (range gathers + workspace indices); dense: "
                          "the no-top-k decode step of a heavily compressed layer (the "
                          "decode_hca workload always takes it); indexer_fp8 / indexer_store: "
@@ -464,6 +466,8 @@ def main():
     p = Pipeline(w, dev)
     p.fill_caches_with_quantized_rows(seed=4321 + rank)
     path = "dense" if w.dense_width > 0 else args.path
+    if path == "auto":  # the pipeline's size rule (fused for latency-bound batches)
+        path = p.default_path
     if path == "workspace" and not w.has_fp8:
         raise SystemExit("the workspace path needs a workload with an FP8 part")
     if path == "dense" and w.dense_width <= 0:
@@ -817,8 +821,11 @@ def run_reference(args, rank, world):
     import oracle
     from paged_sparse_kv_gb300 import synthetic
     oracle.build()
+    from paged_sparse_kv_gb300.pipeline import Pipeline
     w = synthetic.make(args.config)
     path = "dense" if w.dense_width > 0 else args.path
+    if path == "auto":
+        path = Pipeline.default_path_for(w)
     step, n, desc = _oracle_step(w, path, _oracle_state(w))
     for _ in range(args.warmup):
         step()

@@ -141,7 +141,8 @@ class Pipeline:
         # Decode-sized index matrices are gathered by one launch over both
         # caches; larger ones by two column-range launches on two streams,
         # which overlap better (measured on the prefill and mixed batches).
-        self.gather_as_pair = T * self.cols <= self.PAIR_MAX_ITEMS
+        self.gather_as_pair = self.small_batch(w)
+        self.default_path = self.default_path_for(w)
         if w.has_fp8:
             self.sparse_indices = torch.empty((T, self.cols), dtype=torch.int32, device=dev)
             self.lens = torch.empty((T,), dtype=torch.int32, device=dev)
@@ -294,6 +295,19 @@ class Pipeline:
         return L
 
     PAIR_MAX_ITEMS = 1 << 20
+
+    @classmethod
+    def small_batch(cls, w: Workload) -> bool:
+        """An index matrix of at most 2^20 items: a latency-bound batch."""
+        return w.num_tokens * (w.window + w.padded_topk) <= cls.PAIR_MAX_ITEMS
+
+    @classmethod
+    def default_path_for(cls, w: Workload) -> str:
+        """The step a batch runs by default.  Latency-bound batches take the
+        fused gathers, which wait for no index build (decode: 23.2 against
+        27.1 us per step); larger, bandwidth-bound ones the index path
+        (prefill, mixed: 1% faster)."""
+        return "fused" if (w.has_fp8 and cls.small_batch(w)) else "index"
     INDEXER_MAX_POS = 131072
 
     def alloc_indexer(self) -> None:
@@ -464,12 +478,14 @@ class Pipeline:
         # before the side chains take SMs
         run("dequantize_and_gather_k_cache_topk[topk]")
         done = []
-        for st, names in ((sa, ("quantize_and_insert_k_cache",
-                                "dequantize_and_gather_k_cache_window[swa]")),
+        # chains captured in this order: the index builders, the MXFP4 chain,
+        # then the insert and the window gather
+        for st, names in ((sc, ("combine_topk_swa_indices",
+                                "compute_global_topk_indices_and_lens")),
                           (sb, ("write_indexer_mxfp4_cache",
                                 "dequantize_and_gather_k_cache_topk[mxfp4]")),
-                          (sc, ("combine_topk_swa_indices",
-                                "compute_global_topk_indices_and_lens"))):
+                          (sa, ("quantize_and_insert_k_cache",
+                                "dequantize_and_gather_k_cache_window[swa]"))):
             st.wait_event(fork)
             with torch.cuda.stream(st):
                 for n in names:
