@@ -60,6 +60,7 @@ constexpr int kWarps = kThreads / kWarp;
 constexpr int kSbUnroll = PSK_INDEX_SB_UNROLL;
 constexpr int kMaxStagedEntries = 4096;  // 16 KB of int32 page ids per staged row
 constexpr int kMaxTopkStageBytes = 64 * 1024;  // top-k rows of one CTA in shared memory
+constexpr int kTopkBars = 16;                  // staged top-k rows (tokens) per CTA at most
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Waits on the top-k staging barrier that gave up (2 s without the copies
@@ -475,6 +476,18 @@ __device__ __forceinline__ void stage_topk_rows(int32_t* dst, const int32_t* top
         bulk_g2s(dst + (t - t0) * words, topk_local + t * topk_stride, bytes, bar);
 }
 
+// The same with one barrier per token row: row t - t0 completes on
+// bars[t - t0], so each token's warps start as soon as their own row lands.
+__device__ __forceinline__ void stage_topk_rows_each(int32_t* dst, const int32_t* topk_local,
+                                                     int64_t topk_stride, int words, int64_t t0,
+                                                     int64_t t1, uint64_t* bars) {
+    const uint32_t bytes = (uint32_t)words * 4u;
+    for (int64_t t = t0; t < t1; ++t) {
+        mbar_arrive_expect_tx(&bars[t - t0], bytes);
+        bulk_g2s(dst + (t - t0) * words, topk_local + t * topk_stride, bytes, &bars[t - t0]);
+    }
+}
+
 // Loads the lane's first batch of top-k quads of token t (depends on t only).
 template <bool VEC>
 __device__ __forceinline__ void load_first_batch(const IndexParams& p, int64_t t, int64_t t1,
@@ -515,7 +528,7 @@ index_build_kernel(IndexParams p) {
     constexpr bool SB = TMA && POW2;
     extern __shared__ __align__(16) int32_t s_dyn[];
     __shared__ int s_cnt[kWarps];
-    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ __align__(8) uint64_t s_bar[kTopkBars];  // one per staged token row
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int64_t t0 = (int64_t)blockIdx.x * p.tokens_per_cta;
     int64_t t1 = t0 + p.tokens_per_cta;
@@ -532,7 +545,7 @@ index_build_kernel(IndexParams p) {
     int32_t* s_comp = s_dyn + (TMA ? p.tokens_per_cta * p.topk : 0);
     int32_t* s_swa = s_comp + p.stage_comp + 1;
     if (TMA && threadIdx.x == 0) {
-        mbar_init(&s_bar, 1);
+        for (int i = 0; i < kTopkBars; ++i) mbar_init(&s_bar[i], 1);
         mbar_fence_init();
     }
     if (TMA) __syncthreads();
@@ -542,7 +555,7 @@ index_build_kernel(IndexParams p) {
     // Round 1: loads that depend only on token indices (TMA: the CTA's
     // top-k rows, in flight while the metadata arrives).
     if (copy_topk && threadIdx.x == 0)
-        stage_topk_rows(s_topk, p.topk_local, p.topk_stride, p.topk, t0, t1, &s_bar);
+        stage_topk_rows_each(s_topk, p.topk_local, p.topk_stride, p.topk, t0, t1, s_bar);
     const int32_t r0 = __ldg(p.t2r + t0);
     const int32_t r1 = __ldg(p.t2r + t1 - 1);
     const int64_t tf = t0 + tslot;  // this warp's first token
@@ -568,15 +581,15 @@ index_build_kernel(IndexParams p) {
         if (HAS_SWA) stage_row(s_swa, p.swa_bt + (int64_t)staged * p.swa_stride, p.stage_swa);
     }
     __syncthreads();
-    bool rows_ok = true;
-    if (copy_topk) {
-        rows_ok = mbar_wait_bounded(&s_bar, 0, kWaitLimitNs);
-        if (!rows_ok && lane == 0) atomicAdd(&g_index_wait_timeouts, 1u);
-    }
 
     for (int64_t tb = t0; tb < t1; tb += tpp) {
         const int64_t t = tb + tslot;
         int cnt = 0;
+        bool rows_ok = true;  // this token's staged top-k row landed
+        if (copy_topk && t < t1) {
+            rows_ok = mbar_wait_bounded(&s_bar[t - t0], 0, kWaitLimitNs);
+            if (!rows_ok && lane == 0) atomicAdd(&g_index_wait_timeouts, 1u);
+        }
         if (t < t1 && rows_ok) {
             TokMeta m;
             if (tb == t0) {
@@ -615,9 +628,11 @@ index_build_kernel(IndexParams p) {
             __syncthreads();
         }
     }
-    // A CTA whose wait gave up must not retire with copies still landing in
-    // its shared memory: one more bounded wait.
-    if (copy_topk && !rows_ok && threadIdx.x == 0) mbar_wait_bounded(&s_bar, 0, kWaitLimitNs);
+    // No CTA retires with copies still landing in its shared memory: thread 0
+    // waits (bounded) on every row's barrier -- at once for rows that landed,
+    // each used for one phase only.
+    if (copy_topk && threadIdx.x == 0)
+        for (int64_t t = t0; t < t1; ++t) mbar_wait_bounded(&s_bar[t - t0], 0, kWaitLimitNs);
 }
 
 // ---- workspace-relative form ------------------------------------------------------
@@ -958,7 +973,7 @@ cudaError_t launch_index_build(IndexParams p, bool has_swa, cudaStream_t stream)
                      (p.topk_stride % 4 == 0) && (!has_swa || p.window % 4 == 0);
     // Top-k rows staged by bulk copies: whole 16-byte quads, at most
     // kMaxTopkStageBytes per CTA.
-    const bool tma = vec && p.topk % 4 == 0 &&
+    const bool tma = vec && p.topk % 4 == 0 && p.tokens_per_cta <= kTopkBars &&
                      (int64_t)p.tokens_per_cta * p.topk * 4 <= kMaxTopkStageBytes;
     const bool pow2 = p.comp_shift >= 0 && (!has_swa || p.swa_shift >= 0);
     const size_t smem =
