@@ -1,0 +1,31 @@
+"""Host-side pipeline choices that need no GPU: which step a batch runs by
+default, and which gather form its index matrix takes."""
+import pytest
+
+from paged_sparse_kv_gb300 import synthetic
+from paged_sparse_kv_gb300.pipeline import Pipeline
+
+
+@pytest.mark.parametrize("name,small,path", [("tiny", True, "fused"), ("decode", True, "fused"),
+                                             ("prefill", False, "index"),
+                                             ("mixed", False, "index"),
+                                             ("mxfp4", True, "index")])
+def test_default_path_follows_the_batch_size_rule(name, small, path):
+    w = synthetic.make(name)
+    items = w.num_tokens * (w.window + w.padded_topk)
+    assert Pipeline.small_batch(w) == small == (items <= Pipeline.PAIR_MAX_ITEMS)
+    # without an FP8 part (the MXFP4 indexer batch) there is no fused step
+    assert Pipeline.default_path_for(w) == path
+
+
+def test_rule_boundary():
+    """The rule reads the token count, the window and the padded top-k width:
+    one token past 2^20 index items flips both choices."""
+    from types import SimpleNamespace
+    w = synthetic.make("decode")
+    cols = w.window + w.padded_topk
+    at = SimpleNamespace(num_tokens=Pipeline.PAIR_MAX_ITEMS // cols, window=w.window,
+                         padded_topk=w.padded_topk, has_fp8=True)
+    past = SimpleNamespace(**{**vars(at), "num_tokens": at.num_tokens + 1})
+    assert Pipeline.small_batch(at) and Pipeline.default_path_for(at) == "fused"
+    assert not Pipeline.small_batch(past) and Pipeline.default_path_for(past) == "index"
