@@ -26,13 +26,16 @@ constexpr int kThreads = 256;  // state writer
 // exp of a binary32 by Cody and Waite's argument reduction and the Taylor
 // series to r^7/7!, evaluated by Horner with fused multiply-adds: k = nearest
 // integer to x / ln 2, r = x - k * ln2_hi - k * ln2_lo (ln2_hi with 16
-// significant bits), result = p(r) * 2^k with one rounding.
+// significant bits), result = p(r) * 2^k with one rounding (two multiplies,
+// the second exact or the final one, when 2^k is not a normal binary32).
+// Branch-free, so that a thread's independent exps interleave: the core runs
+// on x clamped to [-103.98, 88.7228] -- unchanged inside that range -- and
+// NaN, overflow and underflow are selected at the end, so every result equals
+// the case-by-case form's.
 __device__ __forceinline__ float cw_exp(float x) {
-    if (x != x) return x;
-    if (x > 88.7228f) return __int_as_float(0x7F800000);
-    if (x < -103.98f) return 0.0f;
-    const float k = rintf(__fmul_rn(x, 1.44269504f));
-    float r = __fmaf_rn(-k, 0.693145751953125f, x);
+    const float xc = fminf(fmaxf(x, -103.98f), 88.7228f);
+    const float k = rintf(__fmul_rn(xc, 1.44269504f));
+    float r = __fmaf_rn(-k, 0.693145751953125f, xc);
     r = __fmaf_rn(-k, 1.42860677e-06f, r);
     float p = 1.98412698e-04f;
     p = __fmaf_rn(p, r, 1.38888889e-03f);
@@ -42,10 +45,11 @@ __device__ __forceinline__ float cw_exp(float x) {
     p = __fmaf_rn(p, r, 0.5f);
     p = __fmaf_rn(p, r, 1.0f);
     p = __fmaf_rn(p, r, 1.0f);
-    const int ki = (int)k;
-    if (ki < -126) return __fmul_rn(__fmul_rn(p, exp2_int(ki + 64)), exp2_int(-64));
-    if (ki > 127) return __fmul_rn(__fmul_rn(p, exp2_int(ki - 1)), 2.0f);
-    return __fmul_rn(p, exp2_int(ki));
+    const int ki = (int)k;  // in [-150, 128]
+    const int a = ki < -126 ? ki + 64 : (ki > 127 ? ki - 1 : ki);  // in [-86, 127]
+    const float f = ki < -126 ? __uint_as_float(0x1F800000u) /* 2^-64 */ : (ki > 127 ? 2.0f : 1.0f);
+    const float v = __fmul_rn(__fmul_rn(p, __uint_as_float((uint32_t)(a + 127) << 23)), f);
+    return x != x ? x : (x > 88.7228f ? __int_as_float(0x7F800000) : (x < -103.98f ? 0.0f : v));
 }
 
 // ---- compressor state ----------------------------------------------------------------
