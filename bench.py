@@ -341,6 +341,7 @@ KERNEL_SOURCES = {
     "dequantize_and_gather_k_cache_topk": _FAMILY["gather"],
     "dequantize_and_gather_k_cache_window": _FAMILY["gather"],
     "dequantize_and_gather_k_cache_pair": _FAMILY["gather"],
+    "dequantize_and_gather_k_cache_dense": _FAMILY["gather"],
     "indexer_mxfp4_paged_gather": _FAMILY["gather"],
 }
 SHARED_SOURCES = ("psk_common.cuh", "launch.h")
@@ -425,7 +426,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--path", default="auto",
-                    choices=["auto", "index", "fused", "workspace", "dense", "indexer_fp8",
+                    choices=["auto", "index", "fused", "workspace", "dense", "dense_fused",
+                             "indexer_fp8",
                              "indexer_store", "compressor"],
                     help="auto: fused for index matrices of up to 2^20 items (latency-bound "
                          "batches), else index; "
@@ -465,12 +467,14 @@ def main():
     w = synthetic.make(args.config, seed_offset=1000 * rank)
     p = Pipeline(w, dev)
     p.fill_caches_with_quantized_rows(seed=4321 + rank)
-    path = "dense" if w.dense_width > 0 else args.path
+    path = args.path
     if path == "auto":  # the pipeline's size rule (fused for latency-bound batches)
         path = p.default_path
+    if w.dense_width > 0 and not path.startswith("dense"):
+        path = "dense"
     if path == "workspace" and not w.has_fp8:
         raise SystemExit("the workspace path needs a workload with an FP8 part")
-    if path == "dense" and w.dense_width <= 0:
+    if path.startswith("dense") and w.dense_width <= 0:
         raise SystemExit("the dense path needs a workload with dense compressed entries")
     if path.startswith("indexer_") and (w.index_k is None or w.index_head_dim != 128):
         raise SystemExit("the indexer paths need 128-dim indexer keys")
@@ -482,6 +486,7 @@ def main():
         launches = p.compressor_launches()
     else:
         launches = {"workspace": p.workspace_launches, "dense": p.dense_launches,
+                    "dense_fused": p.dense_fused_launches,
                     "index": p.launches, "fused": p.fused_launches}[path]()
     names = [n for n, _ in launches]
     flush = L2Flush(torch, dev)
@@ -494,9 +499,17 @@ def main():
 
     if path == "workspace":
         alg = workspace_algorithmic_bytes(p)
-    elif path == "dense":
+    elif path.startswith("dense"):
         alg = dense_algorithmic_bytes(p, {"swa_indices": p.swa_indices.cpu().numpy(),
                                           "dense_indices": p.dense_indices.cpu().numpy()})
+        if path == "dense_fused":
+            # the same rows; slots from per-token metadata instead of index columns
+            T = w.num_tokens
+            alg["dequantize_and_gather_k_cache_window[swa]"] = (
+                alg.pop("dequantize_and_gather_k_cache[swa]") - T * w.window * 4 + T * 16)
+            alg["dequantize_and_gather_k_cache_dense[compressed]"] = (
+                alg.pop("dequantize_and_gather_k_cache[compressed]") - T * w.dense_width * 4 +
+                T * 16)
     elif path.startswith("indexer_"):
         alg = indexer_algorithmic_bytes(p, path.split("_")[1],
                                         {"global_topk": p.global_topk.cpu().numpy()})
@@ -716,7 +729,7 @@ def run_e2e(p, args, dev, flush, path="index"):
                        p.t2r, p.replay, p.topk) if t is not None]
     if path == "workspace":
         outs = [p.ws, p.ws_indices, p.ws_lens, p.raw_values, p.raw_scales]
-    elif path == "dense":
+    elif path.startswith("dense"):
         ins = [t for t in (p.k, p.insert_slots, p.qsl, p.seq_lens, p.t2r, p.positions)
                if t is not None]
         outs = [p.swa_indices, p.swa_lens, p.dense_indices, p.dense_lens, p.dense_gathered]
@@ -797,7 +810,7 @@ def _oracle_step(w, path: str, caches):
         return (lambda: run_indexer_step(w, variant, cache, inputs, toks), nt,
                 f"oracle step of the {w.name} batch ({path} path) per timed step; gathers over "
                 f"{nt} of {w.num_tokens} tokens")
-    if path == "dense":
+    if path.startswith("dense"):
         return (lambda: run_dense_step(w, caches["swa_cache"], caches["comp_cache"]),
                 w.num_tokens, f"oracle step of the {w.name} batch (dense path) per timed step")
     if path == "workspace":
@@ -823,9 +836,11 @@ def run_reference(args, rank, world):
     oracle.build()
     from paged_sparse_kv_gb300.pipeline import Pipeline
     w = synthetic.make(args.config)
-    path = "dense" if w.dense_width > 0 else args.path
+    path = args.path
     if path == "auto":
         path = Pipeline.default_path_for(w)
+    if w.dense_width > 0 and not path.startswith("dense"):
+        path = "dense"
     step, n, desc = _oracle_step(w, path, _oracle_state(w))
     for _ in range(args.warmup):
         step()

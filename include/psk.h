@@ -631,6 +631,27 @@ psk_status dequantize_and_gather_k_cache_pair(
     int32_t rope_dim, const int32_t* indices, int64_t idx_stride, int64_t rows, int32_t cols,
     int32_t split, psk_stream_t stream);
 
+/*
+ * dequantize_and_gather_k_cache_dense -- every visible compressed entry of a
+ * token gathered straight from its position (the HCA decode read of a heavily
+ * compressed layer, [BE] _decode_compressed_attention_indices_and_lens with
+ * all (pos + 1) // ratio entries).  Output identical to
+ * compute_dense_compressed_indices_and_lens (same arguments) followed by
+ * dequantize_and_gather_k_cache over that matrix, in one launch: out row
+ * (t, c), c < width, is compressed entry c when c < clamp((positions[t] + 1)
+ * // compress_ratio, 0, width) and the token is valid, else a zero row.
+ * fp8_ds_mla records with UE8M0 scales; out as in
+ * dequantize_and_gather_k_cache_topk.  Errors: PSK_ERR_INVALID_ARGUMENT as the
+ * two calls it stands for; PSK_ERR_CUDA if the launch fails.
+ */
+psk_status dequantize_and_gather_k_cache_dense(
+    void* out, int64_t out_stride_t, int64_t out_stride_j, const uint8_t* cache,
+    int64_t num_pages, int64_t page_stride, int32_t block_size, int32_t head_dim,
+    int32_t rope_dim, const int64_t* positions, int64_t num_tokens, const int32_t* token_to_req,
+    int32_t num_reqs, const int32_t* block_table, int64_t bt_stride, int32_t bt_width,
+    const int32_t* base_offsets, int32_t compress_ratio, int32_t width,
+    const uint8_t* is_valid_token, psk_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -69,6 +69,9 @@ SIGNATURES = {
     "dequantize_and_gather_k_cache_topk": (
         _I32, [_P, _I64, _I64, _P, _I64, _I64, _I32, _I32, _I32, _I32, _P, _I64, _I64, _I32, _P, _P,
                _I64, _I32, _I32, _P, _P, _P]),
+    "dequantize_and_gather_k_cache_dense": (
+        _I32, [_P, _I64, _I64, _P, _I64, _I64, _I32, _I32, _I32, _P, _I64, _P, _I32, _P, _I64,
+               _I32, _P, _I32, _I32, _P, _P]),
     "dequantize_and_gather_k_cache_pair": (
         _I32, [_P, _I64, _I64, _P, _I64, _I64, _I32, _P, _I64, _I64, _I32, _I32, _I32, _P, _I64,
                _I64, _I32, _I32, _P]),

@@ -79,7 +79,7 @@ extern "C" {
 
 const char* psk_last_error(void) { return g_last_error.c_str(); }
 
-int32_t psk_abi_version(void) { return 4; }
+int32_t psk_abi_version(void) { return 5; }
 
 psk_status psk_device_wait_timeouts(uint32_t* count) {
     CHECK(count != nullptr, "count must be non-null");
@@ -794,6 +794,43 @@ psk_status dequantize_and_gather_k_cache_pair(
     psk::PairSource pr{cache_b, num_pages_b, page_stride_b, block_size_b, -1, split};
     return cuda_status(psk::launch_gather_pair(p, pr, reinterpret_cast<cudaStream_t>(stream)),
                        "dequantize_and_gather_k_cache_pair launch");
+}
+
+psk_status dequantize_and_gather_k_cache_dense(
+    void* out, int64_t out_stride_t, int64_t out_stride_j, const uint8_t* cache,
+    int64_t num_pages, int64_t page_stride, int32_t block_size, int32_t head_dim,
+    int32_t rope_dim, const int64_t* positions, int64_t num_tokens, const int32_t* token_to_req,
+    int32_t num_reqs, const int32_t* block_table, int64_t bt_stride, int32_t bt_width,
+    const int32_t* base_offsets, int32_t compress_ratio, int32_t width,
+    const uint8_t* is_valid_token, psk_stream_t stream) {
+    CHECK(num_tokens >= 0 && width >= 0, "num_tokens and width must be >= 0");
+    CHECK(compress_ratio >= 1, "compress_ratio must be >= 1");
+    CHECK(fp8_head_dim_ok(head_dim),
+          "head_dim must be one of 64, 128, 256, 512, 1024 (got %d)", head_dim);
+    CHECK(rope_dim >= 0 && rope_dim < head_dim && rope_dim % 64 == 0,
+          "rope_dim must be a multiple of 64 in [0, head_dim) (got %d)", rope_dim);
+    psk_status st = check_cache(cache, num_pages, page_stride, block_size,
+                                fp8_record_bytes(head_dim, rope_dim, 1));
+    if (st != PSK_OK) return st;
+    CHECK(bt_width >= 0 && bt_stride >= bt_width, "need 0 <= bt_width <= bt_stride");
+    if (num_tokens == 0 || width == 0) return ok();
+    CHECK(num_reqs >= 1, "num_reqs must be >= 1");
+    CHECK(out && positions && token_to_req, "out, positions and token_to_req must be non-null");
+    CHECK(bt_width == 0 || block_table, "block_table must be non-null");
+    CHECK(aligned(out, 16), "out must be 16-byte aligned");
+    CHECK(out_stride_t >= 0 && out_stride_j >= 0 && out_stride_t % 8 == 0 && out_stride_j % 8 == 0,
+          "output strides must be non-negative multiples of 8 elements");
+    CHECK(aligned(positions, 8), "positions must be 8-byte aligned");
+    CHECK(aligned(token_to_req, 4) && aligned(block_table, 4) && aligned(base_offsets, 4),
+          "int32 arrays must be 4-byte aligned");
+    CHECK(num_tokens <= INT64_MAX / width, "num_tokens * width overflows");
+    psk::GatherParams p{static_cast<uint16_t*>(out), out_stride_t, out_stride_j, cache,
+                        num_pages, page_stride, block_size, 0, head_dim, rope_dim, 1, nullptr, 0,
+                        num_tokens, width};
+    psk::DenseSource ds{positions, token_to_req, is_valid_token, num_reqs, block_table, bt_stride,
+                        bt_width, base_offsets, compress_ratio};
+    return cuda_status(psk::launch_gather_dense(p, ds, reinterpret_cast<cudaStream_t>(stream)),
+                       "dequantize_and_gather_k_cache_dense launch");
 }
 
 }  // extern "C"

@@ -64,7 +64,8 @@ __device__ __forceinline__ void item_to_tj(int64_t item, int32_t cols, bool smal
 // request's position range through its block-table row (RANGE form), a
 // token's local top-k index through its request's table (TOPK form) or a
 // token's window position through the SWA table (WINDOW form).
-enum : int { kSrcIndex = 0, kSrcRange = 1, kSrcTopk = 2, kSrcWindow = 3, kSrcPair = 4 };
+enum : int { kSrcIndex = 0, kSrcRange = 1, kSrcTopk = 2, kSrcWindow = 3, kSrcPair = 4,
+              kSrcDense = 5 };
 
 struct ItemSource {
     GatherParams g;      // index form (and cache geometry and output for every form)
@@ -72,6 +73,7 @@ struct ItemSource {
     TopkSource tk;       // top-k form
     WindowSource wn;     // window form
     PairSource pr;       // pair form: index form over two caches split by column
+    DenseSource ds;      // dense form: every visible compressed entry of a token
 };
 
 // Slot of position p through one table row (the block-table rule), or -1.
@@ -123,6 +125,25 @@ __device__ __forceinline__ int32_t window_item_slot(const WindowSource& s, int32
     const int64_t p = lo + c;
     if (p > pos) return -1;
     const int32_t raw = table_slot(s.bt + (int64_t)r * s.bt_stride, s.bt_width, base, bs, shift, p);
+    return (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
+}
+
+// Slot of item (t, c) of the DENSE form: the rule of
+// compute_dense_compressed_indices_and_lens (padding token -> -1; entries past
+// the visible count -> -1) then the gather's capacity check.
+__device__ __forceinline__ int32_t dense_item_slot(const DenseSource& s, int32_t cols, int32_t bs,
+                                                   int32_t shift, int64_t capacity, int64_t t,
+                                                   int32_t c) {
+    const int32_t r = __ldg(s.t2r + t);
+    const bool valid = s.valid == nullptr || __ldg(s.valid + t) != 0;
+    if (!valid || r < 0 || r >= s.num_reqs) return -1;
+    const int64_t num = __ldg(s.positions + t) + 1;
+    if (num <= 0) return -1;
+    const int64_t n = num <= 0xFFFFFFFFll ? (int64_t)((uint32_t)num / (uint32_t)s.ratio)
+                                          : num / s.ratio;
+    if (c >= n || c >= cols) return -1;
+    const int64_t base = s.base ? __ldg(s.base + r) : 0;
+    const int32_t raw = table_slot(s.bt + (int64_t)r * s.bt_stride, s.bt_width, base, bs, shift, c);
     return (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
 }
 
@@ -212,6 +233,9 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
                         } else if (SRC == kSrcWindow) {
                             slot[q] = window_item_slot(src.wn, p.cols, bs, p.block_shift, capacity,
                                                        t, j);
+                        } else if (SRC == kSrcDense) {
+                            slot[q] = dense_item_slot(src.ds, p.cols, bs, p.block_shift, capacity,
+                                                      t, j);
                         } else if (SRC == kSrcPair) {
                             second[q] = j >= src.pr.split;
                             const int64_t cap = second[q] ? capacity2 : capacity;
@@ -601,6 +625,17 @@ cudaError_t launch_gather_pair(const GatherParams& params, const PairSource& pr,
     src.pr = pr;
     src.pr.block_shift = log2_if_pow2(pr.block_size);
     return fp8_by_dim<kSrcPair>(src, p.rows * (int64_t)p.cols, stream);
+}
+
+cudaError_t launch_gather_dense(const GatherParams& params, const DenseSource& ds,
+                                cudaStream_t stream) {
+    GatherParams p = params;
+    p.block_shift = log2_if_pow2(p.block_size);
+    if (p.record != 0) return cudaErrorInvalidValue;
+    ItemSource src{};
+    src.g = p;
+    src.ds = ds;
+    return fp8_by_dim<kSrcDense>(src, p.rows * (int64_t)p.cols, stream);
 }
 
 cudaError_t launch_gather_ranges(const RangeParams& r, cudaStream_t stream) {

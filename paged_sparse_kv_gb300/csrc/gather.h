@@ -116,6 +116,23 @@ struct PairSource {
 };
 
 cudaError_t launch_gather_pair(const GatherParams& p, const PairSource& s, cudaStream_t stream);
+
+// Every visible compressed entry of a token (the HCA decode rule): entry c of
+// token t is compressed position c when c < clamp(floor((positions[t] + 1) /
+// ratio), 0, cols), mapped through its request's table.
+struct DenseSource {
+    const int64_t* positions;
+    const int32_t* t2r;
+    const uint8_t* valid;   // may be null
+    int32_t num_reqs;
+    const int32_t* bt;
+    int64_t bt_stride;
+    int32_t bt_width;
+    const int32_t* base;    // may be null
+    int32_t ratio;
+};
+
+cudaError_t launch_gather_dense(const GatherParams& p, const DenseSource& s, cudaStream_t stream);
 cudaError_t launch_gather_topk(const GatherParams& p, const TopkSource& s, cudaStream_t stream);
 cudaError_t launch_gather_window(const GatherParams& p, const WindowSource& s,
                                  cudaStream_t stream);

@@ -525,3 +525,28 @@ def dequantize_and_gather_k_cache_pair(out: torch.Tensor, cache_a: torch.Tensor,
               out.shape[2], rope_dim, _ptr(indices), _rows(indices, "indices"), R, C, split,
               _stream(out.device))
     return out
+
+
+def dequantize_and_gather_k_cache_dense(out: torch.Tensor, cache: torch.Tensor,
+                                        positions: torch.Tensor, token_to_req: torch.Tensor,
+                                        block_table: torch.Tensor, block_size: int,
+                                        compress_ratio: int, *, rope_dim: int = 64,
+                                        num_reqs: Optional[int] = None,
+                                        base_offsets: Optional[torch.Tensor] = None,
+                                        is_valid_token: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """out[t, c] = compressed entry c of token t when visible (= the dense
+    compressed indices followed by the gather)."""
+    _need_cuda(out, cache, positions, token_to_req, block_table, base_offsets, is_valid_token)
+    _need(out, torch.bfloat16, "out")
+    T = positions.shape[0]
+    if out.dim() != 3 or out.shape[0] != T or out.stride(2) != 1:
+        raise ValueError("out must be [T, width, D] with unit inner stride")
+    num_pages, page_stride = _pages(cache)
+    valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
+    R = block_table.shape[0] if num_reqs is None else num_reqs
+    _abi.call("dequantize_and_gather_k_cache_dense", _ptr(out), out.stride(0), out.stride(1),
+              _ptr(cache), num_pages, page_stride, block_size, out.shape[2], rope_dim,
+              _ptr(positions), T, _ptr(token_to_req), R, _ptr(block_table),
+              _rows(block_table, "block_table"), block_table.shape[1], _ptr(base_offsets),
+              compress_ratio, out.shape[1], _ptr(valid), _stream(out.device))
+    return out

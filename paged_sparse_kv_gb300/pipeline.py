@@ -76,6 +76,14 @@ ratio-4 (overlapping window) and a ratio-128 layer, one per stream:
   stream M:  decode_swa_indices_and_lens -> (wait for the insert) -> gather[swa]
   stream A:  quantize_and_insert_k_cache
   stream B:  compute_dense_compressed_indices_and_lens -> gather[compressed]
+
+``path="dense_fused"`` produces the same outputs with gathers that compute their
+own slots (the window rule; every visible compressed entry), so neither waits
+for a builder:
+
+  stream M:  gather_dense[compressed]  (issued first)
+  stream B:  decode_swa_indices_and_lens -> compute_dense_compressed_indices_and_lens
+  stream A:  quantize_and_insert_k_cache -> gather_window[swa]
 """
 from __future__ import annotations
 
@@ -249,6 +257,26 @@ class Pipeline:
                  w.comp_cache.block_size, rope_dim=w.rope_dim)),
         ]
 
+    def dense_fused_launches(self) -> list[tuple[str, Callable[[], None]]]:
+        """The dense decode step with gathers that compute their own slots (the
+        window rule; every visible compressed entry), as (name, launch) pairs."""
+        w = self.w
+        base = dict(self.dense_launches())
+        W = w.window
+        return [(n, base[n]) for n in ("quantize_and_insert_k_cache", "decode_swa_indices_and_lens",
+                                       "compute_dense_compressed_indices_and_lens")] + [
+            ("dequantize_and_gather_k_cache_window[swa]",
+             lambda: ops.dequantize_and_gather_k_cache_window(
+                 self.dense_gathered[:, :W, :], self.swa_cache, self.qsl, self.seq_lens,
+                 self.t2r, None, self.swa_bt, w.swa_cache.block_size, W, rope_dim=w.rope_dim,
+                 is_valid_token=self.valid)),
+            ("dequantize_and_gather_k_cache_dense[compressed]",
+             lambda: ops.dequantize_and_gather_k_cache_dense(
+                 self.dense_gathered[:, W:, :], self.comp_cache, self.positions, self.t2r,
+                 self.comp_bt, w.comp_cache.block_size, w.compress_ratio, rope_dim=w.rope_dim,
+                 num_reqs=w.num_reqs, is_valid_token=self.valid)),
+        ]
+
     COMPRESSOR_EPS = 1e-6
 
     def alloc_compressor(self, seed: int = 777) -> None:
@@ -307,6 +335,8 @@ class Pipeline:
         fused gathers, which wait for no index build (decode: 23.2 against
         27.1 us per step); larger, bandwidth-bound ones the index path
         (prefill, mixed: 1% faster)."""
+        if w.dense_width > 0:
+            return "dense_fused" if cls.small_batch(w) else "dense"
         return "fused" if (w.has_fp8 and cls.small_batch(w)) else "index"
     INDEXER_MAX_POS = 131072
 
@@ -507,6 +537,8 @@ class Pipeline:
             return self._fused_step(concurrent, hooks or {})
         if path == "dense":
             return self._dense_step(concurrent, hooks or {})
+        if path == "dense_fused":
+            return self._dense_fused_step(concurrent, hooks or {})
         if path in ("indexer_fp8", "indexer_store"):
             return self._indexer_step(concurrent, hooks or {}, path.split("_")[1])
         if path == "compressor":
@@ -707,6 +739,47 @@ class Pipeline:
         main.wait_event(inserted)
         run("dequantize_and_gather_k_cache[swa]")
         main.wait_event(done_b)
+
+
+    def _dense_fused_step(self, concurrent: bool, hooks: dict) -> None:
+        L = self.dense_fused_launches()
+        fns = dict(L)
+
+        def run(name):
+            pre, post = hooks.get(name, (None, None))
+            if pre:
+                pre()
+            fns[name]()
+            if post:
+                post()
+
+        if not concurrent:
+            for name, _ in L:
+                run(name)
+            return
+        main = torch.cuda.current_stream(self.dev)
+        if not hasattr(self, "_side3"):
+            self._side3 = tuple(torch.cuda.Stream(self.dev) for _ in range(3))
+        sa, sb, _ = self._side3
+        fork = torch.cuda.Event()
+        fork.record(main)
+        # the compressed entries first (they read no row this step writes), then
+        # the builders' chain, then the insert and the window gather
+        run("dequantize_and_gather_k_cache_dense[compressed]")
+        done = []
+        for st, names in ((sb, ("decode_swa_indices_and_lens",
+                                "compute_dense_compressed_indices_and_lens")),
+                          (sa, ("quantize_and_insert_k_cache",
+                                "dequantize_and_gather_k_cache_window[swa]"))):
+            st.wait_event(fork)
+            with torch.cuda.stream(st):
+                for n in names:
+                    run(n)
+                ev = torch.cuda.Event()
+                ev.record(st)
+                done.append(ev)
+        for ev in done:
+            main.wait_event(ev)
 
 
 def workspace_geometry(w: Workload) -> dict:

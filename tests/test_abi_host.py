@@ -466,3 +466,28 @@ def test_gather_pair_rejects_bad_arguments(psk_lib, kw):
 def test_gather_pair_zero_work_ok(psk_lib):
     assert _gather_pair(rows=0, out=None, idx=None) == OK
     assert _gather_pair(cols=0, ids=0, split=0, out=None, idx=None) == OK
+
+
+def _gather_dense(**kw):
+    a = dict(out=A, ost=40 * 512, osj=512, cache=B, num_pages=8, page_stride=64 * 584, bs=64,
+             D=512, rope=64, pos=C, T=4, t2r=C + 4096, R=2, bt=C + 8192, bts=16, btw=16,
+             base=None, ratio=128, width=40, valid=None)
+    a.update(kw)
+    return _abi.status("dequantize_and_gather_k_cache_dense", a["out"], a["ost"], a["osj"],
+                       a["cache"], a["num_pages"], a["page_stride"], a["bs"], a["D"], a["rope"],
+                       a["pos"], a["T"], a["t2r"], a["R"], a["bt"], a["bts"], a["btw"], a["base"],
+                       a["ratio"], a["width"], a["valid"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(D=100), dict(rope=16), dict(out=A + 8), dict(osj=4),
+                                dict(ost=-8), dict(pos=None), dict(t2r=None), dict(bt=None),
+                                dict(out=None), dict(T=-1), dict(width=-1), dict(R=0),
+                                dict(ratio=0), dict(bts=8), dict(page_stride=1000),
+                                dict(pos=C + 4), dict(t2r=C + 4098), dict(cache=None)])
+def test_gather_dense_rejects_bad_arguments(psk_lib, kw):
+    assert _gather_dense(**kw) == INV
+
+
+def test_gather_dense_zero_work_ok(psk_lib):
+    assert _gather_dense(T=0, out=None, pos=None, t2r=None) == OK
+    assert _gather_dense(width=0, out=None, pos=None, t2r=None) == OK

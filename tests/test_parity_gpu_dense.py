@@ -205,9 +205,11 @@ def test_decode_swa_at_workload_size(cuda_device, name):
     assert np.array_equal(out.cpu().numpy(), want) and np.array_equal(lens.cpu().numpy(), wl)
 
 
+@pytest.mark.parametrize("path", ["dense", "dense_fused"])
 @pytest.mark.parametrize("mode", ["serial", "concurrent", "graph"])
-def test_dense_step_matches_oracle(cuda_device, mode):
-    """The whole dense decode step as the benchmark launches it."""
+def test_dense_step_matches_oracle(cuda_device, mode, path):
+    """The whole dense decode step as the benchmark launches it (builders then
+    gathers, or gathers that compute their own slots beside the builders)."""
     w = synthetic.make("decode_hca")
     p = Pipeline(w, cuda_device)
     swa = synthetic.random_cache_bytes(61, w.swa_cache)
@@ -220,12 +222,12 @@ def test_dense_step_matches_oracle(cuda_device, mode):
         side = torch.cuda.Stream(cuda_device)
         side.wait_stream(torch.cuda.current_stream(cuda_device))
         with torch.cuda.graph(g, stream=side):
-            p.step(concurrent=True, path="dense")
+            p.step(concurrent=True, path=path)
         torch.cuda.synchronize()
         assert np.array_equal(p.swa_cache.cpu().numpy(), swa)  # capture launched nothing
         g.replay()
     else:
-        p.step(concurrent=(mode == "concurrent"), path="dense")
+        p.step(concurrent=(mode == "concurrent"), path=path)
     torch.cuda.synchronize(cuda_device)
     want = run_dense_step(w, swa, comp)
     assert np.array_equal(p.swa_indices.cpu().numpy(), want["swa_indices"])
@@ -235,3 +237,39 @@ def test_dense_step_matches_oracle(cuda_device, mode):
     assert np.array_equal(_u16(p.dense_gathered), want["gathered"])
     assert np.array_equal(p.swa_cache.cpu().numpy(), swa)
     assert int(p.err.item()) == want["err"]
+
+
+@pytest.mark.parametrize("bs,ratio,width", [(64, 128, 40), (5, 3, 12), (16, 4, 64)])
+def test_dense_gather_matches_builder_then_gather(cuda_device, bs, ratio, width):
+    """dequantize_and_gather_k_cache_dense == compute_dense_compressed_indices_and_lens
+    + dequantize_and_gather_k_cache: negative and large positions, padding and
+    out-of-range requests, base offsets, -1 pages and pages past the int32 slot
+    range, visible counts below and above the width."""
+    rng = np.random.default_rng(bs * 7 + ratio + width)
+    d = cuda_device
+    R, T, bt_w, pages, D, rope = 5, 97, 30, 40, 512, 64
+    table = rng.integers(-1, pages, size=(R, bt_w)).astype(np.int32)
+    table[0, 3] = (2**31 - 1) // bs + 1  # slots past INT32_MAX
+    base = rng.integers(0, 3, size=R).astype(np.int32)
+    t2r = rng.integers(0, R, size=T).astype(np.int32)
+    t2r[::13] = R  # out of range
+    pos = rng.integers(-5, (bt_w + 3) * bs * ratio // max(ratio, 1), size=T).astype(np.int64)
+    pos[1] = 2**40
+    valid = (rng.random(T) < 0.9).astype(np.uint8)
+    rec = oracle.fp8_record_bytes(D, rope, True)
+    geom = synthetic.CacheGeom(pages, bs, (bs * rec + 15) // 16 * 16)
+    host = synthetic.random_cache_bytes(77, geom)
+    idx, _ = oracle.compute_dense_compressed_indices_and_lens(
+        pos, t2r, table, bs, ratio, width, base_offsets=base, is_valid_token=valid)
+    want = oracle.dequantize_and_gather_k_cache(host, bs, 0, D, rope, idx)
+    out = torch.full((T, width + 1, D), 9, dtype=torch.bfloat16, device=d)
+    ops.dequantize_and_gather_k_cache_dense(
+        out[:, :width], torch.from_numpy(host).to(d), torch.from_numpy(pos).to(d),
+        torch.from_numpy(t2r).to(d), torch.from_numpy(table).to(d), bs, ratio, rope_dim=rope,
+        num_reqs=R, base_offsets=torch.from_numpy(base).to(d),
+        is_valid_token=torch.from_numpy(valid).to(d))
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got[:, :width], want)
+    nine = np.uint16(torch.tensor(9.0, dtype=torch.bfloat16).view(torch.int16).item())
+    assert np.all(got[:, width] == nine)
+    assert (idx >= 0).any() and (idx < 0).any()

@@ -9,12 +9,14 @@ from paged_sparse_kv_gb300.pipeline import Pipeline
 @pytest.mark.parametrize("name,small,path", [("tiny", True, "fused"), ("decode", True, "fused"),
                                              ("prefill", False, "index"),
                                              ("mixed", False, "index"),
-                                             ("mxfp4", True, "index")])
+                                             ("mxfp4", True, "index"),
+                                             ("decode_hca", True, "dense_fused")])
 def test_default_path_follows_the_batch_size_rule(name, small, path):
     w = synthetic.make(name)
     items = w.num_tokens * (w.window + w.padded_topk)
     assert Pipeline.small_batch(w) == small == (items <= Pipeline.PAIR_MAX_ITEMS)
-    # without an FP8 part (the MXFP4 indexer batch) there is no fused step
+    # without an FP8 part (the MXFP4 indexer batch) there is no fused step; the
+    # heavily compressed decode batch takes the dense step, fused when small
     assert Pipeline.default_path_for(w) == path
 
 
@@ -25,7 +27,7 @@ def test_rule_boundary():
     w = synthetic.make("decode")
     cols = w.window + w.padded_topk
     at = SimpleNamespace(num_tokens=Pipeline.PAIR_MAX_ITEMS // cols, window=w.window,
-                         padded_topk=w.padded_topk, has_fp8=True)
+                         padded_topk=w.padded_topk, has_fp8=True, dense_width=0)
     past = SimpleNamespace(**{**vars(at), "num_tokens": at.num_tokens + 1})
     assert Pipeline.small_batch(at) and Pipeline.default_path_for(at) == "fused"
     assert not Pipeline.small_batch(past) and Pipeline.default_path_for(past) == "index"
