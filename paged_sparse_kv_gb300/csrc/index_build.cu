@@ -552,7 +552,7 @@ index_build_kernel(IndexParams p) {
     pdl_wait();
     pdl_launch_dependents();
 
-    // Round 1: loads that depend only on token indices (TMA: the CTA's
+    // First memory round trip: loads that depend only on token indices (TMA: the CTA's
     // top-k rows, in flight while the metadata arrives).
     if (copy_topk && threadIdx.x == 0)
         stage_topk_rows_each(s_topk, p.topk_local, p.topk_stride, p.topk, t0, t1, s_bar);
@@ -563,7 +563,7 @@ index_build_kernel(IndexParams p) {
     int4 pre[PSK_INDEX_BATCH];
     if (tf < t1) rf = __ldg(p.t2r + tf);
     if (!TMA) load_first_batch<VEC>(p, tf, t1, first, stride, W, pre);
-    // Round 2: the first token's request metadata and, when the tile is one
+    // Second round trip: the first token's request metadata and, when the tile is one
     // request, its block-table rows into shared memory.
     TokMeta mf;
     if (tf < t1) mf = load_meta<HAS_SWA>(p, tf, rf);
