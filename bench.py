@@ -669,12 +669,14 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16/fp8/fp4",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/int32",
         "data": "synthetic",
         "config": {"workload": f"{w.name}: {w.num_reqs} requests, {w.num_tokens} query tokens, "
                                f"head_dim {w.head_dim} (rope {w.rope_dim}), window {w.window}, "
                                f"top-k {w.topk}, ratio {w.compress_ratio}",
                    "path": path,
+                   "storage": "bf16 rows in and out; fp8 e4m3 records with UE8M0 scales; "
+                              "MXFP4 (e2m1 + E8M0) indexer keys",
                    "seed": w.seed, "l2": ("flushed before every step: 512 MiB memset, then a 256 MiB read so "
                          "the lines left in L2 are clean"),
                    "parallelism": f"dp{world} (independent batch per GPU)",
@@ -855,7 +857,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16/fp8/fp4", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f32/int32", "data": "synthetic",
         "config": {"workload": w.name, "seed": w.seed, "path": path},
         "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "host": host_description(),
