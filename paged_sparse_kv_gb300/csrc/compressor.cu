@@ -52,6 +52,67 @@ __device__ __forceinline__ float cw_exp(float x) {
     return x != x ? x : (x > 88.7228f ? __int_as_float(0x7F800000) : (x < -103.98f ? 0.0f : v));
 }
 
+// Packed binary32 pairs (each lane the scalar IEEE operation, round to
+// nearest even).  Used only where the product feeds a conversion, a multiply
+// or an explicit fma: a packed product feeding a packed add may be contracted
+// into a fused multiply-add by the compiler.
+__device__ __forceinline__ float2 pk_mul(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 y, {%4, %5};\n\t"
+        "mul.rn.f32x2 z, x, y;\n\t"
+        "mov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 pk_fma(float2 a, float2 b, float2 c) {
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z, w;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 y, {%4, %5};\n\t"
+        "mov.b64 z, {%6, %7};\n\t"
+        "fma.rn.f32x2 w, x, y, z;\n\t"
+        "mov.b64 {%0, %1}, w;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 pk_splat(float v) { return make_float2(v, v); }
+
+// cw_exp of two arguments at once: the same operations lane by lane, the
+// multiplies and fused multiply-adds issued as packed pairs.
+__device__ __forceinline__ void cw_exp2(float x0, float x1, float& y0, float& y1) {
+    const float2 xc = make_float2(fminf(fmaxf(x0, -103.98f), 88.7228f),
+                                  fminf(fmaxf(x1, -103.98f), 88.7228f));
+    const float2 t = pk_mul(xc, pk_splat(1.44269504f));
+    const float k0 = rintf(t.x), k1 = rintf(t.y);
+    const float2 nk = make_float2(-k0, -k1);
+    float2 r = pk_fma(nk, pk_splat(0.693145751953125f), xc);
+    r = pk_fma(nk, pk_splat(1.42860677e-06f), r);
+    float2 p = pk_splat(1.98412698e-04f);
+    p = pk_fma(p, r, pk_splat(1.38888889e-03f));
+    p = pk_fma(p, r, pk_splat(8.33333333e-03f));
+    p = pk_fma(p, r, pk_splat(4.16666667e-02f));
+    p = pk_fma(p, r, pk_splat(1.66666667e-01f));
+    p = pk_fma(p, r, pk_splat(0.5f));
+    p = pk_fma(p, r, pk_splat(1.0f));
+    p = pk_fma(p, r, pk_splat(1.0f));
+    const int i0 = (int)k0, i1 = (int)k1;
+    const int a0 = i0 < -126 ? i0 + 64 : (i0 > 127 ? i0 - 1 : i0);
+    const int a1 = i1 < -126 ? i1 + 64 : (i1 > 127 ? i1 - 1 : i1);
+    const float f0 = i0 < -126 ? __uint_as_float(0x1F800000u) : (i0 > 127 ? 2.0f : 1.0f);
+    const float f1 = i1 < -126 ? __uint_as_float(0x1F800000u) : (i1 > 127 ? 2.0f : 1.0f);
+    const float2 v = pk_mul(pk_mul(p, make_float2(__uint_as_float((uint32_t)(a0 + 127) << 23),
+                                                  __uint_as_float((uint32_t)(a1 + 127) << 23))),
+                            make_float2(f0, f1));
+    y0 = x0 != x0 ? x0 : (x0 > 88.7228f ? __int_as_float(0x7F800000) : (x0 < -103.98f ? 0.0f : v.x));
+    y1 = x1 != x1 ? x1 : (x1 > 88.7228f ? __int_as_float(0x7F800000) : (x1 < -103.98f ? 0.0f : v.y));
+}
+
 // ---- compressor state ----------------------------------------------------------------
 //
 // state[slot] = [kv[t], score[t] + ape[pos % ratio]] (binary32 adds), one warp
@@ -129,6 +190,7 @@ template <int THREADS>
 __device__ __forceinline__ void compress_token(const CompressParams& p, int32_t kv_shift, int64_t t,
                                                int64_t* s_row, float* s_part, float* s_y) {
     constexpr int CPT = kHead / THREADS;  // columns per thread
+    static_assert(CPT % 2 == 0, "the exps are evaluated in column pairs");
     constexpr int NW = THREADS / kWarp;
     constexpr int WREG = 8;               // window rows held in registers
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -181,12 +243,14 @@ __device__ __forceinline__ void compress_token(const CompressParams& p, int32_t 
         float ex[WREG][CPT];
 #pragma unroll
         for (int j = 0; j < WREG; ++j)
-            if (j < window)
+            if (j < window) {
 #pragma unroll
-                for (int e = 0; e < CPT; ++e) {
-                    ex[j][e] = cw_exp(__fsub_rn(sv[j][e], mx[e]));
-                    sum[e] = __fadd_rn(sum[e], ex[j][e]);
-                }
+                for (int e = 0; e < CPT; e += 2)
+                    cw_exp2(__fsub_rn(sv[j][e], mx[e]), __fsub_rn(sv[j][e + 1], mx[e + 1]),
+                            ex[j][e], ex[j][e + 1]);
+#pragma unroll
+                for (int e = 0; e < CPT; ++e) sum[e] = __fadd_rn(sum[e], ex[j][e]);
+            }
 #pragma unroll
         for (int j = 0; j < WREG; ++j)
             if (j < window)
@@ -404,7 +468,9 @@ __device__ __forceinline__ float slice_pool(float* s_sc, const float* s_kv, floa
     for (; j + U <= j1; j += U) {
         float e[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) e[u] = cw_exp(__fsub_rn(s_sc[(j + u) * kSliceCols + c], mx));
+        for (int u = 0; u < U; u += 2)
+            cw_exp2(__fsub_rn(s_sc[(j + u) * kSliceCols + c], mx),
+                    __fsub_rn(s_sc[(j + u + 1) * kSliceCols + c], mx), e[u], e[u + 1]);
 #pragma unroll
         for (int u = 0; u < U; ++u) s_sc[(j + u) * kSliceCols + c] = e[u];
     }
