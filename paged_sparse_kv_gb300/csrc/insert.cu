@@ -12,15 +12,16 @@
 //  * A quant block is 8 chunks (FP8, 64 dims) or 4 chunks (MXFP4, 32 dims),
 //    held by 8 or 4 consecutive lanes: its amax is a 3- or 2-step
 //    __shfl_xor reduction.
-//  * amax is a 16-bit unsigned max over the bf16 magnitude bits, and the
+//  * amax is exact (a max of bf16 values): a float max in the FP8 insert, a
+//    16-bit unsigned max over the bf16 magnitude bits in the MXFP4 ones.  The
 //    scale exponent ceil(log2(amax / max_code)) is read off amax's own bits
-//    (exact for bf16 amax; no divide, no log2); scaling is a packed
-//    mul.rn.f32x2 per pair.
+//    (no divide, no log2); scaling is a packed mul.rn.f32x2 per pair.
 //  * Codes are packed with cvt.rn.satfinite.{e4m3x2,e2m1x2}.f32 and stored as
 //    8-byte (FP8) / 4-byte (MXFP4) words: a group's stores of one record are
 //    contiguous and coalesce; the rope tail moves as untouched 16-byte chunks.
-//  * The scale bytes of a token are collected by shuffles into one lane and
-//    written with a single aligned store.
+//  * Each quant block's first lane stores the block's scale byte (or binary32
+//    scale): the bytes of one token are adjacent, so the stores of a group
+//    coalesce into one request per chunk column.
 //  * Each group handles UNROLL tokens with all loads issued before any use,
 //    so enough bytes are in flight to cover HBM latency.
 #include "insert.h"
@@ -31,45 +32,14 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <int NBYTES>
-__device__ __forceinline__ void store_scale_word(uint8_t* p, uint64_t w) {
-    if constexpr (NBYTES >= 8) {
-        *reinterpret_cast<uint64_t*>(p) = w;
-    } else if constexpr (NBYTES == 4) {
-        *reinterpret_cast<uint32_t*>(p) = (uint32_t)w;
-    } else if constexpr (NBYTES == 2) {
-        *reinterpret_cast<uint16_t*>(p) = (uint16_t)w;
-    } else {
-        *p = (uint8_t)w;
-    }
-}
-
-// Gather one byte per quant block (held by the first lane of each block's
-// lane run) into the group's first lane and store the token's scale bytes.
-// CHUNKS_PER_BLOCK lanes cover one block.
-template <int LANES, int CPL, int CHUNKS_PER_BLOCK>
-__device__ __forceinline__ void store_scale_bytes(const uint32_t (&sb)[CPL], unsigned gmask,
-                                                  int grp, int gl, uint8_t* scl) {
-    constexpr int NBLK = CPL * LANES / CHUNKS_PER_BLOCK;
-    constexpr int WORD = NBLK < 8 ? NBLK : 8;
-    uint64_t word = 0;
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-#pragma unroll
-        for (int kk = 0; kk < LANES / CHUNKS_PER_BLOCK; ++kk) {
-            const uint32_t bv = __shfl_sync(gmask, sb[i], grp * LANES + kk * CHUNKS_PER_BLOCK);
-            const int b = i * (LANES / CHUNKS_PER_BLOCK) + kk;
-            word |= (uint64_t)(bv & 0xFFu) << (8 * (b % 8));
-            if ((b % 8) == 7 || b == NBLK - 1) {
-                if (gl == 0) store_scale_word<WORD>(scl + (b / 8) * 8, word);
-                word = 0;
-            }
-        }
-    }
-}
+// Blocks of the FP8 insert resident per SM: 8 (32 registers, no spills, 64
+// warps each with one token's loads in flight) up to 512 dims; wider rows hold
+// four chunks per lane and would spill at 32 registers.
+template <int D>
+constexpr int fp8_insert_min_blocks() { return D <= 512 ? 8 : 1; }
 
 template <int D, bool UE8M0, int UNROLL>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, fp8_insert_min_blocks<D>())
 fp8_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
                   const int64_t* __restrict__ slots, int64_t n,
                   uint8_t* __restrict__ cache, int64_t capacity, int64_t page_stride,
@@ -119,40 +89,41 @@ fp8_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
         uint8_t* data = base + off * ts;
         uint8_t* scl = base + (int64_t)bs * ts + off * SDIM;
 
-        uint32_t sb[CPL];
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
             const int c = gl + i * LANES;
             const uint4 w = v[u][i];
             float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                           bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-            uint32_t amb = absmax_bf16x8_bits(w);
-            amb = max(amb, __shfl_xor_sync(gmask, amb, 1));
-            amb = max(amb, __shfl_xor_sync(gmask, amb, 2));
-            amb = max(amb, __shfl_xor_sync(gmask, amb, 4));
-            const float am = __uint_as_float(amb << 16);
+            // fmaxf passes over NaN, as an ordered "a > amax" scan does.
+            float am = fmaxf(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))),
+                             fmaxf(fmaxf(fabsf(x[4]), fabsf(x[5])), fmaxf(fabsf(x[6]), fabsf(x[7]))));
+            am = fmaxf(am, __shfl_xor_sync(gmask, am, 1));
+            am = fmaxf(am, __shfl_xor_sync(gmask, am, 2));
+            am = fmaxf(am, __shfl_xor_sync(gmask, am, 4));
+            const bool lead = (c & 7) == 0;
             if (8 * c < nope) {  // uniform over the block's 8 lanes
+                // No clamp to +-448 before the conversion: .satfinite maps
+                // every finite value above 448 and +-inf to +-448, keeps NaN,
+                // and leaves smaller values alone, as the clamp would.
                 float y[8];
                 if constexpr (UE8M0) {
                     const float a = fmaxf(am, 1.0e-4f);
                     const int e = ceil_log2_div_const(a, 0x600000u, 8);  // / 448
-                    const int b = min(max(e + 127, 0), 255);
                     const uint64_t pw2 = splat_f32x2(exp2_int(-e));
 #pragma unroll
                     for (int j = 0; j < 8; j += 2) {
                         y[j] = x[j];
                         y[j + 1] = x[j + 1];
                         mul2_rn(y[j], y[j + 1], pw2);
-                        y[j] = clamp_sym(y[j], 448.0f);
-                        y[j + 1] = clamp_sym(y[j + 1], 448.0f);
                     }
-                    sb[i] = (uint32_t)b;
+                    if (lead) scl[c / 8] = (uint8_t)min(max(e + 127, 0), 255);
                 } else {
                     const float a = fmaxf(am, 1.0e-12f);
                     const float sc = __fdiv_rn(a, 448.0f);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) y[j] = clamp_sym(__fdiv_rn(x[j], sc), 448.0f);
-                    sb[i] = __float_as_uint(sc);
+                    for (int j = 0; j < 8; ++j) y[j] = __fdiv_rn(x[j], sc);
+                    if (lead) *reinterpret_cast<float*>(scl + 4 * (c / 8)) = sc;
                 }
                 uint2 q;
                 q.x = cvt_e4m3x2(y[0], y[1]) | (cvt_e4m3x2(y[2], y[3]) << 16);
@@ -160,16 +131,13 @@ fp8_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
                 st_v2(data + 8 * c, q);
             } else {
                 st_v4(data + 16 * c - nope, w);  // rope tail: bf16 verbatim
-                sb[i] = 0;
-            }
-        }
-        if constexpr (UE8M0) {
-            store_scale_bytes<LANES, CPL, 8>(sb, gmask, grp, gl, scl);
-        } else {
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) {
-                const int c = gl + i * LANES;
-                if ((c & 7) == 0) *reinterpret_cast<uint32_t*>(scl + 4 * (c / 8)) = sb[i];
+                if (lead) {  // rope blocks carry a zero scale slot
+                    if constexpr (UE8M0) {
+                        scl[c / 8] = 0;
+                    } else {
+                        *reinterpret_cast<uint32_t*>(scl + 4 * (c / 8)) = 0;
+                    }
+                }
             }
         }
     }
@@ -603,9 +571,12 @@ __global__ void __launch_bounds__(kThreads) norm_rope_store_kernel(NormRopeParam
     for (int u = 0; u < U; ++u) nrs_compute_store<FP4>(p, shift, gl, k[u]);
 }
 
+// One token per lane group: with the 32-register bound above, a 1M-token
+// insert at 512 dims ran 271 us against 275-285 us for two tokens per group
+// (40-46 registers) and 277 us for four (64 registers).
 template <int D, bool UE8M0>
 cudaError_t fp8_insert_dispatch(const InsertParams& p, cudaStream_t stream) {
-    constexpr int UNROLL = 2;
+    constexpr int UNROLL = 1;
     constexpr int LANES = (D / 8) < kWarp ? (D / 8) : kWarp;
     const int64_t groups = (p.num_tokens + UNROLL - 1) / UNROLL;
     const int64_t threads = groups * LANES;

@@ -206,11 +206,6 @@ __device__ __forceinline__ uint64_t splat_f32x2(float s) {
     return (b << 32) | b;
 }
 
-// Clamp to [-lim, lim] keeping NaN and the sign of zero.
-__device__ __forceinline__ float clamp_sym(float v, float lim) {
-    return v > lim ? lim : (v < -lim ? -lim : v);
-}
-
 // ---- programmatic dependent launch ------------------------------------------------
 //
 // Every libpsk kernel is launched with programmatic stream serialisation, so

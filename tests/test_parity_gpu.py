@@ -113,6 +113,58 @@ def test_fp8_insert_exhaustive_codes(cuda_device):
     _assert_same(dev_cache.cpu().numpy(), host, "exhaustive fp8 codes")
 
 
+def _fp8_code_positions(slots, num_pages, page_stride, bs, ts, nope):
+    """Flat byte offsets of the e4m3 codes of each inserted token."""
+    page, off = slots // bs, slots % bs
+    start = page * page_stride + off * ts
+    return (start[:, None] + np.arange(nope)[None, :]).reshape(-1)
+
+
+@pytest.mark.parametrize("ue8m0", [True, False])
+def test_fp8_insert_non_finite_inputs(cuda_device, ue8m0):
+    """+-inf, NaN of both signs (quiet and signalling payloads), all-NaN and
+    all-zero blocks, -0 and the largest finite bf16, planted in random rows.
+    amax passes over NaN; +-inf saturates to +-448.  E4M3 has two NaN codes
+    (S.1111.111): where the oracle writes NaN the kernel's byte must be a NaN
+    of either sign, every other byte must match."""
+    rng = np.random.default_rng(11)
+    D, rope, N, bs = 512, 64, 96, 16
+    nope = D - rope
+    vals = rng.standard_normal((N, D)).astype(np.float32) * 3
+    k = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    specials = np.array([0x7F80, 0xFF80, 0x7FC0, 0xFFC0, 0x7F81, 0xFF81, 0x8000, 0x7F7F, 0xFF7F],
+                        np.uint16)
+    for t in range(N):
+        for b in range(nope // 64):
+            kind = (t * 7 + b) % 5
+            if kind == 0:    # a few scattered specials
+                pos = rng.choice(64, size=3, replace=False)
+                k[t, b * 64 + pos] = rng.choice(specials, size=3)
+            elif kind == 1 and t % 3 == 0:   # whole block NaN
+                k[t, b * 64:(b + 1) * 64] = rng.choice(specials[2:6], size=64)
+            elif kind == 2 and t % 4 == 1:   # whole block zero, signs mixed
+                k[t, b * 64:(b + 1) * 64] = rng.choice(np.array([0, 0x8000], np.uint16), size=64)
+    rec = oracle.fp8_record_bytes(D, rope, ue8m0)
+    pages = N // bs + 2
+    geom = synthetic.CacheGeom(pages, bs, (bs * rec + 15) // 16 * 16)
+    host = np.full((geom.num_pages, geom.page_stride), 0x5A, np.uint8)
+    slots = rng.permutation(pages * bs)[:N].astype(np.int64)
+    dev_cache = torch.from_numpy(host).to(cuda_device)
+    ops.quantize_and_insert_k_cache(_bf16_dev(k, cuda_device), dev_cache,
+                                    torch.from_numpy(slots).to(cuda_device), bs,
+                                    rope_dim=rope, is_ue8m0=ue8m0)
+    oracle.quantize_and_insert_k_cache(k, slots, host, bs, D, rope, ue8m0)
+    got = dev_cache.cpu().numpy().reshape(-1).copy()
+    want = host.reshape(-1)
+    codes = _fp8_code_positions(slots, pages, geom.page_stride, bs, nope + 2 * rope, nope)
+    nan_at = codes[want[codes] == 0x7F]
+    assert nan_at.size > 0
+    assert np.all((got[nan_at] & 0x7F) == 0x7F), "NaN input must give an E4M3 NaN code"
+    got[nan_at] = 0x7F
+    assert np.any(want[codes] == 0x7E) and np.any(want[codes] == 0xFE)
+    _assert_same(got, want, f"non-finite fp8 insert ue8m0={ue8m0}")
+
+
 def test_mxfp4_insert_exhaustive_codes(cuda_device):
     rows = _exhaustive_rows(6.0, -15, 126, 32, 4)
     N, bs = rows.shape[0], 64
