@@ -12,9 +12,9 @@
 // then the exps summed in window order, then each weight = exp / sum and the
 // weighted kv summed in window order), the RMSNorm (pairwise sum of squares,
 // IEEE square root and reciprocal) and GPT-J RoPE.  exp itself is
-// cw_exp below -- Cody and Waite's argument reduction and the Taylor series --
-// the same operation sequence as the oracle's, not a library call, so the two
-// agree to the bit.
+// cw_exp_nonpos below -- Cody and Waite's argument reduction and the Taylor
+// series -- the same operation sequence as the oracle's, not a library call,
+// so the two agree to the bit.
 #include "compressor.h"
 #include "psk_common.cuh"
 
@@ -28,12 +28,14 @@ constexpr int kThreads = 256;  // state writer
 // integer to x / ln 2, r = x - k * ln2_hi - k * ln2_lo (ln2_hi with 16
 // significant bits), result = p(r) * 2^k with one rounding (two multiplies,
 // the second exact or the final one, when 2^k is not a normal binary32).
-// Branch-free, so that a thread's independent exps interleave: the core runs
-// on x clamped to [-103.98, 88.7228] -- unchanged inside that range -- and
-// NaN, overflow and underflow are selected at the end, so every result equals
-// the case-by-case form's.
-__device__ __forceinline__ float cw_exp(float x) {
-    const float xc = fminf(fmaxf(x, -103.98f), 88.7228f);
+// Only for x <= 0 or NaN: every argument here is a score minus the window's
+// maximum, so the overflow side (x > 88.7228, 2^k above the binary32 range)
+// cannot occur and is left out; on this domain the result is the general
+// case-by-case function's.  Branch-free, so that a thread's independent exps
+// interleave: the core runs on max(x, -103.98) -- x itself inside the range --
+// and NaN and underflow are selected at the end.
+__device__ __forceinline__ float cw_exp_nonpos(float x) {
+    const float xc = fmaxf(x, -103.98f);
     const float k = rintf(__fmul_rn(xc, 1.44269504f));
     float r = __fmaf_rn(-k, 0.693145751953125f, xc);
     r = __fmaf_rn(-k, 1.42860677e-06f, r);
@@ -45,11 +47,12 @@ __device__ __forceinline__ float cw_exp(float x) {
     p = __fmaf_rn(p, r, 0.5f);
     p = __fmaf_rn(p, r, 1.0f);
     p = __fmaf_rn(p, r, 1.0f);
-    const int ki = (int)k;  // in [-150, 128]
-    const int a = ki < -126 ? ki + 64 : (ki > 127 ? ki - 1 : ki);  // in [-86, 127]
-    const float f = ki < -126 ? __uint_as_float(0x1F800000u) /* 2^-64 */ : (ki > 127 ? 2.0f : 1.0f);
+    const int ki = (int)k;  // in [-150, 0]
+    const bool sub = ki < -126;
+    const int a = sub ? ki + 64 : ki;  // in [-126, 0]
+    const float f = sub ? __uint_as_float(0x1F800000u) /* 2^-64 */ : 1.0f;
     const float v = __fmul_rn(__fmul_rn(p, __uint_as_float((uint32_t)(a + 127) << 23)), f);
-    return x != x ? x : (x > 88.7228f ? __int_as_float(0x7F800000) : (x < -103.98f ? 0.0f : v));
+    return x != x ? x : (x < -103.98f ? 0.0f : v);
 }
 
 // Packed binary32 pairs (each lane the scalar IEEE operation, round to
@@ -83,11 +86,10 @@ __device__ __forceinline__ float2 pk_fma(float2 a, float2 b, float2 c) {
 
 __device__ __forceinline__ float2 pk_splat(float v) { return make_float2(v, v); }
 
-// cw_exp of two arguments at once: the same operations lane by lane, the
-// multiplies and fused multiply-adds issued as packed pairs.
-__device__ __forceinline__ void cw_exp2(float x0, float x1, float& y0, float& y1) {
-    const float2 xc = make_float2(fminf(fmaxf(x0, -103.98f), 88.7228f),
-                                  fminf(fmaxf(x1, -103.98f), 88.7228f));
+// cw_exp_nonpos of two arguments at once: the same operations lane by lane,
+// the multiplies and fused multiply-adds issued as packed pairs.
+__device__ __forceinline__ void cw_exp2_nonpos(float x0, float x1, float& y0, float& y1) {
+    const float2 xc = make_float2(fmaxf(x0, -103.98f), fmaxf(x1, -103.98f));
     const float2 t = pk_mul(xc, pk_splat(1.44269504f));
     const float k0 = rintf(t.x), k1 = rintf(t.y);
     const float2 nk = make_float2(-k0, -k1);
@@ -102,15 +104,15 @@ __device__ __forceinline__ void cw_exp2(float x0, float x1, float& y0, float& y1
     p = pk_fma(p, r, pk_splat(1.0f));
     p = pk_fma(p, r, pk_splat(1.0f));
     const int i0 = (int)k0, i1 = (int)k1;
-    const int a0 = i0 < -126 ? i0 + 64 : (i0 > 127 ? i0 - 1 : i0);
-    const int a1 = i1 < -126 ? i1 + 64 : (i1 > 127 ? i1 - 1 : i1);
-    const float f0 = i0 < -126 ? __uint_as_float(0x1F800000u) : (i0 > 127 ? 2.0f : 1.0f);
-    const float f1 = i1 < -126 ? __uint_as_float(0x1F800000u) : (i1 > 127 ? 2.0f : 1.0f);
+    const bool s0 = i0 < -126, s1 = i1 < -126;
+    const int a0 = s0 ? i0 + 64 : i0, a1 = s1 ? i1 + 64 : i1;
+    const float f0 = s0 ? __uint_as_float(0x1F800000u) : 1.0f;
+    const float f1 = s1 ? __uint_as_float(0x1F800000u) : 1.0f;
     const float2 v = pk_mul(pk_mul(p, make_float2(__uint_as_float((uint32_t)(a0 + 127) << 23),
                                                   __uint_as_float((uint32_t)(a1 + 127) << 23))),
                             make_float2(f0, f1));
-    y0 = x0 != x0 ? x0 : (x0 > 88.7228f ? __int_as_float(0x7F800000) : (x0 < -103.98f ? 0.0f : v.x));
-    y1 = x1 != x1 ? x1 : (x1 > 88.7228f ? __int_as_float(0x7F800000) : (x1 < -103.98f ? 0.0f : v.y));
+    y0 = x0 != x0 ? x0 : (x0 < -103.98f ? 0.0f : v.x);
+    y1 = x1 != x1 ? x1 : (x1 < -103.98f ? 0.0f : v.y);
 }
 
 // ---- compressor state ----------------------------------------------------------------
@@ -246,8 +248,8 @@ __device__ __forceinline__ void compress_token(const CompressParams& p, int32_t 
             if (j < window) {
 #pragma unroll
                 for (int e = 0; e < CPT; e += 2)
-                    cw_exp2(__fsub_rn(sv[j][e], mx[e]), __fsub_rn(sv[j][e + 1], mx[e + 1]),
-                            ex[j][e], ex[j][e + 1]);
+                    cw_exp2_nonpos(__fsub_rn(sv[j][e], mx[e]),
+                                   __fsub_rn(sv[j][e + 1], mx[e + 1]), ex[j][e], ex[j][e + 1]);
 #pragma unroll
                 for (int e = 0; e < CPT; ++e) sum[e] = __fadd_rn(sum[e], ex[j][e]);
             }
@@ -469,12 +471,13 @@ __device__ __forceinline__ float slice_pool(float* s_sc, const float* s_kv, floa
         float e[U];
 #pragma unroll
         for (int u = 0; u < U; u += 2)
-            cw_exp2(__fsub_rn(s_sc[(j + u) * kSliceCols + c], mx),
-                    __fsub_rn(s_sc[(j + u + 1) * kSliceCols + c], mx), e[u], e[u + 1]);
+            cw_exp2_nonpos(__fsub_rn(s_sc[(j + u) * kSliceCols + c], mx),
+                           __fsub_rn(s_sc[(j + u + 1) * kSliceCols + c], mx), e[u], e[u + 1]);
 #pragma unroll
         for (int u = 0; u < U; ++u) s_sc[(j + u) * kSliceCols + c] = e[u];
     }
-    for (; j < j1; ++j) s_sc[j * kSliceCols + c] = cw_exp(__fsub_rn(s_sc[j * kSliceCols + c], mx));
+    for (; j < j1; ++j)
+        s_sc[j * kSliceCols + c] = cw_exp_nonpos(__fsub_rn(s_sc[j * kSliceCols + c], mx));
     __syncthreads();
     if (q == 0) {
         float sum = 0.0f;
