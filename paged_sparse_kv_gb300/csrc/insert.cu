@@ -7,18 +7,20 @@
 //
 // Design (HBM-bound scatter, no tensor cores):
 //  * A group of LANES lanes owns one token row; each lane holds 16-byte chunks
-//    (8 bf16) loaded with ld.global.nc.L1::no_allocate, so a 512-dim row is
-//    two chunks per lane and one warp-wide load instruction moves 512 bytes.
-//  * A quant block is 8 chunks (FP8, 64 dims) or 4 chunks (MXFP4, 32 dims),
-//    held by 8 or 4 consecutive lanes: its amax is a 3- or 2-step
-//    __shfl_xor reduction.
-//  * amax is exact (a max of bf16 values): a float max in the FP8 insert, a
-//    16-bit unsigned max over the bf16 magnitude bits in the MXFP4 ones.  The
+//    (8 bf16) loaded through the read-only path, so a 512-dim row is two
+//    chunks per lane and one warp-wide load instruction moves 512 bytes.
+//  * A quant block is 8 chunks (FP8, 64 dims) or 4 chunks (MXFP4, 32 dims).
+//    FP8: 8 consecutive lanes, one chunk each, a 3-step __shfl_xor reduction.
+//    MXFP4: each lane holds adjacent chunks, so the block spans fewer lanes.
+//  * amax is exact and passes over NaN, as the oracle's ordered scan does: a
+//    binary32 max tree of the magnitudes (FP8, MXFP4) or a packed max.bf16x2
+//    (FP8 indexer: measured faster there), then shuffles across lanes.  The
 //    scale exponent ceil(log2(amax / max_code)) is read off amax's own bits
 //    (no divide, no log2); scaling is a packed mul.rn.f32x2 per pair.
 //  * Codes are packed with cvt.rn.satfinite.{e4m3x2,e2m1x2}.f32 and stored as
-//    8-byte (FP8) / 4-byte (MXFP4) words: a group's stores of one record are
-//    contiguous and coalesce; the rope tail moves as untouched 16-byte chunks.
+//    8-byte words (FP8: one per chunk; MXFP4: a lane's adjacent chunks at 128
+//    dims): a group's stores of one record are contiguous and coalesce; the
+//    rope tail moves as untouched 16-byte chunks.
 //  * Each quant block's first lane stores the block's scale byte (or binary32
 //    scale): the bytes of one token are adjacent, so the stores of a group
 //    coalesce into one request per chunk column.
@@ -95,9 +97,7 @@ fp8_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
             const uint4 w = v[u][i];
             float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                           bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-            // fmaxf passes over NaN, as an ordered "a > amax" scan does.
-            float am = fmaxf(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))),
-                             fmaxf(fmaxf(fabsf(x[4]), fabsf(x[5])), fmaxf(fabsf(x[6]), fabsf(x[7]))));
+            float am = absmax_bf16x8(w);
             am = fmaxf(am, __shfl_xor_sync(gmask, am, 1));
             am = fmaxf(am, __shfl_xor_sync(gmask, am, 2));
             am = fmaxf(am, __shfl_xor_sync(gmask, am, 4));
@@ -145,7 +145,9 @@ fp8_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
 
 // Lanes per token of the MXFP4 insert: two 16-byte chunks per lane where the
 // row allows it (halving the per-token slot, address and branch work of one
-// chunk per lane), at least the 4 lanes of one 32-element block.
+// chunk per lane), at least the 4 lanes of one 32-element block.  In the insert a
+// lane holds adjacent chunks, so a block spans 4 / chunks-per-lane lanes (2 at
+// 128 dims: one shuffle step) and the lane's codes leave in one store.
 template <int D>
 __host__ __device__ constexpr int mxfp4_lanes() {
     constexpr int half = D / 16;
@@ -161,8 +163,9 @@ mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
     constexpr int CHUNKS = D / 8;
     constexpr int LANES = mxfp4_lanes<D>();
     constexpr int CPL = CHUNKS / LANES;
-    constexpr int VB = D / 2;   // value bytes per token
-    static_assert(CPL * LANES == CHUNKS && LANES % 4 == 0, "a block spans 4 lanes");
+    constexpr int LPB = CPL >= 4 ? 1 : 4 / CPL;   // lanes per 32-element block
+    constexpr int VB = D / 2;
+    static_assert(CPL * LANES == CHUNKS && (CPL == 1 || CPL == 2 || CPL == 4), "chunks per lane");
 
     const int lane = threadIdx.x & 31;
     const int grp = lane / LANES, gl = lane % LANES;
@@ -181,9 +184,11 @@ mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
         s[u] = -1;
         if (t < n) {
             s[u] = __ldg(slots + t);
-            const uint16_t* row = k + t * k_row_stride;
+            // the lane's CPL chunks are adjacent: the second 16-byte load of a
+            // 32-byte sector hits in L1
+            const uint4* row = reinterpret_cast<const uint4*>(k + t * k_row_stride) + CPL * gl;
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) v[u][i] = ld_stream_v4(row + 8 * (gl + i * LANES));
+            for (int i = 0; i < CPL; ++i) v[u][i] = __ldg(row + i);
         }
     }
 
@@ -201,29 +206,52 @@ mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
         uint8_t* vals = base + off * VB;
         uint8_t* scl = base + (int64_t)bs * VB + off * (D / 32);
 
+        float x[CPL][8];
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
-            const int c = gl + i * LANES;
             const uint4 w = v[u][i];
-            float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                          bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-            uint32_t amb = absmax_bf16x8_bits(w);
-            amb = max(amb, __shfl_xor_sync(gmask, amb, 1));
-            amb = max(amb, __shfl_xor_sync(gmask, amb, 2));
-            const float a = fmaxf(__uint_as_float(amb << 16), 1.0e-4f);
-            const int e = ceil_log2_div_const(a, 0x400000u, 2);  // / 6
-            const uint64_t pw2 = splat_f32x2(exp2_int(-e));
-            uint32_t word = 0;
+            const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                x[i][2 * h] = bf16_lo(q[h]);
+                x[i][2 * h + 1] = bf16_hi(q[h]);
+            }
+        }
+        // A lane's chunks all lie in one block; fmaxf passes over NaN, as an
+        // ordered "a > amax" scan does.
+        float am = 0.0f;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(x[i][j]));
+#pragma unroll
+        for (int m = 1; m < LPB; m <<= 1) am = fmaxf(am, __shfl_xor_sync(gmask, am, m));
+        const float a = fmaxf(am, 1.0e-4f);
+        const int e = ceil_log2_div_const(a, 0x400000u, 2);  // / 6
+        const uint64_t pw2 = splat_f32x2(exp2_int(-e));
+        uint32_t words[CPL];
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            uint32_t cd[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                float lo = x[2 * j], hi = x[2 * j + 1];
+                float lo = x[i][2 * j], hi = x[i][2 * j + 1];
                 mul2_rn(lo, hi, pw2);
-                word |= (cvt_e2m1x2(lo, hi) & 0xFFu) << (8 * j);
+                cd[j] = cvt_e2m1x2(lo, hi);
             }
-            *reinterpret_cast<uint32_t*>(vals + 4 * c) = word;
-            // the block's first lane writes its scale byte
-            if ((gl & 3) == 0) scl[c / 4] = (uint8_t)min(max(e + 127, 0), 254);
+            words[i] = __byte_perm(__byte_perm(cd[0], cd[1], 0x0040),
+                                   __byte_perm(cd[2], cd[3], 0x0040), 0x5410);
         }
+        uint8_t* vp = vals + 4 * CPL * gl;
+        if constexpr (CPL == 1) {
+            *reinterpret_cast<uint32_t*>(vp) = words[0];
+        } else if constexpr (CPL == 2) {
+            *reinterpret_cast<uint2*>(vp) = make_uint2(words[0], words[1]);
+        } else {
+            *reinterpret_cast<uint4*>(vp) = make_uint4(words[0], words[1], words[2], words[3]);
+        }
+        // the block's first lane writes its scale byte
+        if (gl % LPB == 0) scl[CPL * gl / 4] = (uint8_t)min(max(e + 127, 0), 254);
     }
 }
 
@@ -234,7 +262,8 @@ mxfp4_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
 // binary32 scale per token, 2^ceil(log2(max(amax / 448, 1e-10))) -- the
 // quotient is floored, not amax -- and codes e4m3(x / scale), computed as
 // x * 2^-e (the same single rounding of the same exact value).  Lanes as the
-// MXFP4 insert; the row amax is an integer shuffle-max over the token's lanes.
+// MXFP4 insert; the row amax is a packed bf16x2 max per lane, then a float
+// shuffle-max over the token's lanes.
 template <int D, int UNROLL>
 __global__ void __launch_bounds__(kThreads)
 fp8_indexer_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
@@ -282,14 +311,15 @@ fp8_indexer_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
         uint8_t* base = cache + page * page_stride;
         uint8_t* vals = base + off * D;
 
-        uint32_t amb = 0;
+        uint32_t mp = absmax_bf16x8_pair(v[u][0]);
 #pragma unroll
-        for (int i = 0; i < CPL; ++i) amb = max(amb, absmax_bf16x8_bits(v[u][i]));
+        for (int i = 1; i < CPL; ++i) mp = bmax2(mp, absmax_bf16x8_pair(v[u][i]));
+        float am = absmax_of_pair(mp);
 #pragma unroll
-        for (int m = 1; m < LANES; m <<= 1) amb = max(amb, __shfl_xor_sync(gmask, amb, m));
-        const float q = fmaxf(__fdiv_rn(__uint_as_float(amb << 16), 448.0f), 1.0e-10f);
+        for (int m = 1; m < LANES; m <<= 1) am = fmaxf(am, __shfl_xor_sync(gmask, am, m));
+        const float q = fmaxf(__fdiv_rn(am, 448.0f), 1.0e-10f);
         const int e = ceil_log2_pos(q);
-        const uint64_t pw2 = splat_f32x2(exp2_int(-e));
+        const uint64_t pw2 = splat_f32x2(inv_pow2_scale(e));  // codes e4m3(x / 2^e)
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
             const int c = gl + i * LANES;
@@ -524,7 +554,7 @@ __device__ __forceinline__ void nrs_compute_store(const NormRopeParams& p, int32
         for (int m = 1; m < LPT; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, m));
         // max(a / 448, 1e-10) then ceil(log2): the floor's exponent is -33
         const int e = max(ceil_log2_div_const(a, 0x600000u, 8), -33);
-        const uint64_t pw = splat_f32x2(exp2_int(-e));
+        const uint64_t pw = splat_f32x2(inv_pow2_scale(e));  // codes e4m3(y / 2^e)
         uint32_t qa[2], qb[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {

@@ -81,6 +81,12 @@ __device__ __forceinline__ float exp2_int(int k) {
     return __uint_as_float(1u << (k + 149));
 }
 
+// The factor f with x * f == x / scale for a power-of-two binary32 scale
+// 2^e, e in [-127, 128]: 2^-e while 2^e is finite (both a single rounding of
+// the same exact value); at e = 128 the scale itself rounds to +inf, and
+// x / inf (+-0 for finite x, NaN for +-inf and NaN) is x * 0.
+__device__ __forceinline__ float inv_pow2_scale(int e) { return e >= 128 ? 0.0f : exp2_int(-e); }
+
 // Smallest e with 2^e >= q for finite q > 0 (normal q): read off the bits.
 // q = +inf gives 128.
 __device__ __forceinline__ int ceil_log2_pos(float q) {
@@ -110,14 +116,32 @@ __device__ __forceinline__ int ceil_log2_div_const(float a, uint32_t cs_mant, in
     return x - cx + ((b & 0x7FFFFFu) > cs_mant ? 1 : 0);
 }
 
-// Largest |x| of eight bf16 values (packed in a uint4) as the bf16 bit pattern
-// of the magnitude, zero-extended: for non-negative finite values the bit order
-// is the numeric order, so a 16-bit unsigned max is exact.
-__device__ __forceinline__ uint32_t absmax_bf16x8_bits(uint4 w) {
-    uint32_t m = __vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu);
-    m = __vmaxu2(m, w.z & 0x7FFF7FFFu);
-    m = __vmaxu2(m, w.w & 0x7FFF7FFFu);
-    return max(m & 0xFFFFu, m >> 16);
+// Elementwise max of two bf16x2 words.  max.bf16x2 (no .NaN) returns the
+// other operand where one is NaN and NaN only where both are.
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Per-half largest |x| of eight bf16 values (packed in a uint4), as a bf16x2
+// word: NaN entries are passed over, as an ordered "a > amax" scan does.
+__device__ __forceinline__ uint32_t absmax_bf16x8_pair(uint4 w) {
+    constexpr uint32_t M = 0x7FFF7FFFu;
+    return bmax2(bmax2(w.x & M, w.y & M), bmax2(w.z & M, w.w & M));
+}
+
+// The same over a whole bf16x2 word, as a binary32 (exact).
+__device__ __forceinline__ float absmax_of_pair(uint32_t m) { return fmaxf(bf16_lo(m), bf16_hi(m)); }
+
+// Largest |x| of eight bf16 values (packed in a uint4) as a binary32 max tree
+// (exact); fmaxf passes over NaN like max.bf16x2.  Cheaper than the packed
+// form where the kernel unpacks the values anyway.
+__device__ __forceinline__ float absmax_bf16x8(uint4 w) {
+    return fmaxf(fmaxf(fmaxf(fabsf(bf16_lo(w.x)), fabsf(bf16_hi(w.x))),
+                       fmaxf(fabsf(bf16_lo(w.y)), fabsf(bf16_hi(w.y)))),
+                 fmaxf(fmaxf(fabsf(bf16_lo(w.z)), fabsf(bf16_hi(w.z))),
+                       fmaxf(fabsf(bf16_lo(w.w)), fabsf(bf16_hi(w.w)))));
 }
 
 // {lo, hi} * {s, s} in one packed multiply (IEEE RN per element, no flush).

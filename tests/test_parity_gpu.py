@@ -113,6 +113,29 @@ def test_fp8_insert_exhaustive_codes(cuda_device):
     _assert_same(dev_cache.cpu().numpy(), host, "exhaustive fp8 codes")
 
 
+_SPECIALS = np.array([0x7F80, 0xFF80, 0x7FC0, 0xFFC0, 0x7F81, 0xFF81, 0x8000, 0x7F7F, 0xFF7F],
+                     np.uint16)   # +-inf, +-qNaN, +-sNaN, -0, +-largest finite
+
+
+def _rows_with_specials(rng, N, D, block, nblk):
+    """bf16 rows ~ 3 N(0,1) with, in the first nblk blocks of `block` elements:
+    a few scattered specials, whole blocks of NaN, whole blocks of +-0."""
+    vals = rng.standard_normal((N, D)).astype(np.float32) * 3
+    k = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for t in range(N):
+        for b in range(nblk):
+            kind = (t * 7 + b) % 5
+            if kind == 0:
+                pos = rng.choice(block, size=3, replace=False)
+                k[t, b * block + pos] = rng.choice(_SPECIALS, size=3)
+            elif kind == 1 and t % 3 == 0:
+                k[t, b * block:(b + 1) * block] = rng.choice(_SPECIALS[2:6], size=block)
+            elif kind == 2 and t % 4 == 1:
+                k[t, b * block:(b + 1) * block] = rng.choice(np.array([0, 0x8000], np.uint16),
+                                                             size=block)
+    return k
+
+
 def _fp8_code_positions(slots, num_pages, page_stride, bs, ts, nope):
     """Flat byte offsets of the e4m3 codes of each inserted token."""
     page, off = slots // bs, slots % bs
@@ -130,20 +153,7 @@ def test_fp8_insert_non_finite_inputs(cuda_device, ue8m0):
     rng = np.random.default_rng(11)
     D, rope, N, bs = 512, 64, 96, 16
     nope = D - rope
-    vals = rng.standard_normal((N, D)).astype(np.float32) * 3
-    k = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-    specials = np.array([0x7F80, 0xFF80, 0x7FC0, 0xFFC0, 0x7F81, 0xFF81, 0x8000, 0x7F7F, 0xFF7F],
-                        np.uint16)
-    for t in range(N):
-        for b in range(nope // 64):
-            kind = (t * 7 + b) % 5
-            if kind == 0:    # a few scattered specials
-                pos = rng.choice(64, size=3, replace=False)
-                k[t, b * 64 + pos] = rng.choice(specials, size=3)
-            elif kind == 1 and t % 3 == 0:   # whole block NaN
-                k[t, b * 64:(b + 1) * 64] = rng.choice(specials[2:6], size=64)
-            elif kind == 2 and t % 4 == 1:   # whole block zero, signs mixed
-                k[t, b * 64:(b + 1) * 64] = rng.choice(np.array([0, 0x8000], np.uint16), size=64)
+    k = _rows_with_specials(rng, N, D, 64, nope // 64)
     rec = oracle.fp8_record_bytes(D, rope, ue8m0)
     pages = N // bs + 2
     geom = synthetic.CacheGeom(pages, bs, (bs * rec + 15) // 16 * 16)
@@ -176,6 +186,23 @@ def test_mxfp4_insert_exhaustive_codes(cuda_device):
                                   torch.from_numpy(slots).to(cuda_device), bs)
     oracle.write_indexer_mxfp4_cache(rows, slots, host, bs, 128)
     _assert_same(dev_cache.cpu().numpy(), host, "exhaustive mxfp4 codes")
+
+
+def test_mxfp4_insert_non_finite_inputs(cuda_device):
+    """+-inf, NaN of both signs, all-NaN and all-zero blocks in 128-dim keys:
+    amax passes over NaN, +-inf and NaN saturate to the E2M1 codes the oracle
+    gives (E2M1 has neither), every byte must match."""
+    rng = np.random.default_rng(12)
+    D, N, bs = 128, 200, 16
+    k = _rows_with_specials(rng, N, D, 32, D // 32)
+    pages = N // bs + 3
+    host = np.full((pages, bs * (D // 2 + D // 32)), 0x5A, np.uint8)
+    slots = rng.permutation(pages * bs)[:N].astype(np.int64)
+    dev_cache = torch.from_numpy(host).to(cuda_device)
+    ops.write_indexer_mxfp4_cache(_bf16_dev(k, cuda_device), dev_cache,
+                                  torch.from_numpy(slots).to(cuda_device), bs)
+    oracle.write_indexer_mxfp4_cache(k, slots, host, bs, D)
+    _assert_same(dev_cache.cpu().numpy(), host, "non-finite mxfp4 insert")
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "mxfp4"])

@@ -36,6 +36,31 @@ def test_fp8_indexer_insert_exhaustive_codes(cuda_device):
     _assert_same(dev_cache.cpu().numpy(), host, "exhaustive fp8 indexer codes")
 
 
+def test_fp8_indexer_insert_non_finite_inputs(cuda_device):
+    """+-inf, NaN of both signs, all-NaN and all-zero stretches in 128-dim keys:
+    the row amax passes over NaN, +-inf saturates to +-448.  Where the oracle
+    writes an E4M3 NaN the kernel's byte must be a NaN of either sign; every
+    other byte (codes and binary32 scales) must match."""
+    from test_parity_gpu import _fp8_code_positions, _rows_with_specials
+    rng = np.random.default_rng(13)
+    D, N, bs = 128, 200, 16
+    k = _rows_with_specials(rng, N, D, 32, D // 32)
+    pages = N // bs + 3
+    host = np.full((pages, bs * (D + 4)), 0x5A, np.uint8)
+    slots = rng.permutation(pages * bs)[:N].astype(np.int64)
+    dev_cache = torch.from_numpy(host).to(cuda_device)
+    ops.write_indexer_fp8_cache(_bf16_dev(k, cuda_device), dev_cache, _i64(slots, cuda_device), bs)
+    oracle.write_indexer_fp8_cache(k, slots, host, bs, D)
+    got = dev_cache.cpu().numpy().reshape(-1).copy()
+    want = host.reshape(-1)
+    codes = _fp8_code_positions(slots, pages, bs * (D + 4), bs, D, D)
+    nan_at = codes[want[codes] == 0x7F]
+    assert nan_at.size > 0
+    assert np.all((got[nan_at] & 0x7F) == 0x7F), "NaN input must give an E4M3 NaN code"
+    got[nan_at] = 0x7F
+    _assert_same(got, want, "non-finite fp8 indexer insert")
+
+
 @pytest.mark.parametrize("bs", [64, 7])
 @pytest.mark.parametrize("D", [32, 64, 128, 256, 512, 1024])
 def test_fp8_indexer_insert_shapes_and_skips(cuda_device, D, bs):
@@ -136,6 +161,43 @@ def test_norm_rope_store_fuzz(cuda_device, fp4, ratio, bs, cs_pad):
                                              slots, ratio, 1 if fp4 else 2, host, bs)
     _assert_same(dev_cache.cpu().numpy(), host, f"norm rope store fp4={fp4} ratio={ratio}")
     assert int(err.item()) == n_err and n_err >= 2
+
+
+@pytest.mark.parametrize("fp4", [True, False])
+def test_norm_rope_store_overflowing_weights(cuda_device, fp4):
+    """Norm weights near the binary32 maximum push some normalised values to
+    +-inf: the FP8 row scale 2^ceil(log2(amax / 448)) then rounds to +inf and
+    the codes are e4m3(y / inf) (+-0, NaN for +-inf); MXFP4 codes are
+    e2m1(y * 2^-128) (+-6 for +-inf).  E4M3 NaN bytes may carry either sign."""
+    from test_parity_gpu import _fp8_code_positions
+    rng = np.random.default_rng(31 + fp4)
+    N, bs, max_pos = 300, 16, 1024
+    pages = N // bs + 2
+    x = rng.standard_normal((N, 128)).astype(np.float32)
+    k = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    pos = rng.integers(0, max_pos, size=N).astype(np.int64)
+    slots = rng.permutation(pages * bs)[:N].astype(np.int64)
+    cs = _gptj_table(max_pos)
+    w = rng.uniform(0.25, 4.0, size=128).astype(np.float32)
+    w[[3, 40, 70, 101]] = [3.0e38, -3.0e38, 3.0e38, 3.0e38]
+    rec = 68 if fp4 else 132
+    stride = bs * rec
+    host = np.full((pages, stride), 0x5A, np.uint8)
+    d = cuda_device
+    dev_cache = torch.from_numpy(host).to(d)
+    ops.indexer_k_norm_rope_store(_bf16_dev(k, d), _i64(pos, d), torch.from_numpy(cs).to(d),
+                                  torch.from_numpy(w).to(d), 1e-6, dev_cache, _i64(slots, d), 1,
+                                  fp4, bs)
+    oracle.indexer_k_norm_rope_store(k, pos, cs, w, 1e-6, slots, 1, 1 if fp4 else 2, host, bs)
+    got = dev_cache.cpu().numpy().reshape(-1).copy()
+    want = host.reshape(-1)
+    if not fp4:
+        codes = _fp8_code_positions(slots, pages, stride, bs, 128, 128)
+        nan_at = codes[want[codes] == 0x7F]
+        assert nan_at.size > 0
+        assert np.all((got[nan_at] & 0x7F) == 0x7F), "NaN must give an E4M3 NaN code"
+        got[nan_at] = 0x7F
+    _assert_same(got, want, f"norm rope store, overflowing weights, fp4={fp4}")
 
 
 def test_norm_rope_store_prefill_size(cuda_device):
