@@ -51,8 +51,15 @@ namespace {
 #ifndef PSK_INDEX_MIN_CTAS
 #define PSK_INDEX_MIN_CTAS 3
 #endif
+// Resident CTAs per SM asked of the staged-row builders: the top-k map fits 5
+// without spilling (20.7 -> 19.3 us on the 16384-token prefill); the fused
+// window + top-k build keeps 4 (at 5 it spills and gains nothing, at 6 it
+// slows to 24.6 us from 22.5).
 #ifndef PSK_INDEX_TMA_MIN_CTAS
-#define PSK_INDEX_TMA_MIN_CTAS 4
+#define PSK_INDEX_TMA_MIN_CTAS 5
+#endif
+#ifndef PSK_INDEX_TMA_MIN_CTAS_SWA
+#define PSK_INDEX_TMA_MIN_CTAS_SWA 4
 #endif
 
 constexpr int kThreads = 256;
@@ -520,7 +527,9 @@ __device__ __forceinline__ void stage_row(int32_t* dst, const int32_t* src, int 
 }
 
 template <bool HAS_SWA, bool VEC, bool POW2, bool TMA>
-__global__ void __launch_bounds__(kThreads, TMA ? PSK_INDEX_TMA_MIN_CTAS : PSK_INDEX_MIN_CTAS)
+__global__ void __launch_bounds__(kThreads, TMA ? (HAS_SWA ? PSK_INDEX_TMA_MIN_CTAS_SWA
+                                                           : PSK_INDEX_TMA_MIN_CTAS)
+                                                : PSK_INDEX_MIN_CTAS)
 index_build_kernel(IndexParams p) {
     // Dynamic shared memory: [TMA: tokens_per_cta top-k rows][compressed
     // table row + 1][SWA table row + 1].  With staged top-k rows and
