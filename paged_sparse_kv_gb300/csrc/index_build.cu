@@ -51,15 +51,18 @@ namespace {
 #ifndef PSK_INDEX_MIN_CTAS
 #define PSK_INDEX_MIN_CTAS 3
 #endif
-// Resident CTAs per SM asked of the staged-row builders: the top-k map fits 5
-// without spilling (20.7 -> 19.3 us on the 16384-token prefill); the fused
-// window + top-k build keeps 4 (at 5 it spills and gains nothing, at 6 it
-// slows to 24.6 us from 22.5).
+// Resident CTAs per SM asked of the staged-row builders (launch bounds).  Four
+// by default.  The top-k map also has a build for 5 (46 registers instead of 53,
+// no spills), taken when the grid exceeds one wave at 4 per SM: on the
+// 16384-token prefill (3.4 waves) it runs 19.9 us against 20.8; inside one wave
+// (the 4352-token mixed batch) the 53-register build is faster (14.3 us against
+// 16.3).  The fused window + top-k build stays at 4 (at 5 it spills and gains
+// nothing, at 3 or 6 it slows from 22.5 to 24.6 us).
 #ifndef PSK_INDEX_TMA_MIN_CTAS
-#define PSK_INDEX_TMA_MIN_CTAS 5
+#define PSK_INDEX_TMA_MIN_CTAS 4
 #endif
-#ifndef PSK_INDEX_TMA_MIN_CTAS_SWA
-#define PSK_INDEX_TMA_MIN_CTAS_SWA 4
+#ifndef PSK_INDEX_TMA_MIN_CTAS_WIDE
+#define PSK_INDEX_TMA_MIN_CTAS_WIDE 5
 #endif
 
 constexpr int kThreads = 256;
@@ -526,10 +529,8 @@ __device__ __forceinline__ void stage_row(int32_t* dst, const int32_t* src, int 
     }
 }
 
-template <bool HAS_SWA, bool VEC, bool POW2, bool TMA>
-__global__ void __launch_bounds__(kThreads, TMA ? (HAS_SWA ? PSK_INDEX_TMA_MIN_CTAS_SWA
-                                                           : PSK_INDEX_TMA_MIN_CTAS)
-                                                : PSK_INDEX_MIN_CTAS)
+template <bool HAS_SWA, bool VEC, bool POW2, bool TMA, int MINB = PSK_INDEX_TMA_MIN_CTAS>
+__global__ void __launch_bounds__(kThreads, TMA ? MINB : PSK_INDEX_MIN_CTAS)
 index_build_kernel(IndexParams p) {
     // Dynamic shared memory: [TMA: tokens_per_cta top-k rows][compressed
     // table row + 1][SWA table row + 1].  With staged top-k rows and
@@ -999,7 +1000,10 @@ cudaError_t launch_index_build(IndexParams p, bool has_swa, cudaStream_t stream)
           index_build_kernel<true, true, false, true>},
          {index_build_kernel<true, false, true, false>, index_build_kernel<true, true, true, false>,
           index_build_kernel<true, true, true, true>}}};
-    const Kern kern = kTable[has_swa][pow2][tma ? 2 : (vec ? 1 : 0)];
+    Kern kern = kTable[has_swa][pow2][tma ? 2 : (vec ? 1 : 0)];
+    if (tma && !has_swa && blocks > (int64_t)sms * PSK_INDEX_TMA_MIN_CTAS)
+        kern = pow2 ? index_build_kernel<false, true, true, true, PSK_INDEX_TMA_MIN_CTAS_WIDE>
+                    : index_build_kernel<false, true, false, true, PSK_INDEX_TMA_MIN_CTAS_WIDE>;
     const cudaError_t e = allow_dynamic_smem(kern, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), smem, stream, p);
