@@ -24,8 +24,9 @@
 //  * Each quant block's first lane stores the block's scale byte (or binary32
 //    scale): the bytes of one token are adjacent, so the stores of a group
 //    coalesce into one request per chunk column.
-//  * Each group handles UNROLL tokens with all loads issued before any use,
-//    so enough bytes are in flight to cover HBM latency.
+//  * Each group handles UNROLL tokens with all loads issued before any use
+//    (two for the MXFP4 and indexer inserts; one for the FP8 insert, whose
+//    32-register build keeps 64 warps per SM in flight instead).
 #include "insert.h"
 #include "psk_common.cuh"
 
