@@ -27,6 +27,19 @@
  * - Data-dependent problems never fault: a slot, page or index outside the
  *   cache or table is skipped or emitted as -1 ("fail closed", [MDL]
  *   _deepseek_v4_swa_slot_mapping), as each entry point states.
+ * - Every kernel is launched with programmatic dependent launch: it may start
+ *   while the previous kernel on `stream` is finishing, and waits for that
+ *   kernel to complete before it reads a cache, reads an index matrix or
+ *   writes any output.  compute_global_topk_indices_and_lens,
+ *   combine_topk_swa_indices, decode_swa_indices_and_lens and the gathers that
+ *   compute their own slots (_topk, _window, _dense, _ranges) read their
+ *   metadata inputs (positions, query_start_loc, seq_lens, token_to_req,
+ *   replay_start, base offsets, is_valid_token, top-k indices, block tables)
+ *   before that wait.
+ *   No libpsk kernel writes those inputs, and a kernel that does not itself
+ *   trigger its dependents early is complete before a libpsk kernel starts;
+ *   so only a caller's own programmatic-launch kernel that triggers early
+ *   must have finished writing them before it triggers.
  *
  * Cache records ("pages")
  * -----------------------
