@@ -251,3 +251,65 @@ def test_fp32_scale_record_division_identity(oracle_mod):
             data = cache[page, off * ts + b * 64: off * ts + (b + 1) * 64]
             assert np.array_equal(data, codes)
         assert scl[7] == 0.0
+
+
+# ---- non-finite inputs (closed forms) ----------------------------------------------------
+
+_NAN, _NNAN, _INF, _NINF = 0x7FC0, 0xFFC0, 0x7F80, 0xFF80
+
+
+def test_codec_specials():
+    """E4M3: NaN -> S.1111.111 (0x7F), +-inf and anything >= 448 saturate to
+    +-448 (0x7E / 0xFE).  E2M1 has no NaN or inf: +-inf saturate to +-6, NaN -> +6."""
+    import oracle
+    v = np.array([np.nan, -np.nan, np.inf, -np.inf, 448.0, 1e30, -500.0], np.float32)
+    assert oracle.e4m3_encode(v).tolist() == [0x7F, 0x7F, 0x7E, 0xFE, 0x7E, 0x7E, 0xFE]
+    assert oracle.e2m1_encode(v).tolist() == [0x7, 0x7, 0x7, 0xF, 0x7, 0x7, 0xF]
+
+
+def _fp8_insert_one(row_bits):
+    import oracle
+    D, rope, bs = 128, 0, 1
+    cache = np.zeros((1, oracle.fp8_record_bytes(D, rope)), np.uint8)
+    oracle.quantize_and_insert_k_cache(row_bits[None, :], np.zeros(1, np.int64), cache, bs, D, rope)
+    return cache[0, :D], cache[0, D:D + 2]
+
+
+def test_fp8_insert_block_amax_passes_over_nan():
+    """Block 0 = [NaN, 3, -1, 0...]: amax 3 (NaN skipped), e = ceil(log2(3/448)) = -7,
+    byte 120, codes 3 * 2^7 = 384 -> 0x7C, -128 -> 0xF0, NaN -> 0x7F.  Block 1 all NaN:
+    amax 0 -> the 1e-4 floor, e = ceil(log2(1e-4/448)) = -22, byte 105, codes NaN."""
+    row = np.zeros(128, np.uint16)
+    row[0], row[1], row[2] = _NAN, _bf16_bits([3.0])[0], _bf16_bits([-1.0])[0]
+    row[64:128] = _NNAN
+    codes, scales = _fp8_insert_one(row)
+    assert scales.tolist() == [120, 105]
+    assert codes[:3].tolist() == [0x7F, 0x7C, 0xF0] and not codes[3:64].any()
+    assert np.all(codes[64:] == 0x7F)
+
+
+def test_fp8_insert_block_with_inf():
+    """Block 0 = [inf, -inf, 1, 0...]: amax inf, e = 128, byte clamped to 255;
+    codes +-inf * 2^-128 = +-inf -> +-448 (0x7E / 0xFE), 1 * 2^-128 -> 0."""
+    row = np.zeros(128, np.uint16)
+    row[0], row[1], row[2] = _INF, _NINF, _bf16_bits([1.0])[0]
+    codes, scales = _fp8_insert_one(row)
+    assert scales[0] == 255
+    assert codes[:3].tolist() == [0x7E, 0xFE, 0x00]
+
+
+def test_mxfp4_insert_block_amax_passes_over_nan():
+    """Block 0 = [NaN, 3, 0...]: amax 3, e = ceil(log2(3/6)) = -1, byte 126; codes
+    NaN -> 0x7 (low nibble), 3 * 2 = 6 -> 0x7 (high nibble).  Block 1 = [inf, 0...]:
+    e = 128, byte clamped to 254, inf -> 0x7."""
+    import oracle
+    D = 128
+    row = np.zeros(D, np.uint16)
+    row[0], row[1] = _NAN, _bf16_bits([3.0])[0]
+    row[32] = _INF
+    cache = np.zeros((1, oracle.mxfp4_record_bytes(D)), np.uint8)
+    oracle.write_indexer_mxfp4_cache(row[None, :], np.zeros(1, np.int64), cache, 1, D)
+    vals, scales = cache[0, :D // 2], cache[0, D // 2:]
+    assert vals[0] == 0x77 and not vals[1:16].any()
+    assert scales[0] == 126 and scales[1] == 254
+    assert vals[16] == 0x07 and not vals[17:32].any()
