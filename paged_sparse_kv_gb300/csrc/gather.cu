@@ -378,6 +378,13 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
 // scale) before it converts and stores anything.
 // REC 1: MXFP4 (TokenSpeed read_deepseek_v4_indexer_mxfp4_cache); REC 2: the
 // FP8 indexer record (write_deepseek_v4_indexer_fp8_cache's layout).
+// Rows per lane group in one batch of the small-record gather.  Four keeps the
+// kernel at 32-36 registers: the decode step, where it shares the SMs with the
+// FP8 gathers and the builders, ran 22.2-22.5 us against 23.1 with eight (52
+// registers) and 27.3 with sixteen (80); the 262,144-row MXFP4 gather alone is
+// the same (20.5 us) with four or eight.
+constexpr int kSmallSteps = 4;
+
 template <int D, int REC, int SRC>
 __global__ void __launch_bounds__(kThreads)
 gather_small_kernel(GatherParams p, TopkSource tk) {
@@ -385,7 +392,7 @@ gather_small_kernel(GatherParams p, TopkSource tk) {
     constexpr int LANES = CHUNKS < kWarp ? CHUNKS : kWarp;
     constexpr int CPL = CHUNKS / LANES;
     constexpr int GPW = kWarp / LANES;
-    constexpr int STEPS = (kWarp / GPW) < 8 ? (kWarp / GPW) : 8;
+    constexpr int STEPS = (kWarp / GPW) < kSmallSteps ? (kWarp / GPW) : kSmallSteps;
     constexpr int BATCH = STEPS * GPW;  // <= 32 items, one slot id per lane
     constexpr int VB = REC == 1 ? D / 2 : D;    // value bytes per token
     constexpr int SB = REC == 1 ? D / 32 : 4;   // scale bytes per token
@@ -554,7 +561,7 @@ cudaError_t gather_small_dispatch(const GatherParams& p, const TopkSource& tk,
                                   cudaStream_t stream) {
     constexpr int LANES = (D / 8) < kWarp ? (D / 8) : kWarp;
     constexpr int GPW = kWarp / LANES;
-    constexpr int STEPS = (kWarp / GPW) < 8 ? (kWarp / GPW) : 8;
+    constexpr int STEPS = (kWarp / GPW) < kSmallSteps ? (kWarp / GPW) : kSmallSteps;
     const int64_t items = p.rows * (int64_t)p.cols;
     auto kern = gather_small_kernel<D, REC, SRC>;
     const int64_t batches = (items + STEPS * GPW - 1) / (STEPS * GPW);
