@@ -21,8 +21,10 @@
  *   [MX]   OCP Microscaling Formats (MX) v1.0, E2M1 element and E8M0 scale
  *
  * Parity pins live in tests/test_oracle_*.py.  The fp32-scale FP8 record
- * (is_ue8m0 = 0) is "parity unpinned" beyond its IEEE-division identity: no
- * page prints that rule.
+ * (is_ue8m0 = 0) is printed on no page; its rule (scale = max(amax, 1e-12) /
+ * 448 and the codes of x / scale, both IEEE binary32 divisions) is pinned by a
+ * hand-worked golden record (insert and gather) and against torch's e4m3
+ * encode and decode.
  */
 #include "psk_oracle.h"
 
@@ -201,7 +203,7 @@ int64_t oracle_fp8_scale_bytes(int32_t head_dim, int32_t is_ue8m0) {
  *       e = ceil(log2(amax / 448)) taken exactly on the binary32 quotient;
  *       scale byte = clamp(e + 127, 0, 255);
  *       code = e4m3(clamp(x * 2^-e, -448, 448)).
- *     is_ue8m0 = 0 (fp32 scales, not on the pages -- parity unpinned):
+ *     is_ue8m0 = 0 (fp32 scales, not on the pages):
  *       scale = max(amax, 1e-12) / 448 (binary32, stored little-endian);
  *       code = e4m3(clamp(x / scale, -448, 448)).
  *   The rope dims are copied as bf16 bit patterns; unused scale slots are 0.

@@ -11,9 +11,9 @@
  * Parity pins: every function below is pinned by the CPU test-suite against
  * something other than itself (format definitions enumerated exhaustively, a
  * library cast, brute-force enumeration of windows and slots, hand-worked
- * golden records, invariants).  One function has a weaker pin and is marked
- * "parity unpinned" where it is defined: the fp32-scale FP8 record
- * (is_ue8m0 = 0), whose rule no page prints.  indexer_k_norm_rope_store takes
+ * golden records, invariants).  The fp32-scale FP8 record (is_ue8m0 = 0),
+ * whose rule no page prints, is pinned by a hand-worked record (insert and
+ * gather) and by torch's e4m3 encode and decode.  indexer_k_norm_rope_store takes
  * two readings (pairwise summation, IEEE binary32 square root then division) that fix
  * the rounding of steps the pages leave open; its pins check the arithmetic
  * against closed forms, not a printed result.

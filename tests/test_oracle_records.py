@@ -67,6 +67,45 @@ def test_fp8_record_golden(oracle_mod):
         _check_expected(cache.reshape(-1), case["fill"], case["expected"])
 
 
+def _golden_row_bits(spec_runs, rope_bits):
+    """bf16 bit patterns of an expected gathered row: runs of hex bf16 words,
+    with "rope" standing for the row's verbatim RoPE tail."""
+    out = []
+    for count, v in spec_runs:
+        if v == "rope":
+            out.extend(rope_bits.tolist())
+        elif isinstance(v, list):
+            out.extend([int(x, 16) for x in v] * count)
+        else:
+            out.extend([int(v, 16)] * count)
+    return np.array(out, dtype=np.uint16)
+
+
+def test_fp8_record_golden_gather(oracle_mod):
+    """Cases with a hand-worked gather: the inserted record read back through
+    dequantize_and_gather_k_cache, every bf16 word as worked out by hand."""
+    spec = json.load(open(os.path.join(GOLDEN, "fp8_record_golden.json")))
+    cases = [c for c in spec["cases"] if "gather" in c]
+    assert cases, "no hand-worked gather"
+    for case in cases:
+        D, rope = case["head_dim"], case["rope_dim"]
+        rows = [_row_from_runs(r["runs"], D, rope, r.get("rope")) for r in case["rows"]]
+        k = np.stack(rows)
+        slots = np.array([r["slot"] for r in case["rows"]], dtype=np.int64)
+        cache = np.full((case["num_pages"], case["page_stride"]), case["fill"], np.uint8)
+        oracle_mod.quantize_and_insert_k_cache(k, slots, cache, case["block_size"], D, rope,
+                                               case["is_ue8m0"])
+        g = case["gather"]
+        idx = np.array([g["indices"]], dtype=np.int32)
+        out = oracle_mod.dequantize_and_gather_k_cache(cache, case["block_size"], 0, D, rope, idx,
+                                                       is_ue8m0=case["is_ue8m0"])
+        for j, want_runs in enumerate(g["rows"]):
+            s = g["indices"][j]
+            rope_bits = k[list(slots).index(s), D - rope:] if s >= 0 else None
+            want = _golden_row_bits(want_runs, rope_bits)
+            assert np.array_equal(out[0, j], want), (case["name"], j)
+
+
 def test_mxfp4_record_golden(oracle_mod):
     spec = json.load(open(os.path.join(GOLDEN, "mxfp4_record_golden.json")))
     for case in spec["cases"]:
@@ -187,6 +226,49 @@ def test_fp8_gather_decode_vs_torch_on_random_bytes(oracle_mod):
         assert np.array_equal(out[0, j, D - rope:], data[D - rope:].view(np.uint16))
 
 
+def test_fp32_scale_gather_decode_vs_torch_on_random_bytes(oracle_mod):
+    """fp32-scale records (is_ue8m0 = 0) of arbitrary bytes: every e4m3 code
+    but the two NaNs and binary32 scales of random finite bit patterns
+    (normals of every exponent, subnormals, zeros of both signs), so the
+    products round, overflow to +-inf and underflow.  Expected: torch's e4m3
+    decode, a binary32 multiply by the little-endian scale, torch's bf16
+    rounding -- with slots past the nope blocks (the pad) never read."""
+    rng = np.random.default_rng(19)
+    bs, D, rope, pages = 8, 512, 64, 6
+    nope, ts, nb = D - rope, D - rope + 2 * rope, D // 64
+    rec = oracle_mod.fp8_record_bytes(D, rope, is_ue8m0=False)
+    assert rec == ts + 4 * nb
+    cache = rng.integers(0, 254, size=(pages, bs * rec), dtype=np.uint8)
+    cache[cache >= 0x7F] += 1                       # no 0x7F / 0xFF codes
+    data = cache[:, :bs * ts].reshape(pages, bs, ts)
+    scl = rng.integers(0, 1 << 32, size=(pages, bs, nb), dtype=np.uint64).astype(np.uint32)
+    expo = (scl >> 23) & 0xFF
+    scl[expo == 0xFF] &= ~np.uint32(0x40000000)     # inf/NaN exponent -> a finite one
+    scl[0, 0, :] = np.array([0, 0x80000000, 1, 0x807FFFFF, 0x7F7FFFFF, 0x00800000, 0x3F800000,
+                             0x3B800000], np.uint32)
+    cache[:, bs * ts:] = scl.view(np.uint8).reshape(pages, bs * 4 * nb)
+    idx = np.arange(pages * bs, dtype=np.int32).reshape(pages, bs)
+    idx[1, 3] = -1
+    idx[2, 5] = pages * bs        # beyond the cache: a zero row
+    out = oracle_mod.dequantize_and_gather_k_cache(cache, bs, 0, D, rope, idx, is_ue8m0=False)
+    for r in range(pages):
+        for j in range(bs):
+            s = int(idx[r, j])
+            if s < 0 or s >= pages * bs:
+                assert np.all(out[r, j] == 0)
+                continue
+            page, off = divmod(s, bs)
+            vals = torch.from_numpy(data[page, off, :nope].copy()).view(
+                torch.float8_e4m3fn).to(torch.float32)
+            sc = torch.from_numpy(np.repeat(scl[page, off, :nope // 64], 64).view(np.float32))
+            ref = (vals * sc).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            assert np.array_equal(out[r, j, :nope], ref), (r, j)
+            assert np.array_equal(out[r, j, nope:], data[page, off, nope:].view(np.uint16))
+    flat = out[:, :, :nope].reshape(-1)
+    assert np.any(flat == 0x7F80) or np.any(flat == 0xFF80), "no product overflowed"
+    assert np.any(((flat & 0x7F80) == 0) & ((flat & 0x7FFF) != 0)), "no subnormal result"
+
+
 def test_mxfp4_gather_decode_vs_torch_on_random_bytes(oracle_mod):
     rng = np.random.default_rng(10)
     bs, D, pages = 4, 128, 3
@@ -224,7 +306,8 @@ def test_insert_skips_negative_and_counts_out_of_range(oracle_mod):
 
 
 def test_fp32_scale_record_division_identity(oracle_mod):
-    """fp32-scale record (parity unpinned beyond this identity): the stored
+    """fp32-scale record (also pinned by a hand-worked golden record and by
+    the decode against torch above): the stored
     scale is binary32 max(amax, 1e-12) / 448 and every code is the e4m3 of the
     binary32 quotient x / scale, clamped."""
     rng = np.random.default_rng(2)
