@@ -29,17 +29,9 @@
  *   _deepseek_v4_swa_slot_mapping), as each entry point states.
  * - Every kernel is launched with programmatic dependent launch: it may start
  *   while the previous kernel on `stream` is finishing, and waits for that
- *   kernel to complete before it reads a cache, reads an index matrix or
- *   writes any output.  compute_global_topk_indices_and_lens,
- *   combine_topk_swa_indices, decode_swa_indices_and_lens and the gathers that
- *   compute their own slots (_topk, _window, _dense, _ranges) read their
- *   metadata inputs (positions, query_start_loc, seq_lens, token_to_req,
- *   replay_start, base offsets, is_valid_token, top-k indices, block tables)
- *   before that wait.
- *   No libpsk kernel writes those inputs, and a kernel that does not itself
- *   trigger its dependents early is complete before a libpsk kernel starts;
- *   so only a caller's own programmatic-launch kernel that triggers early
- *   must have finished writing them before it triggers.
+ *   kernel to complete (griddepcontrol.wait, after which its writes are
+ *   visible) before it reads any global memory, so every input may be
+ *   written by the kernel just before it on the stream.
  *
  * Cache records ("pages")
  * -----------------------

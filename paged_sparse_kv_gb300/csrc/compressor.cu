@@ -749,13 +749,10 @@ cudaError_t launch_compress_kv_insert(const CompressParams& p, cudaStream_t stre
     // longer windows: clusters of kSlices CTAs, as many as can be resident
     auto kern = compress_cluster_kernel;
     const size_t smem = (size_t)window * kSliceCols * 2 * sizeof(float);
-    static bool attr_set = false;
-    if (!attr_set) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)(kMaxWindow * kSliceCols * 2 * sizeof(float)));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> limit_set{0};
+    const cudaError_t e = set_smem_limit_per_device(
+        kern, (int)(kMaxWindow * kSliceCols * 2 * sizeof(float)), limit_set);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kSlices);
     cfg.blockDim = dim3(kClusterThreads);

@@ -559,10 +559,9 @@ index_build_kernel(IndexParams p) {
         mbar_fence_init();
     }
     if (TMA) __syncthreads();
-    // Both round trips below read only inputs no libpsk kernel writes (top-k
-    // rows, token -> request map, request metadata, block tables), so they
-    // overlap the previous kernel on the stream; the wait for it comes before
-    // the first output store.
+    // Every input may come from the previous kernel on the stream: nothing
+    // global is read before its grid is done.
+    pdl_wait();
     pdl_launch_dependents();
 
     // First memory round trip: loads that depend only on token indices (TMA: the CTA's
@@ -594,7 +593,6 @@ index_build_kernel(IndexParams p) {
         if (HAS_SWA) stage_row(s_swa, p.swa_bt + (int64_t)staged * p.swa_stride, p.stage_swa);
     }
     __syncthreads();
-    pdl_wait();
 
     for (int64_t tb = t0; tb < t1; tb += tpp) {
         const int64_t t = tb + tslot;

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 namespace psk {
@@ -30,5 +31,23 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Number of SMs on the current device (queried once per device).
 int sm_count();
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device.  The attribute belongs to the device, so each call site keeps one
+// `done` mask (bit d: set on device d) and the attribute is set once per
+// device; device ids past 63 set it on every call.  Safe to call from several
+// host threads (setting it twice is harmless).
+template <typename... KArgs>
+cudaError_t set_smem_limit_per_device(void (*kernel)(KArgs...), int bytes,
+                                      std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 }  // namespace psk

@@ -27,10 +27,29 @@ def _stream(dev: torch.device) -> int:
     return torch.cuda.current_stream(dev).cuda_stream
 
 
+def _call(dev: torch.device, name: str, *args) -> None:
+    """Call a libpsk entry point on ``dev``'s current stream with ``dev`` as
+    the current CUDA device (the library launches, sizes grids and sets kernel
+    attributes on the current device)."""
+    if torch.cuda.current_device() != dev.index:
+        with torch.cuda.device(dev):
+            _abi.call(name, *args, _stream(dev))
+    else:
+        _abi.call(name, *args, _stream(dev))
+
+
 def _need_cuda(*ts):
+    dev = None
     for t in ts:
-        if t is not None and not t.is_cuda:
+        if t is None:
+            continue
+        if not t.is_cuda:
             raise ValueError("libpsk operates on CUDA tensors only (no CPU fallback)")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"all tensors of one call must be on one device ({dev} and "
+                             f"{t.device})")
 
 
 def _need(t: torch.Tensor, dtype: torch.dtype, name: str):
@@ -71,9 +90,9 @@ def quantize_and_insert_k_cache(k: torch.Tensor, k_cache: torch.Tensor,
         raise ValueError("slot_mapping must be 1-D contiguous")
     D = k.shape[1] if head_dim is None else head_dim
     num_pages, page_stride = _pages(k_cache)
-    _abi.call("quantize_and_insert_k_cache", _ptr(k), _rows(k, "k"), _ptr(slot_mapping),
-              slot_mapping.shape[0], _ptr(k_cache), num_pages, page_stride, block_size, D,
-              rope_dim, int(bool(is_ue8m0)), _ptr(err_count), _stream(k.device))
+    _call(k.device, "quantize_and_insert_k_cache", _ptr(k), _rows(k, "k"), _ptr(slot_mapping),
+          slot_mapping.shape[0], _ptr(k_cache), num_pages, page_stride, block_size, D,
+          rope_dim, int(bool(is_ue8m0)), _ptr(err_count))
 
 
 def write_indexer_mxfp4_cache(index_k: torch.Tensor, cache: torch.Tensor,
@@ -86,9 +105,9 @@ def write_indexer_mxfp4_cache(index_k: torch.Tensor, cache: torch.Tensor,
     if slot_mapping.dim() != 1 or not slot_mapping.is_contiguous():
         raise ValueError("slot_mapping must be 1-D contiguous")
     num_pages, page_stride = _pages(cache)
-    _abi.call("write_indexer_mxfp4_cache", _ptr(index_k), _rows(index_k, "index_k"),
-              _ptr(slot_mapping), slot_mapping.shape[0], _ptr(cache), num_pages, page_stride,
-              block_size, index_k.shape[1], _ptr(err_count), _stream(index_k.device))
+    _call(index_k.device, "write_indexer_mxfp4_cache", _ptr(index_k), _rows(index_k, "index_k"),
+          _ptr(slot_mapping), slot_mapping.shape[0], _ptr(cache), num_pages, page_stride,
+          block_size, index_k.shape[1], _ptr(err_count))
 
 
 def compute_global_topk_indices_and_lens(topk_indices: torch.Tensor,
@@ -109,11 +128,11 @@ def compute_global_topk_indices_and_lens(topk_indices: torch.Tensor,
     if lens is None:
         lens = torch.empty((T,), dtype=torch.int32, device=topk_indices.device)
     valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
-    _abi.call("compute_global_topk_indices_and_lens", _ptr(topk_indices),
-              _rows(topk_indices, "topk_indices"), T, K, _ptr(token_to_req_indices),
-              _ptr(block_table), _rows(block_table, "block_table"), block_table.shape[1],
-              block_table.shape[0], block_size, _ptr(base_offsets), _ptr(valid), _ptr(out),
-              _rows(out, "out"), _ptr(lens), _stream(topk_indices.device))
+    _call(topk_indices.device, "compute_global_topk_indices_and_lens", _ptr(topk_indices),
+          _rows(topk_indices, "topk_indices"), T, K, _ptr(token_to_req_indices),
+          _ptr(block_table), _rows(block_table, "block_table"), block_table.shape[1],
+          block_table.shape[0], block_size, _ptr(base_offsets), _ptr(valid), _ptr(out),
+          _rows(out, "out"), _ptr(lens))
     return out, lens
 
 
@@ -143,15 +162,15 @@ def combine_topk_swa_indices(query_start_loc: torch.Tensor, seq_lens: torch.Tens
         lens = torch.empty((T,), dtype=torch.int32, device=dev)
     cbt = compressed_block_table
     valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
-    _abi.call("combine_topk_swa_indices", _ptr(query_start_loc), _ptr(seq_lens),
-              _ptr(token_to_req_indices), _ptr(replay_start), seq_lens.shape[0], T,
-              _ptr(swa_block_table), _rows(swa_block_table, "swa_block_table"),
-              swa_block_table.shape[1], _ptr(swa_base_offsets), swa_block_size,
-              _ptr(cbt), _rows(cbt, "compressed_block_table") if cbt is not None else 0,
-              cbt.shape[1] if cbt is not None else 0, _ptr(compressed_base_offsets),
-              compressed_block_size, window_size, compress_ratio, _ptr(topk_indices),
-              _rows(topk_indices, "topk_indices"), K, _ptr(valid), _ptr(out), _rows(out, "out"),
-              _ptr(lens), _stream(dev))
+    _call(dev, "combine_topk_swa_indices", _ptr(query_start_loc), _ptr(seq_lens),
+          _ptr(token_to_req_indices), _ptr(replay_start), seq_lens.shape[0], T,
+          _ptr(swa_block_table), _rows(swa_block_table, "swa_block_table"),
+          swa_block_table.shape[1], _ptr(swa_base_offsets), swa_block_size,
+          _ptr(cbt), _rows(cbt, "compressed_block_table") if cbt is not None else 0,
+          cbt.shape[1] if cbt is not None else 0, _ptr(compressed_base_offsets),
+          compressed_block_size, window_size, compress_ratio, _ptr(topk_indices),
+          _rows(topk_indices, "topk_indices"), K, _ptr(valid), _ptr(out), _rows(out, "out"),
+          _ptr(lens))
     return out, lens
 
 
@@ -170,10 +189,10 @@ def dequantize_and_gather_k_cache(out: torch.Tensor, cache: torch.Tensor,
     if out.shape[0] != T or out.shape[1] != C:
         raise ValueError(f"out {tuple(out.shape)} does not match indices {tuple(indices.shape)}")
     num_pages, page_stride = _pages(cache)
-    _abi.call("dequantize_and_gather_k_cache", _ptr(out), out.stride(0), out.stride(1),
-              _ptr(cache), num_pages, page_stride, block_size, record, out.shape[2],
-              rope_dim if record == PSK_REC_FP8_DS_MLA else 0, int(bool(is_ue8m0)),
-              _ptr(indices), _rows(indices, "indices"), T, C, _stream(out.device))
+    _call(out.device, "dequantize_and_gather_k_cache", _ptr(out), out.stride(0), out.stride(1),
+          _ptr(cache), num_pages, page_stride, block_size, record, out.shape[2],
+          rope_dim if record == PSK_REC_FP8_DS_MLA else 0, int(bool(is_ue8m0)),
+          _ptr(indices), _rows(indices, "indices"), T, C)
     return out
 
 
@@ -195,12 +214,11 @@ def dequantize_and_gather_k_cache_ranges(out: torch.Tensor, cache: torch.Tensor,
     for t, n in ((seq_lens, "seq_lens"), (block_table, "block_table")):
         _need(t, torch.int32, n)
     num_pages, page_stride = _pages(cache)
-    _abi.call("dequantize_and_gather_k_cache_ranges", _ptr(out), out.stride(0), out.stride(1),
-              out.shape[1], _ptr(cache), num_pages, page_stride, block_size,
-              PSK_REC_FP8_DS_MLA, out.shape[2], rope_dim, int(bool(is_ue8m0)), _ptr(seq_lens),
-              _ptr(gather_lens), _ptr(block_table), _rows(block_table, "block_table"),
-              block_table.shape[1], _ptr(base_offsets), seq_lens.shape[0], offset,
-              _stream(out.device))
+    _call(out.device, "dequantize_and_gather_k_cache_ranges", _ptr(out), out.stride(0), out.stride(1),
+          out.shape[1], _ptr(cache), num_pages, page_stride, block_size,
+          PSK_REC_FP8_DS_MLA, out.shape[2], rope_dim, int(bool(is_ue8m0)), _ptr(seq_lens),
+          _ptr(gather_lens), _ptr(block_table), _rows(block_table, "block_table"),
+          block_table.shape[1], _ptr(base_offsets), seq_lens.shape[0], offset)
     return out
 
 
@@ -223,11 +241,11 @@ def combine_topk_swa_workspace_indices(topk_indices: torch.Tensor,
     if lens is None:
         lens = torch.empty((T,), dtype=torch.int32, device=dev)
     valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
-    _abi.call("combine_topk_swa_workspace_indices", _ptr(query_start_loc), _ptr(seq_lens),
-              _ptr(gather_lens), _ptr(token_to_req), seq_lens.shape[0], T, window_size,
-              compress_ratio, _ptr(topk_indices), _rows(topk_indices, "topk_indices"), K,
-              workspace_width, compressed_base, _ptr(valid), _ptr(out), _rows(out, "out"),
-              _ptr(lens), _stream(dev))
+    _call(dev, "combine_topk_swa_workspace_indices", _ptr(query_start_loc), _ptr(seq_lens),
+          _ptr(gather_lens), _ptr(token_to_req), seq_lens.shape[0], T, window_size,
+          compress_ratio, _ptr(topk_indices), _rows(topk_indices, "topk_indices"), K,
+          workspace_width, compressed_base, _ptr(valid), _ptr(out), _rows(out, "out"),
+          _ptr(lens))
     return out, lens
 
 
@@ -243,10 +261,10 @@ def indexer_mxfp4_paged_gather(cache: torch.Tensor, block_table: torch.Tensor,
     if scales_out is None:
         scales_out = torch.empty((total_rows, head_dim // 32), dtype=torch.uint8, device=dev)
     num_pages, page_stride = _pages(cache)
-    _abi.call("indexer_mxfp4_paged_gather", _ptr(values_out), _ptr(scales_out), _ptr(cache),
-              num_pages, page_stride, block_size, head_dim, _ptr(block_table),
-              _rows(block_table, "block_table"), block_table.shape[1], _ptr(cu_seq_lens),
-              cu_seq_lens.shape[0] - 1, total_rows, _stream(dev))
+    _call(dev, "indexer_mxfp4_paged_gather", _ptr(values_out), _ptr(scales_out), _ptr(cache),
+          num_pages, page_stride, block_size, head_dim, _ptr(block_table),
+          _rows(block_table, "block_table"), block_table.shape[1], _ptr(cu_seq_lens),
+          cu_seq_lens.shape[0] - 1, total_rows)
     return values_out, scales_out
 
 
@@ -269,11 +287,10 @@ def decode_swa_indices_and_lens(query_start_loc: torch.Tensor, seq_lens: torch.T
     if lens is None:
         lens = torch.empty((T,), dtype=torch.int32, device=dev)
     valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
-    _abi.call("decode_swa_indices_and_lens", _ptr(query_start_loc), _ptr(seq_lens),
-              _ptr(token_to_req), seq_lens.shape[0], T, _ptr(block_table),
-              _rows(block_table, "block_table"), block_table.shape[1], _ptr(base_offsets),
-              block_size, window_size, _ptr(valid), _ptr(out), _rows(out, "out"), _ptr(lens),
-              _stream(dev))
+    _call(dev, "decode_swa_indices_and_lens", _ptr(query_start_loc), _ptr(seq_lens),
+          _ptr(token_to_req), seq_lens.shape[0], T, _ptr(block_table),
+          _rows(block_table, "block_table"), block_table.shape[1], _ptr(base_offsets),
+          block_size, window_size, _ptr(valid), _ptr(out), _rows(out, "out"), _ptr(lens))
     return out, lens
 
 
@@ -297,10 +314,10 @@ def compute_dense_compressed_indices_and_lens(positions: torch.Tensor,
         lens = torch.empty((T,), dtype=torch.int32, device=dev)
     valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
     R = block_table.shape[0] if num_reqs is None else num_reqs
-    _abi.call("compute_dense_compressed_indices_and_lens", _ptr(positions), T,
-              _ptr(token_to_req), R, _ptr(block_table), _rows(block_table, "block_table"),
-              block_table.shape[1], _ptr(base_offsets), block_size, compress_ratio, width,
-              _ptr(valid), _ptr(out), _rows(out, "out"), _ptr(lens), _stream(dev))
+    _call(dev, "compute_dense_compressed_indices_and_lens", _ptr(positions), T,
+          _ptr(token_to_req), R, _ptr(block_table), _rows(block_table, "block_table"),
+          block_table.shape[1], _ptr(base_offsets), block_size, compress_ratio, width,
+          _ptr(valid), _ptr(out), _rows(out, "out"), _ptr(lens))
     return out, lens
 
 
@@ -314,8 +331,8 @@ def build_dense_prefill_local_compressed_indices(positions: torch.Tensor, compre
     T = positions.shape[0]
     if out is None:
         out = torch.empty((T, width), dtype=torch.int32, device=dev)
-    _abi.call("build_dense_prefill_local_compressed_indices", _ptr(positions), T,
-              compress_ratio, width, _ptr(out), _rows(out, "out"), _stream(dev))
+    _call(dev, "build_dense_prefill_local_compressed_indices", _ptr(positions), T,
+          compress_ratio, width, _ptr(out), _rows(out, "out"))
     return out
 
 
@@ -334,9 +351,9 @@ def combine_dense_swa_indices(positions: torch.Tensor, token_to_req: torch.Tenso
         out = torch.empty((T, window_size), dtype=torch.int32, device=dev)
     if lens is None:
         lens = torch.empty((T,), dtype=torch.int32, device=dev)
-    _abi.call("combine_dense_swa_indices", _ptr(positions), _ptr(token_to_req), _ptr(seq_lens),
-              _ptr(gather_lens), seq_lens.shape[0], T, window_size, workspace_width,
-              compressed_base, _ptr(out), _rows(out, "out"), _ptr(lens), _stream(dev))
+    _call(dev, "combine_dense_swa_indices", _ptr(positions), _ptr(token_to_req), _ptr(seq_lens),
+          _ptr(gather_lens), seq_lens.shape[0], T, window_size, workspace_width,
+          compressed_base, _ptr(out), _rows(out, "out"), _ptr(lens))
     return out, lens
 
 
@@ -349,9 +366,9 @@ def write_indexer_fp8_cache(index_k: torch.Tensor, cache: torch.Tensor, slot_map
     _need(index_k, torch.bfloat16, "index_k")
     _need(slot_mapping, torch.int64, "slot_mapping")
     num_pages, page_stride = _pages(cache)
-    _abi.call("write_indexer_fp8_cache", _ptr(index_k), _rows(index_k, "index_k"),
-              _ptr(slot_mapping), slot_mapping.shape[0], _ptr(cache), num_pages, page_stride,
-              block_size, index_k.shape[1], _ptr(err_count), _stream(index_k.device))
+    _call(index_k.device, "write_indexer_fp8_cache", _ptr(index_k), _rows(index_k, "index_k"),
+          _ptr(slot_mapping), slot_mapping.shape[0], _ptr(cache), num_pages, page_stride,
+          block_size, index_k.shape[1], _ptr(err_count))
 
 
 def indexer_k_norm_rope_store(k_pre: torch.Tensor, positions: torch.Tensor,
@@ -373,11 +390,11 @@ def indexer_k_norm_rope_store(k_pre: torch.Tensor, positions: torch.Tensor,
         raise ValueError("k_pre must be [num_tokens, 128]")
     num_pages, page_stride = _pages(k_cache)
     record = PSK_REC_MXFP4 if use_fp4_cache else PSK_REC_FP8_INDEXER
-    _abi.call("indexer_k_norm_rope_store", _ptr(k_pre), _rows(k_pre, "k_pre"), _ptr(positions),
-              _ptr(cos_sin_cache), _rows(cos_sin_cache, "cos_sin_cache"), cos_sin_cache.shape[0],
-              _ptr(rms_norm_weight.contiguous()), float(rms_norm_eps), _ptr(kv_slot_mapping),
-              kv_slot_mapping.shape[0], compress_ratio, record, _ptr(k_cache), num_pages,
-              page_stride, block_size, _ptr(err_count), _stream(k_pre.device))
+    _call(k_pre.device, "indexer_k_norm_rope_store", _ptr(k_pre), _rows(k_pre, "k_pre"), _ptr(positions),
+          _ptr(cos_sin_cache), _rows(cos_sin_cache, "cos_sin_cache"), cos_sin_cache.shape[0],
+          _ptr(rms_norm_weight.contiguous()), float(rms_norm_eps), _ptr(kv_slot_mapping),
+          kv_slot_mapping.shape[0], compress_ratio, record, _ptr(k_cache), num_pages,
+          page_stride, block_size, _ptr(err_count))
 
 
 # ---- compressed-KV producer -------------------------------------------------------------
@@ -399,10 +416,10 @@ def save_compressor_state(kv: torch.Tensor, score: torch.Tensor, ape: torch.Tens
     if state_cache.dim() != 3 or state_cache.shape[1] != block_size or \
             state_cache.shape[2] != 2 * sw or not state_cache.is_contiguous():
         raise ValueError("state_cache must be contiguous [pages, block_size, 2 * state_width]")
-    _abi.call("save_compressor_state", _ptr(kv), _ptr(score), _rows(kv, "kv"),
-              _ptr(ape.contiguous()), sw, _ptr(slot_mapping), _ptr(positions),
-              slot_mapping.shape[0], compress_ratio, _ptr(state_cache), state_cache.shape[0],
-              block_size, _ptr(err_count), _stream(kv.device))
+    _call(kv.device, "save_compressor_state", _ptr(kv), _ptr(score), _rows(kv, "kv"),
+          _ptr(ape.contiguous()), sw, _ptr(slot_mapping), _ptr(positions),
+          slot_mapping.shape[0], compress_ratio, _ptr(state_cache), state_cache.shape[0],
+          block_size, _ptr(err_count))
 
 
 def compress_kv_cache_insert(state_cache: torch.Tensor, token_to_req_indices: torch.Tensor,
@@ -428,16 +445,15 @@ def compress_kv_cache_insert(state_cache: torch.Tensor, token_to_req_indices: to
     if state_cache.dim() != 3 or not state_cache.is_contiguous():
         raise ValueError("state_cache must be contiguous [pages, block_size, 2 * state_width]")
     num_pages, page_stride = _pages(kv_cache_2d)
-    _abi.call("compress_kv_cache_insert", _ptr(state_cache), state_cache.shape[0],
-              compressor_block_size, state_cache.shape[2] // 2, _ptr(token_to_req_indices),
-              _ptr(positions), _ptr(compressor_slot_mapping), _ptr(block_table),
-              _rows(block_table, "block_table"), block_table.shape[1],
-              _ptr(block_table_base_offsets), block_table.shape[0], positions.shape[0],
-              compress_ratio, int(bool(overlap)), _ptr(rms_norm_weight.contiguous()),
-              float(rms_norm_eps), _ptr(cos_sin_cache), _rows(cos_sin_cache, "cos_sin_cache"),
-              cos_sin_cache.shape[0], _ptr(kv_cache_2d), num_pages, page_stride,
-              kv_cache_block_size, _ptr(kv_slot_mapping), _ptr(err_count),
-              _stream(state_cache.device))
+    _call(state_cache.device, "compress_kv_cache_insert", _ptr(state_cache), state_cache.shape[0],
+          compressor_block_size, state_cache.shape[2] // 2, _ptr(token_to_req_indices),
+          _ptr(positions), _ptr(compressor_slot_mapping), _ptr(block_table),
+          _rows(block_table, "block_table"), block_table.shape[1],
+          _ptr(block_table_base_offsets), block_table.shape[0], positions.shape[0],
+          compress_ratio, int(bool(overlap)), _ptr(rms_norm_weight.contiguous()),
+          float(rms_norm_eps), _ptr(cos_sin_cache), _rows(cos_sin_cache, "cos_sin_cache"),
+          cos_sin_cache.shape[0], _ptr(kv_cache_2d), num_pages, page_stride,
+          kv_cache_block_size, _ptr(kv_slot_mapping), _ptr(err_count))
 
 
 # ---- fused gathers ------------------------------------------------------------------------
@@ -461,12 +477,12 @@ def dequantize_and_gather_k_cache_topk(out: torch.Tensor, cache: torch.Tensor,
     num_pages, page_stride = _pages(cache)
     valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
     R = block_table.shape[0] if num_reqs is None else num_reqs
-    _abi.call("dequantize_and_gather_k_cache_topk", _ptr(out), out.stride(0), out.stride(1),
-              _ptr(cache), num_pages, page_stride, block_size, record, out.shape[2],
-              rope_dim if record == PSK_REC_FP8_DS_MLA else 0, _ptr(topk_indices),
-              _rows(topk_indices, "topk_indices"), T, K, _ptr(token_to_req_indices),
-              _ptr(block_table), _rows(block_table, "block_table"), block_table.shape[1], R,
-              _ptr(base_offsets), _ptr(valid), _stream(out.device))
+    _call(out.device, "dequantize_and_gather_k_cache_topk", _ptr(out), out.stride(0), out.stride(1),
+          _ptr(cache), num_pages, page_stride, block_size, record, out.shape[2],
+          rope_dim if record == PSK_REC_FP8_DS_MLA else 0, _ptr(topk_indices),
+          _rows(topk_indices, "topk_indices"), T, K, _ptr(token_to_req_indices),
+          _ptr(block_table), _rows(block_table, "block_table"), block_table.shape[1], R,
+          _ptr(base_offsets), _ptr(valid))
     return out
 
 
@@ -488,12 +504,11 @@ def dequantize_and_gather_k_cache_window(out: torch.Tensor, cache: torch.Tensor,
         raise ValueError("out must be [T, window, D] with unit inner stride")
     num_pages, page_stride = _pages(cache)
     valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
-    _abi.call("dequantize_and_gather_k_cache_window", _ptr(out), out.stride(0), out.stride(1),
-              _ptr(cache), num_pages, page_stride, block_size, out.shape[2], rope_dim,
-              _ptr(query_start_loc), _ptr(seq_lens), _ptr(token_to_req), _ptr(replay_start),
-              seq_lens.shape[0], T, _ptr(block_table), _rows(block_table, "block_table"),
-              block_table.shape[1], _ptr(base_offsets), window_size, _ptr(valid),
-              _stream(out.device))
+    _call(out.device, "dequantize_and_gather_k_cache_window", _ptr(out), out.stride(0), out.stride(1),
+          _ptr(cache), num_pages, page_stride, block_size, out.shape[2], rope_dim,
+          _ptr(query_start_loc), _ptr(seq_lens), _ptr(token_to_req), _ptr(replay_start),
+          seq_lens.shape[0], T, _ptr(block_table), _rows(block_table, "block_table"),
+          block_table.shape[1], _ptr(base_offsets), window_size, _ptr(valid))
     return out
 
 
@@ -504,7 +519,7 @@ def device_wait_timeouts() -> int:
 
 def device_wait_selftest(limit_ns: int, device: torch.device) -> None:
     """Launch one bounded wait that nothing completes (counted when it expires)."""
-    _abi.call("psk_device_wait_selftest", int(limit_ns), _stream(device))
+    _call(device, "psk_device_wait_selftest", int(limit_ns))
 
 
 def dequantize_and_gather_k_cache_pair(out: torch.Tensor, cache_a: torch.Tensor, block_size_a: int,
@@ -520,10 +535,9 @@ def dequantize_and_gather_k_cache_pair(out: torch.Tensor, cache_a: torch.Tensor,
         raise ValueError("out must be [rows, cols, D] with unit inner stride")
     np_a, ps_a = _pages(cache_a)
     np_b, ps_b = _pages(cache_b)
-    _abi.call("dequantize_and_gather_k_cache_pair", _ptr(out), out.stride(0), out.stride(1),
-              _ptr(cache_a), np_a, ps_a, block_size_a, _ptr(cache_b), np_b, ps_b, block_size_b,
-              out.shape[2], rope_dim, _ptr(indices), _rows(indices, "indices"), R, C, split,
-              _stream(out.device))
+    _call(out.device, "dequantize_and_gather_k_cache_pair", _ptr(out), out.stride(0), out.stride(1),
+          _ptr(cache_a), np_a, ps_a, block_size_a, _ptr(cache_b), np_b, ps_b, block_size_b,
+          out.shape[2], rope_dim, _ptr(indices), _rows(indices, "indices"), R, C, split)
     return out
 
 
@@ -544,9 +558,9 @@ def dequantize_and_gather_k_cache_dense(out: torch.Tensor, cache: torch.Tensor,
     num_pages, page_stride = _pages(cache)
     valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
     R = block_table.shape[0] if num_reqs is None else num_reqs
-    _abi.call("dequantize_and_gather_k_cache_dense", _ptr(out), out.stride(0), out.stride(1),
-              _ptr(cache), num_pages, page_stride, block_size, out.shape[2], rope_dim,
-              _ptr(positions), T, _ptr(token_to_req), R, _ptr(block_table),
-              _rows(block_table, "block_table"), block_table.shape[1], _ptr(base_offsets),
-              compress_ratio, out.shape[1], _ptr(valid), _stream(out.device))
+    _call(out.device, "dequantize_and_gather_k_cache_dense", _ptr(out), out.stride(0), out.stride(1),
+          _ptr(cache), num_pages, page_stride, block_size, out.shape[2], rope_dim,
+          _ptr(positions), T, _ptr(token_to_req), R, _ptr(block_table),
+          _rows(block_table, "block_table"), block_table.shape[1], _ptr(base_offsets),
+          compress_ratio, out.shape[1], _ptr(valid))
     return out

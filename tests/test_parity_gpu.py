@@ -147,9 +147,9 @@ def _fp8_code_positions(slots, num_pages, page_stride, bs, ts, nope):
 def test_fp8_insert_non_finite_inputs(cuda_device, ue8m0):
     """+-inf, NaN of both signs (quiet and signalling payloads), all-NaN and
     all-zero blocks, -0 and the largest finite bf16, planted in random rows.
-    amax passes over NaN; +-inf saturates to +-448.  E4M3 has two NaN codes
-    (S.1111.111): where the oracle writes NaN the kernel's byte must be a NaN
-    of either sign, every other byte must match."""
+    amax passes over NaN; +-inf saturates to +-448.  NaN of either sign
+    encodes as 0x7F, the one NaN code both sides write; every byte must
+    match."""
     rng = np.random.default_rng(11)
     D, rope, N, bs = 512, 64, 96, 16
     nope = D - rope
@@ -167,10 +167,7 @@ def test_fp8_insert_non_finite_inputs(cuda_device, ue8m0):
     got = dev_cache.cpu().numpy().reshape(-1).copy()
     want = host.reshape(-1)
     codes = _fp8_code_positions(slots, pages, geom.page_stride, bs, nope + 2 * rope, nope)
-    nan_at = codes[want[codes] == 0x7F]
-    assert nan_at.size > 0
-    assert np.all((got[nan_at] & 0x7F) == 0x7F), "NaN input must give an E4M3 NaN code"
-    got[nan_at] = 0x7F
+    assert np.any(want[codes] == 0x7F)  # NaN inputs reached the codes
     assert np.any(want[codes] == 0x7E) and np.any(want[codes] == 0xFE)
     _assert_same(got, want, f"non-finite fp8 insert ue8m0={ue8m0}")
 

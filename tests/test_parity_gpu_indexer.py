@@ -38,9 +38,8 @@ def test_fp8_indexer_insert_exhaustive_codes(cuda_device):
 
 def test_fp8_indexer_insert_non_finite_inputs(cuda_device):
     """+-inf, NaN of both signs, all-NaN and all-zero stretches in 128-dim keys:
-    the row amax passes over NaN, +-inf saturates to +-448.  Where the oracle
-    writes an E4M3 NaN the kernel's byte must be a NaN of either sign; every
-    other byte (codes and binary32 scales) must match."""
+    the row amax passes over NaN, +-inf saturates to +-448, NaN of either sign
+    encodes as 0x7F; every byte (codes and binary32 scales) must match."""
     from test_parity_gpu import _fp8_code_positions, _rows_with_specials
     rng = np.random.default_rng(13)
     D, N, bs = 128, 200, 16
@@ -54,10 +53,7 @@ def test_fp8_indexer_insert_non_finite_inputs(cuda_device):
     got = dev_cache.cpu().numpy().reshape(-1).copy()
     want = host.reshape(-1)
     codes = _fp8_code_positions(slots, pages, bs * (D + 4), bs, D, D)
-    nan_at = codes[want[codes] == 0x7F]
-    assert nan_at.size > 0
-    assert np.all((got[nan_at] & 0x7F) == 0x7F), "NaN input must give an E4M3 NaN code"
-    got[nan_at] = 0x7F
+    assert np.any(want[codes] == 0x7F)  # NaN inputs reached the codes
     _assert_same(got, want, "non-finite fp8 indexer insert")
 
 
@@ -168,7 +164,7 @@ def test_norm_rope_store_overflowing_weights(cuda_device, fp4):
     """Norm weights near the binary32 maximum push some normalised values to
     +-inf: the FP8 row scale 2^ceil(log2(amax / 448)) then rounds to +inf and
     the codes are e4m3(y / inf) (+-0, NaN for +-inf); MXFP4 codes are
-    e2m1(y * 2^-128) (+-6 for +-inf).  E4M3 NaN bytes may carry either sign."""
+    e2m1(y * 2^-128) (+-6 for +-inf).  E4M3 NaN is 0x7F on both sides."""
     from test_parity_gpu import _fp8_code_positions
     rng = np.random.default_rng(31 + fp4)
     N, bs, max_pos = 300, 16, 1024
@@ -193,10 +189,7 @@ def test_norm_rope_store_overflowing_weights(cuda_device, fp4):
     want = host.reshape(-1)
     if not fp4:
         codes = _fp8_code_positions(slots, pages, stride, bs, 128, 128)
-        nan_at = codes[want[codes] == 0x7F]
-        assert nan_at.size > 0
-        assert np.all((got[nan_at] & 0x7F) == 0x7F), "NaN must give an E4M3 NaN code"
-        got[nan_at] = 0x7F
+        assert np.any(want[codes] == 0x7F)  # NaN inputs reached the codes
     _assert_same(got, want, f"norm rope store, overflowing weights, fp4={fp4}")
 
 
