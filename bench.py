@@ -1,27 +1,35 @@
 """Benchmark of the paged K-cache pipeline on GB300 (one JSON line on stdout).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config prefill]
+                    [--configs tiny,decode,mixed,mxfp4] [--path auto]
                     [--impl mine|reference] [--no-cpu-baseline]
 
 A step is one pass of every hot-path row over one synthetic batch (see
-paged_sparse_kv_gb300/pipeline.py): FP8 insert, MXFP4 insert, fused index build,
-the two-part FP8 gather, the global top-k mapping and the MXFP4 gather.  The
-default workload is the decode batch (64 requests x 1 token, contexts
-U[1024, 8192], head_dim 512 = 448 fp8 + 64 bf16 rope, page 64, window 128,
-top-k 512).
+paged_sparse_kv_gb300/pipeline.py): FP8 insert, MXFP4 insert, fused window +
+top-k index build, the dequantize-and-gather of the window and top-k columns,
+the global top-k mapping and the MXFP4 gather.  The headline workload is the
+prefill chunk, the largest single-GPU configuration: 4 requests x 4096 new
+tokens, head_dim 512 = 448 fp8 + 64 bf16 rope, page 64, window 128, top-k 512
+-> sparse_indices [16384, 640] and a [16384, 640, 512] bf16 gather.  It runs
+the index path (build, then gathers keyed by the index matrix) on three
+streams.  The tiny, decode, mixed and MXFP4 workloads are measured after it
+in the same run and reported under `configs`, each with its own per-kernel
+table and dominant-kernel roofline (decode-sized batches take the fused path).
 
 Timing: W untimed warm-up steps, then K steps, each preceded by an L2 flush
 (a 512 MiB memset, then a 256 MiB read so no dirty line of the memset is left
-to write back; outside the timed events) and bracketed by CUDA events on
-the launching stream; per-kernel events give each kernel's average duration.
-`value` is query tokens per second over all ranks (weak scaling: every rank
-runs its own full batch).  `e2e` repeats the step through the public API with
-the step's inputs copied from pinned host memory and every output copied back,
-all inside the timed region.  `roofline` is for the kernel with the largest
-share of the step: algorithmic bytes per launch / its mean event duration,
-against the measured HBM copy bandwidth.  `cpu_baseline` times the CPU oracle
-(test infrastructure, single-threaded C) on a bounded sample of the same
-workload on this host.
+to write back; outside the timed events) and bracketed by CUDA events on the
+launching stream around an un-instrumented graph replay of the step.  `value`
+is query tokens per second over all ranks (weak scaling: every rank runs its
+own full batch).  `roofline` is for the kernel with the largest share of the
+serialised step: algorithmic bytes per launch / its mean launch duration from
+events around it in a serialised replay after each timed step, against the
+measured HBM copy bandwidth; `roofline.in_step` is the same kernel timed inside
+the concurrent step, where it shares the GPU with the other chains.  `e2e`
+repeats the headline step through the public API with the step's inputs copied
+from pinned host memory and every output copied back, all inside the timed
+region.  `cpu_baseline` times the CPU oracle (test infrastructure,
+single-threaded C) on a bounded sample of the same workload on this host.
 
 --impl reference times the CPU oracle itself as the reference arm.
 """
@@ -46,6 +54,10 @@ if ROOT not in sys.path:
 METRIC = "K-cache tokens/s and achieved HBM GB/s (% of GB300 peak) per kernel, 1 GPU"
 UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0
+# the headline workload (the largest single-GPU configuration) and the ones
+# measured after it
+DEFAULT_CONFIG = "prefill"
+SIDE_CONFIGS = ("tiny", "decode", "mixed", "mxfp4")
 
 
 def _peaks():
@@ -414,60 +426,103 @@ def _capture(torch, dev, stream, fn):
 
 # ---- main ------------------------------------------------------------------------------
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="decode",
-                    choices=["tiny", "decode", "prefill", "mixed", "mxfp4", "prefill_small",
-                             "decode_hca"])
-    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--path", default="auto",
-                    choices=["auto", "index", "fused", "workspace", "dense", "dense_fused",
-                             "indexer_fp8",
-                             "indexer_store", "compressor"],
-                    help="auto: fused for index matrices of up to 2^20 items (latency-bound "
-                         "batches), else index; "
-                         "index: the index-keyed gather into [T, W+P, D]; workspace: the "
-                         "prefill workspace path (range gathers + workspace indices); dense: "
-                         "the no-top-k decode step of a heavily compressed layer (the "
-                         "decode_hca workload always takes it); indexer_fp8 / indexer_store: "
-                         "the mxfp4 workload's step with the FP8 indexer record or the fused "
-                         "norm-RoPE store as the key writer; compressor: the compressed-KV "
-                         "producer (ratio 4 and 128 layers) of a prefill batch")
-    ap.add_argument("--eager", action="store_true",
-                    help="launch the step eagerly instead of replaying a CUDA graph")
-    args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
+def step_layout(p, path: str, graph: bool) -> str:
+    """How the step's launches are laid out on streams (the config's `launch`)."""
+    w = p.w
+    if path == "fused":
+        s = ("four streams: [fused top-k gather], [index build -> top-k mapping], "
+             "[MXFP4 insert -> fused MXFP4 gather], [FP8 insert -> fused window gather]")
+    elif path == "index" and not w.has_fp8:
+        s = "a side stream: [top-k mapping -> MXFP4 insert -> MXFP4 gather]"
+    elif path == "index" and p.gather_as_pair:
+        s = ("two streams: [FP8 insert -> index build -> pair gather] (one PDL chain), "
+             "[top-k mapping -> MXFP4 insert -> MXFP4 gather]")
+    elif path == "index":
+        s = ("three streams: [index build -> top-k gather], [FP8 insert -> (after the index "
+             "build) window gather], [top-k mapping -> MXFP4 insert -> MXFP4 gather]")
+    elif path == "workspace":
+        s = ("three streams: [compressed range gather -> workspace index build], [FP8 insert "
+             "-> window range gather], [MXFP4 insert -> raw MXFP4 gather]")
+    elif path == "dense":
+        s = ("three streams: [decode SWA indices -> (after the insert) window gather], [FP8 "
+             "insert], [dense compressed indices -> compressed gather]")
+    elif path == "dense_fused":
+        s = ("three streams: [dense gather], [decode SWA indices -> dense compressed "
+             "indices], [FP8 insert -> fused window gather]")
+    elif path.startswith("indexer_"):
+        s = "two streams: [key writer], [top-k mapping], then the gather of the top-k keys"
+    elif path == "compressor":
+        s = "two streams: one per layer, [state write -> compressed insert]"
+    else:
+        s = path
+    return ("CUDA graph of the step on " if graph else "eager, ") + s
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
-    if args.impl == "reference":
-        return run_reference(args, rank, world)
+def step_alg_bytes(p, path: str, names) -> dict:
+    """Algorithmic bytes of each launch of the step on ``path``."""
+    w = p.w
+    if path == "workspace":
+        return workspace_algorithmic_bytes(p)
+    if path.startswith("dense"):
+        alg = dense_algorithmic_bytes(p, {"swa_indices": p.swa_indices.cpu().numpy(),
+                                          "dense_indices": p.dense_indices.cpu().numpy()})
+        if path == "dense_fused":
+            # the same rows; slots from per-token metadata instead of index columns
+            T = w.num_tokens
+            alg["dequantize_and_gather_k_cache_window[swa]"] = (
+                alg.pop("dequantize_and_gather_k_cache[swa]") - T * w.window * 4 + T * 16)
+            alg["dequantize_and_gather_k_cache_dense[compressed]"] = (
+                alg.pop("dequantize_and_gather_k_cache[compressed]") - T * w.dense_width * 4 +
+                T * 16)
+        return alg
+    if path.startswith("indexer_"):
+        return indexer_algorithmic_bytes(p, path.split("_")[1],
+                                         {"global_topk": p.global_topk.cpu().numpy()})
+    if path == "compressor":
+        return compressor_algorithmic_bytes(p)
+    outputs = {"global_topk": p.global_topk.cpu().numpy()}
+    if w.has_fp8:
+        outputs["sparse_indices"] = p.sparse_indices.cpu().numpy()
+    alg = algorithmic_bytes(p, outputs)
+    if path == "index" and "dequantize_and_gather_k_cache_pair" in names:
+        # one launch over both column ranges: the two parts' bytes
+        alg["dequantize_and_gather_k_cache_pair"] = (
+            alg.pop("dequantize_and_gather_k_cache[swa]") +
+            alg.pop("dequantize_and_gather_k_cache[topk]"))
+    if path == "fused":
+        # the fused gathers move the same rows; the top-k forms read a top-k
+        # entry per item where the index form read a slot id, the window form
+        # reads per-token metadata instead of its index columns
+        alg["dequantize_and_gather_k_cache_topk[mxfp4]"] = alg.pop(
+            "dequantize_and_gather_k_cache[mxfp4]")
+        if w.has_fp8:
+            alg["dequantize_and_gather_k_cache_topk[topk]"] = alg.pop(
+                "dequantize_and_gather_k_cache[topk]")
+            alg["dequantize_and_gather_k_cache_window[swa]"] = (
+                alg.pop("dequantize_and_gather_k_cache[swa]") -
+                w.num_tokens * w.window * 4 + w.num_tokens * 16)
+    return alg
 
-    import torch
-    from paged_sparse_kv_gb300 import build as psk_build
+
+def _max_over_ranks(torch, dist, dev, x: float) -> float:
+    if not dist:
+        return x
+    t = torch.tensor([x], device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_config(args, torch, dev, dist, world, rank, flush, config: str, steps: int,
+               warmup: int, headline: bool) -> dict:
+    """Measure one workload's step.  Returns the fields of its JSON entry;
+    the headline workload also gets the end-to-end leg."""
     from paged_sparse_kv_gb300 import synthetic
     from paged_sparse_kv_gb300.pipeline import Pipeline
 
-    psk_build.build()
-    dev = torch.device(f"cuda:{local_rank}")
-    torch.cuda.set_device(dev)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-
-    w = synthetic.make(args.config, seed_offset=1000 * rank)
+    w = synthetic.make(config, seed_offset=1000 * rank)
     p = Pipeline(w, dev)
     p.fill_caches_with_quantized_rows(seed=4321 + rank)
-    path = args.path
+    path = args.path if headline else "auto"
     if path == "auto":  # the pipeline's size rule (fused for latency-bound batches)
         path = p.default_path
     if w.dense_width > 0 and not path.startswith("dense"):
@@ -489,56 +544,16 @@ def main():
                     "dense_fused": p.dense_fused_launches,
                     "index": p.launches, "fused": p.fused_launches}[path]()
     names = [n for n, _ in launches]
-    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush()
         p.step(concurrent=True, path=path)
     torch.cuda.synchronize(dev)
-
-    if path == "workspace":
-        alg = workspace_algorithmic_bytes(p)
-    elif path.startswith("dense"):
-        alg = dense_algorithmic_bytes(p, {"swa_indices": p.swa_indices.cpu().numpy(),
-                                          "dense_indices": p.dense_indices.cpu().numpy()})
-        if path == "dense_fused":
-            # the same rows; slots from per-token metadata instead of index columns
-            T = w.num_tokens
-            alg["dequantize_and_gather_k_cache_window[swa]"] = (
-                alg.pop("dequantize_and_gather_k_cache[swa]") - T * w.window * 4 + T * 16)
-            alg["dequantize_and_gather_k_cache_dense[compressed]"] = (
-                alg.pop("dequantize_and_gather_k_cache[compressed]") - T * w.dense_width * 4 +
-                T * 16)
-    elif path.startswith("indexer_"):
-        alg = indexer_algorithmic_bytes(p, path.split("_")[1],
-                                        {"global_topk": p.global_topk.cpu().numpy()})
-    elif path == "compressor":
-        alg = compressor_algorithmic_bytes(p)
-    else:
-        outputs = {"global_topk": p.global_topk.cpu().numpy()}
-        if w.has_fp8:
-            outputs["sparse_indices"] = p.sparse_indices.cpu().numpy()
-        alg = algorithmic_bytes(p, outputs)
-        if path == "index" and "dequantize_and_gather_k_cache_pair" in names:
-            # one launch over both column ranges: the two parts' bytes
-            alg["dequantize_and_gather_k_cache_pair"] = (
-                alg.pop("dequantize_and_gather_k_cache[swa]") +
-                alg.pop("dequantize_and_gather_k_cache[topk]"))
-        if path == "fused":
-            # the fused gathers move the same rows; the top-k forms read a top-k
-            # entry per item where the index form read a slot id, the window form
-            # reads per-token metadata instead of its index columns
-            alg["dequantize_and_gather_k_cache_topk[mxfp4]"] = alg.pop(
-                "dequantize_and_gather_k_cache[mxfp4]")
-            if w.has_fp8:
-                alg["dequantize_and_gather_k_cache_topk[topk]"] = alg.pop(
-                    "dequantize_and_gather_k_cache[topk]")
-                alg["dequantize_and_gather_k_cache_window[swa]"] = (
-                    alg.pop("dequantize_and_gather_k_cache[swa]") -
-                    w.num_tokens * w.window * 4 + w.num_tokens * 16)
+    alg = step_alg_bytes(p, path, names)
 
     visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x]
+    local_rank = dev.index or 0
     clocks = ClockSampler(visible[local_rank] if local_rank < len(visible) else str(local_rank))
     use_graph = not args.eager and _graph_events_supported(torch)
 
@@ -546,10 +561,11 @@ def main():
     # an event between consecutive kernels.  Each figure includes the cost of
     # the event node in front of the kernel.
     kern_ms = {n: [] for n in names}
+    n_ser = max(5, min(steps, 30))
     if use_graph:
         evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(names) + 1)]
         g_ser = _capture(torch, dev, stream, lambda: _instrumented(launches, names, evs))
-        for _ in range(max(5, min(args.steps, 30))):
+        for _ in range(n_ser):
             flush()
             g_ser.replay()
             torch.cuda.synchronize(dev)
@@ -557,7 +573,7 @@ def main():
                 kern_ms[n].append(evs[i].elapsed_time(evs[i + 1]))
         del g_ser
     else:
-        for _ in range(max(5, min(args.steps, 30))):
+        for _ in range(n_ser):
             evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
             flush()
             _instrumented(launches, names, evs)
@@ -566,35 +582,40 @@ def main():
                 kern_ms[n].append(evs[i].elapsed_time(evs[i + 1]))
     top = max(names, key=lambda n: statistics.mean(kern_ms[n]))
 
-    # (2) Timed region: K steps.  Each step replays the concurrent step (three
-    # streams) as a CUDA graph with no event inside, timed by events on either
-    # side (-> value); then, after another L2 flush, an instrumented replay of
-    # the same step with events around the dominant kernel on its own stream
-    # (-> roofline).  Event nodes inside a graph cost a few microseconds each,
-    # so they are kept out of the replay that gives the step time.
+    # (2) Timed region: K steps.  Each step replays the concurrent step as a
+    # CUDA graph with no event inside, timed by events on either side
+    # (-> value).  After each timed step, two instrumented replays give the
+    # dominant kernel's launch duration: the step serialised on one stream with
+    # events only around that kernel, so it has the GPU to itself (-> roofline),
+    # and the concurrent step with events around it on its own stream, where it
+    # shares the GPU with the other chains (-> roofline.in_step).  Event nodes
+    # inside a graph cost a few microseconds each, so they are kept out of the
+    # replay that gives the step time.
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    k_pre = torch.cuda.Event(enable_timing=True, external=use_graph)
-    k_post = torch.cuda.Event(enable_timing=True, external=use_graph)
-    hooks = {top: (lambda: k_pre.record(), lambda: k_post.record())}
-    g_plain = g_inst = None
+    marks = {k: torch.cuda.Event(enable_timing=True, external=use_graph)
+             for k in ("iso0", "iso1", "cc0", "cc1")}
+    hooks_iso = {top: (lambda: marks["iso0"].record(), lambda: marks["iso1"].record())}
+    hooks_cc = {top: (lambda: marks["cc0"].record(), lambda: marks["cc1"].record())}
+    g_plain = g_cc = g_iso = None
     if use_graph:
         g_plain = _capture(torch, dev, stream, lambda: p.step(concurrent=True, path=path))
-        g_inst = _capture(torch, dev, stream,
-                          lambda: p.step(concurrent=True, hooks=hooks, path=path))
-        for _ in range(args.warmup):
-            flush()
-            g_plain.replay()
-            flush()
-            g_inst.replay()
+        g_cc = _capture(torch, dev, stream,
+                        lambda: p.step(concurrent=True, hooks=hooks_cc, path=path))
+        g_iso = _capture(torch, dev, stream,
+                         lambda: p.step(concurrent=False, hooks=hooks_iso, path=path))
+        for _ in range(warmup):
+            for g in (g_plain, g_cc, g_iso):
+                flush()
+                g.replay()
         torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
     t_wall0 = time.perf_counter()
-    step_ms, top_ms = [], []
-    for _ in range(args.steps):
+    step_ms, iso_ms, cc_ms = [], [], []
+    for _ in range(steps):
         flush()
         t_start.record(stream)
         if g_plain is not None:
@@ -603,14 +624,20 @@ def main():
             p.step(concurrent=True, path=path)
         t_end.record(stream)
         flush()
-        if g_inst is not None:
-            g_inst.replay()
+        if g_cc is not None:
+            g_cc.replay()
         else:
-            p.step(concurrent=True, hooks=hooks, path=path)
-        k_post.synchronize()
+            p.step(concurrent=True, hooks=hooks_cc, path=path)
+        flush()
+        if g_iso is not None:
+            g_iso.replay()
+        else:
+            p.step(concurrent=False, hooks=hooks_iso, path=path)
+        marks["iso1"].synchronize()
         torch.cuda.synchronize(dev)
         step_ms.append(t_start.elapsed_time(t_end))
-        top_ms.append(k_pre.elapsed_time(k_post))
+        iso_ms.append(marks["iso0"].elapsed_time(marks["iso1"]))
+        cc_ms.append(marks["cc0"].elapsed_time(marks["cc1"]))
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
@@ -633,20 +660,8 @@ def main():
         torch.cuda.synchronize(dev)
         b2b = {"ms_per_step": round(b0.elapsed_time(b1) / n_b2b, 5), "steps": n_b2b,
                "note": "step graph replayed back to back, no L2 flush between"}
-    ms_per_step = statistics.mean(step_ms)
-    if dist:
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = _max_over_ranks(torch, dist, dev, statistics.mean(step_ms))
     value = w.num_tokens * world / (ms_per_step / 1e3)
-
-    # ---- end to end through the public API with host buffers ----
-    e2e = run_e2e(p, args, dev, flush, path)
-    if dist:
-        t = torch.tensor([e2e["ms_per_step"]], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["ms_per_step"] = float(t.item())
-    e2e_value = w.num_tokens * world / (e2e["ms_per_step"] / 1e3)
 
     peak, peak_kind = _peaks()
     kernels = {}
@@ -657,50 +672,150 @@ def main():
                       "alg_bytes": int(alg[n]), "GBps": round(gbs, 1),
                       "frac_measured": round(gbs / peak, 3),
                       "frac_nominal_8TBps": round(gbs / NOMINAL_HBM_GBS, 3)}
-    top_mean = statistics.mean(top_ms)
-    achieved = alg[top] / (top_mean / 1e3) / 1e9
+    iso_mean = _max_over_ranks(torch, dist, dev, statistics.mean(iso_ms))
+    cc_mean = _max_over_ranks(torch, dist, dev, statistics.mean(cc_ms))
+    achieved = alg[top] / (iso_mean / 1e3) / 1e9
+    cc_gbs = alg[top] / (cc_mean / 1e3) / 1e9
     roof = {"kernel": top, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 3),
-            "traffic": None, "us_per_launch": round(top_mean * 1e3, 2),
+            "traffic": recorded_traffic(config, top), "us_per_launch": round(iso_mean * 1e3, 2),
             "alg_bytes_per_launch": int(alg[top]),
-            "frac_nominal_8TBps": round(achieved / NOMINAL_HBM_GBS, 3)}
-    roof["traffic"] = recorded_traffic(args.config, top)
+            "frac_nominal_8TBps": round(achieved / NOMINAL_HBM_GBS, 3),
+            "timing": "events around the kernel in a serialised replay of the step after each "
+                      "timed step (the kernel has the GPU to itself)",
+            "in_step": {"us_per_launch": round(cc_mean * 1e3, 2), "achieved": round(cc_gbs, 1),
+                        "frac": round(cc_gbs / peak, 3),
+                        "timing": "events around the kernel on its own stream in a concurrent "
+                                  "replay of the step (it shares the GPU with the other chains)"}}
     step_bytes = sum(alg.values())
-    line = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/int32",
-        "data": "synthetic",
-        "config": {"workload": f"{w.name}: {w.num_reqs} requests, {w.num_tokens} query tokens, "
-                               f"head_dim {w.head_dim} (rope {w.rope_dim}), window {w.window}, "
-                               f"top-k {w.topk}, ratio {w.compress_ratio}",
-                   "path": path,
-                   "storage": "bf16 rows in and out; fp8 e4m3 records with UE8M0 scales; "
-                              "MXFP4 (e2m1 + E8M0) indexer keys",
-                   "seed": w.seed, "l2": ("flushed before every step: 512 MiB memset, then a 256 MiB read so "
-                         "the lines left in L2 are clean"),
-                   "parallelism": f"dp{world} (independent batch per GPU)",
-                   "launch": ("cuda graph of the step on three streams" if g_plain is not None
-                              else "eager, three streams"),
-                   "timing": "value: events around an un-instrumented graph replay of each "
-                             "step; roofline: events around the dominant kernel in a second, "
-                             "instrumented replay of the same step after each timed step"},
-        "roofline": roof,
-        "kernels": kernels,
-        "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
-                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "ms_per_step": round(e2e["ms_per_step"], 4),
-                "launch": e2e["mode"] + " of [pinned host->device input copies, the step, "
-                          "device->host output copies], host clock around each replay"},
-        "gpu_launches": 2 * len(launches) * args.steps,
+    res = {
+        "workload": (f"{w.name}: {w.num_reqs} requests, {w.num_tokens} query tokens, "
+                     f"head_dim {w.head_dim} (rope {w.rope_dim}), window {w.window}, "
+                     f"top-k {w.topk}, ratio {w.compress_ratio}"),
+        "path": path, "seed": w.seed, "tokens_per_step": w.num_tokens,
+        "launch": step_layout(p, path, g_plain is not None),
+        "ms_per_step": round(ms_per_step, 5), "value": round(value, 1),
+        "roofline": roof, "kernels": kernels,
         "step_alg_bytes": int(step_bytes),
         "step_GBps": round(step_bytes / (ms_per_step / 1e3) / 1e9, 1),
-        "clocks": clk,
-        "wall_s_timed_region": round(t_wall, 4),
-        "back_to_back": b2b,
+        "step_frac_measured": round(step_bytes / (ms_per_step / 1e3) / 1e9 / peak, 3),
+        "gpu_launches": 3 * len(launches) * steps,
+        "clocks": clk, "wall_s_timed_region": round(t_wall, 4), "back_to_back": b2b,
+    }
+    del g_plain, g_cc, g_iso
+    if headline:
+        e2e = run_e2e(p, args, dev, flush, path)
+        e2e_ms = _max_over_ranks(torch, dist, dev, e2e["ms_per_step"])
+        res["e2e"] = {"value": round(w.num_tokens * world / (e2e_ms / 1e3), 1), "unit": UNIT,
+                      "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                      "ms_per_step": round(e2e_ms, 4),
+                      "launch": e2e["mode"] + " of [pinned host->device input copies, the "
+                                "step, device->host output copies], host clock around each "
+                                "replay"}
+        res["_w"] = w
+    del p
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG,
+                    choices=["tiny", "decode", "prefill", "mixed", "mxfp4", "prefill_small",
+                             "decode_hca"])
+    ap.add_argument("--configs", default=",".join(SIDE_CONFIGS),
+                    help="comma-separated workloads measured after the headline one, each "
+                         "reported under `configs` (empty: none)")
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--path", default="auto",
+                    choices=["auto", "index", "fused", "workspace", "dense", "dense_fused",
+                             "indexer_fp8",
+                             "indexer_store", "compressor"],
+                    help="auto: fused for index matrices of up to 2^20 items (latency-bound "
+                         "batches), else index; "
+                         "index: the index-keyed gather into [T, W+P, D]; workspace: the "
+                         "prefill workspace path (range gathers + workspace indices); dense: "
+                         "the no-top-k decode step of a heavily compressed layer (the "
+                         "decode_hca workload always takes it); indexer_fp8 / indexer_store: "
+                         "the mxfp4 workload's step with the FP8 indexer record or the fused "
+                         "norm-RoPE store as the key writer; compressor: the compressed-KV "
+                         "producer (ratio 4 and 128 layers) of a prefill batch.  Applies to "
+                         "the headline workload; the others take auto")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch the step eagerly instead of replaying a CUDA graph")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    from paged_sparse_kv_gb300 import build as psk_build
+
+    psk_build.build()
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    flush = L2Flush(torch, dev)
+    head = run_config(args, torch, dev, dist, world, rank, flush, args.config, args.steps,
+                      args.warmup, headline=True)
+    w = head.pop("_w")
+    side = {}
+    for name in [c for c in args.configs.split(",") if c and c != args.config]:
+        r = run_config(args, torch, dev, dist, world, rank, flush, name, min(args.steps, 20),
+                       args.warmup, headline=False)
+        side[name] = {k: r[k] for k in ("workload", "path", "value", "ms_per_step",
+                                        "step_GBps", "step_frac_measured", "roofline",
+                                        "kernels", "launch", "back_to_back", "clocks",
+                                        "gpu_launches")}
+        side[name]["unit"] = UNIT
+
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/int32",
+        "data": "synthetic",
+        "config": {"workload": head["workload"], "path": head["path"],
+                   "storage": "bf16 rows in and out; fp8 e4m3 records with UE8M0 scales; "
+                              "MXFP4 (e2m1 + E8M0) indexer keys",
+                   "seed": head["seed"],
+                   "l2": ("flushed before every step: 512 MiB memset, then a 256 MiB read so "
+                          "the lines left in L2 are clean"),
+                   "parallelism": f"dp{world} (independent batch per GPU)",
+                   "launch": head["launch"],
+                   "timing": "value: events around an un-instrumented graph replay of each "
+                             "step; roofline: events around the dominant kernel in a "
+                             "serialised instrumented replay after each timed step "
+                             "(roofline.in_step: in a concurrent instrumented replay)"},
+        "roofline": head["roofline"],
+        "kernels": head["kernels"],
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
+        "step_alg_bytes": head["step_alg_bytes"],
+        "step_GBps": head["step_GBps"],
+        "step_frac_measured": head["step_frac_measured"],
+        "clocks": head["clocks"],
+        "wall_s_timed_region": head["wall_s_timed_region"],
+        "back_to_back": head["back_to_back"],
+        "configs": side,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, desc = time_oracle(w, args.cpu_budget, path=path)
+        v, desc = time_oracle(w, args.cpu_budget, path=head["path"])
         line["cpu_baseline"] = {"value": round(v, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": desc, "host": host_description()}
     if rank == 0:

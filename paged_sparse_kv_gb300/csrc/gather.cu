@@ -187,12 +187,9 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
         mbar_fence_init();
     }
     __syncthreads();
-    // The forms that compute slots (every form but INDEX and PAIR) read only
-    // inputs no libpsk kernel writes (positions, top-k indices, tables) to do
-    // so: the producer resolves its first round of slots before waiting for
-    // the previous kernel on the stream, and copies no cache row before.
-    constexpr bool kEarlySlots = SRC != kSrcIndex && SRC != kSrcPair;
-    if (!kEarlySlots || warp != 0) pdl_wait();
+    // Every input, the slot metadata included, may come from the previous
+    // kernel on the stream: nothing global is read before its grid is done.
+    pdl_wait();
     pdl_launch_dependents();
 
     if (warp == 0) {
@@ -203,7 +200,6 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
         const int half = lane >> 4, r = lane & 15;
         int i = 0;
         bool ok = true;
-        bool waited = !kEarlySlots;
         for (int64_t base = blockIdx.x; base < tiles && ok; base += (int64_t)kLoadTiles * gridDim.x) {
             int32_t slot[kLoadTiles / 2];
             int64_t oof[kLoadTiles / 2];
@@ -257,10 +253,6 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
                     slot[q] = -2;
                 }
             }
-            if (!waited) {
-                pdl_wait();
-                waited = true;
-            }
 #pragma unroll
             for (int k = 0; k < kLoadTiles; ++k) {
                 const int64_t tile = base + (int64_t)k * gridDim.x;
@@ -308,7 +300,6 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
                 ++i;
             }
         }
-        if (!waited) pdl_wait();
         if (!ok && lane == 0) atomicAdd(&g_wait_timeouts, 1u);
         // Drain: the last phase issued on every stage must land before exit.
         if (lane == 0) {
@@ -404,13 +395,8 @@ gather_small_kernel(GatherParams p, TopkSource tk) {
     const int64_t items = p.rows * (int64_t)p.cols;
     const int64_t capacity = p.num_pages * (int64_t)p.block_size;
     const bool small = items <= 0xFFFFFFFFll;
-    // The TOPK form computes slots from inputs no libpsk kernel writes: its
-    // first batch of slots is resolved before waiting for the previous kernel
-    // on the stream (no record is read before).
-    constexpr bool kEarlySlots = SRC == kSrcTopk;
-    if (!kEarlySlots) pdl_wait();
+    pdl_wait();
     pdl_launch_dependents();
-    bool waited = !kEarlySlots;
 
     for (int64_t b0 = warp_id * BATCH; b0 < items; b0 += nwarps * BATCH) {
         // slot id and output offset of item b0 + lane
@@ -435,10 +421,6 @@ gather_small_kernel(GatherParams p, TopkSource tk) {
                 my_slot = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
             }
             my_off = t * p.out_stride_t + (int64_t)j * p.out_stride_j;
-        }
-        if (!waited) {
-            pdl_wait();
-            waited = true;
         }
         uint2 raw[STEPS][CPL];     // REC 1: .x = 4 value bytes; REC 2: 8 e4m3 bytes
         uint32_t scl[STEPS][CPL];  // REC 1: scale byte; REC 2: binary32 scale bits
@@ -518,13 +500,9 @@ cudaError_t gather_fp8_dispatch(const ItemSource& src, int64_t items, cudaStream
                         2 * kStages * sizeof(uint64_t) +
                         kStages * kRowsPerTile * (sizeof(int64_t) + sizeof(int32_t));
     auto kern = gather_fp8_tma_kernel<D, UE8M0, SRC>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             200 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> limit_set{0};
+    const cudaError_t e = set_smem_limit_per_device(kern, 200 * 1024, limit_set);
+    if (e != cudaSuccess) return e;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTmaThreads, smem) !=
             cudaSuccess || per_sm < 1)

@@ -457,6 +457,8 @@ def random_cache_bytes(seed: int, geom: CacheGeom) -> np.ndarray:
     E4M3 NaN codes), so that every record decodes to finite or infinite
     values and both implementations see identical bytes."""
     rng = np.random.default_rng(seed)
-    b = rng.integers(0, 254, size=(geom.num_pages, geom.page_stride), dtype=np.uint8)
-    b[b >= 0x7F] += 1          # 0..253 -> 0..126, 128..254: skips 0x7F and 0xFF
+    n = geom.num_pages * geom.page_stride
+    b = np.frombuffer(rng.bytes(n), dtype=np.uint8).reshape(geom.num_pages, geom.page_stride)
+    b = b.copy()
+    b[(b & 0x7F) == 0x7F] ^= 1  # 0x7F -> 0x7E, 0xFF -> 0xFE
     return b
