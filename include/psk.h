@@ -101,6 +101,11 @@ int32_t psk_abi_version(void);
  * that launch is incomplete.  This call copies the current device's count
  * (the sum over those kernels; 0 in normal operation) into *count.  Synchronous (it waits for the
  * device); returns PSK_ERR_CUDA if the copy fails.
+ * Once the count has risen, treat every output written on the device since
+ * the last check as invalid: the launch that gave up left rows unwritten, and
+ * a CTA whose final drain also expired may have retired with bulk copies
+ * still landing in its shared memory, which a CTA of a launch running beside
+ * it could then be using.
  */
 psk_status psk_device_wait_timeouts(uint32_t* count);
 

@@ -47,6 +47,14 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ unsigned int g_wait_timeouts = 0;
 
+// Shuffle of a 32- or 64-bit record offset from lane `src`.
+__device__ __forceinline__ uint32_t shfl_off(uint32_t v, int src) {
+    return __shfl_sync(0xFFFFFFFFu, v, src);
+}
+__device__ __forceinline__ uint64_t shfl_off(uint64_t v, int src) {
+    return __shfl_sync(0xFFFFFFFFu, (unsigned long long)v, src);
+}
+
 __device__ __forceinline__ void item_to_tj(int64_t item, int32_t cols, bool small, int64_t& t,
                                            int32_t& j) {
     if (small) {
@@ -362,31 +370,33 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
 //
 // A 68-byte MXFP4 record (or a 132-byte FP8 indexer record at head_dim 128)
 // is too small for a bulk copy to pay off, so this gather uses plain loads
-// arranged for memory-level parallelism: a warp takes a batch of STEPS * GPW
-// consecutive (t, j) items, loads their slot ids with one coalesced load, then
-// issues every record load of the batch (per lane and item: 4 bytes of packed
-// E2M1 values and their scale byte, or 8 e4m3 bytes and the row's binary32
-// scale) before it converts and stores anything.
+// arranged for memory-level parallelism.  A warp resolves up to 32 consecutive
+// (t, j) items at a time (rpr of them), one per lane: the item's slot (from the index
+// matrix, or its local top-k entry through the request's table), the byte
+// offsets of its record's values and scales in the cache, and its output
+// offset.  It then walks those items in groups of STEPS * GPW: each lane group
+// takes an item's offsets from the owner lane by shuffles, every record load
+// of the group (per lane and item: 4 bytes of packed E2M1 values and their
+// scale byte, or 8 e4m3 bytes and the row's binary32 scale) is issued before
+// any conversion, then the group is converted and stored.  Offsets are 32-bit
+// when the cache is below 4 GiB (OFF = uint32_t), else 64-bit.
 // REC 1: MXFP4 (TokenSpeed read_deepseek_v4_indexer_mxfp4_cache); REC 2: the
 // FP8 indexer record (write_deepseek_v4_indexer_fp8_cache's layout).
-// Rows per lane group in one batch of the small-record gather.  Four keeps the
-// kernel at 32-36 registers: the decode step, where it shares the SMs with the
-// FP8 gathers and the builders, ran 22.2-22.5 us against 23.1 with eight (52
-// registers) and 27.3 with sixteen (80); the 262,144-row MXFP4 gather alone is
-// the same (20.5 us) with four or eight.
+// Rows per lane group in one group of the small-record gather.
 constexpr int kSmallSteps = 4;
 
-template <int D, int REC, int SRC>
+template <int D, int REC, int SRC, typename OFF>
 __global__ void __launch_bounds__(kThreads)
-gather_small_kernel(GatherParams p, TopkSource tk) {
+gather_small_kernel(GatherParams p, TopkSource tk, int rpr) {
     constexpr int CHUNKS = D / 8;
     constexpr int LANES = CHUNKS < kWarp ? CHUNKS : kWarp;
     constexpr int CPL = CHUNKS / LANES;
     constexpr int GPW = kWarp / LANES;
     constexpr int STEPS = (kWarp / GPW) < kSmallSteps ? (kWarp / GPW) : kSmallSteps;
-    constexpr int BATCH = STEPS * GPW;  // <= 32 items, one slot id per lane
+    constexpr int GROUP = STEPS * GPW;          // items per group, a divisor of 32
     constexpr int VB = REC == 1 ? D / 2 : D;    // value bytes per token
     constexpr int SB = REC == 1 ? D / 32 : 4;   // scale bytes per token
+    constexpr OFF kZeroRow = ~(OFF)0;           // value offset of an item with no record
 
     const int lane = threadIdx.x & 31;
     const int grp = lane / LANES, gl = lane % LANES;
@@ -395,14 +405,16 @@ gather_small_kernel(GatherParams p, TopkSource tk) {
     const int64_t items = p.rows * (int64_t)p.cols;
     const int64_t capacity = p.num_pages * (int64_t)p.block_size;
     const bool small = items <= 0xFFFFFFFFll;
+    const OFF scale_region = (OFF)((int64_t)p.block_size * VB);
     pdl_wait();
     pdl_launch_dependents();
 
-    for (int64_t b0 = warp_id * BATCH; b0 < items; b0 += nwarps * BATCH) {
-        // slot id and output offset of item b0 + lane
-        int32_t my_slot = -1;
-        int64_t my_off = -1;
-        if (lane < BATCH && b0 + lane < items) {
+    for (int64_t b0 = warp_id * rpr; b0 < items; b0 += nwarps * rpr) {
+        // item b0 + lane (lane < rpr): its record's value and scale offsets and
+        // its output offset
+        OFF my_vo = kZeroRow, my_so = 0;
+        int64_t my_out = -1;
+        if (lane < rpr && b0 + lane < items) {
             const int64_t item = b0 + lane;
             int64_t t;
             int32_t j;
@@ -414,66 +426,77 @@ gather_small_kernel(GatherParams p, TopkSource tk) {
                 t = item / p.cols;
                 j = (int32_t)(item - t * p.cols);
             }
+            int32_t slot;
             if (SRC == kSrcTopk) {
-                my_slot = topk_item_slot(tk, p.block_size, p.block_shift, capacity, t, j);
+                slot = topk_item_slot(tk, p.block_size, p.block_shift, capacity, t, j);
             } else {
                 const int32_t raw = __ldg(p.idx + t * p.idx_stride + j);
-                my_slot = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
+                slot = (raw >= 0 && (int64_t)raw < capacity) ? raw : -1;
             }
-            my_off = t * p.out_stride_t + (int64_t)j * p.out_stride_j;
-        }
-        uint2 raw[STEPS][CPL];     // REC 1: .x = 4 value bytes; REC 2: 8 e4m3 bytes
-        uint32_t scl[STEPS][CPL];  // REC 1: scale byte; REC 2: binary32 scale bits
-        int32_t slot[STEPS];
-#pragma unroll
-        for (int st = 0; st < STEPS; ++st) {
-            slot[st] = __shfl_sync(0xFFFFFFFFu, my_slot, st * GPW + grp);
-            if (slot[st] >= 0) {
+            if (slot >= 0) {
                 int32_t off;
-                const int32_t page = div_block32(slot[st], p.block_size, p.block_shift, off);
-                const uint8_t* base = p.cache + (int64_t)page * p.page_stride;
-                const uint8_t* vals = base + (int64_t)off * VB;
-                const uint8_t* sc = base + (int64_t)p.block_size * VB + (int64_t)off * SB;
+                const int32_t page = div_block32(slot, p.block_size, p.block_shift, off);
+                const OFF pb = (OFF)((int64_t)page * p.page_stride);
+                my_vo = pb + (OFF)off * VB;
+                my_so = pb + scale_region + (OFF)off * SB;
+            }
+            my_out = t * p.out_stride_t + (int64_t)j * p.out_stride_j;
+        }
+        const int n_here = items - b0 < rpr ? (int)(items - b0) : rpr;
+        for (int g = 0; g < n_here; g += GROUP) {
+            uint2 raw[STEPS][CPL];     // REC 1: .x = 4 value bytes; REC 2: 8 e4m3 bytes
+            uint32_t scl[STEPS][CPL];  // REC 1: scale byte; REC 2: binary32 scale bits
+            bool has[STEPS];
 #pragma unroll
-                for (int i = 0; i < CPL; ++i) {
-                    const int c = gl + i * LANES;
-                    if constexpr (REC == 1) {
-                        raw[st][i].x = ld_nc_u32(vals + 4 * c);
-                        scl[st][i] = ld_nc_u8(sc + c / 4);
-                    } else {
-                        raw[st][i] = ld_nc_v2(vals + 8 * c);
-                        scl[st][i] = ld_nc_u32(sc);
+            for (int st = 0; st < STEPS; ++st) {
+                const int src = g + st * GPW + grp;
+                const OFF vo = shfl_off(my_vo, src);
+                const OFF so = shfl_off(my_so, src);
+                has[st] = vo != kZeroRow;
+                if (has[st]) {
+                    const uint8_t* vals = p.cache + vo;
+                    const uint8_t* sc = p.cache + so;
+#pragma unroll
+                    for (int i = 0; i < CPL; ++i) {
+                        const int c = gl + i * LANES;
+                        if constexpr (REC == 1) {
+                            raw[st][i].x = ld_nc_u32(vals + 4 * c);
+                            scl[st][i] = ld_nc_u8(sc + c / 4);
+                        } else {
+                            raw[st][i] = ld_nc_v2(vals + 8 * c);
+                            scl[st][i] = ld_nc_u32(sc);
+                        }
                     }
                 }
             }
-        }
 #pragma unroll
-        for (int st = 0; st < STEPS; ++st) {
-            const int64_t off = __shfl_sync(0xFFFFFFFFu, my_off, st * GPW + grp);
-            if (off < 0) continue;
-            uint16_t* orow = p.out + off;
+            for (int st = 0; st < STEPS; ++st) {
+                const int64_t off = __shfl_sync(0xFFFFFFFFu, my_out, g + st * GPW + grp);
+                if (off < 0) continue;
+                uint16_t* orow = p.out + off;
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) {
-                const int c = gl + i * LANES;
-                uint4 o;
-                if (slot[st] < 0) {
-                    o = make_uint4(0u, 0u, 0u, 0u);
-                } else if constexpr (REC == 1) {
-                    const uint64_t s2 = splat_f32x2(ue8m0_scale(scl[st][i]));
-                    const uint32_t w = raw[st][i].x;
-                    o.x = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(w & 0xFFu), s2);
-                    o.y = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((w >> 8) & 0xFFu), s2);
-                    o.z = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((w >> 16) & 0xFFu), s2);
-                    o.w = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(w >> 24), s2);
-                } else {
-                    const uint64_t s2 = splat_f32x2(__uint_as_float(scl[st][i]));
-                    const uint2 w = raw[st][i];
-                    o.x = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x & 0xFFFFu), s2);
-                    o.y = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x >> 16), s2);
-                    o.z = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y & 0xFFFFu), s2);
-                    o.w = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y >> 16), s2);
+                for (int i = 0; i < CPL; ++i) {
+                    const int c = gl + i * LANES;
+                    uint4 o;
+                    if (!has[st]) {
+                        o = make_uint4(0u, 0u, 0u, 0u);
+                    } else if constexpr (REC == 1) {
+                        const uint64_t s2 = splat_f32x2(ue8m0_scale(scl[st][i]));
+                        const uint32_t w = raw[st][i].x;
+                        o.x = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(w & 0xFFu), s2);
+                        o.y = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((w >> 8) & 0xFFu), s2);
+                        o.z = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((w >> 16) & 0xFFu), s2);
+                        o.w = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(w >> 24), s2);
+                    } else {
+                        const uint64_t s2 = splat_f32x2(__uint_as_float(scl[st][i]));
+                        const uint2 w = raw[st][i];
+                        o.x = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x & 0xFFFFu), s2);
+                        o.y = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x >> 16), s2);
+                        o.z = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y & 0xFFFFu), s2);
+                        o.w = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y >> 16), s2);
+                    }
+                    st_stream_v4(orow + 8 * c, o);
                 }
-                st_stream_v4(orow + 8 * c, o);
             }
         }
     }
@@ -508,6 +531,9 @@ cudaError_t gather_fp8_dispatch(const ItemSource& src, int64_t items, cudaStream
             cudaSuccess || per_sm < 1)
         per_sm = 1;
     const int64_t tiles = (items + kRowsPerTile - 1) / kRowsPerTile;
+#ifdef PSK_GATHER_CTAS_PER_SM
+    if (per_sm > PSK_GATHER_CTAS_PER_SM) per_sm = PSK_GATHER_CTAS_PER_SM;
+#endif
     int64_t blocks = (int64_t)sm_count() * per_sm;
     if (blocks > tiles) blocks = tiles;
     return launch_pdl(kern, dim3((unsigned)blocks), dim3(kTmaThreads), smem, stream, src,
@@ -534,17 +560,47 @@ cudaError_t fp8_by_dim(const ItemSource& src, int64_t items, cudaStream_t stream
     }
 }
 
-template <int D, int REC, int SRC>
-cudaError_t gather_small_dispatch(const GatherParams& p, const TopkSource& tk,
-                                  cudaStream_t stream) {
+#ifndef PSK_SMALL_RPR
+#define PSK_SMALL_RPR 0  // items a warp resolves per round; 0: chosen per launch
+#endif
+
+template <int D, int REC, int SRC, typename OFF>
+cudaError_t gather_small_launch(const GatherParams& p, const TopkSource& tk,
+                                cudaStream_t stream) {
     constexpr int LANES = (D / 8) < kWarp ? (D / 8) : kWarp;
     constexpr int GPW = kWarp / LANES;
     constexpr int STEPS = (kWarp / GPW) < kSmallSteps ? (kWarp / GPW) : kSmallSteps;
+    constexpr int GROUP = STEPS * GPW;
+    auto kern = gather_small_kernel<D, REC, SRC, OFF>;
     const int64_t items = p.rows * (int64_t)p.cols;
-    auto kern = gather_small_kernel<D, REC, SRC>;
-    const int64_t batches = (items + STEPS * GPW - 1) / (STEPS * GPW);
-    const int64_t blocks = persistent_blocks(kern, batches, kWarp);
-    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p, tk);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t resident_warps = (int64_t)sm_count() * per_sm * (kThreads / kWarp);
+    // Items per warp round: 32 (one per lane, the fewest instructions per row)
+    // when the batch still gives every resident warp a full round, else fewer,
+    // so that small batches keep every warp's loads in flight.  Measured alone
+    // (events, L2 flushed): the 8.4 M-row prefill gather 411.7 / 397.3 /
+    // 387.1 us at 8 / 16 / 32 items per round, the 262,144-row MXFP4 batch
+    // 20.5 / 20.5 / 18.4 us, the 32,768-row decode batch 8.2 / 10.2 / 14.3 us.
+    int rpr = GROUP;
+    while (rpr < kWarp && items >= (int64_t)2 * rpr * resident_warps) rpr *= 2;
+    if (PSK_SMALL_RPR > 0) rpr = PSK_SMALL_RPR;
+    const int64_t warps = (items + rpr - 1) / rpr;
+    const int64_t need = (warps * kWarp + kThreads - 1) / kThreads;
+    const int64_t full = (int64_t)sm_count() * per_sm;
+    const int64_t blocks = need < full ? need : full;
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p, tk, rpr);
+}
+
+template <int D, int REC, int SRC>
+cudaError_t gather_small_dispatch(const GatherParams& p, const TopkSource& tk,
+                                  cudaStream_t stream) {
+    // 32-bit record offsets while every byte of the cache is below 4 GiB
+    if (p.num_pages * p.page_stride < (int64_t(1) << 32) - 1)
+        return gather_small_launch<D, REC, SRC, uint32_t>(p, tk, stream);
+    return gather_small_launch<D, REC, SRC, uint64_t>(p, tk, stream);
 }
 
 template <int REC, int SRC>
