@@ -412,6 +412,48 @@ def test_fp8_gather_random_records(cuda_device, D, rope, ue8m0, bs):
     assert np.all(got[:, 0] == seven) and np.all(got[:, Cc + 1] == seven)
 
 
+@pytest.mark.parametrize("ue8m0", [True, False])
+def test_fp8_gather_every_scale(cuda_device, ue8m0):
+    """Every scale a record can hold: UE8M0 bytes cycling through 0..254 (127,
+    the scale 2^0, included), or binary32 scale words of random finite bit
+    patterns (normals of every exponent, subnormals, +-0), so the binary32
+    products round, overflow to +-inf and go subnormal; random non-NaN codes."""
+    rng = np.random.default_rng(31 + ue8m0)
+    D, rope, bs, pages = 512, 64, 16, 20
+    nope, ts, nb = D - rope, D - rope + 2 * rope, D // 64
+    rec = oracle.fp8_record_bytes(D, rope, ue8m0)
+    geom = synthetic.CacheGeom(pages, bs, bs * rec)
+    host = synthetic.random_cache_bytes(41 + ue8m0, geom)
+    n = pages * bs
+    if ue8m0:
+        scl = (np.arange(n * nb) % 255).astype(np.uint8).reshape(n, nb)
+        scl[:, nb - 1] = 0  # the pad slot
+        for s_ in range(n):
+            page, off = divmod(s_, bs)
+            host[page, bs * ts + off * nb: bs * ts + (off + 1) * nb] = scl[s_]
+        assert set(np.unique(scl[:, :nb - 1])) == set(range(255))
+    else:
+        w = rng.integers(0, 1 << 32, size=(n, nb), dtype=np.uint64).astype(np.uint32)
+        w[((w >> 23) & 0xFF) == 0xFF] &= ~np.uint32(0x40000000)
+        w[0] = np.array([0, 0x80000000, 1, 0x807FFFFF, 0x7F7FFFFF, 0x00800000, 0x3F800000, 0],
+                        np.uint32)
+        for s_ in range(n):
+            page, off = divmod(s_, bs)
+            host[page, bs * ts + off * 4 * nb: bs * ts + (off + 1) * 4 * nb] = w[s_].view(np.uint8)
+    idx = rng.permutation(n).astype(np.int32).reshape(20, 16)
+    idx[3, 5] = -1
+    out = torch.empty((20, 16, D), dtype=torch.bfloat16, device=cuda_device)
+    ops.dequantize_and_gather_k_cache(out, torch.from_numpy(host).to(cuda_device),
+                                      _dev_i32(idx, cuda_device), bs, rope_dim=rope,
+                                      is_ue8m0=ue8m0)
+    want = oracle.dequantize_and_gather_k_cache(host, bs, 0, D, rope, idx, is_ue8m0=ue8m0)
+    got = _u16(out)
+    _assert_same(got, want, f"every scale, ue8m0={ue8m0}")
+    flat = want[:, :, :nope].reshape(-1)
+    assert np.any((flat & 0x7FFF) == 0x7F80), "no product reached +-inf"
+    assert np.any(((flat & 0x7F80) == 0) & ((flat & 0x7FFF) != 0)), "no subnormal result"
+
+
 @pytest.mark.parametrize("bs", [8, 3])
 @pytest.mark.parametrize("D", [32, 64, 128, 256, 512, 1024])
 def test_mxfp4_gather_random_records(cuda_device, D, bs):
