@@ -10,9 +10,10 @@
 //    that moves records into shared memory with 1-D bulk copies (TMA) and
 //    dequantizes from there (details above the kernel).
 //  * MXFP4 records (68 B per 128-dim row): batched plain loads.
-// Both write each output row as 16-byte chunks, one warp store instruction
-// covering 512 contiguous bytes, issued as streaming (evict-first) stores so
-// the gathered output does not push reused cache rows out of L2.  Decode is
+// Both write each output row as 32-byte chunks (one 256-bit store per lane
+// when the output is 32-byte aligned), a warp store instruction covering up to
+// 1 KB of contiguous output, issued as streaming (evict-first) stores so the
+// gathered output does not push reused cache rows out of L2.  Decode is
 // exact: cvt.rn.f16x2.{e4m3x2,e2m1x2}, a binary32 multiply by the scale, and
 // cvt.rn.bf16x2.f32.  Invalid slots (negative or beyond the cache) give zero
 // rows.  The scale multiply is one packed mul.rn.f32x2 per pair of elements.
@@ -39,13 +40,37 @@ constexpr int kThreads = 256;
 // the thread counts a timeout in g_wait_timeouts and stops; the producer
 // always drains the copies it issued before it exits.
 
-constexpr int kStages = 4;
+// Ring depth and residency of the FP8 gather: three stages of 16 rows (29 KB of
+// shared memory at head_dim 512) and launch bounds for six CTAs per SM up to
+// head_dim 512, which hold the kernel to 32 registers, so seven are resident.
+// Against four stages at five CTAs per SM (40 registers), interleaved on one
+// box, each launch alone after an L2 flush: the prefill top-k gather 1585 ->
+// 1475 us, its window gather 401 -> 383 us, the fused top-k and window forms
+// 1661 -> 1449 / 498 -> 387 us, the mixed window gather 110.6 -> 106.5 us; the
+// mixed top-k gather (many padding entries, whose zero rows need no record and
+// let the consumers outrun a shallower ring) 779 -> 817 us.  Six and eight
+// stages at fewer CTAs per SM were slower still; boxes differ by up to ~9% on
+// the same build.
+#ifndef PSK_GATHER_STAGES
+#define PSK_GATHER_STAGES 3
+#endif
+#ifndef PSK_GATHER_MIN_CTAS
+#define PSK_GATHER_MIN_CTAS 6
+#endif
+constexpr int kStages = PSK_GATHER_STAGES;
 constexpr int kRowsPerTile = 16;
 constexpr int kConsumerWarps = 8;
 constexpr int kTmaThreads = kWarp * (1 + kConsumerWarps);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ unsigned int g_wait_timeouts = 0;
+
+// 1 when every output row start (out + a * stride_a + b * stride_b elements)
+// is 32-byte aligned, so a gather can store 32-byte chunks.
+inline int out32_aligned(const void* out, int64_t stride_a, int64_t stride_b) {
+    return (reinterpret_cast<uintptr_t>(out) % 32 == 0 && (stride_a * 2) % 32 == 0 &&
+            (stride_b * 2) % 32 == 0) ? 1 : 0;
+}
 
 // Shuffle of a 32- or 64-bit record offset from lane `src`.
 __device__ __forceinline__ uint32_t shfl_off(uint32_t v, int src) {
@@ -156,10 +181,13 @@ __device__ __forceinline__ int32_t dense_item_slot(const DenseSource& s, int32_t
 }
 
 template <int D, bool UE8M0, int SRC>
-__global__ void __launch_bounds__(kTmaThreads)
-gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
+__global__ void __launch_bounds__(kTmaThreads, D <= 512 ? PSK_GATHER_MIN_CTAS : 1)
+gather_fp8_tma_kernel(ItemSource src, int slot_bytes, int v8) {
     const GatherParams& p = src.g;
-    constexpr int CHUNKS = D / 8;
+    // A consumer lane owns 32-byte output chunks (16 bf16 values): with a
+    // 32-byte aligned output each is one 256-bit store and a warp's store covers
+    // 1 KB of contiguous output (v8 != 0), else two 16-byte stores.
+    constexpr int CHUNKS = D / 16;
     constexpr int LANES = CHUNKS < kWarp ? CHUNKS : kWarp;
     constexpr int CPL = CHUNKS / LANES;
     constexpr int GPW = kWarp / LANES;
@@ -338,27 +366,33 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
             const uint8_t* srow = ring + (size_t)(s * kRowsPerTile + r) * slot_bytes;
 #pragma unroll
             for (int ci = 0; ci < CPL; ++ci) {
-                const int c = gl + ci * LANES;
-                uint4 o;
+                const int c = gl + ci * LANES;  // values [16c, 16c + 16)
+                uint4 lo, hi;
                 if (soff < 0) {
-                    o = make_uint4(0u, 0u, 0u, 0u);
-                } else if (8 * c < nope) {
-                    const uint2 w = lds_v2(srow + 8 * c);
+                    lo = hi = make_uint4(0u, 0u, 0u, 0u);
+                } else if (16 * c < nope) {
+                    const uint4 w = lds_v4(srow + 16 * c);
                     float sc;
                     if constexpr (UE8M0) {
-                        sc = ue8m0_scale(lds_u8(srow + ts + soff + c / 8));
+                        sc = ue8m0_scale(lds_u8(srow + ts + soff + c / 4));
                     } else {
-                        sc = __uint_as_float(lds_u32(srow + ts + soff + 4 * (c / 8)));
+                        sc = __uint_as_float(lds_u32(srow + ts + soff + 4 * (c / 4)));
                     }
                     const uint64_t s2 = splat_f32x2(sc);
-                    o.x = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x & 0xFFFFu), s2);
-                    o.y = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x >> 16), s2);
-                    o.z = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y & 0xFFFFu), s2);
-                    o.w = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y >> 16), s2);
+                    lo.x = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x & 0xFFFFu), s2);
+                    lo.y = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x >> 16), s2);
+                    lo.z = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y & 0xFFFFu), s2);
+                    lo.w = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y >> 16), s2);
+                    hi.x = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.z & 0xFFFFu), s2);
+                    hi.y = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.z >> 16), s2);
+                    hi.z = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.w & 0xFFFFu), s2);
+                    hi.w = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.w >> 16), s2);
                 } else {
-                    o = lds_v4(srow + 16 * c - nope);
+                    // RoPE values: bf16 bytes [nope + 2 (16c - nope), + 32) of the record
+                    lo = lds_v4(srow + 32 * c - nope);
+                    hi = lds_v4(srow + 32 * c - nope + 16);
                 }
-                st_stream_v4(orow + 8 * c, o);
+                store_out32(orow + 16 * c, lo, hi, v8);
             }
         }
         __syncwarp();
@@ -376,9 +410,10 @@ gather_fp8_tma_kernel(ItemSource src, int slot_bytes) {
 // offsets of its record's values and scales in the cache, and its output
 // offset.  It then walks those items in groups of STEPS * GPW: each lane group
 // takes an item's offsets from the owner lane by shuffles, every record load
-// of the group (per lane and item: 4 bytes of packed E2M1 values and their
-// scale byte, or 8 e4m3 bytes and the row's binary32 scale) is issued before
-// any conversion, then the group is converted and stored.  Offsets are 32-bit
+// of the group (per lane and item: 8 bytes of packed E2M1 values and their
+// scale byte, or 16 e4m3 bytes and the row's binary32 scale) is issued before
+// any conversion, then the group is converted and each lane stores its 16
+// values as one 32-byte chunk.  Offsets are 32-bit
 // when the cache is below 4 GiB (OFF = uint32_t), else 64-bit.
 // REC 1: MXFP4 (TokenSpeed read_deepseek_v4_indexer_mxfp4_cache); REC 2: the
 // FP8 indexer record (write_deepseek_v4_indexer_fp8_cache's layout).
@@ -387,8 +422,8 @@ constexpr int kSmallSteps = 4;
 
 template <int D, int REC, int SRC, typename OFF>
 __global__ void __launch_bounds__(kThreads)
-gather_small_kernel(GatherParams p, TopkSource tk, int rpr) {
-    constexpr int CHUNKS = D / 8;
+gather_small_kernel(GatherParams p, TopkSource tk, int rpr, int v8) {
+    constexpr int CHUNKS = D / 16;  // 32-byte output chunks (16 values) per row
     constexpr int LANES = CHUNKS < kWarp ? CHUNKS : kWarp;
     constexpr int CPL = CHUNKS / LANES;
     constexpr int GPW = kWarp / LANES;
@@ -444,7 +479,7 @@ gather_small_kernel(GatherParams p, TopkSource tk, int rpr) {
         }
         const int n_here = items - b0 < rpr ? (int)(items - b0) : rpr;
         for (int g = 0; g < n_here; g += GROUP) {
-            uint2 raw[STEPS][CPL];     // REC 1: .x = 4 value bytes; REC 2: 8 e4m3 bytes
+            uint4 raw[STEPS][CPL];     // REC 1: .x, .y = 8 value bytes; REC 2: 16 e4m3 bytes
             uint32_t scl[STEPS][CPL];  // REC 1: scale byte; REC 2: binary32 scale bits
             bool has[STEPS];
 #pragma unroll
@@ -460,10 +495,12 @@ gather_small_kernel(GatherParams p, TopkSource tk, int rpr) {
                     for (int i = 0; i < CPL; ++i) {
                         const int c = gl + i * LANES;
                         if constexpr (REC == 1) {
-                            raw[st][i].x = ld_nc_u32(vals + 4 * c);
-                            scl[st][i] = ld_nc_u8(sc + c / 4);
+                            const uint2 v = ld_nc_v2(vals + 8 * c);
+                            raw[st][i].x = v.x;
+                            raw[st][i].y = v.y;
+                            scl[st][i] = ld_nc_u8(sc + c / 2);
                         } else {
-                            raw[st][i] = ld_nc_v2(vals + 8 * c);
+                            raw[st][i] = ld_nc_v4(vals + 16 * c);
                             scl[st][i] = ld_nc_u32(sc);
                         }
                     }
@@ -476,26 +513,34 @@ gather_small_kernel(GatherParams p, TopkSource tk, int rpr) {
                 uint16_t* orow = p.out + off;
 #pragma unroll
                 for (int i = 0; i < CPL; ++i) {
-                    const int c = gl + i * LANES;
-                    uint4 o;
+                    const int c = gl + i * LANES;  // values [16c, 16c + 16)
+                    uint4 lo, hi;
                     if (!has[st]) {
-                        o = make_uint4(0u, 0u, 0u, 0u);
+                        lo = hi = make_uint4(0u, 0u, 0u, 0u);
                     } else if constexpr (REC == 1) {
                         const uint64_t s2 = splat_f32x2(ue8m0_scale(scl[st][i]));
-                        const uint32_t w = raw[st][i].x;
-                        o.x = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(w & 0xFFu), s2);
-                        o.y = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((w >> 8) & 0xFFu), s2);
-                        o.z = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((w >> 16) & 0xFFu), s2);
-                        o.w = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(w >> 24), s2);
+                        const uint32_t a = raw[st][i].x, b = raw[st][i].y;
+                        lo.x = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(a & 0xFFu), s2);
+                        lo.y = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((a >> 8) & 0xFFu), s2);
+                        lo.z = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((a >> 16) & 0xFFu), s2);
+                        lo.w = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(a >> 24), s2);
+                        hi.x = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(b & 0xFFu), s2);
+                        hi.y = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((b >> 8) & 0xFFu), s2);
+                        hi.z = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2((b >> 16) & 0xFFu), s2);
+                        hi.w = scale_f16x2_to_bf16x2(cvt_e2m1x2_to_f16x2(b >> 24), s2);
                     } else {
                         const uint64_t s2 = splat_f32x2(__uint_as_float(scl[st][i]));
-                        const uint2 w = raw[st][i];
-                        o.x = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x & 0xFFFFu), s2);
-                        o.y = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x >> 16), s2);
-                        o.z = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y & 0xFFFFu), s2);
-                        o.w = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y >> 16), s2);
+                        const uint4 w = raw[st][i];
+                        lo.x = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x & 0xFFFFu), s2);
+                        lo.y = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.x >> 16), s2);
+                        lo.z = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y & 0xFFFFu), s2);
+                        lo.w = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.y >> 16), s2);
+                        hi.x = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.z & 0xFFFFu), s2);
+                        hi.y = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.z >> 16), s2);
+                        hi.z = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.w & 0xFFFFu), s2);
+                        hi.w = scale_f16x2_to_bf16x2(cvt_e4m3x2_to_f16x2(w.w >> 16), s2);
                     }
-                    st_stream_v4(orow + 8 * c, o);
+                    store_out32(orow + 16 * c, lo, hi, v8);
                 }
             }
         }
@@ -536,8 +581,11 @@ cudaError_t gather_fp8_dispatch(const ItemSource& src, int64_t items, cudaStream
 #endif
     int64_t blocks = (int64_t)sm_count() * per_sm;
     if (blocks > tiles) blocks = tiles;
+    const bool range = SRC == kSrcRange;
+    const int v8 = out32_aligned(src.g.out, range ? src.r.out_stride_r : src.g.out_stride_t,
+                                 range ? src.r.out_stride_i : src.g.out_stride_j);
     return launch_pdl(kern, dim3((unsigned)blocks), dim3(kTmaThreads), smem, stream, src,
-                      slot_bytes);
+                      slot_bytes, v8);
 }
 
 template <int SRC>
@@ -567,7 +615,7 @@ cudaError_t fp8_by_dim(const ItemSource& src, int64_t items, cudaStream_t stream
 template <int D, int REC, int SRC, typename OFF>
 cudaError_t gather_small_launch(const GatherParams& p, const TopkSource& tk,
                                 cudaStream_t stream) {
-    constexpr int LANES = (D / 8) < kWarp ? (D / 8) : kWarp;
+    constexpr int LANES = (D / 16) < kWarp ? (D / 16) : kWarp;
     constexpr int GPW = kWarp / LANES;
     constexpr int STEPS = (kWarp / GPW) < kSmallSteps ? (kWarp / GPW) : kSmallSteps;
     constexpr int GROUP = STEPS * GPW;
@@ -591,7 +639,8 @@ cudaError_t gather_small_launch(const GatherParams& p, const TopkSource& tk,
     const int64_t need = (warps * kWarp + kThreads - 1) / kThreads;
     const int64_t full = (int64_t)sm_count() * per_sm;
     const int64_t blocks = need < full ? need : full;
-    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p, tk, rpr);
+    const int v8 = out32_aligned(p.out, p.out_stride_t, p.out_stride_j);
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p, tk, rpr, v8);
 }
 
 template <int D, int REC, int SRC>
