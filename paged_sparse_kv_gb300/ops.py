@@ -214,7 +214,8 @@ def dequantize_and_gather_k_cache_ranges(out: torch.Tensor, cache: torch.Tensor,
     for t, n in ((seq_lens, "seq_lens"), (block_table, "block_table")):
         _need(t, torch.int32, n)
     num_pages, page_stride = _pages(cache)
-    _call(out.device, "dequantize_and_gather_k_cache_ranges", _ptr(out), out.stride(0), out.stride(1),
+    _call(out.device, "dequantize_and_gather_k_cache_ranges",
+          _ptr(out), out.stride(0), out.stride(1),
           out.shape[1], _ptr(cache), num_pages, page_stride, block_size,
           PSK_REC_FP8_DS_MLA, out.shape[2], rope_dim, int(bool(is_ue8m0)), _ptr(seq_lens),
           _ptr(gather_lens), _ptr(block_table), _rows(block_table, "block_table"),
@@ -390,7 +391,8 @@ def indexer_k_norm_rope_store(k_pre: torch.Tensor, positions: torch.Tensor,
         raise ValueError("k_pre must be [num_tokens, 128]")
     num_pages, page_stride = _pages(k_cache)
     record = PSK_REC_MXFP4 if use_fp4_cache else PSK_REC_FP8_INDEXER
-    _call(k_pre.device, "indexer_k_norm_rope_store", _ptr(k_pre), _rows(k_pre, "k_pre"), _ptr(positions),
+    _call(k_pre.device, "indexer_k_norm_rope_store",
+          _ptr(k_pre), _rows(k_pre, "k_pre"), _ptr(positions),
           _ptr(cos_sin_cache), _rows(cos_sin_cache, "cos_sin_cache"), cos_sin_cache.shape[0],
           _ptr(rms_norm_weight.contiguous()), float(rms_norm_eps), _ptr(kv_slot_mapping),
           kv_slot_mapping.shape[0], compress_ratio, record, _ptr(k_cache), num_pages,
@@ -504,7 +506,8 @@ def dequantize_and_gather_k_cache_window(out: torch.Tensor, cache: torch.Tensor,
         raise ValueError("out must be [T, window, D] with unit inner stride")
     num_pages, page_stride = _pages(cache)
     valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
-    _call(out.device, "dequantize_and_gather_k_cache_window", _ptr(out), out.stride(0), out.stride(1),
+    _call(out.device, "dequantize_and_gather_k_cache_window",
+          _ptr(out), out.stride(0), out.stride(1),
           _ptr(cache), num_pages, page_stride, block_size, out.shape[2], rope_dim,
           _ptr(query_start_loc), _ptr(seq_lens), _ptr(token_to_req), _ptr(replay_start),
           seq_lens.shape[0], T, _ptr(block_table), _rows(block_table, "block_table"),
@@ -558,7 +561,8 @@ def dequantize_and_gather_k_cache_dense(out: torch.Tensor, cache: torch.Tensor,
     num_pages, page_stride = _pages(cache)
     valid = None if is_valid_token is None else is_valid_token.to(torch.uint8)
     R = block_table.shape[0] if num_reqs is None else num_reqs
-    _call(out.device, "dequantize_and_gather_k_cache_dense", _ptr(out), out.stride(0), out.stride(1),
+    _call(out.device, "dequantize_and_gather_k_cache_dense",
+          _ptr(out), out.stride(0), out.stride(1),
           _ptr(cache), num_pages, page_stride, block_size, out.shape[2], rope_dim,
           _ptr(positions), T, _ptr(token_to_req), R, _ptr(block_table),
           _rows(block_table, "block_table"), block_table.shape[1], _ptr(base_offsets),

@@ -412,6 +412,50 @@ def test_fp8_gather_random_records(cuda_device, D, rope, ue8m0, bs):
     assert np.all(got[:, 0] == seven) and np.all(got[:, Cc + 1] == seven)
 
 
+@pytest.mark.parametrize("record", ["fp8_ds_mla", "mxfp4", "fp8_indexer"])
+@pytest.mark.parametrize("shift", [8, 72])
+def test_gather_output_16_byte_aligned_only(cuda_device, record, shift):
+    """Outputs whose rows start on 16-byte but not 32-byte boundaries (a base
+    offset of 16 bytes, or a row stride of an odd number of 16-byte units) take
+    the gathers' two-16-byte-store path: same bytes as the oracle, and nothing
+    outside the rows is written."""
+    rng = np.random.default_rng(17 + shift)
+    D, rope, bs, pages = (512, 64, 16, 8) if record == "fp8_ds_mla" else (128, 0, 16, 8)
+    if record == "fp8_ds_mla":
+        rec, code = oracle.fp8_record_bytes(D, rope), 0
+    elif record == "mxfp4":
+        rec, code = D // 2 + D // 32, ops.PSK_REC_MXFP4
+    else:
+        rec, code = D + 4, ops.PSK_REC_FP8_INDEXER
+    geom = synthetic.CacheGeom(pages, bs, (bs * rec + 15) // 16 * 16)
+    host = synthetic.random_cache_bytes(23, geom)
+    if record == "fp8_indexer":  # finite binary32 row scales
+        sc = rng.integers(0, 1 << 32, size=(pages, bs), dtype=np.uint64).astype(np.uint32)
+        sc[((sc >> 23) & 0xFF) == 0xFF] &= ~np.uint32(0x40000000)
+        host[:, bs * D: bs * D + 4 * bs] = sc.view(np.uint8).reshape(pages, 4 * bs)
+    R, Cc = 13, 9
+    idx = rng.integers(-1, pages * bs, size=(R, Cc)).astype(np.int32)
+    # shift 8: rows of D values from element 8 (16 bytes past a 32-byte boundary);
+    # shift 72: a row stride of D + 72 values ((2 D + 144) bytes, 16- but not 32-aligned)
+    stride_j = D if shift == 8 else D + shift
+    base = torch.full((R * Cc * stride_j + 64,), 7, dtype=torch.bfloat16, device=cuda_device)
+    off = 8 if shift == 8 else 0
+    out = base[off:off + R * Cc * stride_j].view(R, Cc, stride_j)[:, :, :D]
+    assert (out.data_ptr() % 32 != 0) or ((stride_j * 2) % 32 != 0)
+    ops.dequantize_and_gather_k_cache(out, torch.from_numpy(host).to(cuda_device),
+                                      _dev_i32(idx, cuda_device), bs, rope_dim=rope, record=code)
+    want = oracle.dequantize_and_gather_k_cache(host, bs, code, D, rope, idx)
+    _assert_same(_u16(out), want, f"16-byte-aligned output, {record}, shift {shift}")
+    seven = np.uint16(torch.tensor(7.0, dtype=torch.bfloat16).view(torch.int16).item())
+    flat = _u16(base)
+    mask = np.ones(flat.size, bool)
+    for t in range(R):
+        for j in range(Cc):
+            st = off + (t * Cc + j) * stride_j
+            mask[st:st + D] = False
+    assert np.all(flat[mask] == seven), "bytes outside the rows were written"
+
+
 @pytest.mark.parametrize("ue8m0", [True, False])
 def test_fp8_gather_every_scale(cuda_device, ue8m0):
     """Every scale a record can hold: UE8M0 bytes cycling through 0..254 (127,
