@@ -10,6 +10,9 @@ compressor-state writer and the window-pooling insert.
   normalises to exactly 1, the overlap window takes the first kv slice from the
   older positions and the second from the newer ones, a dominant score selects
   its row, absent pages drop out, and the emission rule / counted skips.
+* The RMSNorm reading (binary32 square root, then a binary32 division) on a
+  pooled row whose factor differs in the last bit from a correctly rounded
+  reciprocal square root, with a weight that turns that bit into a bf16 code.
   Expected records are built through the FP8 insert of a hand-written bf16
   row (the insert is pinned on its own).
 """
@@ -155,6 +158,41 @@ def test_compress_dominant_score_and_absent_pages(oracle_mod):
     y = (v * r).astype(np.float32)
     want = _record(oracle_mod, y, y[D - R64:])
     assert kv_cache[0].tolist() == want.tolist()
+
+
+def test_compress_rsqrt_reading(oracle_mod):
+    """The pooled row's RMSNorm factor is RN(1 / RN(sqrt(v + eps))), not a
+    correctly rounded reciprocal square root.  HCA window 0..127, equal scores
+    (weights 1/128, exact), every row c = (3, 3, 3, 3, 1, ..., 1): the pooled row
+    is c exactly, its sum of squares 544, v = 1.0625, eps = 2^-7, v + eps =
+    137/128.  The binary32 reading gives r = 0x3F7772CA, one rounded step gives
+    0x3F7772CB.  Weight 0x3F8006D5 on the first RoPE dim (identity row) makes
+    RN(r * w) = 0x3F777FFF under the first, which rounds to the bfloat16
+    0x3F77, and exactly the bfloat16 midpoint 0x3F778000 under the second,
+    whose tie goes to the even 0x3F78."""
+    rA, rB = (np.array([b], np.uint32).view(np.float32)[0] for b in (0x3F7772CA, 0x3F7772CB))
+    w_t = np.array([0x3F8006D5], np.uint32).view(np.float32)[0]
+    assert np.float32(1.0) / np.sqrt(np.float32(137.0 / 128.0)) == rA
+    assert np.float32(1.0 / np.sqrt(137.0 / 128.0)) == rB
+    c = np.ones(D, np.float32)
+    c[:4] = 3.0
+    w = np.ones(D, np.float32)
+    w[D - R64] = w_t
+    st, table, bs = _setup(128, False, 127, D, lambda p: np.concatenate([c, np.zeros(D)]))
+    kv_cache = np.zeros((1, 584), np.uint8)
+    n = oracle_mod.compress_kv_cache_insert(
+        st, np.array([0], np.int32), np.array([127], np.int64), np.array([127], np.int64),
+        table, bs, w, 2.0 ** -7, _cos_sin(128), kv_cache, np.array([0], np.int64), 1, 128,
+        False)
+    assert n == 0
+    rope = kv_cache[0, D - R64:D + R64].view(np.uint16)  # bf16 tail after the 448 FP8 bytes
+    assert rope[0] == 0x3F77  # 0x3F78 under a correctly rounded rsqrt
+    records = {}
+    for tag, r in (("binary32", rA), ("rounded once", rB)):
+        y = ((c * r).astype(np.float32) * w).astype(np.float32)
+        records[tag] = _record(oracle_mod, y, y[D - R64:])
+    assert kv_cache[0].tolist() == records["binary32"].tolist()
+    assert records["binary32"].tolist() != records["rounded once"].tolist()
 
 
 def test_compress_emission_and_skips(oracle_mod):

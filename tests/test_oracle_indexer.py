@@ -10,6 +10,9 @@ and reader) and indexer_k_norm_rope_store.
   (e, o) to (-o, e), and the quantised bytes of those values are worked by
   hand; the emission rule (slot >= 0 and a group boundary) and the RoPE row
   (the group's first position) are checked by which rows change.
+* The RMSNorm reading (binary32 square root, then a binary32 division) against
+  a correctly rounded reciprocal square root, on a row whose factor differs in
+  the last bit between the two and a weight that turns that bit into a code.
 """
 import json
 import os
@@ -171,6 +174,45 @@ def test_norm_rope_store_weight_and_eps(oracle_mod):
                                          np.array([1], np.int64), 1, REC_FP8_INDEXER, cache, bs)
     vals, scl = _read_fp8(cache, 1, bs)
     assert vals == [0x78] * 128 and scl == [0, 0, 0, 0x3C]
+
+
+def _f32(bits):
+    return np.array([bits], np.uint32).view(np.float32)[0]
+
+
+def test_norm_rope_store_rsqrt_reading(oracle_mod):
+    """The RMSNorm factor is a binary32 square root followed by a binary32
+    division, r = RN(1 / RN(sqrt(v + eps))), and not a correctly rounded
+    reciprocal square root.  x = (3, 1, ..., 1), eps = 2^-7: the sum of squares
+    is 136, v = 1.0625 and v + eps = 137/128, all exact.  RN(sqrt(137/128)) =
+    1.03455913066864..., and 1 over it is 0.96659530649..., which rounds down
+    to 0x3F7772CA (0.96659529209...); 1 / sqrt(137/128) = 0.96659534932... lies
+    above the midpoint 0.96659532189... of the two and rounds up to 0x3F7772CB.
+    Weight 0x3F80490B on dim 1 makes y_1 = RN(r * w_1) one binary32 step below
+    31/32 under the first reading and exactly 31/32 under the second.  The row's
+    amax is RN(3 r) = 2.89978..., so the FP8 scale is 2^-7 and 31/32 is 124
+    scale units, the midpoint of the codes 120 (0x6F) and 128 (0x70): the first
+    reading stores 0x6F and the second, its tie going to the even code, 0x70.
+    Dim 0 stores 384 (0x7C, 371.17 units), every other dim 120 (0x6F, 123.70)."""
+    rA, rB = _f32(0x3F7772CA), _f32(0x3F7772CB)
+    s = np.float32(137.0 / 128.0)
+    assert np.float32(1.0) / np.sqrt(s) == rA  # the binary32 reading (numpy: IEEE ops)
+    assert np.float32(1.0 / np.sqrt(np.float64(s))) == rB  # rounded once
+    w1 = _f32(0x3F80490B)
+    assert np.float32(rA * w1) < np.float32(31 / 32) == np.float32(rB * w1)
+    bs = 2
+    x = np.ones((1, 128), np.float32)
+    x[0, 0] = 3.0
+    w = np.ones(128, np.float32)
+    w[1] = w1
+    cache = np.zeros((1, bs * 132), np.uint8)
+    n = oracle_mod.indexer_k_norm_rope_store(_bf16(x), np.array([0], np.int64), _cos_sin(4), w,
+                                             2.0 ** -7, np.array([1], np.int64), 1,
+                                             REC_FP8_INDEXER, cache, bs)
+    assert n == 0
+    vals, scl = _read_fp8(cache, 1, bs)
+    assert vals == [0x7C] + [0x6F] * 127  # a correctly rounded rsqrt stores 0x70 at dim 1
+    assert scl == [0, 0, 0, 0x3C]
 
 
 def test_norm_rope_store_emission_and_rope_row(oracle_mod):

@@ -97,6 +97,43 @@ def test_compress_fuzz(cuda_device, ratio, overlap, bs_state, kv_bs):
     assert int(err.item()) == n and n >= 1
 
 
+@pytest.mark.parametrize("ratio,overlap", [(4, True), (128, False)])
+def test_compress_rsqrt_reading(cuda_device, ratio, overlap):
+    """The pooled row on which a binary32 square root followed by a division and
+    a correctly rounded reciprocal square root round the first RoPE dim to
+    different bfloat16 values (every state row c = (3, 3, 3, 3, 1, ..., 1),
+    equal scores, eps = 2^-7, v + eps = 137/128, weight 0x3F8006D5 there): the
+    kernel stores the oracle's bytes, bfloat16 0x3F77, for the short-window
+    kernel (window 8) and the clustered one (window 128)."""
+    d, D, bs = cuda_device, 512, 8
+    sw = (2 if overlap else 1) * D
+    pos = 2 * ratio - 1 if overlap else ratio - 1
+    c = np.ones(D, np.float32)
+    c[:4] = 3.0
+    npages = (pos + bs) // bs + 1
+    state = np.zeros((npages, bs, 2 * sw), np.float32)
+    state[:, :, :sw] = np.tile(c, sw // D)
+    table = np.arange(npages, dtype=np.int32)[None, :]
+    w = np.ones(D, np.float32)
+    w[D - 64] = np.array([0x3F8006D5], np.uint32).view(np.float32)[0]
+    cs = np.zeros((pos + 1, 64), np.float32)
+    cs[:, :32] = 1.0
+    t2r, p64 = np.zeros(1, np.int32), np.array([pos], np.int64)
+    kv_slots = np.array([0], np.int64)
+    host = np.zeros((1, 592), np.uint8)
+    dev_cache = _t(host, d)
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    ops.compress_kv_cache_insert(_t(state, d), _t(t2r, d), _t(p64, d), _t(p64, d), _t(table, d),
+                                 bs, _t(w, d), 2.0 ** -7, _t(cs, d), dev_cache, _t(kv_slots, d),
+                                 1, ratio, overlap=overlap, err_count=err)
+    n = oracle.compress_kv_cache_insert(state, t2r, p64, p64, table, bs, w, 2.0 ** -7, cs, host,
+                                        kv_slots, 1, ratio, overlap)
+    got = dev_cache.cpu().numpy()
+    _assert_same(got, host, f"compress rsqrt reading row, ratio={ratio}")
+    assert int(err.item()) == n == 0
+    assert got[0, D - 64:D - 62].view(np.uint16)[0] == 0x3F77
+
+
 @pytest.mark.parametrize("mode", ["serial", "concurrent"])
 def test_compressor_step_matches_oracle(cuda_device, mode):
     """The compressor step of the prefill batch (16384 tokens) for the ratio-4

@@ -193,6 +193,34 @@ def test_norm_rope_store_overflowing_weights(cuda_device, fp4):
     _assert_same(got, want, f"norm rope store, overflowing weights, fp4={fp4}")
 
 
+def test_norm_rope_store_rsqrt_reading(cuda_device):
+    """The row on which a binary32 square root followed by a division and a
+    correctly rounded reciprocal square root store different FP8 codes
+    (x = (3, 1, ..., 1), eps = 2^-7, v + eps = 137/128, weight 0x3F80490B on
+    dim 1): the kernel stores the oracle's bytes, code 0x6F at dim 1."""
+    d, bs = cuda_device, 2
+    x = np.ones((1, 128), np.float32)
+    x[0, 0] = 3.0
+    k = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    w = np.ones(128, np.float32)
+    w[1] = np.array([0x3F80490B], np.uint32).view(np.float32)[0]
+    cs = np.zeros((4, 64), np.float32)
+    cs[:, :32] = 1.0
+    pos, slots = np.array([0], np.int64), np.array([1], np.int64)
+    for fp4 in (False, True):
+        host = np.zeros((1, bs * (68 if fp4 else 132)), np.uint8)
+        dev_cache = torch.from_numpy(host).to(d)
+        ops.indexer_k_norm_rope_store(_bf16_dev(k, d), _i64(pos, d), torch.from_numpy(cs).to(d),
+                                      torch.from_numpy(w).to(d), 2.0 ** -7, dev_cache,
+                                      _i64(slots, d), 1, fp4, bs)
+        oracle.indexer_k_norm_rope_store(k, pos, cs, w, 2.0 ** -7, slots, 1, 1 if fp4 else 2,
+                                         host, bs)
+        got = dev_cache.cpu().numpy()
+        _assert_same(got, host, f"norm rope store, rsqrt reading row, fp4={fp4}")
+        if not fp4:
+            assert got[0, 128:131].tolist() == [0x7C, 0x6F, 0x6F]
+
+
 def test_norm_rope_store_prefill_size(cuda_device):
     """The prefill batch's 16384 tokens at ratio 4 (a key per 4 tokens) into the
     MXFP4 and FP8 indexer caches, strided k_pre and a padded cos_sin table."""
