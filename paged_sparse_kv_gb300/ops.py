@@ -61,6 +61,8 @@ def _pages(cache: torch.Tensor):
     _need(cache, torch.uint8, "cache")
     if cache.dim() < 2 or not cache[0].is_contiguous():
         raise ValueError("cache must be [num_pages, ...] uint8 with contiguous pages")
+    if cache.shape[0] == 1:  # a size-1 dim may carry any stride (0 from broadcasting)
+        return 1, max(cache.stride(0), cache[0].numel())
     return cache.shape[0], cache.stride(0)
 
 
@@ -71,6 +73,8 @@ def _rows(t: torch.Tensor, name: str):
         return t.shape[1]
     if t.stride(1) != 1 and t.shape[1] > 1:
         raise ValueError(f"{name} must have unit inner stride")
+    if t.shape[0] == 1:  # a size-1 dim may carry any stride (0 from broadcasting)
+        return max(t.stride(0), t.shape[1])
     return t.stride(0)
 
 

@@ -198,7 +198,7 @@ def test_norm_rope_store_rsqrt_reading(cuda_device):
     correctly rounded reciprocal square root store different FP8 codes
     (x = (3, 1, ..., 1), eps = 2^-7, v + eps = 137/128, weight 0x3F80490B on
     dim 1): the kernel stores the oracle's bytes, code 0x6F at dim 1."""
-    d, bs = cuda_device, 2
+    d, bs = cuda_device, 4  # page strides of 528 and 272 bytes (multiples of 16)
     x = np.ones((1, 128), np.float32)
     x[0, 0] = 3.0
     k = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)

@@ -31,3 +31,20 @@ def test_rule_boundary():
     past = SimpleNamespace(**{**vars(at), "num_tokens": at.num_tokens + 1})
     assert Pipeline.small_batch(at) and Pipeline.default_path_for(at) == "fused"
     assert not Pipeline.small_batch(past) and Pipeline.default_path_for(past) == "index"
+
+
+def test_size_one_leading_dims_ignore_their_stride():
+    """A one-row table or one-page cache may carry any stride on its size-1
+    dim (numpy broadcasting gives 0); the binding passes the row's extent
+    instead, and keeps the stride of every other shape."""
+    import numpy as np
+    import torch
+    from paged_sparse_kv_gb300 import ops
+    table = torch.from_numpy(np.arange(6, dtype=np.int32)[None, :])
+    assert table.stride(0) == 0 and ops._rows(table, "table") == 6
+    wide = torch.zeros(1, 8, dtype=torch.int32)[:, :5]
+    assert ops._rows(wide, "table") == 8
+    assert ops._rows(torch.zeros(3, 8, dtype=torch.int32)[:, :5], "table") == 8
+    cache = torch.from_numpy(np.zeros(592, np.uint8)[None, :])
+    assert cache.stride(0) == 0 and ops._pages(cache) == (1, 592)
+    assert ops._pages(torch.zeros(4, 600, dtype=torch.uint8)[:, :592]) == (4, 600)
