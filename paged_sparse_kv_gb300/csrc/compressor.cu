@@ -149,127 +149,89 @@ __global__ void __launch_bounds__(kThreads) save_state_kernel(SaveStateParams p)
 // ---- compressed rows ------------------------------------------------------------------
 //
 // Windows of at most 8 rows (CSA: ratio 4, overlapping): one CTA of 128
-// threads per token, four columns per thread, the whole window loaded into
-// registers in one round trip.  Every column's softmax is computed by one
-// thread in window order, so the split of columns does not change any result.
-// The normalised row goes through shared memory to the epilogue: 128 threads,
-// four dims each (RoPE on the tail, bf16, the fp8_ds_mla record).  Longer
-// windows take the cluster kernel further below.
+// threads per 32-token chunk, four columns per thread.  After the chunk's scan
+// every writing token's window rows are resolved in one round of table
+// look-ups; each token's window then reaches the threads through a per-thread
+// shared-memory buffer filled by cp.async, so the next token's copies are in
+// flight while the current token computes: its scores as soon as the current
+// scores have been read, its kv as soon as the current kv have.  Every
+// column's softmax is computed by one thread in window order, so neither the
+// split of columns nor the pipelining changes any result.  The normalised row
+// goes through shared memory to the epilogue: 128 threads, four dims each
+// (RoPE on the tail, bf16, the fp8_ds_mla record).  Longer windows take the
+// cluster kernel further below.
 constexpr int kMaxWindow = 256;
 constexpr int kHead = 512;
 constexpr int kRope = 64;
 constexpr int kNope = kHead - kRope;
+constexpr int kWinRows = 8;  // rows of a short window
 
-// Score / kv float4 (or float) of column group `col` of window row j.
-template <int CPT>
-__device__ __forceinline__ void load_slice(const CompressParams& p, int64_t row, int j, int col,
-                                           float (&s)[CPT], float (&k)[CPT], bool want_kv) {
-    const int off = (p.overlap && j >= p.ratio) ? kHead : 0;
-    if (row < 0) {
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's committed copy groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// State row of window row j of a writing token (request r, position pos), or
+// -1: a negative position, a logical page outside the table row, a missing
+// page or a row beyond the state cache.
+__device__ __forceinline__ int64_t window_state_row(const CompressParams& p, int32_t r, int64_t pos,
+                                                    int window, int j) {
+    const int64_t ps = pos - window + 1 + j;
+    if (ps < 0) return -1;
+    const int64_t base = p.base ? __ldg(p.base + r) : 0;
+    const int64_t lp = ps / p.state_bs - base;
+    if (lp < 0 || lp >= p.bt_width) return -1;
+    const int32_t entry = __ldg(p.bt + (int64_t)r * p.bt_stride + lp);
+    if (entry < 0) return -1;
+    const int64_t sr = (int64_t)entry * p.state_bs + ps % p.state_bs;
+    return sr < p.state_pages * (int64_t)p.state_bs ? sr : -1;
+}
+
+// Issues this thread's copies of one half of a token's window (its four
+// columns of every present row: the scores, or the kv) into its own buffer
+// slots: buf[(2 j + half) * THREADS + tid].  The slots hold the previous
+// token's values of this thread; `after` is a value computed from all of them,
+// and the copies' addresses are made to depend on it, so the copies are issued
+// (in program order, hence after those values were read) only once it exists.
+template <int THREADS>
+__device__ __forceinline__ void prefetch_window(const CompressParams& p, const int64_t* rows,
+                                                int window, int half, float4* buf, float after) {
+    const int tid = threadIdx.x;
+    const float* state = p.state;
+    asm volatile("" : "+l"(state) : "f"(after));
 #pragma unroll
-        for (int e = 0; e < CPT; ++e) {
-            s[e] = -1.0e30f;
-            k[e] = 0.0f;
-        }
-        return;
-    }
-    const float* rp = p.state + row * 2 * (int64_t)p.state_width + off + col;
-    if constexpr (CPT == 4) {
-        const float4 s4 = __ldg(reinterpret_cast<const float4*>(rp + p.state_width));
-        s[0] = s4.x; s[1] = s4.y; s[2] = s4.z; s[3] = s4.w;
-        if (want_kv) {
-            const float4 k4 = __ldg(reinterpret_cast<const float4*>(rp));
-            k[0] = k4.x; k[1] = k4.y; k[2] = k4.z; k[3] = k4.w;
-        }
-    } else {
-        s[0] = __ldg(rp + p.state_width);
-        if (want_kv) k[0] = __ldg(rp);
+    for (int j = 0; j < kWinRows; ++j) {
+        if (j >= window || rows[j] < 0) continue;
+        const int off = (p.overlap && j >= p.ratio) ? kHead : 0;
+        const float* rp = state + rows[j] * 2 * (int64_t)p.state_width + off + 4 * tid +
+                          (half == 0 ? p.state_width : 0);
+        cp_async16(buf + (2 * j + half) * THREADS + tid, rp);
     }
 }
 
-// One token's compressed row (the whole CTA; every thread calls it).
+// The RMSNorm, RoPE and record of one pooled row (acc: this thread's four
+// columns); every thread of the CTA calls it.
 template <int THREADS>
-__device__ __forceinline__ void compress_token(const CompressParams& p, int32_t kv_shift, int64_t t,
-                                               int64_t* s_row, float* s_part, float* s_y) {
-    constexpr int CPT = kHead / THREADS;  // columns per thread
-    static_assert(CPT % 2 == 0, "the exps are evaluated in column pairs");
+__device__ __forceinline__ void finish_token(const CompressParams& p, int32_t kv_shift, int64_t ks,
+                                             int64_t prow, const float (&acc)[4], float* s_part,
+                                             float* s_y) {
+    constexpr int CPT = 4;
     constexpr int NW = THREADS / kWarp;
-    constexpr int WREG = 8;               // window rows held in registers
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t ks = __ldg(p.kv_slots + t);
-    const int64_t pos = __ldg(p.positions + t);
-    int64_t grp = pos / p.ratio;
-    if (pos % p.ratio != 0 && pos < 0) grp -= 1;
-    const int64_t prow = grp * p.ratio;
-    const int32_t r = __ldg(p.t2r + t);
-    const int window = (p.overlap ? 2 : 1) * p.ratio;
-    const int64_t state_cap = p.state_pages * (int64_t)p.state_bs;
-    const int64_t base = p.base ? __ldg(p.base + r) : 0;
-    for (int j = tid; j < window; j += THREADS) {
-        const int64_t ps = pos - window + 1 + j;
-        int64_t row = -1;
-        if (ps >= 0) {
-            const int64_t lp = ps / p.state_bs - base;
-            if (lp >= 0 && lp < p.bt_width) {
-                const int32_t entry = __ldg(p.bt + (int64_t)r * p.bt_stride + lp);
-                if (entry >= 0) {
-                    const int64_t sr = (int64_t)entry * p.state_bs + ps % p.state_bs;
-                    if (sr < state_cap) row = sr;
-                }
-            }
-        }
-        s_row[j] = row;
-    }
-    __syncthreads();
-
     const int col = CPT * tid;
-    float mx[CPT], sum[CPT], acc[CPT];
-#pragma unroll
-    for (int e = 0; e < CPT; ++e) {
-        sum[e] = 0.0f;
-        acc[e] = 0.0f;
-    }
-    {
-        // the whole window (<= 8 rows) in registers: one round of loads
-        float sv[WREG][CPT], kv[WREG][CPT];
-#pragma unroll
-        for (int j = 0; j < WREG; ++j)
-            if (j < window) load_slice<CPT>(p, s_row[j], j, col, sv[j], kv[j], true);
-#pragma unroll
-        for (int e = 0; e < CPT; ++e) mx[e] = sv[0][e];
-#pragma unroll
-        for (int j = 1; j < WREG; ++j)
-            if (j < window)
-#pragma unroll
-                for (int e = 0; e < CPT; ++e) mx[e] = sv[j][e] > mx[e] ? sv[j][e] : mx[e];
-        float ex[WREG][CPT];
-#pragma unroll
-        for (int j = 0; j < WREG; ++j)
-            if (j < window) {
-#pragma unroll
-                for (int e = 0; e < CPT; e += 2)
-                    cw_exp2_nonpos(__fsub_rn(sv[j][e], mx[e]),
-                                   __fsub_rn(sv[j][e + 1], mx[e + 1]), ex[j][e], ex[j][e + 1]);
-#pragma unroll
-                for (int e = 0; e < CPT; ++e) sum[e] = __fadd_rn(sum[e], ex[j][e]);
-            }
-#pragma unroll
-        for (int j = 0; j < WREG; ++j)
-            if (j < window)
-#pragma unroll
-                for (int e = 0; e < CPT; ++e)
-                    acc[e] = __fadd_rn(acc[e], __fmul_rn(kv[j][e], __fdiv_rn(ex[j][e], sum[e])));
-    }
-
     // RMSNorm: pairwise sum of squares over the 512 columns -- in the thread
-    // (CPT = 4: (a + b) + (c + d)), across the warp's lanes, then a pairwise
-    // tree over the warps' partial sums
-    float ssq;
-    if constexpr (CPT == 4)
-        ssq = __fadd_rn(__fadd_rn(__fmul_rn(acc[0], acc[0]), __fmul_rn(acc[1], acc[1])),
-                        __fadd_rn(__fmul_rn(acc[2], acc[2]), __fmul_rn(acc[3], acc[3])));
-    else
-        ssq = __fmul_rn(acc[0], acc[0]);
+    // ((a + b) + (c + d)), across the warp's lanes, then a pairwise tree over
+    // the warps' partial sums
+    float ssq = __fadd_rn(__fadd_rn(__fmul_rn(acc[0], acc[0]), __fmul_rn(acc[1], acc[1])),
+                          __fadd_rn(__fmul_rn(acc[2], acc[2]), __fmul_rn(acc[3], acc[3])));
 #pragma unroll
     for (int m = 1; m < kWarp; m <<= 1) ssq = __fadd_rn(ssq, __shfl_xor_sync(0xFFFFFFFFu, ssq, m));
     if (lane == 0) s_part[warp] = ssq;
@@ -332,16 +294,23 @@ __device__ __forceinline__ void compress_token(const CompressParams& p, int32_t 
 // Persistent CTAs: each scans contiguous CHUNK-token chunks (warp 0: one
 // coalesced read of the chunk's slots and positions, a ballot of the tokens
 // that write, counted skips), lists the writing tokens in ascending order in
-// shared memory, and processes them one at a time with the whole CTA -- most
-// tokens of a batch do not close a group, so no CTA is spent on them.
+// shared memory with their requests, positions and record slots, resolves
+// every listed token's window rows, and pools the tokens one at a time with
+// the whole CTA -- most tokens of a batch do not close a group, so no CTA is
+// spent on them.
 template <int THREADS, int CHUNK>
-__global__ void __launch_bounds__(THREADS) compress_kernel(CompressParams p, int32_t kv_shift) {
-    __shared__ int64_t s_row[kMaxWindow];
+__global__ void __launch_bounds__(THREADS, 4) compress_kernel(CompressParams p, int32_t kv_shift) {
+    static_assert(THREADS * 4 == kHead, "four columns per thread");
+    constexpr int CPT = 4;
+    __shared__ __align__(16) float4 s_win[2 * kWinRows * THREADS];  // [row][scores | kv][thread]
+    __shared__ int64_t s_rows[CHUNK][kWinRows];
+    __shared__ int64_t s_tok[CHUNK], s_pos[CHUNK], s_ks[CHUNK], s_prow[CHUNK];
+    __shared__ int32_t s_req[CHUNK];
     __shared__ float s_part[THREADS / kWarp];
     __shared__ __align__(16) float s_y[kHead];
-    __shared__ int64_t s_list[kWarp];
     __shared__ int s_count;
     const int tid = threadIdx.x, lane = tid & 31;
+    const int window = (p.overlap ? 2 : 1) * p.ratio;
     pdl_wait();
     pdl_launch_dependents();
     for (int64_t c0 = (int64_t)blockIdx.x * CHUNK; c0 < p.num_tokens;
@@ -349,17 +318,20 @@ __global__ void __launch_bounds__(THREADS) compress_kernel(CompressParams p, int
         if (tid < kWarp) {
             const int64_t t = c0 + lane;
             bool emit = false;
+            int64_t pos = 0, ks = 0, prow = 0;
+            int32_t r = 0;
             if (lane < CHUNK && t < p.num_tokens) {
-                const int64_t ss = __ldg(p.state_slots + t), ks = __ldg(p.kv_slots + t);
-                const int64_t pos = __ldg(p.positions + t);
+                const int64_t ss = __ldg(p.state_slots + t);
+                ks = __ldg(p.kv_slots + t);
+                pos = __ldg(p.positions + t);
                 if (ss >= 0 && ks >= 0) {
                     int64_t rem = (pos + 1) % p.ratio;
                     if (rem < 0) rem += p.ratio;
                     if (rem == 0) {
                         int64_t grp = pos / p.ratio;
                         if (pos % p.ratio != 0 && pos < 0) grp -= 1;
-                        const int64_t prow = grp * p.ratio;
-                        const int32_t r = __ldg(p.t2r + t);
+                        prow = grp * p.ratio;
+                        r = __ldg(p.t2r + t);
                         if (ks >= p.kv_pages * (int64_t)p.kv_bs || prow < 0 || prow >= p.max_pos ||
                             r < 0 || r >= p.num_reqs) {
                             if (p.err_count) atomicAdd(p.err_count, 1);
@@ -370,16 +342,111 @@ __global__ void __launch_bounds__(THREADS) compress_kernel(CompressParams p, int
                 }
             }
             const unsigned mask = __ballot_sync(0xFFFFFFFFu, emit);
-            if (emit) s_list[__popc(mask & ((1u << lane) - 1u))] = t;
+            if (emit) {
+                const int k = __popc(mask & ((1u << lane) - 1u));
+                s_tok[k] = t;
+                s_pos[k] = pos;
+                s_ks[k] = ks;
+                s_prow[k] = prow;
+                s_req[k] = r;
+            }
             if (lane == 0) s_count = __popc(mask);
         }
         __syncthreads();
         const int n = s_count;
+        // every listed token's window rows: one round of table look-ups
+        for (int k = tid; k < n * window; k += THREADS) {
+            const int i = k / window, j = k - i * window;
+            s_rows[i][j] = window_state_row(p, s_req[i], s_pos[i], window, j);
+        }
+        __syncthreads();
+        if (n > 0) {
+            prefetch_window<THREADS>(p, s_rows[0], window, 0, s_win, 0.0f);
+            cp_async_commit();
+            prefetch_window<THREADS>(p, s_rows[0], window, 1, s_win, 0.0f);
+            cp_async_commit();
+        }
         for (int i = 0; i < n; ++i) {
-            compress_token<THREADS>(p, kv_shift, s_list[i], s_row, s_part, s_y);
+            const bool more = i + 1 < n;
+            float mx[CPT], sum[CPT], acc[CPT];
+#pragma unroll
+            for (int e = 0; e < CPT; ++e) {
+                sum[e] = 0.0f;
+                acc[e] = 0.0f;
+            }
+            float ex[kWinRows][CPT];
+            {
+                // scores: the token's score copies have landed (its kv copies may not)
+                cp_async_wait<1>();
+                float sv[kWinRows][CPT];
+#pragma unroll
+                for (int j = 0; j < kWinRows; ++j) {
+                    if (j >= window) continue;
+                    if (s_rows[i][j] < 0) {
+#pragma unroll
+                        for (int e = 0; e < CPT; ++e) sv[j][e] = -1.0e30f;
+                    } else {
+                        const float4 v = s_win[(2 * j) * THREADS + tid];
+                        sv[j][0] = v.x; sv[j][1] = v.y; sv[j][2] = v.z; sv[j][3] = v.w;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < CPT; ++e) mx[e] = sv[0][e];
+#pragma unroll
+                for (int j = 1; j < kWinRows; ++j)
+                    if (j < window)
+#pragma unroll
+                        for (int e = 0; e < CPT; ++e) mx[e] = sv[j][e] > mx[e] ? sv[j][e] : mx[e];
+#pragma unroll
+                for (int j = 0; j < kWinRows; ++j)
+                    if (j < window) {
+#pragma unroll
+                        for (int e = 0; e < CPT; e += 2)
+                            cw_exp2_nonpos(__fsub_rn(sv[j][e], mx[e]),
+                                           __fsub_rn(sv[j][e + 1], mx[e + 1]), ex[j][e],
+                                           ex[j][e + 1]);
+#pragma unroll
+                        for (int e = 0; e < CPT; ++e) sum[e] = __fadd_rn(sum[e], ex[j][e]);
+                    }
+            }
+            // the scores have been read (the exps depend on them): the next
+            // token's scores may overwrite them
+            if (more)
+                prefetch_window<THREADS>(p, s_rows[i + 1], window, 0, s_win,
+                                         __fadd_rn(__fadd_rn(sum[0], sum[1]), __fadd_rn(sum[2], sum[3])));
+            cp_async_commit();
+            // kv: every group but the one just committed has landed
+            cp_async_wait<1>();
+            {
+                float kv[kWinRows][CPT];
+#pragma unroll
+                for (int j = 0; j < kWinRows; ++j) {
+                    if (j >= window) continue;
+                    if (s_rows[i][j] < 0) {
+#pragma unroll
+                        for (int e = 0; e < CPT; ++e) kv[j][e] = 0.0f;
+                    } else {
+                        const float4 v = s_win[(2 * j + 1) * THREADS + tid];
+                        kv[j][0] = v.x; kv[j][1] = v.y; kv[j][2] = v.z; kv[j][3] = v.w;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kWinRows; ++j)
+                    if (j < window)
+#pragma unroll
+                        for (int e = 0; e < CPT; ++e)
+                            acc[e] = __fadd_rn(acc[e], __fmul_rn(kv[j][e], __fdiv_rn(ex[j][e], sum[e])));
+            }
+            // the kv have been read: the next token's kv may overwrite them
+            if (more)
+                prefetch_window<THREADS>(p, s_rows[i + 1], window, 1, s_win,
+                                         __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3])));
+            cp_async_commit();
+            finish_token<THREADS>(p, kv_shift, s_ks[i], s_prow[i], acc, s_part, s_y);
             __syncthreads();
         }
-        __syncthreads();  // every thread has read s_count / s_list before the next scan
+        cp_async_wait<0>();
+        __syncthreads();  // every thread has read the chunk's lists before the next scan
     }
 }
 
