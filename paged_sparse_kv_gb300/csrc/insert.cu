@@ -342,35 +342,67 @@ fp8_indexer_insert_kernel(const uint16_t* __restrict__ k, int64_t k_row_stride,
 // ---- indexer_k_norm_rope_store ---------------------------------------------------------
 //
 // vLLM deepseek_v41 ops, indexer_k_norm_rope_store: k_norm -> RoPE -> quant ->
-// paged store of 128-dim indexer keys.  Eight lanes per key, four keys per
-// warp; lane g holds the chunk A = dims [8g, 8g + 8) of the un-rotated half
-// and the chunk B = dims [64 + 8g, 64 + 8g + 8) of the RoPE half, so every
-// lane rotates four pairs.
+// paged store of 128-dim indexer keys.  Four lanes per key, eight keys per
+// warp; lane g holds the chunk A = dims [16g, 16g + 16) of the un-rotated half
+// and the chunk B = dims [64 + 16g, 64 + 16g + 16) of the RoPE half, so every
+// lane rotates eight pairs.  The multiplies run on packed binary32 pairs
+// (mul.rn.f32x2: each half the scalar IEEE product), with the pairs chosen so
+// that a packed multiply does the same operation on two elements; a sum or
+// difference of two products is a scalar add.rn / sub.rn, which the compiler
+// never fuses with the products (a packed add after packed products may be
+// contracted into a fused multiply-add, which rounds once less).
 //  * Emission: slot >= 0 and the token closes its compress group,
 //    (pos + 1) % ratio == 0 (TokenSpeed _compress_v4_state_windows_capturable's
 //    valid_token rule); other rows are not read (except that with ratio 1,
 //    where every row with a slot writes, the row is loaded with the slot).
 //  * RMSNorm in binary32, every operation rounded once (no contraction): the
 //    sum of squares is a pairwise sum (recursive halving of the index range):
-//    each half of the row is a tree over its eight 8-dim chunks -- a 3-level
-//    tree in the lane, then xor-shuffles over 1, 2, 4 lanes -- and the sum is
-//    the two halves' sum.  variance = sum * 2^-7 (= sum / 128 exactly);
-//    r = 1 / sqrt(variance + eps) as an IEEE binary32 square root then an IEEE
-//    reciprocal (= the IEEE quotient 1 / s); y = (x * r) * weight.
+//    each half of the row is a tree over its four 16-dim chunks -- a 4-level
+//    tree in the lane (the two halves side by side in one packed pair), then
+//    xor-shuffles over 1 and 2 lanes -- and the sum is the two halves' sum.
+//    variance = sum * 2^-7 (= sum / 128 exactly); r = 1 / sqrt(variance + eps)
+//    as an IEEE binary32 square root then an IEEE reciprocal (= the IEEE
+//    quotient 1 / s); y = (x * r) * weight.
 //  * GPT-J RoPE (TokenSpeed _apply_gptj_rope_tail_rows) on chunk B at the
 //    cos_sin row of the group's first position floor(pos / ratio) * ratio.
-//  * MXFP4 record (a 32-block is one chunk of four lanes) or FP8 indexer record
+//  * MXFP4 record (a 32-block is one chunk of two lanes) or FP8 indexer record
 //    (row amax), with the inserts' rules; the scale exponents are read off the
 //    binary32 amax without dividing (exact for any normal binary32 amax, as
 //    for bf16: see ceil_log2_div_const).
 // Keys of a warp that do not write still take part in every shuffle.
+constexpr int kKeyLanes = 4;
+
+__device__ __forceinline__ float2 f2_op_mul(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "mul.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 f2_op_add(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "add.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
 // One key's state between the stages of the kernel below.
 struct NormRopeKey {
     bool act;
     int64_t sl, pos, prow;
-    uint4 ka, kb;     // chunks A and B of the bf16 row
-    float c4[4], s4[4];
+    uint4 ka0, ka1, kb0, kb1;  // chunks A and B of the bf16 row
+    float4 c0, c1, s0, s1;     // cos and sin of chunk B's eight pairs
 };
+
+__device__ __forceinline__ void nrs_load_row(const NormRopeParams& p, int64_t t, int gl,
+                                             NormRopeKey& k) {
+    const uint16_t* row = p.k + t * p.k_row_stride + 16 * gl;
+    k.ka0 = ld_stream_v4(row);
+    k.ka1 = ld_stream_v4(row + 8);
+    k.kb0 = ld_stream_v4(row + 64);
+    k.kb1 = ld_stream_v4(row + 72);
+}
 
 // Round trip 1: the slot and the position; with ratio 1 (EVERY_ROW: every row
 // with a slot writes) the key row too.
@@ -380,20 +412,16 @@ __device__ __forceinline__ void nrs_load(const NormRopeParams& p, int64_t t, int
     k.act = t < p.num_tokens;
     k.sl = -1;
     k.pos = k.prow = 0;
-    k.ka = k.kb = make_uint4(0u, 0u, 0u, 0u);
+    k.ka0 = k.ka1 = k.kb0 = k.kb1 = make_uint4(0u, 0u, 0u, 0u);
     if (k.act) {
         k.sl = __ldg(p.slots + t);
         k.pos = __ldg(p.positions + t);
-        if (EVERY_ROW) {
-            const uint16_t* row = p.k + t * p.k_row_stride + 8 * gl;
-            k.ka = ld_stream_v4(row);
-            k.kb = ld_stream_v4(row + 64);
-        }
+        if (EVERY_ROW) nrs_load_row(p, t, gl, k);
     }
 }
 
 // The emission rule and range checks, then round trip 2: the key row (unless
-// already loaded) and chunk B's four cos and four sin values.
+// already loaded) and chunk B's eight cos and eight sin values.
 template <bool EVERY_ROW, bool CS_VEC>
 __device__ __forceinline__ void nrs_resolve(const NormRopeParams& p, int64_t t, int gl,
                                             NormRopeKey& k) {
@@ -427,29 +455,21 @@ __device__ __forceinline__ void nrs_resolve(const NormRopeParams& p, int64_t t, 
             k.act = false;
         }
     }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        k.c4[j] = 1.0f;
-        k.s4[j] = 0.0f;
-    }
+    k.c0 = k.c1 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+    k.s0 = k.s1 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (k.act) {
-        if (!EVERY_ROW) {
-            const uint16_t* row = p.k + t * p.k_row_stride + 8 * gl;
-            k.ka = ld_stream_v4(row);
-            k.kb = ld_stream_v4(row + 64);
-        }
-        const float* cs = p.cos_sin + k.prow * p.cs_stride + 4 * gl;
+        if (!EVERY_ROW) nrs_load_row(p, t, gl, k);
+        const float* cs = p.cos_sin + k.prow * p.cs_stride + 8 * gl;
         if (CS_VEC) {
-            const float4 cv = __ldg(reinterpret_cast<const float4*>(cs));
-            const float4 sv = __ldg(reinterpret_cast<const float4*>(cs + 32));
-            k.c4[0] = cv.x; k.c4[1] = cv.y; k.c4[2] = cv.z; k.c4[3] = cv.w;
-            k.s4[0] = sv.x; k.s4[1] = sv.y; k.s4[2] = sv.z; k.s4[3] = sv.w;
+            k.c0 = __ldg(reinterpret_cast<const float4*>(cs));
+            k.c1 = __ldg(reinterpret_cast<const float4*>(cs + 4));
+            k.s0 = __ldg(reinterpret_cast<const float4*>(cs + 32));
+            k.s1 = __ldg(reinterpret_cast<const float4*>(cs + 36));
         } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                k.c4[j] = __ldg(cs + j);
-                k.s4[j] = __ldg(cs + 32 + j);
-            }
+            k.c0 = make_float4(__ldg(cs), __ldg(cs + 1), __ldg(cs + 2), __ldg(cs + 3));
+            k.c1 = make_float4(__ldg(cs + 4), __ldg(cs + 5), __ldg(cs + 6), __ldg(cs + 7));
+            k.s0 = make_float4(__ldg(cs + 32), __ldg(cs + 33), __ldg(cs + 34), __ldg(cs + 35));
+            k.s1 = make_float4(__ldg(cs + 36), __ldg(cs + 37), __ldg(cs + 38), __ldg(cs + 39));
         }
     }
 }
@@ -459,92 +479,113 @@ __device__ __forceinline__ void nrs_resolve(const NormRopeParams& p, int64_t t, 
 template <bool FP4>
 __device__ __forceinline__ void nrs_compute_store(const NormRopeParams& p, int32_t shift, int gl,
                                                   const NormRopeKey& k) {
-    constexpr int LPT = 8;
     const bool act = k.act;
     // (an inactive key's values are whatever was loaded: its lanes reduce only
     // among themselves and store nothing)
-    float ya[8], yb[8];
-    {
-        const uint32_t wa[4] = {k.ka.x, k.ka.y, k.ka.z, k.ka.w};
-        const uint32_t wb[4] = {k.kb.x, k.kb.y, k.kb.z, k.kb.w};
+    const uint32_t wa[8] = {k.ka0.x, k.ka0.y, k.ka0.z, k.ka0.w, k.ka1.x, k.ka1.y, k.ka1.z, k.ka1.w};
+    const uint32_t wb[8] = {k.kb0.x, k.kb0.y, k.kb0.z, k.kb0.w, k.kb1.x, k.kb1.y, k.kb1.z, k.kb1.w};
+    // sum of squares: the pair (A dim i, B dim i) side by side, the 4-level
+    // pairwise tree of each chunk in the lane
+    float2 t1[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            ya[2 * i] = bf16_lo(wa[i]);
-            ya[2 * i + 1] = bf16_hi(wa[i]);
-            yb[2 * i] = bf16_lo(wb[i]);
-            yb[2 * i + 1] = bf16_hi(wb[i]);
+    for (int i = 0; i < 8; ++i) {
+        const float2 lo = make_float2(bf16_lo(wa[i]), bf16_lo(wb[i]));
+        const float2 hi = make_float2(bf16_hi(wa[i]), bf16_hi(wb[i]));
+        const float2 sl = f2_op_mul(lo, lo), sh = f2_op_mul(hi, hi);
+        t1[i] = make_float2(__fadd_rn(sl.x, sh.x), __fadd_rn(sl.y, sh.y));
+    }
+    const float2 t2[4] = {f2_op_add(t1[0], t1[1]), f2_op_add(t1[2], t1[3]),
+                          f2_op_add(t1[4], t1[5]), f2_op_add(t1[6], t1[7])};
+    float2 h = f2_op_add(f2_op_add(t2[0], t2[1]), f2_op_add(t2[2], t2[3]));
+    // over the half's four chunks (lanes)
+#pragma unroll
+    for (int m = 1; m < kKeyLanes; m <<= 1)
+        h = f2_op_add(h, make_float2(__shfl_xor_sync(0xFFFFFFFFu, h.x, m),
+                                     __shfl_xor_sync(0xFFFFFFFFu, h.y, m)));
+    const float variance = __fmul_rn(__fadd_rn(h.x, h.y), 0.0078125f);
+    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(variance, p.eps)));
+    const float2 r2 = make_float2(r, r);
+    const float4* wv = reinterpret_cast<const float4*>(p.weight) + 4 * gl;
+    // chunk A: y = (x r) w, in the pairs (2i, 2i + 1)
+    float2 ya[8];
+    {
+        const float4 w0 = __ldg(wv), w1 = __ldg(wv + 1), w2 = __ldg(wv + 2), w3 = __ldg(wv + 3);
+        const float2 w2p[8] = {make_float2(w0.x, w0.y), make_float2(w0.z, w0.w),
+                               make_float2(w1.x, w1.y), make_float2(w1.z, w1.w),
+                               make_float2(w2.x, w2.y), make_float2(w2.z, w2.w),
+                               make_float2(w3.x, w3.y), make_float2(w3.z, w3.w)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            ya[i] = f2_op_mul(f2_op_mul(make_float2(bf16_lo(wa[i]), bf16_hi(wa[i])), r2), w2p[i]);
+    }
+    // chunk B: pair j of the lane is (e_j, o_j) = dims (2j, 2j + 1) of the
+    // chunk; held as E = (e_2q, e_2q+1) and O = (o_2q, o_2q+1), q = 0..3
+    float2 e[4], o[4];
+    {
+        const float4 w0 = __ldg(wv + 16), w1 = __ldg(wv + 17), w2 = __ldg(wv + 18),
+                     w3 = __ldg(wv + 19);
+        const float wbv[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
+                               w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+        const float cs[8] = {k.c0.x, k.c0.y, k.c0.z, k.c0.w, k.c1.x, k.c1.y, k.c1.z, k.c1.w};
+        const float sn[8] = {k.s0.x, k.s0.y, k.s0.z, k.s0.w, k.s1.x, k.s1.y, k.s1.z, k.s1.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            // words 2q, 2q + 1 hold pairs 2q, 2q + 1: (e, o) as (lo, hi)
+            const float2 ex = make_float2(bf16_lo(wb[2 * q]), bf16_lo(wb[2 * q + 1]));
+            const float2 ox = make_float2(bf16_hi(wb[2 * q]), bf16_hi(wb[2 * q + 1]));
+            const float2 ey = f2_op_mul(f2_op_mul(ex, r2),
+                                        make_float2(wbv[4 * q], wbv[4 * q + 2]));
+            const float2 oy = f2_op_mul(f2_op_mul(ox, r2),
+                                        make_float2(wbv[4 * q + 1], wbv[4 * q + 3]));
+            const float2 c = make_float2(cs[2 * q], cs[2 * q + 1]);
+            const float2 s = make_float2(sn[2 * q], sn[2 * q + 1]);
+            const float2 ec = f2_op_mul(ey, c), os = f2_op_mul(oy, s);
+            const float2 es = f2_op_mul(ey, s), oc = f2_op_mul(oy, c);
+            e[q] = make_float2(__fsub_rn(ec.x, os.x), __fsub_rn(ec.y, os.y));
+            o[q] = make_float2(__fadd_rn(es.x, oc.x), __fadd_rn(es.y, oc.y));
         }
     }
-    // pairwise sum of squares of each chunk (8 -> 4 -> 2 -> 1), then over the
-    // half's eight chunks (lanes), then the two halves
-    float sa[4], sb[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        sa[i] = __fadd_rn(__fmul_rn(ya[2 * i], ya[2 * i]), __fmul_rn(ya[2 * i + 1], ya[2 * i + 1]));
-        sb[i] = __fadd_rn(__fmul_rn(yb[2 * i], yb[2 * i]), __fmul_rn(yb[2 * i + 1], yb[2 * i + 1]));
-    }
-    float ha = __fadd_rn(__fadd_rn(sa[0], sa[1]), __fadd_rn(sa[2], sa[3]));
-    float hb = __fadd_rn(__fadd_rn(sb[0], sb[1]), __fadd_rn(sb[2], sb[3]));
-#pragma unroll
-    for (int m = 1; m < LPT; m <<= 1) {
-        ha = __fadd_rn(ha, __shfl_xor_sync(0xFFFFFFFFu, ha, m));
-        hb = __fadd_rn(hb, __shfl_xor_sync(0xFFFFFFFFu, hb, m));
-    }
-    const float variance = __fmul_rn(__fadd_rn(ha, hb), 0.0078125f);
-    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(variance, p.eps)));
-    const float4* wv = reinterpret_cast<const float4*>(p.weight) + 2 * gl;
-    const float4 w0 = __ldg(wv), w1 = __ldg(wv + 1), w2 = __ldg(wv + 16), w3 = __ldg(wv + 17);
-    const float wa8[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    const float wb8[8] = {w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        ya[i] = __fmul_rn(__fmul_rn(ya[i], r), wa8[i]);
-        yb[i] = __fmul_rn(__fmul_rn(yb[i], r), wb8[i]);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float e = yb[2 * j], o = yb[2 * j + 1];
-        yb[2 * j] = __fsub_rn(__fmul_rn(e, k.c4[j]), __fmul_rn(o, k.s4[j]));
-        yb[2 * j + 1] = __fadd_rn(__fmul_rn(e, k.s4[j]), __fmul_rn(o, k.c4[j]));
-    }
-
     float aa = 0.0f, ab = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        aa = fmaxf(aa, fabsf(ya[i]));
-        ab = fmaxf(ab, fabsf(yb[i]));
-    }
+    for (int i = 0; i < 8; ++i) aa = fmaxf(aa, fmaxf(fabsf(ya[i].x), fabsf(ya[i].y)));
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        ab = fmaxf(ab, fmaxf(fmaxf(fabsf(e[q].x), fabsf(e[q].y)),
+                             fmaxf(fabsf(o[q].x), fabsf(o[q].y))));
     int64_t off = 0;
     uint8_t* base = p.cache;
     if (act) {
         const int64_t page = div_block(k.sl, p.block_size, shift, off);
         base = p.cache + page * p.page_stride;
     }
+    // byte / code order of chunk B: dims (2j, 2j + 1) = (e_j, o_j)
     if constexpr (FP4) {
-        // 32-blocks: chunk A of lanes 0-3 / 4-7 (blocks 0, 1), chunk B (blocks 2, 3)
-#pragma unroll
-        for (int m = 1; m < 4; m <<= 1) {
-            aa = fmaxf(aa, __shfl_xor_sync(0xFFFFFFFFu, aa, m));
-            ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, m));
-        }
+        // 32-blocks: chunk A of lanes 0-1 / 2-3 (blocks 0, 1), chunk B (blocks 2, 3)
+        aa = fmaxf(aa, __shfl_xor_sync(0xFFFFFFFFu, aa, 1));
+        ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 1));
         const int ea = ceil_log2_div_const(fmaxf(aa, 1.0e-4f), 0x400000u, 2);  // / 6
         const int eb = ceil_log2_div_const(fmaxf(ab, 1.0e-4f), 0x400000u, 2);
-        const uint64_t pa = splat_f32x2(exp2_int(-ea)), pb = splat_f32x2(exp2_int(-eb));
-        uint32_t qa = 0u, qb = 0u;
+        const float2 pa = make_float2(exp2_int(-ea), exp2_int(-ea));
+        const float2 pb = make_float2(exp2_int(-eb), exp2_int(-eb));
+        uint32_t qa[2] = {0u, 0u}, qb[2] = {0u, 0u};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float a0 = ya[2 * j], a1 = ya[2 * j + 1], b0 = yb[2 * j], b1 = yb[2 * j + 1];
-            mul2_rn(a0, a1, pa);
-            mul2_rn(b0, b1, pb);
-            qa |= (cvt_e2m1x2(a0, a1) & 0xFFu) << (8 * j);
-            qb |= (cvt_e2m1x2(b0, b1) & 0xFFu) << (8 * j);
+        for (int i = 0; i < 8; ++i) {
+            const float2 v = f2_op_mul(ya[i], pa);
+            qa[i / 4] |= (cvt_e2m1x2(v.x, v.y) & 0xFFu) << (8 * (i % 4));
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 ve = f2_op_mul(e[q], pb), vo = f2_op_mul(o[q], pb);
+            // pairs 2q and 2q + 1: bytes 2q, 2q + 1 of the chunk
+            const uint32_t b0 = cvt_e2m1x2(ve.x, vo.x) & 0xFFu, b1 = cvt_e2m1x2(ve.y, vo.y) & 0xFFu;
+            qb[q / 2] |= (b0 | (b1 << 8)) << (16 * (q % 2));
         }
         if (act) {
             uint8_t* vals = base + off * 64;
-            *reinterpret_cast<uint32_t*>(vals + 4 * gl) = qa;
-            *reinterpret_cast<uint32_t*>(vals + 32 + 4 * gl) = qb;
-            if ((gl & 3) == 0) {
-                uint8_t* scl = base + (int64_t)p.block_size * 64 + off * 4 + gl / 4;
+            *reinterpret_cast<uint2*>(vals + 8 * gl) = make_uint2(qa[0], qa[1]);
+            *reinterpret_cast<uint2*>(vals + 32 + 8 * gl) = make_uint2(qb[0], qb[1]);
+            if ((gl & 1) == 0) {
+                uint8_t* scl = base + (int64_t)p.block_size * 64 + off * 4 + gl / 2;
                 scl[0] = (uint8_t)min(max(ea + 127, 0), 254);
                 scl[2] = (uint8_t)min(max(eb + 127, 0), 254);
             }
@@ -552,45 +593,52 @@ __device__ __forceinline__ void nrs_compute_store(const NormRopeParams& p, int32
     } else {
         float a = fmaxf(aa, ab);
 #pragma unroll
-        for (int m = 1; m < LPT; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, m));
+        for (int m = 1; m < kKeyLanes; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, m));
         // max(a / 448, 1e-10) then ceil(log2): the floor's exponent is -33
-        const int e = max(ceil_log2_div_const(a, 0x600000u, 8), -33);
-        const uint64_t pw = splat_f32x2(inv_pow2_scale(e));  // codes e4m3(y / 2^e)
-        uint32_t qa[2], qb[2];
+        const int ex = max(ceil_log2_div_const(a, 0x600000u, 8), -33);
+        const float pwf = inv_pow2_scale(ex);  // codes e4m3(y / 2^e)
+        const float2 pw = make_float2(pwf, pwf);
+        uint32_t qa[4], qb[4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float a0 = ya[4 * h], a1 = ya[4 * h + 1], a2 = ya[4 * h + 2], a3 = ya[4 * h + 3];
-            float b0 = yb[4 * h], b1 = yb[4 * h + 1], b2 = yb[4 * h + 2], b3 = yb[4 * h + 3];
-            mul2_rn(a0, a1, pw);
-            mul2_rn(a2, a3, pw);
-            mul2_rn(b0, b1, pw);
-            mul2_rn(b2, b3, pw);
-            qa[h] = cvt_e4m3x2(a0, a1) | (cvt_e4m3x2(a2, a3) << 16);
-            qb[h] = cvt_e4m3x2(b0, b1) | (cvt_e4m3x2(b2, b3) << 16);
+        for (int i = 0; i < 4; ++i) {
+            const float2 v0 = f2_op_mul(ya[2 * i], pw), v1 = f2_op_mul(ya[2 * i + 1], pw);
+            qa[i] = cvt_e4m3x2(v0.x, v0.y) | (cvt_e4m3x2(v1.x, v1.y) << 16);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 ve = f2_op_mul(e[q], pw), vo = f2_op_mul(o[q], pw);
+            // dims 4q .. 4q + 3 of the chunk: e_2q, o_2q, e_2q+1, o_2q+1
+            qb[q] = cvt_e4m3x2(ve.x, vo.x) | (cvt_e4m3x2(ve.y, vo.y) << 16);
         }
         if (act) {
             uint8_t* vals = base + off * 128;
-            *reinterpret_cast<uint2*>(vals + 8 * gl) = make_uint2(qa[0], qa[1]);
-            *reinterpret_cast<uint2*>(vals + 64 + 8 * gl) = make_uint2(qb[0], qb[1]);
+            *reinterpret_cast<uint4*>(vals + 16 * gl) = make_uint4(qa[0], qa[1], qa[2], qa[3]);
+            *reinterpret_cast<uint4*>(vals + 64 + 16 * gl) = make_uint4(qb[0], qb[1], qb[2], qb[3]);
             if (gl == 0)
-                *reinterpret_cast<float*>(base + (int64_t)p.block_size * 128 + off * 4) = exp2_int(e);
+                *reinterpret_cast<float*>(base + (int64_t)p.block_size * 128 + off * 4) = exp2_int(ex);
         }
     }
 }
 
 #ifndef PSK_NORM_ROPE_UNROLL
-#define PSK_NORM_ROPE_UNROLL 2
+#define PSK_NORM_ROPE_UNROLL 1
 #endif
+// Resident CTAs per SM asked of the compiler.  On the 1,048,576-key store
+// (one key per group): four (64 registers, 16 bytes spilled) ran 100.4 us,
+// no request (78 registers, three CTAs) 104.5 us, one (104 registers) 131 us.
+#ifndef PSK_NORM_ROPE_MIN_CTAS
+#define PSK_NORM_ROPE_MIN_CTAS 4
+#endif
+#define PSK_NR_BOUNDS __launch_bounds__(kThreads, PSK_NORM_ROPE_MIN_CTAS)
 
-// U keys per 8-lane group: all of the keys' first-round loads are issued
+// U keys per 4-lane group: all of the keys' first-round loads are issued
 // before any is used, then all second-round loads, then the arithmetic.
 template <bool FP4, bool EVERY_ROW, bool CS_VEC, int U>
-__global__ void __launch_bounds__(kThreads) norm_rope_store_kernel(NormRopeParams p,
+__global__ void PSK_NR_BOUNDS norm_rope_store_kernel(NormRopeParams p,
                                                                    int32_t shift) {
-    constexpr int LPT = 8;  // lanes per key
-    const int gl = (threadIdx.x & 31) % LPT;
-    const int64_t g = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / LPT;
-    const int64_t ngroups = (int64_t)gridDim.x * kThreads / LPT;
+    const int gl = (threadIdx.x & 31) % kKeyLanes;
+    const int64_t g = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / kKeyLanes;
+    const int64_t ngroups = (int64_t)gridDim.x * kThreads / kKeyLanes;
     pdl_wait();
     pdl_launch_dependents();
     NormRopeKey k[U];
@@ -662,9 +710,9 @@ cudaError_t launch_fp8_indexer_insert(const InsertParams& p, cudaStream_t stream
 
 cudaError_t launch_norm_rope_store(const NormRopeParams& p, cudaStream_t stream) {
     constexpr int U = PSK_NORM_ROPE_UNROLL;
-    // 8 lanes per key, U keys per lane group (keys g, g + G, ... for G groups)
+    // kKeyLanes lanes per key, U keys per lane group (keys g, g + G, ... for G groups)
     const int64_t groups = (p.num_tokens + U - 1) / U;
-    const int64_t blocks = (groups * 8 + kThreads - 1) / kThreads;
+    const int64_t blocks = (groups * kKeyLanes + kThreads - 1) / kThreads;
     const int32_t shift = log2_if_pow2(p.block_size);
     const bool every = p.ratio == 1;
     const bool cs_vec = (reinterpret_cast<uintptr_t>(p.cos_sin) & 15) == 0 && p.cs_stride % 4 == 0;
@@ -675,9 +723,9 @@ cudaError_t launch_norm_rope_store(const NormRopeParams& p, cudaStream_t stream)
          {norm_rope_store_kernel<false, true, false, U>, norm_rope_store_kernel<false, true, true, U>}},
         {{norm_rope_store_kernel<true, false, false, U>, norm_rope_store_kernel<true, false, true, U>},
          {norm_rope_store_kernel<true, true, false, U>, norm_rope_store_kernel<true, true, true, U>}}};
-    const Kern kern = kTable[p.record == 1][every][cs_vec];
     NormRopeParams q = p;
     q.ratio_shift = log2_if_pow2(p.ratio);
+    const Kern kern = kTable[p.record == 1][every][cs_vec];
     return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, q, shift);
 }
 
