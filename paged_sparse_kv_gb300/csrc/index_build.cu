@@ -654,24 +654,49 @@ index_build_kernel(IndexParams p) {
 // r * workspace_width, compressed entries at rows 0.., the gathered window
 // positions g0 = seq - gather_len .. seq - 1 at rows compressed_base...  No
 // table look-ups: every column is arithmetic on the token's metadata.
-// Workspace row of column c (top-k entry l_in for c >= W) for a token with
-// the given metadata, or -1.
+// A token's metadata, and both column rules in 32-bit form.  Window column
+// c < W holds position ps = lo + c: row rbase + compressed_base + (ps - g0)
+// when g0 <= ps <= pos, i.e. row wb + c for c in [wc_lo, wc_lo + wc_n) (the
+// range also clipped to rows <= INT32_MAX, which become -1).  Top-k column
+// with entry l: row rbase + l when 0 <= l < lc, i.e. for (uint32)l < tk_n (the
+// bound also clipped to rows <= INT32_MAX).  Both are worked out once per
+// token in 64-bit arithmetic (ws_forms).
 struct WsMeta {
     bool ok;
     int64_t pos, lo, g0, lc, rbase;
+    int32_t wc_lo, wb, rb;
+    uint32_t wc_n, tk_n;
 };
 
+__device__ __forceinline__ void ws_forms(const WorkspaceIndexParams& p, WsMeta& m) {
+    m.wc_lo = m.wb = m.rb = 0;
+    m.wc_n = m.tk_n = 0u;
+    if (!m.ok) return;
+    const int64_t base = m.rbase + p.compressed_base - m.g0 + m.lo;  // row of column 0
+    const int64_t clo = m.g0 > m.lo ? m.g0 - m.lo : 0;
+    int64_t chi = (int64_t)p.window - 1;
+    if (m.pos - m.lo < chi) chi = m.pos - m.lo;
+    if (0x7FFFFFFFll - base < chi) chi = 0x7FFFFFFFll - base;
+    if (chi >= clo) {
+        m.wc_lo = (int32_t)clo;
+        m.wc_n = (uint32_t)(chi - clo + 1);
+        m.wb = (int32_t)(uint32_t)(uint64_t)base;  // base + c is exact modulo 2^32
+    }
+    int64_t hi = m.lc;
+    if (0x80000000ll - m.rbase < hi) hi = 0x80000000ll - m.rbase;
+    if (hi > 0) {
+        m.tk_n = (uint32_t)hi;
+        m.rb = (int32_t)(uint32_t)(uint64_t)m.rbase;
+    }
+}
+
+// Workspace row of column c (top-k entry l_in for c >= W; -1 past the top-k
+// columns), or -1.
 __device__ __forceinline__ int ws_col(const WorkspaceIndexParams& p, const WsMeta& m, int c,
                                       int l_in) {
-    if (!m.ok) return -1;
-    int64_t v = -1;
-    if (c < p.window) {
-        const int64_t ps = m.lo + c;
-        if (ps <= m.pos && ps >= m.g0) v = m.rbase + p.compressed_base + (ps - m.g0);
-    } else if (c - p.window < p.topk) {
-        if (l_in >= 0 && l_in < m.lc) v = m.rbase + l_in;
-    }
-    return v > 0x7FFFFFFFll ? -1 : (int)v;
+    if (c < p.window)
+        return (uint32_t)(c - m.wc_lo) < m.wc_n ? (int)((uint32_t)m.wb + (uint32_t)c) : -1;
+    return (uint32_t)l_in < m.tk_n ? (int)((uint32_t)m.rb + (uint32_t)l_in) : -1;
 }
 
 template <bool VEC, bool TMA>
@@ -709,6 +734,8 @@ __global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceInde
         WsMeta m;
         m.ok = false;
         m.pos = m.lo = m.g0 = m.lc = m.rbase = 0;
+        m.wc_lo = m.wb = m.rb = 0;
+        m.wc_n = m.tk_n = 0u;
         if (t < t1) {
             const int32_t r = __ldg(p.t2r + t);
             if (VEC && !TMA) {
@@ -744,6 +771,7 @@ __global__ void __launch_bounds__(kThreads) workspace_index_kernel(WorkspaceInde
                 m.lo = m.pos - W + 1;
                 if (m.lo < 0) m.lo = 0;
             }
+            ws_forms(p, m);
         }
         if (copy_topk && tb == t0) {
             rows_ok = mbar_wait_bounded(&s_bar, 0, kWaitLimitNs);
