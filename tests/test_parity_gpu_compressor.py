@@ -71,7 +71,8 @@ def _compress_case(rng, ratio, overlap, bs_state, kv_bs, R=3, T=260):
 
 @pytest.mark.parametrize("kv_bs", [64, 5])
 @pytest.mark.parametrize("ratio,overlap,bs_state", [(4, True, 8), (4, True, 3), (128, False, 64),
-                                                    (128, False, 7), (2, False, 4), (8, True, 16)])
+                                                    (128, False, 7), (2, False, 4), (8, True, 16),
+                                                    (1, False, 4), (3, True, 5)])
 def test_compress_fuzz(cuda_device, ratio, overlap, bs_state, kv_bs):
     rng = np.random.default_rng(ratio * 100 + bs_state + kv_bs)
     d = cuda_device

@@ -121,6 +121,45 @@ def test_workspace_indices_fuzz(cuda_device, seed):
         assert np.array_equal(gl.cpu().numpy(), wl)
 
 
+@pytest.mark.parametrize("case", ["window_rows_cross", "topk_rows_cross"])
+def test_workspace_indices_int32_edges(cuda_device, case):
+    """Workspace rows near INT32_MAX: request r's rows start at r * width, so a
+    wide workspace puts one request's window rows (or top-k rows) across
+    INT32_MAX -- those become -1, the rows below stay -- and the last request
+    past it entirely (all -1, not counted in lens)."""
+    rng = np.random.default_rng(31 if case == "window_rows_cross" else 32)
+    R, W, ratio, K = 3, 128, 4, 64
+    qlens = np.array([40, 50, 30])
+    seq = np.array([900, 16000, 700], np.int32)
+    qsl = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    T = int(qsl[-1])
+    t2r = np.repeat(np.arange(R, dtype=np.int32), qlens)
+    glen = (qlens + np.minimum(seq - qlens, W - 1)).astype(np.int32)
+    lc = seq // ratio
+    if case == "window_rows_cross":
+        ww = 1_100_000_000               # request 1 at 1.1e9, request 2 past INT32_MAX
+        cb = 2_147_483_600 - ww          # request 1's window rows cross INT32_MAX
+    else:
+        ww = 2_147_480_000               # request 1's top-k rows cross at l = 3648
+        cb = 8
+    topk = np.where(rng.random((T, K)) < 0.1, -1,
+                    rng.integers(0, np.repeat(lc, qlens)[:, None] + 1, size=(T, K))).astype(np.int32)
+    topk[qsl[1]:qsl[2], :8] = np.arange(3640, 3648 + 8, 2, dtype=np.int32)[None, :8]
+    d = cuda_device
+    got, gl = ops.combine_topk_swa_workspace_indices(
+        _i32(topk, d), _i32(qsl, d), _i32(seq, d), _i32(glen, d), _i32(t2r, d), W, ratio, ww, cb)
+    want, wl = oracle.combine_topk_swa_workspace_indices(qsl, seq, glen, t2r, W, ratio, topk, ww,
+                                                         cb)
+    g = got.cpu().numpy()
+    assert np.array_equal(g, want)
+    assert np.array_equal(gl.cpu().numpy(), wl)
+    # the case is what it says: request 1 has both kept and dropped rows, request 2 none
+    r1 = want[qsl[1]:qsl[2]]
+    part = r1[:, :W] if case == "window_rows_cross" else r1[:, W:]
+    assert (part >= 0).any() and (part > 2_000_000_000).any()
+    assert np.all(want[qsl[2]:qsl[3]] == -1) and np.all(wl[qsl[2]:qsl[3]] == 0)
+
+
 def test_prefill_workspace_full_size(cuda_device):
     """Both range gathers into one workspace at the prefill workload's size."""
     w = synthetic.make("prefill")
