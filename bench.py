@@ -44,6 +44,7 @@ import sys
 import tempfile
 import threading
 import time
+from types import SimpleNamespace
 
 import numpy as np
 
@@ -429,6 +430,28 @@ def _capture(torch, dev, stream, fn):
 
 # ---- main ------------------------------------------------------------------------------
 
+def workload_description(w) -> str:
+    return (f"{w.name}: {w.num_reqs} requests, {w.num_tokens} query tokens, "
+            f"head_dim {w.head_dim} (rope {w.rope_dim}), window {w.window}, "
+            f"top-k {w.topk}, ratio {w.compress_ratio}")
+
+
+def line_config(workload: str, path: str, seed: int, world: int, launch: str) -> dict:
+    """The `config` of the JSON line; both arms print the same one."""
+    return {"workload": workload, "path": path,
+            "storage": "bf16 rows in and out; fp8 e4m3 records with UE8M0 scales; "
+                       "MXFP4 (e2m1 + E8M0) indexer keys",
+            "seed": seed,
+            "l2": ("flushed before every step: 512 MiB memset, then a 256 MiB read so "
+                   "the lines left in L2 are clean"),
+            "parallelism": f"dp{world} (independent batch per GPU)",
+            "launch": launch,
+            "timing": "value: events around an un-instrumented graph replay of each "
+                      "step; roofline: events around the dominant kernel in a "
+                      "serialised instrumented replay after each timed step "
+                      "(roofline.in_step: in a concurrent instrumented replay)"}
+
+
 def step_layout(p, path: str, graph: bool) -> str:
     """How the step's launches are laid out on streams (the config's `launch`)."""
     w = p.w
@@ -702,9 +725,7 @@ def run_config(args, torch, dev, dist, world, rank, flush, config: str, steps: i
                                   "replay of the step (it shares the GPU with the other chains)"}}
     step_bytes = sum(alg.values())
     res = {
-        "workload": (f"{w.name}: {w.num_reqs} requests, {w.num_tokens} query tokens, "
-                     f"head_dim {w.head_dim} (rope {w.rope_dim}), window {w.window}, "
-                     f"top-k {w.topk}, ratio {w.compress_ratio}"),
+        "workload": workload_description(w),
         "path": path, "seed": w.seed, "tokens_per_step": w.num_tokens,
         "launch": step_layout(p, path, g_plain is not None),
         "ms_per_step": round(ms_per_step, 5), "value": round(value, 1),
@@ -816,18 +837,8 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/int32",
         "data": "synthetic",
-        "config": {"workload": head["workload"], "path": head["path"],
-                   "storage": "bf16 rows in and out; fp8 e4m3 records with UE8M0 scales; "
-                              "MXFP4 (e2m1 + E8M0) indexer keys",
-                   "seed": head["seed"],
-                   "l2": ("flushed before every step: 512 MiB memset, then a 256 MiB read so "
-                          "the lines left in L2 are clean"),
-                   "parallelism": f"dp{world} (independent batch per GPU)",
-                   "launch": head["launch"],
-                   "timing": "value: events around an un-instrumented graph replay of each "
-                             "step; roofline: events around the dominant kernel in a "
-                             "serialised instrumented replay after each timed step "
-                             "(roofline.in_step: in a concurrent instrumented replay)"},
+        "config": line_config(head["workload"], head["path"], head["seed"], world,
+                              head["launch"]),
         "roofline": head["roofline"],
         "kernels": head["kernels"],
         "kernels_note": ("us_serial_with_event_node: events between consecutive kernels of "
@@ -1004,7 +1015,9 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32/int32", "data": "synthetic",
-        "config": {"workload": w.name, "seed": w.seed, "path": path},
+        "config": line_config(workload_description(w), path, w.seed, world,
+                              step_layout(SimpleNamespace(w=w, gather_as_pair=Pipeline.small_batch(w)),
+                                          path, not args.eager)),
         "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "host": host_description(),
                          "sample": desc},

@@ -1,6 +1,8 @@
 """Host-side logic of the benchmark that the roofline figures rest on, with no
-GPU: the compulsory-byte accounting, and the source hashing that decides
-whether a recorded DRAM traffic figure still belongs to the current kernels."""
+GPU: the compulsory-byte accounting, the source hashing that decides whether a
+recorded DRAM traffic figure still belongs to the current kernels, and the
+reference arm's JSON line (the oracle on the same workload and config)."""
+import json
 import os
 import shutil
 from types import SimpleNamespace
@@ -67,3 +69,20 @@ def test_algorithmic_bytes_of_the_tiny_step():
     # the gathers read at most every index entry's record once
     assert all(v >= 0 for v in got.values())
     assert len(distinct) <= len(entries)
+
+
+def test_reference_arm_prints_the_same_config(capsys):
+    """bench.py --impl reference times the oracle on the same workload and
+    prints the same `config` object as the GPU arm builds for it."""
+    from paged_sparse_kv_gb300.pipeline import Pipeline
+    args = SimpleNamespace(config="tiny", path="auto", steps=1, warmup=1, eager=False)
+    bench.run_reference(args, 0, 1)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    w = synthetic.make("tiny")
+    path = Pipeline.default_path_for(w)
+    layout = bench.step_layout(SimpleNamespace(w=w, gather_as_pair=Pipeline.small_batch(w)),
+                               path, True)
+    assert line["config"] == bench.line_config(bench.workload_description(w), path, w.seed, 1,
+                                               layout)
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
