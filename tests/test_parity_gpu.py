@@ -523,7 +523,9 @@ SAMPLE = {"tiny": None, "decode": None, "prefill": 48, "mixed": 48, "mxfp4": Non
 @pytest.mark.parametrize("name,mode", [("tiny", "serial"), ("decode", "serial"),
                                        ("prefill", "serial"), ("mixed", "serial"),
                                        ("mxfp4", "serial"), ("tiny", "graph"),
-                                       ("decode", "graph"), ("mixed", "concurrent")])
+                                       ("decode", "graph"), ("mixed", "concurrent"),
+                                       ("prefill", "graph"), ("mixed", "graph"),
+                                       ("mxfp4", "graph")])
 def test_pipeline_step_matches_oracle(cuda_device, name, mode):
     """The whole step at full size, launched the way the benchmark launches it
     (serial, three concurrent streams, or a CUDA graph of the concurrent step)."""
