@@ -179,14 +179,14 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// State row of window row j of a writing token (request r, position pos), or
-// -1: a negative position, a logical page outside the table row, a missing
-// page or a row beyond the state cache.
-__device__ __forceinline__ int64_t window_state_row(const CompressParams& p, int32_t r, int64_t pos,
-                                                    int window, int j) {
+// State row of window row j of a writing token (request r, position pos; the
+// request's block-table base offset `base`), or -1: a negative position, a
+// logical page outside the table row, a missing page or a row beyond the
+// state cache.
+__device__ __forceinline__ int64_t window_row(const CompressParams& p, int64_t pos, int32_t r,
+                                              int64_t base, int window, int j) {
     const int64_t ps = pos - window + 1 + j;
     if (ps < 0) return -1;
-    const int64_t base = p.base ? __ldg(p.base + r) : 0;
     const int64_t lp = ps / p.state_bs - base;
     if (lp < 0 || lp >= p.bt_width) return -1;
     const int32_t entry = __ldg(p.bt + (int64_t)r * p.bt_stride + lp);
@@ -357,7 +357,8 @@ __global__ void __launch_bounds__(THREADS, 4) compress_kernel(CompressParams p, 
         // every listed token's window rows: one round of table look-ups
         for (int k = tid; k < n * window; k += THREADS) {
             const int i = k / window, j = k - i * window;
-            s_rows[i][j] = window_state_row(p, s_req[i], s_pos[i], window, j);
+            const int64_t base = p.base ? __ldg(p.base + s_req[i]) : 0;
+            s_rows[i][j] = window_row(p, s_pos[i], s_req[i], base, window, j);
         }
         __syncthreads();
         if (n > 0) {
@@ -606,19 +607,6 @@ __device__ __forceinline__ void scan_chunk(const CompressParams& p, int64_t c0, 
     const unsigned mask = __ballot_sync(0xFFFFFFFFu, emit);
     if (emit) s_list[__popc(mask & ((1u << lane) - 1u))] = t;
     if (lane == 0) *s_count = __popc(mask);
-}
-
-// State row of window entry j of token t (-1: absent), as the oracle forms it.
-__device__ __forceinline__ int64_t window_row(const CompressParams& p, int64_t pos, int32_t r,
-                                              int64_t base, int window, int j) {
-    const int64_t ps = pos - window + 1 + j;
-    if (ps < 0) return -1;
-    const int64_t lp = ps / p.state_bs - base;
-    if (lp < 0 || lp >= p.bt_width) return -1;
-    const int32_t entry = __ldg(p.bt + (int64_t)r * p.bt_stride + lp);
-    if (entry < 0) return -1;
-    const int64_t sr = (int64_t)entry * p.state_bs + ps % p.state_bs;
-    return sr < p.state_pages * (int64_t)p.state_bs ? sr : -1;
 }
 
 // Column col0 + tid of the normalised row into token t's record: CTA k < 7
