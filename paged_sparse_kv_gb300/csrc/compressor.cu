@@ -419,24 +419,17 @@ __global__ void __launch_bounds__(THREADS, 4) compress_kernel(CompressParams p, 
             // kv: every group but the one just committed has landed
             cp_async_wait<1>();
             {
-                float kv[kWinRows][CPT];
+                // each row's kv read where it is used (fewer live registers)
 #pragma unroll
                 for (int j = 0; j < kWinRows; ++j) {
                     if (j >= window) continue;
-                    if (s_rows[i][j] < 0) {
+                    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    if (s_rows[i][j] >= 0) v = s_win[(2 * j + 1) * THREADS + tid];
+                    const float kv4[CPT] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                        for (int e = 0; e < CPT; ++e) kv[j][e] = 0.0f;
-                    } else {
-                        const float4 v = s_win[(2 * j + 1) * THREADS + tid];
-                        kv[j][0] = v.x; kv[j][1] = v.y; kv[j][2] = v.z; kv[j][3] = v.w;
-                    }
+                    for (int e = 0; e < CPT; ++e)
+                        acc[e] = __fadd_rn(acc[e], __fmul_rn(kv4[e], __fdiv_rn(ex[j][e], sum[e])));
                 }
-#pragma unroll
-                for (int j = 0; j < kWinRows; ++j)
-                    if (j < window)
-#pragma unroll
-                        for (int e = 0; e < CPT; ++e)
-                            acc[e] = __fadd_rn(acc[e], __fmul_rn(kv[j][e], __fdiv_rn(ex[j][e], sum[e])));
             }
             // the kv have been read: the next token's kv may overwrite them
             if (more)
