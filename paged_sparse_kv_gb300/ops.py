@@ -59,8 +59,8 @@ def _need(t: torch.Tensor, dtype: torch.dtype, name: str):
 
 def _pages(cache: torch.Tensor):
     _need(cache, torch.uint8, "cache")
-    if cache.dim() < 2 or not cache[0].is_contiguous():
-        raise ValueError("cache must be [num_pages, ...] uint8 with contiguous pages")
+    if cache.dim() < 2 or cache.shape[0] == 0 or not cache[0].is_contiguous():
+        raise ValueError("cache must be [num_pages >= 1, ...] uint8 with contiguous pages")
     if cache.shape[0] == 1:  # a size-1 dim may carry any stride (0 from broadcasting)
         return 1, max(cache.stride(0), cache[0].numel())
     return cache.shape[0], cache.stride(0)

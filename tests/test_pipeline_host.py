@@ -48,3 +48,5 @@ def test_size_one_leading_dims_ignore_their_stride():
     cache = torch.from_numpy(np.zeros(592, np.uint8)[None, :])
     assert cache.stride(0) == 0 and ops._pages(cache) == (1, 592)
     assert ops._pages(torch.zeros(4, 600, dtype=torch.uint8)[:, :592]) == (4, 600)
+    with pytest.raises(ValueError):
+        ops._pages(torch.zeros(0, 592, dtype=torch.uint8))
